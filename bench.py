@@ -1,0 +1,539 @@
+#!/usr/bin/env python
+"""Benchmark: Medusa verify steps per second on one GB300 (or N replicas).
+
+One step = the whole hot path on one batch of synthetic inputs: tree-masked
+attention with KV append, LM head over every tree row, acceptance, KV
+compaction, the Medusa heads with top-s, and the next candidate tree -- six
+libmedusa calls (11 kernels), captured once in a CUDA graph.
+
+Default workload: Vicuna-7B shape (d=4096, V=32000, 32x128 heads), prefix
+1024, 64-node greedy sparse tree (65 rows), 4 Medusa heads, batch 1, greedy
+acceptance, bf16.  Weights and activations are seeded synthetic tensors;
+1.48 GB of weights stream per step, more than the 126 MB L2, so nothing is
+served from L2 across steps.
+
+Prints one JSON line (rank 0).  `--impl reference` times the CPU oracle on a
+bounded sample of the same workload instead.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import threading
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "Medusa verify-steps/s, 7B shape, 64-node tree, bs1; % of HBM roofline"
+UNIT = "verify-steps/s"
+
+
+def parse_args():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=100)
+    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--impl", choices=["native", "reference"], default="native")
+    ap.add_argument("--workload", default=None)
+    ap.add_argument("--plant-depth", type=int, default=3)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-e2e", action="store_true")
+    return ap.parse_args()
+
+
+# ------------------------------------------------------------------ bytes --
+
+def algorithmic_bytes(w: dict, T: int, s_heads, L_list) -> dict:
+    """Bytes each call must move at least once per step (weights once, KV
+    prefix once, activations and logits once each way)."""
+    e = 2 if w["dtype"] == "bf16" else 4
+    B, H, Dh, d, V = w["B"], w["H"], w["Dh"], w["d"], w["V"]
+    k_used = sum(1 for s in s_heads if s > 0)
+    sumL = int(np.sum(L_list))
+    attn = (2 * sumL * H * Dh * e          # cached K, V read
+            + 3 * B * T * H * Dh * e       # q, k_new, v_new read
+            + 2 * B * T * H * Dh * e       # K', V appended
+            + B * T * H * Dh * e)          # out written
+    lm = V * d * e + B * T * d * e + B * T * V * 4
+    accept = B * T * V * 4
+    compact = 2 * 2 * B * (w["K"] + 1) * H * Dh * e
+    heads = k_used * (d * d + V * d) * e + B * k_used * V * 4 * 2
+    cand = B * T * 4
+    out = dict(tree_attn=attn, lm_head_verify=lm, accept=accept, kv_compact=compact,
+               heads_topk=heads, build_candidates=cand)
+    out["step"] = sum(out.values())
+    return out
+
+
+def algorithmic_flops(w, T, s_heads, L_list):
+    B, H, Dh, d, V = w["B"], w["H"], w["Dh"], w["d"], w["V"]
+    k_used = sum(1 for s in s_heads if s > 0)
+    return dict(tree_attn=4 * T * (int(np.sum(L_list)) + T) * H * Dh,
+                lm_head_verify=2 * B * T * d * V,
+                heads_topk=2 * B * k_used * (d * d + d * V))
+
+
+def load_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            j = json.load(f)
+        return dict(hbm_gbs=float(j["hbm_gbs"]), bf16_tflops=float(j["bf16_tflops"]),
+                    bf16_tflops_sustained=float(j.get("bf16_tflops_sustained", j["bf16_tflops"])),
+                    source="measured")
+    return dict(hbm_gbs=6800.0, bf16_tflops=1900.0, bf16_tflops_sustained=1700.0, source="fallback")
+
+
+def ncu_traffic(kernel_key: str):
+    """DRAM bytes per launch from the committed ncu summary, or None when the
+    kernel's source changed since the counters were taken."""
+    p = os.path.join(ROOT, "profiles", "ncu_traffic.json")
+    if not os.path.exists(p):
+        return None
+    with open(p) as f:
+        j = json.load(f)
+    ent = j.get(kernel_key)
+    if not ent:
+        return None
+    src = os.path.join(ROOT, ent["source"])
+    if not os.path.exists(src) or hashlib.sha256(open(src, "rb").read()).hexdigest()[:16] != ent["sha"]:
+        return None
+    return ent["dram_bytes_per_launch_full"]
+
+
+# ----------------------------------------------------------------- clocks --
+
+class ClockSampler:
+    """nvidia-smi samples (SM clock, throttle reasons) during the timed region."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.path = None
+
+    def __enter__(self):
+        fd, self.path = tempfile.mkstemp(suffix=".csv")
+        os.close(fd)
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "100", "-f", self.path], stdout=subprocess.DEVNULL, stderr=subprocess.DEVNULL)
+        except FileNotFoundError:
+            self.proc = None
+        time.sleep(0.3)
+        return self
+
+    def __exit__(self, *exc):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+
+    def summary(self):
+        rows = []
+        if self.path and os.path.exists(self.path):
+            for line in open(self.path):
+                parts = [p.strip() for p in line.split(",")]
+                if len(parts) >= 9 and parts[1].replace(".", "").isdigit():
+                    rows.append(parts)
+            os.remove(self.path)
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unsampled"]}
+        sm = [float(r[1]) for r in rows]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in rows for i in range(4) if r[5 + i].lower().startswith("active")})
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(float(r[2]) for r in rows),
+                "reasons": reasons, "samples": len(rows)}
+
+
+# ---------------------------------------------------------------- native --
+
+def plant(w, tree, st, x, depth, torch):
+    """Set the tokens along one root->node path (node at `depth`) to the
+    parent-row argmax of the LM head, so acceptance takes that path; off the
+    path, tokens differ from the parent's argmax.  Setup only, untimed."""
+    from medusa_tree_speculative_gb300 import medusa as M
+
+    ht = tree.host
+    M.medusa_lm_head_verify(x["hidden"], st.w_lm, st.logits)
+    am = torch.argmax(st.logits, dim=-1).cpu().numpy()  # [B, T]
+    cands = np.nonzero(ht.depth == min(depth, ht.K))[0]
+    tok = x["tokens"].cpu().numpy()
+    for b in range(w["B"]):
+        node = int(cands[(7 * b + 3) % len(cands)])
+        path = set()
+        n = node
+        while n > 0:
+            path.add(n)
+            n = int(ht.parent[n])
+        for c in range(1, ht.T):
+            p = int(ht.parent[c])
+            tok[b, c] = am[b, p] if c in path else (am[b, p] + 1 + c) % w["V"]
+    x["tokens"].copy_(torch.from_numpy(tok))
+
+
+def run_native(args, w, rank, world, local_rank):
+    import torch
+    import torch.distributed as dist
+
+    from medusa_tree_speculative_gb300 import medusa as M
+    from medusa_tree_speculative_gb300 import step, synth
+
+    torch.cuda.set_device(local_rank)
+    dev = torch.device("cuda", local_rank)
+    ht = step.build_tree(w)
+    tree = M.DeviceTree(ht, dev)
+    T = tree.T
+    seed = 0  # every replica runs the same workload
+    wts = synth.make_weights(w, seed)
+    xh = synth.make_step(w, T, seed)
+    dt = w["dtype"]
+    wd = {k: (None if v is None else step.host_to_torch(v, dt).to(dev)) for k, v in wts.items()}
+    del wts
+    x = {}
+    for k, v in xh.items():
+        x[k] = step.host_to_torch(v, dt).to(dev) if v.dtype in (np.uint16, np.float32) else torch.from_numpy(v).to(dev)
+    L_list = xh["prefix_len"].copy()
+    st = step.VerifyStep(w, wd, tree, max_prefix=int(L_list.max()), device=dev)
+    plant(w, tree, st, x, args.plant_depth, torch)
+    prefix0 = x["prefix_len"].clone()
+    s = torch.cuda.Stream(device=dev)
+    # eager warm-up (JIT, attributes) then one checked step
+    with torch.cuda.stream(s):
+        for _ in range(2):
+            x["prefix_len"].copy_(prefix0)
+            st.run(x, s)
+    torch.cuda.synchronize()
+    if int(st.err.item()) != 0:
+        raise RuntimeError(f"device error flag {int(st.err.item())} after warm-up")
+    accept_len = st.accept_len.cpu().numpy().tolist()
+
+    # one graph holds K steps with timing events at every call boundary
+    calls = ["tree_attn", "lm_head_verify", "accept", "kv_compact", "heads_topk", "build_candidates"]
+
+    def capture(nsteps, with_events):
+        g = torch.cuda.CUDAGraph()
+        evs = []
+        with torch.cuda.graph(g, stream=s):
+            for _ in range(nsteps):
+                x["prefix_len"].copy_(prefix0)
+                if with_events:
+                    e = [torch.cuda.Event(enable_timing=True, external=True) for _ in range(len(calls) + 1)]
+                    evs.append(e)
+                    run_calls(st, x, s, e)
+                else:
+                    st.run(x, s)
+        return g, evs
+
+    def run_calls(st, x, s, e):
+        e[0].record(s)
+        M.medusa_tree_attn(x["q"], x["k_new"], x["v_new"], x["k_cache"], x["v_cache"], x["seq_start"],
+                           x["prefix_len"], x["seq_cap"], st.tree, st.max_prefix, st.rope_theta, st.scale,
+                           st.out, st.ws_attn, st.err, s)
+        e[1].record(s)
+        M.medusa_lm_head_verify(x["hidden"], st.w_lm, st.logits, None, s)
+        e[2].record(s)
+        M.medusa_accept(st.logits, x["tokens"], st.tree, st.mode, st.temperature, st.eps, st.delta,
+                        st.accept_len, st.accepted_nodes, st.next_root, st.best_node, st.best_logp,
+                        st.ws_accept, st.err, s)
+        e[3].record(s)
+        M.medusa_kv_compact(x["k_cache"], x["v_cache"], x["seq_start"], x["prefix_len"], st.accepted_nodes,
+                            st.accept_len, st.tree.K, st.src_slots, st.err, s)
+        e[4].record(s)
+        M.medusa_heads_topk(x["hidden"], st.best_node, st.w1, st.b1, st.w2, st.s_heads, st.head_logits,
+                            st.topk, st.ws_heads, st.err, s)
+        e[5].record(s)
+        M.medusa_build_candidates(st.next_root, st.topk, st.tree, st.next_tokens, s)
+        e[6].record(s)
+
+    g_warm, _ = capture(1, False)
+    g_timed, evs = capture(args.steps, True)
+    g_plain, _ = capture(args.steps, False)
+    for _ in range(args.warmup):
+        g_warm.replay()
+    torch.cuda.synchronize()
+
+    def timed(graph):
+        if world > 1:
+            dist.barrier()
+        torch.cuda.synchronize()
+        t0 = torch.cuda.Event(enable_timing=True)
+        t1 = torch.cuda.Event(enable_timing=True)
+        t0.record(s)
+        graph.replay()
+        t1.record(s)
+        torch.cuda.synchronize()
+        if world > 1:
+            dist.barrier()
+        return t0.elapsed_time(t1)
+
+    with ClockSampler(local_rank) as clk:
+        ms_plain = timed(g_plain)   # the headline number: no event nodes in the graph
+        ms_events = timed(g_timed)  # same steps with per-call events
+    clocks = clk.summary()
+    per_call = {c: statistics.mean(e[i].elapsed_time(e[i + 1]) for e in evs) for i, c in enumerate(calls)}
+    if int(st.err.item()) != 0:
+        raise RuntimeError(f"device error flag {int(st.err.item())} in the timed region")
+
+    ms_total = ms_plain
+    if world > 1:
+        t = torch.tensor([ms_total], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ms_total = float(t.item())
+    ms_step = ms_total / args.steps
+
+    e2e = None
+    if not args.no_e2e:
+        e2e = measure_e2e(args, w, st, x, xh, prefix0, s, torch, M)
+
+    return dict(ms_step=ms_step, ms_events_step=ms_events / args.steps, per_call_ms=per_call, clocks=clocks,
+                T=T, s_heads=st.s_heads, L_list=L_list, accept_len=accept_len, e2e=e2e,
+                launches=st.launches_per_step * args.steps, tree=ht)
+
+
+def measure_e2e(args, w, st, x, xh, prefix0, s, torch, M):
+    """Same metric through the public C-ABI calls with host buffers: per step,
+    pinned host inputs -> device, the six calls, results -> pinned host."""
+    names_in = ["q", "k_new", "v_new", "hidden", "tokens"]
+    host_in = {k: x[k].cpu().pin_memory() for k in names_in}
+    host_pl = prefix0.cpu().pin_memory()
+    outs = [st.accept_len, st.accepted_nodes, st.next_root, st.next_tokens]
+    host_out = [o.cpu().pin_memory() for o in outs]
+    h2d = sum(t.numel() * t.element_size() for t in host_in.values()) + host_pl.numel() * 4
+    d2h = sum(t.numel() * t.element_size() for t in host_out)
+    steps = max(10, args.steps // 2)
+
+    def one():
+        with torch.cuda.stream(s):
+            for k in names_in:
+                x[k].copy_(host_in[k], non_blocking=True)
+            x["prefix_len"].copy_(host_pl, non_blocking=True)
+            st.run(x, s)
+            for h, d in zip(host_out, outs):
+                h.copy_(d, non_blocking=True)
+        s.synchronize()
+
+    for _ in range(3):
+        one()
+    torch.cuda.synchronize()
+    t0 = time.perf_counter()
+    for _ in range(steps):
+        one()
+    dt = time.perf_counter() - t0
+    return {"value": steps / dt, "unit": UNIT, "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h),
+            "steps": steps}
+
+
+# ------------------------------------------------------------- CPU oracle --
+
+class OracleSample:
+    """The CPU oracle on a bounded sample of one step, scaled to a full step:
+    attention on 1/frac of the heads, the LM head and W2 on 1/frac of the
+    vocabulary rows (each timed and scaled by frac), W1, acceptance (on a full
+    [T, V] logit array), compaction and candidate fill in full.  Inputs are
+    drawn once; each call times only the oracle."""
+
+    def __init__(self, w, frac=32, seed=0):
+        import oracle
+        from medusa_tree_speculative_gb300 import synth
+
+        oracle.build()
+        self.w, self.frac = w, frac
+        if w["tree"][0] == "cartesian":
+            s = list(w["tree"][1])
+            n = w["tree"][2] or sum(math.prod(s[:k]) for k in range(1, len(s) + 1))
+            paths, plen = oracle.tree_cartesian(s, n)
+        else:
+            paths, plen = oracle.tree_greedy(synth.accuracy_table(w["K"], w["tree"][2]), w["tree"][1])
+        self.ot = ot = oracle.tree_compile(paths, plen, paths.shape[1])
+        T, B, H, d, V = ot.T, w["B"], w["H"], w["d"], w["V"]
+        dt = w["dtype"]
+        self.hs = max(1, H // frac)
+        self.vs = max(1, V // frac)
+        self.x = synth.make_step(dict(w, H=self.hs), T, seed)
+        self.w_lm = synth.normal(seed, "w_lm_sample", (self.vs, d), 1 / math.sqrt(d), dt)
+        s_heads = [int(ot.s[k]) if k < ot.K else 0 for k in range(w["K"])]
+        self.k_used = [k for k in range(w["K"]) if s_heads[k] > 0]
+        self.s_used = [s_heads[k] for k in self.k_used]
+        ku = len(self.k_used)
+        self.w1 = synth.normal(seed, "w1_sample", (ku, d, d), 1 / math.sqrt(d), dt)
+        self.w2 = synth.normal(seed, "w2_sample", (ku, self.vs, d), 1 / math.sqrt(d), dt)
+        self.w2_one = np.ascontiguousarray(self.w2[:, :1])
+        self.logits = synth.normal(seed, "logits_sample", (B, T, V), 2.0, "f32")
+
+    def step(self):
+        import oracle
+
+        w, x, ot = self.w, self.x, self.ot
+        H, V = w["H"], w["V"]
+        t_all = {}
+        kc, vc = x["k_cache"].copy(), x["v_cache"].copy()
+        t = time.perf_counter()
+        oracle.tree_attn(x["q"], x["k_new"], x["v_new"], kc, vc, x["seq_start"], x["prefix_len"], ot)
+        t_all["tree_attn"] = (time.perf_counter() - t) * (H / self.hs)
+        t = time.perf_counter()
+        oracle.lm_head(x["hidden"], self.w_lm)
+        t_all["lm_head_verify"] = (time.perf_counter() - t) * (V / self.vs)
+        mode = 1 if w["mode"] == "typical" else 0
+        t = time.perf_counter()
+        r = oracle.accept(self.logits, x["tokens"], ot, mode, w.get("temperature", 1.0), w.get("eps", 0.09),
+                          w.get("delta", 0.3))
+        t_all["accept"] = time.perf_counter() - t
+        t = time.perf_counter()
+        oracle.kv_compact(kc, vc, x["seq_start"], x["prefix_len"].copy(), r["accepted_nodes"], r["accept_len"],
+                          ot.K)
+        t_all["kv_compact"] = (time.perf_counter() - t) * (H / self.hs)
+        t = time.perf_counter()
+        _, tk, _ = oracle.heads(x["hidden"], r["best_node"], self.w1, None, self.w2, self.s_used, max(self.s_used))
+        t_heads = time.perf_counter() - t
+        # W1's share: the same call with a one-row vocabulary
+        t = time.perf_counter()
+        oracle.heads(x["hidden"], r["best_node"], self.w1, None, self.w2_one, [1] * len(self.k_used), 1)
+        t_w1 = time.perf_counter() - t
+        t_all["heads_topk"] = t_w1 + max(0.0, t_heads - t_w1) * (V / self.vs)
+        t = time.perf_counter()
+        oracle.build_candidates(r["next_root"], tk, ot)
+        t_all["build_candidates"] = time.perf_counter() - t
+        return sum(t_all.values()), t_all
+
+
+def cpu_baseline(w, reps=3):
+    smp = OracleSample(w)
+    vals = []
+    parts = None
+    for _ in range(reps):
+        tot, parts = smp.step()
+        vals.append(tot)
+    sec = statistics.median(vals)
+    return {"value": 1.0 / sec, "unit": UNIT, "cores": 1, "kind": "oracle",
+            "sample": ("single-threaded C oracle on the host; per step: attention on 1/32 of the heads and the "
+                       "LM head and W2 on 1/32 of the vocabulary rows, timed and scaled x32; W1, acceptance "
+                       "(on a full [T,V] logit array), compaction and candidate fill in full; "
+                       f"median of {reps} sampled steps; host has {os.cpu_count()} cores"),
+            "seconds_per_step_est": sec, "parts_s": {k: round(v, 4) for k, v in parts.items()}}
+
+
+def run_reference(args, w, rank, world):
+    """--impl reference: the CPU oracle as it stands, on host cores."""
+    if rank != 0:
+        return
+    import oracle
+
+    oracle.build()
+    smp = OracleSample(w, frac=64)
+    for _ in range(min(args.warmup, 1)):
+        smp.step()
+    vals = []
+    t0 = time.perf_counter()
+    parts = None
+    for _ in range(args.steps):
+        sec, parts = smp.step()
+        vals.append(sec)
+    wall = time.perf_counter() - t0
+    sec = statistics.mean(vals)
+    v = 1.0 / sec
+    line = {
+        "impl": "reference", "metric": METRIC, "value": v, "unit": UNIT, "n_gpus": args.gpus,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": sec * 1e3, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": config_dict(w),
+        "cpu_baseline": {"value": v, "unit": UNIT, "cores": 1, "kind": "oracle",
+                         "sample": ("each step: attention on 1/64 of the heads (at least one), LM head and W2 on "
+                                    "1/64 of the vocabulary rows (scaled up), the rest in full; single-threaded C "
+                                    "oracle; "
+                                    f"{args.steps} steps in {wall:.1f} s wall")},
+        "e2e": {"value": v, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+        "parts_s": {k: round(x, 4) for k, x in parts.items()},
+    }
+    print(json.dumps(line), flush=True)
+
+
+def config_dict(w, extra=None):
+    c = {"workload": w["name"], "dtype": w["dtype"], "d": w["d"], "V": w["V"], "H": w["H"], "Dh": w["Dh"],
+         "B": w["B"], "prefix": str(w["L"]), "K_heads": w["K"], "tree": str(w["tree"]), "accept": w["mode"],
+         "l2": "inputs larger than L2 (1.48 GB of weights stream per step)"}
+    if extra:
+        c.update(extra)
+    return c
+
+
+def main():
+    args = parse_args()
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local_rank = int(os.environ.get("LOCAL_RANK", "0"))
+    from medusa_tree_speculative_gb300 import workloads
+
+    w = workloads.get(args.workload or workloads.HEADLINE)
+    if args.impl == "reference":
+        if world > 1:
+            import torch.distributed as dist
+
+            dist.init_process_group("gloo")
+        run_reference(args, w, rank, world)
+        return
+    import torch
+
+    if world > 1:
+        import torch.distributed as dist
+
+        torch.cuda.set_device(local_rank)
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local_rank))
+    r = run_native(args, w, rank, world, local_rank)
+    if rank != 0:
+        return
+    peaks = load_peaks()
+    by = algorithmic_bytes(w, r["T"], r["s_heads"], r["L_list"])
+    fl = algorithmic_flops(w, r["T"], r["s_heads"], r["L_list"])
+    ms = r["ms_step"]
+    value = world * 1e3 / ms
+    step_gbs = by["step"] / (ms * 1e-3) / 1e9
+    dom = max(("heads_topk", "lm_head_verify", "tree_attn"), key=lambda c: r["per_call_ms"][c])
+    dom_ms = r["per_call_ms"][dom]
+    achieved = by[dom] / (dom_ms * 1e-3) / 1e9
+    traffic = ncu_traffic(dom)
+    line = {
+        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": w["dtype"], "data": "synthetic (seeded random weights and activations)",
+        "config": config_dict(w, {"parallelism": f"replicas{world}" if world > 1 else "single-gpu",
+                                  "T_rows": r["T"], "s": r["s_heads"], "planted_accept_len": r["accept_len"]}),
+        "roofline": {"bound": "hbm", "kernel": f"medusa_{dom}", "achieved": achieved, "peak": peaks["hbm_gbs"],
+                     "unit": "GB/s", "frac": achieved / peaks["hbm_gbs"], "traffic": traffic,
+                     "algorithmic_bytes_per_launch": by[dom], "ms_per_launch": dom_ms,
+                     "peak_source": peaks["source"] + " hbm_gbs (copy)"},
+        "step_roofline": {"algorithmic_bytes": by["step"], "achieved_gbs": step_gbs,
+                          "frac_of_measured": step_gbs / peaks["hbm_gbs"], "frac_of_8tbs": step_gbs / 8000.0},
+        "per_call": {c: {"ms": round(r["per_call_ms"][c], 5), "bytes": by[c],
+                         "gbs": round(by[c] / (r["per_call_ms"][c] * 1e-3) / 1e9, 1),
+                         **({"tflops": round(fl[c] / (r["per_call_ms"][c] * 1e-3) / 1e12, 1)} if c in fl else {})}
+                     for c in r["per_call_ms"]},
+        "ms_per_step_with_call_events": r["ms_events_step"],
+        "clocks": r["clocks"],
+        "gpu_launches": r["launches"],
+    }
+    if r["e2e"] is not None:
+        line["e2e"] = r["e2e"]
+    if world == 1 and not args.no_cpu_baseline:
+        line["cpu_baseline"] = cpu_baseline(w)
+    print(json.dumps(line), flush=True)
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,252 @@
+/*
+ * medusa.h -- C ABI of libmedusa: the data-parallel hot path of one Medusa
+ * tree-speculative decoding step on a single GB300 (sm_103a).
+ *
+ * Sources (cited by page title and section):
+ *   [MED]  "Medusa: Simple LLM Inference Acceleration Framework with Multiple
+ *          Decoding Heads" (paper digest): Method items 1-5; the box
+ *          "Algorithm: Medusa decoding step"; "Paper vs code"; "Pitfalls".
+ *   [MEDZ] "085 | Medusa" explainer: section 二.2 (tree attention) and 二.3
+ *          (strict and typical acceptance).
+ *
+ * One verify step is six calls, enqueued in this order on one stream:
+ *   medusa_tree_attn        tree-masked attention + KV append   (box step 3)
+ *   medusa_lm_head_verify   LM head over every tree row          (box step 3)
+ *   medusa_accept           greedy / typical acceptance          (box 4-5)
+ *   medusa_kv_compact       accepted path's KV into place        (box 6)
+ *   medusa_heads_topk       K Medusa heads + top-s               (box 1)
+ *   medusa_build_candidates next step's candidate tokens         (box 2)
+ *
+ * Conventions
+ *   - Every step call returns MEDUSA_OK (0) or a negative status; on error
+ *     nothing was enqueued and medusa_last_error() (per thread) says why.
+ *   - The library never allocates, frees or synchronises.  All pointers are
+ *     owned by the caller; tensors are dense, row-major, with the shapes given
+ *     below.  "device" pointers must be CUDA device (or managed) memory of the
+ *     current device; "host" pointers are read during the call only.
+ *   - Work is enqueued on `stream` (a cudaStream_t; 0 = legacy default).
+ *   - Scratch ("workspace") is caller-provided device memory of at least the
+ *     size returned by the matching *_workspace_size query, 256-byte aligned.
+ *     Its contents need no initialisation and are not preserved.
+ *   - Device-side data errors (a token or node index out of range, a prefix
+ *     that overflows its sequence's capacity) cannot be seen by the host
+ *     without a synchronisation.  Calls that read such data take `err`, a
+ *     nullable device int32: a kernel that meets bad data ORs a
+ *     MEDUSA_DEVERR_* bit into *err and skips the offending access.  Nothing
+ *     traps.
+ *   - Element types: MEDUSA_F32 (IEEE binary32) or MEDUSA_BF16 (bfloat16).
+ *     Logits are always float32; accumulation is always float32.
+ *
+ * Tree layout (medusa_tree_t)
+ *   T = 1 + N rows: row 0 is the root (the token chosen by the previous step),
+ *   rows 1..N the candidate nodes in breadth-first order (depth, then
+ *   lexicographic rank path), so every parent precedes its children.  A node
+ *   at depth k with rank r holds the r-th best token of Medusa head k
+ *   ([MED] Method 2).  anc_mask row i, bit j (word j/32, bit j%32) is set iff
+ *   node j is an ancestor of i or i itself ([MED] Method 3).
+ */
+#ifndef MEDUSA_H
+#define MEDUSA_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define MEDUSA_MAX_T 512  /* tree rows, root included */
+#define MEDUSA_MAX_K 8    /* tree depth / Medusa heads */
+#define MEDUSA_MAX_S 16   /* top-s per head */
+#define MEDUSA_MAX_B 16   /* sequences per call */
+
+typedef enum { MEDUSA_F32 = 0, MEDUSA_BF16 = 1 } medusa_dtype;
+
+enum {
+  MEDUSA_OK = 0,
+  MEDUSA_ERR_INVALID = -1,     /* null pointer, bad shape or tree */
+  MEDUSA_ERR_UNSUPPORTED = -2, /* dtype or size outside the supported set */
+  MEDUSA_ERR_CAPACITY = -3,    /* a known size exceeds a buffer's capacity */
+  MEDUSA_ERR_WORKSPACE = -4,   /* workspace smaller than the query returned */
+  MEDUSA_ERR_CUDA = -5         /* a CUDA runtime call or launch failed */
+};
+
+/* bits ORed into the device error word */
+enum {
+  MEDUSA_DEVERR_TOKEN = 1,    /* token outside [0, V) */
+  MEDUSA_DEVERR_NODE = 2,     /* node index outside [0, T) */
+  MEDUSA_DEVERR_CAPACITY = 4, /* prefix_len + T exceeds seq_cap */
+  MEDUSA_DEVERR_LENGTH = 8    /* accept_len outside [0, K] */
+};
+
+typedef struct medusa_tree {
+  const int32_t* parent;    /* device [T]; parent[0] = -1, parent[i] < i */
+  const int32_t* depth;     /* device [T]; depth[0] = 0 */
+  const int32_t* rank;      /* device [T]; 1-based rank, rank[0] = 0 */
+  const uint32_t* anc_mask; /* device [T][W] ancestor-or-self bitmask */
+  int32_t T;                /* rows, 1 <= T <= MEDUSA_MAX_T */
+  int32_t W;                /* words per mask row = ceil(T / 32) */
+  int32_t K;                /* tree depth (deepest node), <= MEDUSA_MAX_K */
+  int32_t s[MEDUSA_MAX_K];  /* largest rank used at depth k+1 (host values) */
+} medusa_tree_t;
+
+/* Thread-local description of the last error returned on this thread. */
+const char* medusa_last_error(void);
+/* Library version string. */
+const char* medusa_version(void);
+
+/* ======================= host tree helpers (no CUDA) ===================== */
+
+/* Compile a set of rank paths into the breadth-first layout above
+ * ([MED] Method 2 and 3).  paths: host [n_paths][max_depth], 1-based ranks,
+ * row i uses its first path_len[i] entries; any order.  Every proper prefix
+ * of a path must itself be in the set.  Outputs (host, caller-sized):
+ * parent/depth/rank [n_paths+1], anc_mask [(n_paths+1) * W] with
+ * W = ceil((n_paths+1)/32), s [max_depth], node_paths [n_paths+1][max_depth]
+ * (nullable; zero padded).  *T_out = n_paths + 1, *K_out = deepest level.
+ * Returns MEDUSA_ERR_INVALID on a duplicate, a missing prefix or a rank < 1,
+ * MEDUSA_ERR_UNSUPPORTED if T > MEDUSA_MAX_T or depth > MEDUSA_MAX_K or a
+ * rank > MEDUSA_MAX_S. */
+int medusa_tree_compile(const int32_t* paths, const int32_t* path_len,
+                        int n_paths, int max_depth, int32_t* parent,
+                        int32_t* depth, int32_t* rank, uint32_t* anc_mask,
+                        int32_t* s, int32_t* node_paths, int* T_out,
+                        int* K_out);
+
+/* Cartesian candidate tree ([MED] Method 2, fig. 2): all paths with
+ * i_k <= s[k], breadth-first, cut after max_nodes non-root nodes.
+ * paths: host [max_nodes][K]; returns the node count or a negative status. */
+int medusa_tree_cartesian(const int32_t* s, int K, int max_nodes,
+                          int32_t* paths, int32_t* path_len);
+
+/* Greedy sparse tree ([MED] Method 4): node accuracy is the product of the
+ * per-head top-i accuracies acc[k][i-1] along its path; starting from the
+ * root, add the connected node of highest accuracy (ties within 1e-9 in log
+ * space go to the lexicographically smallest path) until `budget` nodes.
+ * acc: host [K][R]; paths: host [budget][K].  Returns the node count. */
+int medusa_tree_greedy(const double* acc, int K, int R, int budget,
+                       int32_t* paths, int32_t* path_len);
+
+/* =============================== step calls ============================== */
+
+/* Scratch bytes medusa_tree_attn needs for these sizes. */
+size_t medusa_tree_attn_workspace_size(int B, int H, int Dh, int T,
+                                       int max_prefix);
+
+/* Tree-masked attention with tree position ids ([MED] Method 3, Pitfalls;
+ * [MEDZ] 二.2).
+ *   q, k_new, v_new: device [B][T][H][Dh], pre-rotation projections of the
+ *                    tree rows.
+ *   k_cache, v_cache: device [tokens][H][Dh]; sequence b owns rows
+ *                    [seq_start[b], seq_start[b] + seq_cap[b]); its first
+ *                    prefix_len[b] rows hold already-rotated keys.
+ *   seq_start [B] int64, prefix_len [B] int32, seq_cap [B] int64: device.
+ *   max_prefix: host upper bound on every prefix_len[b] (sizes the grid).
+ * For row i of sequence b at depth d_i, with L = prefix_len[b]:
+ *   pos = L + d_i;  q', k' = RoPE(q, pos), RoPE(k_new, pos) (rotate-half
+ *   pairs (j, j + Dh/2), inv_freq_j = rope_theta^(-2j/Dh), angle formed in
+ *   float32);  k', v_new are written to slot seq_start[b] + L + i;
+ *   out[b][i] = softmax(scale * q' . K_S^T) V_S over S = the L prefix slots
+ *   plus the slots of every ancestor-or-self of i.
+ * out: device [B][T][H][Dh] (dtype).  Dh must be 64 or 128.
+ * A sequence with L + T > seq_cap[b] sets MEDUSA_DEVERR_CAPACITY and is
+ * skipped; L > max_prefix does the same. */
+int medusa_tree_attn(const void* q, const void* k_new, const void* v_new,
+                     void* k_cache, void* v_cache, const int64_t* seq_start,
+                     const int32_t* prefix_len, const int64_t* seq_cap,
+                     const medusa_tree_t* tree, int B, int H, int Dh,
+                     int max_prefix, float rope_theta, float scale,
+                     medusa_dtype dtype, void* out, void* workspace,
+                     size_t workspace_bytes, int32_t* err, void* stream);
+
+/* Scratch bytes medusa_lm_head_verify needs (currently 0). */
+size_t medusa_lm_head_workspace_size(int rows, int d, int V);
+
+/* Verification LM head over every tree row ([MED] Method 3, box step 3):
+ *   logits[r][v] = sum_j hidden[r][j] * w_lm[v][j]
+ * hidden: device [rows][d]; w_lm: device [V][d] (nn.Linear layout);
+ * logits: device [rows][V] float32.  d must be a multiple of 64 for bf16
+ * (of 4 for f32). */
+int medusa_lm_head_verify(const void* hidden, const void* w_lm, float* logits,
+                          int rows, int d, int V, medusa_dtype dtype,
+                          void* workspace, size_t workspace_bytes,
+                          void* stream);
+
+/* Scratch bytes medusa_accept needs. */
+size_t medusa_accept_workspace_size(int B, int T);
+
+/* Acceptance ([MED] Method 5, box steps 4-5; [MEDZ] 二.3).
+ *   logits: device [B][T][V] float32 (the LM head at every tree row);
+ *   tokens: device [B][T] int32, the candidate tokens that were verified.
+ * Node c (c >= 1, parent p) passes when
+ *   mode 0 (greedy):  argmax_v logits[p][v] == tokens[c]  (lowest index wins
+ *                     among equal maxima);
+ *   mode 1 (typical): p^(tokens[c]) > min(eps, delta * exp(-H(p^))), with
+ *                     p^ = softmax(logits[p] / temperature) and H its entropy.
+ * The root always passes; a node is accepted when it and all its ancestors
+ * pass.  The best node is the accepted node of greatest depth; ties go to the
+ * larger summed log p^ (typical), then to the lower node index.
+ * Outputs (device): accept_len [B] = depth of the best node;
+ * accepted_nodes [B][K+1] (root .. best, -1 padded; K = tree->K);
+ * next_root [B] = argmax of the best node's row; best_node [B];
+ * best_logp [B] float32 (summed log p^ of the accepted non-root nodes;
+ * 0 for greedy; nullable). */
+int medusa_accept(const float* logits, const int32_t* tokens,
+                  const medusa_tree_t* tree, int B, int V, int mode,
+                  float temperature, float eps, float delta,
+                  int32_t* accept_len, int32_t* accepted_nodes,
+                  int32_t* next_root, int32_t* best_node, float* best_logp,
+                  void* workspace, size_t workspace_bytes, int32_t* err,
+                  void* stream);
+
+/* KV compaction to the accepted path ([MED] box step 6, Pitfalls: the
+ * accepted KV must be gathered into contiguous slots, not sliced).
+ * For each sequence b with L = prefix_len[b], A = accept_len[b]:
+ *   slot L + j <- slot L + accepted_nodes[b][j] for j = 0..A (K and V; every
+ *   source is read before any destination is written);
+ *   prefix_len[b] = L + A + 1;  src_slots[b][j] = L + accepted_nodes[b][j]
+ *   for j <= A, -1 after (nullable).
+ * accepted_nodes, accept_len, prefix_len (in-out), src_slots: device.
+ * Kmax: the row stride of accepted_nodes minus one (= tree->K). */
+int medusa_kv_compact(void* k_cache, void* v_cache, const int64_t* seq_start,
+                      int32_t* prefix_len, const int32_t* accepted_nodes,
+                      const int32_t* accept_len, int B, int H, int Dh,
+                      int Kmax, medusa_dtype dtype, int32_t* src_slots,
+                      int32_t* err, void* stream);
+
+/* Scratch bytes medusa_heads_topk needs. */
+size_t medusa_heads_topk_workspace_size(int B, int K, int d, int V,
+                                        int s_max);
+
+/* Medusa heads and top-s ([MED] Method 1 and 2; "Paper vs code": optional
+ * ResBlock bias).  For each sequence b and each head k with s[k] > 0:
+ *   h = hidden[b][last_node[b]];
+ *   u = dtype( SiLU(W1_k h + b1_k) + h )        (rounded to the weight type)
+ *   head_logits[b][k] = W2_k u                  (float32)
+ *   topk[b][k][0 .. s[k]-1] = indices of the s[k] largest logits (value
+ *   descending, index ascending); topk[b][k][s[k] ..] = -1.
+ * hidden: device [B][T][d]; last_node: device [B] (row index < T, usually
+ * medusa_accept's best_node); w1: device [K][d][d] (out x in); b1: device
+ * [K][d] or NULL; w2: device [K][V][d]; s: host [K], 0 <= s[k] <= s_max <=
+ * MEDUSA_MAX_S; head_logits: device [B][K][V] (rows of skipped heads are not
+ * written); topk: device [B][K][s_max]. */
+int medusa_heads_topk(const void* hidden, const int32_t* last_node, int T,
+                      const void* w1, const void* b1, const void* w2,
+                      const int32_t* s, int K, int B, int d, int V,
+                      medusa_dtype dtype, float* head_logits, int32_t* topk,
+                      int s_max, void* workspace, size_t workspace_bytes,
+                      int32_t* err, void* stream);
+
+/* Candidate fill for the next step ([MED] box steps 1-2):
+ *   tokens[b][0] = next_root[b];
+ *   tokens[b][n] = topk[b][depth[n]-1][rank[n]-1] for n >= 1.
+ * next_root: device [B]; topk: device [B][K][s_max] with K >= tree->K;
+ * tokens: device [B][T]. */
+int medusa_build_candidates(const int32_t* next_root, const int32_t* topk,
+                            int s_max, int K, const medusa_tree_t* tree,
+                            int B, int32_t* tokens, void* stream);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* MEDUSA_H */

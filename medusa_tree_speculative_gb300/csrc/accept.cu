@@ -1,0 +1,252 @@
+// Acceptance of the longest verified root path.
+//
+// "Medusa: Simple LLM Inference Acceleration Framework with Multiple Decoding
+// Heads", Method 5 (section 2.3.1) and the decoding-step box (steps 4-5):
+// greedy acceptance keeps a candidate while it equals the backbone's argmax at
+// its parent; typical acceptance always takes the first token and keeps each
+// later one while p(x) > min(eps, delta * exp(-H(p))); the step keeps the
+// longest accepted prefix, ties broken by summed log-probability ("Paper vs
+// code", typical acceptance).  Explainer "085 | Medusa", section 二.3: a
+// rejected token ends the accepted prefix.
+//
+// Kernel 1 (one CTA per tree row): argmax of the row and, for typical
+// acceptance, the row's log-sum-exp and entropy at the given temperature.
+// Kernel 2 (one CTA per sequence, one thread per node): per-node decision,
+// the accepted-prefix chain level by level, and the best node.
+#include <math.h>
+
+#include "common.cuh"
+#include "internal.h"
+
+namespace medusa {
+namespace {
+
+struct RowStat {
+  int argmax;
+  float lse;      // log sum_v exp(z_v), z = logits / temperature
+  float entropy;  // H(p^)
+  float pad;
+};
+
+// Running (max, sum e^(z-max), sum e^(z-max)(z-max)) of a softmax, mergeable.
+struct Soft {
+  float m, S, A;
+};
+
+__device__ __forceinline__ Soft soft_merge(Soft x, Soft y) {
+  if (x.m == -INFINITY) return y;
+  if (y.m == -INFINITY) return x;
+  const float M = fmaxf(x.m, y.m);
+  const float ex = expf(x.m - M), ey = expf(y.m - M);
+  Soft r;
+  r.m = M;
+  r.S = x.S * ex + y.S * ey;
+  r.A = ex * (x.A + (x.m - M) * x.S) + ey * (y.A + (y.m - M) * y.S);
+  return r;
+}
+
+template <bool TYPICAL>
+__global__ void __launch_bounds__(512) accept_rowstat_kernel(const float* logits, int T, int V,
+                                                             float inv_temp, RowStat* stats) {
+  const int p = blockIdx.x, b = blockIdx.y;
+  const float* z = logits + ((int64_t)b * T + p) * V;
+  float bv = -INFINITY;
+  int bi = 0x7fffffff;
+  Soft sf{-INFINITY, 0.f, 0.f};
+  for (int v = threadIdx.x; v < V; v += blockDim.x) {
+    const float x = z[v];
+    if (ranks_before(x, v, bv, bi)) { bv = x; bi = v; }
+    if (TYPICAL) {
+      const float y = x * inv_temp;
+      if (y > sf.m) {
+        const float e = expf(sf.m - y);  // 0 when the old max is -inf
+        sf.A = e * (sf.A + (sf.m - y) * sf.S);
+        if (sf.m == -INFINITY) sf.A = 0.f;
+        sf.S = sf.S * e + 1.f;
+        sf.m = y;
+      } else {
+        const float e = expf(y - sf.m);
+        sf.S += e;
+        sf.A += e * (y - sf.m);
+      }
+    }
+  }
+  __shared__ float sv[16], sS[16], sA[16], sm[16];
+  __shared__ int si[16];
+  warp_argmax(bv, bi);
+  if (TYPICAL) {
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+      Soft y{__shfl_xor_sync(0xffffffffu, sf.m, o), __shfl_xor_sync(0xffffffffu, sf.S, o),
+             __shfl_xor_sync(0xffffffffu, sf.A, o)};
+      sf = soft_merge(sf, y);
+    }
+  }
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, nw = blockDim.x >> 5;
+  if (lane == 0) { sv[warp] = bv; si[warp] = bi; sm[warp] = sf.m; sS[warp] = sf.S; sA[warp] = sf.A; }
+  __syncthreads();
+  if (warp == 0) {
+    bv = lane < nw ? sv[lane] : -INFINITY;
+    bi = lane < nw ? si[lane] : 0x7fffffff;
+    warp_argmax(bv, bi);
+    if (TYPICAL) {
+      sf = lane < nw ? Soft{sm[lane], sS[lane], sA[lane]} : Soft{-INFINITY, 0.f, 0.f};
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) {
+        Soft y{__shfl_xor_sync(0xffffffffu, sf.m, o), __shfl_xor_sync(0xffffffffu, sf.S, o),
+               __shfl_xor_sync(0xffffffffu, sf.A, o)};
+        sf = soft_merge(sf, y);
+      }
+    }
+    if (lane == 0) {
+      RowStat r;
+      r.argmax = bi;
+      // H = log S - A / S  (p^_v = e^(z_v - m) / S)
+      r.lse = TYPICAL ? sf.m + logf(sf.S) : 0.f;
+      r.entropy = TYPICAL ? logf(sf.S) - sf.A / sf.S : 0.f;
+      r.pad = 0.f;
+      stats[(int64_t)b * T + p] = r;
+    }
+  }
+}
+
+__global__ void __launch_bounds__(MEDUSA_MAX_T) accept_select_kernel(
+    const float* logits, const int32_t* tokens, medusa_tree_t tree, int V, int mode, float inv_temp,
+    float eps, float delta, const RowStat* stats, int32_t* accept_len, int32_t* accepted_nodes,
+    int32_t* next_root, int32_t* best_node, float* best_logp, int32_t* err) {
+  const int b = blockIdx.x, c = threadIdx.x;
+  const int T = tree.T;
+  __shared__ uint8_t ok[MEDUSA_MAX_T];
+  __shared__ float lp[MEDUSA_MAX_T];
+  __shared__ int dep[MEDUSA_MAX_T];
+  // key of the best node: depth (high bits) then -node index; typical also
+  // compares the summed log-probability, so it is resolved in a second pass
+  __shared__ int red_key[32];
+  __shared__ float red_lp[32];
+  int depth_c = 0, parent_c = -1;
+  bool pass = false;
+  float lpc = 0.f;
+  if (c < T) {
+    depth_c = tree.depth[c];
+    parent_c = tree.parent[c];
+    if (c == 0) {
+      pass = true;
+      depth_c = 0;
+    } else if (parent_c < 0 || parent_c >= c || depth_c < 1 || depth_c > tree.K) {
+      // malformed tree row: never accepted, never followed
+      set_err(err, MEDUSA_DEVERR_NODE);
+      parent_c = 0;
+      depth_c = 0;
+    } else {
+      const int tok = tokens[(int64_t)b * T + c];
+      const RowStat st = stats[(int64_t)b * T + parent_c];
+      if (mode == 0) {
+        pass = tok == st.argmax;
+      } else if (tok < 0 || tok >= V) {
+        set_err(err, MEDUSA_DEVERR_TOKEN);
+      } else {
+        const float zt = logits[((int64_t)b * T + parent_c) * V + tok] * inv_temp;
+        lpc = zt - st.lse;
+        const float thr = fminf(eps, delta * expf(-st.entropy));
+        pass = expf(lpc) > thr;
+      }
+    }
+    dep[c] = depth_c;
+    ok[c] = c == 0 ? 1 : 0;
+    lp[c] = 0.f;
+  }
+  __syncthreads();
+  // the accepted-prefix chain, one depth level at a time
+  for (int k = 1; k <= tree.K; ++k) {
+    if (c < T && depth_c == k) {
+      ok[c] = (pass && ok[parent_c]) ? 1 : 0;
+      lp[c] = lp[parent_c] + lpc;
+    }
+    __syncthreads();
+  }
+  // best node: max depth; typical: then max log-prob; then min index
+  const int warp = c >> 5, lane = c & 31, nw = (blockDim.x + 31) >> 5;
+  int key = (c < T && ok[c]) ? (depth_c << 16) | (0xffff - c) : -1;
+  float mylp = (c < T && ok[c]) ? lp[c] : -INFINITY;
+  // pass 1: deepest accepted depth
+  int kmax = key;
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) kmax = max(kmax, __shfl_xor_sync(0xffffffffu, kmax, o));
+  if (lane == 0) red_key[warp] = kmax;
+  __syncthreads();
+  if (c == 0) {
+    int m = -1;
+    for (int w = 0; w < nw; ++w) m = max(m, red_key[w]);
+    red_key[0] = m;
+  }
+  __syncthreads();
+  const int best_depth = red_key[0] >> 16;
+  __syncthreads();
+  // pass 2 among nodes at that depth: (log-prob for typical, then low index)
+  float cand_lp = (key >= 0 && depth_c == best_depth) ? (mode == 1 ? mylp : 0.f) : -INFINITY;
+  int cand_i = (key >= 0 && depth_c == best_depth) ? c : 0x7fffffff;
+  warp_argmax(cand_lp, cand_i);
+  if (lane == 0) { red_lp[warp] = cand_lp; red_key[warp] = cand_i; }
+  __syncthreads();
+  if (c == 0) {
+    float bl = -INFINITY;
+    int bi = 0x7fffffff;
+    for (int w = 0; w < nw; ++w)
+      if (ranks_before(red_lp[w], red_key[w], bl, bi)) { bl = red_lp[w]; bi = red_key[w]; }
+    if (bi < 0 || bi >= T) bi = 0;  // the root is always accepted
+    const int K = tree.K;
+    int32_t* an = accepted_nodes + (int64_t)b * (K + 1);
+    for (int j = 0; j <= K; ++j) an[j] = -1;
+    // walk parents from the best node: one step per level, depth dep[bi] <= K
+    int n = bi;
+    for (int j = dep[bi]; j >= 0 && n >= 0 && n < T; --j) {
+      an[j] = n;
+      n = j > 0 ? tree.parent[n] : -1;
+    }
+    accept_len[b] = dep[bi];
+    next_root[b] = stats[(int64_t)b * T + bi].argmax;
+    best_node[b] = bi;
+    if (best_logp) best_logp[b] = mode == 1 ? lp[bi] : 0.f;
+  }
+}
+
+}  // namespace
+}  // namespace medusa
+
+using namespace medusa;
+
+extern "C" size_t medusa_accept_workspace_size(int B, int T) {
+  if (B < 1 || T < 1) return 0;
+  return align_up((size_t)B * T * sizeof(RowStat), 256);
+}
+
+extern "C" int medusa_accept(const float* logits, const int32_t* tokens, const medusa_tree_t* tree,
+                             int B, int V, int mode, float temperature, float eps, float delta,
+                             int32_t* accept_len, int32_t* accepted_nodes, int32_t* next_root,
+                             int32_t* best_node, float* best_logp, void* workspace,
+                             size_t workspace_bytes, int32_t* err, void* stream) {
+  const char* fn = "medusa_accept";
+  if (int rc = check_tree(tree, fn)) return rc;
+  if (!logits || !tokens || !accept_len || !accepted_nodes || !next_root || !best_node)
+    return fail(MEDUSA_ERR_INVALID, "%s: NULL tensor", fn);
+  if (B < 1 || B > MEDUSA_MAX_B || V < 1) return fail(MEDUSA_ERR_INVALID, "%s: B=%d V=%d", fn, B, V);
+  if (mode != 0 && mode != 1) return fail(MEDUSA_ERR_INVALID, "%s: mode %d", fn, mode);
+  if (mode == 1 && !(temperature > 0.f)) return fail(MEDUSA_ERR_INVALID, "%s: temperature must be > 0", fn);
+  const size_t need = medusa_accept_workspace_size(B, tree->T);
+  if (!workspace || workspace_bytes < need)
+    return fail(MEDUSA_ERR_WORKSPACE, "%s: workspace %zu < %zu bytes", fn, workspace_bytes, need);
+  cudaStream_t s = as_stream(stream);
+  RowStat* stats = static_cast<RowStat*>(workspace);
+  const float inv_temp = mode == 1 ? 1.f / temperature : 1.f;
+  dim3 g(tree->T, B);
+  if (mode == 1)
+    accept_rowstat_kernel<true><<<g, 512, 0, s>>>(logits, tree->T, V, inv_temp, stats);
+  else
+    accept_rowstat_kernel<false><<<g, 512, 0, s>>>(logits, tree->T, V, inv_temp, stats);
+  if (int rc = check_launch(fn)) return rc;
+  const int threads = (tree->T + 31) / 32 * 32;
+  accept_select_kernel<<<B, threads, 0, s>>>(logits, tokens, *tree, V, mode, inv_temp, eps, delta,
+                                             stats, accept_len, accepted_nodes, next_root, best_node,
+                                             best_logp, err);
+  return check_launch(fn);
+}

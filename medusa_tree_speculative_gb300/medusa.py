@@ -1,0 +1,264 @@
+"""ctypes binding of libmedusa (include/medusa.h): argument marshalling only.
+
+Every function here has the name of the C entry point it calls and takes torch
+tensors (device tensors on the current CUDA device, host tensors or numpy
+arrays where the header says "host").  No arithmetic of the method happens in
+Python; if the library is missing this module raises on import.
+"""
+from __future__ import annotations
+
+import ctypes as C
+import os
+
+import numpy as np
+
+_PKG = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_PKG, "libmedusa.so")
+
+MEDUSA_F32, MEDUSA_BF16 = 0, 1
+MAX_T, MAX_K, MAX_S, MAX_B = 512, 8, 16, 16
+STATUS = {0: "OK", -1: "INVALID", -2: "UNSUPPORTED", -3: "CAPACITY", -4: "WORKSPACE", -5: "CUDA"}
+DEVERR = {1: "TOKEN", 2: "NODE", 4: "CAPACITY", 8: "LENGTH"}
+
+if not os.path.exists(LIB_PATH):
+    raise ImportError(
+        f"{LIB_PATH} is not built; run `python -m medusa_tree_speculative_gb300.build` "
+        "(the CUDA library is required; there is no fallback)")
+
+_lib = C.CDLL(LIB_PATH)
+
+
+class medusa_tree_t(C.Structure):
+    _fields_ = [
+        ("parent", C.c_void_p), ("depth", C.c_void_p), ("rank", C.c_void_p),
+        ("anc_mask", C.c_void_p), ("T", C.c_int32), ("W", C.c_int32), ("K", C.c_int32),
+        ("s", C.c_int32 * MAX_K),
+    ]
+
+
+P, I, F, SZ = C.c_void_p, C.c_int, C.c_float, C.c_size_t
+TREE = C.POINTER(medusa_tree_t)
+
+_SIGS = {
+    "medusa_last_error": (C.c_char_p, []),
+    "medusa_version": (C.c_char_p, []),
+    "medusa_tree_compile": (I, [P, P, I, I, P, P, P, P, P, P, P, P]),
+    "medusa_tree_cartesian": (I, [P, I, I, P, P]),
+    "medusa_tree_greedy": (I, [P, I, I, I, P, P]),
+    "medusa_tree_attn_workspace_size": (SZ, [I, I, I, I, I]),
+    "medusa_tree_attn": (I, [P, P, P, P, P, P, P, P, TREE, I, I, I, I, F, F, I, P, P, SZ, P, P]),
+    "medusa_lm_head_workspace_size": (SZ, [I, I, I]),
+    "medusa_lm_head_verify": (I, [P, P, P, I, I, I, I, P, SZ, P]),
+    "medusa_accept_workspace_size": (SZ, [I, I]),
+    "medusa_accept": (I, [P, P, TREE, I, I, I, F, F, F, P, P, P, P, P, P, SZ, P, P]),
+    "medusa_kv_compact": (I, [P, P, P, P, P, P, I, I, I, I, I, P, P, P]),
+    "medusa_heads_topk_workspace_size": (SZ, [I, I, I, I, I]),
+    "medusa_heads_topk": (I, [P, P, I, P, P, P, P, I, I, I, I, I, P, P, I, P, SZ, P, P]),
+    "medusa_build_candidates": (I, [P, P, I, I, TREE, I, P, P]),
+}
+for _name, (_res, _args) in _SIGS.items():
+    _f = getattr(_lib, _name)
+    _f.restype = _res
+    _f.argtypes = _args
+
+EXPORTS = tuple(_SIGS)
+
+
+class MedusaError(RuntimeError):
+    pass
+
+
+def _check(rc: int, name: str):
+    if rc < 0:
+        msg = _lib.medusa_last_error().decode(errors="replace")
+        raise MedusaError(f"{name} -> {STATUS.get(rc, rc)}: {msg}")
+    return rc
+
+
+def _ptr(t):
+    if t is None:
+        return None
+    if isinstance(t, np.ndarray):
+        assert t.flags["C_CONTIGUOUS"]
+        return t.ctypes.data
+    assert t.is_contiguous(), "libmedusa takes dense row-major tensors"
+    return t.data_ptr()
+
+
+def _dtype(t) -> int:
+    import torch
+
+    if t.dtype == torch.bfloat16:
+        return MEDUSA_BF16
+    if t.dtype == torch.float32:
+        return MEDUSA_F32
+    raise TypeError(f"libmedusa element type must be bfloat16 or float32, got {t.dtype}")
+
+
+def _stream(stream):
+    import torch
+
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream)
+
+
+def medusa_version() -> str:
+    return _lib.medusa_version().decode()
+
+
+# ------------------------------------------------------------ host trees ---
+
+class HostTree:
+    """A compiled tree in host memory (numpy int32 / uint32 arrays)."""
+
+    def __init__(self, parent, depth, rank, anc_mask, s, node_paths, T, K):
+        self.parent, self.depth, self.rank = parent, depth, rank
+        self.anc_mask, self.s, self.node_paths = anc_mask, s, node_paths
+        self.T, self.K, self.W = T, K, (T + 31) // 32
+
+
+def medusa_tree_compile(paths, path_len, max_depth: int) -> HostTree:
+    paths = np.ascontiguousarray(paths, np.int32).reshape(-1, max_depth)
+    path_len = np.ascontiguousarray(path_len, np.int32)
+    n = len(path_len)
+    T = n + 1
+    W = (T + 31) // 32
+    parent = np.zeros(T, np.int32)
+    depth = np.zeros(T, np.int32)
+    rank = np.zeros(T, np.int32)
+    anc = np.zeros(T * W, np.uint32)
+    s = np.zeros(max_depth, np.int32)
+    node_paths = np.zeros((T, max_depth), np.int32)
+    To, Ko = C.c_int(0), C.c_int(0)
+    _check(_lib.medusa_tree_compile(_ptr(paths), _ptr(path_len), n, max_depth, _ptr(parent),
+                                    _ptr(depth), _ptr(rank), _ptr(anc), _ptr(s), _ptr(node_paths),
+                                    C.addressof(To), C.addressof(Ko)), "medusa_tree_compile")
+    return HostTree(parent, depth, rank, anc.reshape(T, W), s, node_paths, To.value, Ko.value)
+
+
+def medusa_tree_cartesian(s, max_nodes: int):
+    s = np.ascontiguousarray(s, np.int32)
+    K = len(s)
+    paths = np.zeros((max(max_nodes, 1), K), np.int32)
+    plen = np.zeros(max(max_nodes, 1), np.int32)
+    n = _check(_lib.medusa_tree_cartesian(_ptr(s), K, max_nodes, _ptr(paths), _ptr(plen)),
+               "medusa_tree_cartesian")
+    return paths[:n].copy(), plen[:n].copy()
+
+
+def medusa_tree_greedy(acc, budget: int):
+    acc = np.ascontiguousarray(acc, np.float64)
+    K, R = acc.shape
+    paths = np.zeros((max(budget, 1), K), np.int32)
+    plen = np.zeros(max(budget, 1), np.int32)
+    n = _check(_lib.medusa_tree_greedy(_ptr(acc), K, R, budget, _ptr(paths), _ptr(plen)),
+               "medusa_tree_greedy")
+    return paths[:n].copy(), plen[:n].copy()
+
+
+class DeviceTree:
+    """A HostTree copied to the GPU, with the medusa_tree_t that points at it."""
+
+    def __init__(self, ht: HostTree, device="cuda"):
+        import torch
+
+        self.host = ht
+        self.parent = torch.from_numpy(ht.parent).to(device)
+        self.depth = torch.from_numpy(ht.depth).to(device)
+        self.rank = torch.from_numpy(ht.rank).to(device)
+        self.anc_mask = torch.from_numpy(ht.anc_mask.view(np.int32).copy()).to(device)
+        self.T, self.K, self.W = ht.T, ht.K, ht.W
+        self.struct = medusa_tree_t()
+        self.struct.parent = self.parent.data_ptr()
+        self.struct.depth = self.depth.data_ptr()
+        self.struct.rank = self.rank.data_ptr()
+        self.struct.anc_mask = self.anc_mask.data_ptr()
+        self.struct.T, self.struct.W, self.struct.K = ht.T, ht.W, ht.K
+        for k in range(min(len(ht.s), MAX_K)):
+            self.struct.s[k] = int(ht.s[k])
+
+    @property
+    def ref(self):
+        return C.byref(self.struct)
+
+    @property
+    def s(self):
+        return [int(self.struct.s[k]) for k in range(self.K)]
+
+
+# ------------------------------------------------------------ step calls ---
+
+def medusa_tree_attn_workspace_size(B, H, Dh, T, max_prefix) -> int:
+    return int(_lib.medusa_tree_attn_workspace_size(B, H, Dh, T, max_prefix))
+
+
+def medusa_tree_attn(q, k_new, v_new, k_cache, v_cache, seq_start, prefix_len, seq_cap,
+                     tree: DeviceTree, max_prefix: int, rope_theta: float, scale: float, out,
+                     workspace, err=None, stream=None):
+    B, T, H, Dh = q.shape
+    _check(_lib.medusa_tree_attn(_ptr(q), _ptr(k_new), _ptr(v_new), _ptr(k_cache), _ptr(v_cache),
+                                 _ptr(seq_start), _ptr(prefix_len), _ptr(seq_cap), tree.ref, B, H, Dh,
+                                 max_prefix, rope_theta, scale, _dtype(q), _ptr(out), _ptr(workspace),
+                                 workspace.numel() * workspace.element_size(), _ptr(err),
+                                 _stream(stream)), "medusa_tree_attn")
+
+
+def medusa_lm_head_workspace_size(rows, d, V) -> int:
+    return int(_lib.medusa_lm_head_workspace_size(rows, d, V))
+
+
+def medusa_lm_head_verify(hidden, w_lm, logits, workspace=None, stream=None):
+    d = hidden.shape[-1]
+    rows = hidden.numel() // d
+    V = w_lm.shape[0]
+    nbytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    _check(_lib.medusa_lm_head_verify(_ptr(hidden), _ptr(w_lm), _ptr(logits), rows, d, V, _dtype(hidden),
+                                      _ptr(workspace), nbytes, _stream(stream)), "medusa_lm_head_verify")
+
+
+def medusa_accept_workspace_size(B, T) -> int:
+    return int(_lib.medusa_accept_workspace_size(B, T))
+
+
+def medusa_accept(logits, tokens, tree: DeviceTree, mode: int, temperature: float, eps: float,
+                  delta: float, accept_len, accepted_nodes, next_root, best_node, best_logp, workspace,
+                  err=None, stream=None):
+    B, T, V = logits.shape
+    _check(_lib.medusa_accept(_ptr(logits), _ptr(tokens), tree.ref, B, V, mode, temperature, eps, delta,
+                              _ptr(accept_len), _ptr(accepted_nodes), _ptr(next_root), _ptr(best_node),
+                              _ptr(best_logp), _ptr(workspace),
+                              workspace.numel() * workspace.element_size(), _ptr(err), _stream(stream)),
+           "medusa_accept")
+
+
+def medusa_kv_compact(k_cache, v_cache, seq_start, prefix_len, accepted_nodes, accept_len, Kmax: int,
+                      src_slots=None, err=None, stream=None):
+    _, H, Dh = k_cache.shape
+    B = prefix_len.numel()
+    _check(_lib.medusa_kv_compact(_ptr(k_cache), _ptr(v_cache), _ptr(seq_start), _ptr(prefix_len),
+                                  _ptr(accepted_nodes), _ptr(accept_len), B, H, Dh, Kmax, _dtype(k_cache),
+                                  _ptr(src_slots), _ptr(err), _stream(stream)), "medusa_kv_compact")
+
+
+def medusa_heads_topk_workspace_size(B, K, d, V, s_max) -> int:
+    return int(_lib.medusa_heads_topk_workspace_size(B, K, d, V, s_max))
+
+
+def medusa_heads_topk(hidden, last_node, w1, b1, w2, s, head_logits, topk, workspace, err=None,
+                      stream=None):
+    B, T, d = hidden.shape
+    K, V = w2.shape[0], w2.shape[1]
+    s_arr = np.ascontiguousarray(s, np.int32)
+    assert len(s_arr) == K
+    s_max = topk.shape[-1]
+    _check(_lib.medusa_heads_topk(_ptr(hidden), _ptr(last_node), T, _ptr(w1), _ptr(b1), _ptr(w2),
+                                  _ptr(s_arr), K, B, d, V, _dtype(hidden), _ptr(head_logits), _ptr(topk),
+                                  s_max, _ptr(workspace), workspace.numel() * workspace.element_size(),
+                                  _ptr(err), _stream(stream)), "medusa_heads_topk")
+
+
+def medusa_build_candidates(next_root, topk, tree: DeviceTree, tokens, stream=None):
+    B, K, s_max = topk.shape
+    _check(_lib.medusa_build_candidates(_ptr(next_root), _ptr(topk), s_max, K, tree.ref, B, _ptr(tokens),
+                                        _stream(stream)), "medusa_build_candidates")

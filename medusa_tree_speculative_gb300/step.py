@@ -1,0 +1,105 @@
+"""One Medusa verify step on one GPU: device buffers and the order of the six
+library calls.  Plumbing only: every step of the method runs in libmedusa.
+
+Call order (decoding-step box of the Medusa paper digest, steps 3-6 then 1-2
+for the next step):
+  medusa_tree_attn -> medusa_lm_head_verify -> medusa_accept ->
+  medusa_kv_compact -> medusa_heads_topk -> medusa_build_candidates
+"""
+from __future__ import annotations
+
+import math
+
+import numpy as np
+import torch
+
+from . import medusa as M
+
+TORCH_DT = {"bf16": torch.bfloat16, "f32": torch.float32}
+
+
+def host_to_torch(a: np.ndarray, dt: str) -> torch.Tensor:
+    """numpy (float32, or bf16 bits as uint16) -> CPU torch tensor of dtype dt."""
+    if a.dtype == np.uint16:
+        return torch.from_numpy(a.view(np.int16)).view(torch.bfloat16)
+    t = torch.from_numpy(a)
+    return t if dt == "f32" else t.to(torch.bfloat16)
+
+
+def build_tree(w: dict) -> M.HostTree:
+    """The workload's candidate tree via the library's host helpers."""
+    kind = w["tree"][0]
+    if kind == "cartesian":
+        s, max_nodes = w["tree"][1], w["tree"][2]
+        n = max_nodes if max_nodes is not None else sum(math.prod(s[:k]) for k in range(1, len(s) + 1))
+        paths, plen = M.medusa_tree_cartesian(list(s), n)
+        return M.medusa_tree_compile(paths, plen, len(s))
+    budget, R = w["tree"][1], w["tree"][2]
+    from .synth import accuracy_table
+
+    paths, plen = M.medusa_tree_greedy(accuracy_table(w["K"], R), budget)
+    return M.medusa_tree_compile(paths, plen, w["K"])
+
+
+class VerifyStep:
+    """Owns the outputs and scratch of one verify step for fixed shapes."""
+
+    def __init__(self, w: dict, weights: dict, tree: M.DeviceTree, max_prefix: int, device="cuda"):
+        self.w, self.tree, self.max_prefix = w, tree, max_prefix
+        B, H, Dh, d, V, K = w["B"], w["H"], w["Dh"], w["d"], w["V"], w["K"]
+        T = tree.T
+        self.B, self.T = B, T
+        dt = TORCH_DT[w["dtype"]]
+        self.w_lm, self.w1, self.b1, self.w2 = weights["w_lm"], weights["w1"], weights.get("b1"), weights["w2"]
+        # heads that feed a tree level run; the others are skipped (s_k = 0)
+        self.s_heads = [tree.s[k] if k < tree.K else 0 for k in range(K)]
+        self.s_max = max(1, max(self.s_heads))
+        self.mode = 1 if w["mode"] == "typical" else 0
+        self.temperature = float(w.get("temperature", 1.0))
+        self.eps, self.delta = float(w.get("eps", 0.09)), float(w.get("delta", 0.3))
+        self.rope_theta = float(w.get("rope_theta", 10000.0))
+        self.scale = 1.0 / math.sqrt(Dh)
+        i32 = dict(dtype=torch.int32, device=device)
+        self.out = torch.empty((B, T, H, Dh), dtype=dt, device=device)
+        self.logits = torch.empty((B, T, V), dtype=torch.float32, device=device)
+        self.accept_len = torch.zeros(B, **i32)
+        self.accepted_nodes = torch.zeros((B, tree.K + 1), **i32)
+        self.next_root = torch.zeros(B, **i32)
+        self.best_node = torch.zeros(B, **i32)
+        self.best_logp = torch.zeros(B, dtype=torch.float32, device=device)
+        self.src_slots = torch.zeros((B, tree.K + 1), **i32)
+        self.head_logits = torch.zeros((B, K, V), dtype=torch.float32, device=device)
+        self.topk = torch.zeros((B, K, self.s_max), **i32)
+        self.next_tokens = torch.zeros((B, T), **i32)
+        self.err = torch.zeros(1, **i32)
+
+        def ws(n):
+            return torch.empty(max(int(n), 256), dtype=torch.uint8, device=device)
+
+        self.ws_attn = ws(M.medusa_tree_attn_workspace_size(B, H, Dh, T, max_prefix))
+        self.ws_accept = ws(M.medusa_accept_workspace_size(B, T))
+        self.ws_heads = ws(M.medusa_heads_topk_workspace_size(B, K, d, V, self.s_max))
+
+    def run(self, x: dict, stream=None):
+        """x: device tensors q, k_new, v_new, hidden, tokens, k_cache, v_cache,
+        seq_start, prefix_len, seq_cap.  Updates the cache and prefix_len."""
+        B, T = self.B, self.T
+        M.medusa_tree_attn(x["q"], x["k_new"], x["v_new"], x["k_cache"], x["v_cache"], x["seq_start"],
+                           x["prefix_len"], x["seq_cap"], self.tree, self.max_prefix, self.rope_theta,
+                           self.scale, self.out, self.ws_attn, self.err, stream)
+        M.medusa_lm_head_verify(x["hidden"], self.w_lm, self.logits, None, stream)
+        M.medusa_accept(self.logits, x["tokens"], self.tree, self.mode, self.temperature, self.eps,
+                        self.delta, self.accept_len, self.accepted_nodes, self.next_root, self.best_node,
+                        self.best_logp, self.ws_accept, self.err, stream)
+        M.medusa_kv_compact(x["k_cache"], x["v_cache"], x["seq_start"], x["prefix_len"],
+                            self.accepted_nodes, self.accept_len, self.tree.K, self.src_slots, self.err,
+                            stream)
+        M.medusa_heads_topk(x["hidden"], self.best_node, self.w1, self.b1, self.w2, self.s_heads,
+                            self.head_logits, self.topk, self.ws_heads, self.err, stream)
+        M.medusa_build_candidates(self.next_root, self.topk, self.tree, self.next_tokens, stream)
+
+    @property
+    def launches_per_step(self) -> int:
+        """Kernels one run() launches: attention 3 (2 for f32), LM head 1,
+        accept 2, compaction 1, heads 3, candidates 1."""
+        return (3 if self.w["dtype"] == "bf16" else 2) + 1 + 2 + 1 + 3 + 1

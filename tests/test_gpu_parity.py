@@ -1,0 +1,410 @@
+"""GPU parity: every libmedusa call against the CPU oracle on the same seeded
+inputs, through the C ABI.
+
+Bars: integer and index outputs (accepted path, lengths, next root, top-s
+indices, candidate tokens, compacted cache rows) bit-exact; floating point
+within the stated tolerances: attention max-abs 2e-2 and logits
+2e-2 * max|logit| for bf16 (float32: 1e-4 and 1e-5 * max|logit|, from the
+float32 accumulation error bound at these sizes).  Where floating point decides
+an integer (an argmax or a top-s boundary), decisions are compared where the
+oracle's margin exceeds the GPU's rounding error and checked for validity
+against the GPU's own logits elsewhere.
+"""
+import math
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from medusa_tree_speculative_gb300 import synth
+from parity_util import (ancestors, as_double, both_trees, plant_tokens, row_gaps, to_dev, to_host)
+
+pytestmark = pytest.mark.gpu
+
+TOL = {"f32": dict(attn=1e-4, logit=1e-5), "bf16": dict(attn=2e-2, logit=2e-2)}
+
+
+@pytest.fixture(scope="module")
+def M():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    from medusa_tree_speculative_gb300 import build
+
+    build.build()
+    from medusa_tree_speculative_gb300 import medusa
+
+    return medusa
+
+
+def err_flag():
+    return torch.zeros(1, dtype=torch.int32, device="cuda")
+
+
+# ----------------------------------------------------------- tree attention
+
+def _attn_case(M, dt, H, Dh, L, spec, seed):
+    ot, dtree = both_trees(M, spec)
+    T, B = ot.T, len(L)
+    q = synth.normal(seed, "q", (B, T, H, Dh), 1.0, dt)
+    kn = synth.normal(seed, "k_new", (B, T, H, Dh), 1.0, dt)
+    vn = synth.normal(seed, "v_new", (B, T, H, Dh), 1.0, dt)
+    cap = np.array(L, np.int64) + T + 3
+    st = np.concatenate([[0], np.cumsum(cap)[:-1]]).astype(np.int64)
+    edt = np.uint16 if dt == "bf16" else np.float32
+    kc = np.zeros((int(cap.sum()), H, Dh), edt)
+    vc = np.zeros_like(kc)
+    for b in range(B):
+        kc[st[b]:st[b] + L[b]] = synth.normal(seed, f"kp{b}", (L[b], H, Dh), 1.0, dt)
+        vc[st[b]:st[b] + L[b]] = synth.normal(seed, f"vp{b}", (L[b], H, Dh), 1.0, dt)
+    pl = np.array(L, np.int32)
+    return ot, dtree, q, kn, vn, kc, vc, st, pl, cap
+
+
+ATTN_CASES = [
+    # dtype, H, Dh, prefix lengths, tree
+    ("f32", 4, 64, [64], ("cartesian", (2, 2, 2), None)),
+    ("f32", 2, 128, [33, 0], ("cartesian", (2, 3), None)),
+    ("bf16", 4, 64, [64], ("cartesian", (2, 2, 2), None)),
+    ("bf16", 4, 64, [100, 37], ("cartesian", (2, 2, 2), None)),
+    ("bf16", 2, 128, [1000], ("greedy", 4, 10, 64)),
+    ("bf16", 3, 128, [0], ("greedy", 4, 10, 64)),
+    ("bf16", 2, 128, [130], ("cartesian", (1,), 0)),              # root only
+    ("bf16", 2, 128, [300], ("cartesian", (4, 4, 4, 4), 256)),     # 257 rows
+    ("bf16", 1, 64, [70], ("cartesian", (8, 8, 8), 511)),          # 512 rows (maximum)
+    ("bf16", 3, 128, [4096, 777, 5], ("greedy", 5, 10, 64)),
+]
+
+
+@pytest.mark.parametrize("case", ATTN_CASES, ids=lambda c: f"{c[0]}-H{c[1]}-Dh{c[2]}-L{c[3]}-{c[4][0]}")
+def test_tree_attn(M, case):
+    dt, H, Dh, L, spec = case
+    ot, dtree, q, kn, vn, kc, vc, st, pl, cap = _attn_case(M, dt, H, Dh, L, spec, seed=3)
+    B, T = len(L), ot.T
+    scale = 1.0 / math.sqrt(Dh)
+    # GPU
+    kc_d, vc_d = to_dev(kc), to_dev(vc)
+    out_d = to_dev(np.zeros_like(q))
+    ws = torch.empty(M.medusa_tree_attn_workspace_size(B, H, Dh, T, max(L)), dtype=torch.uint8, device="cuda")
+    e = err_flag()
+    M.medusa_tree_attn(to_dev(q), to_dev(kn), to_dev(vn), kc_d, vc_d, to_dev(st), to_dev(pl), to_dev(cap),
+                       dtree, max(L), 10000.0, scale, out_d, ws, e)
+    torch.cuda.synchronize()
+    assert int(e.item()) == 0
+    # oracle
+    kc_o, vc_o = kc.copy(), vc.copy()
+    _, ref = oracle.tree_attn(q, kn, vn, kc_o, vc_o, st, pl, ot, 10000.0, scale)
+    got = as_double(to_host(out_d))
+    err = np.abs(got - ref).max()
+    assert err <= TOL[dt]["attn"], f"attention max-abs error {err}"
+    # cache: prefix untouched, V rows copied exactly, K rows rotated
+    kg, vg = to_host(kc_d), to_host(vc_d)
+    for b in range(B):
+        assert np.array_equal(kg[st[b]:st[b] + L[b]], kc[st[b]:st[b] + L[b]])
+        tail = slice(st[b] + L[b], st[b] + L[b] + T)
+        assert np.array_equal(vg[tail], vc_o[tail])
+        # rotation in float32 (GPU) vs double (oracle), then rounding to the
+        # cache type: at most one unit in the last place apart
+        kref = as_double(kc_o[tail])
+        kerr = np.abs(as_double(kg[tail]) - kref)
+        bound = (2.0 ** -7 if dt == "bf16" else 2.0 ** -21) * np.abs(kref) + 1e-6
+        assert np.all(kerr <= bound)
+        # slots past the tree rows stay zero
+        assert not np.any(vg[st[b] + L[b] + T:st[b] + cap[b]].astype(np.float64))
+
+
+def test_tree_attn_capacity_flag(M):
+    ot, dtree, q, kn, vn, kc, vc, st, pl, cap = _attn_case(M, "bf16", 2, 64, [40, 20], ("cartesian", (2, 2), None), 5)
+    cap = cap.copy()
+    cap[1] = pl[1] + ot.T - 1  # one slot short
+    B, T = 2, ot.T
+    ws = torch.empty(M.medusa_tree_attn_workspace_size(B, 2, 64, T, 40), dtype=torch.uint8, device="cuda")
+    out = torch.full((B, T, 2, 64), 7.0, dtype=torch.bfloat16, device="cuda")
+    e = err_flag()
+    kc_d = to_dev(kc)
+    M.medusa_tree_attn(to_dev(q), to_dev(kn), to_dev(vn), kc_d, to_dev(vc), to_dev(st), to_dev(pl), to_dev(cap),
+                       dtree, 40, 10000.0, 0.125, out, ws, e)
+    torch.cuda.synchronize()
+    assert int(e.item()) & 4
+    o = out.float().cpu().numpy()
+    assert np.all(o[1] == 7.0)          # skipped sequence untouched
+    assert not np.all(o[0] == 7.0)      # the other one computed
+    assert np.array_equal(to_host(kc_d)[st[1]:st[1] + 40], kc[st[1]:st[1] + 40])
+
+
+# ----------------------------------------------------------------- LM head
+
+LM_CASES = [("f32", 15, 256, 1024), ("bf16", 15, 256, 1024), ("bf16", 65, 256, 1000),
+            ("bf16", 130, 512, 3000), ("bf16", 1, 64, 17), ("bf16", 260, 128, 333),
+            ("bf16", 65, 4096, 2048)]
+
+
+@pytest.mark.parametrize("case", LM_CASES, ids=lambda c: "-".join(map(str, c)))
+def test_lm_head(M, case):
+    dt, rows, d, V = case
+    h = synth.normal(11, "h", (rows, d), 1.0, dt)
+    w = synth.normal(11, "w", (V, d), 1.0 / math.sqrt(d), dt)
+    logits = torch.empty((rows, V), dtype=torch.float32, device="cuda")
+    M.medusa_lm_head_verify(to_dev(h), to_dev(w), logits)
+    torch.cuda.synchronize()
+    ref = oracle.lm_head(h, w)
+    err = np.abs(to_host(logits) - ref).max()
+    scale = np.abs(ref).max()
+    assert err <= TOL[dt]["logit"] * scale, f"logit error {err} vs max|logit| {scale}"
+
+
+# -------------------------------------------------------------- acceptance
+
+def _accept_inputs(ot, B, V, mode, seed, plant_nodes):
+    """Synthetic float32 logits; tokens planted so that the node passes."""
+    rng = np.random.default_rng(seed)
+    T = ot.T
+    logits = (rng.standard_normal((B, T, V)) * 2.0).astype(np.float32)
+    tokens = np.zeros((B, T), np.int32)
+    for b in range(B):
+        node = plant_nodes[b]
+        path = set(ancestors(ot.parent, node))
+        for c in range(1, T):
+            p = ot.parent[c]
+            if c in path:
+                if mode == 0:
+                    tokens[b, c] = int(np.argmax(logits[b, p]))
+                else:
+                    t = int(rng.integers(0, V))
+                    logits[b, p, t] = logits[b, p].max() + 1.0  # a confident token passes
+                    tokens[b, c] = t
+            else:
+                t = int(rng.integers(0, V))
+                if mode == 0 and t == int(np.argmax(logits[b, p])):
+                    t = (t + 1) % V  # off the planted path nothing passes
+                tokens[b, c] = t
+    return logits, tokens
+
+
+def _gpu_accept(M, dtree, logits, tokens, mode, temp=0.7, eps=0.09, delta=0.3):
+    B, T, V = logits.shape
+    K = dtree.K
+    out = dict(accept_len=torch.zeros(B, dtype=torch.int32, device="cuda"),
+               accepted_nodes=torch.zeros((B, K + 1), dtype=torch.int32, device="cuda"),
+               next_root=torch.zeros(B, dtype=torch.int32, device="cuda"),
+               best_node=torch.zeros(B, dtype=torch.int32, device="cuda"),
+               best_logp=torch.zeros(B, dtype=torch.float32, device="cuda"))
+    ws = torch.empty(M.medusa_accept_workspace_size(B, T), dtype=torch.uint8, device="cuda")
+    e = err_flag()
+    M.medusa_accept(to_dev(logits), to_dev(tokens), dtree, mode, temp, eps, delta, out["accept_len"],
+                    out["accepted_nodes"], out["next_root"], out["best_node"], out["best_logp"], ws, e)
+    torch.cuda.synchronize()
+    return {k: to_host(v) for k, v in out.items()}, int(e.item())
+
+
+ACCEPT_CASES = [
+    (("cartesian", (3, 2, 2), None), 50, 0),
+    (("cartesian", (3, 2, 2), None), 50, 1),
+    (("greedy", 4, 10, 64), 32000, 0),
+    (("greedy", 4, 10, 64), 32000, 1),
+    (("cartesian", (4, 4, 4, 4), 256), 1000, 0),
+    (("cartesian", (8, 8, 8), 511), 100, 1),
+    (("cartesian", (1,), 0), 100, 0),
+]
+
+
+@pytest.mark.parametrize("case", ACCEPT_CASES, ids=lambda c: f"{c[0][0]}{c[0][1]}-V{c[1]}-mode{c[2]}")
+def test_accept(M, case):
+    spec, V, mode = case
+    ot, dtree = both_trees(M, spec)
+    T = ot.T
+    rng = np.random.default_rng(7)
+    # every node once as the planted endpoint, three sequences per call
+    nodes = list(range(T)) if T <= 70 else list(rng.integers(0, T, 12))
+    for i in range(0, len(nodes), 3):
+        plant = [int(n) for n in nodes[i:i + 3]]
+        B = len(plant)
+        for attempt in range(20):
+            logits, tokens = _accept_inputs(ot, B, V, mode, seed=100 + i + 1000 * attempt, plant_nodes=plant)
+            r = oracle.accept(logits, tokens, ot, mode, temperature=0.7, eps=0.09, delta=0.3)
+            # a typical decision closer to its threshold than float32 rounding
+            # of p-hat could go either way; draw another input instead
+            if mode == 0 or T == 1 or np.abs(r["node_margin"][:, 1:]).min() > 1e-6:
+                break
+        else:
+            raise AssertionError("no unambiguous typical input found")
+        g, e = _gpu_accept(M, dtree, logits, tokens, mode)
+        assert e == 0
+        for key in ("accept_len", "accepted_nodes", "next_root", "best_node"):
+            assert np.array_equal(g[key], r[key]), (key, g[key], r[key])
+        if mode == 0:
+            for b, n in enumerate(plant):
+                assert g["accept_len"][b] == ot.depth[n]
+        else:
+            assert np.allclose(g["best_logp"], r["best_logp"], rtol=1e-4, atol=1e-4)
+
+
+def test_accept_typical_tie_break_and_low_temperature(M):
+    ot, dtree = both_trees(M, ("cartesian", (2,), None))
+    V = 4
+    logits = np.log(np.array([[[0.1, 0.5, 0.4, 1e-9]] * 3], np.float64)).astype(np.float32)
+    tokens = np.array([[0, 2, 1]], np.int32)
+    g, _ = _gpu_accept(M, dtree, logits, tokens, 1, temp=1.0)
+    assert g["best_node"][0] == 2 and g["accept_len"][0] == 1
+    # temperature -> 0: typical reduces to greedy
+    ot2, dt2 = both_trees(M, ("cartesian", (3, 2, 2), None))
+    for node in range(0, ot2.T, 4):
+        lg, tk = _accept_inputs(ot2, 1, 64, 0, seed=500 + node, plant_nodes=[node])
+        gg, _ = _gpu_accept(M, dt2, lg, tk, 0)
+        gt, _ = _gpu_accept(M, dt2, lg, tk, 1, temp=1e-3)
+        for key in ("accept_len", "accepted_nodes", "next_root", "best_node"):
+            assert np.array_equal(gg[key], gt[key])
+
+
+def test_accept_bad_token_flag(M):
+    ot, dtree = both_trees(M, ("cartesian", (2, 2), None))
+    logits = np.zeros((1, ot.T, 10), np.float32)
+    tokens = np.array([[0, 3, 99, 1, 1, 1, 1]], np.int32)
+    g, e = _gpu_accept(M, dtree, logits, tokens, 1, temp=1.0)
+    assert e & 1
+    assert g["accept_len"][0] >= 0
+
+
+# ------------------------------------------------------------ KV compaction
+
+@pytest.mark.parametrize("dt", ["bf16", "f32"])
+def test_kv_compact(M, dt):
+    ot, dtree = both_trees(M, ("greedy", 4, 10, 64))
+    H, Dh, K = 4, 64, ot.K
+    L = [50, 9, 300]
+    B, T = 3, ot.T
+    cap = np.array(L, np.int64) + T
+    st = np.concatenate([[0], np.cumsum(cap)[:-1]]).astype(np.int64)
+    kc = synth.normal(9, "kc", (int(cap.sum()), H, Dh), 1.0, dt)
+    vc = synth.normal(9, "vc", (int(cap.sum()), H, Dh), 1.0, dt)
+    rng = np.random.default_rng(9)
+    nodes = [int(rng.integers(0, T)) for _ in range(B)]
+    nodes[0] = max(range(T), key=lambda n: ot.depth[n])  # a deepest node
+    acc_nodes = np.full((B, K + 1), -1, np.int32)
+    acc_len = np.zeros(B, np.int32)
+    for b, n in enumerate(nodes):
+        path = ancestors(ot.parent, n)
+        acc_nodes[b, :len(path)] = path
+        acc_len[b] = len(path) - 1
+    pl = np.array(L, np.int32)
+    kd, vd, pld = to_dev(kc), to_dev(vc), to_dev(pl)
+    src = torch.zeros((B, K + 1), dtype=torch.int32, device="cuda")
+    e = err_flag()
+    M.medusa_kv_compact(kd, vd, to_dev(st), pld, to_dev(acc_nodes), to_dev(acc_len), K, src, e)
+    torch.cuda.synchronize()
+    assert int(e.item()) == 0
+    ko, vo, plo = kc.copy(), vc.copy(), pl.copy()
+    so = oracle.kv_compact(ko, vo, st, plo, acc_nodes, acc_len, K)
+    assert np.array_equal(to_host(kd), ko) and np.array_equal(to_host(vd), vo)
+    assert np.array_equal(to_host(pld), plo) and np.array_equal(to_host(src), so)
+
+
+def test_kv_compact_in_place_hazard(M):
+    # accepted nodes (0, 2, 3): row 1 reads slot L+2, which row 2 overwrites
+    H, Dh = 2, 64
+    kc = np.arange(20 * H * Dh, dtype=np.float32).reshape(20, H, Dh)
+    vc = -kc
+    st, pl = np.array([0], np.int64), np.array([5], np.int32)
+    an, al = np.array([[0, 2, 3, -1]], np.int32), np.array([2], np.int32)
+    kd, vd, pld = to_dev(kc), to_dev(vc), to_dev(pl)
+    M.medusa_kv_compact(kd, vd, to_dev(st), pld, to_dev(an), to_dev(al), 3)
+    ko, vo = kc.copy(), vc.copy()
+    oracle.kv_compact(ko, vo, st, pl.copy(), an, al, 3)
+    torch.cuda.synchronize()
+    assert np.array_equal(to_host(kd), ko) and np.array_equal(to_host(vd), vo)
+    assert to_host(pld)[0] == 8
+
+
+# ------------------------------------------------------------------- heads
+
+HEAD_CASES = [
+    # dtype, B, T, d, V, s per head, bias, W2 = LM head + noise
+    ("f32", 1, 15, 256, 1024, (2, 2, 2), False, True),
+    ("bf16", 1, 65, 256, 1000, (8, 6, 5, 2), False, False),
+    ("bf16", 3, 65, 512, 3000, (8, 6, 5, 2, 0), True, False),
+    ("bf16", 4, 9, 640, 5000, (16, 1), False, False),
+    ("bf16", 1, 65, 4096, 32000, (8, 6, 5, 2), False, False),
+]
+
+
+@pytest.mark.parametrize("case", HEAD_CASES, ids=lambda c: f"{c[0]}-B{c[1]}-d{c[3]}-V{c[4]}-s{len(c[5])}")
+def test_heads_topk(M, case):
+    dt, B, T, d, V, s, bias, lm_noise = case
+    K = len(s)
+    s_max = max(s)
+    hidden = synth.normal(13, "hidden", (B, T, d), 1.0, dt)
+    w1 = synth.normal(13, "w1", (K, d, d), 0.02 if lm_noise else 1 / math.sqrt(d), dt)
+    if lm_noise:
+        lm = synth.normal(13, "lm", (V, d), 1 / math.sqrt(d), "f32")
+        w2 = np.stack([lm + synth.normal(13, f"n{k}", (V, d), 0.01, "f32") for k in range(K)])
+        w2 = w2 if dt == "f32" else synth.f32_to_bf16_bits(w2)
+    else:
+        w2 = synth.normal(13, "w2", (K, V, d), 1 / math.sqrt(d), dt)
+    b1 = synth.normal(13, "b1", (K, d), 0.5, dt) if bias else None
+    last = np.array([(3 * b + 1) % T for b in range(B)], np.int32)
+    hl = torch.zeros((B, K, V), dtype=torch.float32, device="cuda")
+    tk = torch.zeros((B, K, s_max), dtype=torch.int32, device="cuda")
+    ws = torch.empty(M.medusa_heads_topk_workspace_size(B, K, d, V, s_max), dtype=torch.uint8, device="cuda")
+    e = err_flag()
+    M.medusa_heads_topk(to_dev(hidden), to_dev(last), to_dev(w1), None if b1 is None else to_dev(b1), to_dev(w2),
+                        list(s), hl, tk, ws, e)
+    torch.cuda.synchronize()
+    assert int(e.item()) == 0
+    z_ref, tk_ref, _ = oracle.heads(hidden, last, w1, b1, w2, list(s), s_max)
+    zg, tg = to_host(hl), to_host(tk)
+    for b in range(B):
+        for k in range(K):
+            if s[k] == 0:
+                assert np.all(tg[b, k] == 0)  # skipped head: untouched
+                continue
+            scale = np.abs(z_ref[b, k]).max()
+            err = np.abs(zg[b, k] - z_ref[b, k]).max()
+            assert err <= TOL[dt]["logit"] * scale, f"head logit error {err} (max {scale})"
+            # validity: the GPU's top-s is the exact top-s of its own logits
+            order = np.lexsort((np.arange(V), -zg[b, k].astype(np.float64)))[:s[k]]
+            assert list(tg[b, k, :s[k]]) == list(order)
+            assert np.all(tg[b, k, s[k]:] == -1)
+            # parity with the oracle where the ranking is decided by more than
+            # the GPU's rounding error
+            srt = np.sort(z_ref[b, k])[::-1]
+            gaps = srt[:s[k]] - srt[1:s[k] + 1]
+            if gaps.min() > 1e-3 * scale:
+                assert list(tg[b, k, :s[k]]) == list(tk_ref[b, k, :s[k]])
+
+
+def test_heads_init_reproduce_lm_head(M):
+    """W1 = 0, W2 = the LM head: every head's top-1 is the LM head's argmax."""
+    d, V, K, T = 256, 1000, 3, 7
+    hidden = synth.normal(17, "h", (1, T, d), 1.0, "bf16")
+    wlm = synth.normal(17, "w", (V, d), 1 / math.sqrt(d), "bf16")
+    w1 = np.zeros((K, d, d), np.uint16)
+    w2 = np.ascontiguousarray(np.broadcast_to(wlm, (K, V, d)))
+    last = np.array([4], np.int32)
+    hl = torch.zeros((1, K, V), dtype=torch.float32, device="cuda")
+    tk = torch.zeros((1, K, 2), dtype=torch.int32, device="cuda")
+    ws = torch.empty(M.medusa_heads_topk_workspace_size(1, K, d, V, 2), dtype=torch.uint8, device="cuda")
+    M.medusa_heads_topk(to_dev(hidden), to_dev(last), to_dev(w1), None, to_dev(w2), [2, 2, 2], hl, tk, ws)
+    logits = torch.empty((T, V), dtype=torch.float32, device="cuda")
+    M.medusa_lm_head_verify(to_dev(hidden), to_dev(wlm), logits)
+    torch.cuda.synchronize()
+    am = int(torch.argmax(logits[4]).item())
+    assert all(int(tk[0, k, 0].item()) == am for k in range(K))
+    lm = oracle.lm_head(hidden, wlm)
+    assert int(np.argmax(lm[4])) == am
+
+
+# -------------------------------------------------------------- candidates
+
+def test_build_candidates(M):
+    for spec in [("cartesian", (2, 2, 2), None), ("greedy", 4, 10, 64), ("cartesian", (8, 8, 8), 511)]:
+        ot, dtree = both_trees(M, spec)
+        B, K = 3, ot.K + 1
+        s_max = int(max(ot.s[:ot.K]))
+        rng = np.random.default_rng(19)
+        topk = rng.integers(0, 32000, (B, K, s_max)).astype(np.int32)
+        root = rng.integers(0, 32000, B).astype(np.int32)
+        out = torch.zeros((B, ot.T), dtype=torch.int32, device="cuda")
+        M.medusa_build_candidates(to_dev(root), to_dev(topk), dtree, out)
+        torch.cuda.synchronize()
+        ref = oracle.build_candidates(root, topk, ot)
+        assert np.array_equal(to_host(out), ref)
