@@ -265,8 +265,9 @@ def run_native(args, w, rank, world, local_rank):
     g_warm, _ = capture(1, False)
     g_timed, evs = capture(args.steps, True)
     g_plain, _ = capture(args.steps, False)
-    for _ in range(args.warmup):
-        g_warm.replay()
+    with torch.cuda.stream(s):
+        for _ in range(args.warmup):
+            g_warm.replay()
     torch.cuda.synchronize()
 
     def timed(graph):
@@ -275,9 +276,10 @@ def run_native(args, w, rank, world, local_rank):
         torch.cuda.synchronize()
         t0 = torch.cuda.Event(enable_timing=True)
         t1 = torch.cuda.Event(enable_timing=True)
-        t0.record(s)
-        graph.replay()
-        t1.record(s)
+        with torch.cuda.stream(s):  # replay() launches on the current stream
+            t0.record(s)
+            graph.replay()
+            t1.record(s)
         torch.cuda.synchronize()
         if world > 1:
             dist.barrier()

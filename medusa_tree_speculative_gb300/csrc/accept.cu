@@ -53,15 +53,13 @@ __global__ void __launch_bounds__(512) accept_rowstat_kernel(const float* logits
   float bv = -INFINITY;
   int bi = 0x7fffffff;
   Soft sf{-INFINITY, 0.f, 0.f};
-  for (int v = threadIdx.x; v < V; v += blockDim.x) {
-    const float x = z[v];
+  auto consume = [&](float x, int v) {
     if (ranks_before(x, v, bv, bi)) { bv = x; bi = v; }
     if (TYPICAL) {
       const float y = x * inv_temp;
       if (y > sf.m) {
         const float e = expf(sf.m - y);  // 0 when the old max is -inf
-        sf.A = e * (sf.A + (sf.m - y) * sf.S);
-        if (sf.m == -INFINITY) sf.A = 0.f;
+        sf.A = sf.m == -INFINITY ? 0.f : e * (sf.A + (sf.m - y) * sf.S);
         sf.S = sf.S * e + 1.f;
         sf.m = y;
       } else {
@@ -70,6 +68,31 @@ __global__ void __launch_bounds__(512) accept_rowstat_kernel(const float* logits
         sf.A += e * (y - sf.m);
       }
     }
+  };
+  if ((V & 3) == 0) {
+    // 16-byte loads, four in flight per thread
+    const float4* z4 = reinterpret_cast<const float4*>(z);
+    const int n4 = V >> 2;
+    for (int i = threadIdx.x; i < n4; i += 4 * blockDim.x) {
+      float4 r[4];
+#pragma unroll
+      for (int u = 0; u < 4; ++u) {
+        const int ii = i + u * blockDim.x;
+        if (ii < n4) r[u] = __ldg(z4 + ii);
+      }
+#pragma unroll
+      for (int u = 0; u < 4; ++u) {
+        const int ii = i + u * blockDim.x;
+        if (ii < n4) {
+          consume(r[u].x, 4 * ii);
+          consume(r[u].y, 4 * ii + 1);
+          consume(r[u].z, 4 * ii + 2);
+          consume(r[u].w, 4 * ii + 3);
+        }
+      }
+    }
+  } else {
+    for (int v = threadIdx.x; v < V; v += blockDim.x) consume(z[v], v);
   }
   __shared__ float sv[16], sS[16], sA[16], sm[16];
   __shared__ int si[16];

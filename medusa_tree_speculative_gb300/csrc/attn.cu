@@ -19,6 +19,7 @@
 #include <math.h>
 
 #include <algorithm>
+#include <cmath>
 
 #include "common.cuh"
 #include "internal.h"
@@ -42,7 +43,7 @@ struct AttnArgs {
   const int32_t* depth;
   const uint32_t* anc;
   int T, W, B, H, Dh, max_prefix;
-  float rope_theta;
+  float inv_freq[64];  // float(theta^(-2j/Dh)), j < Dh/2, formed on the host in double
   float qscale;  // folded into q': scale (f32 path) or scale*log2(e) (bf16)
   void* out;
   void* qrot;      // [B][T][H][Dh] element type
@@ -107,9 +108,8 @@ __global__ void __launch_bounds__(256) rope_append_kernel(AttnArgs a) {
   __shared__ float cs[64], sn[64];
   const int64_t pos = (int64_t)L + a.depth[i];
   for (int j = threadIdx.x; j < half; j += blockDim.x) {
-    // inv_freq_j = theta^(-2j/Dh) rounded to float; angle formed in float
-    const float inv = (float)(1.0 / pow((double)a.rope_theta, (2.0 * j) / (double)a.Dh));
-    const float ang = __fmul_rn((float)pos, inv);
+    // angle formed in float: float(pos) * inv_freq_j
+    const float ang = __fmul_rn((float)pos, a.inv_freq[j]);
     float s, c;
     sincosf(ang, &s, &c);
     cs[j] = c;
@@ -463,7 +463,9 @@ extern "C" int medusa_tree_attn(const void* q, const void* k_new, const void* v_
   a.q = q; a.k_new = k_new; a.v_new = v_new; a.k_cache = k_cache; a.v_cache = v_cache;
   a.seq_start = seq_start; a.prefix_len = prefix_len; a.seq_cap = seq_cap;
   a.depth = tree->depth; a.anc = tree->anc_mask; a.T = tree->T; a.W = tree->W;
-  a.B = B; a.H = H; a.Dh = Dh; a.max_prefix = max_prefix; a.rope_theta = rope_theta;
+  a.B = B; a.H = H; a.Dh = Dh; a.max_prefix = max_prefix;
+  for (int j = 0; j < Dh / 2; ++j)
+    a.inv_freq[j] = (float)(1.0 / std::pow((double)rope_theta, (2.0 * j) / (double)Dh));
   a.qscale = bf16 ? scale * LOG2E : scale;
   a.out = out;
   uint8_t* ws = static_cast<uint8_t*>(workspace);

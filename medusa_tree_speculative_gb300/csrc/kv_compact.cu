@@ -8,17 +8,18 @@
 // L+accepted[j], and since accepted[i] may equal j for some i < j, every
 // source is read before any destination is written.
 //
-// One CTA per sequence.  Each thread owns a set of 16-byte columns of the
-// (K, V) rows; it loads all A+1 source vectors of its columns into registers
-// and only then stores them, so no column is written before it is read and no
-// barrier is needed between CTAs.
+// One CTA per sequence (it alone reads and then advances prefix_len[b]).
+// Each thread owns 16-byte columns of the (K, V) rows; it loads all A+1
+// source vectors of its columns into registers and only then stores them, so
+// no column is written before it is read and no barrier is needed.
 #include "common.cuh"
 #include "internal.h"
 
 namespace medusa {
 namespace {
 
-__global__ void __launch_bounds__(256) kv_compact_kernel(uint8_t* k_cache, uint8_t* v_cache,
+template <int MAXR, int CPT>
+__global__ void __launch_bounds__(512) kv_compact_kernel(uint8_t* k_cache, uint8_t* v_cache,
                                                           const int64_t* seq_start, int32_t* prefix_len,
                                                           const int32_t* accepted_nodes,
                                                           const int32_t* accept_len, int row_bytes,
@@ -29,34 +30,50 @@ __global__ void __launch_bounds__(256) kv_compact_kernel(uint8_t* k_cache, uint8
   const int A = accept_len[b];
   const int32_t* an = accepted_nodes + (int64_t)b * (Kmax + 1);
   __shared__ int src[MEDUSA_MAX_K + 1];
-  __shared__ int bad;
+  __shared__ int64_t soff[MEDUSA_MAX_K + 1], doff[MEDUSA_MAX_K + 1];  // byte offsets of moved rows
+  __shared__ int bad, nmove;
   if (threadIdx.x == 0) {
     bad = (A < 0 || A > Kmax || L < 0) ? MEDUSA_DEVERR_LENGTH : 0;
+    int n = 0;
     if (!bad) {
       for (int j = 0; j <= A; ++j) {
         const int a = an[j];
         if (a < j || a >= MEDUSA_MAX_T) bad = MEDUSA_DEVERR_NODE;
         src[j] = a;
+        if (a != j) {  // row j moves: slot L+a -> slot L+j
+          soff[n] = (st + L + a) * (int64_t)row_bytes;
+          doff[n] = (st + L + j) * (int64_t)row_bytes;
+          ++n;
+        }
       }
     }
+    nmove = n;
     if (bad) set_err(err, bad);
   }
   __syncthreads();
   if (bad) return;
-  const int vecs = row_bytes / 16;  // 16-byte columns per K (or V) row
-  constexpr int MAXR = MEDUSA_MAX_K + 1;
-  for (int col = threadIdx.x; col < 2 * vecs; col += blockDim.x) {
-    uint8_t* base = col < vecs ? k_cache : v_cache;
-    const int c = col < vecs ? col : col - vecs;
-    uint4 tmp[MAXR];
+  const int vecs = row_bytes / 16;  // 16-byte columns per K (or V) row; CPT per thread per pass
+  const int nm = nmove;
+  for (int col0 = threadIdx.x; col0 < 2 * vecs; col0 += CPT * blockDim.x) {
+    uint4 tmp[CPT][MAXR];
 #pragma unroll
-    for (int j = 0; j < MAXR; ++j)
-      if (j <= A && src[j] != j)
-        tmp[j] = *reinterpret_cast<const uint4*>(base + (st + L + src[j]) * row_bytes + (int64_t)c * 16);
+    for (int q = 0; q < CPT; ++q) {
+      const int col = col0 + q * blockDim.x;
+      if (col >= 2 * vecs) continue;
+      const uint8_t* base = (col < vecs ? k_cache : v_cache) + (int64_t)(col < vecs ? col : col - vecs) * 16;
 #pragma unroll
-    for (int j = 0; j < MAXR; ++j)
-      if (j <= A && src[j] != j)
-        *reinterpret_cast<uint4*>(base + (st + L + j) * row_bytes + (int64_t)c * 16) = tmp[j];
+      for (int t = 0; t < MAXR; ++t)
+        if (t < nm) tmp[q][t] = *reinterpret_cast<const uint4*>(base + soff[t]);
+    }
+#pragma unroll
+    for (int q = 0; q < CPT; ++q) {
+      const int col = col0 + q * blockDim.x;
+      if (col >= 2 * vecs) continue;
+      uint8_t* base = (col < vecs ? k_cache : v_cache) + (int64_t)(col < vecs ? col : col - vecs) * 16;
+#pragma unroll
+      for (int t = 0; t < MAXR; ++t)
+        if (t < nm) *reinterpret_cast<uint4*>(base + doff[t]) = tmp[q][t];
+    }
   }
   __syncthreads();
   if (threadIdx.x == 0) {
@@ -86,8 +103,13 @@ extern "C" int medusa_kv_compact(void* k_cache, void* v_cache, const int64_t* se
   if (row_bytes % 16) return fail(MEDUSA_ERR_UNSUPPORTED, "%s: H*Dh row of %d bytes is not a multiple of 16", fn, row_bytes);
   if ((reinterpret_cast<uintptr_t>(k_cache) | reinterpret_cast<uintptr_t>(v_cache)) % 16)
     return fail(MEDUSA_ERR_INVALID, "%s: caches not 16-byte aligned", fn);
-  kv_compact_kernel<<<B, 256, 0, as_stream(stream)>>>(
-      static_cast<uint8_t*>(k_cache), static_cast<uint8_t*>(v_cache), seq_start, prefix_len,
-      accepted_nodes, accept_len, row_bytes, Kmax, src_slots, err);
+  auto* kc = static_cast<uint8_t*>(k_cache);
+  auto* vc = static_cast<uint8_t*>(v_cache);
+  if (Kmax <= 4)
+    kv_compact_kernel<5, 2><<<B, 512, 0, as_stream(stream)>>>(kc, vc, seq_start, prefix_len, accepted_nodes,
+                                                            accept_len, row_bytes, Kmax, src_slots, err);
+  else
+    kv_compact_kernel<MEDUSA_MAX_K + 1, 1><<<B, 512, 0, as_stream(stream)>>>(
+        kc, vc, seq_start, prefix_len, accepted_nodes, accept_len, row_bytes, Kmax, src_slots, err);
   return check_launch(fn);
 }
