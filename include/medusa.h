@@ -199,6 +199,34 @@ int medusa_accept(const float* logits, const int32_t* tokens,
                   void* workspace, size_t workspace_bytes, int32_t* err,
                   void* stream);
 
+/* Allocation-free variant of medusa_accept.  The paper has no counterpart:
+ * this entry point exists for callers that cannot allocate device memory,
+ * such as a plugin or a plain C host program that is handed only input and
+ * output pointers by the framework that owns the GPU's memory, or a decode
+ * loop that must not call cudaMalloc because it can synchronise the device
+ * and take unbounded time.
+ * Arguments, outputs and errors are those of medusa_accept, without the
+ * workspace.  Its scratch is one file-scope __device__ array of
+ * MEDUSA_ACCEPT_NOALLOC_MAX_ROWS row records of 16 bytes (128 KiB), which
+ * every GPU that loads the library holds until the process exits.
+ *   - The first call on each device looks up the array's device address
+ *     (cudaGetSymbolAddress, with that device current) and caches it; make
+ *     that first call before any stream capture.
+ *   - B * tree->T above MEDUSA_ACCEPT_NOALLOC_MAX_ROWS returns
+ *     MEDUSA_ERR_CAPACITY.
+ *   - It calls no cudaMalloc, cudaFree or other allocating routine.
+ *   - Every call shares the one array, which keeps the last call's contents.
+ *     Nothing in it needs to start at zero (a call writes every record it
+ *     reads), but calls that overlap on the GPU (other streams or threads
+ *     without ordering between them) race on it: the caller serialises them. */
+#define MEDUSA_ACCEPT_NOALLOC_MAX_ROWS (MEDUSA_MAX_B * MEDUSA_MAX_T)
+int medusa_accept_noalloc(const float* logits, const int32_t* tokens,
+                          const medusa_tree_t* tree, int B, int V, int mode,
+                          float temperature, float eps, float delta,
+                          int32_t* accept_len, int32_t* accepted_nodes,
+                          int32_t* next_root, int32_t* best_node,
+                          float* best_logp, int32_t* err, void* stream);
+
 /* KV compaction to the accepted path ([MED] box step 6, Pitfalls: the
  * accepted KV must be gathered into contiguous slots, not sliced).
  * For each sequence b with L = prefix_len[b], A = accept_len[b]:

@@ -15,6 +15,8 @@
 // the accepted-prefix chain level by level, and the best node.
 #include <math.h>
 
+#include <mutex>
+
 #include "common.cuh"
 #include "internal.h"
 
@@ -233,6 +235,34 @@ __global__ void __launch_bounds__(MEDUSA_MAX_T) accept_select_kernel(
   }
 }
 
+// Scratch of medusa_accept_noalloc: one row record per (sequence, tree row)
+// at the library's maximum sizes, 16 x 512 x 16 bytes = 128 KiB per device.
+constexpr int kNoAllocRows = MEDUSA_ACCEPT_NOALLOC_MAX_ROWS;
+static __device__ __align__(256) RowStat g_accept_scratch[kNoAllocRows];
+
+std::mutex g_noalloc_mu;
+void* g_noalloc_addr[64] = {};
+
+// Device address of g_accept_scratch on the current device.  The host-side
+// symbol is only a stand-in, so the address is looked up once per device,
+// with that device current, and cached.
+int noalloc_scratch(const char* fn, void** out) {
+  int dev = -1;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess || dev < 0 || dev >= 64)
+    return fail(MEDUSA_ERR_CUDA, "%s: cudaGetDevice: %s", fn, cudaGetErrorString(e));
+  std::lock_guard<std::mutex> lock(g_noalloc_mu);
+  if (!g_noalloc_addr[dev]) {
+    void* p = nullptr;
+    e = cudaGetSymbolAddress(&p, g_accept_scratch);
+    if (e != cudaSuccess || !p)
+      return fail(MEDUSA_ERR_CUDA, "%s: cudaGetSymbolAddress: %s", fn, cudaGetErrorString(e));
+    g_noalloc_addr[dev] = p;
+  }
+  *out = g_noalloc_addr[dev];
+  return MEDUSA_OK;
+}
+
 }  // namespace
 }  // namespace medusa
 
@@ -272,4 +302,25 @@ extern "C" int medusa_accept(const float* logits, const int32_t* tokens, const m
                                              stats, accept_len, accepted_nodes, next_root, best_node,
                                              best_logp, err);
   return check_launch(fn);
+}
+
+// Allocation-free acceptance for callers that cannot allocate device memory:
+// the same kernels as medusa_accept, with the file-scope scratch above in
+// place of a caller workspace.  It allocates nothing; the first call on a
+// device looks up the scratch address.
+extern "C" int medusa_accept_noalloc(const float* logits, const int32_t* tokens, const medusa_tree_t* tree,
+                                     int B, int V, int mode, float temperature, float eps, float delta,
+                                     int32_t* accept_len, int32_t* accepted_nodes, int32_t* next_root,
+                                     int32_t* best_node, float* best_logp, int32_t* err, void* stream) {
+  const char* fn = "medusa_accept_noalloc";
+  if (int rc = check_tree(tree, fn)) return rc;
+  if (B < 1) return fail(MEDUSA_ERR_INVALID, "%s: B=%d", fn, B);
+  if ((long)B * tree->T > kNoAllocRows)
+    return fail(MEDUSA_ERR_CAPACITY, "%s: B*T = %ld tree rows exceed the static scratch of %d rows", fn,
+                (long)B * tree->T, kNoAllocRows);
+  void* scratch = nullptr;
+  if (int rc = noalloc_scratch(fn, &scratch)) return rc;
+  return medusa_accept(logits, tokens, tree, B, V, mode, temperature, eps, delta, accept_len, accepted_nodes,
+                       next_root, best_node, best_logp, scratch, sizeof(RowStat) * (size_t)kNoAllocRows, err,
+                       stream);
 }

@@ -51,6 +51,7 @@ _SIGS = {
     "medusa_lm_head_verify": (I, [P, P, P, I, I, I, I, P, SZ, P]),
     "medusa_accept_workspace_size": (SZ, [I, I]),
     "medusa_accept": (I, [P, P, TREE, I, I, I, F, F, F, P, P, P, P, P, P, SZ, P, P]),
+    "medusa_accept_noalloc": (I, [P, P, TREE, I, I, I, F, F, F, P, P, P, P, P, P, P]),
     "medusa_kv_compact": (I, [P, P, P, P, P, P, I, I, I, I, I, P, P, P]),
     "medusa_heads_topk_workspace_size": (SZ, [I, I, I, I, I]),
     "medusa_heads_topk": (I, [P, P, I, P, P, P, P, I, I, I, I, I, P, P, I, P, SZ, P, P]),
@@ -230,6 +231,17 @@ def medusa_accept(logits, tokens, tree: DeviceTree, mode: int, temperature: floa
                               _ptr(best_logp), _ptr(workspace),
                               workspace.numel() * workspace.element_size(), _ptr(err), _stream(stream)),
            "medusa_accept")
+
+
+def medusa_accept_noalloc(logits, tokens, tree: DeviceTree, mode: int, temperature: float, eps: float,
+                          delta: float, accept_len, accepted_nodes, next_root, best_node, best_logp, err=None,
+                          stream=None):
+    """medusa_accept without a workspace: for callers that cannot allocate
+    device memory (the library's static scratch is used instead)."""
+    B, T, V = logits.shape
+    _check(_lib.medusa_accept_noalloc(_ptr(logits), _ptr(tokens), tree.ref, B, V, mode, temperature, eps, delta,
+                                      _ptr(accept_len), _ptr(accepted_nodes), _ptr(next_root), _ptr(best_node),
+                                      _ptr(best_logp), _ptr(err), _stream(stream)), "medusa_accept_noalloc")
 
 
 def medusa_kv_compact(k_cache, v_cache, seq_start, prefix_len, accepted_nodes, accept_len, Kmax: int,
