@@ -76,7 +76,8 @@ enum {
   MEDUSA_DEVERR_TOKEN = 1,    /* token outside [0, V) */
   MEDUSA_DEVERR_NODE = 2,     /* node index outside [0, T) */
   MEDUSA_DEVERR_CAPACITY = 4, /* prefix_len + T exceeds seq_cap */
-  MEDUSA_DEVERR_LENGTH = 8    /* accept_len outside [0, K] */
+  MEDUSA_DEVERR_LENGTH = 8,   /* accept_len outside [0, K] */
+  MEDUSA_DEVERR_TIMEOUT = 16  /* a bounded on-chip wait gave up (internal fault) */
 };
 
 typedef struct medusa_tree {
@@ -165,12 +166,15 @@ size_t medusa_lm_head_workspace_size(int rows, int d, int V);
 /* Verification LM head over every tree row ([MED] Method 3, box step 3):
  *   logits[r][v] = sum_j hidden[r][j] * w_lm[v][j]
  * hidden: device [rows][d]; w_lm: device [V][d] (nn.Linear layout);
- * logits: device [rows][V] float32.  d must be a multiple of 64 for bf16
- * (of 4 for f32). */
+ * logits: device [rows][V] float32.  bf16: d must be a multiple of 64 and
+ * both inputs 16-byte aligned; the tensor-core kernel's bounded on-chip
+ * waits report MEDUSA_DEVERR_TIMEOUT through err (nullable) if they ever
+ * give up.  Rows beyond 256 are processed in balanced chunks of at most 256
+ * (the weights are streamed once per chunk). */
 int medusa_lm_head_verify(const void* hidden, const void* w_lm, float* logits,
                           int rows, int d, int V, medusa_dtype dtype,
                           void* workspace, size_t workspace_bytes,
-                          void* stream);
+                          int32_t* err, void* stream);
 
 /* Scratch bytes medusa_accept needs. */
 size_t medusa_accept_workspace_size(int B, int T);

@@ -6,16 +6,24 @@
 // its own ancestors (and itself) only; its position id is prefix length +
 // depth.  Explainer "085 | Medusa", section 二.2: siblings must stay invisible.
 //
-// Three kernels per call:
-//   1. rope_append   rotate q and k_new at pos = L + depth, write k', v_new
-//                    into cache slots L + i, stage q' (pre-scaled) in scratch.
-//   2. attn_partial  flash-decoding split over the L + T keys of each
-//                    sequence: one CTA per (key split, head, row block); the
-//                    ancestor bitmask is applied to the tree keys; QK^T and PV
-//                    run on tensor cores (bf16 in, fp32 accumulate), the
-//                    online softmax in registers (log2 domain).
-//   3. attn_combine  merge the splits' (max, sum, unnormalised O).
-// The f32 element type runs a plain CUDA-core kernel in place of 2-3.
+// bf16: one kernel.  A thread-block cluster of CL CTAs serves one (sequence,
+// head, block of query rows).  The sequence's L + T keys (L cached prefix
+// keys, then the T tree keys) are cut into CL contiguous ranges, one per CTA
+// (flash-decoding split).  Each CTA
+//   * rotates its query rows at pos = L + depth and folds in scale * log2(e),
+//   * streams its key range through double-buffered shared tiles: prefix keys
+//     by cp.async from the cache; tree keys rotated from k_new on the fly and,
+//     by the CTAs of the last row block, appended to the cache at slot L + i,
+//   * applies the ancestor bitmask to tree keys, runs QK^T and PV on tensor
+//     cores (bf16 in, fp32 accumulate) with the online softmax in registers,
+//   * leaves its partial (max, sum, unnormalised O) in its shared memory.
+// After a cluster barrier each CTA merges a share of the rows by reading the
+// CL partials through distributed shared memory and writes the output; a
+// second barrier keeps every CTA's shared memory alive until all reads end.
+// No scratch memory, no inter-kernel combine pass.
+//
+// f32: rope_append (RoPE + KV append, q' staged in scratch) and a plain
+// CUDA-core kernel, one CTA per (row, head, sequence).
 #include <math.h>
 
 #include <algorithm>
@@ -27,8 +35,9 @@
 namespace medusa {
 namespace {
 
-constexpr int KT = 64;         // keys per shared-memory tile
-constexpr int MAX_WARPS = 8;   // 16 query rows per warp
+constexpr int KT = 64;        // keys per shared-memory tile
+constexpr int MAX_WARPS = 5;  // 16 query rows per warp; two CTAs per SM
+constexpr int CL = 8;         // CTAs per cluster (key splits)
 constexpr float LOG2E = 1.4426950408889634f;
 
 struct AttnArgs {
@@ -42,47 +51,26 @@ struct AttnArgs {
   const int64_t* seq_cap;
   const int32_t* depth;
   const uint32_t* anc;
-  int T, W, B, H, Dh, max_prefix;
+  int T, W, K, B, H, Dh, max_prefix;
   float inv_freq[64];  // float(theta^(-2j/Dh)), j < Dh/2, formed on the host in double
-  float qscale;  // folded into q': scale (f32 path) or scale*log2(e) (bf16)
+  float qscale;        // scale (f32 path) or scale * log2(e) (bf16 path)
   void* out;
-  void* qrot;      // [B][T][H][Dh] element type
-  float* part_o;   // [B][H][n_splits][T][Dh]
-  float* part_ml;  // [B][H][n_splits][T][2]
-  int n_splits, chunk, warps, rowblocks;
+  void* qrot;  // f32 path: [B][T][H][Dh]
+  int warps, rowblocks;
   int32_t* err;
 };
 
-struct Plan {
-  int warps, rowblocks, n_splits, chunk;
-  size_t q_bytes, o_bytes, ml_bytes, total;
-};
+// Query rows are split into row blocks of at most 16 * MAX_WARPS rows, balanced.
+void row_split(int T, int& rowblocks, int& warps) {
+  rowblocks = (T + 16 * MAX_WARPS - 1) / (16 * MAX_WARPS);
+  const int rows = (T + rowblocks - 1) / rowblocks;
+  warps = (rows + 15) / 16;
+}
 
-Plan make_plan(int B, int H, int Dh, int T, int max_prefix, size_t esz, bool mma_path) {
-  Plan p{};
-  p.warps = std::min(MAX_WARPS, (T + 15) / 16);
-  p.rowblocks = (T + 16 * p.warps - 1) / (16 * p.warps);
-  const long keys = (long)max_prefix + T;
-  if (mma_path) {
-    const long per_split = (long)B * H * p.rowblocks;
-    const long target = 2L * sm_count();
-    long ns = (target + per_split - 1) / per_split;
-    ns = std::max(1L, std::min(ns, (keys + KT - 1) / KT));
-    long chunk = (keys + ns - 1) / ns;
-    chunk = (chunk + KT - 1) / KT * KT;
-    p.chunk = (int)chunk;
-    p.n_splits = (int)((keys + chunk - 1) / chunk);
-  } else {
-    p.chunk = (int)keys;
-    p.n_splits = 1;
-  }
-  p.q_bytes = align_up((size_t)B * T * H * Dh * esz, 256);
-  if (mma_path) {
-    p.o_bytes = align_up((size_t)B * H * p.n_splits * T * Dh * sizeof(float), 256);
-    p.ml_bytes = align_up((size_t)B * H * p.n_splits * T * 2 * sizeof(float), 256);
-  }
-  p.total = p.q_bytes + p.o_bytes + p.ml_bytes;
-  return p;
+size_t smem_bytes(int Dh, int warps, int K) {
+  return (size_t)2 * 2 * KT * Dh * 2            // K and V tiles, double-buffered, bf16
+         + (size_t)warps * 16 * Dh * 2          // rotated query rows, bf16
+         + (size_t)2 * (K + 1) * (Dh / 2) * 4;  // cos / sin per tree depth
 }
 
 // Sequence b is usable iff 0 <= L <= max_prefix and L + T fits its capacity.
@@ -90,53 +78,6 @@ __device__ bool seq_ok(const AttnArgs& a, int b, int& L, int64_t& st) {
   L = a.prefix_len[b];
   st = a.seq_start[b];
   return L >= 0 && L <= a.max_prefix && (int64_t)L + a.T <= a.seq_cap[b];
-}
-
-// ---------------------------------------------------------------------------
-// 1. RoPE + KV append
-// ---------------------------------------------------------------------------
-template <typename TE>
-__global__ void __launch_bounds__(256) rope_append_kernel(AttnArgs a) {
-  const int i = blockIdx.x, b = blockIdx.y;
-  int L;
-  int64_t st;
-  if (!seq_ok(a, b, L, st)) {
-    if (i == 0 && threadIdx.x == 0) set_err(a.err, MEDUSA_DEVERR_CAPACITY);
-    return;
-  }
-  const int half = a.Dh / 2;
-  __shared__ float cs[64], sn[64];
-  const int64_t pos = (int64_t)L + a.depth[i];
-  for (int j = threadIdx.x; j < half; j += blockDim.x) {
-    // angle formed in float: float(pos) * inv_freq_j
-    const float ang = __fmul_rn((float)pos, a.inv_freq[j]);
-    float s, c;
-    sincosf(ang, &s, &c);
-    cs[j] = c;
-    sn[j] = s;
-  }
-  __syncthreads();
-  const TE* q = static_cast<const TE*>(a.q);
-  const TE* kn = static_cast<const TE*>(a.k_new);
-  const TE* vn = static_cast<const TE*>(a.v_new);
-  TE* kc = static_cast<TE*>(a.k_cache);
-  TE* vc = static_cast<TE*>(a.v_cache);
-  TE* qr = static_cast<TE*>(a.qrot);
-  const int64_t row = ((int64_t)b * a.T + i) * a.H * a.Dh;
-  const int64_t slot = (st + L + i) * (int64_t)a.H * a.Dh;
-  for (int e = threadIdx.x; e < a.H * half; e += blockDim.x) {
-    const int h = e / half, j = e % half;
-    const int64_t o1 = (int64_t)h * a.Dh + j, o2 = o1 + half;
-    const float c = cs[j], s = sn[j];
-    const float q1 = to_f32(q[row + o1]), q2 = to_f32(q[row + o2]);
-    const float k1 = to_f32(kn[row + o1]), k2 = to_f32(kn[row + o2]);
-    qr[row + o1] = from_f32<TE>((q1 * c - q2 * s) * a.qscale);
-    qr[row + o2] = from_f32<TE>((q2 * c + q1 * s) * a.qscale);
-    kc[slot + o1] = from_f32<TE>(k1 * c - k2 * s);
-    kc[slot + o2] = from_f32<TE>(k2 * c + k1 * s);
-    vc[slot + o1] = vn[row + o1];
-    vc[slot + o2] = vn[row + o2];
-  }
 }
 
 // Key j of a sequence is visible to query row r iff j is in the prefix or j
@@ -148,42 +89,166 @@ __device__ __forceinline__ bool key_visible(const AttnArgs& a, int L, int r, int
   return (__ldg(a.anc + (int64_t)r * a.W + (node >> 5)) >> (node & 31)) & 1u;
 }
 
+// Rotate eight (x1, x2) pairs of bf16: x1' = x1 c - x2 s, x2' = x2 c + x1 s,
+// each times `mul`, rounded back to bf16.
+__device__ __forceinline__ void rope8(const uint4& lo, const uint4& hi, const float* c, const float* s,
+                                      float mul, uint4& olo, uint4& ohi) {
+  float a[8], b[8];
+  unpack8_bf16(lo, a);
+  unpack8_bf16(hi, b);
+  float r1[8], r2[8];
+#pragma unroll
+  for (int i = 0; i < 8; ++i) {
+    r1[i] = (a[i] * c[i] - b[i] * s[i]) * mul;
+    r2[i] = (b[i] * c[i] + a[i] * s[i]) * mul;
+  }
+  olo = make_uint4(pack2_bf16(r1[0], r1[1]), pack2_bf16(r1[2], r1[3]), pack2_bf16(r1[4], r1[5]),
+                   pack2_bf16(r1[6], r1[7]));
+  ohi = make_uint4(pack2_bf16(r2[0], r2[1]), pack2_bf16(r2[2], r2[3]), pack2_bf16(r2[4], r2[5]),
+                   pack2_bf16(r2[6], r2[7]));
+}
+
+MDEV uint32_t cluster_ctarank() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%cluster_ctarank;\n" : "=r"(r));
+  return r;
+}
+MDEV void cluster_sync() {
+  asm volatile("barrier.cluster.arrive.release.aligned;\n" ::: "memory");
+  asm volatile("barrier.cluster.wait.acquire.aligned;\n" ::: "memory");
+}
+MDEV uint32_t map_to_rank(uint32_t local_smem_addr, uint32_t rank) {
+  uint32_t r;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;\n" : "=r"(r) : "r"(local_smem_addr), "r"(rank));
+  return r;
+}
+MDEV float2 ld_cluster_f32x2(uint32_t addr) {
+  float2 v;
+  asm volatile("ld.shared::cluster.v2.f32 {%0, %1}, [%2];\n" : "=f"(v.x), "=f"(v.y) : "r"(addr) : "memory");
+  return v;
+}
+
 // ---------------------------------------------------------------------------
-// 2. split-K partial attention on tensor cores (bf16)
+// bf16: clustered split-K tree attention
 // ---------------------------------------------------------------------------
 template <int DH>
-__global__ void __launch_bounds__(MAX_WARPS * 32) attn_partial_kernel(AttnArgs a) {
+__global__ void __cluster_dims__(CL, 1, 1) __launch_bounds__(MAX_WARPS * 32, 2)
+    attn_tree_kernel(const __grid_constant__ AttnArgs a) {
   constexpr int CH = DH / 8;  // 16-byte chunks per row
+  constexpr int HALF = DH / 2;
+  constexpr int HCH = CH / 2;  // chunks per rotary half
   extern __shared__ __align__(128) uint8_t smem[];
   uint16_t* kbuf = reinterpret_cast<uint16_t*>(smem);  // [2][KT][DH]
   uint16_t* vbuf = kbuf + 2 * KT * DH;                // [2][KT][DH]
-
-  const int split = blockIdx.x, h = blockIdx.y;
-  const int b = blockIdx.z / a.rowblocks, rb = blockIdx.z % a.rowblocks;
-  int L;
-  int64_t st;
-  if (!seq_ok(a, b, L, st)) return;
-  const int n_keys = L + a.T;
-  const int k_begin = split * a.chunk;
-  const int k_end = min(n_keys, k_begin + a.chunk);
-  if (k_begin >= k_end) return;  // combine skips splits past n_keys
-
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int nthr = blockDim.x;
-  const int row0 = rb * a.warps * 16;
+  uint16_t* qbuf = vbuf + 2 * KT * DH;                // [rows][DH]
   const int nrows = a.warps * 16;
+  float* cs = reinterpret_cast<float*>(qbuf + nrows * DH);  // [K+1][HALF]
+  float* sn = cs + (a.K + 1) * HALF;
+  // after the key loop: this CTA's partial, over the K/V tiles and q rows
+  float* part_o = reinterpret_cast<float*>(smem);   // [rows][DH]
+  float* part_ml = reinterpret_cast<float*>(qbuf);  // [rows][2]
+
+  const uint32_t crank = cluster_ctarank();
+  const int h = blockIdx.y, b = blockIdx.z / a.rowblocks, rb = blockIdx.z % a.rowblocks;
+  const int tid = threadIdx.x, nthr = blockDim.x;
+  const int warp = tid >> 5, lane = tid & 31;
+  const int row0 = rb * nrows;
   const int HD = a.H * DH;
 
-  // ---- stage q' rows (already rotated and scaled) through shared memory
-  const uint16_t* qrot = static_cast<const uint16_t*>(a.qrot);
-  for (int e = threadIdx.x; e < nrows * CH; e += nthr) {
-    const int rr = e / CH, c = e % CH;
-    const int r = row0 + rr;
-    const uint16_t* src = qrot + ((int64_t)b * a.T + min(r, a.T - 1)) * HD + (int64_t)h * DH + c * 8;
-    cp_async16(smem_u32(kbuf + rr * DH + ((c ^ (rr & 7)) * 8)), src, r < a.T ? 16 : 0);
+  int L;
+  int64_t st;
+  const bool ok = seq_ok(a, b, L, st);
+  if (!ok && crank == 0 && h == 0 && rb == 0 && tid == 0) set_err(a.err, MEDUSA_DEVERR_CAPACITY);
+  // this CTA's key range (every CTA reaches both cluster barriers below)
+  const int nkeys = ok ? L + a.T : 0;
+  const int per = ((nkeys + CL - 1) / CL + 15) / 16 * 16;
+  const int k_begin = min(nkeys, (int)crank * per);
+  const int k_end = min(nkeys, k_begin + per);
+  const int last_row = min(a.T, row0 + nrows) - 1;  // tree keys past it are no one's ancestor here
+  const int k_stop = min(k_end, L + last_row + 1);
+
+  const uint16_t* kcache = static_cast<const uint16_t*>(a.k_cache);
+  const uint16_t* vcache = static_cast<const uint16_t*>(a.v_cache);
+  uint16_t* kcache_w = static_cast<uint16_t*>(a.k_cache);
+  uint16_t* vcache_w = static_cast<uint16_t*>(a.v_cache);
+  const uint16_t* knew = static_cast<const uint16_t*>(a.k_new);
+  const uint16_t* vnew = static_cast<const uint16_t*>(a.v_new);
+
+  // ---- cos/sin at positions L + d for every tree depth d
+  if (ok) {
+    for (int e = tid; e < (a.K + 1) * HALF; e += nthr) {
+      const int d = e / HALF, j = e % HALF;
+      const float ang = __fmul_rn((float)(L + d), a.inv_freq[j]);
+      float s, c;
+      sincosf(ang, &s, &c);
+      cs[e] = c;
+      sn[e] = s;
+    }
   }
+  __syncthreads();
+
+  // ---- tile loader: prefix keys by cp.async, tree keys rotated here
+  auto load_tile = [&](int kt, int buf) {
+    for (int e = tid; e < KT * HCH; e += nthr) {
+      const int rr = e / HCH, c = e % HCH;
+      const int j = kt + rr;
+      uint16_t* kd = kbuf + (buf * KT + rr) * DH;
+      uint16_t* vd = vbuf + (buf * KT + rr) * DH;
+      const int s1 = (c ^ (rr & 7)) * 8, s2 = ((c + HCH) ^ (rr & 7)) * 8;
+      if (j < k_stop && j < L) {
+        const int64_t off = (st + j) * HD + (int64_t)h * DH;
+        cp_async16(smem_u32(kd + s1), kcache + off + c * 8, 16);
+        cp_async16(smem_u32(kd + s2), kcache + off + (c + HCH) * 8, 16);
+        cp_async16(smem_u32(vd + s1), vcache + off + c * 8, 16);
+        cp_async16(smem_u32(vd + s2), vcache + off + (c + HCH) * 8, 16);
+      } else if (j < k_stop) {
+        const int n = j - L;  // tree node
+        const int64_t src = (((int64_t)b * a.T + n) * a.H + h) * DH;
+        const int d = min(max(__ldg(a.depth + n), 0), a.K);
+        uint4 klo, khi;
+        rope8(ldg_v4(knew + src + c * 8), ldg_v4(knew + src + (c + HCH) * 8), cs + d * HALF + c * 8,
+              sn + d * HALF + c * 8, 1.f, klo, khi);
+        const uint4 vlo = ldg_v4(vnew + src + c * 8), vhi = ldg_v4(vnew + src + (c + HCH) * 8);
+        *reinterpret_cast<uint4*>(kd + s1) = klo;
+        *reinterpret_cast<uint4*>(kd + s2) = khi;
+        *reinterpret_cast<uint4*>(vd + s1) = vlo;
+        *reinterpret_cast<uint4*>(vd + s2) = vhi;
+        if (rb == a.rowblocks - 1) {  // the last row block loads every tree key: append K', V at L + n
+          const int64_t dst = (st + L + n) * HD + (int64_t)h * DH;
+          *reinterpret_cast<uint4*>(kcache_w + dst + c * 8) = klo;
+          *reinterpret_cast<uint4*>(kcache_w + dst + (c + HCH) * 8) = khi;
+          *reinterpret_cast<uint4*>(vcache_w + dst + c * 8) = vlo;
+          *reinterpret_cast<uint4*>(vcache_w + dst + (c + HCH) * 8) = vhi;
+        }
+      } else {
+        const uint4 z = make_uint4(0, 0, 0, 0);
+        *reinterpret_cast<uint4*>(kd + s1) = z;
+        *reinterpret_cast<uint4*>(kd + s2) = z;
+        *reinterpret_cast<uint4*>(vd + s1) = z;
+        *reinterpret_cast<uint4*>(vd + s2) = z;
+      }
+    }
+  };
+
+  const int ntiles = k_begin < k_stop ? (k_stop - k_begin + KT - 1) / KT : 0;
+  if (ntiles > 0) load_tile(k_begin, 0);
   cp_async_commit();
-  cp_async_wait<0>();
+
+  // ---- query rows: rotate at L + depth, scale, round to bf16
+  const uint16_t* q = static_cast<const uint16_t*>(a.q);
+  for (int e = tid; e < nrows * HCH; e += nthr) {
+    const int rr = e / HCH, c = e % HCH;
+    const int r = row0 + rr;
+    uint4 lo = make_uint4(0, 0, 0, 0), hi = lo;
+    if (ok && r < a.T) {
+      const int64_t src = (((int64_t)b * a.T + r) * a.H + h) * DH;
+      const int d = min(max(__ldg(a.depth + r), 0), a.K);
+      rope8(ldg_v4(q + src + c * 8), ldg_v4(q + src + (c + HCH) * 8), cs + d * HALF + c * 8,
+            sn + d * HALF + c * 8, a.qscale, lo, hi);
+    }
+    *reinterpret_cast<uint4*>(qbuf + rr * DH + ((c ^ (rr & 7)) * 8)) = lo;
+    *reinterpret_cast<uint4*>(qbuf + rr * DH + (((c + HCH) ^ (rr & 7)) * 8)) = hi;
+  }
   __syncthreads();
   uint32_t qf[DH / 16][4];
   {
@@ -191,24 +256,9 @@ __global__ void __launch_bounds__(MAX_WARPS * 32) attn_partial_kernel(AttnArgs a
 #pragma unroll
     for (int kk = 0; kk < DH / 16; ++kk) {
       const int c = kk * 2 + (lane >> 4);
-      ldmatrix_x4(qf[kk], smem_u32(kbuf + rr * DH + ((c ^ (rr & 7)) * 8)));
+      ldmatrix_x4(qf[kk], smem_u32(qbuf + rr * DH + ((c ^ (rr & 7)) * 8)));
     }
   }
-  __syncthreads();
-
-  const uint16_t* kcache = static_cast<const uint16_t*>(a.k_cache);
-  const uint16_t* vcache = static_cast<const uint16_t*>(a.v_cache);
-  auto load_tile = [&](int kt, int buf) {
-    for (int e = threadIdx.x; e < KT * CH; e += nthr) {
-      const int rr = e / CH, c = e % CH;
-      const int j = kt + rr;
-      const bool ok = j < k_end;
-      const int64_t off = (st + (ok ? j : k_begin)) * HD + (int64_t)h * DH + c * 8;
-      const int sw = (c ^ (rr & 7)) * 8;
-      cp_async16(smem_u32(kbuf + (buf * KT + rr) * DH + sw), kcache + off, ok ? 16 : 0);
-      cp_async16(smem_u32(vbuf + (buf * KT + rr) * DH + sw), vcache + off, ok ? 16 : 0);
-    }
-  };
 
   const int ra = row0 + warp * 16 + (lane >> 2);  // this thread's two rows
   const int rbw = ra + 8;
@@ -217,9 +267,6 @@ __global__ void __launch_bounds__(MAX_WARPS * 32) attn_partial_kernel(AttnArgs a
 #pragma unroll
   for (int n = 0; n < DH / 8; ++n) o[n][0] = o[n][1] = o[n][2] = o[n][3] = 0.f;
 
-  const int ntiles = (k_end - k_begin + KT - 1) / KT;
-  load_tile(k_begin, 0);
-  cp_async_commit();
   for (int t = 0; t < ntiles; ++t) {
     const int kt = k_begin + t * KT;
     const int buf = t & 1;
@@ -250,17 +297,15 @@ __global__ void __launch_bounds__(MAX_WARPS * 32) attn_partial_kernel(AttnArgs a
         mma_bf16_16816(s[2 * np + 1], qf[kk], r[2], r[3]);
       }
     }
-    // mask: the tail past k_end everywhere; ancestor bits on tree keys
-    const bool tail = kt + KT > k_end;
-    const bool tree = kt + KT > L;
-    if (tail || tree) {
+    // mask: keys past this CTA's range; ancestor bits on tree keys
+    if (kt + KT > k_stop || kt + KT > L) {
 #pragma unroll
       for (int n = 0; n < KT / 8; ++n) {
 #pragma unroll
         for (int e = 0; e < 4; ++e) {
           const int j = kt + n * 8 + (lane & 3) * 2 + (e & 1);
           const int r = e < 2 ? ra : rbw;
-          if (j >= k_end || !key_visible(a, L, r, j)) s[n][e] = -INFINITY;
+          if (j >= k_stop || !key_visible(a, L, r, j)) s[n][e] = -INFINITY;
         }
       }
     }
@@ -313,56 +358,119 @@ __global__ void __launch_bounds__(MAX_WARPS * 32) attn_partial_kernel(AttnArgs a
     }
     __syncthreads();
   }
+  cp_async_wait<0>();
+  __syncthreads();
   l_a += __shfl_xor_sync(0xffffffffu, l_a, 1);
   l_a += __shfl_xor_sync(0xffffffffu, l_a, 2);
   l_b += __shfl_xor_sync(0xffffffffu, l_b, 1);
   l_b += __shfl_xor_sync(0xffffffffu, l_b, 2);
 
-  const int64_t base = (((int64_t)b * a.H + h) * a.n_splits + split) * a.T;
+  // ---- this CTA's partial into its own shared memory (rows local to the block)
+  const int la = warp * 16 + (lane >> 2), lb = la + 8;
 #pragma unroll
   for (int n = 0; n < DH / 8; ++n) {
     const int col = n * 8 + (lane & 3) * 2;
-    if (ra < a.T)
-      *reinterpret_cast<float2*>(a.part_o + (base + ra) * DH + col) = make_float2(o[n][0], o[n][1]);
-    if (rbw < a.T)
-      *reinterpret_cast<float2*>(a.part_o + (base + rbw) * DH + col) = make_float2(o[n][2], o[n][3]);
+    *reinterpret_cast<float2*>(part_o + la * DH + col) = make_float2(o[n][0], o[n][1]);
+    *reinterpret_cast<float2*>(part_o + lb * DH + col) = make_float2(o[n][2], o[n][3]);
   }
   if ((lane & 3) == 0) {
-    if (ra < a.T) *reinterpret_cast<float2*>(a.part_ml + (base + ra) * 2) = make_float2(m_a, l_a);
-    if (rbw < a.T) *reinterpret_cast<float2*>(a.part_ml + (base + rbw) * 2) = make_float2(m_b, l_b);
+    *reinterpret_cast<float2*>(part_ml + la * 2) = make_float2(m_a, l_a);
+    *reinterpret_cast<float2*>(part_ml + lb * 2) = make_float2(m_b, l_b);
   }
+  cluster_sync();
+
+  // ---- merge: this CTA takes local rows crank, crank + CL, ...
+  __shared__ float wgt[(MAX_WARPS * 16 + CL - 1) / CL][CL];  // per (row, rank): weight / denominator
+  const uint32_t ml_local = smem_u32(part_ml), o_local = smem_u32(part_o);
+  const int my_rows = ok ? (nrows - (int)crank + CL - 1) / CL : 0;
+  for (int i = tid; i < my_rows; i += nthr) {
+    const int rr = (int)crank + i * CL;
+    float m[CL], l[CL], M = -INFINITY;
+#pragma unroll
+    for (int c = 0; c < CL; ++c) {
+      const float2 v = ld_cluster_f32x2(map_to_rank(ml_local + rr * 8, c));
+      m[c] = v.x;
+      l[c] = v.y;
+      M = fmaxf(M, m[c]);
+    }
+    float den = 0.f, w[CL];
+#pragma unroll
+    for (int c = 0; c < CL; ++c) {
+      w[c] = m[c] == -INFINITY ? 0.f : exp2f(m[c] - M);
+      den += w[c] * l[c];
+    }
+#pragma unroll
+    for (int c = 0; c < CL; ++c) wgt[i][c] = den > 0.f ? w[c] / den : 0.f;
+  }
+  __syncthreads();
+  uint16_t* out = static_cast<uint16_t*>(a.out);
+  for (int e = tid; e < my_rows * (DH / 2); e += nthr) {
+    const int i = e / (DH / 2), d = (e % (DH / 2)) * 2;
+    const int rr = (int)crank + i * CL;
+    const int r = row0 + rr;
+    if (r >= a.T) continue;
+    float2 acc = make_float2(0.f, 0.f);
+#pragma unroll
+    for (int c = 0; c < CL; ++c) {
+      const float wc = wgt[i][c];
+      if (wc != 0.f) {
+        const float2 v = ld_cluster_f32x2(map_to_rank(o_local + (rr * DH + d) * 4, c));
+        acc.x += wc * v.x;
+        acc.y += wc * v.y;
+      }
+    }
+    *reinterpret_cast<uint32_t*>(out + (((int64_t)b * a.T + r) * a.H + h) * DH + d) = pack2_bf16(acc.x, acc.y);
+  }
+  cluster_sync();  // keep this CTA's partial alive until every rank has read it
 }
 
 // ---------------------------------------------------------------------------
-// 3. merge the key splits
+// f32: RoPE + KV append, then one CTA per (row, head, sequence)
 // ---------------------------------------------------------------------------
-__global__ void __launch_bounds__(128) attn_combine_kernel(AttnArgs a) {
-  const int i = blockIdx.x, h = blockIdx.y, b = blockIdx.z;
+__global__ void __launch_bounds__(256) rope_append_f32_kernel(const __grid_constant__ AttnArgs a) {
+  const int i = blockIdx.x, b = blockIdx.y;
   int L;
   int64_t st;
-  if (!seq_ok(a, b, L, st)) return;
-  const int used = (L + a.T + a.chunk - 1) / a.chunk;
-  const int64_t base = ((int64_t)b * a.H + h) * a.n_splits * a.T;
-  float M = -INFINITY;
-  for (int sp = 0; sp < used; ++sp) M = fmaxf(M, a.part_ml[(base + (int64_t)sp * a.T + i) * 2]);
-  const float Mb = M == -INFINITY ? 0.f : M;
-  uint16_t* out = static_cast<uint16_t*>(a.out);
-  for (int d = threadIdx.x; d < a.Dh; d += blockDim.x) {
-    float num = 0.f, den = 0.f;
-    for (int sp = 0; sp < used; ++sp) {
-      const int64_t r = base + (int64_t)sp * a.T + i;
-      const float w = exp2f(a.part_ml[r * 2] - Mb);
-      den += w * a.part_ml[r * 2 + 1];
-      num += w * a.part_o[r * a.Dh + d];
-    }
-    out[(((int64_t)b * a.T + i) * a.H + h) * a.Dh + d] = f32_to_bf16_bits(den > 0.f ? num / den : 0.f);
+  if (!seq_ok(a, b, L, st)) {
+    if (i == 0 && threadIdx.x == 0) set_err(a.err, MEDUSA_DEVERR_CAPACITY);
+    return;
+  }
+  const int half = a.Dh / 2;
+  __shared__ float cs[64], sn[64];
+  const int64_t pos = (int64_t)L + a.depth[i];
+  for (int j = threadIdx.x; j < half; j += blockDim.x) {
+    const float ang = __fmul_rn((float)pos, a.inv_freq[j]);
+    float s, c;
+    sincosf(ang, &s, &c);
+    cs[j] = c;
+    sn[j] = s;
+  }
+  __syncthreads();
+  const float* __restrict__ q = static_cast<const float*>(a.q);
+  const float* __restrict__ kn = static_cast<const float*>(a.k_new);
+  const float* __restrict__ vn = static_cast<const float*>(a.v_new);
+  float* kc = static_cast<float*>(a.k_cache);
+  float* vc = static_cast<float*>(a.v_cache);
+  float* qr = static_cast<float*>(a.qrot);
+  const int64_t row = ((int64_t)b * a.T + i) * a.H * a.Dh;
+  const int64_t slot = (st + L + i) * (int64_t)a.H * a.Dh;
+  for (int e = threadIdx.x; e < a.H * half; e += blockDim.x) {
+    const int h = e / half, j = e % half;
+    const int64_t o1 = (int64_t)h * a.Dh + j, o2 = o1 + half;
+    const float c = cs[j], s = sn[j];
+    const float q1 = q[row + o1], q2 = q[row + o2];
+    const float k1 = kn[row + o1], k2 = kn[row + o2];
+    qr[row + o1] = (q1 * c - q2 * s) * a.qscale;
+    qr[row + o2] = (q2 * c + q1 * s) * a.qscale;
+    kc[slot + o1] = k1 * c - k2 * s;
+    kc[slot + o2] = k2 * c + k1 * s;
+    vc[slot + o1] = vn[row + o1];
+    vc[slot + o2] = vn[row + o2];
   }
 }
 
-// ---------------------------------------------------------------------------
-// f32: one CTA per (row, head, sequence); warps stride over the visible keys
-// with an online softmax; lanes split the head dimension.
-// ---------------------------------------------------------------------------
+// Warps stride over the visible keys with an online softmax; lanes split the
+// head dimension.
 __global__ void __launch_bounds__(128) attn_f32_kernel(AttnArgs a) {
   const int i = blockIdx.x, h = blockIdx.y, b = blockIdx.z;
   int L;
@@ -431,10 +539,8 @@ using namespace medusa;
 
 extern "C" size_t medusa_tree_attn_workspace_size(int B, int H, int Dh, int T, int max_prefix) {
   if (B < 1 || H < 1 || Dh < 1 || T < 1 || max_prefix < 0) return 0;
-  // the bf16 plan is the larger of the two; callers may size for either type
-  Plan p = make_plan(B, H, Dh, T, max_prefix, 4, true);
-  Plan pb = make_plan(B, H, Dh, T, max_prefix, 2, true);
-  return std::max(p.q_bytes + pb.o_bytes + pb.ml_bytes, pb.total);
+  // the f32 path stages q' in scratch; the bf16 path needs none
+  return align_up((size_t)B * T * H * Dh * sizeof(float), 256);
 }
 
 extern "C" int medusa_tree_attn(const void* q, const void* k_new, const void* v_new, void* k_cache,
@@ -453,47 +559,44 @@ extern "C" int medusa_tree_attn(const void* q, const void* k_new, const void* v_
   if (dtype != MEDUSA_F32 && dtype != MEDUSA_BF16) return fail(MEDUSA_ERR_UNSUPPORTED, "%s: dtype", fn);
   if (!(rope_theta > 0.f) || !(scale > 0.f)) return fail(MEDUSA_ERR_INVALID, "%s: rope_theta/scale", fn);
   const bool bf16 = dtype == MEDUSA_BF16;
-  Plan p = make_plan(B, H, Dh, tree->T, max_prefix, bf16 ? 2 : 4, bf16);
-  if (!workspace || workspace_bytes < p.total)
-    return fail(MEDUSA_ERR_WORKSPACE, "%s: workspace %zu < %zu bytes", fn, workspace_bytes, p.total);
-  if (reinterpret_cast<uintptr_t>(workspace) % 256)
+  if (bf16 && ((reinterpret_cast<uintptr_t>(q) | reinterpret_cast<uintptr_t>(k_new) |
+                reinterpret_cast<uintptr_t>(v_new) | reinterpret_cast<uintptr_t>(k_cache) |
+                reinterpret_cast<uintptr_t>(v_cache)) % 16))
+    return fail(MEDUSA_ERR_INVALID, "%s: tensors not 16-byte aligned", fn);
+  const size_t need = bf16 ? 0 : medusa_tree_attn_workspace_size(B, H, Dh, tree->T, max_prefix);
+  if (need && (!workspace || workspace_bytes < need))
+    return fail(MEDUSA_ERR_WORKSPACE, "%s: workspace %zu < %zu bytes", fn, workspace_bytes, need);
+  if (need && reinterpret_cast<uintptr_t>(workspace) % 256)
     return fail(MEDUSA_ERR_INVALID, "%s: workspace not 256-byte aligned", fn);
 
   AttnArgs a{};
   a.q = q; a.k_new = k_new; a.v_new = v_new; a.k_cache = k_cache; a.v_cache = v_cache;
   a.seq_start = seq_start; a.prefix_len = prefix_len; a.seq_cap = seq_cap;
-  a.depth = tree->depth; a.anc = tree->anc_mask; a.T = tree->T; a.W = tree->W;
+  a.depth = tree->depth; a.anc = tree->anc_mask; a.T = tree->T; a.W = tree->W; a.K = tree->K;
   a.B = B; a.H = H; a.Dh = Dh; a.max_prefix = max_prefix;
   for (int j = 0; j < Dh / 2; ++j)
     a.inv_freq[j] = (float)(1.0 / std::pow((double)rope_theta, (2.0 * j) / (double)Dh));
   a.qscale = bf16 ? scale * LOG2E : scale;
   a.out = out;
-  uint8_t* ws = static_cast<uint8_t*>(workspace);
-  a.qrot = ws;
-  a.part_o = reinterpret_cast<float*>(ws + p.q_bytes);
-  a.part_ml = reinterpret_cast<float*>(ws + p.q_bytes + p.o_bytes);
-  a.n_splits = p.n_splits; a.chunk = p.chunk; a.warps = p.warps; a.rowblocks = p.rowblocks;
+  a.qrot = workspace;
   a.err = err;
+  row_split(tree->T, a.rowblocks, a.warps);
   cudaStream_t s = as_stream(stream);
 
-  dim3 g1(tree->T, B);
   if (bf16) {
-    rope_append_kernel<uint16_t><<<g1, 256, 0, s>>>(a);
-    if (int rc = check_launch(fn)) return rc;
-    dim3 g2(p.n_splits, H, B * p.rowblocks);
-    const size_t sm = 2 * 2 * KT * Dh * sizeof(uint16_t);
+    dim3 grid(CL, H, B * a.rowblocks);
+    const size_t sm = smem_bytes(Dh, a.warps, a.K);
     if (Dh == 128) {
-      cudaFuncSetAttribute(attn_partial_kernel<128>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sm);
-      attn_partial_kernel<128><<<g2, p.warps * 32, sm, s>>>(a);
+      cudaFuncSetAttribute(attn_tree_kernel<128>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sm);
+      attn_tree_kernel<128><<<grid, a.warps * 32, sm, s>>>(a);
     } else {
-      attn_partial_kernel<64><<<g2, p.warps * 32, sm, s>>>(a);
+      cudaFuncSetAttribute(attn_tree_kernel<64>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sm);
+      attn_tree_kernel<64><<<grid, a.warps * 32, sm, s>>>(a);
     }
-    if (int rc = check_launch(fn)) return rc;
-    dim3 g3(tree->T, H, B);
-    attn_combine_kernel<<<g3, 128, 0, s>>>(a);
     return check_launch(fn);
   }
-  rope_append_kernel<float><<<g1, 256, 0, s>>>(a);
+  dim3 g1(tree->T, B);
+  rope_append_f32_kernel<<<g1, 256, 0, s>>>(a);
   if (int rc = check_launch(fn)) return rc;
   dim3 g2(tree->T, H, B);
   attn_f32_kernel<<<g2, 128, 0, s>>>(a);

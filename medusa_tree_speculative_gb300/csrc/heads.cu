@@ -13,8 +13,9 @@
 // eight loads in flight per lane, the input vector re-read from L1.
 //   gemv<W1>  u[b][k] = dtype(SiLU(W1_k h_b + b1_k) + h_b)   (scratch)
 //   gemv<W2>  head_logits[b][k] = W2_k u[b][k]              (fp32)
-//   topk      per (head, sequence): per-lane sorted lists, then two rounds of
-//             warp-level merging (value descending, index ascending)
+//   topk      per (head, sequence) in chunks of ~1024 logits, one CTA each:
+//             per-lane sorted lists merged warp by warp (value descending,
+//             index ascending); the last chunk to finish merges the chunks
 #include <math.h>
 
 #include <algorithm>
@@ -36,6 +37,8 @@ struct GemvArgs {
   const void* b1;       // [K][d] or null
   void* u;              // [B][K][d] element type
   float* logits;        // [B][K][V]
+  int* counters;        // top-s arrival counters, zeroed by the W1 pass
+  int ncounters;
   int32_t* err;
 };
 
@@ -65,6 +68,8 @@ __global__ void __launch_bounds__(256) heads_gemv_kernel(GemvArgs a) {
   const TE* W = static_cast<const TE*>(a.w);
   __shared__ int head_id[MEDUSA_MAX_K];
   if (threadIdx.x < MEDUSA_MAX_K) head_id[threadIdx.x] = a.heads[threadIdx.x];
+  if (W1 && blockIdx.x == 0)
+    for (int i = threadIdx.x; i < a.ncounters; i += blockDim.x) a.counters[i] = 0;
   __syncthreads();
 
   // input vectors of this call, one per sequence (W1: hidden[b][last_node]);
@@ -189,20 +194,21 @@ struct HeadTable {
   int32_t s[MEDUSA_MAX_K];  // their s_k
 };
 
+struct TopkArgs {
+  const float* logits;  // [B][K][V]
+  int K, V, s_max, nchunk;
+  HeadTable tab;
+  float* cand_v;  // [nused][B][nchunk][S] candidate values (scratch)
+  int* cand_i;    // same layout, indices
+  int* counters;  // [nused][B] arrivals, zero on entry
+  int32_t* topk;  // [B][K][s_max]
+};
+
+// Block-wide: the S best of all threads' lists, valid in warp 0.  Consumes
+// the lists; `wv`/`wi` are [32][S] shared staging.
 template <int S>
-__global__ void __launch_bounds__(1024) topk_kernel(const float* logits, int K, int V, HeadTable tab,
-                                                    int s_max, int32_t* topk) {
-  const int k = tab.h[blockIdx.x], b = blockIdx.y;
-  const int s = tab.s[blockIdx.x];
-  const float* z = logits + ((int64_t)b * K + k) * V;
-  TopList<S> L;
-  L.init();
-  for (int v = threadIdx.x; v < V; v += blockDim.x) L.insert(z[v], v);
-  __shared__ float wv[32][S];
-  __shared__ int wi[32][S];
+MDEV void block_select(TopList<S>& L, float (*wv)[S], int (*wi)[S], float* ov, int* oi) {
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, nw = blockDim.x >> 5;
-  float ov[S];
-  int oi[S];
   L.warp_select(ov, oi);
   if (lane == 0) {
 #pragma unroll
@@ -217,16 +223,76 @@ __global__ void __launch_bounds__(1024) topk_kernel(const float* logits, int K, 
       M.i[t] = lane < nw ? wi[lane][t] : 0x7fffffff;
     }
     M.warp_select(ov, oi);
-    int32_t* out = topk + ((int64_t)b * K + k) * s_max;
-    for (int t = lane; t < s_max; t += 32) {
+  }
+}
+
+// Grid (nchunk, nused, B).  Each CTA selects the top S of one contiguous
+// chunk of a head's logits; the last CTA of the head to finish merges the
+// nchunk candidate lists and writes the head's top s.
+template <int S>
+__global__ void __launch_bounds__(256) topk_kernel(const __grid_constant__ TopkArgs a) {
+  const int chunk = blockIdx.x, slot = blockIdx.y, b = blockIdx.z;
+  const int k = a.tab.h[slot], s = a.tab.s[slot];
+  const int nused = gridDim.y;
+  const float* z = a.logits + ((int64_t)b * a.K + k) * a.V;
+  const int per = (a.V + a.nchunk - 1) / a.nchunk;
+  const int v0 = chunk * per, v1 = min(a.V, v0 + per);
+  __shared__ float wv[32][S];
+  __shared__ int wi[32][S];
+  __shared__ bool last;
+  TopList<S> L;
+  L.init();
+  for (int base = v0 + threadIdx.x; base < v1; base += 4 * blockDim.x) {
+    float x[4];
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+      const int v = base + u * blockDim.x;
+      x[u] = v < v1 ? z[v] : -INFINITY;
+    }
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+      const int v = base + u * blockDim.x;
+      if (v < v1) L.insert(x[u], v);
+    }
+  }
+  float ov[S];
+  int oi[S];
+  block_select<S>(L, wv, wi, ov, oi);
+  const int64_t cbase = (((int64_t)slot * gridDim.z + b) * a.nchunk + chunk) * S;
+  if (threadIdx.x < 32 && threadIdx.x == 0) {
+#pragma unroll
+    for (int t = 0; t < S; ++t) { a.cand_v[cbase + t] = ov[t]; a.cand_i[cbase + t] = oi[t]; }
+  }
+  // the last chunk of this (head, sequence) to arrive merges all chunks
+  if (threadIdx.x == 0) {
+    __threadfence();
+    const int prev = atomicAdd(a.counters + slot * gridDim.z + b, 1);
+    last = prev == a.nchunk - 1;
+  }
+  __syncthreads();
+  if (!last) return;
+  __threadfence();
+  const int64_t hbase = ((int64_t)slot * gridDim.z + b) * a.nchunk * S;
+  L.init();
+  for (int e = threadIdx.x; e < a.nchunk * S; e += blockDim.x)
+    L.insert(__ldcg(a.cand_v + hbase + e), __ldcg(a.cand_i + hbase + e));
+  __syncthreads();
+  block_select<S>(L, wv, wi, ov, oi);
+  if (threadIdx.x < 32) {
+    int32_t* out = a.topk + ((int64_t)b * a.K + k) * a.s_max;
+    for (int t = threadIdx.x; t < a.s_max; t += 32) {
       int idx = -1;
 #pragma unroll
       for (int q = 0; q < S; ++q)
         if (q == t) idx = oi[q];
-      out[t] = (t < s && idx >= 0 && idx < V) ? idx : -1;
+      out[t] = (t < s && idx >= 0 && idx < a.V) ? idx : -1;
     }
   }
+  if (threadIdx.x == 0) a.counters[slot * gridDim.z + b] = 0;  // ready for the next call
+  (void)nused;
 }
+
+int topk_chunks(int V) { return std::max(1, std::min(64, (V + 1023) / 1024)); }
 
 template <typename TE, int NB>
 void launch_gemv(const GemvArgs& a, bool w1, cudaStream_t s) {
@@ -252,8 +318,10 @@ using namespace medusa;
 extern "C" size_t medusa_heads_topk_workspace_size(int B, int K, int d, int V, int s_max) {
   (void)V; (void)s_max;
   if (B < 1 || K < 1 || d < 1) return 0;
-  // u [B][K][d] (fp32 size covers both element types)
-  return align_up((size_t)B * K * d * sizeof(float), 256);
+  // u [B][K][d] (fp32 size covers both element types), top-s candidates and counters
+  const size_t u = align_up((size_t)B * K * d * sizeof(float), 256);
+  const size_t cand = align_up((size_t)K * B * topk_chunks(V) * MEDUSA_MAX_S * 4, 256);
+  return u + 2 * cand + align_up((size_t)K * B * sizeof(int), 256);
 }
 
 extern "C" int medusa_heads_topk(const void* hidden, const int32_t* last_node, int T, const void* w1,
@@ -287,6 +355,11 @@ extern "C" int medusa_heads_topk(const void* hidden, const int32_t* last_node, i
   if (a.nused == 0) return MEDUSA_OK;
   cudaStream_t st = as_stream(stream);
   uint8_t* ws = static_cast<uint8_t*>(workspace);
+  const size_t u_bytes = align_up((size_t)B * K * d * sizeof(float), 256);
+  const int nchunk = topk_chunks(V);
+  const size_t cand_bytes = align_up((size_t)K * B * nchunk * MEDUSA_MAX_S * 4, 256);
+  a.counters = reinterpret_cast<int*>(ws + u_bytes + 2 * cand_bytes);
+  a.ncounters = K * B;
   a.hidden = hidden; a.last_node = last_node; a.T = T; a.B = B; a.K = K; a.d = d;
   a.b1 = b1; a.u = ws; a.logits = head_logits; a.err = err;
 
@@ -299,12 +372,17 @@ extern "C" int medusa_heads_topk(const void* hidden, const int32_t* last_node, i
   if (dtype == MEDUSA_BF16) launch_gemv_b<uint16_t>(a, false, st); else launch_gemv_b<float>(a, false, st);
   if (int rc = check_launch(fn)) return rc;
   // top-s over each used head's logits (the head table travels by value)
-  HeadTable tab{};
-  for (int i = 0; i < a.nused; ++i) { tab.h[i] = a.heads[i]; tab.s[i] = s[a.heads[i]]; }
-  dim3 g(a.nused, B);
-  if (smax_used <= 2) topk_kernel<2><<<g, 1024, 0, st>>>(head_logits, K, V, tab, s_max, topk);
-  else if (smax_used <= 4) topk_kernel<4><<<g, 1024, 0, st>>>(head_logits, K, V, tab, s_max, topk);
-  else if (smax_used <= 8) topk_kernel<8><<<g, 1024, 0, st>>>(head_logits, K, V, tab, s_max, topk);
-  else topk_kernel<16><<<g, 1024, 0, st>>>(head_logits, K, V, tab, s_max, topk);
+  TopkArgs ta{};
+  for (int i = 0; i < a.nused; ++i) { ta.tab.h[i] = a.heads[i]; ta.tab.s[i] = s[a.heads[i]]; }
+  ta.logits = head_logits; ta.K = K; ta.V = V; ta.s_max = s_max; ta.nchunk = nchunk;
+  ta.cand_v = reinterpret_cast<float*>(ws + u_bytes);
+  ta.cand_i = reinterpret_cast<int*>(ws + u_bytes + cand_bytes);
+  ta.counters = a.counters;
+  ta.topk = topk;
+  dim3 g(nchunk, a.nused, B);
+  if (smax_used <= 2) topk_kernel<2><<<g, 256, 0, st>>>(ta);
+  else if (smax_used <= 4) topk_kernel<4><<<g, 256, 0, st>>>(ta);
+  else if (smax_used <= 8) topk_kernel<8><<<g, 256, 0, st>>>(ta);
+  else topk_kernel<16><<<g, 256, 0, st>>>(ta);
   return check_launch(fn);
 }

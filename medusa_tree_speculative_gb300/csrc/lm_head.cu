@@ -8,138 +8,202 @@
 //
 // logits[r][v] = sum_j hidden[r][j] * w[v][j]
 //
-// bf16: swap-AB tensor-core GEMM (vocabulary rows are the M dimension, tree
-// rows the N dimension).  One persistent CTA per SM owns a contiguous slice of
-// the vocabulary, so every weight byte is read once and no partial sums are
-// exchanged; the slice streams through a 4-stage cp.async pipeline while the
-// few hundred tree rows are re-read from L2.
+// bf16: tcgen05 tensor-core GEMM with TMEM accumulators, swap-AB: the
+// vocabulary is the MMA's M dimension (128-row tiles of W, K-major) and the
+// tree rows its N dimension (all rows of a chunk, padded to 16, K-major), so
+// one instruction covers every tree row.  Persistent CTAs, one per SM, own
+// contiguous runs of vocabulary tiles: each weight byte is read once and no
+// partial sums are exchanged.  Warp roles:
+//   warp 0     one thread issues TMA loads of W and hidden k-blocks (64 wide,
+//              128-byte swizzle) into a ring of shared stages,
+//   warp 1     allocates TMEM; one thread issues the MMAs (4 per stage) and
+//              commits stage releases and finished accumulators to mbarriers,
+//   warps 2-5  read the accumulator back from TMEM (one TMEM lane per
+//              vocabulary row) and store fp32 logits, coalesced along the
+//              vocabulary.
+// Two accumulators alternate so the epilogue of one tile overlaps the MMAs of
+// the next.  Every mbarrier wait is bounded; a timeout sets
+// MEDUSA_DEVERR_TIMEOUT and the kernel winds down.
 // f32: a plain CUDA-core kernel (one warp per output element).
+#include <cuda.h>
+
 #include <algorithm>
+#include <mutex>
 
 #include "common.cuh"
 #include "internal.h"
+#include "sm100.cuh"
 
 namespace medusa {
 namespace {
 
-constexpr int KB = 64;           // k per pipeline stage (128 bytes of bf16)
-constexpr int STAGES = 4;
-constexpr int NWARP = 8;
-constexpr int WM = 32;           // vocabulary rows per warp (two m16 tiles)
-constexpr int CM = NWARP * WM;   // vocabulary rows per CTA pass
-constexpr int NT = 9;            // n8 tiles per pass: 72 tree rows
-constexpr int CN = NT * 8;
-constexpr int W_STAGE = CM * KB;  // elements
-constexpr int H_STAGE = CN * KB;
-constexpr size_t SMEM = (size_t)STAGES * (W_STAGE + H_STAGE) * sizeof(uint16_t);
+using namespace sm100;
+
+constexpr int BM = 128;        // vocabulary rows per tile (MMA M)
+constexpr int BK = 64;         // k per stage: 128 bytes of bf16, one swizzle span
+constexpr int UK = 16;         // k per MMA instruction
+constexpr int kThreads = 192;  // 6 warps
+constexpr int kMaxN = 256;     // tree rows per chunk (MMA N)
+constexpr size_t kSmemBudget = 200 * 1024;
 
 struct LmArgs {
-  const uint16_t* hidden;
-  const uint16_t* w;
   float* logits;
-  int rows, d, V, nblk;
+  int rows, d, V;
+  int npad;     // MMA N of every chunk (multiple of 16, <= kMaxN)
+  int nchunks;  // chunks of tree rows
+  int ntiles;   // vocabulary tiles
+  int stages;
+  uint32_t tmem_cols;
+  int32_t* err;
 };
 
-__global__ void __launch_bounds__(NWARP * 32, 1) lm_head_mma_kernel(LmArgs a) {
-  extern __shared__ __align__(128) uint8_t smem[];
-  uint16_t* ws = reinterpret_cast<uint16_t*>(smem);
-  uint16_t* hs = ws + STAGES * W_STAGE;
+MDEV bool wait_or_abort(uint64_t* bar, uint32_t parity, volatile int* abort_flag) {
+  for (uint32_t i = 0; i < kSpinLimit; ++i) {
+    if (mbar_try_wait(bar, parity)) return true;
+    if ((i & 255) == 255 && *abort_flag) return false;
+  }
+  *abort_flag = 1;
+  return false;
+}
+
+__global__ void __launch_bounds__(kThreads, 1)
+    lm_head_tc_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CUtensorMap tmH,
+                      const __grid_constant__ LmArgs a) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  const uint32_t a_bytes = BM * BK * 2;
+  const uint32_t b_bytes = (uint32_t)a.npad * BK * 2;
+  const uint32_t stage_bytes = a_bytes + b_bytes;
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + (size_t)a.stages * stage_bytes);
+  uint64_t* empty = full + a.stages;
+  uint64_t* tfull = empty + a.stages;
+  uint64_t* tempty = tfull + 2;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(tempty + 2);
+  __shared__ int s_abort;
+
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < a.stages; ++s) {
+      mbar_init(&full[s], 1);
+      mbar_init(&empty[s], 1);
+    }
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(&tfull[i], 1);
+      mbar_init(&tempty[i], 4 * 32);
+    }
+    fence_barrier_init();
+    s_abort = 0;
+    tma_prefetch_desc(&tmW);
+    tma_prefetch_desc(&tmH);
+  }
+  if (warp == 1) {
+    tmem_alloc(tmem_slot, a.tmem_cols);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem_base = *tmem_slot;
+  volatile int* abort_flag = &s_abort;
 
-  // contiguous vocabulary slice of this CTA, in multiples of 16 rows
-  const int v16 = (a.V + 15) / 16;
-  const int v_lo = (int)((long)blockIdx.x * v16 / a.nblk) * 16;
-  const int v_hi = min(a.V, (int)((long)(blockIdx.x + 1) * v16 / a.nblk) * 16);
-  const int nkb = a.d / KB;
+  const int items = a.ntiles * a.nchunks;
+  const int i0 = (int)((long)blockIdx.x * items / gridDim.x);
+  const int i1 = (int)((long)(blockIdx.x + 1) * items / gridDim.x);
+  const int nkb = a.d / BK;
 
-  for (int vp = v_lo; vp < v_hi; vp += CM) {
-    for (int np = 0; np < a.rows; np += CN) {
-      auto load = [&](int stage, int kb) {
-        uint16_t* wst = ws + stage * W_STAGE;
-        uint16_t* hst = hs + stage * H_STAGE;
-        const int k0 = kb * KB;
-        for (int e = threadIdx.x; e < CM * 8; e += blockDim.x) {
-          const int rr = e >> 3, c = e & 7;
-          const int v = vp + rr;
-          const bool ok = v < v_hi;
-          const uint16_t* src = a.w + (int64_t)(ok ? v : v_lo) * a.d + k0 + c * 8;
-          cp_async16(smem_u32(wst + rr * KB + ((c ^ (rr & 7)) * 8)), src, ok ? 16 : 0);
-        }
-        for (int e = threadIdx.x; e < CN * 8; e += blockDim.x) {
-          const int rr = e >> 3, c = e & 7;
-          const int r = np + rr;
-          const bool ok = r < a.rows;
-          const uint16_t* src = a.hidden + (int64_t)(ok ? r : 0) * a.d + k0 + c * 8;
-          cp_async16(smem_u32(hst + rr * KB + ((c ^ (rr & 7)) * 8)), src, ok ? 16 : 0);
-        }
-      };
-      float acc[2][NT][4];
-#pragma unroll
-      for (int m = 0; m < 2; ++m)
-#pragma unroll
-        for (int n = 0; n < NT; ++n) acc[m][n][0] = acc[m][n][1] = acc[m][n][2] = acc[m][n][3] = 0.f;
-
-#pragma unroll
-      for (int s = 0; s < STAGES - 1; ++s) {
-        if (s < nkb) load(s, s);
-        cp_async_commit();
-      }
-      for (int kb = 0; kb < nkb; ++kb) {
-        cp_async_wait<STAGES - 2>();
-        __syncthreads();
-        if (kb + STAGES - 1 < nkb) load((kb + STAGES - 1) % STAGES, kb + STAGES - 1);
-        cp_async_commit();
-        const uint16_t* wst = ws + (kb % STAGES) * W_STAGE;
-        const uint16_t* hst = hs + (kb % STAGES) * H_STAGE;
-#pragma unroll
-        for (int kk = 0; kk < KB / 16; ++kk) {
-          uint32_t af[2][4];
-#pragma unroll
-          for (int m = 0; m < 2; ++m) {
-            const int rr = warp * WM + m * 16 + (lane & 15);
-            const int c = kk * 2 + (lane >> 4);
-            ldmatrix_x4(af[m], smem_u32(wst + rr * KB + ((c ^ (rr & 7)) * 8)));
-          }
-#pragma unroll
-          for (int n = 0; n + 1 < NT; n += 2) {
-            const int rr = n * 8 + (lane & 7) + ((lane >> 4) << 3);
-            const int c = kk * 2 + ((lane >> 3) & 1);
-            uint32_t bf[4];
-            ldmatrix_x4(bf, smem_u32(hst + rr * KB + ((c ^ (rr & 7)) * 8)));
-#pragma unroll
-            for (int m = 0; m < 2; ++m) {
-              mma_bf16_16816(acc[m][n], af[m], bf[0], bf[1]);
-              mma_bf16_16816(acc[m][n + 1], af[m], bf[2], bf[3]);
-            }
-          }
-          if (NT & 1) {
-            // last n8 tile: lanes 16..31 repeat rows of lanes 0..15
-            const int n = NT - 1;
-            const int rr = n * 8 + (lane & 7);
-            const int c = kk * 2 + ((lane >> 3) & 1);
-            uint32_t bf[4];
-            ldmatrix_x4(bf, smem_u32(hst + rr * KB + ((c ^ (rr & 7)) * 8)));
-#pragma unroll
-            for (int m = 0; m < 2; ++m) mma_bf16_16816(acc[m][n], af[m], bf[0], bf[1]);
-          }
+  if (warp == 0) {
+    // ---------------- TMA producer
+    if (lane == 0) {
+      int it = 0;
+      bool ok = true;
+      for (int item = i0; item < i1 && ok; ++item) {
+        const int v0 = (item / a.nchunks) * BM;
+        const int r0 = (item % a.nchunks) * a.npad;
+        for (int kb = 0; kb < nkb; ++kb, ++it) {
+          const int s = it % a.stages;
+          const uint32_t ph = (uint32_t)(it / a.stages) & 1u;
+          if (!wait_or_abort(&empty[s], ph ^ 1u, abort_flag)) { ok = false; break; }
+          uint8_t* st = smem + (size_t)s * stage_bytes;
+          mbar_expect_tx(&full[s], stage_bytes);
+          tma_load_2d(st, &tmW, &full[s], kb * BK, v0);
+          tma_load_2d(st + a_bytes, &tmH, &full[s], kb * BK, r0);
         }
       }
-      cp_async_wait<0>();
-      __syncthreads();
-      // epilogue: fp32 logits
-#pragma unroll
-      for (int m = 0; m < 2; ++m) {
-#pragma unroll
-        for (int n = 0; n < NT; ++n) {
-#pragma unroll
-          for (int e = 0; e < 4; ++e) {
-            const int v = vp + warp * WM + m * 16 + (lane >> 2) + (e >= 2 ? 8 : 0);
-            const int r = np + n * 8 + (lane & 3) * 2 + (e & 1);
-            if (v < v_hi && r < a.rows) a.logits[(int64_t)r * a.V + v] = acc[m][n][e];
-          }
-        }
+      if (!ok) {
+        // let the loads already issued land before the CTA can exit
+        for (int j = max(0, it - a.stages); j < it; ++j)
+          mbar_wait(&full[j % a.stages], (uint32_t)(j / a.stages) & 1u);
+        set_err(a.err, MEDUSA_DEVERR_TIMEOUT);
       }
     }
+  } else if (warp == 1) {
+    // ---------------- MMA issuer
+    if (lane == 0) {
+      const uint32_t idesc = idesc_bf16_f32(BM, a.npad);
+      int it = 0, local = 0;
+      bool ok = true;
+      for (int item = i0; item < i1 && ok; ++item, ++local) {
+        const int acc = local & 1;
+        const uint32_t aph = (uint32_t)(local >> 1) & 1u;
+        if (!wait_or_abort(&tempty[acc], aph ^ 1u, abort_flag)) { ok = false; break; }
+        tc_fence_after();
+        const uint32_t d_tmem = tmem_base + (uint32_t)(acc * a.npad);
+        for (int kb = 0; kb < nkb; ++kb, ++it) {
+          const int s = it % a.stages;
+          const uint32_t ph = (uint32_t)(it / a.stages) & 1u;
+          if (!wait_or_abort(&full[s], ph, abort_flag)) { ok = false; break; }
+          tc_fence_after();
+          const uint32_t sa = smem_u32(smem + (size_t)s * stage_bytes);
+          const uint64_t da = desc_kmajor_sw128(sa), db = desc_kmajor_sw128(sa + a_bytes);
+#pragma unroll
+          for (int kk = 0; kk < BK / UK; ++kk)  // +32 bytes of K per instruction
+            umma_bf16(d_tmem, da + (uint64_t)(kk * 2), db + (uint64_t)(kk * 2), idesc, (kb | kk) != 0);
+          umma_commit(&empty[s]);  // the stage is free once these MMAs have read it
+        }
+        if (ok) umma_commit(&tfull[acc]);  // accumulator complete
+      }
+      if (!ok) {
+        if (it > 0) mbar_wait(&empty[(it - 1) % a.stages], (uint32_t)((it - 1) / a.stages) & 1u);
+        set_err(a.err, MEDUSA_DEVERR_TIMEOUT);
+      }
+    }
+  } else {
+    // ---------------- epilogue: TMEM -> registers -> logits
+    const int g = warp & 3;  // this warp may read TMEM lanes 32g .. 32g+31
+    int local = 0;
+    for (int item = i0; item < i1; ++item, ++local) {
+      const int acc = local & 1;
+      const uint32_t aph = (uint32_t)(local >> 1) & 1u;
+      const bool got = wait_or_abort(&tfull[acc], aph, abort_flag);
+      if (__any_sync(0xffffffffu, !got)) {
+        if (lane == 0) set_err(a.err, MEDUSA_DEVERR_TIMEOUT);
+        break;
+      }
+      __syncwarp();
+      tc_fence_after();
+      const int v = (item / a.nchunks) * BM + 32 * g + lane;
+      const int r0 = (item % a.nchunks) * a.npad;
+      for (int c = 0; c < a.npad / 16; ++c) {
+        uint32_t r[16];
+        tmem_ld_32x32b_x16(tmem_base + ((uint32_t)(32 * g) << 16) + (uint32_t)(acc * a.npad + c * 16), r);
+        tmem_ld_wait();
+        if (v < a.V) {
+#pragma unroll
+          for (int i = 0; i < 16; ++i) {
+            const int row = r0 + c * 16 + i;
+            if (row < a.rows) a.logits[(int64_t)row * a.V + v] = __uint_as_float(r[i]);
+          }
+        }
+      }
+      tc_fence_before();
+      mbar_arrive(&tempty[acc]);
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem_base, a.tmem_cols);
   }
 }
 
@@ -158,6 +222,40 @@ __global__ void __launch_bounds__(256) lm_head_f32_kernel(const float* hidden, c
   if (lane == 0) logits[(int64_t)r * V + v] = acc;
 }
 
+// ------------------------------------------------------------------ host --
+
+using EncodeTiled = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                                 const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
+                                 CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiled encode_fn() {
+  static EncodeTiled fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<EncodeTiled>(p);
+  });
+  return fn;
+}
+
+// Row-major bf16 matrix [outer][inner] -> tiles of box_outer rows x 64
+// columns, 128-byte swizzle, zero fill outside the matrix.
+bool make_map(CUtensorMap* m, const void* base, uint64_t inner, uint64_t outer, uint32_t box_outer) {
+  EncodeTiled enc = encode_fn();
+  if (!enc) return false;
+  const cuuint64_t dims[2] = {inner, outer};
+  const cuuint64_t strides[1] = {inner * 2};
+  const cuuint32_t box[2] = {(cuuint32_t)BK, box_outer};
+  const cuuint32_t estr[2] = {1, 1};
+  return enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box, estr,
+             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 }  // namespace
 }  // namespace medusa
 
@@ -168,22 +266,36 @@ extern "C" size_t medusa_lm_head_workspace_size(int rows, int d, int V) {
   return 0;
 }
 
-extern "C" int medusa_lm_head_verify(const void* hidden, const void* w_lm, float* logits, int rows,
-                                     int d, int V, medusa_dtype dtype, void* workspace,
-                                     size_t workspace_bytes, void* stream) {
+extern "C" int medusa_lm_head_verify(const void* hidden, const void* w_lm, float* logits, int rows, int d,
+                                     int V, medusa_dtype dtype, void* workspace, size_t workspace_bytes,
+                                     int32_t* err, void* stream) {
   const char* fn = "medusa_lm_head_verify";
   (void)workspace; (void)workspace_bytes;
   if (!hidden || !w_lm || !logits) return fail(MEDUSA_ERR_INVALID, "%s: NULL tensor", fn);
   if (rows < 1 || d < 1 || V < 1) return fail(MEDUSA_ERR_INVALID, "%s: rows=%d d=%d V=%d", fn, rows, d, V);
   cudaStream_t s = as_stream(stream);
   if (dtype == MEDUSA_BF16) {
-    if (d % KB) return fail(MEDUSA_ERR_UNSUPPORTED, "%s: d=%d not a multiple of %d", fn, d, KB);
+    if (d % BK) return fail(MEDUSA_ERR_UNSUPPORTED, "%s: d=%d not a multiple of %d", fn, d, BK);
     if ((reinterpret_cast<uintptr_t>(hidden) | reinterpret_cast<uintptr_t>(w_lm)) % 16)
       return fail(MEDUSA_ERR_INVALID, "%s: hidden / w_lm not 16-byte aligned", fn);
-    LmArgs a{static_cast<const uint16_t*>(hidden), static_cast<const uint16_t*>(w_lm), logits, rows, d, V, 0};
-    a.nblk = std::min(sm_count(), (V + 15) / 16);
-    cudaFuncSetAttribute(lm_head_mma_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)SMEM);
-    lm_head_mma_kernel<<<a.nblk, NWARP * 32, SMEM, s>>>(a);
+    LmArgs a{};
+    a.logits = logits; a.rows = rows; a.d = d; a.V = V; a.err = err;
+    a.nchunks = (rows + kMaxN - 1) / kMaxN;
+    a.npad = ((rows + a.nchunks - 1) / a.nchunks + 15) / 16 * 16;
+    a.ntiles = (V + BM - 1) / BM;
+    const size_t stage_bytes = (size_t)BM * BK * 2 + (size_t)a.npad * BK * 2;
+    a.stages = (int)std::min<size_t>(8, (kSmemBudget - 1024 - 256) / stage_bytes);
+    uint32_t cols = 32;
+    while (cols < (uint32_t)(2 * a.npad)) cols <<= 1;
+    a.tmem_cols = cols;
+    CUtensorMap tmW, tmH;
+    if (!make_map(&tmW, w_lm, (uint64_t)d, (uint64_t)V, BM) ||
+        !make_map(&tmH, hidden, (uint64_t)d, (uint64_t)rows, (uint32_t)a.npad))
+      return fail(MEDUSA_ERR_CUDA, "%s: cuTensorMapEncodeTiled failed", fn);
+    const size_t smem = 1024 + (size_t)a.stages * stage_bytes + (2 * a.stages + 4) * 8 + 16;
+    cudaFuncSetAttribute(lm_head_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    const int grid = std::min(sm_count(), a.ntiles * a.nchunks);
+    lm_head_tc_kernel<<<grid, kThreads, smem, s>>>(tmW, tmH, a);
     return check_launch(fn);
   }
   if (dtype != MEDUSA_F32) return fail(MEDUSA_ERR_UNSUPPORTED, "%s: dtype", fn);

@@ -18,7 +18,7 @@ LIB_PATH = os.path.join(_PKG, "libmedusa.so")
 MEDUSA_F32, MEDUSA_BF16 = 0, 1
 MAX_T, MAX_K, MAX_S, MAX_B = 512, 8, 16, 16
 STATUS = {0: "OK", -1: "INVALID", -2: "UNSUPPORTED", -3: "CAPACITY", -4: "WORKSPACE", -5: "CUDA"}
-DEVERR = {1: "TOKEN", 2: "NODE", 4: "CAPACITY", 8: "LENGTH"}
+DEVERR = {1: "TOKEN", 2: "NODE", 4: "CAPACITY", 8: "LENGTH", 16: "TIMEOUT"}
 
 if not os.path.exists(LIB_PATH):
     raise ImportError(
@@ -48,7 +48,7 @@ _SIGS = {
     "medusa_tree_attn_workspace_size": (SZ, [I, I, I, I, I]),
     "medusa_tree_attn": (I, [P, P, P, P, P, P, P, P, TREE, I, I, I, I, F, F, I, P, P, SZ, P, P]),
     "medusa_lm_head_workspace_size": (SZ, [I, I, I]),
-    "medusa_lm_head_verify": (I, [P, P, P, I, I, I, I, P, SZ, P]),
+    "medusa_lm_head_verify": (I, [P, P, P, I, I, I, I, P, SZ, P, P]),
     "medusa_accept_workspace_size": (SZ, [I, I]),
     "medusa_accept": (I, [P, P, TREE, I, I, I, F, F, F, P, P, P, P, P, P, SZ, P, P]),
     "medusa_accept_noalloc": (I, [P, P, TREE, I, I, I, F, F, F, P, P, P, P, P, P, P]),
@@ -209,13 +209,14 @@ def medusa_lm_head_workspace_size(rows, d, V) -> int:
     return int(_lib.medusa_lm_head_workspace_size(rows, d, V))
 
 
-def medusa_lm_head_verify(hidden, w_lm, logits, workspace=None, stream=None):
+def medusa_lm_head_verify(hidden, w_lm, logits, workspace=None, err=None, stream=None):
     d = hidden.shape[-1]
     rows = hidden.numel() // d
     V = w_lm.shape[0]
     nbytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
     _check(_lib.medusa_lm_head_verify(_ptr(hidden), _ptr(w_lm), _ptr(logits), rows, d, V, _dtype(hidden),
-                                      _ptr(workspace), nbytes, _stream(stream)), "medusa_lm_head_verify")
+                                      _ptr(workspace), nbytes, _ptr(err), _stream(stream)),
+           "medusa_lm_head_verify")
 
 
 def medusa_accept_workspace_size(B, T) -> int:

@@ -87,7 +87,7 @@ class VerifyStep:
         M.medusa_tree_attn(x["q"], x["k_new"], x["v_new"], x["k_cache"], x["v_cache"], x["seq_start"],
                            x["prefix_len"], x["seq_cap"], self.tree, self.max_prefix, self.rope_theta,
                            self.scale, self.out, self.ws_attn, self.err, stream)
-        M.medusa_lm_head_verify(x["hidden"], self.w_lm, self.logits, None, stream)
+        M.medusa_lm_head_verify(x["hidden"], self.w_lm, self.logits, None, self.err, stream)
         M.medusa_accept(self.logits, x["tokens"], self.tree, self.mode, self.temperature, self.eps,
                         self.delta, self.accept_len, self.accepted_nodes, self.next_root, self.best_node,
                         self.best_logp, self.ws_accept, self.err, stream)

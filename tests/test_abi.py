@@ -158,12 +158,14 @@ def test_validation_statuses(M):
     assert L.medusa_tree_attn(FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, ref, 1, 4, 64, 64, 1e4, 0.1,
                               7, FAKE, FAKE, 1 << 30, None, None) == -2
     assert L.medusa_tree_attn(FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, ref, 1, 4, 64, 64, 1e4, 0.1,
-                              1, FAKE, FAKE, 16, None, None) == -4
+                              0, FAKE, FAKE, 16, None, None) == -4   # f32 stages q' in scratch
+    assert L.medusa_tree_attn(FAKE + 2, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, ref, 1, 4, 64, 64, 1e4, 0.1,
+                              1, FAKE, None, 0, None, None) == -1    # bf16 needs 16-byte alignment
     assert L.medusa_tree_attn(FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, ref, 17, 4, 64, 64, 1e4, 0.1,
                               1, FAKE, FAKE, 1 << 30, None, None) == -1
     # LM head: d not a multiple of 64 for bf16; misaligned pointers
-    assert L.medusa_lm_head_verify(FAKE, FAKE, FAKE, 15, 100, 1000, 1, None, 0, None) == -2
-    assert L.medusa_lm_head_verify(FAKE + 2, FAKE, FAKE, 15, 256, 1000, 1, None, 0, None) == -1
+    assert L.medusa_lm_head_verify(FAKE, FAKE, FAKE, 15, 100, 1000, 1, None, 0, None, None) == -2
+    assert L.medusa_lm_head_verify(FAKE + 2, FAKE, FAKE, 15, 256, 1000, 1, None, 0, None, None) == -1
     # KV compaction: Kmax above the maximum, misaligned cache
     assert L.medusa_kv_compact(FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, 1, 4, 64, 9, 1, None, None, None) == -2
     assert L.medusa_kv_compact(FAKE + 4, FAKE, FAKE, FAKE, FAKE, FAKE, 1, 4, 64, 3, 1, None, None, None) == -1
@@ -183,5 +185,5 @@ def test_workspace_queries(M):
     assert M.medusa_accept_workspace_size(1, 65) >= 65 * 16
     assert M.medusa_heads_topk_workspace_size(1, 4, 4096, 32000, 8) >= 4 * 4096 * 2
     n = M.medusa_tree_attn_workspace_size(1, 32, 128, 65, 1024)
-    assert n >= 65 * 32 * 128 * 2
+    assert n >= 65 * 32 * 128 * 4
     assert M.medusa_lm_head_workspace_size(65, 4096, 32000) == 0
