@@ -48,6 +48,8 @@ def parse_args():
     ap.add_argument("--plant-depth", type=int, default=3)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--attn-branch", choices=["serial", "fork"], default="fork",
+                    help="tree attention before the LM head on one stream, or on a forked graph branch")
     return ap.parse_args()
 
 
@@ -226,6 +228,7 @@ def run_native(args, w, rank, world, local_rank):
 
     # one graph holds K steps with timing events at every call boundary
     calls = ["tree_attn", "lm_head_verify", "accept", "kv_compact", "heads_topk", "build_candidates"]
+    s2 = torch.cuda.Stream(device=dev) if args.attn_branch == "fork" else None  # side branch for attention
 
     def capture(nsteps, with_events):
         g = torch.cuda.CUDAGraph()
@@ -238,7 +241,7 @@ def run_native(args, w, rank, world, local_rank):
                     evs.append(e)
                     run_calls(st, x, s, e)
                 else:
-                    st.run(x, s)
+                    st.run(x, s, side_stream=s2)
         return g, evs
 
     def run_calls(st, x, s, e):
@@ -302,14 +305,14 @@ def run_native(args, w, rank, world, local_rank):
 
     e2e = None
     if not args.no_e2e:
-        e2e = measure_e2e(args, w, st, x, xh, prefix0, s, torch, M)
+        e2e = measure_e2e(args, w, st, x, xh, prefix0, s, s2, torch, M)
 
     return dict(ms_step=ms_step, ms_events_step=ms_events / args.steps, per_call_ms=per_call, clocks=clocks,
                 T=T, s_heads=st.s_heads, L_list=L_list, accept_len=accept_len, e2e=e2e,
                 launches=st.launches_per_step * args.steps, tree=ht)
 
 
-def measure_e2e(args, w, st, x, xh, prefix0, s, torch, M):
+def measure_e2e(args, w, st, x, xh, prefix0, s, s2, torch, M):
     """Same metric through the public C-ABI calls with host buffers: per step,
     pinned host inputs -> device, the six calls, results -> pinned host."""
     names_in = ["q", "k_new", "v_new", "hidden", "tokens"]
@@ -326,7 +329,7 @@ def measure_e2e(args, w, st, x, xh, prefix0, s, torch, M):
             for k in names_in:
                 x[k].copy_(host_in[k], non_blocking=True)
             x["prefix_len"].copy_(host_pl, non_blocking=True)
-            st.run(x, s)
+            st.run(x, s, side_stream=s2)
             for h, d in zip(host_out, outs):
                 h.copy_(d, non_blocking=True)
         s.synchronize()
@@ -514,7 +517,7 @@ def main():
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": w["dtype"], "data": "synthetic (seeded random weights and activations)",
-        "config": config_dict(w, {"parallelism": f"replicas{world}" if world > 1 else "single-gpu",
+        "config": config_dict(w, {"parallelism": f"replicas{world}" if world > 1 else "single-gpu", "attn_branch": args.attn_branch,
                                   "T_rows": r["T"], "s": r["s_heads"], "planted_accept_len": r["accept_len"]}),
         "roofline": {"bound": "hbm", "kernel": f"medusa_{dom}", "achieved": achieved, "peak": peaks["hbm_gbs"],
                      "unit": "GB/s", "frac": achieved / peaks["hbm_gbs"], "traffic": traffic,

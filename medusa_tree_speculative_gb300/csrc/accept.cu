@@ -293,14 +293,13 @@ extern "C" int medusa_accept(const float* logits, const int32_t* tokens, const m
   const float inv_temp = mode == 1 ? 1.f / temperature : 1.f;
   dim3 g(tree->T, B);
   if (mode == 1)
-    accept_rowstat_kernel<true><<<g, 512, 0, s>>>(logits, tree->T, V, inv_temp, stats);
+    launch_kernel(accept_rowstat_kernel<true>, g, dim3(512), 0, s, logits, tree->T, V, inv_temp, stats);
   else
-    accept_rowstat_kernel<false><<<g, 512, 0, s>>>(logits, tree->T, V, inv_temp, stats);
+    launch_kernel(accept_rowstat_kernel<false>, g, dim3(512), 0, s, logits, tree->T, V, inv_temp, stats);
   if (int rc = check_launch(fn)) return rc;
   const int threads = (tree->T + 31) / 32 * 32;
-  accept_select_kernel<<<B, threads, 0, s>>>(logits, tokens, *tree, V, mode, inv_temp, eps, delta,
-                                             stats, accept_len, accepted_nodes, next_root, best_node,
-                                             best_logp, err);
+  launch_kernel(accept_select_kernel, dim3(B), dim3(threads), 0, s, logits, tokens, *tree, V, mode, inv_temp, eps,
+             delta, (const RowStat*)stats, accept_len, accepted_nodes, next_root, best_node, best_logp, err);
   return check_launch(fn);
 }
 

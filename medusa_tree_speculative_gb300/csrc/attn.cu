@@ -588,17 +588,17 @@ extern "C" int medusa_tree_attn(const void* q, const void* k_new, const void* v_
     const size_t sm = smem_bytes(Dh, a.warps, a.K);
     if (Dh == 128) {
       cudaFuncSetAttribute(attn_tree_kernel<128>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sm);
-      attn_tree_kernel<128><<<grid, a.warps * 32, sm, s>>>(a);
+      launch_kernel(attn_tree_kernel<128>, grid, dim3(a.warps * 32), sm, s, a);
     } else {
       cudaFuncSetAttribute(attn_tree_kernel<64>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sm);
-      attn_tree_kernel<64><<<grid, a.warps * 32, sm, s>>>(a);
+      launch_kernel(attn_tree_kernel<64>, grid, dim3(a.warps * 32), sm, s, a);
     }
     return check_launch(fn);
   }
   dim3 g1(tree->T, B);
-  rope_append_f32_kernel<<<g1, 256, 0, s>>>(a);
+  launch_kernel(rope_append_f32_kernel, g1, dim3(256), 0, s, a);
   if (int rc = check_launch(fn)) return rc;
   dim3 g2(tree->T, H, B);
-  attn_f32_kernel<<<g2, 128, 0, s>>>(a);
+  launch_kernel(attn_f32_kernel, g2, dim3(128), 0, s, a);
   return check_launch(fn);
 }

@@ -40,7 +40,7 @@ extern "C" int medusa_build_candidates(const int32_t* next_root, const int32_t* 
     return fail(MEDUSA_ERR_INVALID, "%s: B=%d s_max=%d K=%d (tree depth %d)", fn, B, s_max, K, tree->K);
   for (int k = 0; k < tree->K; ++k)
     if (tree->s[k] > s_max) return fail(MEDUSA_ERR_INVALID, "%s: tree s[%d]=%d > s_max=%d", fn, k, tree->s[k], s_max);
-  build_candidates_kernel<<<B, (tree->T + 31) / 32 * 32, 0, as_stream(stream)>>>(next_root, topk, s_max, K,
-                                                                                 *tree, tokens);
+  launch_kernel(build_candidates_kernel, dim3(B), dim3((tree->T + 31) / 32 * 32), 0, as_stream(stream), next_root,
+             topk, s_max, K, *tree, tokens);
   return check_launch(fn);
 }

@@ -68,9 +68,9 @@ __global__ void __launch_bounds__(256) heads_gemv_kernel(GemvArgs a) {
   const TE* W = static_cast<const TE*>(a.w);
   __shared__ int head_id[MEDUSA_MAX_K];
   if (threadIdx.x < MEDUSA_MAX_K) head_id[threadIdx.x] = a.heads[threadIdx.x];
+  __syncthreads();
   if (W1 && blockIdx.x == 0)
     for (int i = threadIdx.x; i < a.ncounters; i += blockDim.x) a.counters[i] = 0;
-  __syncthreads();
 
   // input vectors of this call, one per sequence (W1: hidden[b][last_node]);
   // an out-of-range node reads row 0 and raises the error bit
@@ -298,9 +298,9 @@ template <typename TE, int NB>
 void launch_gemv(const GemvArgs& a, bool w1, cudaStream_t s) {
   const int blocks = std::max(1, std::min(sm_count() * 4, (int)((int64_t(a.nused) * a.rows + 7) / 8)));
   if (w1)
-    heads_gemv_kernel<TE, NB, true><<<blocks, 256, 0, s>>>(a);
+    launch_kernel(heads_gemv_kernel<TE, NB, true>, dim3(blocks), dim3(256), 0, s, a);
   else
-    heads_gemv_kernel<TE, NB, false><<<blocks, 256, 0, s>>>(a);
+    launch_kernel(heads_gemv_kernel<TE, NB, false>, dim3(blocks), dim3(256), 0, s, a);
 }
 
 template <typename TE>
@@ -380,9 +380,9 @@ extern "C" int medusa_heads_topk(const void* hidden, const int32_t* last_node, i
   ta.counters = a.counters;
   ta.topk = topk;
   dim3 g(nchunk, a.nused, B);
-  if (smax_used <= 2) topk_kernel<2><<<g, 256, 0, st>>>(ta);
-  else if (smax_used <= 4) topk_kernel<4><<<g, 256, 0, st>>>(ta);
-  else if (smax_used <= 8) topk_kernel<8><<<g, 256, 0, st>>>(ta);
-  else topk_kernel<16><<<g, 256, 0, st>>>(ta);
+  if (smax_used <= 2) launch_kernel(topk_kernel<2>, g, dim3(256), 0, st, ta);
+  else if (smax_used <= 4) launch_kernel(topk_kernel<4>, g, dim3(256), 0, st, ta);
+  else if (smax_used <= 8) launch_kernel(topk_kernel<8>, g, dim3(256), 0, st, ta);
+  else launch_kernel(topk_kernel<16>, g, dim3(256), 0, st, ta);
   return check_launch(fn);
 }

@@ -106,10 +106,10 @@ extern "C" int medusa_kv_compact(void* k_cache, void* v_cache, const int64_t* se
   auto* kc = static_cast<uint8_t*>(k_cache);
   auto* vc = static_cast<uint8_t*>(v_cache);
   if (Kmax <= 4)
-    kv_compact_kernel<5, 2><<<B, 512, 0, as_stream(stream)>>>(kc, vc, seq_start, prefix_len, accepted_nodes,
-                                                            accept_len, row_bytes, Kmax, src_slots, err);
+    launch_kernel(kv_compact_kernel<5, 2>, dim3(B), dim3(512), 0, as_stream(stream), kc, vc, seq_start, prefix_len,
+               accepted_nodes, accept_len, row_bytes, Kmax, src_slots, err);
   else
-    kv_compact_kernel<MEDUSA_MAX_K + 1, 1><<<B, 512, 0, as_stream(stream)>>>(
-        kc, vc, seq_start, prefix_len, accepted_nodes, accept_len, row_bytes, Kmax, src_slots, err);
+    launch_kernel(kv_compact_kernel<MEDUSA_MAX_K + 1, 1>, dim3(B), dim3(512), 0, as_stream(stream), kc, vc,
+               seq_start, prefix_len, accepted_nodes, accept_len, row_bytes, Kmax, src_slots, err);
   return check_launch(fn);
 }

@@ -11,9 +11,12 @@
 // bf16: tcgen05 tensor-core GEMM with TMEM accumulators, swap-AB: the
 // vocabulary is the MMA's M dimension (128-row tiles of W, K-major) and the
 // tree rows its N dimension (all rows of a chunk, padded to 16, K-major), so
-// one instruction covers every tree row.  Persistent CTAs, one per SM, own
-// contiguous runs of vocabulary tiles: each weight byte is read once and no
-// partial sums are exchanged.  Warp roles:
+// one instruction covers every tree row.  When the vocabulary has more tiles
+// than there are SMs, a work item is a pair of adjacent tiles that share each
+// hidden k-block (halving the L2->SM traffic per weight byte).  Persistent
+// CTAs, balanced to the same number of work items each, own contiguous runs
+// of the vocabulary: each weight byte is read once and no partial sums are
+// exchanged.  Warp roles:
 //   warp 0     one thread issues TMA loads of W and hidden k-blocks (64 wide,
 //              128-byte swizzle) into a ring of shared stages,
 //   warp 1     allocates TMEM; one thread issues the MMAs (4 per stage) and
@@ -51,7 +54,8 @@ struct LmArgs {
   int rows, d, V;
   int npad;     // MMA N of every chunk (multiple of 16, <= kMaxN)
   int nchunks;  // chunks of tree rows
-  int ntiles;   // vocabulary tiles
+  int nt;       // vocabulary tiles per work item (1 or 2): they share each hidden k-block
+  int ngroups;  // work items along the vocabulary = ceil(tiles / nt)
   int stages;
   uint32_t tmem_cols;
   int32_t* err;
@@ -71,7 +75,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                       const __grid_constant__ LmArgs a) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  const uint32_t a_bytes = BM * BK * 2;
+  const uint32_t a_bytes = (uint32_t)a.nt * BM * BK * 2;  // nt W tiles, 16 KB each
   const uint32_t b_bytes = (uint32_t)a.npad * BK * 2;
   const uint32_t stage_bytes = a_bytes + b_bytes;
   uint64_t* full = reinterpret_cast<uint64_t*>(smem + (size_t)a.stages * stage_bytes);
@@ -106,7 +110,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint32_t tmem_base = *tmem_slot;
   volatile int* abort_flag = &s_abort;
 
-  const int items = a.ntiles * a.nchunks;
+  const int items = a.ngroups * a.nchunks;
+  const uint32_t acc_cols = (uint32_t)(a.nt * a.npad);  // one accumulator: nt tiles side by side
   const int i0 = (int)((long)blockIdx.x * items / gridDim.x);
   const int i1 = (int)((long)(blockIdx.x + 1) * items / gridDim.x);
   const int nkb = a.d / BK;
@@ -117,7 +122,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       int it = 0;
       bool ok = true;
       for (int item = i0; item < i1 && ok; ++item) {
-        const int v0 = (item / a.nchunks) * BM;
+        const int v0 = (item / a.nchunks) * a.nt * BM;
         const int r0 = (item % a.nchunks) * a.npad;
         for (int kb = 0; kb < nkb; ++kb, ++it) {
           const int s = it % a.stages;
@@ -125,11 +130,13 @@ __global__ void __launch_bounds__(kThreads, 1)
           if (!wait_or_abort(&empty[s], ph ^ 1u, abort_flag)) { ok = false; break; }
           uint8_t* st = smem + (size_t)s * stage_bytes;
           mbar_expect_tx(&full[s], stage_bytes);
-          tma_load_2d(st, &tmW, &full[s], kb * BK, v0);
+          for (int t = 0; t < a.nt; ++t)  // rows past V (a missing second tile) read as zeros
+            tma_load_2d(st + t * (BM * BK * 2), &tmW, &full[s], kb * BK, v0 + t * BM);
           tma_load_2d(st + a_bytes, &tmH, &full[s], kb * BK, r0);
         }
       }
-      if (!ok) {
+      // every load of this CTA is in flight: the next kernel may start launching
+          if (!ok) {
         // let the loads already issued land before the CTA can exit
         for (int j = max(0, it - a.stages); j < it; ++j)
           mbar_wait(&full[j % a.stages], (uint32_t)(j / a.stages) & 1u);
@@ -147,17 +154,21 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint32_t aph = (uint32_t)(local >> 1) & 1u;
         if (!wait_or_abort(&tempty[acc], aph ^ 1u, abort_flag)) { ok = false; break; }
         tc_fence_after();
-        const uint32_t d_tmem = tmem_base + (uint32_t)(acc * a.npad);
+        const uint32_t d_tmem = tmem_base + (uint32_t)acc * acc_cols;
         for (int kb = 0; kb < nkb; ++kb, ++it) {
           const int s = it % a.stages;
           const uint32_t ph = (uint32_t)(it / a.stages) & 1u;
           if (!wait_or_abort(&full[s], ph, abort_flag)) { ok = false; break; }
           tc_fence_after();
           const uint32_t sa = smem_u32(smem + (size_t)s * stage_bytes);
-          const uint64_t da = desc_kmajor_sw128(sa), db = desc_kmajor_sw128(sa + a_bytes);
+          const uint64_t db = desc_kmajor_sw128(sa + a_bytes);
+          for (int t = 0; t < a.nt; ++t) {
+            const uint64_t da = desc_kmajor_sw128(sa + t * (BM * BK * 2));
 #pragma unroll
-          for (int kk = 0; kk < BK / UK; ++kk)  // +32 bytes of K per instruction
-            umma_bf16(d_tmem, da + (uint64_t)(kk * 2), db + (uint64_t)(kk * 2), idesc, (kb | kk) != 0);
+            for (int kk = 0; kk < BK / UK; ++kk)  // +32 bytes of K per instruction
+              umma_bf16(d_tmem + (uint32_t)(t * a.npad), da + (uint64_t)(kk * 2), db + (uint64_t)(kk * 2),
+                        idesc, (kb | kk) != 0);
+          }
           umma_commit(&empty[s]);  // the stage is free once these MMAs have read it
         }
         if (ok) umma_commit(&tfull[acc]);  // accumulator complete
@@ -181,17 +192,21 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       __syncwarp();
       tc_fence_after();
-      const int v = (item / a.nchunks) * BM + 32 * g + lane;
       const int r0 = (item % a.nchunks) * a.npad;
-      for (int c = 0; c < a.npad / 16; ++c) {
-        uint32_t r[16];
-        tmem_ld_32x32b_x16(tmem_base + ((uint32_t)(32 * g) << 16) + (uint32_t)(acc * a.npad + c * 16), r);
-        tmem_ld_wait();
-        if (v < a.V) {
+      for (int t = 0; t < a.nt; ++t) {
+        const int v = (item / a.nchunks) * a.nt * BM + t * BM + 32 * g + lane;
+        for (int c = 0; c < a.npad / 16; ++c) {
+          uint32_t r[16];
+          tmem_ld_32x32b_x16(tmem_base + ((uint32_t)(32 * g) << 16) + (uint32_t)acc * acc_cols +
+                                 (uint32_t)(t * a.npad + c * 16),
+                             r);
+          tmem_ld_wait();
+          if (v < a.V) {
 #pragma unroll
-          for (int i = 0; i < 16; ++i) {
-            const int row = r0 + c * 16 + i;
-            if (row < a.rows) a.logits[(int64_t)row * a.V + v] = __uint_as_float(r[i]);
+            for (int i = 0; i < 16; ++i) {
+              const int row = r0 + c * 16 + i;
+              if (row < a.rows) a.logits[(int64_t)row * a.V + v] = __uint_as_float(r[i]);
+            }
           }
         }
       }
@@ -282,11 +297,15 @@ extern "C" int medusa_lm_head_verify(const void* hidden, const void* w_lm, float
     a.logits = logits; a.rows = rows; a.d = d; a.V = V; a.err = err;
     a.nchunks = (rows + kMaxN - 1) / kMaxN;
     a.npad = ((rows + a.nchunks - 1) / a.nchunks + 15) / 16 * 16;
-    a.ntiles = (V + BM - 1) / BM;
-    const size_t stage_bytes = (size_t)BM * BK * 2 + (size_t)a.npad * BK * 2;
+    const int ntiles = (V + BM - 1) / BM;
+    // two vocabulary tiles per work item halve the hidden re-reads per weight
+    // byte; used while both accumulators of both tiles fit in TMEM
+    a.nt = (a.npad <= 128 && ntiles > sm_count()) ? 2 : 1;
+    a.ngroups = (ntiles + a.nt - 1) / a.nt;
+    const size_t stage_bytes = (size_t)a.nt * BM * BK * 2 + (size_t)a.npad * BK * 2;
     a.stages = (int)std::min<size_t>(8, (kSmemBudget - 1024 - 256) / stage_bytes);
     uint32_t cols = 32;
-    while (cols < (uint32_t)(2 * a.npad)) cols <<= 1;
+    while (cols < (uint32_t)(2 * a.nt * a.npad)) cols <<= 1;
     a.tmem_cols = cols;
     CUtensorMap tmW, tmH;
     if (!make_map(&tmW, w_lm, (uint64_t)d, (uint64_t)V, BM) ||
@@ -294,13 +313,16 @@ extern "C" int medusa_lm_head_verify(const void* hidden, const void* w_lm, float
       return fail(MEDUSA_ERR_CUDA, "%s: cuTensorMapEncodeTiled failed", fn);
     const size_t smem = 1024 + (size_t)a.stages * stage_bytes + (2 * a.stages + 4) * 8 + 16;
     cudaFuncSetAttribute(lm_head_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-    const int grid = std::min(sm_count(), a.ntiles * a.nchunks);
-    lm_head_tc_kernel<<<grid, kThreads, smem, s>>>(tmW, tmH, a);
+    // balanced: every CTA gets ceil or floor of items / grid work items
+    const int items = a.ngroups * a.nchunks;
+    const int per_cta = (items + sm_count() - 1) / sm_count();
+    const int grid = (items + per_cta - 1) / per_cta;
+    launch_kernel(lm_head_tc_kernel, dim3(grid), dim3(kThreads), smem, s, tmW, tmH, a);
     return check_launch(fn);
   }
   if (dtype != MEDUSA_F32) return fail(MEDUSA_ERR_UNSUPPORTED, "%s: dtype", fn);
   const int64_t total = (int64_t)rows * V;
-  lm_head_f32_kernel<<<(unsigned)((total + 7) / 8), 256, 0, s>>>(
-      static_cast<const float*>(hidden), static_cast<const float*>(w_lm), logits, rows, d, V);
+  launch_kernel(lm_head_f32_kernel, dim3((unsigned)((total + 7) / 8)), dim3(256), 0, s,
+             static_cast<const float*>(hidden), static_cast<const float*>(w_lm), logits, rows, d, V);
   return check_launch(fn);
 }

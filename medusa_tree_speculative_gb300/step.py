@@ -3,8 +3,9 @@ library calls.  Plumbing only: every step of the method runs in libmedusa.
 
 Call order (decoding-step box of the Medusa paper digest, steps 3-6 then 1-2
 for the next step):
-  medusa_tree_attn -> medusa_lm_head_verify -> medusa_accept ->
-  medusa_kv_compact -> medusa_heads_topk -> medusa_build_candidates
+  main chain: medusa_lm_head_verify -> medusa_accept -> medusa_heads_topk ->
+  medusa_build_candidates; medusa_tree_attn and then medusa_kv_compact either
+  on the same stream or on a forked branch that joins at the end
 """
 from __future__ import annotations
 
@@ -80,23 +81,38 @@ class VerifyStep:
         self.ws_accept = ws(M.medusa_accept_workspace_size(B, T))
         self.ws_heads = ws(M.medusa_heads_topk_workspace_size(B, K, d, V, self.s_max))
 
-    def run(self, x: dict, stream=None):
+    def run(self, x: dict, stream=None, side_stream=None):
         """x: device tensors q, k_new, v_new, hidden, tokens, k_cache, v_cache,
-        seq_start, prefix_len, seq_cap.  Updates the cache and prefix_len."""
-        B, T = self.B, self.T
+        seq_start, prefix_len, seq_cap.  Updates the cache and prefix_len.
+
+        One stream: tree attention, LM head, acceptance, heads, candidates,
+        KV compaction.  With `side_stream`: the chain LM head -> acceptance ->
+        heads -> candidates stays on `stream` while the tree attention and
+        then the KV compaction (which needs the acceptance result) run on a
+        forked branch that joins `stream` at the end."""
+        import torch
+
+        main = stream if stream is not None else torch.cuda.current_stream()
+        side = side_stream if side_stream is not None else main
+        if side is not main:
+            side.wait_stream(main)
         M.medusa_tree_attn(x["q"], x["k_new"], x["v_new"], x["k_cache"], x["v_cache"], x["seq_start"],
                            x["prefix_len"], x["seq_cap"], self.tree, self.max_prefix, self.rope_theta,
-                           self.scale, self.out, self.ws_attn, self.err, stream)
-        M.medusa_lm_head_verify(x["hidden"], self.w_lm, self.logits, None, self.err, stream)
+                           self.scale, self.out, self.ws_attn, self.err, side)
+        M.medusa_lm_head_verify(x["hidden"], self.w_lm, self.logits, None, self.err, main)
         M.medusa_accept(self.logits, x["tokens"], self.tree, self.mode, self.temperature, self.eps,
                         self.delta, self.accept_len, self.accepted_nodes, self.next_root, self.best_node,
-                        self.best_logp, self.ws_accept, self.err, stream)
+                        self.best_logp, self.ws_accept, self.err, main)
+        if side is not main:
+            side.wait_stream(main)  # compaction needs the accepted path
         M.medusa_kv_compact(x["k_cache"], x["v_cache"], x["seq_start"], x["prefix_len"],
                             self.accepted_nodes, self.accept_len, self.tree.K, self.src_slots, self.err,
-                            stream)
+                            side)
         M.medusa_heads_topk(x["hidden"], self.best_node, self.w1, self.b1, self.w2, self.s_heads,
-                            self.head_logits, self.topk, self.ws_heads, self.err, stream)
-        M.medusa_build_candidates(self.next_root, self.topk, self.tree, self.next_tokens, stream)
+                            self.head_logits, self.topk, self.ws_heads, self.err, main)
+        M.medusa_build_candidates(self.next_root, self.topk, self.tree, self.next_tokens, main)
+        if side is not main:
+            main.wait_stream(side)
 
     @property
     def launches_per_step(self) -> int:

@@ -136,7 +136,7 @@ def test_tree_attn_capacity_flag(M):
 
 LM_CASES = [("f32", 15, 256, 1024), ("bf16", 15, 256, 1024), ("bf16", 65, 256, 1000),
             ("bf16", 130, 512, 3000), ("bf16", 1, 64, 17), ("bf16", 260, 128, 333),
-            ("bf16", 65, 4096, 2048)]
+            ("bf16", 65, 4096, 2048), ("bf16", 65, 256, 20000), ("bf16", 17, 128, 40000)]
 
 
 @pytest.mark.parametrize("case", LM_CASES, ids=lambda c: "-".join(map(str, c)))
