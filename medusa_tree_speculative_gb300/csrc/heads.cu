@@ -9,13 +9,18 @@
 //
 // At batch size 1 both projections are matrix-vector products over weights
 // read once per step (about 80% of a 7B-shaped step's bytes), so they are
-// HBM-bound GEMVs: one warp per output row, 16-byte streaming loads with
-// eight loads in flight per lane, the input vector re-read from L1.
-//   gemv<W1>  u[b][k] = dtype(SiLU(W1_k h_b + b1_k) + h_b)   (scratch)
-//   gemv<W2>  head_logits[b][k] = W2_k u[b][k]              (fp32)
-//   topk      per (head, sequence) in chunks of ~1024 logits, one CTA each:
-//             per-lane sorted lists merged warp by warp (value descending,
-//             index ascending); the last chunk to finish merges the chunks
+// HBM-bound GEMVs: 16-byte streaming loads, eight in flight per lane, the
+// input vector re-read from L1.  Two kernels:
+//   w1        u[b][k] = dtype(SiLU(W1_k h_b + b1_k) + h_b) into scratch.  A CTA
+//             takes four rows at a time, two warps per row (one half each),
+//             so the 16384 rows of a 7B-shaped step spread evenly over the
+//             CTAs; the halves meet in shared memory for the epilogue.
+//   w2_topk   head_logits[b][k] = W2_k u[b][k] (fp32), fused with top-s: a
+//             CTA owns a contiguous slice of one head's vocabulary; after its
+//             warps have streamed the slice it selects the slice's top S from
+//             the logits it just wrote (per-thread sorted lists merged warp by
+//             warp), and the last CTA of a head to finish merges every CTA's
+//             list into topk (value descending, index ascending).
 #include <math.h>
 
 #include <algorithm>
@@ -26,19 +31,27 @@
 namespace medusa {
 namespace {
 
-struct GemvArgs {
-  const void* w;        // [K][rows][d]
-  int rows, d;
-  int nused;
-  int heads[MEDUSA_MAX_K];  // ids of the heads with s_k > 0
-  const void* hidden;   // [B][T][d]
+constexpr int kWarps = 8;  // 256-thread CTAs
+constexpr int UNROLL = 8;  // 16-byte loads in flight per lane
+constexpr int kMaxS = MEDUSA_MAX_S;
+
+struct HeadsArgs {
+  const void* w1;      // [K][d][d]
+  const void* w2;      // [K][V][d]
+  const void* b1;      // [K][d] or null
+  const void* hidden;  // [B][T][d]
   const int32_t* last_node;
-  int T, B, K;
-  const void* b1;       // [K][d] or null
-  void* u;              // [B][K][d] element type
-  float* logits;        // [B][K][V]
-  int* counters;        // top-s arrival counters, zeroed by the W1 pass
-  int ncounters;
+  int T, B, K, d, V, s_max;
+  int nused;
+  int32_t heads[MEDUSA_MAX_K];  // ids of the heads with s_k > 0
+  int32_t s[MEDUSA_MAX_K];      // their s_k
+  void* u;                      // [B][K][d] element type (scratch)
+  float* logits;                // [B][K][V]
+  int32_t* topk;                // [B][K][s_max]
+  float* cand_v;                // [nused][B][cpc][kMaxS] per-CTA candidates (scratch)
+  int* cand_i;
+  int* counters;                // [nused] CTA arrivals per head, zeroed by w1
+  int cpc;                      // w2 CTAs per used head
   int32_t* err;
 };
 
@@ -55,99 +68,97 @@ template <> struct Vec<float> {
   }
 };
 
-constexpr int UNROLL = 8;
-
-template <typename TE, int NB, bool W1>
-__global__ void __launch_bounds__(256) heads_gemv_kernel(GemvArgs a) {
+// acc[b] += w . x[b] over this lane's share of `nvec` 16-byte vectors.
+template <typename TE, int NB>
+MDEV void dot_rows(const TE* w, const TE* const* x, int nvec, int B, int lane, float* acc) {
   constexpr int EPV = Vec<TE>::N;
-  const int lane = threadIdx.x & 31;
-  const int64_t warp_g = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
-  const int64_t nwarps = ((int64_t)gridDim.x * blockDim.x) >> 5;
-  const int nvec = a.d / EPV;
-  const int64_t total = (int64_t)a.nused * a.rows;
-  const TE* W = static_cast<const TE*>(a.w);
-  __shared__ int head_id[MEDUSA_MAX_K];
-  if (threadIdx.x < MEDUSA_MAX_K) head_id[threadIdx.x] = a.heads[threadIdx.x];
-  __syncthreads();
-  if (W1 && blockIdx.x == 0)
-    for (int i = threadIdx.x; i < a.ncounters; i += blockDim.x) a.counters[i] = 0;
-
-  // input vectors of this call, one per sequence (W1: hidden[b][last_node]);
-  // an out-of-range node reads row 0 and raises the error bit
-  const TE* xin[NB];
+  for (int c0 = lane; c0 < nvec; c0 += 32 * UNROLL) {
+    uint4 wv[UNROLL];
 #pragma unroll
-  for (int b = 0; b < NB; ++b) {
-    if (W1) {
-      int n = b < a.B ? a.last_node[b] : 0;
-      if (n < 0 || n >= a.T) {
-        if (lane == 0 && warp_g == 0) set_err(a.err, MEDUSA_DEVERR_NODE);
-        n = 0;
-      }
-      xin[b] = static_cast<const TE*>(a.hidden) + ((int64_t)(b < a.B ? b : 0) * a.T + n) * a.d;
-    } else {
-      xin[b] = nullptr;
+    for (int u = 0; u < UNROLL; ++u) {
+      const int c = c0 + u * 32;
+      if (c < nvec) wv[u] = ldg_stream(w + (int64_t)c * EPV);
     }
-  }
-
-  for (int64_t g = warp_g; g < total; g += nwarps) {
-    const int slot = (int)(g / a.rows);
-    const int j = (int)(g % a.rows);
-    const int k = head_id[slot];
-    const TE* wrow = W + ((int64_t)k * a.rows + j) * a.d;
-    const TE* x[NB];
 #pragma unroll
-    for (int b = 0; b < NB; ++b)
-      x[b] = W1 ? xin[b] : static_cast<const TE*>(a.u) + ((int64_t)(b < a.B ? b : 0) * a.K + k) * a.d;
-    float acc[NB];
+    for (int u = 0; u < UNROLL; ++u) {
+      const int c = c0 + u * 32;
+      if (c < nvec) {
+        float wf[EPV];
+        Vec<TE>::unpack(wv[u], wf);
 #pragma unroll
-    for (int b = 0; b < NB; ++b) acc[b] = 0.f;
-    for (int c0 = lane; c0 < nvec; c0 += 32 * UNROLL) {
-      uint4 wv[UNROLL];
+        for (int b = 0; b < NB; ++b) {
+          if (b < B) {
+            float xf[EPV];
+            Vec<TE>::unpack(ldg_v4(x[b] + (int64_t)c * EPV), xf);
 #pragma unroll
-      for (int u = 0; u < UNROLL; ++u) {
-        const int c = c0 + u * 32;
-        if (c < nvec) wv[u] = ldg_stream(wrow + (int64_t)c * EPV);
-      }
-#pragma unroll
-      for (int u = 0; u < UNROLL; ++u) {
-        const int c = c0 + u * 32;
-        if (c < nvec) {
-          float wf[EPV];
-          Vec<TE>::unpack(wv[u], wf);
-#pragma unroll
-          for (int b = 0; b < NB; ++b) {
-            if (b < a.B) {
-              float xf[EPV];
-              Vec<TE>::unpack(ldg_v4(x[b] + (int64_t)c * EPV), xf);
-#pragma unroll
-              for (int e = 0; e < EPV; ++e) acc[b] = fmaf(wf[e], xf[e], acc[b]);
-            }
+            for (int e = 0; e < EPV; ++e) acc[b] = fmaf(wf[e], xf[e], acc[b]);
           }
         }
-      }
-    }
-#pragma unroll
-    for (int b = 0; b < NB; ++b) acc[b] = warp_sum(acc[b]);
-    if (lane < NB && lane < a.B) {
-      float y = 0.f;
-#pragma unroll
-      for (int b = 0; b < NB; ++b)
-        if (b == lane) y = acc[b];
-      const int b = lane;
-      if (W1) {
-        if (a.b1) y += to_f32(static_cast<const TE*>(a.b1)[(int64_t)k * a.d + j]);
-        const float silu = y / (1.f + expf(-y));
-        const float u = silu + to_f32(xin[b][j]);
-        static_cast<TE*>(a.u)[((int64_t)b * a.K + k) * a.d + j] = from_f32<TE>(u);
-      } else {
-        a.logits[((int64_t)b * a.K + k) * a.rows + j] = y;
       }
     }
   }
 }
 
-// ---------------------------------------------------------------- top-s --
+// ---------------------------------------------------------------- W1 pass --
+template <typename TE, int NB>
+__global__ void __launch_bounds__(kWarps * 32) heads_w1_kernel(const __grid_constant__ HeadsArgs a) {
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  __shared__ float part[kWarps][NB];
+  if (blockIdx.x == 0 && threadIdx.x < a.nused) a.counters[threadIdx.x] = 0;  // for w2_topk
 
+  // h_b = hidden[b][last_node[b]]; an out-of-range node reads row 0 and raises the error bit
+  const TE* x[NB];
+#pragma unroll
+  for (int b = 0; b < NB; ++b) {
+    int n = b < a.B ? a.last_node[b] : 0;
+    if (n < 0 || n >= a.T) {
+      if (threadIdx.x == 0 && blockIdx.x == 0) set_err(a.err, MEDUSA_DEVERR_NODE);
+      n = 0;
+    }
+    x[b] = static_cast<const TE*>(a.hidden) + ((int64_t)(b < a.B ? b : 0) * a.T + n) * a.d;
+  }
+  const TE* W = static_cast<const TE*>(a.w1);
+  const int half = a.d / 2;
+  const int hvec = half / Vec<TE>::N;
+  const int64_t total = (int64_t)a.nused * a.d;
+  const int64_t nquads = (total + kWarps / 2 - 1) / (kWarps / 2);
+  const int hf = warp & 1;
+  for (int64_t q = blockIdx.x; q < nquads; q += gridDim.x) {
+    const int64_t g = q * (kWarps / 2) + (warp >> 1);  // row of the stacked used heads
+    float acc[NB];
+#pragma unroll
+    for (int b = 0; b < NB; ++b) acc[b] = 0.f;
+    int k = 0, j = 0;
+    if (g < total) {
+      const int slot = (int)(g / a.d);
+      j = (int)(g % a.d);
+      k = a.heads[slot];
+      const TE* xs[NB];
+#pragma unroll
+      for (int b = 0; b < NB; ++b) xs[b] = x[b] + hf * half;
+      dot_rows<TE, NB>(W + ((int64_t)k * a.d + j) * a.d + hf * half, xs, hvec, a.B, lane, acc);
+    }
+#pragma unroll
+    for (int b = 0; b < NB; ++b) acc[b] = warp_sum(acc[b]);
+    if (lane == 0) {
+#pragma unroll
+      for (int b = 0; b < NB; ++b) part[warp][b] = acc[b];
+    }
+    __syncthreads();
+    if (hf == 0 && g < total && lane < a.B && lane < NB) {
+      const int b = lane;
+      float y = part[warp][b] + part[warp + 1][b];
+      if (a.b1) y += to_f32(static_cast<const TE*>(a.b1)[(int64_t)k * a.d + j]);
+      const float silu = y / (1.f + expf(-y));
+      static_cast<TE*>(a.u)[((int64_t)b * a.K + k) * a.d + j] = from_f32<TE>(silu + to_f32(x[b][j]));
+    }
+    __syncthreads();
+  }
+}
+
+// ---------------------------------------------------------- top-s helpers --
+
+// A register list of the S best (value, index) pairs, sorted.
 template <int S>
 struct TopList {
   float v[S];
@@ -174,8 +185,7 @@ struct TopList {
     v[S - 1] = -INFINITY;
     i[S - 1] = 0x7fffffff;
   }
-  // Warp-wide: the S best of all lanes' lists, in order, to out_v/out_i
-  // (valid on every lane).  Consumes the lists.
+  // Warp-wide: the S best of all lanes' lists, in order, on every lane.
   MDEV void warp_select(float* out_v, int* out_i) {
 #pragma unroll
     for (int r = 0; r < S; ++r) {
@@ -189,23 +199,7 @@ struct TopList {
   }
 };
 
-struct HeadTable {
-  int32_t h[MEDUSA_MAX_K];  // ids of the used heads
-  int32_t s[MEDUSA_MAX_K];  // their s_k
-};
-
-struct TopkArgs {
-  const float* logits;  // [B][K][V]
-  int K, V, s_max, nchunk;
-  HeadTable tab;
-  float* cand_v;  // [nused][B][nchunk][S] candidate values (scratch)
-  int* cand_i;    // same layout, indices
-  int* counters;  // [nused][B] arrivals, zero on entry
-  int32_t* topk;  // [B][K][s_max]
-};
-
-// Block-wide: the S best of all threads' lists, valid in warp 0.  Consumes
-// the lists; `wv`/`wi` are [32][S] shared staging.
+// Block-wide: the S best of all threads' lists, valid in warp 0.
 template <int S>
 MDEV void block_select(TopList<S>& L, float (*wv)[S], int (*wi)[S], float* ov, int* oi) {
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, nw = blockDim.x >> 5;
@@ -226,88 +220,129 @@ MDEV void block_select(TopList<S>& L, float (*wv)[S], int (*wi)[S], float* ov, i
   }
 }
 
-// Grid (nchunk, nused, B).  Each CTA selects the top S of one contiguous
-// chunk of a head's logits; the last CTA of the head to finish merges the
-// nchunk candidate lists and writes the head's top s.
-template <int S>
-__global__ void __launch_bounds__(256) topk_kernel(const __grid_constant__ TopkArgs a) {
-  const int chunk = blockIdx.x, slot = blockIdx.y, b = blockIdx.z;
-  const int k = a.tab.h[slot], s = a.tab.s[slot];
-  const int nused = gridDim.y;
-  const float* z = a.logits + ((int64_t)b * a.K + k) * a.V;
-  const int per = (a.V + a.nchunk - 1) / a.nchunk;
-  const int v0 = chunk * per, v1 = min(a.V, v0 + per);
+// ------------------------------------------------------- W2 pass + top-s --
+template <typename TE, int NB, int S>
+__global__ void __launch_bounds__(kWarps * 32) heads_w2_topk_kernel(const __grid_constant__ HeadsArgs a) {
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int slot = blockIdx.x / a.cpc, part = blockIdx.x % a.cpc;
+  const int k = a.heads[slot];
+  const int j0 = (int)((int64_t)part * a.V / a.cpc), j1 = (int)((int64_t)(part + 1) * a.V / a.cpc);
   __shared__ float wv[32][S];
   __shared__ int wi[32][S];
   __shared__ bool last;
-  TopList<S> L;
-  L.init();
-  for (int base = v0 + threadIdx.x; base < v1; base += 4 * blockDim.x) {
-    float x[4];
+
+  const TE* x[NB];
 #pragma unroll
-    for (int u = 0; u < 4; ++u) {
-      const int v = base + u * blockDim.x;
-      x[u] = v < v1 ? z[v] : -INFINITY;
-    }
+  for (int b = 0; b < NB; ++b)
+    x[b] = static_cast<const TE*>(a.u) + ((int64_t)(b < a.B ? b : 0) * a.K + k) * a.d;
+  const TE* W = static_cast<const TE*>(a.w2) + (int64_t)k * a.V * a.d;
+  const int nvec = a.d / Vec<TE>::N;
+  for (int j = j0 + warp; j < j1; j += kWarps) {
+    float acc[NB];
 #pragma unroll
-    for (int u = 0; u < 4; ++u) {
-      const int v = base + u * blockDim.x;
-      if (v < v1) L.insert(x[u], v);
+    for (int b = 0; b < NB; ++b) acc[b] = 0.f;
+    dot_rows<TE, NB>(W + (int64_t)j * a.d, x, nvec, a.B, lane, acc);
+#pragma unroll
+    for (int b = 0; b < NB; ++b) acc[b] = warp_sum(acc[b]);
+    if (lane < a.B && lane < NB) {
+      float y = 0.f;
+#pragma unroll
+      for (int b = 0; b < NB; ++b)
+        if (b == lane) y = acc[b];
+      a.logits[((int64_t)lane * a.K + k) * a.V + j] = y;
     }
   }
-  float ov[S];
-  int oi[S];
-  block_select<S>(L, wv, wi, ov, oi);
-  const int64_t cbase = (((int64_t)slot * gridDim.z + b) * a.nchunk + chunk) * S;
-  if (threadIdx.x < 32 && threadIdx.x == 0) {
+  __syncthreads();  // this CTA's logits are written (visible to the whole CTA)
+
+  // this CTA's top S of its slice, per sequence, selected after the stream
+  for (int b = 0; b < a.B; ++b) {
+    const float* z = a.logits + ((int64_t)b * a.K + k) * a.V;
+    TopList<S> L;
+    L.init();
+    for (int j = j0 + threadIdx.x; j < j1; j += blockDim.x) L.insert(z[j], j);
+    float ov[S];
+    int oi[S];
+    block_select<S>(L, wv, wi, ov, oi);
+    if (threadIdx.x == 0) {
+      const int64_t base = (((int64_t)slot * a.B + b) * a.cpc + part) * kMaxS;
 #pragma unroll
-    for (int t = 0; t < S; ++t) { a.cand_v[cbase + t] = ov[t]; a.cand_i[cbase + t] = oi[t]; }
+      for (int t = 0; t < S; ++t) { a.cand_v[base + t] = ov[t]; a.cand_i[base + t] = oi[t]; }
+    }
+    __syncthreads();
   }
-  // the last chunk of this (head, sequence) to arrive merges all chunks
+  // the last CTA of this head to arrive merges all its CTAs' candidates
+  __syncthreads();
   if (threadIdx.x == 0) {
     __threadfence();
-    const int prev = atomicAdd(a.counters + slot * gridDim.z + b, 1);
-    last = prev == a.nchunk - 1;
+    last = atomicAdd(a.counters + slot, 1) == a.cpc - 1;
   }
   __syncthreads();
   if (!last) return;
   __threadfence();
-  const int64_t hbase = ((int64_t)slot * gridDim.z + b) * a.nchunk * S;
-  L.init();
-  for (int e = threadIdx.x; e < a.nchunk * S; e += blockDim.x)
-    L.insert(__ldcg(a.cand_v + hbase + e), __ldcg(a.cand_i + hbase + e));
-  __syncthreads();
-  block_select<S>(L, wv, wi, ov, oi);
-  if (threadIdx.x < 32) {
-    int32_t* out = a.topk + ((int64_t)b * a.K + k) * a.s_max;
-    for (int t = threadIdx.x; t < a.s_max; t += 32) {
-      int idx = -1;
-#pragma unroll
-      for (int q = 0; q < S; ++q)
-        if (q == t) idx = oi[q];
-      out[t] = (t < s && idx >= 0 && idx < a.V) ? idx : -1;
+  const int s_k = a.s[slot];
+  for (int b = 0; b < a.B; ++b) {
+    const int64_t base = ((int64_t)slot * a.B + b) * a.cpc * kMaxS;
+    TopList<S> L;
+    L.init();
+    for (int e = threadIdx.x; e < a.cpc * S; e += blockDim.x) {
+      const int c = e / S, t = e % S;
+      L.insert(__ldcg(a.cand_v + base + (int64_t)c * kMaxS + t), __ldcg(a.cand_i + base + (int64_t)c * kMaxS + t));
     }
+    float ov[S];
+    int oi[S];
+    block_select<S>(L, wv, wi, ov, oi);
+    if (warp == 0) {
+      int32_t* out = a.topk + ((int64_t)b * a.K + k) * a.s_max;
+      for (int t = lane; t < a.s_max; t += 32) {
+        int idx = -1;
+#pragma unroll
+        for (int q = 0; q < S; ++q)
+          if (q == t) idx = oi[q];
+        out[t] = (t < s_k && idx >= 0 && idx < a.V) ? idx : -1;
+      }
+    }
+    __syncthreads();
   }
-  if (threadIdx.x == 0) a.counters[slot * gridDim.z + b] = 0;  // ready for the next call
-  (void)nused;
+  if (threadIdx.x == 0) a.counters[slot] = 0;  // ready for the next call
 }
 
-int topk_chunks(int V) { return std::max(1, std::min(64, (V + 1023) / 1024)); }
+// W2 CTAs per used head: about four per SM in total, at least 8 rows each.
+int w2_ctas_per_head(int nused, int V) {
+  const int target = std::max(1, 4 * sm_count() / std::max(1, nused));
+  return std::max(1, std::min(target, (V + 7) / 8));
+}
 
 template <typename TE, int NB>
-void launch_gemv(const GemvArgs& a, bool w1, cudaStream_t s) {
-  const int blocks = std::max(1, std::min(sm_count() * 4, (int)((int64_t(a.nused) * a.rows + 7) / 8)));
-  if (w1)
-    launch_kernel(heads_gemv_kernel<TE, NB, true>, dim3(blocks), dim3(256), 0, s, a);
+int launch_heads(const HeadsArgs& a, int smax_used, cudaStream_t s) {
+  const int64_t quads = ((int64_t)a.nused * a.d + kWarps / 2 - 1) / (kWarps / 2);
+  const int g1 = (int)std::max<int64_t>(1, std::min<int64_t>(4 * sm_count(), quads));
+  launch_kernel(heads_w1_kernel<TE, NB>, dim3(g1), dim3(kWarps * 32), 0, s, a);
+  const dim3 g2(a.nused * a.cpc);
+  if (smax_used <= 8)
+    launch_kernel(heads_w2_topk_kernel<TE, NB, 8>, g2, dim3(kWarps * 32), 0, s, a);
   else
-    launch_kernel(heads_gemv_kernel<TE, NB, false>, dim3(blocks), dim3(256), 0, s, a);
+    launch_kernel(heads_w2_topk_kernel<TE, NB, 16>, g2, dim3(kWarps * 32), 0, s, a);
+  return check_launch("medusa_heads_topk");
 }
 
 template <typename TE>
-void launch_gemv_b(const GemvArgs& a, bool w1, cudaStream_t s) {
-  if (a.B == 1) launch_gemv<TE, 1>(a, w1, s);
-  else if (a.B <= 4) launch_gemv<TE, 4>(a, w1, s);
-  else launch_gemv<TE, MEDUSA_MAX_B>(a, w1, s);
+int launch_heads_b(const HeadsArgs& a, int smax_used, cudaStream_t s) {
+  if (a.B == 1) return launch_heads<TE, 1>(a, smax_used, s);
+  if (a.B <= 4) return launch_heads<TE, 4>(a, smax_used, s);
+  return launch_heads<TE, MEDUSA_MAX_B>(a, smax_used, s);
+}
+
+// Scratch: u [B][K][d] | candidate values | candidate indices | counters.
+struct Layout {
+  size_t u, cand, counters, total;
+};
+Layout heads_layout(int B, int K, int nused, int d, int V) {
+  Layout l;
+  l.u = align_up((size_t)B * K * d * sizeof(float), 256);  // fp32 size covers both element types
+  l.cand = align_up((size_t)nused * B * w2_ctas_per_head(nused, V) * kMaxS * 4, 256);
+  l.counters = align_up((size_t)MEDUSA_MAX_K * sizeof(int), 256);
+  l.total = l.u + 2 * l.cand + l.counters;
+  return l;
 }
 
 }  // namespace
@@ -316,12 +351,11 @@ void launch_gemv_b(const GemvArgs& a, bool w1, cudaStream_t s) {
 using namespace medusa;
 
 extern "C" size_t medusa_heads_topk_workspace_size(int B, int K, int d, int V, int s_max) {
-  (void)V; (void)s_max;
-  if (B < 1 || K < 1 || d < 1) return 0;
-  // u [B][K][d] (fp32 size covers both element types), top-s candidates and counters
-  const size_t u = align_up((size_t)B * K * d * sizeof(float), 256);
-  const size_t cand = align_up((size_t)K * B * topk_chunks(V) * MEDUSA_MAX_S * 4, 256);
-  return u + 2 * cand + align_up((size_t)K * B * sizeof(int), 256);
+  (void)s_max;
+  if (B < 1 || K < 1 || d < 1 || V < 1) return 0;
+  size_t best = 0;  // large enough whichever heads are in use
+  for (int n = 1; n <= K; ++n) best = std::max(best, heads_layout(B, K, n, d, V).total);
+  return best;
 }
 
 extern "C" int medusa_heads_topk(const void* hidden, const int32_t* last_node, int T, const void* w1,
@@ -337,52 +371,39 @@ extern "C" int medusa_heads_topk(const void* hidden, const int32_t* last_node, i
     return fail(MEDUSA_ERR_UNSUPPORTED, "%s: K=%d B=%d s_max=%d above the maximum", fn, K, B, s_max);
   if (dtype != MEDUSA_F32 && dtype != MEDUSA_BF16) return fail(MEDUSA_ERR_UNSUPPORTED, "%s: dtype", fn);
   const int epv = dtype == MEDUSA_BF16 ? 8 : 4;
-  if (d % epv) return fail(MEDUSA_ERR_UNSUPPORTED, "%s: d=%d not a multiple of %d", fn, d, epv);
+  if (d % (2 * epv)) return fail(MEDUSA_ERR_UNSUPPORTED, "%s: d=%d not a multiple of %d", fn, d, 2 * epv);
   if ((reinterpret_cast<uintptr_t>(hidden) | reinterpret_cast<uintptr_t>(w1) |
        reinterpret_cast<uintptr_t>(w2)) % 16)
     return fail(MEDUSA_ERR_INVALID, "%s: hidden / w1 / w2 not 16-byte aligned", fn);
   const size_t need = medusa_heads_topk_workspace_size(B, K, d, V, s_max);
   if (!workspace || workspace_bytes < need)
     return fail(MEDUSA_ERR_WORKSPACE, "%s: workspace %zu < %zu bytes", fn, workspace_bytes, need);
-  GemvArgs a{};
-  a.nused = 0;
+  if (reinterpret_cast<uintptr_t>(workspace) % 256)
+    return fail(MEDUSA_ERR_INVALID, "%s: workspace not 256-byte aligned", fn);
+  HeadsArgs a{};
   int smax_used = 0;
   for (int k = 0; k < K; ++k) {
     if (s[k] < 0 || s[k] > s_max || s[k] > V)
       return fail(MEDUSA_ERR_INVALID, "%s: s[%d]=%d outside [0, min(s_max, V)]", fn, k, s[k]);
-    if (s[k] > 0) { a.heads[a.nused++] = k; smax_used = std::max(smax_used, (int)s[k]); }
+    if (s[k] > 0) {
+      a.heads[a.nused] = k;
+      a.s[a.nused] = s[k];
+      ++a.nused;
+      smax_used = std::max(smax_used, (int)s[k]);
+    }
   }
   if (a.nused == 0) return MEDUSA_OK;
-  cudaStream_t st = as_stream(stream);
+  const Layout l = heads_layout(B, K, a.nused, d, V);
   uint8_t* ws = static_cast<uint8_t*>(workspace);
-  const size_t u_bytes = align_up((size_t)B * K * d * sizeof(float), 256);
-  const int nchunk = topk_chunks(V);
-  const size_t cand_bytes = align_up((size_t)K * B * nchunk * MEDUSA_MAX_S * 4, 256);
-  a.counters = reinterpret_cast<int*>(ws + u_bytes + 2 * cand_bytes);
-  a.ncounters = K * B;
-  a.hidden = hidden; a.last_node = last_node; a.T = T; a.B = B; a.K = K; a.d = d;
-  a.b1 = b1; a.u = ws; a.logits = head_logits; a.err = err;
-
-  // W1 + SiLU + residual
-  a.w = w1; a.rows = d;
-  if (dtype == MEDUSA_BF16) launch_gemv_b<uint16_t>(a, true, st); else launch_gemv_b<float>(a, true, st);
-  if (int rc = check_launch(fn)) return rc;
-  // W2
-  a.w = w2; a.rows = V;
-  if (dtype == MEDUSA_BF16) launch_gemv_b<uint16_t>(a, false, st); else launch_gemv_b<float>(a, false, st);
-  if (int rc = check_launch(fn)) return rc;
-  // top-s over each used head's logits (the head table travels by value)
-  TopkArgs ta{};
-  for (int i = 0; i < a.nused; ++i) { ta.tab.h[i] = a.heads[i]; ta.tab.s[i] = s[a.heads[i]]; }
-  ta.logits = head_logits; ta.K = K; ta.V = V; ta.s_max = s_max; ta.nchunk = nchunk;
-  ta.cand_v = reinterpret_cast<float*>(ws + u_bytes);
-  ta.cand_i = reinterpret_cast<int*>(ws + u_bytes + cand_bytes);
-  ta.counters = a.counters;
-  ta.topk = topk;
-  dim3 g(nchunk, a.nused, B);
-  if (smax_used <= 2) launch_kernel(topk_kernel<2>, g, dim3(256), 0, st, ta);
-  else if (smax_used <= 4) launch_kernel(topk_kernel<4>, g, dim3(256), 0, st, ta);
-  else if (smax_used <= 8) launch_kernel(topk_kernel<8>, g, dim3(256), 0, st, ta);
-  else launch_kernel(topk_kernel<16>, g, dim3(256), 0, st, ta);
-  return check_launch(fn);
+  a.w1 = w1; a.w2 = w2; a.b1 = b1; a.hidden = hidden; a.last_node = last_node;
+  a.T = T; a.B = B; a.K = K; a.d = d; a.V = V; a.s_max = s_max;
+  a.u = ws;
+  a.cand_v = reinterpret_cast<float*>(ws + l.u);
+  a.cand_i = reinterpret_cast<int*>(ws + l.u + l.cand);
+  a.counters = reinterpret_cast<int*>(ws + l.u + 2 * l.cand);
+  a.cpc = w2_ctas_per_head(a.nused, V);
+  a.logits = head_logits; a.topk = topk; a.err = err;
+  cudaStream_t st = as_stream(stream);
+  return dtype == MEDUSA_BF16 ? launch_heads_b<uint16_t>(a, smax_used, st)
+                              : launch_heads_b<float>(a, smax_used, st);
 }

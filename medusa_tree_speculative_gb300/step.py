@@ -116,6 +116,6 @@ class VerifyStep:
 
     @property
     def launches_per_step(self) -> int:
-        """Kernels one run() launches: attention 3 (2 for f32), LM head 1,
-        accept 2, compaction 1, heads 3, candidates 1."""
-        return (3 if self.w["dtype"] == "bf16" else 2) + 1 + 2 + 1 + 3 + 1
+        """Kernels one run() launches: attention 1 (2 for f32), LM head 1,
+        acceptance 2, compaction 1, heads 2, candidates 1."""
+        return (1 if self.w["dtype"] == "bf16" else 2) + 1 + 2 + 1 + 2 + 1

@@ -1,0 +1,173 @@
+"""Whole verify steps at the full sizes of the other workloads, run the way
+bench.py runs them (VerifyStep with the attention/compaction side branch):
+
+  vicuna13b_L2048_tree64_typical   d=5120, 40x128 heads, L=2048, typical
+  vicuna7b_L4096_tree64            d=4096, 32x128 heads, L=4096, 64-node tree
+  vicuna7b_L4096_dense256          same, 256-node dense tree (T=257)
+  vicuna33b_bs4_ragged             d=6656, 52x128 heads, 4 sequences with
+                                   prefixes in [512, 8192], typical
+
+Checks against the oracle on samples it computes one by one (two attention
+heads of every sequence, 256 vocabulary rows of the LM head for every tree
+row, the W1 pass in full and 256 vocabulary rows of every head), and
+properties that hold at any size: the accepted path follows the acceptance
+rule on the GPU's own logits wherever the decision is clear of rounding, the
+compacted cache holds exactly the accepted rows, the top-s are the top-s of
+the GPU's own head logits, and the next candidates are filled from them.
+"""
+import math
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from medusa_tree_speculative_gb300 import synth, workloads
+from parity_util import ancestors, as_double, both_trees, to_dev, to_host
+
+pytestmark = pytest.mark.gpu
+
+CONFIGS = ["vicuna13b_L2048_tree64_typical", "vicuna7b_L4096_tree64", "vicuna7b_L4096_dense256",
+           "vicuna33b_bs4_ragged"]
+
+
+@pytest.fixture(scope="module")
+def M():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    from medusa_tree_speculative_gb300 import build
+
+    build.build()
+    from medusa_tree_speculative_gb300 import medusa
+
+    return medusa
+
+
+def _tree_spec(w):
+    t = w["tree"]
+    return ("cartesian", t[1], t[2]) if t[0] == "cartesian" else ("greedy", w["K"], t[2], t[1])
+
+
+def _typical_decisions(logits_row, tok, tau, eps, delta):
+    """(passes, margin, threshold) of the typical rule in float64 from float32 logits."""
+    z = logits_row.astype(np.float64) / tau
+    m = z.max()
+    lse = m + np.log(np.exp(z - m).sum())
+    lp = z - lse
+    H = -(np.exp(lp) * lp).sum()
+    thr = min(eps, delta * math.exp(-H))
+    p = math.exp(lp[tok])
+    return p > thr, p - thr, thr
+
+
+@pytest.mark.parametrize("name", CONFIGS)
+def test_config_step(M, name):
+    from medusa_tree_speculative_gb300 import step
+
+    w = workloads.get(name)
+    ot, dtree = both_trees(M, _tree_spec(w))
+    T, B, H, Dh, d, V = ot.T, w["B"], w["H"], w["Dh"], w["d"], w["V"]
+    wts = synth.make_weights(w, 0)
+    x = synth.make_step(w, T, 0)
+    dev = {k: to_dev(v) for k, v in x.items()}
+    wd = {k: (None if v is None else to_dev(v)) for k, v in wts.items()}
+    L = x["prefix_len"].astype(np.int64)
+    st = step.VerifyStep(w, wd, dtree, max_prefix=int(L.max()))
+
+    # plant one path per sequence with the GPU's own LM-head argmax (setup)
+    M.medusa_lm_head_verify(dev["hidden"], st.w_lm, st.logits)
+    am = torch.argmax(st.logits, dim=-1).cpu().numpy()
+    tok = x["tokens"].copy()
+    deep = [n for n in range(T) if ot.depth[n] == min(3, ot.K)]
+    for b in range(B):
+        path = set(ancestors(ot.parent, deep[(5 * b + 1) % len(deep)]))
+        for c in range(1, T):
+            if c in path:
+                tok[b, c] = am[b, ot.parent[c]]
+    dev["tokens"] = to_dev(tok)
+    side = torch.cuda.Stream()
+    st.run(dev, torch.cuda.current_stream(), side_stream=side)
+    torch.cuda.synchronize()
+    assert int(st.err.item()) == 0
+
+    # ---- attention: two heads of every sequence against the oracle
+    out = as_double(to_host(st.out))
+    for h in (0, H - 1):
+        sl = lambda a: np.ascontiguousarray(a[..., h:h + 1, :])
+        kc, vc = sl(x["k_cache"]), sl(x["v_cache"])
+        _, ref = oracle.tree_attn(sl(x["q"]), sl(x["k_new"]), sl(x["v_new"]), kc, vc, x["seq_start"],
+                                  x["prefix_len"], ot)
+        assert np.abs(out[..., h:h + 1, :] - ref).max() <= 2e-2
+
+    # ---- LM head: 256 sampled vocabulary rows for every tree row
+    logits = to_host(st.logits).reshape(B * T, V)
+    cols = np.random.default_rng(1).choice(V, 256, replace=False)
+    ref = oracle.lm_head(np.ascontiguousarray(x["hidden"].reshape(B * T, d)),
+                         np.ascontiguousarray(wts["w_lm"][cols]))
+    assert np.abs(logits[:, cols] - ref).max() <= 2e-2 * np.abs(ref).max()
+    logits = logits.reshape(B, T, V)
+
+    # ---- acceptance: the rule on the GPU's own logits, where decisions are clear
+    mode = 1 if w["mode"] == "typical" else 0
+    tau, eps, delta = w.get("temperature", 1.0), w.get("eps", 0.09), w.get("delta", 0.3)
+    acc_len = to_host(st.accept_len)
+    acc_nodes = to_host(st.accepted_nodes)
+    best = to_host(st.best_node)
+    checked = 0
+    for b in range(B):
+        gam = np.argmax(logits[b], axis=1)
+        ok = np.zeros(T, bool)
+        clear = np.ones(T, bool)
+        ok[0] = True
+        for c in range(1, T):
+            p = ot.parent[c]
+            if mode == 0:
+                passes = tok[b, c] == gam[p]
+            else:
+                passes, margin, thr = _typical_decisions(logits[b, p], tok[b, c], tau, eps, delta)
+                clear[c] = abs(margin) > 1e-4 * thr  # float32 p-hat is far closer than this
+            ok[c] = ok[p] and passes
+        if not clear.all():
+            continue  # a decision within rounding of its threshold: skip the exact check
+        depth_best = max(ot.depth[n] for n in range(T) if ok[n])
+        assert acc_len[b] == depth_best
+        assert ok[best[b]] and ot.depth[best[b]] == depth_best
+        path = ancestors(ot.parent, int(best[b]))
+        assert list(acc_nodes[b, :len(path)]) == path and np.all(acc_nodes[b, len(path):] == -1)
+        assert int(to_host(st.next_root)[b]) == int(gam[best[b]])
+        if mode == 0:
+            assert acc_len[b] >= min(3, ot.K)  # the planted path is accepted
+        checked += 1
+    assert checked >= 1
+
+    # ---- compaction: slot L+j holds tree row a_j (V exact, K rotated)
+    vcd, kcd = to_host(dev["v_cache"]), to_host(dev["k_cache"])
+    st_b = x["seq_start"]
+    for b in range(B):
+        for j in range(acc_len[b] + 1):
+            a = acc_nodes[b, j]
+            assert np.array_equal(vcd[st_b[b] + L[b] + j], x["v_new"][b, a])
+            kref = np.stack([oracle.rope(x_h, L[b] + ot.depth[a]) for x_h in as_double(x["k_new"][b, a])])
+            kerr = np.abs(as_double(kcd[st_b[b] + L[b] + j]) - kref)
+            assert np.all(kerr <= 2.0 ** -7 * np.abs(kref) + 1e-6)
+    assert np.array_equal(to_host(dev["prefix_len"]), (L + acc_len + 1).astype(np.int32))
+
+    # ---- heads: W1 in full and 256 vocabulary rows of each head, on the best node
+    s_heads = st.s_heads
+    used = [k for k in range(w["K"]) if s_heads[k] > 0]
+    hl, tk = to_host(st.head_logits), to_host(st.topk)
+    one = np.ascontiguousarray(wts["w2"][:, :1])
+    _, _, u = oracle.heads(x["hidden"], best.astype(np.int32), wts["w1"], None, one,
+                           [1 if k in used else 0 for k in range(w["K"])], 1)
+    for b in range(B):
+        for k in used:
+            ref = oracle.lm_head(np.ascontiguousarray(u[b, k][None]), np.ascontiguousarray(wts["w2"][k][cols]))[0]
+            assert np.abs(hl[b, k, cols] - ref).max() <= 2e-2 * np.abs(ref).max()
+            order = np.lexsort((np.arange(V), -hl[b, k].astype(np.float64)))[:s_heads[k]]
+            assert list(tk[b, k, :s_heads[k]]) == list(order)
+    # ---- next candidates from the GPU's own top-s and root
+    nt = to_host(st.next_tokens)
+    for b in range(B):
+        assert nt[b, 0] == int(to_host(st.next_root)[b])
+        for n in range(1, T):
+            assert nt[b, n] == tk[b, ot.depth[n] - 1, ot.rank[n] - 1]
