@@ -250,7 +250,7 @@ def run_native(args, w, rank, world, local_rank):
                            x["prefix_len"], x["seq_cap"], st.tree, st.max_prefix, st.rope_theta, st.scale,
                            st.out, st.ws_attn, st.err, s)
         e[1].record(s)
-        M.medusa_lm_head_verify(x["hidden"], st.w_lm, st.logits, None, st.err, s)
+        M.medusa_lm_head_verify(x["hidden"], st.w_lm_run, st.logits, None, st.err, s, layout=st.w_layout)
         e[2].record(s)
         M.medusa_accept(st.logits, x["tokens"], st.tree, st.mode, st.temperature, st.eps, st.delta,
                         st.accept_len, st.accepted_nodes, st.next_root, st.best_node, st.best_logp,

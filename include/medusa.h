@@ -163,18 +163,46 @@ int medusa_tree_attn(const void* q, const void* k_new, const void* v_new,
 /* Scratch bytes medusa_lm_head_verify needs (currently 0). */
 size_t medusa_lm_head_workspace_size(int rows, int d, int V);
 
+/* Layout of the vocabulary matrix handed to medusa_lm_head_verify.
+ *   MEDUSA_W_ROWS   [V][d] row-major (nn.Linear layout).
+ *   MEDUSA_W_TILES  bf16 only: the matrix cut into tiles of 128 vocabulary
+ *                   rows x 64 columns, each tile 16 KB contiguous (row-major
+ *                   inside), tiles ordered by vocabulary block, then column
+ *                   block.  Element (v, j) sits at element offset
+ *                     ((v / 128) * (d / 64) + j / 64) * 8192
+ *                       + (v % 128) * 64 + j % 64,
+ *                   rows v >= V of the last block are zero.  Every load the
+ *                   tensor-core kernel issues is then one contiguous 16 KB
+ *                   run of HBM instead of 128 runs of 128 bytes; the decode
+ *                   step is memory-bound ([MED] "Problem"), so this is the
+ *                   layout to keep resident.  Written by medusa_lm_head_tile. */
+typedef enum { MEDUSA_W_ROWS = 0, MEDUSA_W_TILES = 1 } medusa_w_layout;
+
+/* Bytes of the MEDUSA_W_TILES copy of a bf16 [V][d] matrix:
+ * ceil(V / 128) * 128 * d * 2 (d a multiple of 64), 0 for invalid sizes. */
+size_t medusa_lm_head_tiled_bytes(int d, int V);
+
+/* Rewrite a row-major bf16 w_lm [V][d] (device) into the MEDUSA_W_TILES
+ * layout at w_tiled (device, medusa_lm_head_tiled_bytes(d, V) bytes, 16-byte
+ * aligned, must not overlap w_lm).  A one-off preparation step with no
+ * counterpart in the paper; the copy is exact.  Returns
+ * MEDUSA_ERR_UNSUPPORTED when d is not a multiple of 64. */
+int medusa_lm_head_tile(const void* w_lm, void* w_tiled, int d, int V,
+                        void* stream);
+
 /* Verification LM head over every tree row ([MED] Method 3, box step 3):
  *   logits[r][v] = sum_j hidden[r][j] * w_lm[v][j]
- * hidden: device [rows][d]; w_lm: device [V][d] (nn.Linear layout);
- * logits: device [rows][V] float32.  bf16: d must be a multiple of 64 and
- * both inputs 16-byte aligned; the tensor-core kernel's bounded on-chip
+ * hidden: device [rows][d]; w_lm: device, [V][d] in the layout w_layout
+ * names; logits: device [rows][V] float32.  bf16: d must be a multiple of 64
+ * and both inputs 16-byte aligned; both layouts give bit-identical logits.
+ * f32 accepts MEDUSA_W_ROWS only.  The tensor-core kernel's bounded on-chip
  * waits report MEDUSA_DEVERR_TIMEOUT through err (nullable) if they ever
  * give up.  Rows beyond 256 are processed in balanced chunks of at most 256
  * (the weights are streamed once per chunk). */
 int medusa_lm_head_verify(const void* hidden, const void* w_lm, float* logits,
                           int rows, int d, int V, medusa_dtype dtype,
-                          void* workspace, size_t workspace_bytes,
-                          int32_t* err, void* stream);
+                          medusa_w_layout w_layout, void* workspace,
+                          size_t workspace_bytes, int32_t* err, void* stream);
 
 /* Scratch bytes medusa_accept needs. */
 size_t medusa_accept_workspace_size(int B, int T);

@@ -48,7 +48,9 @@ _SIGS = {
     "medusa_tree_attn_workspace_size": (SZ, [I, I, I, I, I]),
     "medusa_tree_attn": (I, [P, P, P, P, P, P, P, P, TREE, I, I, I, I, F, F, I, P, P, SZ, P, P]),
     "medusa_lm_head_workspace_size": (SZ, [I, I, I]),
-    "medusa_lm_head_verify": (I, [P, P, P, I, I, I, I, P, SZ, P, P]),
+    "medusa_lm_head_tiled_bytes": (SZ, [I, I]),
+    "medusa_lm_head_tile": (I, [P, P, I, I, P]),
+    "medusa_lm_head_verify": (I, [P, P, P, I, I, I, I, I, P, SZ, P, P]),
     "medusa_accept_workspace_size": (SZ, [I, I]),
     "medusa_accept": (I, [P, P, TREE, I, I, I, F, F, F, P, P, P, P, P, P, SZ, P, P]),
     "medusa_accept_noalloc": (I, [P, P, TREE, I, I, I, F, F, F, P, P, P, P, P, P, P]),
@@ -209,13 +211,33 @@ def medusa_lm_head_workspace_size(rows, d, V) -> int:
     return int(_lib.medusa_lm_head_workspace_size(rows, d, V))
 
 
-def medusa_lm_head_verify(hidden, w_lm, logits, workspace=None, err=None, stream=None):
+W_ROWS, W_TILES = 0, 1  # medusa_w_layout
+
+
+def medusa_lm_head_tiled_bytes(d, V) -> int:
+    return int(_lib.medusa_lm_head_tiled_bytes(d, V))
+
+
+def medusa_lm_head_tile(w_lm, out=None, stream=None):
+    """The MEDUSA_W_TILES copy of a bf16 [V][d] matrix (a flat bf16 tensor)."""
+    import torch
+
+    V, d = w_lm.shape
+    n = medusa_lm_head_tiled_bytes(d, V) // 2
+    if out is None:
+        out = torch.empty(n, dtype=torch.bfloat16, device=w_lm.device)
+    _check(_lib.medusa_lm_head_tile(_ptr(w_lm), _ptr(out), d, V, _stream(stream)), "medusa_lm_head_tile")
+    return out
+
+
+def medusa_lm_head_verify(hidden, w_lm, logits, workspace=None, err=None, stream=None, layout=W_ROWS):
+    """logits [rows][V] = hidden [rows][d] @ w_lm^T; V is read from logits."""
     d = hidden.shape[-1]
     rows = hidden.numel() // d
-    V = w_lm.shape[0]
+    V = logits.shape[-1]
     nbytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
     _check(_lib.medusa_lm_head_verify(_ptr(hidden), _ptr(w_lm), _ptr(logits), rows, d, V, _dtype(hidden),
-                                      _ptr(workspace), nbytes, _ptr(err), _stream(stream)),
+                                      layout, _ptr(workspace), nbytes, _ptr(err), _stream(stream)),
            "medusa_lm_head_verify")
 
 

@@ -52,6 +52,10 @@ class VerifyStep:
         self.B, self.T = B, T
         dt = TORCH_DT[w["dtype"]]
         self.w_lm, self.w1, self.b1, self.w2 = weights["w_lm"], weights["w1"], weights.get("b1"), weights["w2"]
+        # bf16: the vocabulary matrix is kept resident in the 128 x 64 tile
+        # layout the tensor-core LM head streams fastest (written once here)
+        self.w_layout = M.W_TILES if w["dtype"] == "bf16" else M.W_ROWS
+        self.w_lm_run = M.medusa_lm_head_tile(self.w_lm) if self.w_layout == M.W_TILES else self.w_lm
         # heads that feed a tree level run; the others are skipped (s_k = 0)
         self.s_heads = [tree.s[k] if k < tree.K else 0 for k in range(K)]
         self.s_max = max(1, max(self.s_heads))
@@ -99,7 +103,8 @@ class VerifyStep:
         M.medusa_tree_attn(x["q"], x["k_new"], x["v_new"], x["k_cache"], x["v_cache"], x["seq_start"],
                            x["prefix_len"], x["seq_cap"], self.tree, self.max_prefix, self.rope_theta,
                            self.scale, self.out, self.ws_attn, self.err, side)
-        M.medusa_lm_head_verify(x["hidden"], self.w_lm, self.logits, None, self.err, main)
+        M.medusa_lm_head_verify(x["hidden"], self.w_lm_run, self.logits, None, self.err, main,
+                                layout=self.w_layout)
         M.medusa_accept(self.logits, x["tokens"], self.tree, self.mode, self.temperature, self.eps,
                         self.delta, self.accept_len, self.accepted_nodes, self.next_root, self.best_node,
                         self.best_logp, self.ws_accept, self.err, main)

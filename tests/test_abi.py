@@ -164,8 +164,16 @@ def test_validation_statuses(M):
     assert L.medusa_tree_attn(FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, ref, 17, 4, 64, 64, 1e4, 0.1,
                               1, FAKE, FAKE, 1 << 30, None, None) == -1
     # LM head: d not a multiple of 64 for bf16; misaligned pointers
-    assert L.medusa_lm_head_verify(FAKE, FAKE, FAKE, 15, 100, 1000, 1, None, 0, None, None) == -2
-    assert L.medusa_lm_head_verify(FAKE + 2, FAKE, FAKE, 15, 256, 1000, 1, None, 0, None, None) == -1
+    assert L.medusa_lm_head_verify(FAKE, FAKE, FAKE, 15, 100, 1000, 1, 0, None, 0, None, None) == -2
+    assert L.medusa_lm_head_verify(FAKE + 2, FAKE, FAKE, 15, 256, 1000, 1, 0, None, 0, None, None) == -1
+    # LM head layouts: unknown layout, tiles are bf16 only
+    assert L.medusa_lm_head_verify(FAKE, FAKE, FAKE, 15, 256, 1000, 1, 2, None, 0, None, None) == -1
+    assert L.medusa_lm_head_verify(FAKE, FAKE, FAKE, 15, 256, 1000, 0, 1, None, 0, None, None) == -2
+    # tiling: d not a multiple of 64, misaligned, overlapping source and destination
+    assert L.medusa_lm_head_tile(FAKE, FAKE + (1 << 24), 100, 1000, None) == -2
+    assert L.medusa_lm_head_tile(FAKE + 8, FAKE + (1 << 24), 256, 1000, None) == -1
+    assert L.medusa_lm_head_tile(FAKE, FAKE + 4096, 256, 1000, None) == -1
+    assert b"overlaps" in L.medusa_last_error()
     # KV compaction: Kmax above the maximum, misaligned cache
     assert L.medusa_kv_compact(FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, 1, 4, 64, 9, 1, None, None, None) == -2
     assert L.medusa_kv_compact(FAKE + 4, FAKE, FAKE, FAKE, FAKE, FAKE, 1, 4, 64, 3, 1, None, None, None) == -1
@@ -187,3 +195,6 @@ def test_workspace_queries(M):
     n = M.medusa_tree_attn_workspace_size(1, 32, 128, 65, 1024)
     assert n >= 65 * 32 * 128 * 4
     assert M.medusa_lm_head_workspace_size(65, 4096, 32000) == 0
+    assert M.medusa_lm_head_tiled_bytes(4096, 32000) == 32000 * 4096 * 2
+    assert M.medusa_lm_head_tiled_bytes(256, 1000) == 1024 * 256 * 2  # last block padded to 128 rows
+    assert M.medusa_lm_head_tiled_bytes(100, 1000) == 0

@@ -153,6 +153,41 @@ def test_lm_head(M, case):
     assert err <= TOL[dt]["logit"] * scale, f"logit error {err} vs max|logit| {scale}"
 
 
+TILE_CASES = [(256, 1000), (64, 17), (4096, 2048), (128, 40000), (4096, 32000)]
+
+
+@pytest.mark.parametrize("case", TILE_CASES, ids=lambda c: "-".join(map(str, c)))
+def test_lm_head_tiled_layout(M, case):
+    """The tile rewrite is an exact permutation (zero rows past V), and the LM
+    head reading it gives the same logits bit for bit as from row-major W."""
+    d, V = case
+    w = synth.normal(12, "w", (V, d), 1.0 / math.sqrt(d), "bf16")
+    wd = to_dev(w)
+    tiled = M.medusa_lm_head_tile(wd)
+    nt = (V + 127) // 128
+    pad = np.zeros((nt * 128, d), np.uint16)
+    pad[:V] = w
+    want = pad.reshape(nt, 128, d // 64, 64).transpose(0, 2, 1, 3).ravel()
+    got = to_host(tiled)
+    assert got.shape == want.shape and np.array_equal(got, want)
+    # element (v, j) at the documented offset, spot-checked
+    rng = np.random.default_rng(0)
+    for v, j in zip(rng.integers(0, V, 64), rng.integers(0, d, 64)):
+        off = ((v // 128) * (d // 64) + j // 64) * 8192 + (v % 128) * 64 + j % 64
+        assert got[off] == w[v, j]
+    rows = 65 if V <= 32000 else 17
+    h = to_dev(synth.normal(12, "h", (rows, d), 1.0, "bf16"))
+    a_rows = torch.empty((rows, V), dtype=torch.float32, device="cuda")
+    a_tiles = torch.full((rows, V), float("nan"), dtype=torch.float32, device="cuda")
+    M.medusa_lm_head_verify(h, wd, a_rows)
+    M.medusa_lm_head_verify(h, tiled, a_tiles, layout=M.W_TILES)
+    torch.cuda.synchronize()
+    assert torch.equal(a_rows, a_tiles)
+    if d * V <= 4096 * 2048:
+        ref = oracle.lm_head(to_host(h), w)
+        assert np.abs(to_host(a_tiles) - ref).max() <= TOL["bf16"]["logit"] * np.abs(ref).max()
+
+
 # -------------------------------------------------------------- acceptance
 
 def _accept_inputs(ot, B, V, mode, seed, plant_nodes):
