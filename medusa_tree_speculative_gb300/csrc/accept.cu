@@ -9,8 +9,10 @@
 // code", typical acceptance).  Explainer "085 | Medusa", section 二.3: a
 // rejected token ends the accepted prefix.
 //
-// Kernel 1 (one CTA per tree row): argmax of the row and, for typical
-// acceptance, the row's log-sum-exp and entropy at the given temperature.
+// Kernel 1 (one 1024-thread CTA per tree row, eight 16-byte loads in flight
+// per thread, so a 32K-wide row arrives in one round of loads): argmax of the
+// row and, for typical acceptance, the row's log-sum-exp and entropy at the
+// given temperature.
 // Kernel 2 (one CTA per sequence, one thread per node): per-node decision,
 // the accepted-prefix chain level by level, and the best node.
 #include <math.h>
@@ -47,9 +49,12 @@ __device__ __forceinline__ Soft soft_merge(Soft x, Soft y) {
   return r;
 }
 
+constexpr int kRowThreads = 1024;
+constexpr int kRowLoads = 8;  // 16-byte loads in flight per thread: 128 KB per CTA, a 32K-wide row at once
+
 template <bool TYPICAL>
-__global__ void __launch_bounds__(512) accept_rowstat_kernel(const float* logits, int T, int V,
-                                                             float inv_temp, RowStat* stats) {
+__global__ void __launch_bounds__(kRowThreads) accept_rowstat_kernel(const float* logits, int T, int V,
+                                                                     float inv_temp, RowStat* stats) {
   const int p = blockIdx.x, b = blockIdx.y;
   const float* z = logits + ((int64_t)b * T + p) * V;
   float bv = -INFINITY;
@@ -72,19 +77,18 @@ __global__ void __launch_bounds__(512) accept_rowstat_kernel(const float* logits
     }
   };
   if ((V & 3) == 0) {
-    // 16-byte loads, four in flight per thread
     const float4* z4 = reinterpret_cast<const float4*>(z);
     const int n4 = V >> 2;
-    for (int i = threadIdx.x; i < n4; i += 4 * blockDim.x) {
-      float4 r[4];
+    for (int i = threadIdx.x; i < n4; i += kRowLoads * kRowThreads) {
+      float4 r[kRowLoads];
 #pragma unroll
-      for (int u = 0; u < 4; ++u) {
-        const int ii = i + u * blockDim.x;
+      for (int u = 0; u < kRowLoads; ++u) {
+        const int ii = i + u * kRowThreads;
         if (ii < n4) r[u] = __ldg(z4 + ii);
       }
 #pragma unroll
-      for (int u = 0; u < 4; ++u) {
-        const int ii = i + u * blockDim.x;
+      for (int u = 0; u < kRowLoads; ++u) {
+        const int ii = i + u * kRowThreads;
         if (ii < n4) {
           consume(r[u].x, 4 * ii);
           consume(r[u].y, 4 * ii + 1);
@@ -94,10 +98,11 @@ __global__ void __launch_bounds__(512) accept_rowstat_kernel(const float* logits
       }
     }
   } else {
-    for (int v = threadIdx.x; v < V; v += blockDim.x) consume(z[v], v);
+    for (int v = threadIdx.x; v < V; v += kRowThreads) consume(z[v], v);
   }
-  __shared__ float sv[16], sS[16], sA[16], sm[16];
-  __shared__ int si[16];
+  constexpr int NW = kRowThreads / 32;
+  __shared__ float sv[NW], sS[NW], sA[NW], sm[NW];
+  __shared__ int si[NW];
   warp_argmax(bv, bi);
   if (TYPICAL) {
 #pragma unroll
@@ -107,15 +112,15 @@ __global__ void __launch_bounds__(512) accept_rowstat_kernel(const float* logits
       sf = soft_merge(sf, y);
     }
   }
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, nw = blockDim.x >> 5;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   if (lane == 0) { sv[warp] = bv; si[warp] = bi; sm[warp] = sf.m; sS[warp] = sf.S; sA[warp] = sf.A; }
   __syncthreads();
   if (warp == 0) {
-    bv = lane < nw ? sv[lane] : -INFINITY;
-    bi = lane < nw ? si[lane] : 0x7fffffff;
+    bv = sv[lane];
+    bi = si[lane];
     warp_argmax(bv, bi);
     if (TYPICAL) {
-      sf = lane < nw ? Soft{sm[lane], sS[lane], sA[lane]} : Soft{-INFINITY, 0.f, 0.f};
+      sf = Soft{sm[lane], sS[lane], sA[lane]};
 #pragma unroll
       for (int o = 16; o > 0; o >>= 1) {
         Soft y{__shfl_xor_sync(0xffffffffu, sf.m, o), __shfl_xor_sync(0xffffffffu, sf.S, o),
@@ -144,6 +149,8 @@ __global__ void __launch_bounds__(MEDUSA_MAX_T) accept_select_kernel(
   __shared__ uint8_t ok[MEDUSA_MAX_T];
   __shared__ float lp[MEDUSA_MAX_T];
   __shared__ int dep[MEDUSA_MAX_T];
+  __shared__ int par[MEDUSA_MAX_T];
+  __shared__ int amax[MEDUSA_MAX_T];  // each row's argmax (the next root if the row is the best node)
   // key of the best node: depth (high bits) then -node index; typical also
   // compares the summed log-probability, so it is resolved in a second pass
   __shared__ int red_key[32];
@@ -154,6 +161,7 @@ __global__ void __launch_bounds__(MEDUSA_MAX_T) accept_select_kernel(
   if (c < T) {
     depth_c = tree.depth[c];
     parent_c = tree.parent[c];
+    amax[c] = stats[(int64_t)b * T + c].argmax;
     if (c == 0) {
       pass = true;
       depth_c = 0;
@@ -177,6 +185,7 @@ __global__ void __launch_bounds__(MEDUSA_MAX_T) accept_select_kernel(
       }
     }
     dep[c] = depth_c;
+    par[c] = parent_c;
     ok[c] = c == 0 ? 1 : 0;
     lp[c] = 0.f;
   }
@@ -226,10 +235,10 @@ __global__ void __launch_bounds__(MEDUSA_MAX_T) accept_select_kernel(
     int n = bi;
     for (int j = dep[bi]; j >= 0 && n >= 0 && n < T; --j) {
       an[j] = n;
-      n = j > 0 ? tree.parent[n] : -1;
+      n = j > 0 ? par[n] : -1;
     }
     accept_len[b] = dep[bi];
-    next_root[b] = stats[(int64_t)b * T + bi].argmax;
+    next_root[b] = amax[bi];
     best_node[b] = bi;
     if (best_logp) best_logp[b] = mode == 1 ? lp[bi] : 0.f;
   }
@@ -293,9 +302,9 @@ extern "C" int medusa_accept(const float* logits, const int32_t* tokens, const m
   const float inv_temp = mode == 1 ? 1.f / temperature : 1.f;
   dim3 g(tree->T, B);
   if (mode == 1)
-    launch_kernel(accept_rowstat_kernel<true>, g, dim3(512), 0, s, logits, tree->T, V, inv_temp, stats);
+    launch_kernel(accept_rowstat_kernel<true>, g, dim3(kRowThreads), 0, s, logits, tree->T, V, inv_temp, stats);
   else
-    launch_kernel(accept_rowstat_kernel<false>, g, dim3(512), 0, s, logits, tree->T, V, inv_temp, stats);
+    launch_kernel(accept_rowstat_kernel<false>, g, dim3(kRowThreads), 0, s, logits, tree->T, V, inv_temp, stats);
   if (int rc = check_launch(fn)) return rc;
   const int threads = (tree->T + 31) / 32 * 32;
   launch_kernel(accept_select_kernel, dim3(B), dim3(threads), 0, s, logits, tokens, *tree, V, mode, inv_temp, eps,
