@@ -7,20 +7,25 @@
 // depth.  Explainer "085 | Medusa", section 二.2: siblings must stay invisible.
 //
 // bf16: one kernel.  A thread-block cluster of CL CTAs serves one (sequence,
-// head, block of query rows).  The sequence's L + T keys (L cached prefix
-// keys, then the T tree keys) are cut into CL contiguous ranges, one per CTA
-// (flash-decoding split).  Each CTA
-//   * rotates its query rows at pos = L + depth and folds in scale * log2(e),
-//   * streams its key range through double-buffered shared tiles: prefix keys
-//     by cp.async from the cache; tree keys rotated from k_new on the fly and,
+// head, block of query rows).  Each CTA takes a balanced share of the L
+// cached prefix keys and a balanced share of the tree keys (flash-decoding
+// split; tree keys cost more, so every CTA gets a few).  Each CTA
+//   * issues the cp.async copies of its first prefix tile and the loads of
+//     its query rows before building the cos/sin tables at pos = L + depth,
+//   * rotates its query rows and folds in scale * log2(e),
+//   * streams its keys through double-buffered shared tiles: prefix keys by
+//     cp.async from the cache; tree keys rotated from k_new on the fly and,
 //     by the CTAs of the last row block, appended to the cache at slot L + i,
 //   * applies the ancestor bitmask to tree keys, runs QK^T and PV on tensor
-//     cores (bf16 in, fp32 accumulate) with the online softmax in registers,
-//   * leaves its partial (max, sum, unnormalised O) in its shared memory.
-// After a cluster barrier each CTA merges a share of the rows by reading the
-// CL partials through distributed shared memory and writes the output; a
-// second barrier keeps every CTA's shared memory alive until all reads end.
-// No scratch memory, no inter-kernel combine pass.
+//     cores (bf16 in, fp32 accumulate) over the 16-key blocks that hold keys,
+//     with the online softmax in registers,
+//   * pushes its partial (max, sum, unnormalised O) for each query row into
+//     the shared memory of the CTA that owns the row (rows are dealt round
+//     robin), reusing its query buffer, which every CTA has released at an
+//     early split cluster barrier.
+// After one blocking cluster barrier each CTA merges its own rows from local
+// shared memory and writes the output.  No scratch memory, no inter-kernel
+// combine pass.
 //
 // f32: rope_append (RoPE + KV append, q' staged in scratch) and a plain
 // CUDA-core kernel, one CTA per (row, head, sequence).
@@ -67,9 +72,20 @@ void row_split(int T, int& rowblocks, int& warps) {
   warps = (rows + 15) / 16;
 }
 
+// Query rows are dealt to the cluster's CTAs round robin for the merge.
+__host__ __device__ constexpr int rows_per_owner(int nrows) { return (nrows + CL - 1) / CL; }
+
+// Bytes of the region that first holds the rotated query rows (bf16) and
+// later the partials pushed by the cluster's CTAs (fp32 O and (max, sum)).
+__host__ __device__ constexpr int qrecv_bytes(int Dh, int warps) {
+  const int q = warps * 16 * Dh * 2;
+  const int r = CL * rows_per_owner(warps * 16) * (Dh + 2) * 4;
+  return q > r ? q : r;
+}
+
 size_t smem_bytes(int Dh, int warps, int K) {
   return (size_t)2 * 2 * KT * Dh * 2            // K and V tiles, double-buffered, bf16
-         + (size_t)warps * 16 * Dh * 2          // rotated query rows, bf16
+         + (size_t)qrecv_bytes(Dh, warps)       // query rows, then the pushed partials
          + (size_t)2 * (K + 1) * (Dh / 2) * 4;  // cos / sin per tree depth
 }
 
@@ -122,10 +138,10 @@ MDEV uint32_t map_to_rank(uint32_t local_smem_addr, uint32_t rank) {
   asm volatile("mapa.shared::cluster.u32 %0, %1, %2;\n" : "=r"(r) : "r"(local_smem_addr), "r"(rank));
   return r;
 }
-MDEV float2 ld_cluster_f32x2(uint32_t addr) {
-  float2 v;
-  asm volatile("ld.shared::cluster.v2.f32 {%0, %1}, [%2];\n" : "=f"(v.x), "=f"(v.y) : "r"(addr) : "memory");
-  return v;
+MDEV void cluster_arrive() { asm volatile("barrier.cluster.arrive.release.aligned;\n" ::: "memory"); }
+MDEV void cluster_wait() { asm volatile("barrier.cluster.wait.acquire.aligned;\n" ::: "memory"); }
+MDEV void st_cluster_f32x2(uint32_t addr, float x, float y) {
+  asm volatile("st.shared::cluster.v2.f32 [%0], {%1, %2};\n" ::"r"(addr), "f"(x), "f"(y) : "memory");
 }
 
 // ---------------------------------------------------------------------------
@@ -134,19 +150,21 @@ MDEV float2 ld_cluster_f32x2(uint32_t addr) {
 template <int DH>
 __global__ void __cluster_dims__(CL, 1, 1) __launch_bounds__(MAX_WARPS * 32, 2)
     attn_tree_kernel(const __grid_constant__ AttnArgs a) {
-  constexpr int CH = DH / 8;  // 16-byte chunks per row
+  constexpr int CH = DH / 8;    // 16-byte chunks per row
   constexpr int HALF = DH / 2;
-  constexpr int HCH = CH / 2;  // chunks per rotary half
+  constexpr int HCH = CH / 2;   // chunks per rotary half
+  constexpr int QI = HCH / 2;   // query items per thread: rows * HCH / (rows * 2)
   extern __shared__ __align__(128) uint8_t smem[];
   uint16_t* kbuf = reinterpret_cast<uint16_t*>(smem);  // [2][KT][DH]
   uint16_t* vbuf = kbuf + 2 * KT * DH;                // [2][KT][DH]
-  uint16_t* qbuf = vbuf + 2 * KT * DH;                // [rows][DH]
+  uint8_t* qrecv = reinterpret_cast<uint8_t*>(vbuf + 2 * KT * DH);
+  uint16_t* qbuf = reinterpret_cast<uint16_t*>(qrecv);  // [rows][DH] until the q fragments are loaded
   const int nrows = a.warps * 16;
-  float* cs = reinterpret_cast<float*>(qbuf + nrows * DH);  // [K+1][HALF]
+  const int RPO = rows_per_owner(nrows);
+  float* recv_o = reinterpret_cast<float*>(qrecv);             // then [CL][RPO][DH]
+  float* recv_ml = recv_o + CL * RPO * DH;                     //      [CL][RPO][2]
+  float* cs = reinterpret_cast<float*>(qrecv + qrecv_bytes(DH, a.warps));  // [K+1][HALF]
   float* sn = cs + (a.K + 1) * HALF;
-  // after the key loop: this CTA's partial, over the K/V tiles and q rows
-  float* part_o = reinterpret_cast<float*>(smem);   // [rows][DH]
-  float* part_ml = reinterpret_cast<float*>(qbuf);  // [rows][2]
 
   const uint32_t crank = cluster_ctarank();
   const int h = blockIdx.y, b = blockIdx.z / a.rowblocks, rb = blockIdx.z % a.rowblocks;
@@ -159,13 +177,15 @@ __global__ void __cluster_dims__(CL, 1, 1) __launch_bounds__(MAX_WARPS * 32, 2)
   int64_t st;
   const bool ok = seq_ok(a, b, L, st);
   if (!ok && crank == 0 && h == 0 && rb == 0 && tid == 0) set_err(a.err, MEDUSA_DEVERR_CAPACITY);
-  // this CTA's key range (every CTA reaches both cluster barriers below)
-  const int nkeys = ok ? L + a.T : 0;
-  const int per = ((nkeys + CL - 1) / CL + 15) / 16 * 16;
-  const int k_begin = min(nkeys, (int)crank * per);
-  const int k_end = min(nkeys, k_begin + per);
-  const int last_row = min(a.T, row0 + nrows) - 1;  // tree keys past it are no one's ancestor here
-  const int k_stop = min(k_end, L + last_row + 1);
+  // this CTA's keys: a balanced share of the prefix, then a balanced share of
+  // the tree keys that rows of this block can see (all T in the last block,
+  // whose CTAs also append them); every CTA reaches both cluster barriers
+  const int last_row = min(a.T, row0 + nrows) - 1;
+  const int Lk = ok ? L : 0, ntree = ok ? last_row + 1 : 0;
+  const int p0 = (int)((int64_t)crank * Lk / CL), p1 = (int)((int64_t)(crank + 1) * Lk / CL);
+  const int t0 = (int)crank * ntree / CL, t1 = ((int)crank + 1) * ntree / CL;
+  const int np = p1 - p0, nv = np + (t1 - t0);
+  const int ntiles = (nv + KT - 1) / KT;
 
   const uint16_t* kcache = static_cast<const uint16_t*>(a.k_cache);
   const uint16_t* vcache = static_cast<const uint16_t*>(a.v_cache);
@@ -174,35 +194,29 @@ __global__ void __cluster_dims__(CL, 1, 1) __launch_bounds__(MAX_WARPS * 32, 2)
   const uint16_t* knew = static_cast<const uint16_t*>(a.k_new);
   const uint16_t* vnew = static_cast<const uint16_t*>(a.v_new);
 
-  // ---- cos/sin at positions L + d for every tree depth d
-  if (ok) {
-    for (int e = tid; e < (a.K + 1) * HALF; e += nthr) {
-      const int d = e / HALF, j = e % HALF;
-      const float ang = __fmul_rn((float)(L + d), a.inv_freq[j]);
-      float s, c;
-      sincosf(ang, &s, &c);
-      cs[e] = c;
-      sn[e] = s;
-    }
-  }
-  __syncthreads();
-
-  // ---- tile loader: prefix keys by cp.async, tree keys rotated here
-  auto load_tile = [&](int kt, int buf) {
-    for (int e = tid; e < KT * HCH; e += nthr) {
+  // ---- tile loader over this CTA's key list: v < np prefix key p0 + v (by
+  // cp.async), np <= v < nv tree node t0 + v - np (rotated here), other rows
+  // of the 16-key blocks in use are zero.  Pass 0 issues the prefix copies
+  // only; pass 1 the rest; pass 2 everything.
+  auto load_tile = [&](int v0, int buf, int pass) {
+    const int rows = min(KT, (nv - v0 + 15) / 16 * 16);
+    for (int e = tid; e < rows * HCH; e += nthr) {
       const int rr = e / HCH, c = e % HCH;
-      const int j = kt + rr;
+      const int v = v0 + rr;
       uint16_t* kd = kbuf + (buf * KT + rr) * DH;
       uint16_t* vd = vbuf + (buf * KT + rr) * DH;
       const int s1 = (c ^ (rr & 7)) * 8, s2 = ((c + HCH) ^ (rr & 7)) * 8;
-      if (j < k_stop && j < L) {
-        const int64_t off = (st + j) * HD + (int64_t)h * DH;
+      if (v < np) {
+        if (pass == 1) continue;
+        const int64_t off = (st + p0 + v) * HD + (int64_t)h * DH;
         cp_async16(smem_u32(kd + s1), kcache + off + c * 8, 16);
         cp_async16(smem_u32(kd + s2), kcache + off + (c + HCH) * 8, 16);
         cp_async16(smem_u32(vd + s1), vcache + off + c * 8, 16);
         cp_async16(smem_u32(vd + s2), vcache + off + (c + HCH) * 8, 16);
-      } else if (j < k_stop) {
-        const int n = j - L;  // tree node
+      } else if (pass == 0) {
+        continue;
+      } else if (v < nv) {
+        const int n = t0 + v - np;  // tree node
         const int64_t src = (((int64_t)b * a.T + n) * a.H + h) * DH;
         const int d = min(max(__ldg(a.depth + n), 0), a.K);
         uint4 klo, khi;
@@ -213,7 +227,7 @@ __global__ void __cluster_dims__(CL, 1, 1) __launch_bounds__(MAX_WARPS * 32, 2)
         *reinterpret_cast<uint4*>(kd + s2) = khi;
         *reinterpret_cast<uint4*>(vd + s1) = vlo;
         *reinterpret_cast<uint4*>(vd + s2) = vhi;
-        if (rb == a.rowblocks - 1) {  // the last row block loads every tree key: append K', V at L + n
+        if (rb == a.rowblocks - 1) {  // the last row block holds every tree key: append K', V at L + n
           const int64_t dst = (st + L + n) * HD + (int64_t)h * DH;
           *reinterpret_cast<uint4*>(kcache_w + dst + c * 8) = klo;
           *reinterpret_cast<uint4*>(kcache_w + dst + (c + HCH) * 8) = khi;
@@ -230,25 +244,49 @@ __global__ void __cluster_dims__(CL, 1, 1) __launch_bounds__(MAX_WARPS * 32, 2)
     }
   };
 
-  const int ntiles = k_begin < k_stop ? (k_stop - k_begin + KT - 1) / KT : 0;
-  if (ntiles > 0) load_tile(k_begin, 0);
+  // ---- first the long-latency work: tile 0's prefix copies, the query loads
+  if (ntiles > 0) load_tile(0, 0, 0);
   cp_async_commit();
-
-  // ---- query rows: rotate at L + depth, scale, round to bf16
   const uint16_t* q = static_cast<const uint16_t*>(a.q);
-  for (int e = tid; e < nrows * HCH; e += nthr) {
-    const int rr = e / HCH, c = e % HCH;
-    const int r = row0 + rr;
-    uint4 lo = make_uint4(0, 0, 0, 0), hi = lo;
+  uint4 qlo[QI], qhi[QI];
+  int qd[QI];
+#pragma unroll
+  for (int i = 0; i < QI; ++i) {
+    const int e = tid + i * nthr;  // < nrows * HCH
+    const int r = row0 + e / HCH, c = e % HCH;
+    qlo[i] = qhi[i] = make_uint4(0, 0, 0, 0);
+    qd[i] = 0;
     if (ok && r < a.T) {
       const int64_t src = (((int64_t)b * a.T + r) * a.H + h) * DH;
-      const int d = min(max(__ldg(a.depth + r), 0), a.K);
-      rope8(ldg_v4(q + src + c * 8), ldg_v4(q + src + (c + HCH) * 8), cs + d * HALF + c * 8,
-            sn + d * HALF + c * 8, a.qscale, lo, hi);
+      qlo[i] = ldg_v4(q + src + c * 8);
+      qhi[i] = ldg_v4(q + src + (c + HCH) * 8);
+      qd[i] = min(max(__ldg(a.depth + r), 0), a.K);
     }
+  }
+  // ---- cos/sin at positions L + d for every tree depth d
+  if (ok) {
+    for (int e = tid; e < (a.K + 1) * HALF; e += nthr) {
+      const int d = e / HALF, j = e % HALF;
+      const float ang = __fmul_rn((float)(L + d), a.inv_freq[j]);
+      float s, c;
+      sincosf(ang, &s, &c);
+      cs[e] = c;
+      sn[e] = s;
+    }
+  }
+  __syncthreads();
+  // ---- query rows: rotate at L + depth, scale, round to bf16
+#pragma unroll
+  for (int i = 0; i < QI; ++i) {
+    const int e = tid + i * nthr;
+    const int rr = e / HCH, c = e % HCH;
+    uint4 lo = qlo[i], hi = qhi[i];
+    if (ok && row0 + rr < a.T)
+      rope8(qlo[i], qhi[i], cs + qd[i] * HALF + c * 8, sn + qd[i] * HALF + c * 8, a.qscale, lo, hi);
     *reinterpret_cast<uint4*>(qbuf + rr * DH + ((c ^ (rr & 7)) * 8)) = lo;
     *reinterpret_cast<uint4*>(qbuf + rr * DH + (((c + HCH) ^ (rr & 7)) * 8)) = hi;
   }
+  if (ntiles > 0) load_tile(0, 0, 1);  // tree keys and zero rows of tile 0 (needs the tables)
   __syncthreads();
   uint32_t qf[DH / 16][4];
   {
@@ -259,6 +297,10 @@ __global__ void __cluster_dims__(CL, 1, 1) __launch_bounds__(MAX_WARPS * 32, 2)
       ldmatrix_x4(qf[kk], smem_u32(qbuf + rr * DH + ((c ^ (rr & 7)) * 8)));
     }
   }
+  // the query buffer becomes the landing area of the pushed partials: no CTA
+  // pushes before every CTA of the cluster has arrived here
+  __syncthreads();
+  cluster_arrive();
 
   const int ra = row0 + warp * 16 + (lane >> 2);  // this thread's two rows
   const int rbw = ra + 8;
@@ -268,10 +310,10 @@ __global__ void __cluster_dims__(CL, 1, 1) __launch_bounds__(MAX_WARPS * 32, 2)
   for (int n = 0; n < DH / 8; ++n) o[n][0] = o[n][1] = o[n][2] = o[n][3] = 0.f;
 
   for (int t = 0; t < ntiles; ++t) {
-    const int kt = k_begin + t * KT;
+    const int v0 = t * KT;
     const int buf = t & 1;
     if (t + 1 < ntiles) {
-      load_tile(kt + KT, buf ^ 1);
+      load_tile(v0 + KT, buf ^ 1, 2);
       cp_async_commit();
       cp_async_wait<1>();
     } else {
@@ -280,6 +322,7 @@ __global__ void __cluster_dims__(CL, 1, 1) __launch_bounds__(MAX_WARPS * 32, 2)
     __syncthreads();
     const uint16_t* kb = kbuf + buf * KT * DH;
     const uint16_t* vb = vbuf + buf * KT * DH;
+    const int nb = min(KT / 16, (nv - v0 + 15) / 16);  // 16-key blocks holding keys
 
     // S = q' K^T  (16 rows x 64 keys per warp)
     float s[KT / 8][4];
@@ -288,24 +331,26 @@ __global__ void __cluster_dims__(CL, 1, 1) __launch_bounds__(MAX_WARPS * 32, 2)
 #pragma unroll
     for (int kk = 0; kk < DH / 16; ++kk) {
 #pragma unroll
-      for (int np = 0; np < KT / 16; ++np) {
-        const int rr = np * 16 + (lane & 7) + ((lane >> 4) << 3);
-        const int c = kk * 2 + ((lane >> 3) & 1);
-        uint32_t r[4];
-        ldmatrix_x4(r, smem_u32(kb + rr * DH + ((c ^ (rr & 7)) * 8)));
-        mma_bf16_16816(s[2 * np], qf[kk], r[0], r[1]);
-        mma_bf16_16816(s[2 * np + 1], qf[kk], r[2], r[3]);
+      for (int np16 = 0; np16 < KT / 16; ++np16) {
+        if (np16 < nb) {
+          const int rr = np16 * 16 + (lane & 7) + ((lane >> 4) << 3);
+          const int c = kk * 2 + ((lane >> 3) & 1);
+          uint32_t r[4];
+          ldmatrix_x4(r, smem_u32(kb + rr * DH + ((c ^ (rr & 7)) * 8)));
+          mma_bf16_16816(s[2 * np16], qf[kk], r[0], r[1]);
+          mma_bf16_16816(s[2 * np16 + 1], qf[kk], r[2], r[3]);
+        }
       }
     }
-    // mask: keys past this CTA's range; ancestor bits on tree keys
-    if (kt + KT > k_stop || kt + KT > L) {
+    // mask: past this CTA's keys; ancestor bits on tree keys
+    if (v0 + KT > np) {
 #pragma unroll
       for (int n = 0; n < KT / 8; ++n) {
 #pragma unroll
         for (int e = 0; e < 4; ++e) {
-          const int j = kt + n * 8 + (lane & 3) * 2 + (e & 1);
+          const int v = v0 + n * 8 + (lane & 3) * 2 + (e & 1);
           const int r = e < 2 ? ra : rbw;
-          if (j >= k_stop || !key_visible(a, L, r, j)) s[n][e] = -INFINITY;
+          if (v >= nv || (v >= np && !key_visible(a, L, r, L + t0 + v - np))) s[n][e] = -INFINITY;
         }
       }
     }
@@ -346,51 +391,56 @@ __global__ void __cluster_dims__(CL, 1, 1) __launch_bounds__(MAX_WARPS * 32, 2)
     // O += P V
 #pragma unroll
     for (int j = 0; j < KT / 16; ++j) {
+      if (j < nb) {
 #pragma unroll
-      for (int dp = 0; dp < DH / 16; ++dp) {
-        const int rr = j * 16 + (lane & 15);
-        const int c = dp * 2 + (lane >> 4);
-        uint32_t r[4];
-        ldmatrix_x4_trans(r, smem_u32(vb + rr * DH + ((c ^ (rr & 7)) * 8)));
-        mma_bf16_16816(o[2 * dp], pf[j], r[0], r[1]);
-        mma_bf16_16816(o[2 * dp + 1], pf[j], r[2], r[3]);
+        for (int dp = 0; dp < DH / 16; ++dp) {
+          const int rr = j * 16 + (lane & 15);
+          const int c = dp * 2 + (lane >> 4);
+          uint32_t r[4];
+          ldmatrix_x4_trans(r, smem_u32(vb + rr * DH + ((c ^ (rr & 7)) * 8)));
+          mma_bf16_16816(o[2 * dp], pf[j], r[0], r[1]);
+          mma_bf16_16816(o[2 * dp + 1], pf[j], r[2], r[3]);
+        }
       }
     }
     __syncthreads();
   }
   cp_async_wait<0>();
-  __syncthreads();
   l_a += __shfl_xor_sync(0xffffffffu, l_a, 1);
   l_a += __shfl_xor_sync(0xffffffffu, l_a, 2);
   l_b += __shfl_xor_sync(0xffffffffu, l_b, 1);
   l_b += __shfl_xor_sync(0xffffffffu, l_b, 2);
 
-  // ---- this CTA's partial into its own shared memory (rows local to the block)
+  // ---- push this CTA's partial of each local row to the row's owner
+  // (rank rr % CL, slot rr / CL): every CTA has released its query buffer
+  cluster_wait();
   const int la = warp * 16 + (lane >> 2), lb = la + 8;
+  const uint32_t o_base = smem_u32(recv_o), ml_base = smem_u32(recv_ml);
+  {
+    const uint32_t ra_o = map_to_rank(o_base + (((int)crank * RPO + la / CL) * DH) * 4, (uint32_t)(la % CL));
+    const uint32_t rb_o = map_to_rank(o_base + (((int)crank * RPO + lb / CL) * DH) * 4, (uint32_t)(lb % CL));
 #pragma unroll
-  for (int n = 0; n < DH / 8; ++n) {
-    const int col = n * 8 + (lane & 3) * 2;
-    *reinterpret_cast<float2*>(part_o + la * DH + col) = make_float2(o[n][0], o[n][1]);
-    *reinterpret_cast<float2*>(part_o + lb * DH + col) = make_float2(o[n][2], o[n][3]);
+    for (int n = 0; n < DH / 8; ++n) {
+      const int col = n * 8 + (lane & 3) * 2;
+      st_cluster_f32x2(ra_o + col * 4, o[n][0], o[n][1]);
+      st_cluster_f32x2(rb_o + col * 4, o[n][2], o[n][3]);
+    }
+    if ((lane & 3) == 0) {
+      st_cluster_f32x2(map_to_rank(ml_base + (((int)crank * RPO + la / CL) * 2) * 4, (uint32_t)(la % CL)), m_a, l_a);
+      st_cluster_f32x2(map_to_rank(ml_base + (((int)crank * RPO + lb / CL) * 2) * 4, (uint32_t)(lb % CL)), m_b, l_b);
+    }
   }
-  if ((lane & 3) == 0) {
-    *reinterpret_cast<float2*>(part_ml + la * 2) = make_float2(m_a, l_a);
-    *reinterpret_cast<float2*>(part_ml + lb * 2) = make_float2(m_b, l_b);
-  }
-  cluster_sync();
+  cluster_sync();  // every partial has landed; nothing remote is touched after this
 
-  // ---- merge: this CTA takes local rows crank, crank + CL, ...
-  __shared__ float wgt[(MAX_WARPS * 16 + CL - 1) / CL][CL];  // per (row, rank): weight / denominator
-  const uint32_t ml_local = smem_u32(part_ml), o_local = smem_u32(part_o);
+  // ---- merge this CTA's rows (local rows crank, crank + CL, ...) from local shared memory
+  __shared__ float wgt[(MAX_WARPS * 16 + CL - 1) / CL][CL];  // per (row, source rank): weight / denominator
   const int my_rows = ok ? (nrows - (int)crank + CL - 1) / CL : 0;
   for (int i = tid; i < my_rows; i += nthr) {
-    const int rr = (int)crank + i * CL;
     float m[CL], l[CL], M = -INFINITY;
 #pragma unroll
     for (int c = 0; c < CL; ++c) {
-      const float2 v = ld_cluster_f32x2(map_to_rank(ml_local + rr * 8, c));
-      m[c] = v.x;
-      l[c] = v.y;
+      m[c] = recv_ml[(c * RPO + i) * 2];
+      l[c] = recv_ml[(c * RPO + i) * 2 + 1];
       M = fmaxf(M, m[c]);
     }
     float den = 0.f, w[CL];
@@ -406,22 +456,20 @@ __global__ void __cluster_dims__(CL, 1, 1) __launch_bounds__(MAX_WARPS * 32, 2)
   uint16_t* out = static_cast<uint16_t*>(a.out);
   for (int e = tid; e < my_rows * (DH / 2); e += nthr) {
     const int i = e / (DH / 2), d = (e % (DH / 2)) * 2;
-    const int rr = (int)crank + i * CL;
-    const int r = row0 + rr;
+    const int r = row0 + (int)crank + i * CL;
     if (r >= a.T) continue;
     float2 acc = make_float2(0.f, 0.f);
 #pragma unroll
     for (int c = 0; c < CL; ++c) {
       const float wc = wgt[i][c];
       if (wc != 0.f) {
-        const float2 v = ld_cluster_f32x2(map_to_rank(o_local + (rr * DH + d) * 4, c));
+        const float2 v = *reinterpret_cast<const float2*>(recv_o + (c * RPO + i) * DH + d);
         acc.x += wc * v.x;
         acc.y += wc * v.y;
       }
     }
     *reinterpret_cast<uint32_t*>(out + (((int64_t)b * a.T + r) * a.H + h) * DH + d) = pack2_bf16(acc.x, acc.y);
   }
-  cluster_sync();  // keep this CTA's partial alive until every rank has read it
 }
 
 // ---------------------------------------------------------------------------
