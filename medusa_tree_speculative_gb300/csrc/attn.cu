@@ -186,6 +186,20 @@ __global__ void __cluster_dims__(CL, 1, 1) __launch_bounds__(MAX_WARPS * 32, 2)
   const int t0 = (int)crank * ntree / CL, t1 = ((int)crank + 1) * ntree / CL;
   const int np = p1 - p0, nv = np + (t1 - t0);
   const int ntiles = (nv + KT - 1) / KT;
+  // ancestor bits of this CTA's tree keys (nodes t0 .. t0 + 63) for this
+  // thread's two query rows, loaded once
+  const int ra = row0 + (tid >> 5) * 16 + ((tid & 31) >> 2);
+  const int rbw = ra + 8;
+  auto vis_bits = [&](int r) -> uint64_t {
+    if (!ok || r >= a.T || t1 <= t0) return 0;
+    const uint32_t* row = a.anc + (int64_t)r * a.W;
+    const int w0 = t0 >> 5, sh = t0 & 31;
+    const uint64_t lo = __ldg(row + w0);
+    const uint64_t mid = w0 + 1 < a.W ? __ldg(row + w0 + 1) : 0;
+    const uint64_t hi = w0 + 2 < a.W ? __ldg(row + w0 + 2) : 0;
+    return ((lo | (mid << 32)) >> sh) | (sh ? hi << (64 - sh) : 0);
+  };
+  const uint64_t vis_a = vis_bits(ra), vis_b = vis_bits(rbw);
 
   const uint16_t* kcache = static_cast<const uint16_t*>(a.k_cache);
   const uint16_t* vcache = static_cast<const uint16_t*>(a.v_cache);
@@ -302,8 +316,6 @@ __global__ void __cluster_dims__(CL, 1, 1) __launch_bounds__(MAX_WARPS * 32, 2)
   __syncthreads();
   cluster_arrive();
 
-  const int ra = row0 + warp * 16 + (lane >> 2);  // this thread's two rows
-  const int rbw = ra + 8;
   float m_a = -INFINITY, m_b = -INFINITY, l_a = 0.f, l_b = 0.f;
   float o[DH / 8][4];
 #pragma unroll
@@ -350,7 +362,8 @@ __global__ void __cluster_dims__(CL, 1, 1) __launch_bounds__(MAX_WARPS * 32, 2)
         for (int e = 0; e < 4; ++e) {
           const int v = v0 + n * 8 + (lane & 3) * 2 + (e & 1);
           const int r = e < 2 ? ra : rbw;
-          if (v >= nv || (v >= np && !key_visible(a, L, r, L + t0 + v - np))) s[n][e] = -INFINITY;
+          const uint64_t vis = e < 2 ? vis_a : vis_b;
+          if (v >= nv || (v >= np && !((vis >> (v - np)) & 1ull))) s[n][e] = -INFINITY;
         }
       }
     }
@@ -416,18 +429,21 @@ __global__ void __cluster_dims__(CL, 1, 1) __launch_bounds__(MAX_WARPS * 32, 2)
   cluster_wait();
   const int la = warp * 16 + (lane >> 2), lb = la + 8;
   const uint32_t o_base = smem_u32(recv_o), ml_base = smem_u32(recv_ml);
-  {
+  if (row0 + la < a.T) {
     const uint32_t ra_o = map_to_rank(o_base + (((int)crank * RPO + la / CL) * DH) * 4, (uint32_t)(la % CL));
     const uint32_t rb_o = map_to_rank(o_base + (((int)crank * RPO + lb / CL) * DH) * 4, (uint32_t)(lb % CL));
+    const bool push_b = row0 + lb < a.T;
 #pragma unroll
     for (int n = 0; n < DH / 8; ++n) {
       const int col = n * 8 + (lane & 3) * 2;
       st_cluster_f32x2(ra_o + col * 4, o[n][0], o[n][1]);
-      st_cluster_f32x2(rb_o + col * 4, o[n][2], o[n][3]);
+      if (push_b) st_cluster_f32x2(rb_o + col * 4, o[n][2], o[n][3]);
     }
     if ((lane & 3) == 0) {
       st_cluster_f32x2(map_to_rank(ml_base + (((int)crank * RPO + la / CL) * 2) * 4, (uint32_t)(la % CL)), m_a, l_a);
-      st_cluster_f32x2(map_to_rank(ml_base + (((int)crank * RPO + lb / CL) * 2) * 4, (uint32_t)(lb % CL)), m_b, l_b);
+      if (push_b)
+        st_cluster_f32x2(map_to_rank(ml_base + (((int)crank * RPO + lb / CL) * 2) * 4, (uint32_t)(lb % CL)), m_b,
+                         l_b);
     }
   }
   cluster_sync();  // every partial has landed; nothing remote is touched after this
