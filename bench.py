@@ -48,6 +48,9 @@ def parse_args():
     ap.add_argument("--plant-depth", type=int, default=3)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--heads", choices=["split", "fused"], default="fused",
+                    help="heads' W1 over every tree row beside the acceptance, then W2 on the accepted "
+                         "row (split), or both projections on the accepted row after it (fused)")
     ap.add_argument("--attn-branch", choices=["serial", "fork"], default="fork",
                     help="tree attention before the LM head on one stream, or on a forked graph branch")
     return ap.parse_args()
@@ -55,7 +58,7 @@ def parse_args():
 
 # ------------------------------------------------------------------ bytes --
 
-def algorithmic_bytes(w: dict, T: int, s_heads, L_list) -> dict:
+def algorithmic_bytes(w: dict, T: int, s_heads, L_list, split: bool) -> dict:
     """Bytes each call must move at least once per step (weights once, KV
     prefix once, activations and logits once each way)."""
     e = 2 if w["dtype"] == "bf16" else 4
@@ -70,9 +73,16 @@ def algorithmic_bytes(w: dict, T: int, s_heads, L_list) -> dict:
     accept = B * T * V * 4
     compact = 2 * 2 * B * (w["K"] + 1) * H * Dh * e
     heads = k_used * (d * d + V * d) * e + B * k_used * V * 4 * 2
+    # split heads: W1 over every tree row (u of all rows written), then W2 on the accepted row
+    heads_hidden = k_used * d * d * e + B * T * d * e + B * T * k_used * d * e
+    heads_w2 = k_used * V * d * e + B * k_used * d * e + B * k_used * V * 4 * 2
     cand = B * T * 4
     out = dict(tree_attn=attn, lm_head_verify=lm, accept=accept, kv_compact=compact,
-               heads_topk=heads, build_candidates=cand)
+               build_candidates=cand)
+    if split:
+        out.update(heads_hidden=heads_hidden, heads_logits_topk=heads_w2)
+    else:
+        out["heads_topk"] = heads
     out["step"] = sum(out.values())
     return out
 
@@ -82,7 +92,9 @@ def algorithmic_flops(w, T, s_heads, L_list):
     k_used = sum(1 for s in s_heads if s > 0)
     return dict(tree_attn=4 * T * (int(np.sum(L_list)) + T) * H * Dh,
                 lm_head_verify=2 * B * T * d * V,
-                heads_topk=2 * B * k_used * (d * d + d * V))
+                heads_topk=2 * B * k_used * (d * d + d * V),
+                heads_hidden=2 * B * T * k_used * d * d,
+                heads_logits_topk=2 * B * k_used * d * V)
 
 
 def load_peaks():
@@ -190,6 +202,36 @@ def plant(w, tree, st, x, depth, torch):
     x["tokens"].copy_(torch.from_numpy(tok))
 
 
+def step_calls(st, x, s):
+    """The step's library calls in stream order on one stream, as (name, call)."""
+    from medusa_tree_speculative_gb300 import medusa as M
+
+    c = [("tree_attn", lambda: M.medusa_tree_attn(
+            x["q"], x["k_new"], x["v_new"], x["k_cache"], x["v_cache"], x["seq_start"], x["prefix_len"],
+            x["seq_cap"], st.tree, st.max_prefix, st.rope_theta, st.scale, st.out, st.ws_attn, st.err, s)),
+         ("lm_head_verify", lambda: M.medusa_lm_head_verify(x["hidden"], st.w_lm_run, st.logits, None, st.err, s,
+                                                            layout=st.w_layout))]
+    if st.heads == "split":
+        c.append(("heads_hidden", lambda: M.medusa_heads_hidden(x["hidden"], st.w1_run, st.b1, st.s_heads, st.u_all,
+                                                                st.err, s, layout=st.w1_layout)))
+    c += [("accept", lambda: M.medusa_accept(st.logits, x["tokens"], st.tree, st.mode, st.temperature, st.eps,
+                                             st.delta, st.accept_len, st.accepted_nodes, st.next_root,
+                                             st.best_node, st.best_logp, st.ws_accept, st.err, s)),
+          ("kv_compact", lambda: M.medusa_kv_compact(x["k_cache"], x["v_cache"], x["seq_start"], x["prefix_len"],
+                                                     st.accepted_nodes, st.accept_len, st.tree.K, st.src_slots,
+                                                     st.err, s))]
+    if st.heads == "split":
+        c.append(("heads_logits_topk", lambda: M.medusa_heads_logits_topk(
+            st.u_all, st.T, st.best_node, st.w2, st.s_heads, st.head_logits, st.topk, st.ws_w2, st.err, s)))
+    else:
+        c.append(("heads_topk", lambda: M.medusa_heads_topk(x["hidden"], st.best_node, st.w1, st.b1, st.w2,
+                                                            st.s_heads, st.head_logits, st.topk, st.ws_heads,
+                                                            st.err, s)))
+    c.append(("build_candidates", lambda: M.medusa_build_candidates(st.next_root, st.topk, st.tree,
+                                                                    st.next_tokens, s)))
+    return c
+
+
 def run_native(args, w, rank, world, local_rank):
     import torch
     import torch.distributed as dist
@@ -212,7 +254,7 @@ def run_native(args, w, rank, world, local_rank):
     for k, v in xh.items():
         x[k] = step.host_to_torch(v, dt).to(dev) if v.dtype in (np.uint16, np.float32) else torch.from_numpy(v).to(dev)
     L_list = xh["prefix_len"].copy()
-    st = step.VerifyStep(w, wd, tree, max_prefix=int(L_list.max()), device=dev)
+    st = step.VerifyStep(w, wd, tree, max_prefix=int(L_list.max()), device=dev, heads=args.heads)
     plant(w, tree, st, x, args.plant_depth, torch)
     prefix0 = x["prefix_len"].clone()
     s = torch.cuda.Stream(device=dev)
@@ -227,8 +269,9 @@ def run_native(args, w, rank, world, local_rank):
     accept_len = st.accept_len.cpu().numpy().tolist()
 
     # one graph holds K steps with timing events at every call boundary
-    calls = ["tree_attn", "lm_head_verify", "accept", "kv_compact", "heads_topk", "build_candidates"]
+    calls = [c for c, _ in step_calls(st, x, s)]
     s2 = torch.cuda.Stream(device=dev) if args.attn_branch == "fork" else None  # side branch for attention
+    s3 = torch.cuda.Stream(device=dev) if args.heads == "split" else None  # branch for W1 beside the acceptance
 
     def capture(nsteps, with_events):
         g = torch.cuda.CUDAGraph()
@@ -241,29 +284,14 @@ def run_native(args, w, rank, world, local_rank):
                     evs.append(e)
                     run_calls(st, x, s, e)
                 else:
-                    st.run(x, s, side_stream=s2)
+                    st.run(x, s, side_stream=s2, heads_stream=s3)
         return g, evs
 
     def run_calls(st, x, s, e):
-        e[0].record(s)
-        M.medusa_tree_attn(x["q"], x["k_new"], x["v_new"], x["k_cache"], x["v_cache"], x["seq_start"],
-                           x["prefix_len"], x["seq_cap"], st.tree, st.max_prefix, st.rope_theta, st.scale,
-                           st.out, st.ws_attn, st.err, s)
-        e[1].record(s)
-        M.medusa_lm_head_verify(x["hidden"], st.w_lm_run, st.logits, None, st.err, s, layout=st.w_layout)
-        e[2].record(s)
-        M.medusa_accept(st.logits, x["tokens"], st.tree, st.mode, st.temperature, st.eps, st.delta,
-                        st.accept_len, st.accepted_nodes, st.next_root, st.best_node, st.best_logp,
-                        st.ws_accept, st.err, s)
-        e[3].record(s)
-        M.medusa_kv_compact(x["k_cache"], x["v_cache"], x["seq_start"], x["prefix_len"], st.accepted_nodes,
-                            st.accept_len, st.tree.K, st.src_slots, st.err, s)
-        e[4].record(s)
-        M.medusa_heads_topk(x["hidden"], st.best_node, st.w1, st.b1, st.w2, st.s_heads, st.head_logits,
-                            st.topk, st.ws_heads, st.err, s)
-        e[5].record(s)
-        M.medusa_build_candidates(st.next_root, st.topk, st.tree, st.next_tokens, s)
-        e[6].record(s)
+        for i, (_, call) in enumerate(step_calls(st, x, s)):
+            e[i].record(s)
+            call()
+        e[-1].record(s)
 
     g_warm, _ = capture(1, False)
     g_timed, evs = capture(args.steps, True)
@@ -305,14 +333,14 @@ def run_native(args, w, rank, world, local_rank):
 
     e2e = None
     if not args.no_e2e:
-        e2e = measure_e2e(args, w, st, x, xh, prefix0, s, s2, torch, M)
+        e2e = measure_e2e(args, w, st, x, xh, prefix0, s, s2, s3, torch, M)
 
     return dict(ms_step=ms_step, ms_events_step=ms_events / args.steps, per_call_ms=per_call, clocks=clocks,
                 T=T, s_heads=st.s_heads, L_list=L_list, accept_len=accept_len, e2e=e2e,
                 launches=st.launches_per_step * args.steps, tree=ht)
 
 
-def measure_e2e(args, w, st, x, xh, prefix0, s, s2, torch, M):
+def measure_e2e(args, w, st, x, xh, prefix0, s, s2, s3, torch, M):
     """Same metric through the public C-ABI calls with host buffers: per step,
     pinned host inputs -> device, the six calls, results -> pinned host."""
     names_in = ["q", "k_new", "v_new", "hidden", "tokens"]
@@ -329,7 +357,7 @@ def measure_e2e(args, w, st, x, xh, prefix0, s, s2, torch, M):
             for k in names_in:
                 x[k].copy_(host_in[k], non_blocking=True)
             x["prefix_len"].copy_(host_pl, non_blocking=True)
-            st.run(x, s, side_stream=s2)
+            st.run(x, s, side_stream=s2, heads_stream=s3)
             for h, d in zip(host_out, outs):
                 h.copy_(d, non_blocking=True)
         s.synchronize()
@@ -504,12 +532,13 @@ def main():
     if rank != 0:
         return
     peaks = load_peaks()
-    by = algorithmic_bytes(w, r["T"], r["s_heads"], r["L_list"])
+    by = algorithmic_bytes(w, r["T"], r["s_heads"], r["L_list"], args.heads == "split")
     fl = algorithmic_flops(w, r["T"], r["s_heads"], r["L_list"])
     ms = r["ms_step"]
     value = world * 1e3 / ms
     step_gbs = by["step"] / (ms * 1e-3) / 1e9
-    dom = max(("heads_topk", "lm_head_verify", "tree_attn"), key=lambda c: r["per_call_ms"][c])
+    dom = max((c for c in ("heads_topk", "heads_logits_topk", "lm_head_verify", "tree_attn")
+               if c in r["per_call_ms"]), key=lambda c: r["per_call_ms"][c])
     dom_ms = r["per_call_ms"][dom]
     achieved = by[dom] / (dom_ms * 1e-3) / 1e9
     traffic = ncu_traffic(dom)

@@ -15,6 +15,8 @@
  *   medusa_accept           greedy / typical acceptance          (box 4-5)
  *   medusa_kv_compact       accepted path's KV into place        (box 6)
  *   medusa_heads_topk       K Medusa heads + top-s               (box 1)
+ *     (or: medusa_heads_hidden over every tree row, which can run beside the
+ *      acceptance, then medusa_heads_logits_topk on the accepted row)
  *   medusa_build_candidates next step's candidate tokens         (box 2)
  *
  * Conventions
@@ -184,9 +186,10 @@ size_t medusa_lm_head_tiled_bytes(int d, int V);
 
 /* Rewrite a row-major bf16 w_lm [V][d] (device) into the MEDUSA_W_TILES
  * layout at w_tiled (device, medusa_lm_head_tiled_bytes(d, V) bytes, 16-byte
- * aligned, must not overlap w_lm).  A one-off preparation step with no
- * counterpart in the paper; the copy is exact.  Returns
- * MEDUSA_ERR_UNSUPPORTED when d is not a multiple of 64. */
+ * aligned, must not overlap w_lm).  Any row-major [R][d] matrix can be tiled
+ * the same way (the heads' W1 as [K*d][d] for medusa_heads_hidden).  A
+ * one-off preparation step with no counterpart in the paper; the copy is
+ * exact.  Returns MEDUSA_ERR_UNSUPPORTED when d is not a multiple of 64. */
 int medusa_lm_head_tile(const void* w_lm, void* w_tiled, int d, int V,
                         void* stream);
 
@@ -296,6 +299,46 @@ int medusa_heads_topk(const void* hidden, const int32_t* last_node, int T,
                       medusa_dtype dtype, float* head_logits, int32_t* topk,
                       int s_max, void* workspace, size_t workspace_bytes,
                       int32_t* err, void* stream);
+
+/* The heads' first projection for every tree row ([MED] Method 1, computed
+ * ahead of the acceptance):
+ *   u[r][k] = dtype( SiLU(W1_k hidden[r] + b1_k) + hidden[r] )
+ * for every row r < rows and every head k with s[k] > 0 (entries of other
+ * heads are not written).  Running it over all rows, not only the accepted
+ * node's, costs no extra weight bytes (W1 is read once either way: a GEMM
+ * on the tensor cores instead of a GEMV) and no longer depends on the
+ * acceptance, so it can overlap it; medusa_heads_logits_topk then reads the
+ * accepted node's row.  hidden: device [rows][d]; w1: device [K][d][d]
+ * (out x in) in w1_layout (MEDUSA_W_TILES: medusa_lm_head_tile of w1 seen as
+ * a [K*d][d] matrix); b1: device [K][d] or NULL; s: host [K]; u: device
+ * [rows][K][d] of dtype.  bf16: d a multiple of 128, 16-byte aligned
+ * tensors, bounded on-chip waits as medusa_lm_head_verify; f32: rows
+ * layout only.  Rows beyond 256 run in chunks of at most 256 (W1 is read
+ * once per chunk). */
+int medusa_heads_hidden(const void* hidden, int rows, const void* w1,
+                        medusa_w_layout w1_layout, const void* b1,
+                        const int32_t* s, int K, int d, medusa_dtype dtype,
+                        void* u, int32_t* err, void* stream);
+
+/* Scratch bytes medusa_heads_logits_topk needs. */
+size_t medusa_heads_logits_topk_workspace_size(int B, int K, int V, int s_max);
+
+/* The heads' second projection and top-s ([MED] Method 1 and 2) from
+ * medusa_heads_hidden's output: for each sequence b and head k with s[k] > 0,
+ *   head_logits[b][k] = W2_k u[b * T + node[b]][k]   (float32)
+ *   topk[b][k][..] as medusa_heads_topk.
+ * u: device [B*T][K][d]; node: device [B] (usually medusa_accept's
+ * best_node; outside [0, T) raises MEDUSA_DEVERR_NODE and reads row 0); w2,
+ * s, head_logits, topk as medusa_heads_topk.  The workspace holds per-head
+ * arrival counters that must be zero on entry: zero it once (cudaMemset)
+ * before the first call; every call leaves it zeroed again (after a call
+ * that reported MEDUSA_DEVERR_TIMEOUT, zero it again). */
+int medusa_heads_logits_topk(const void* u, int T, const int32_t* node,
+                             const void* w2, const int32_t* s, int K, int B,
+                             int d, int V, medusa_dtype dtype,
+                             float* head_logits, int32_t* topk, int s_max,
+                             void* workspace, size_t workspace_bytes,
+                             int32_t* err, void* stream);
 
 /* Candidate fill for the next step ([MED] box steps 1-2):
  *   tokens[b][0] = next_root[b];

@@ -45,7 +45,8 @@ struct HeadsArgs {
   int nused;
   int32_t heads[MEDUSA_MAX_K];  // ids of the heads with s_k > 0
   int32_t s[MEDUSA_MAX_K];      // their s_k
-  void* u;                      // [B][K][d] element type (scratch)
+  void* u;                      // [B][K][d] element type (scratch), or [B*T][K][d] when u_node is set
+  const int32_t* u_node;        // u rows per sequence: row b * T + u_node[b] of u (null: row b)
   float* logits;                // [B][K][V]
   int32_t* topk;                // [B][K][s_max]
   float* cand_v;                // [nused][B][cpc][kMaxS] per-CTA candidates (scratch)
@@ -233,8 +234,19 @@ __global__ void __launch_bounds__(kWarps * 32) heads_w2_topk_kernel(const __grid
 
   const TE* x[NB];
 #pragma unroll
-  for (int b = 0; b < NB; ++b)
-    x[b] = static_cast<const TE*>(a.u) + ((int64_t)(b < a.B ? b : 0) * a.K + k) * a.d;
+  for (int b = 0; b < NB; ++b) {
+    const int bb = b < a.B ? b : 0;
+    int64_t row = bb;
+    if (a.u_node) {  // an out-of-range node reads row 0 of the sequence and raises the error bit
+      int n = a.u_node[bb];
+      if (n < 0 || n >= a.T) {
+        if (threadIdx.x == 0 && blockIdx.x == 0) set_err(a.err, MEDUSA_DEVERR_NODE);
+        n = 0;
+      }
+      row = (int64_t)bb * a.T + n;
+    }
+    x[b] = static_cast<const TE*>(a.u) + (row * a.K + k) * a.d;
+  }
   const TE* W = static_cast<const TE*>(a.w2) + (int64_t)k * a.V * a.d;
   const int nvec = a.d / Vec<TE>::N;
   for (int j = j0 + warp; j < j1; j += kWarps) {
@@ -325,6 +337,24 @@ int launch_heads(const HeadsArgs& a, int smax_used, cudaStream_t s) {
   return check_launch("medusa_heads_topk");
 }
 
+// W2 pass + top-s alone (u computed elsewhere, counters zero on entry).
+template <typename TE, int NB>
+int launch_w2(const HeadsArgs& a, int smax_used, cudaStream_t s, const char* fn) {
+  const dim3 g2(a.nused * a.cpc);
+  if (smax_used <= 8)
+    launch_kernel(heads_w2_topk_kernel<TE, NB, 8>, g2, dim3(kWarps * 32), 0, s, a);
+  else
+    launch_kernel(heads_w2_topk_kernel<TE, NB, 16>, g2, dim3(kWarps * 32), 0, s, a);
+  return check_launch(fn);
+}
+
+template <typename TE>
+int launch_w2_b(const HeadsArgs& a, int smax_used, cudaStream_t s, const char* fn) {
+  if (a.B == 1) return launch_w2<TE, 1>(a, smax_used, s, fn);
+  if (a.B <= 4) return launch_w2<TE, 4>(a, smax_used, s, fn);
+  return launch_w2<TE, MEDUSA_MAX_B>(a, smax_used, s, fn);
+}
+
 template <typename TE>
 int launch_heads_b(const HeadsArgs& a, int smax_used, cudaStream_t s) {
   if (a.B == 1) return launch_heads<TE, 1>(a, smax_used, s);
@@ -406,4 +436,62 @@ extern "C" int medusa_heads_topk(const void* hidden, const int32_t* last_node, i
   cudaStream_t st = as_stream(stream);
   return dtype == MEDUSA_BF16 ? launch_heads_b<uint16_t>(a, smax_used, st)
                               : launch_heads_b<float>(a, smax_used, st);
+}
+
+extern "C" size_t medusa_heads_logits_topk_workspace_size(int B, int K, int V, int s_max) {
+  (void)s_max;
+  if (B < 1 || K < 1 || V < 1) return 0;
+  size_t best = 0;  // large enough whichever heads are in use
+  for (int n = 1; n <= K; ++n) {
+    const Layout l = heads_layout(B, K, n, 1, V);
+    best = std::max(best, 2 * l.cand + l.counters);
+  }
+  return best;
+}
+
+extern "C" int medusa_heads_logits_topk(const void* u, int T, const int32_t* node, const void* w2,
+                                        const int32_t* s, int K, int B, int d, int V, medusa_dtype dtype,
+                                        float* head_logits, int32_t* topk, int s_max, void* workspace,
+                                        size_t workspace_bytes, int32_t* err, void* stream) {
+  const char* fn = "medusa_heads_logits_topk";
+  if (!u || !node || !w2 || !s || !head_logits || !topk) return fail(MEDUSA_ERR_INVALID, "%s: NULL tensor", fn);
+  if (T < 1 || K < 1 || B < 1 || d < 1 || V < 1 || s_max < 1)
+    return fail(MEDUSA_ERR_INVALID, "%s: T=%d K=%d B=%d d=%d V=%d s_max=%d", fn, T, K, B, d, V, s_max);
+  if (K > MEDUSA_MAX_K || B > MEDUSA_MAX_B || s_max > MEDUSA_MAX_S)
+    return fail(MEDUSA_ERR_UNSUPPORTED, "%s: K=%d B=%d s_max=%d above the maximum", fn, K, B, s_max);
+  if (dtype != MEDUSA_F32 && dtype != MEDUSA_BF16) return fail(MEDUSA_ERR_UNSUPPORTED, "%s: dtype", fn);
+  const int epv = dtype == MEDUSA_BF16 ? 8 : 4;
+  if (d % epv) return fail(MEDUSA_ERR_UNSUPPORTED, "%s: d=%d not a multiple of %d", fn, d, epv);
+  if ((reinterpret_cast<uintptr_t>(u) | reinterpret_cast<uintptr_t>(w2)) % 16)
+    return fail(MEDUSA_ERR_INVALID, "%s: u / w2 not 16-byte aligned", fn);
+  const size_t need = medusa_heads_logits_topk_workspace_size(B, K, V, s_max);
+  if (!workspace || workspace_bytes < need)
+    return fail(MEDUSA_ERR_WORKSPACE, "%s: workspace %zu < %zu bytes", fn, workspace_bytes, need);
+  if (reinterpret_cast<uintptr_t>(workspace) % 256)
+    return fail(MEDUSA_ERR_INVALID, "%s: workspace not 256-byte aligned", fn);
+  HeadsArgs a{};
+  int smax_used = 0;
+  for (int k = 0; k < K; ++k) {
+    if (s[k] < 0 || s[k] > s_max || s[k] > V)
+      return fail(MEDUSA_ERR_INVALID, "%s: s[%d]=%d outside [0, min(s_max, V)]", fn, k, s[k]);
+    if (s[k] > 0) {
+      a.heads[a.nused] = k;
+      a.s[a.nused] = s[k];
+      ++a.nused;
+      smax_used = std::max(smax_used, (int)s[k]);
+    }
+  }
+  if (a.nused == 0) return MEDUSA_OK;
+  const Layout l = heads_layout(B, K, a.nused, 1, V);
+  uint8_t* ws = static_cast<uint8_t*>(workspace);
+  a.w2 = w2; a.u = const_cast<void*>(u); a.u_node = node;
+  a.T = T; a.B = B; a.K = K; a.d = d; a.V = V; a.s_max = s_max;
+  a.cand_v = reinterpret_cast<float*>(ws);
+  a.cand_i = reinterpret_cast<int*>(ws + l.cand);
+  a.counters = reinterpret_cast<int*>(ws + 2 * l.cand);
+  a.cpc = w2_ctas_per_head(a.nused, V);
+  a.logits = head_logits; a.topk = topk; a.err = err;
+  cudaStream_t st = as_stream(stream);
+  return dtype == MEDUSA_BF16 ? launch_w2_b<uint16_t>(a, smax_used, st, fn)
+                              : launch_w2_b<float>(a, smax_used, st, fn);
 }

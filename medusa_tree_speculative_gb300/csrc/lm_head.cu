@@ -30,7 +30,12 @@
 // is one contiguous 16 KB run, which keeps HBM pages open and measured about
 // 9% faster for the 32000 x 4096 matrix.  Every mbarrier wait is bounded; a timeout sets
 // MEDUSA_DEVERR_TIMEOUT and the kernel winds down.
-// f32: a plain CUDA-core kernel (one warp per output element).
+// The same kernel, with a second epilogue, computes the Medusa heads' first
+// projection for every tree row (medusa_heads_hidden; Method 1, "heads over
+// all rows"): M runs over the stacked W1 rows of the heads in use and each
+// accumulator becomes u = bf16(SiLU(acc + b1) + h); the residual values are
+// staged in shared memory by the idle epilogue warps during the main loop.
+// f32: plain CUDA-core kernels (one warp per output element).
 #include <cuda.h>
 
 #include <algorithm>
@@ -61,9 +66,32 @@ struct LmArgs {
   int ngroups;  // work items along the vocabulary = ceil(tiles / nt)
   int stages;
   uint32_t tmem_cols;
-  int tiled;    // W in the 128 x 64 tile layout (each box one contiguous 16 KB run)
+  int tiled;      // W in the 128 x 64 tile layout (each box one contiguous 16 KB run)
+  int ntiles;     // valid 128-row tiles along M
+  int oob_block;  // a weight block index past the tensor (its loads read zeros)
+  // epilogue: mode 0 stores fp32 logits [rows][V]; mode 1 is the Medusa-head
+  // projection u[r][k][j] = bf16(SiLU(acc + b1[k][j]) + hidden[r][j]) for the
+  // stacked rows of the used heads (M = nused * d)
+  int mode;
+  const uint16_t* hidden;
+  const uint16_t* b1;
+  uint16_t* u;
+  int K;                        // heads in u's layout
+  int tpr;                      // 128-row tiles per head (d / 128)
+  int32_t heads[MEDUSA_MAX_K];  // slot -> head id
   int32_t* err;
 };
+
+struct HeadSlots {
+  int32_t id[MEDUSA_MAX_K];
+};
+
+// Weight block (128 rows) that M-tile `tile` reads.
+MDEV int weight_block(const LmArgs& a, int tile) {
+  if (tile >= a.ntiles) return a.oob_block;
+  if (a.mode == 0) return tile;
+  return a.heads[tile / a.tpr] * a.tpr + tile % a.tpr;
+}
 
 MDEV bool wait_or_abort(uint64_t* bar, uint32_t parity, volatile int* abort_flag) {
   for (uint32_t i = 0; i < kSpinLimit; ++i) {
@@ -87,6 +115,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint64_t* tfull = empty + a.stages;
   uint64_t* tempty = tfull + 2;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(tempty + 2);
+  // mode 1: the residual tile hidden[r0 + i][j] of the current item, [nt][npad][128] bf16
+  uint16_t* res = reinterpret_cast<uint16_t*>(smem + (size_t)a.stages * stage_bytes + 1024);
   __shared__ int s_abort;
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -128,17 +158,19 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int item = i0; item < i1 && ok; ++item) {
         const int v0 = (item / a.nchunks) * a.nt * BM;
         const int r0 = (item % a.nchunks) * a.npad;
+        int blk[2];  // weight blocks of the item's tiles (rows past V, a missing second tile, read zeros)
+        for (int t = 0; t < a.nt; ++t) blk[t] = weight_block(a, v0 / BM + t);
         for (int kb = 0; kb < nkb; ++kb, ++it) {
           const int s = it % a.stages;
           const uint32_t ph = (uint32_t)(it / a.stages) & 1u;
           if (!wait_or_abort(&empty[s], ph ^ 1u, abort_flag)) { ok = false; break; }
           uint8_t* st = smem + (size_t)s * stage_bytes;
           mbar_expect_tx(&full[s], stage_bytes);
-          for (int t = 0; t < a.nt; ++t) {  // rows past V (a missing second tile) read as zeros
+          for (int t = 0; t < a.nt; ++t) {
             if (a.tiled)
-              tma_load_2d(st + t * (BM * BK * 2), &tmW, &full[s], 0, ((v0 / BM + t) * nkb + kb) * BM);
+              tma_load_2d(st + t * (BM * BK * 2), &tmW, &full[s], 0, (blk[t] * nkb + kb) * BM);
             else
-              tma_load_2d(st + t * (BM * BK * 2), &tmW, &full[s], kb * BK, v0 + t * BM);
+              tma_load_2d(st + t * (BM * BK * 2), &tmW, &full[s], kb * BK, blk[t] * BM);
           }
           tma_load_2d(st + a_bytes, &tmH, &full[s], kb * BK, r0);
         }
@@ -188,6 +220,27 @@ __global__ void __launch_bounds__(kThreads, 1)
   } else {
     // ---------------- epilogue: TMEM -> registers -> logits
     const int g = warp & 3;  // this warp may read TMEM lanes 32g .. 32g+31
+    // mode 1: the residual values this thread will need, staged in shared
+    // memory while the main loop runs (loads issued after the weight stream
+    // has saturated HBM would each wait out the loaded latency)
+    auto load_res = [&](int item) {
+      const int r0 = (item % a.nchunks) * a.npad;
+      for (int t = 0; t < a.nt; ++t) {
+        const int v = (item / a.nchunks) * a.nt * BM + t * BM + 32 * g + lane;
+        const int j = v % a.d;
+        for (int i0 = 0; i0 < a.npad; i0 += 16) {  // 16 loads in flight, then 16 stores
+          uint16_t hv[16];
+#pragma unroll
+          for (int i = 0; i < 16; ++i) {
+            const int row = r0 + i0 + i;
+            hv[i] = (v < a.V && row < a.rows) ? __ldg(a.hidden + (int64_t)row * a.d + j) : (uint16_t)0;
+          }
+#pragma unroll
+          for (int i = 0; i < 16; ++i) res[(t * a.npad + i0 + i) * BM + 32 * g + lane] = hv[i];
+        }
+      }
+    };
+    if (a.mode == 1 && i0 < i1) load_res(i0);
     int local = 0;
     for (int item = i0; item < i1; ++item, ++local) {
       const int acc = local & 1;
@@ -209,16 +262,35 @@ __global__ void __launch_bounds__(kThreads, 1)
                              r);
           tmem_ld_wait();
           if (v < a.V) {
+            if (a.mode == 0) {
 #pragma unroll
-            for (int i = 0; i < 16; ++i) {
-              const int row = r0 + c * 16 + i;
-              if (row < a.rows) a.logits[(int64_t)row * a.V + v] = __uint_as_float(r[i]);
+              for (int i = 0; i < 16; ++i) {
+                const int row = r0 + c * 16 + i;
+                if (row < a.rows) a.logits[(int64_t)row * a.V + v] = __uint_as_float(r[i]);
+              }
+            } else {
+              const int slot = v / a.d, j = v % a.d, k = a.heads[slot];
+              const float bias = a.b1 ? bf16_bits_to_f32(__ldg(a.b1 + (int64_t)k * a.d + j)) : 0.f;
+#pragma unroll
+              for (int i = 0; i < 16; ++i) {
+                const int row = r0 + c * 16 + i;
+                if (row < a.rows) {
+                  const float y = __uint_as_float(r[i]) + bias;
+                  const float silu = y / (1.f + expf(-y));
+                  const float h = bf16_bits_to_f32(res[(t * a.npad + c * 16 + i) * BM + 32 * g + lane]);
+                  a.u[((int64_t)row * a.K + k) * a.d + j] = f32_to_bf16_bits(silu + h);
+                }
+              }
             }
           }
         }
       }
       tc_fence_before();
       mbar_arrive(&tempty[acc]);
+      if (a.mode == 1 && item + 1 < i1) {
+        __syncwarp();
+        load_res(item + 1);  // this warp's own slice of the tile: no other warp reads it
+      }
     }
   }
   tc_fence_before();
@@ -330,6 +402,69 @@ extern "C" int medusa_lm_head_tile(const void* w_lm, void* w_tiled, int d, int V
   return check_launch(fn);
 }
 
+namespace medusa {
+namespace {
+
+// Plan and launch the tensor-core GEMM: `a` carries the epilogue fields; the
+// weight tensor has `wrows` rows of d (row-major) or is its tile copy.
+int launch_tc(LmArgs& a, const void* w, bool tiled, int64_t wrows, const void* hidden, int rows, int d,
+              cudaStream_t s, const char* fn) {
+  a.rows = rows; a.d = d; a.tiled = tiled;
+  a.nchunks = (rows + kMaxN - 1) / kMaxN;
+  a.npad = ((rows + a.nchunks - 1) / a.nchunks + 15) / 16 * 16;
+  // two tiles per work item halve the hidden re-reads per weight byte; used
+  // while both accumulators of both tiles fit in TMEM
+  a.nt = (a.npad <= 128 && a.ntiles > sm_count()) ? 2 : 1;
+  a.ngroups = (a.ntiles + a.nt - 1) / a.nt;
+  const size_t stage_bytes = (size_t)a.nt * BM * BK * 2 + (size_t)a.npad * BK * 2;
+  const size_t res_bytes = a.mode == 1 ? (size_t)a.nt * a.npad * BM * 2 : 0;
+  a.stages = (int)std::min<size_t>(8, (kSmemBudget - 1024 - 256 - res_bytes) / stage_bytes);
+  uint32_t cols = 32;
+  while (cols < (uint32_t)(2 * a.nt * a.npad)) cols <<= 1;
+  a.tmem_cols = cols;
+  const int64_t wblocks = (wrows + BM - 1) / BM;
+  a.oob_block = (int)wblocks;
+  CUtensorMap tmW, tmH;
+  // tiled: a [blocks * (d / 64) * 128][64] matrix whose 128-row boxes are the tiles
+  const bool okw = tiled ? make_map(&tmW, w, (uint64_t)BK, (uint64_t)wblocks * BM * (d / BK), BM)
+                         : make_map(&tmW, w, (uint64_t)d, (uint64_t)wrows, BM);
+  if (!okw || !make_map(&tmH, hidden, (uint64_t)d, (uint64_t)rows, (uint32_t)a.npad))
+    return fail(MEDUSA_ERR_CUDA, "%s: cuTensorMapEncodeTiled failed", fn);
+  const size_t smem = 1024 + (size_t)a.stages * stage_bytes + 1024 + res_bytes;  // ring | barriers | residuals
+  cudaFuncSetAttribute(lm_head_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  // balanced: every CTA gets ceil or floor of items / grid work items
+  const int items = a.ngroups * a.nchunks;
+  const int per_cta = (items + sm_count() - 1) / sm_count();
+  const int grid = (items + per_cta - 1) / per_cta;
+  launch_kernel(lm_head_tc_kernel, dim3(grid), dim3(kThreads), smem, s, tmW, tmH, a);
+  return check_launch(fn);
+}
+
+// f32 heads projection: one warp per (row, used head, output j).
+__global__ void __launch_bounds__(256) heads_hidden_f32_kernel(const float* hidden, const float* w1, const float* b1,
+                                                               float* u, int rows, int d, int K, int nused,
+                                                               HeadSlots hs) {
+  const int64_t g = (int64_t)blockIdx.x * 8 + (threadIdx.x >> 5);
+  const int lane = threadIdx.x & 31;
+  if (g >= (int64_t)rows * nused * d) return;
+  const int j = (int)(g % d);
+  const int slot = (int)((g / d) % nused);
+  const int r = (int)(g / ((int64_t)d * nused));
+  const int k = hs.id[slot];
+  const float* h = hidden + (int64_t)r * d;
+  const float* wr = w1 + ((int64_t)k * d + j) * d;
+  float acc = 0.f;
+  for (int i = lane; i < d; i += 32) acc += h[i] * wr[i];
+  acc = warp_sum(acc);
+  if (lane == 0) {
+    const float y = acc + (b1 ? b1[(int64_t)k * d + j] : 0.f);
+    u[((int64_t)r * K + k) * d + j] = y / (1.f + expf(-y)) + h[j];
+  }
+}
+
+}  // namespace
+}  // namespace medusa
+
 extern "C" int medusa_lm_head_verify(const void* hidden, const void* w_lm, float* logits, int rows, int d,
                                      int V, medusa_dtype dtype, medusa_w_layout w_layout, void* workspace,
                                      size_t workspace_bytes, int32_t* err, void* stream) {
@@ -345,40 +480,59 @@ extern "C" int medusa_lm_head_verify(const void* hidden, const void* w_lm, float
     if ((reinterpret_cast<uintptr_t>(hidden) | reinterpret_cast<uintptr_t>(w_lm)) % 16)
       return fail(MEDUSA_ERR_INVALID, "%s: hidden / w_lm not 16-byte aligned", fn);
     LmArgs a{};
-    a.logits = logits; a.rows = rows; a.d = d; a.V = V; a.err = err;
-    a.tiled = w_layout == MEDUSA_W_TILES;
-    a.nchunks = (rows + kMaxN - 1) / kMaxN;
-    a.npad = ((rows + a.nchunks - 1) / a.nchunks + 15) / 16 * 16;
-    const int ntiles = (V + BM - 1) / BM;
-    // two vocabulary tiles per work item halve the hidden re-reads per weight
-    // byte; used while both accumulators of both tiles fit in TMEM
-    a.nt = (a.npad <= 128 && ntiles > sm_count()) ? 2 : 1;
-    a.ngroups = (ntiles + a.nt - 1) / a.nt;
-    const size_t stage_bytes = (size_t)a.nt * BM * BK * 2 + (size_t)a.npad * BK * 2;
-    a.stages = (int)std::min<size_t>(8, (kSmemBudget - 1024 - 256) / stage_bytes);
-    uint32_t cols = 32;
-    while (cols < (uint32_t)(2 * a.nt * a.npad)) cols <<= 1;
-    a.tmem_cols = cols;
-    CUtensorMap tmW, tmH;
-    // tiled: a [tiles * (d / 64) * 128][64] matrix whose 128-row boxes are the tiles
-    const bool okw = a.tiled ? make_map(&tmW, w_lm, (uint64_t)BK, (uint64_t)ntiles * BM * (d / BK), BM)
-                             : make_map(&tmW, w_lm, (uint64_t)d, (uint64_t)V, BM);
-    if (!okw ||
-        !make_map(&tmH, hidden, (uint64_t)d, (uint64_t)rows, (uint32_t)a.npad))
-      return fail(MEDUSA_ERR_CUDA, "%s: cuTensorMapEncodeTiled failed", fn);
-    const size_t smem = 1024 + (size_t)a.stages * stage_bytes + (2 * a.stages + 4) * 8 + 16;
-    cudaFuncSetAttribute(lm_head_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-    // balanced: every CTA gets ceil or floor of items / grid work items
-    const int items = a.ngroups * a.nchunks;
-    const int per_cta = (items + sm_count() - 1) / sm_count();
-    const int grid = (items + per_cta - 1) / per_cta;
-    launch_kernel(lm_head_tc_kernel, dim3(grid), dim3(kThreads), smem, s, tmW, tmH, a);
-    return check_launch(fn);
+    a.logits = logits; a.V = V; a.err = err;
+    a.mode = 0;
+    a.ntiles = (V + BM - 1) / BM;
+    return launch_tc(a, w_lm, w_layout == MEDUSA_W_TILES, V, hidden, rows, d, s, fn);
   }
   if (dtype != MEDUSA_F32) return fail(MEDUSA_ERR_UNSUPPORTED, "%s: dtype", fn);
   if (w_layout != MEDUSA_W_ROWS) return fail(MEDUSA_ERR_UNSUPPORTED, "%s: f32 takes MEDUSA_W_ROWS only", fn);
   const int64_t total = (int64_t)rows * V;
   launch_kernel(lm_head_f32_kernel, dim3((unsigned)((total + 7) / 8)), dim3(256), 0, s,
              static_cast<const float*>(hidden), static_cast<const float*>(w_lm), logits, rows, d, V);
+  return check_launch(fn);
+}
+
+extern "C" int medusa_heads_hidden(const void* hidden, int rows, const void* w1, medusa_w_layout w1_layout,
+                                   const void* b1, const int32_t* s_k, int K, int d, medusa_dtype dtype, void* u,
+                                   int32_t* err, void* stream) {
+  const char* fn = "medusa_heads_hidden";
+  if (!hidden || !w1 || !s_k || !u) return fail(MEDUSA_ERR_INVALID, "%s: NULL tensor", fn);
+  if (rows < 1 || K < 1 || d < 1) return fail(MEDUSA_ERR_INVALID, "%s: rows=%d K=%d d=%d", fn, rows, K, d);
+  if (K > MEDUSA_MAX_K) return fail(MEDUSA_ERR_UNSUPPORTED, "%s: K=%d above the maximum", fn, K);
+  if (w1_layout != MEDUSA_W_ROWS && w1_layout != MEDUSA_W_TILES)
+    return fail(MEDUSA_ERR_INVALID, "%s: w1_layout=%d", fn, (int)w1_layout);
+  HeadSlots hs{};
+  int nused = 0;
+  for (int k = 0; k < K; ++k) {
+    if (s_k[k] < 0) return fail(MEDUSA_ERR_INVALID, "%s: s[%d]=%d", fn, k, s_k[k]);
+    if (s_k[k] > 0) hs.id[nused++] = k;
+  }
+  if (nused == 0) return MEDUSA_OK;
+  cudaStream_t s = as_stream(stream);
+  if (dtype == MEDUSA_BF16) {
+    if (d % BM) return fail(MEDUSA_ERR_UNSUPPORTED, "%s: d=%d not a multiple of %d", fn, d, BM);
+    if ((reinterpret_cast<uintptr_t>(hidden) | reinterpret_cast<uintptr_t>(w1) | reinterpret_cast<uintptr_t>(u)) %
+        16)
+      return fail(MEDUSA_ERR_INVALID, "%s: hidden / w1 / u not 16-byte aligned", fn);
+    LmArgs a{};
+    a.mode = 1;
+    a.V = nused * d;
+    a.ntiles = nused * (d / BM);
+    a.tpr = d / BM;
+    a.K = K;
+    for (int i = 0; i < nused; ++i) a.heads[i] = hs.id[i];
+    a.hidden = static_cast<const uint16_t*>(hidden);
+    a.b1 = static_cast<const uint16_t*>(b1);
+    a.u = static_cast<uint16_t*>(u);
+    a.err = err;
+    return launch_tc(a, w1, w1_layout == MEDUSA_W_TILES, (int64_t)K * d, hidden, rows, d, s, fn);
+  }
+  if (dtype != MEDUSA_F32) return fail(MEDUSA_ERR_UNSUPPORTED, "%s: dtype", fn);
+  if (w1_layout != MEDUSA_W_ROWS) return fail(MEDUSA_ERR_UNSUPPORTED, "%s: f32 takes MEDUSA_W_ROWS only", fn);
+  const int64_t warps = (int64_t)rows * nused * d;
+  launch_kernel(heads_hidden_f32_kernel, dim3((unsigned)((warps + 7) / 8)), dim3(256), 0, s,
+                static_cast<const float*>(hidden), static_cast<const float*>(w1), static_cast<const float*>(b1),
+                static_cast<float*>(u), rows, d, K, nused, hs);
   return check_launch(fn);
 }

@@ -58,6 +58,9 @@ _SIGS = {
     "medusa_heads_topk_workspace_size": (SZ, [I, I, I, I, I]),
     "medusa_heads_topk": (I, [P, P, I, P, P, P, P, I, I, I, I, I, P, P, I, P, SZ, P, P]),
     "medusa_build_candidates": (I, [P, P, I, I, TREE, I, P, P]),
+    "medusa_heads_hidden": (I, [P, I, P, I, P, P, I, I, I, P, P, P]),
+    "medusa_heads_logits_topk_workspace_size": (SZ, [I, I, I, I]),
+    "medusa_heads_logits_topk": (I, [P, I, P, P, P, I, I, I, I, I, P, P, I, P, SZ, P, P]),
 }
 for _name, (_res, _args) in _SIGS.items():
     _f = getattr(_lib, _name)
@@ -291,6 +294,31 @@ def medusa_heads_topk(hidden, last_node, w1, b1, w2, s, head_logits, topk, works
                                   _ptr(s_arr), K, B, d, V, _dtype(hidden), _ptr(head_logits), _ptr(topk),
                                   s_max, _ptr(workspace), workspace.numel() * workspace.element_size(),
                                   _ptr(err), _stream(stream)), "medusa_heads_topk")
+
+
+def medusa_heads_hidden(hidden, w1, b1, s, u, err=None, stream=None, layout=W_ROWS):
+    """u [rows][K][d] = dtype(SiLU(W1_k h_r + b1_k) + h_r) for every row of hidden (any leading shape)."""
+    d = hidden.shape[-1]
+    rows = hidden.numel() // d
+    s_arr = np.ascontiguousarray(s, np.int32)
+    _check(_lib.medusa_heads_hidden(_ptr(hidden), rows, _ptr(w1), layout, _ptr(b1), _ptr(s_arr), len(s_arr), d,
+                                    _dtype(hidden), _ptr(u), _ptr(err), _stream(stream)), "medusa_heads_hidden")
+
+
+def medusa_heads_logits_topk_workspace_size(B, K, V, s_max) -> int:
+    return int(_lib.medusa_heads_logits_topk_workspace_size(B, K, V, s_max))
+
+
+def medusa_heads_logits_topk(u, T, node, w2, s, head_logits, topk, workspace, err=None, stream=None):
+    """W2 + top-s on row b*T + node[b] of u [B*T][K][d]; the workspace must be zero on the first call."""
+    K, V, d = w2.shape
+    B = node.shape[0]
+    s_arr = np.ascontiguousarray(s, np.int32)
+    assert len(s_arr) == K
+    _check(_lib.medusa_heads_logits_topk(_ptr(u), T, _ptr(node), _ptr(w2), _ptr(s_arr), K, B, d, V, _dtype(u),
+                                         _ptr(head_logits), _ptr(topk), topk.shape[-1], _ptr(workspace),
+                                         workspace.numel() * workspace.element_size(), _ptr(err),
+                                         _stream(stream)), "medusa_heads_logits_topk")
 
 
 def medusa_build_candidates(next_root, topk, tree: DeviceTree, tokens, stream=None):

@@ -3,9 +3,13 @@ library calls.  Plumbing only: every step of the method runs in libmedusa.
 
 Call order (decoding-step box of the Medusa paper digest, steps 3-6 then 1-2
 for the next step):
-  main chain: medusa_lm_head_verify -> medusa_accept -> medusa_heads_topk ->
+  main chain: medusa_lm_head_verify -> medusa_accept -> heads ->
   medusa_build_candidates; medusa_tree_attn and then medusa_kv_compact either
-  on the same stream or on a forked branch that joins at the end
+  on the same stream or on a forked branch that joins at the end.
+  heads = medusa_heads_topk on the accepted node ("fused"), or ("split")
+  medusa_heads_hidden over every tree row -- forked after the LM head so that
+  it runs beside the acceptance -- then medusa_heads_logits_topk on the
+  accepted node's row.
 """
 from __future__ import annotations
 
@@ -45,7 +49,8 @@ def build_tree(w: dict) -> M.HostTree:
 class VerifyStep:
     """Owns the outputs and scratch of one verify step for fixed shapes."""
 
-    def __init__(self, w: dict, weights: dict, tree: M.DeviceTree, max_prefix: int, device="cuda"):
+    def __init__(self, w: dict, weights: dict, tree: M.DeviceTree, max_prefix: int, device="cuda",
+                 heads: str = "fused"):
         self.w, self.tree, self.max_prefix = w, tree, max_prefix
         B, H, Dh, d, V, K = w["B"], w["H"], w["Dh"], w["d"], w["V"], w["K"]
         T = tree.T
@@ -84,8 +89,18 @@ class VerifyStep:
         self.ws_attn = ws(M.medusa_tree_attn_workspace_size(B, H, Dh, T, max_prefix))
         self.ws_accept = ws(M.medusa_accept_workspace_size(B, T))
         self.ws_heads = ws(M.medusa_heads_topk_workspace_size(B, K, d, V, self.s_max))
+        # split heads: W1 over every tree row (tile layout for bf16), u for all rows,
+        # and the W2 pass's arrival counters (zero once; each call leaves them zero)
+        self.heads = heads
+        if heads == "split":
+            self.w1_layout = M.W_TILES if w["dtype"] == "bf16" else M.W_ROWS
+            self.w1_run = (M.medusa_lm_head_tile(self.w1.reshape(K * d, d)) if self.w1_layout == M.W_TILES
+                           else self.w1)
+            self.u_all = torch.zeros((B * T, K, d), dtype=dt, device=device)
+            self.ws_w2 = torch.zeros(max(256, M.medusa_heads_logits_topk_workspace_size(B, K, V, self.s_max)),
+                                     dtype=torch.uint8, device=device)
 
-    def run(self, x: dict, stream=None, side_stream=None):
+    def run(self, x: dict, stream=None, side_stream=None, heads_stream=None):
         """x: device tensors q, k_new, v_new, hidden, tokens, k_cache, v_cache,
         seq_start, prefix_len, seq_cap.  Updates the cache and prefix_len.
 
@@ -105,6 +120,12 @@ class VerifyStep:
                            self.scale, self.out, self.ws_attn, self.err, side)
         M.medusa_lm_head_verify(x["hidden"], self.w_lm_run, self.logits, None, self.err, main,
                                 layout=self.w_layout)
+        hs = heads_stream if heads_stream is not None else main
+        if self.heads == "split":
+            if hs is not main:
+                hs.wait_stream(main)  # after the LM head: beside the acceptance
+            M.medusa_heads_hidden(x["hidden"], self.w1_run, self.b1, self.s_heads, self.u_all, self.err, hs,
+                                  layout=self.w1_layout)
         M.medusa_accept(self.logits, x["tokens"], self.tree, self.mode, self.temperature, self.eps,
                         self.delta, self.accept_len, self.accepted_nodes, self.next_root, self.best_node,
                         self.best_logp, self.ws_accept, self.err, main)
@@ -113,8 +134,14 @@ class VerifyStep:
         M.medusa_kv_compact(x["k_cache"], x["v_cache"], x["seq_start"], x["prefix_len"],
                             self.accepted_nodes, self.accept_len, self.tree.K, self.src_slots, self.err,
                             side)
-        M.medusa_heads_topk(x["hidden"], self.best_node, self.w1, self.b1, self.w2, self.s_heads,
-                            self.head_logits, self.topk, self.ws_heads, self.err, main)
+        if self.heads == "split":
+            if hs is not main:
+                main.wait_stream(hs)
+            M.medusa_heads_logits_topk(self.u_all, self.T, self.best_node, self.w2, self.s_heads, self.head_logits,
+                                       self.topk, self.ws_w2, self.err, main)
+        else:
+            M.medusa_heads_topk(x["hidden"], self.best_node, self.w1, self.b1, self.w2, self.s_heads,
+                                self.head_logits, self.topk, self.ws_heads, self.err, main)
         M.medusa_build_candidates(self.next_root, self.topk, self.tree, self.next_tokens, main)
         if side is not main:
             main.wait_stream(side)

@@ -187,6 +187,20 @@ def test_validation_statuses(M):
     assert L.medusa_heads_topk(FAKE, FAKE, 15, FAKE, None, FAKE, s, 9, 1, 256, 1000, 1, FAKE, FAKE, 8,
                                FAKE, 1 << 30, None, None) == -2
     assert b"medusa_heads_topk" in L.medusa_last_error()
+    # heads over every row: bf16 needs d a multiple of 128; K above the maximum; bad layout
+    s = (C.c_int32 * 3)(2, 2, 2)
+    assert L.medusa_heads_hidden(FAKE, 65, FAKE, 0, None, s, 3, 320, 1, FAKE, None, None) == -2
+    assert L.medusa_heads_hidden(FAKE, 65, FAKE, 0, None, s, 9, 256, 1, FAKE, None, None) == -2
+    assert L.medusa_heads_hidden(FAKE, 65, FAKE, 5, None, s, 3, 256, 1, FAKE, None, None) == -1
+    assert L.medusa_heads_hidden(FAKE, 65, FAKE, 1, None, s, 3, 256, 0, FAKE, None, None) == -2  # f32: rows only
+    zero = (C.c_int32 * 3)(0, 0, 0)
+    assert L.medusa_heads_hidden(FAKE, 65, FAKE, 0, None, zero, 3, 256, 1, FAKE, None, None) == 0  # nothing to do
+    # W2 on the accepted row: small workspace, s_k above s_max
+    assert L.medusa_heads_logits_topk(FAKE, 65, FAKE, FAKE, s, 3, 1, 256, 1000, 1, FAKE, FAKE, 8, FAKE, 8,
+                                      None, None) == -4
+    s9 = (C.c_int32 * 3)(2, 9, 2)
+    assert L.medusa_heads_logits_topk(FAKE, 65, FAKE, FAKE, s9, 3, 1, 256, 1000, 1, FAKE, FAKE, 8, FAKE, 1 << 30,
+                                      None, None) == -1
 
 
 def test_workspace_queries(M):
@@ -195,6 +209,7 @@ def test_workspace_queries(M):
     n = M.medusa_tree_attn_workspace_size(1, 32, 128, 65, 1024)
     assert n >= 65 * 32 * 128 * 4
     assert M.medusa_lm_head_workspace_size(65, 4096, 32000) == 0
+    assert M.medusa_heads_logits_topk_workspace_size(1, 4, 32000, 8) >= 4 * 4
     assert M.medusa_lm_head_tiled_bytes(4096, 32000) == 32000 * 4096 * 2
     assert M.medusa_lm_head_tiled_bytes(256, 1000) == 1024 * 256 * 2  # last block padded to 128 rows
     assert M.medusa_lm_head_tiled_bytes(100, 1000) == 0

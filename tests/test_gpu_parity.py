@@ -407,6 +407,71 @@ def test_heads_topk(M, case):
                 assert list(tg[b, k, :s[k]]) == list(tk_ref[b, k, :s[k]])
 
 
+@pytest.mark.parametrize("case", HEAD_CASES, ids=lambda c: f"{c[0]}-B{c[1]}-d{c[3]}-V{c[4]}-s{len(c[5])}")
+def test_heads_split(M, case):
+    """medusa_heads_hidden (W1 over every tree row, both weight layouts) and
+    medusa_heads_logits_topk on one row per sequence: u against the oracle
+    row by row, head logits and top-s as in the fused call; the W2 call runs
+    twice on one zeroed workspace (its counters must come back to zero)."""
+    dt, B, T, d, V, s, bias, lm_noise = case
+    K = len(s)
+    s_max = max(s)
+    hidden = synth.normal(14, "hidden", (B, T, d), 1.0, dt)
+    w1 = synth.normal(14, "w1", (K, d, d), 1 / math.sqrt(d), dt)
+    w2 = synth.normal(14, "w2", (K, V, d), 1 / math.sqrt(d), dt)
+    b1 = synth.normal(14, "b1", (K, d), 0.5, dt) if bias else None
+    node = np.array([(5 * b + 2) % T for b in range(B)], np.int32)
+    used = [k for k in range(K) if s[k] > 0]
+    hd, w1d = to_dev(hidden), to_dev(w1)
+    b1d = None if b1 is None else to_dev(b1)
+    layouts = [M.W_ROWS] + ([M.W_TILES] if dt == "bf16" else [])
+    # rows checked against the oracle (all of them for small shapes)
+    rows = list(range(B * T)) if d * d * K * B * T <= 2**28 else [0, 1, T - 1, B * T - 1]
+    one = np.ascontiguousarray(w2[:, :1])
+    flat = hidden.reshape(B * T, 1, d)
+    _, _, u_ref = oracle.heads(np.ascontiguousarray(flat[rows]), np.zeros(len(rows), np.int32), w1, b1, one,
+                               [1 if k in used else 0 for k in range(K)], 1)
+    for lay in layouts:
+        wsrc = M.medusa_lm_head_tile(w1d.reshape(K * d, d)) if lay == M.W_TILES else w1d
+        u = torch.full((B * T, K, d), float("nan"), dtype=hd.dtype, device="cuda")
+        e = err_flag()
+        M.medusa_heads_hidden(hd, wsrc, b1d, list(s), u, e, layout=lay)
+        torch.cuda.synchronize()
+        assert int(e.item()) == 0
+        ug = as_double(to_host(u))
+        for i, r in enumerate(rows):
+            for k in used:
+                ref = as_double(u_ref[i, k])
+                tol = (2.0 ** -7 * np.abs(ref) + 1e-3) if dt == "bf16" else (1e-4 * np.abs(ref) + 1e-4)
+                assert np.all(np.abs(ug[r, k] - ref) <= tol), f"u row {r} head {k}"
+    # W2 + top-s on the accepted rows, twice on one zeroed workspace
+    hl = torch.zeros((B, K, V), dtype=torch.float32, device="cuda")
+    tk = torch.zeros((B, K, s_max), dtype=torch.int32, device="cuda")
+    ws = torch.zeros(M.medusa_heads_logits_topk_workspace_size(B, K, V, s_max), dtype=torch.uint8, device="cuda")
+    e = err_flag()
+    for rep in range(2):
+        M.medusa_heads_logits_topk(u, T, to_dev(node), to_dev(w2), list(s), hl, tk, ws, e)
+        torch.cuda.synchronize()
+        assert int(e.item()) == 0
+        zg, tg = to_host(hl), to_host(tk)
+        if rep == 0:
+            first = (zg.copy(), tg.copy())
+        else:
+            assert np.array_equal(first[0], zg) and np.array_equal(first[1], tg)
+    z_ref, tk_ref, _ = oracle.heads(hidden, node, w1, b1, w2, list(s), s_max)
+    for b in range(B):
+        for k in range(K):
+            if s[k] == 0:
+                assert np.all(tg[b, k] == 0)
+                continue
+            scale = np.abs(z_ref[b, k]).max()
+            err = np.abs(zg[b, k] - z_ref[b, k]).max()
+            assert err <= TOL[dt]["logit"] * scale, f"head logit error {err} (max {scale})"
+            order = np.lexsort((np.arange(V), -zg[b, k].astype(np.float64)))[:s[k]]
+            assert list(tg[b, k, :s[k]]) == list(order)
+            assert np.all(tg[b, k, s[k]:] == -1)
+
+
 def test_heads_init_reproduce_lm_head(M):
     """W1 = 0, W2 = the LM head: every head's top-1 is the LM head's argmax."""
     d, V, K, T = 256, 1000, 3, 7

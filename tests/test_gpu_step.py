@@ -37,7 +37,7 @@ def _tree_spec(w):
     return ("cartesian", t[1], t[2]) if t[0] == "cartesian" else ("greedy", w["K"], t[2], t[1])
 
 
-def _run(M, name, plant_node_fn, seed=0):
+def _run(M, name, plant_node_fn, seed=0, heads="fused"):
     from medusa_tree_speculative_gb300 import step
 
     w = workloads.get(name)
@@ -58,15 +58,17 @@ def _run(M, name, plant_node_fn, seed=0):
     dev = {k: to_dev(v) for k, v in x.items()}
     dev["tokens"] = to_dev(tok)
     wd = {k: (None if v is None else to_dev(v)) for k, v in wts.items()}
-    st = step.VerifyStep(w, wd, dtree, max_prefix=int(x["prefix_len"].max()))
-    st.run(dev)
+    st = step.VerifyStep(w, wd, dtree, max_prefix=int(x["prefix_len"].max()), heads=heads)
+    # split heads: W1 over every tree row on a second stream, beside the acceptance
+    st.run(dev, heads_stream=torch.cuda.Stream() if heads == "split" else None)
     torch.cuda.synchronize()
     return w, ot, wts, x, tok, st, dev, node, path, lg_par, parents, gaps
 
 
-def test_step_tiny_fp32_full(M):
+@pytest.mark.parametrize("heads", ["fused", "split"])
+def test_step_tiny_fp32_full(M, heads):
     w, ot, wts, x, tok, st, dev, node, path, _, _, _ = _run(
-        M, "tiny_fp32", lambda ot: int(np.nonzero(ot.depth == 3)[0][-1]))
+        M, "tiny_fp32", lambda ot: int(np.nonzero(ot.depth == 3)[0][-1]), heads=heads)
     assert int(st.err.item()) == 0
     kc, vc = x["k_cache"].copy(), x["v_cache"].copy()
     _, ref = oracle.tree_attn(x["q"], x["k_new"], x["v_new"], kc, vc, x["seq_start"], x["prefix_len"], ot)
@@ -88,9 +90,10 @@ def test_step_tiny_fp32_full(M):
     assert np.array_equal(to_host(st.next_tokens), oracle.build_candidates(r["next_root"], tk, ot))
 
 
-def test_step_vicuna7b_sampled(M):
+@pytest.mark.parametrize("heads", ["fused", "split"])
+def test_step_vicuna7b_sampled(M, heads):
     w, ot, wts, x, tok, st, dev, node, path, lg_par, parents, gaps = _run(
-        M, "vicuna7b_L1024_tree64", lambda ot: int(np.nonzero(ot.depth == 3)[0][4]))
+        M, "vicuna7b_L1024_tree64", lambda ot: int(np.nonzero(ot.depth == 3)[0][4]), heads=heads)
     assert int(st.err.item()) == 0
     T, V, H, Dh = ot.T, w["V"], w["H"], w["Dh"]
     # --- attention on three heads (oracle on single-head slices)
