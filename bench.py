@@ -48,6 +48,8 @@ def parse_args():
     ap.add_argument("--plant-depth", type=int, default=3)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--loop-steps", type=int, default=48,
+                    help="chained verify steps on the device around the stand-in backbone (0: skip)")
     ap.add_argument("--heads", choices=["split", "fused"], default="fused",
                     help="heads' W1 over every tree row beside the acceptance, then W2 on the accepted "
                          "row (split), or both projections on the accepted row after it (fused)")
@@ -334,10 +336,71 @@ def run_native(args, w, rank, world, local_rank):
     e2e = None
     if not args.no_e2e:
         e2e = measure_e2e(args, w, st, x, xh, prefix0, s, s2, s3, torch, M)
+    dloop = None
+    if args.loop_steps > 0 and world == 1:
+        dloop = measure_loop(args, w, dev, torch, M)
 
     return dict(ms_step=ms_step, ms_events_step=ms_events / args.steps, per_call_ms=per_call, clocks=clocks,
+                dloop=dloop,
                 T=T, s_heads=st.s_heads, L_list=L_list, accept_len=accept_len, e2e=e2e,
                 launches=st.launches_per_step * args.steps, tree=ht)
+
+
+def measure_loop(args, w, dev, torch, M):
+    """Chained steps (the decode loop of medusa_tree_speculative_gb300.loop):
+    each step's tree comes from the previous one, on the device, around the
+    stand-in backbone (an embedding lookup).  One CUDA graph of n steps,
+    re-primed before every replay; the emitted tokens are checked against the
+    stand-in model's greedy continuation."""
+    from medusa_tree_speculative_gb300 import loop, step
+
+    n = args.loop_steps
+    tree = M.DeviceTree(step.build_tree(w), dev)
+    model = loop.StandInModel(w, seed=3, device=dev)
+    x0 = np.array([(97 * b + 5) % w["V"] for b in range(w["B"])])
+    lp = loop.DecodeLoop(w, model, tree, n, L0=int(w["L"][0]), x0=x0, device=dev, heads=args.heads)
+    s = torch.cuda.Stream(device=dev)
+    s2 = torch.cuda.Stream(device=dev) if args.attn_branch == "fork" else None
+    s3 = torch.cuda.Stream(device=dev) if args.heads == "split" else None
+    L0 = int(w["L"][0])
+
+    def reset():
+        with torch.cuda.stream(s):
+            lp.x["prefix_len"].fill_(L0)
+            lp._prime()
+        torch.cuda.synchronize()
+
+    reset()
+    with torch.cuda.stream(s):
+        lp.step(s, s2, s3)  # eager once (attributes, tensor maps)
+    reset()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=s):
+        for _ in range(n):
+            lp.step(s, s2, s3)
+    times = []
+    for _ in range(3):
+        reset()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        with torch.cuda.stream(s):
+            e0.record(s)
+            g.replay()
+            e1.record(s)
+        torch.cuda.synchronize()
+        times.append(e0.elapsed_time(e1))
+    if int(lp.st.err.item()) != 0:
+        raise RuntimeError(f"device error flag {int(lp.st.err.item())} in the decode loop")
+    got = lp.emitted()
+    ref = lp.greedy_reference(max(len(t) for t in got))
+    ok = all(np.array_equal(got[b], ref[b, :len(got[b])]) for b in range(w["B"]))
+    ms = statistics.median(times)
+    tokens = sum(len(t) for t in got)
+    return {"steps": n, "tokens": tokens, "tokens_per_step": tokens / (n * w["B"]),
+            "verify_steps_per_s": n * 1e3 / ms, "tokens_per_s": tokens * 1e3 / ms,
+            "ms_per_step": ms / n, "matches_greedy_decoding": bool(ok),
+            "backbone": "stand-in: hidden state and q/k/v of a token = its embedding row; LM head and heads "
+                        "built on a fixed next-token chain, heads' W2 with Gaussian noise (sigma 0.20-0.29)",
+            "gpu_launches_per_step": lp.launches_per_step()}
 
 
 def measure_e2e(args, w, st, x, xh, prefix0, s, s2, s3, torch, M):
@@ -564,6 +627,8 @@ def main():
     }
     if r["e2e"] is not None:
         line["e2e"] = r["e2e"]
+    if r["dloop"] is not None:
+        line["decode_loop"] = r["dloop"]
     if world == 1 and not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline(w)
     print(json.dumps(line), flush=True)

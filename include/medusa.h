@@ -18,6 +18,8 @@
  *     (or: medusa_heads_hidden over every tree row, which can run beside the
  *      acceptance, then medusa_heads_logits_topk on the accepted row)
  *   medusa_build_candidates next step's candidate tokens         (box 2)
+ * In a decode loop, medusa_append_tokens (box step 6) appends each step's
+ * tokens to the output.
  *
  * Conventions
  *   - Every step call returns MEDUSA_OK (0) or a negative status; on error
@@ -348,6 +350,33 @@ int medusa_heads_logits_topk(const void* u, int T, const int32_t* node,
 int medusa_build_candidates(const int32_t* next_root, const int32_t* topk,
                             int s_max, int K, const medusa_tree_t* tree,
                             int B, int32_t* tokens, void* stream);
+
+/* Append a step's output tokens ([MED] box step 6: "append the root plus the
+ * accepted tokens", 1 + accept_len of them):
+ *   out[b][out_len[b] + j] = tokens[b][accepted_nodes[b][j]], j = 0..accept_len[b]
+ *   out_len[b] += accept_len[b] + 1.
+ * tokens: device [B][T] (the step's tree tokens); accepted_nodes: device
+ * [B][Kmax+1] and accept_len: device [B] (medusa_accept's outputs); out:
+ * device [B][out_cap]; out_len: device [B], in/out.  A sequence whose
+ * accept_len is outside [0, Kmax] (MEDUSA_DEVERR_LENGTH), whose output would
+ * pass out_cap (MEDUSA_DEVERR_CAPACITY) or whose path holds a node outside
+ * [0, T) (MEDUSA_DEVERR_NODE) is left with out_len unchanged. */
+int medusa_append_tokens(const int32_t* tokens, const int32_t* accepted_nodes,
+                         const int32_t* accept_len, int B, int T, int Kmax,
+                         int32_t* out, int32_t* out_len, int out_cap,
+                         int32_t* err, void* stream);
+
+/* A stand-in for the backbone forward, with no counterpart in the paper:
+ *   hidden[r] = emb[tokens[r]], r < rows
+ * so that the verify step can run in a closed loop on the device without a
+ * transformer (the stand-in model's hidden state of a token is its embedding
+ * row; attention inputs are taken from the same rows).  tokens: device
+ * [rows]; emb: device [V][d] of dtype; hidden: device [rows][d].  Rows must
+ * be multiples of 16 bytes, pointers 16-byte aligned.  A token outside
+ * [0, V) gives a zero row and MEDUSA_DEVERR_TOKEN. */
+int medusa_standin_embed(const int32_t* tokens, int rows, const void* emb,
+                         int V, int d, medusa_dtype dtype, void* hidden,
+                         int32_t* err, void* stream);
 
 #ifdef __cplusplus
 }

@@ -59,6 +59,8 @@ _SIGS = {
     "medusa_heads_topk": (I, [P, P, I, P, P, P, P, I, I, I, I, I, P, P, I, P, SZ, P, P]),
     "medusa_build_candidates": (I, [P, P, I, I, TREE, I, P, P]),
     "medusa_heads_hidden": (I, [P, I, P, I, P, P, I, I, I, P, P, P]),
+    "medusa_append_tokens": (I, [P, P, P, I, I, I, P, P, I, P, P]),
+    "medusa_standin_embed": (I, [P, I, P, I, I, I, P, P, P]),
     "medusa_heads_logits_topk_workspace_size": (SZ, [I, I, I, I]),
     "medusa_heads_logits_topk": (I, [P, I, P, P, P, I, I, I, I, I, P, P, I, P, SZ, P, P]),
 }
@@ -325,3 +327,18 @@ def medusa_build_candidates(next_root, topk, tree: DeviceTree, tokens, stream=No
     B, K, s_max = topk.shape
     _check(_lib.medusa_build_candidates(_ptr(next_root), _ptr(topk), s_max, K, tree.ref, B, _ptr(tokens),
                                         _stream(stream)), "medusa_build_candidates")
+
+
+def medusa_append_tokens(tokens, accepted_nodes, accept_len, out, out_len, err=None, stream=None):
+    """out[b][out_len[b]:] += tokens[b][accepted path]; out_len[b] += accept_len[b] + 1."""
+    B, T = tokens.shape
+    _check(_lib.medusa_append_tokens(_ptr(tokens), _ptr(accepted_nodes), _ptr(accept_len), B, T,
+                                     accepted_nodes.shape[1] - 1, _ptr(out), _ptr(out_len), out.shape[1],
+                                     _ptr(err), _stream(stream)), "medusa_append_tokens")
+
+
+def medusa_standin_embed(tokens, emb, hidden, err=None, stream=None):
+    """hidden[r] = emb[tokens[r]] over the flattened tokens (stand-in backbone)."""
+    V, d = emb.shape
+    _check(_lib.medusa_standin_embed(_ptr(tokens), tokens.numel(), _ptr(emb), V, d, _dtype(emb), _ptr(hidden),
+                                     _ptr(err), _stream(stream)), "medusa_standin_embed")

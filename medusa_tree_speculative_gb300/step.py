@@ -100,7 +100,7 @@ class VerifyStep:
             self.ws_w2 = torch.zeros(max(256, M.medusa_heads_logits_topk_workspace_size(B, K, V, self.s_max)),
                                      dtype=torch.uint8, device=device)
 
-    def run(self, x: dict, stream=None, side_stream=None, heads_stream=None):
+    def run(self, x: dict, stream=None, side_stream=None, heads_stream=None, append=None):
         """x: device tensors q, k_new, v_new, hidden, tokens, k_cache, v_cache,
         seq_start, prefix_len, seq_cap.  Updates the cache and prefix_len.
 
@@ -108,7 +108,10 @@ class VerifyStep:
         KV compaction.  With `side_stream`: the chain LM head -> acceptance ->
         heads -> candidates stays on `stream` while the tree attention and
         then the KV compaction (which needs the acceptance result) run on a
-        forked branch that joins `stream` at the end."""
+        forked branch that joins `stream` at the end.  `append` = (out,
+        out_len): the step's root and accepted tokens are appended there right
+        after the acceptance (so x["tokens"] may be the buffer that
+        medusa_build_candidates refills at the end of the step)."""
         import torch
 
         main = stream if stream is not None else torch.cuda.current_stream()
@@ -129,6 +132,9 @@ class VerifyStep:
         M.medusa_accept(self.logits, x["tokens"], self.tree, self.mode, self.temperature, self.eps,
                         self.delta, self.accept_len, self.accepted_nodes, self.next_root, self.best_node,
                         self.best_logp, self.ws_accept, self.err, main)
+        if append is not None:  # box step 6: the root and the accepted tokens to the output
+            M.medusa_append_tokens(x["tokens"], self.accepted_nodes, self.accept_len, append[0], append[1],
+                                   self.err, main)
         if side is not main:
             side.wait_stream(main)  # compaction needs the accepted path
         M.medusa_kv_compact(x["k_cache"], x["v_cache"], x["seq_start"], x["prefix_len"],
