@@ -89,6 +89,8 @@ def _declare(L):
     L.orc_build_candidates.argtypes = [P, P, I, I, P, P, I, I, P]
     L.orc_rejection_emit.restype = D
     L.orc_rejection_emit.argtypes = [P, P, I, P]
+    L.orc_rejection_tree.restype = I
+    L.orc_rejection_tree.argtypes = [P, P, P, P, P, P, I, I, I, I, D, P, I, P, P, P, P]
 
 
 def _p(a):
@@ -320,3 +322,22 @@ def rejection_emit(p, q):
     out = np.zeros_like(p)
     beta = lib().orc_rejection_emit(_p(p), _p(q), len(p), _p(out))
     return out, beta
+
+
+def rejection_tree(logits, draft, tokens, tree: Tree, temperature, u):
+    """logits [B,T,V] f32, draft [B,K,V] f32, tokens [B,T], u [B,T,S1] f32 ->
+    dict(accept_len [B], accepted_nodes [B,K+1], next_token [B], margin [B])."""
+    logits = np.ascontiguousarray(logits, np.float32)
+    draft = np.ascontiguousarray(draft, np.float32)
+    tokens = np.ascontiguousarray(tokens, np.int32)
+    u = np.ascontiguousarray(u, np.float32)
+    B, T, V = logits.shape
+    K = tree.K
+    assert draft.shape == (B, K, V) and u.shape[:2] == (B, T)
+    out = dict(accept_len=np.zeros(B, np.int32), accepted_nodes=np.zeros((B, K + 1), np.int32),
+               next_token=np.zeros(B, np.int32), margin=np.zeros(B, np.float64))
+    _chk(lib().orc_rejection_tree(_p(logits), _p(draft), _p(tokens), _p(tree.parent), _p(tree.depth),
+                                  _p(tree.rank), T, K, B, V, float(temperature), _p(u), u.shape[2],
+                                  _p(out["accept_len"]), _p(out["accepted_nodes"]), _p(out["next_token"]),
+                                  _p(out["margin"])), "rejection_tree")
+    return out

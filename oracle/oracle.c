@@ -619,3 +619,93 @@ double orc_rejection_emit(const double* p, const double* q, int n,
   }
   return beta;
 }
+
+/* softmax(z / tau) of one row, in double */
+static void softmax_row(const float* z, int V, double tau, double* out) {
+  double m = -INFINITY;
+  for (int v = 0; v < V; ++v) m = fmax(m, (double)z[v] / tau);
+  double S = 0.0;
+  for (int v = 0; v < V; ++v) {
+    out[v] = exp((double)z[v] / tau - m);
+    S += out[v];
+  }
+  for (int v = 0; v < V; ++v) out[v] /= S;
+}
+
+int orc_rejection_tree(const float* logits, const float* draft, const int32_t* tokens,
+                       const int32_t* parent, const int32_t* depth, const int32_t* rank, int T,
+                       int K, int B, int V, double temperature, const float* u, int u_stride,
+                       int32_t* accept_len, int32_t* accepted_nodes, int32_t* next_token,
+                       double* margin) {
+  if (T < 1 || B < 1 || V < 1 || K < 0 || u_stride < 1 || !(temperature > 0.0)) return -1;
+  double* p = (double*)malloc(sizeof(double) * (size_t)V);
+  double* q = (double*)malloc(sizeof(double) * (size_t)V);
+  int* kids = (int*)malloc(sizeof(int) * (size_t)T);
+  for (int b = 0; b < B; ++b) {
+    int cur = 0, len = 0;
+    double mg = INFINITY;
+    int32_t* an = accepted_nodes + (int64_t)b * (K + 1);
+    for (int j = 0; j <= K; ++j) an[j] = -1;
+    an[0] = 0;
+    softmax_row(logits + ((int64_t)b * T + 0) * V, V, temperature, p);
+    int m = 0; /* children of the node where the walk stops */
+    for (;;) {
+      /* children of cur, in rank order */
+      m = 0;
+      for (int n = 0; n < T; ++n)
+        if (n > 0 && parent[n] == cur) kids[m++] = n;
+      for (int i = 1; i < m; ++i) /* insertion sort by rank */
+        for (int j = i; j > 0 && rank[kids[j]] < rank[kids[j - 1]]; --j) {
+          int t = kids[j]; kids[j] = kids[j - 1]; kids[j - 1] = t;
+        }
+      if (m == 0 || m >= u_stride) break;
+      const int k = depth[kids[0]];
+      if (k < 1 || k > K) break;
+      softmax_row(draft + ((int64_t)b * K + (k - 1)) * V, V, temperature, q);
+      int acc = -1;
+      for (int j = 0; j < m; ++j) {
+        const int n = kids[j];
+        const int x = tokens[(int64_t)b * T + n];
+        if (x < 0 || x >= V) continue; /* an invalid draft is never accepted */
+        const double uu = (double)u[((int64_t)b * T + cur) * u_stride + j];
+        const double lhs = uu * q[x], rhs = p[x];
+        const double den = fmax(fmax(p[x], q[x]), 1e-300);
+        mg = fmin(mg, fabs(lhs - rhs) / den);
+        if (lhs < rhs) { acc = n; break; }
+        /* rejected: the target becomes the normalised positive residual */
+        double S = 0.0;
+        for (int v = 0; v < V; ++v) S += fmax(0.0, p[v] - q[v]);
+        if (S > 0.0)
+          for (int v = 0; v < V; ++v) p[v] = fmax(0.0, p[v] - q[v]) / S;
+      }
+      if (acc < 0) break;
+      an[++len] = acc;
+      cur = acc;
+      softmax_row(logits + ((int64_t)b * T + cur) * V, V, temperature, p);
+    }
+    /* the final token: inverse CDF of p at u[b][cur][m] */
+    const int mm = m < u_stride ? m : u_stride - 1;
+    const double uu = (double)u[((int64_t)b * T + cur) * u_stride + mm];
+    double c = 0.0;
+    int tok = -1;
+    for (int v = 0; v < V; ++v) {
+      if (p[v] <= 0.0) continue;
+      const double c1 = c + p[v];
+      if (tok < 0 && uu < c1) {
+        tok = v;
+        mg = fmin(mg, fmin(fabs(uu - c), fabs(c1 - uu)));
+      }
+      c = c1;
+    }
+    if (tok < 0) /* u beyond the rounded total: the last token with mass */
+      for (int v = V - 1; v >= 0 && tok < 0; --v)
+        if (p[v] > 0.0) tok = v;
+    accept_len[b] = len;
+    next_token[b] = tok;
+    if (margin) margin[b] = mg;
+  }
+  free(p);
+  free(q);
+  free(kids);
+  return 0;
+}

@@ -150,6 +150,33 @@ int orc_build_candidates(const int32_t* next_root, const int32_t* topk,
 double orc_rejection_emit(const double* p, const double* q, int n,
                           double* emitted);
 
+/* ---- rejection-sampling acceptance over the tree ------------------------ */
+/* [SPEC] "Maths" and the verify rule of its introduction (accept a drafted x
+ * with probability min(1, p(x)/q(x)); at a rejection draw from the residual
+ * [p-q]_+ normalised; a fully accepted draft earns one more target token),
+ * walked along the candidate tree (reading: a node's children are tried in
+ * rank order; after each rejection the target becomes the normalised
+ * residual; q stays the drafting head's distribution).  Lossless when the
+ * children of a node are independent draws from q.  Per sequence b, from the
+ * root: p = softmax(logits[b][node] / tau); child n of depth k is drafted
+ * from q_k = softmax(draft[b][k-1] / tau); child j of node n is accepted iff
+ * u[b][n][j] * q(x) < p(x); the final token is the first x whose running sum
+ * of p exceeds u[b][n][m], m = the number of children of the node where the
+ * walk stopped.  Arrays: logits [B][T][V] and draft [B][K][V] float32,
+ * tokens [B][T], parent/depth/rank [T], u [B][T][u_stride] (u_stride > the
+ * largest child count).  Outputs accept_len [B], accepted_nodes [B][K+1]
+ * (-1 padded), next_token [B]; margin [B] (nullable) = the smallest relative
+ * gap |u q - p| / max(p, q) of the tests made and of the final draw to a
+ * running-sum boundary (a diagnostic of how close float rounding came to
+ * changing a decision).  Returns 0, or -1 on bad arguments. */
+int orc_rejection_tree(const float* logits, const float* draft,
+                       const int32_t* tokens, const int32_t* parent,
+                       const int32_t* depth, const int32_t* rank, int T,
+                       int K, int B, int V, double temperature,
+                       const float* u, int u_stride, int32_t* accept_len,
+                       int32_t* accepted_nodes, int32_t* next_token,
+                       double* margin);
+
 #ifdef __cplusplus
 }
 #endif

@@ -619,3 +619,124 @@ def test_rejection_emits_target_for_random_pairs(orc):
         assert abs(beta - np.minimum(p, q).sum()) < 1e-14
     out, beta = orc.rejection_emit(p, p)
     assert abs(beta - 1.0) < 1e-12 and np.allclose(out, p, atol=1e-14)
+
+
+# --------------------------------------------- rejection sampling over the tree
+
+def _cart_tree(orc, s):
+    n = sum(int(np.prod(s[:k])) for k in range(1, len(s) + 1))
+    paths, plen = orc.tree_cartesian(list(s), n)
+    return orc.tree_compile(paths, plen, len(s))
+
+
+def _first_tokens(r, tokens, n_emit):
+    """The first n_emit emitted tokens of each trial: the accepted path's tokens
+    (after the root), then the final draw."""
+    B = len(r["accept_len"])
+    out = np.full((B, n_emit), -1, np.int64)
+    for b in range(B):
+        seq = [tokens[b, n] for n in r["accepted_nodes"][b, 1:r["accept_len"][b] + 1]] + [r["next_token"][b]]
+        out[b, :min(n_emit, len(seq))] = seq[:n_emit]
+    return out
+
+
+def test_rejection_tree_two_token_example_exact(orc):
+    """The worked two-token example (p = (0.6, 0.4), q = (0.8, 0.2)) on a root with
+    one child drafted from q: integrating the child's token over q and both
+    uniforms over a midpoint grid gives the emitted distribution p."""
+    g = gold("rejection_two_token.json")
+    p, q = np.array(g["p"]), np.array(g["q"])
+    t = _cart_tree(orc, (1,))
+    N = 300
+    uu = (np.arange(N) + 0.5) / N
+    U1, U2 = np.meshgrid(uu, uu, indexing="ij")
+    trials = []
+    for x in (0, 1):
+        B = N * N
+        u = np.zeros((B, 2, 2), np.float32)
+        u[:, 0, 0] = U1.ravel()   # the child's test
+        u[:, 0, 1] = U2.ravel()   # final draw after a rejection at the root
+        u[:, 1, 0] = U2.ravel()   # final draw at the accepted (childless) child
+        logits = np.broadcast_to(np.log(p).astype(np.float32), (B, 2, 2)).copy()
+        draft = np.broadcast_to(np.log(q).astype(np.float32), (B, 1, 2)).copy()
+        tokens = np.zeros((B, 2), np.int32)
+        tokens[:, 1] = x
+        r = orc.rejection_tree(logits, draft, tokens, t, 1.0, u)
+        first = _first_tokens(r, tokens, 1)[:, 0]
+        trials.append((q[x], np.bincount(first, minlength=2) / B))
+    emitted = sum(w * h for w, h in trials)
+    assert np.abs(emitted - p).max() <= 2.0 / N
+    # with the child fixed to token 0 (not drafted from q) the rule emits (0.75, 0.25)
+    assert np.abs(trials[0][1] - np.array([0.75, 0.25])).max() <= 2.0 / N
+
+
+def test_rejection_tree_siblings_lossless(orc):
+    """Three siblings drafted independently from q, tried in rank order with
+    the residual update: the first emitted token is distributed as p
+    (Monte Carlo, 5 sigma)."""
+    rng = np.random.default_rng(23)
+    V, m, B = 5, 3, 120000
+    p = rng.random(V) ** 2; p /= p.sum()
+    q = rng.random(V); q /= q.sum()
+    t = _cart_tree(orc, (m,))
+    logits = np.broadcast_to(np.log(p).astype(np.float32), (B, t.T, V)).copy()
+    draft = np.broadcast_to(np.log(q).astype(np.float32), (B, 1, V)).copy()
+    tokens = np.zeros((B, t.T), np.int32)
+    tokens[:, 1:] = rng.choice(V, size=(B, m), p=q)
+    u = rng.random((B, t.T, m + 1)).astype(np.float32)
+    r = orc.rejection_tree(logits, draft, tokens, t, 1.0, u)
+    first = _first_tokens(r, tokens, 1)[:, 0]
+    emp = np.bincount(first, minlength=V) / B
+    assert np.all(np.abs(emp - p) <= 5 * np.sqrt(p * (1 - p) / B) + 1e-12)
+    # a rejected chain can end on the draw: some trials accept nothing
+    assert 0 < np.mean(r["accept_len"] == 0) < 1
+
+
+def test_rejection_tree_depth_two_lossless(orc):
+    """Root -> two children -> two children each, every level drafted from its
+    own q, the target at a node a function of its token: the first two emitted
+    tokens are distributed as p_root(x1) * p_x1(x2)."""
+    rng = np.random.default_rng(29)
+    V, B = 3, 200000
+    t = _cart_tree(orc, (2, 2))
+    p_root = rng.random(V); p_root /= p_root.sum()
+    table = rng.random((V, V)); table /= table.sum(1, keepdims=True)   # target after token x
+    q1 = rng.random(V); q1 /= q1.sum()
+    q2 = rng.random(V); q2 /= q2.sum()
+    tokens = np.zeros((B, t.T), np.int32)
+    for n in range(1, t.T):
+        tokens[:, n] = rng.choice(V, size=B, p=q1 if t.depth[n] == 1 else q2)
+    logits = np.zeros((B, t.T, V), np.float32)
+    logits[:, 0] = np.log(p_root)
+    for n in range(1, t.T):
+        logits[:, n] = np.log(table[tokens[:, n]])
+    draft = np.zeros((B, 2, V), np.float32)
+    draft[:, 0], draft[:, 1] = np.log(q1), np.log(q2)
+    u = rng.random((B, t.T, 3)).astype(np.float32)
+    r = orc.rejection_tree(logits, draft, tokens, t, 1.0, u)
+    f = _first_tokens(r, tokens, 2)
+    # a trial that stopped after one token continues in the next step, whose
+    # root row is the target after that token: draw it from there
+    short = f[:, 1] < 0
+    cdf = np.cumsum(table[f[short, 0]], axis=1)
+    f[short, 1] = (rng.random(short.sum())[:, None] >= cdf).sum(1)
+    joint = np.zeros((V, V))
+    np.add.at(joint, (f[:, 0], f[:, 1]), 1.0)
+    joint /= B
+    want = p_root[:, None] * table
+    assert np.all(np.abs(joint - want) <= 5 * np.sqrt(want * (1 - want) / B) + 1e-12)
+
+
+def test_rejection_tree_draft_equals_target(orc):
+    """q = p: every first child is accepted (u q < p for u < 1), down to a leaf."""
+    rng = np.random.default_rng(31)
+    V, B = 7, 500
+    t = _cart_tree(orc, (2, 2, 2))
+    z = rng.normal(size=V).astype(np.float32)
+    logits = np.broadcast_to(z, (B, t.T, V)).copy()
+    draft = np.broadcast_to(z, (B, 3, V)).copy()
+    tokens = rng.integers(0, V, (B, t.T)).astype(np.int32)
+    u = rng.random((B, t.T, 3)).astype(np.float32)
+    r = orc.rejection_tree(logits, draft, tokens, t, 0.7, u)
+    assert np.all(r["accept_len"] == 3)
+    assert np.all(r["accepted_nodes"][:, 1] == 1)
