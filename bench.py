@@ -336,14 +336,51 @@ def run_native(args, w, rank, world, local_rank):
     e2e = None
     if not args.no_e2e:
         e2e = measure_e2e(args, w, st, x, xh, prefix0, s, s2, s3, torch, M)
+    rej = measure_rejection(st, x, s, torch, M) if world == 1 else None
     dloop = None
     if args.loop_steps > 0 and world == 1:
         dloop = measure_loop(args, w, dev, torch, M)
 
     return dict(ms_step=ms_step, ms_events_step=ms_events / args.steps, per_call_ms=per_call, clocks=clocks,
-                dloop=dloop,
+                dloop=dloop, rej=rej,
                 T=T, s_heads=st.s_heads, L_list=L_list, accept_len=accept_len, e2e=e2e,
                 launches=st.launches_per_step * args.steps, tree=ht)
+
+
+def measure_rejection(st, x, s, torch, M, reps=20):
+    """medusa_accept_rejection on the step's own logits, with the heads'
+    logits as the drafts and device uniforms: time per call (graph of reps
+    calls) beside the greedy / typical acceptance of the same step."""
+    B, T, V = st.logits.shape
+    g = torch.Generator(device=st.logits.device).manual_seed(7)
+    u = torch.rand((B, T, 17), generator=g, device=st.logits.device)
+    al = torch.zeros(B, dtype=torch.int32, device=u.device)
+    an = torch.zeros((B, st.tree.K + 1), dtype=torch.int32, device=u.device)
+    nt = torch.zeros(B, dtype=torch.int32, device=u.device)
+    ws = torch.empty(M.medusa_accept_rejection_workspace_size(B, V), dtype=torch.uint8, device=u.device)
+    tau = st.temperature if st.mode == 1 else 1.0
+
+    def call():
+        M.medusa_accept_rejection(st.logits, st.head_logits, x["tokens"], st.tree, tau, u, al, an, nt, ws, st.err, s)
+
+    with torch.cuda.stream(s):
+        call()
+    torch.cuda.synchronize()
+    gr = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(gr, stream=s):
+        for _ in range(reps):
+            call()
+    ts = []
+    for _ in range(5):
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        with torch.cuda.stream(s):
+            e0.record(s)
+            gr.replay()
+            e1.record(s)
+        torch.cuda.synchronize()
+        ts.append(e0.elapsed_time(e1) / reps)
+    return {"ms_per_call": statistics.median(ts), "temperature": tau, "accept_len": al.cpu().tolist(),
+            "drafts": "the step's tree tokens, q = the heads' softmax, uniforms from the device generator"}
 
 
 def measure_loop(args, w, dev, torch, M):
@@ -629,6 +666,8 @@ def main():
         line["e2e"] = r["e2e"]
     if r["dloop"] is not None:
         line["decode_loop"] = r["dloop"]
+    if r["rej"] is not None:
+        line["rejection_accept"] = r["rej"]
     if world == 1 and not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline(w)
     print(json.dumps(line), flush=True)

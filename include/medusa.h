@@ -351,6 +351,42 @@ int medusa_build_candidates(const int32_t* next_root, const int32_t* topk,
                             int s_max, int K, const medusa_tree_t* tree,
                             int B, int32_t* tokens, void* stream);
 
+/* Scratch bytes medusa_accept_rejection needs (B rows of V floats). */
+size_t medusa_accept_rejection_workspace_size(int B, int V);
+
+/* Rejection-sampling acceptance over the tree, an alternative to
+ * medusa_accept's greedy / typical rules that keeps the target
+ * distribution ([MED] Method 5; [SPEC] introduction and "Maths": accept a
+ * drafted x with probability min(1, p(x)/q(x)), at a rejection draw from the
+ * normalised residual [p - q]_+).  Walked along the tree: from the root, the
+ * children of the current node are tried in rank order, child n (depth k,
+ * token x = tokens[b][n]) being accepted iff
+ *     uniforms[b][cur][j] * q_k(x) < p(x)        (j = its position in that order)
+ * with p = softmax(logits[b][cur] / temperature), replaced by the normalised
+ * residual after each rejection, and q_k = softmax(draft_logits[b][k-1] /
+ * temperature), the distribution of the head that drafted depth k.  The walk
+ * moves to the accepted child and repeats; where it stops (no child accepted,
+ * or a node without children) the next token is the first x, in vocabulary
+ * order, whose running sum of p exceeds uniforms[b][cur][m], m = the number
+ * of children of that node.  Lossless when the children of every node are
+ * independent draws from q_k.
+ * logits: device [B][T][V] float32; draft_logits: device [B][Kd][V] float32
+ * (Kd >= tree->K; e.g. medusa_heads_topk's head_logits of the previous
+ * step); tokens: device [B][T]; uniforms: device [B][T][u_stride] in [0, 1),
+ * u_stride greater than every node's child count (MEDUSA_MAX_S + 1 always
+ * suffices).  Outputs (device): accept_len [B], accepted_nodes [B][K+1] (root
+ * .. last accepted node, -1 padded), next_token [B] (the token drawn after the
+ * accepted path).  B may be up to 65535 here.  A draft token outside [0, V)
+ * is never accepted and raises MEDUSA_DEVERR_TOKEN. */
+int medusa_accept_rejection(const float* logits, const float* draft_logits,
+                            int Kd, const int32_t* tokens,
+                            const medusa_tree_t* tree, int B, int V,
+                            float temperature, const float* uniforms,
+                            int u_stride, int32_t* accept_len,
+                            int32_t* accepted_nodes, int32_t* next_token,
+                            void* workspace, size_t workspace_bytes,
+                            int32_t* err, void* stream);
+
 /* Append a step's output tokens ([MED] box step 6: "append the root plus the
  * accepted tokens", 1 + accept_len of them):
  *   out[b][out_len[b] + j] = tokens[b][accepted_nodes[b][j]], j = 0..accept_len[b]

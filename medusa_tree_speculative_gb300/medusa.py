@@ -60,6 +60,8 @@ _SIGS = {
     "medusa_build_candidates": (I, [P, P, I, I, TREE, I, P, P]),
     "medusa_heads_hidden": (I, [P, I, P, I, P, P, I, I, I, P, P, P]),
     "medusa_append_tokens": (I, [P, P, P, I, I, I, P, P, I, P, P]),
+    "medusa_accept_rejection_workspace_size": (SZ, [I, I]),
+    "medusa_accept_rejection": (I, [P, P, I, P, TREE, I, I, F, P, I, P, P, P, P, SZ, P, P]),
     "medusa_standin_embed": (I, [P, I, P, I, I, I, P, P, P]),
     "medusa_heads_logits_topk_workspace_size": (SZ, [I, I, I, I]),
     "medusa_heads_logits_topk": (I, [P, I, P, P, P, I, I, I, I, I, P, P, I, P, SZ, P, P]),
@@ -342,3 +344,18 @@ def medusa_standin_embed(tokens, emb, hidden, err=None, stream=None):
     V, d = emb.shape
     _check(_lib.medusa_standin_embed(_ptr(tokens), tokens.numel(), _ptr(emb), V, d, _dtype(emb), _ptr(hidden),
                                      _ptr(err), _stream(stream)), "medusa_standin_embed")
+
+
+def medusa_accept_rejection_workspace_size(B, V) -> int:
+    return int(_lib.medusa_accept_rejection_workspace_size(B, V))
+
+
+def medusa_accept_rejection(logits, draft_logits, tokens, tree: DeviceTree, temperature, uniforms, accept_len,
+                            accepted_nodes, next_token, workspace, err=None, stream=None):
+    """Rejection-sampling acceptance over the tree (uniforms [B][T][u_stride] are inputs)."""
+    B, T, V = logits.shape
+    _check(_lib.medusa_accept_rejection(_ptr(logits), _ptr(draft_logits), draft_logits.shape[1], _ptr(tokens),
+                                        tree.ref, B, V, float(temperature), _ptr(uniforms), uniforms.shape[2],
+                                        _ptr(accept_len), _ptr(accepted_nodes), _ptr(next_token), _ptr(workspace),
+                                        workspace.numel() * workspace.element_size(), _ptr(err),
+                                        _stream(stream)), "medusa_accept_rejection")
