@@ -50,6 +50,11 @@ def parse_args():
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--loop-steps", type=int, default=48,
                     help="chained verify steps on the device around the stand-in backbone (0: skip)")
+    ap.add_argument("--accept", choices=["separate", "fused"], default="separate",
+                    help="acceptance reading the logits (separate) or the row statistics fused into the LM "
+                         "head's epilogue (fused)")
+    ap.add_argument("--no-logits", dest="logits", action="store_false",
+                    help="with --accept fused and greedy acceptance: do not write the logits")
     ap.add_argument("--heads", choices=["split", "fused"], default="fused",
                     help="heads' W1 over every tree row beside the acceptance, then W2 on the accepted "
                          "row (split), or both projections on the accepted row after it (fused)")
@@ -60,7 +65,8 @@ def parse_args():
 
 # ------------------------------------------------------------------ bytes --
 
-def algorithmic_bytes(w: dict, T: int, s_heads, L_list, split: bool) -> dict:
+def algorithmic_bytes(w: dict, T: int, s_heads, L_list, split: bool, fused_accept: bool = False,
+                      logits: bool = True) -> dict:
     """Bytes each call must move at least once per step (weights once, KV
     prefix once, activations and logits once each way)."""
     e = 2 if w["dtype"] == "bf16" else 4
@@ -71,8 +77,14 @@ def algorithmic_bytes(w: dict, T: int, s_heads, L_list, split: bool) -> dict:
             + 3 * B * T * H * Dh * e       # q, k_new, v_new read
             + 2 * B * T * H * Dh * e       # K', V appended
             + B * T * H * Dh * e)          # out written
-    lm = V * d * e + B * T * d * e + B * T * V * 4
+    lm = V * d * e + B * T * d * e + (B * T * V * 4 if logits else 0)
     accept = B * T * V * 4
+    if fused_accept:  # per-group row records instead of a logits pass
+        from medusa_tree_speculative_gb300 import medusa as M
+
+        rec = M.medusa_lm_head_stat_groups(B * T, V) * B * T * 16
+        lm += rec
+        accept = rec
     compact = 2 * 2 * B * (w["K"] + 1) * H * Dh * e
     heads = k_used * (d * d + V * d) * e + B * k_used * V * 4 * 2
     # split heads: W1 over every tree row (u of all rows written), then W2 on the accepted row
@@ -211,14 +223,21 @@ def step_calls(st, x, s):
     c = [("tree_attn", lambda: M.medusa_tree_attn(
             x["q"], x["k_new"], x["v_new"], x["k_cache"], x["v_cache"], x["seq_start"], x["prefix_len"],
             x["seq_cap"], st.tree, st.max_prefix, st.rope_theta, st.scale, st.out, st.ws_attn, st.err, s)),
-         ("lm_head_verify", lambda: M.medusa_lm_head_verify(x["hidden"], st.w_lm_run, st.logits, None, st.err, s,
-                                                            layout=st.w_layout))]
+         ("lm_head_verify", (lambda: M.medusa_lm_head_verify_stats(
+             x["hidden"], st.w_lm_run, st.logits if st.write_logits else None, st.stats, st.mode, st.temperature,
+             st.logits.shape[-1], st.err, s, layout=st.w_layout)) if st.accept == "fused" else
+          (lambda: M.medusa_lm_head_verify(x["hidden"], st.w_lm_run, st.logits, None, st.err, s,
+                                           layout=st.w_layout)))]
     if st.heads == "split":
         c.append(("heads_hidden", lambda: M.medusa_heads_hidden(x["hidden"], st.w1_run, st.b1, st.s_heads, st.u_all,
                                                                 st.err, s, layout=st.w1_layout)))
-    c += [("accept", lambda: M.medusa_accept(st.logits, x["tokens"], st.tree, st.mode, st.temperature, st.eps,
-                                             st.delta, st.accept_len, st.accepted_nodes, st.next_root,
-                                             st.best_node, st.best_logp, st.ws_accept, st.err, s)),
+    c += [("accept", (lambda: M.medusa_accept_stats(
+              st.stats, st.stat_groups, st.logits if st.write_logits else None, x["tokens"], st.tree, st.mode,
+              st.temperature, st.eps, st.delta, st.logits.shape[-1], st.accept_len, st.accepted_nodes, st.next_root,
+              st.best_node, st.best_logp, st.err, s)) if st.accept == "fused" else
+           (lambda: M.medusa_accept(st.logits, x["tokens"], st.tree, st.mode, st.temperature, st.eps, st.delta,
+                                    st.accept_len, st.accepted_nodes, st.next_root, st.best_node, st.best_logp,
+                                    st.ws_accept, st.err, s))),
           ("kv_compact", lambda: M.medusa_kv_compact(x["k_cache"], x["v_cache"], x["seq_start"], x["prefix_len"],
                                                      st.accepted_nodes, st.accept_len, st.tree.K, st.src_slots,
                                                      st.err, s))]
@@ -256,7 +275,8 @@ def run_native(args, w, rank, world, local_rank):
     for k, v in xh.items():
         x[k] = step.host_to_torch(v, dt).to(dev) if v.dtype in (np.uint16, np.float32) else torch.from_numpy(v).to(dev)
     L_list = xh["prefix_len"].copy()
-    st = step.VerifyStep(w, wd, tree, max_prefix=int(L_list.max()), device=dev, heads=args.heads)
+    st = step.VerifyStep(w, wd, tree, max_prefix=int(L_list.max()), device=dev, heads=args.heads,
+                         accept=args.accept, write_logits=args.logits)
     plant(w, tree, st, x, args.plant_depth, torch)
     prefix0 = x["prefix_len"].clone()
     s = torch.cuda.Stream(device=dev)
@@ -632,7 +652,8 @@ def main():
     if rank != 0:
         return
     peaks = load_peaks()
-    by = algorithmic_bytes(w, r["T"], r["s_heads"], r["L_list"], args.heads == "split")
+    by = algorithmic_bytes(w, r["T"], r["s_heads"], r["L_list"], args.heads == "split", args.accept == "fused",
+                           args.logits or w["mode"] == "typical")
     fl = algorithmic_flops(w, r["T"], r["s_heads"], r["L_list"])
     ms = r["ms_step"]
     value = world * 1e3 / ms
@@ -646,7 +667,8 @@ def main():
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": w["dtype"], "data": "synthetic (seeded random weights and activations)",
-        "config": config_dict(w, {"parallelism": f"replicas{world}" if world > 1 else "single-gpu", "attn_branch": args.attn_branch,
+        "config": config_dict(w, {"parallelism": f"replicas{world}" if world > 1 else "single-gpu", "attn_branch": args.attn_branch, "heads": args.heads, "accept_impl": args.accept,
+                                  "logits_written": bool(args.logits or w["mode"] == "typical"),
                                   "T_rows": r["T"], "s": r["s_heads"], "planted_accept_len": r["accept_len"]}),
         "roofline": {"bound": "hbm", "kernel": f"medusa_{dom}", "achieved": achieved, "peak": peaks["hbm_gbs"],
                      "unit": "GB/s", "frac": achieved / peaks["hbm_gbs"], "traffic": traffic,

@@ -209,6 +209,39 @@ int medusa_lm_head_verify(const void* hidden, const void* w_lm, float* logits,
                           medusa_w_layout w_layout, void* workspace,
                           size_t workspace_bytes, int32_t* err, void* stream);
 
+/* The LM head with the acceptance's row statistics fused into its epilogue
+ * (the logits round trip skipped).  For every tree row r and vocabulary group
+ * g (a run of 128 or 256 vocabulary rows; medusa_lm_head_stat_groups(rows, V)
+ * groups on the current device) one 16-byte record
+ *   { max_v z[r][v], its index (lowest among equal maxima),
+ *     sum_v e^(y_v - m), sum_v e^(y_v - m)(y_v - m) }   over v in g,
+ * y = z / temperature, m = max y (the sums are 0 in greedy mode), stored as
+ * float4 at stats[g * rows + r] (the index's bits in the second float).
+ * medusa_accept_stats merges them.  logits (device [rows][V] float32) is
+ * optional in greedy mode (NULL: not written) and required in typical mode
+ * (p^(token) is read from it).  mode 0 greedy, 1 typical.  bf16 only; the
+ * other arguments as medusa_lm_head_verify.  Returns MEDUSA_ERR_CAPACITY if
+ * stats_bytes < groups * rows * 16. */
+int medusa_lm_head_stat_groups(int rows, int V);
+int medusa_lm_head_verify_stats(const void* hidden, const void* w_lm,
+                                float* logits, int rows, int d, int V,
+                                medusa_dtype dtype, medusa_w_layout w_layout,
+                                int mode, float temperature, void* stats,
+                                size_t stats_bytes, int32_t* err,
+                                void* stream);
+
+/* medusa_accept from the statistics of medusa_lm_head_verify_stats (groups =
+ * medusa_lm_head_stat_groups(B*T, V), stats covering B*T rows): the same
+ * rules, ties and outputs as medusa_accept, one kernel, no workspace;
+ * logits (device [B][T][V]) is read only in typical mode. */
+int medusa_accept_stats(const void* stats, int groups, const float* logits,
+                        const int32_t* tokens, const medusa_tree_t* tree,
+                        int B, int V, int mode, float temperature, float eps,
+                        float delta, int32_t* accept_len,
+                        int32_t* accepted_nodes, int32_t* next_root,
+                        int32_t* best_node, float* best_logp, int32_t* err,
+                        void* stream);
+
 /* Scratch bytes medusa_accept needs. */
 size_t medusa_accept_workspace_size(int B, int T);
 

@@ -21,6 +21,7 @@
 
 #include "common.cuh"
 #include "internal.h"
+#include "stats.cuh"
 
 namespace medusa {
 namespace {
@@ -140,11 +141,13 @@ __global__ void __launch_bounds__(kRowThreads) accept_rowstat_kernel(const float
   }
 }
 
-__global__ void __launch_bounds__(MEDUSA_MAX_T) accept_select_kernel(
-    const float* logits, const int32_t* tokens, medusa_tree_t tree, int V, int mode, float inv_temp,
-    float eps, float delta, const RowStat* stats, int32_t* accept_len, int32_t* accepted_nodes,
-    int32_t* next_root, int32_t* best_node, float* best_logp, int32_t* err) {
-  const int b = blockIdx.x, c = threadIdx.x;
+// Sequence b's decisions from its rows' statistics `st` ([T], global or
+// shared memory); one thread per node, any block size >= T.
+MDEV void select_body(int b, const float* logits, const int32_t* tokens, const medusa_tree_t& tree, int V,
+                      int mode, float inv_temp, float eps, float delta, const RowStat* st, int32_t* accept_len,
+                      int32_t* accepted_nodes, int32_t* next_root, int32_t* best_node, float* best_logp,
+                      int32_t* err) {
+  const int c = threadIdx.x;
   const int T = tree.T;
   __shared__ uint8_t ok[MEDUSA_MAX_T];
   __shared__ float lp[MEDUSA_MAX_T];
@@ -161,7 +164,7 @@ __global__ void __launch_bounds__(MEDUSA_MAX_T) accept_select_kernel(
   if (c < T) {
     depth_c = tree.depth[c];
     parent_c = tree.parent[c];
-    amax[c] = stats[(int64_t)b * T + c].argmax;
+    amax[c] = st[c].argmax;
     if (c == 0) {
       pass = true;
       depth_c = 0;
@@ -172,15 +175,15 @@ __global__ void __launch_bounds__(MEDUSA_MAX_T) accept_select_kernel(
       depth_c = 0;
     } else {
       const int tok = tokens[(int64_t)b * T + c];
-      const RowStat st = stats[(int64_t)b * T + parent_c];
+      const RowStat rp = st[parent_c];
       if (mode == 0) {
-        pass = tok == st.argmax;
+        pass = tok == rp.argmax;
       } else if (tok < 0 || tok >= V) {
         set_err(err, MEDUSA_DEVERR_TOKEN);
       } else {
         const float zt = logits[((int64_t)b * T + parent_c) * V + tok] * inv_temp;
-        lpc = zt - st.lse;
-        const float thr = fminf(eps, delta * expf(-st.entropy));
+        lpc = zt - rp.lse;
+        const float thr = fminf(eps, delta * expf(-rp.entropy));
         pass = expf(lpc) > thr;
       }
     }
@@ -242,6 +245,55 @@ __global__ void __launch_bounds__(MEDUSA_MAX_T) accept_select_kernel(
     best_node[b] = bi;
     if (best_logp) best_logp[b] = mode == 1 ? lp[bi] : 0.f;
   }
+}
+
+__global__ void __launch_bounds__(MEDUSA_MAX_T) accept_select_kernel(
+    const float* logits, const int32_t* tokens, medusa_tree_t tree, int V, int mode, float inv_temp,
+    float eps, float delta, const RowStat* stats, int32_t* accept_len, int32_t* accepted_nodes,
+    int32_t* next_root, int32_t* best_node, float* best_logp, int32_t* err) {
+  const int b = blockIdx.x;
+  select_body(b, logits, tokens, tree, V, mode, inv_temp, eps, delta, stats + (int64_t)b * tree.T, accept_len,
+              accepted_nodes, next_root, best_node, best_logp, err);
+}
+
+// Acceptance from the LM head's fused statistics (medusa_lm_head_verify_stats):
+// the rows' per-group records are merged (a fixed share of the groups per
+// thread, then the shares in order), then the same decisions as above.
+constexpr int kStatThreads = 1024;
+
+__global__ void __launch_bounds__(kStatThreads) accept_stats_kernel(
+    const float4* part, int groups, int rows_total, const float* logits, const int32_t* tokens,
+    medusa_tree_t tree, int V, int mode, float inv_temp, float eps, float delta, int32_t* accept_len,
+    int32_t* accepted_nodes, int32_t* next_root, int32_t* best_node, float* best_logp, int32_t* err) {
+  const int b = blockIdx.x, tid = threadIdx.x, T = tree.T;
+  __shared__ RowStat rs[MEDUSA_MAX_T];
+  __shared__ float4 share[kStatThreads];
+  const int P = max(1, kStatThreads / T);  // threads per row
+  const int r = tid / P, sh = tid % P;
+  StatRec m = stat_empty();
+  if (r < T)
+    for (int g = sh; g < groups; g += P) {
+      const float4 x = __ldg(part + (int64_t)g * rows_total + (int64_t)b * T + r);
+      m = mode == 1 ? stat_merge<true>(m, stat_load(x), inv_temp) : stat_merge<false>(m, stat_load(x), inv_temp);
+    }
+  share[tid] = stat_store(m);
+  __syncthreads();
+  if (r < T && sh == 0) {
+    StatRec a = stat_empty();
+    for (int q = 0; q < P; ++q)
+      a = mode == 1 ? stat_merge<true>(a, stat_load(share[tid + q]), inv_temp)
+                    : stat_merge<false>(a, stat_load(share[tid + q]), inv_temp);
+    RowStat o;
+    o.argmax = a.i;
+    // H = log S - A / S  (p^_v = e^(y_v - m) / S, m = max y)
+    o.lse = mode == 1 ? a.v * inv_temp + logf(a.S) : 0.f;
+    o.entropy = mode == 1 ? logf(a.S) - a.A / a.S : 0.f;
+    o.pad = 0.f;
+    rs[r] = o;
+  }
+  __syncthreads();
+  select_body(b, logits, tokens, tree, V, mode, inv_temp, eps, delta, rs, accept_len, accepted_nodes, next_root,
+              best_node, best_logp, err);
 }
 
 // Scratch of medusa_accept_noalloc: one row record per (sequence, tree row)
@@ -331,4 +383,25 @@ extern "C" int medusa_accept_noalloc(const float* logits, const int32_t* tokens,
   return medusa_accept(logits, tokens, tree, B, V, mode, temperature, eps, delta, accept_len, accepted_nodes,
                        next_root, best_node, best_logp, scratch, sizeof(RowStat) * (size_t)kNoAllocRows, err,
                        stream);
+}
+
+extern "C" int medusa_accept_stats(const void* stats, int groups, const float* logits, const int32_t* tokens,
+                                   const medusa_tree_t* tree, int B, int V, int mode, float temperature, float eps,
+                                   float delta, int32_t* accept_len, int32_t* accepted_nodes, int32_t* next_root,
+                                   int32_t* best_node, float* best_logp, int32_t* err, void* stream) {
+  const char* fn = "medusa_accept_stats";
+  if (int rc = check_tree(tree, fn)) return rc;
+  if (!stats || !tokens || !accept_len || !accepted_nodes || !next_root || !best_node)
+    return fail(MEDUSA_ERR_INVALID, "%s: NULL tensor", fn);
+  if (B < 1 || B > MEDUSA_MAX_B || V < 1 || groups < 1)
+    return fail(MEDUSA_ERR_INVALID, "%s: B=%d V=%d groups=%d", fn, B, V, groups);
+  if (mode != 0 && mode != 1) return fail(MEDUSA_ERR_INVALID, "%s: mode %d", fn, mode);
+  if (mode == 1 && !(temperature > 0.f)) return fail(MEDUSA_ERR_INVALID, "%s: temperature must be > 0", fn);
+  if (mode == 1 && !logits) return fail(MEDUSA_ERR_INVALID, "%s: typical acceptance needs the logits", fn);
+  if (reinterpret_cast<uintptr_t>(stats) % 16) return fail(MEDUSA_ERR_INVALID, "%s: stats not 16-byte aligned", fn);
+  const float inv_temp = mode == 1 ? 1.f / temperature : 1.f;
+  launch_kernel(accept_stats_kernel, dim3(B), dim3(kStatThreads), 0, as_stream(stream),
+                static_cast<const float4*>(stats), groups, B * tree->T, logits, tokens, *tree, V, mode, inv_temp, eps,
+                delta, accept_len, accepted_nodes, next_root, best_node, best_logp, err);
+  return check_launch(fn);
 }

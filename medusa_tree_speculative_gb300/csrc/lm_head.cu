@@ -44,6 +44,7 @@
 #include "common.cuh"
 #include "internal.h"
 #include "sm100.cuh"
+#include "stats.cuh"
 
 namespace medusa {
 namespace {
@@ -79,8 +80,72 @@ struct LmArgs {
   int K;                        // heads in u's layout
   int tpr;                      // 128-row tiles per head (d / 128)
   int32_t heads[MEDUSA_MAX_K];  // slot -> head id
+  // mode 0, acceptance statistics (fused epilogue): per (vocabulary group,
+  // row) a record {max logit, its index (lowest on ties), and for typical
+  // acceptance sum e^(y-m), sum e^(y-m)(y-m) with y = logit * inv_temp,
+  // m = max y}; stat_mode 0 none, 1 argmax, 2 argmax + softmax sums
+  float4* stats;
+  int stat_mode;
+  float inv_temp;
+  int write_logits;
+  uint32_t part_off;  // byte offset of the per-warp partial records in shared memory
   int32_t* err;
 };
+
+// ---- acceptance statistics (records and their merge: stats.cuh)
+
+template <bool TYP>
+MDEV StatRec rec_shfl(const StatRec& x, int mask) {
+  StatRec r;
+  r.v = __shfl_xor_sync(0xffffffffu, x.v, mask);
+  r.i = __shfl_xor_sync(0xffffffffu, x.i, mask);
+  r.S = TYP ? __shfl_xor_sync(0xffffffffu, x.S, mask) : 0.f;
+  r.A = TYP ? __shfl_xor_sync(0xffffffffu, x.A, mask) : 0.f;
+  return r;
+}
+
+// One halving step of the transpose-reduce: lanes with (lane & D) keep the
+// upper half of their N records and send the lower half to lane ^ D.
+template <bool TYP, int N, int D>
+MDEV void tr_step(StatRec (&x)[16], int lane, float inv_temp) {
+  const bool hi = lane & D;
+#pragma unroll
+  for (int j = 0; j < N / 2; ++j) {
+    const StatRec keep = hi ? x[j + N / 2] : x[j];
+    const StatRec send = hi ? x[j] : x[j + N / 2];
+    x[j] = stat_merge<TYP>(keep, rec_shfl<TYP>(send, D), inv_temp);
+  }
+}
+
+// 32 lanes x 16 columns -> each column reduced over the 32 lanes; lane L (and
+// L ^ 1) ends with column 8 b4 + 4 b3 + 2 b2 + b1 of L's bits.  16 shuffles
+// per field instead of 80 for column-by-column butterflies.
+template <bool TYP>
+MDEV StatRec transpose_reduce(StatRec (&x)[16], int lane, float inv_temp) {
+  tr_step<TYP, 16, 16>(x, lane, inv_temp);
+  tr_step<TYP, 8, 8>(x, lane, inv_temp);
+  tr_step<TYP, 4, 4>(x, lane, inv_temp);
+  tr_step<TYP, 2, 2>(x, lane, inv_temp);
+  return stat_merge<TYP>(x[0], rec_shfl<TYP>(x[0], 1), inv_temp);
+}
+MDEV int tr_column(int lane) {
+  return ((lane >> 4) & 1) * 8 + ((lane >> 3) & 1) * 4 + ((lane >> 2) & 1) * 2 + ((lane >> 1) & 1);
+}
+
+// Named barrier 1 over the four epilogue warps, OR-reducing a predicate.
+MDEV bool epilogue_any(bool p) {
+  uint32_t r;
+  asm volatile(
+      "{\n\t.reg .pred p, q;\n\t"
+      "setp.ne.u32 p, %1, 0;\n\t"
+      "bar.red.or.pred q, 1, 128, p;\n\t"
+      "selp.u32 %0, 1, 0, q;\n\t}\n"
+      : "=r"(r)
+      : "r"((uint32_t)p)
+      : "memory");
+  return r != 0;
+}
+MDEV void epilogue_sync() { asm volatile("bar.sync 1, 128;\n" ::: "memory"); }
 
 struct HeadSlots {
   int32_t id[MEDUSA_MAX_K];
@@ -102,6 +167,9 @@ MDEV bool wait_or_abort(uint64_t* bar, uint32_t parity, volatile int* abort_flag
   return false;
 }
 
+// STATS: the epilogue also produces the acceptance statistics (a separate
+// instantiation, so that the plain path keeps its registers and barriers).
+template <bool STATS>
 __global__ void __launch_bounds__(kThreads, 1)
     lm_head_tc_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CUtensorMap tmH,
                       const __grid_constant__ LmArgs a) {
@@ -117,6 +185,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(tempty + 2);
   // mode 1: the residual tile hidden[r0 + i][j] of the current item, [nt][npad][128] bf16
   uint16_t* res = reinterpret_cast<uint16_t*>(smem + (size_t)a.stages * stage_bytes + 1024);
+  // acceptance statistics: partial records [nt][4 warps][npad]
+  float4* part = reinterpret_cast<float4*>(smem + a.part_off);
   __shared__ int s_abort;
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -246,7 +316,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int acc = local & 1;
       const uint32_t aph = (uint32_t)(local >> 1) & 1u;
       const bool got = wait_or_abort(&tfull[acc], aph, abort_flag);
-      if (__any_sync(0xffffffffu, !got)) {
+      // with statistics the four warps share named barriers, so they take one decision
+      if (STATS ? epilogue_any(!got) : __any_sync(0xffffffffu, !got)) {
         if (lane == 0) set_err(a.err, MEDUSA_DEVERR_TIMEOUT);
         break;
       }
@@ -261,12 +332,30 @@ __global__ void __launch_bounds__(kThreads, 1)
                                  (uint32_t)(t * a.npad + c * 16),
                              r);
           tmem_ld_wait();
+          if (STATS) {  // this warp's 32 vocabulary rows reduced per column
+            StatRec x[16];
+#pragma unroll
+            for (int i = 0; i < 16; ++i) {
+              const bool valid = v < a.V && r0 + c * 16 + i < a.rows;
+              x[i].v = valid ? __uint_as_float(r[i]) : -INFINITY;
+              x[i].i = v;
+              x[i].S = valid ? 1.f : 0.f;
+              x[i].A = 0.f;
+            }
+            const StatRec red = a.stat_mode == 2 ? transpose_reduce<true>(x, lane, a.inv_temp)
+                                             : transpose_reduce<false>(x, lane, a.inv_temp);
+            if (!(lane & 1))
+              part[(t * 4 + g) * a.npad + c * 16 + tr_column(lane)] =
+                  make_float4(red.v, __int_as_float(red.i), red.S, red.A);
+          }
           if (v < a.V) {
             if (a.mode == 0) {
+              if (a.write_logits) {
 #pragma unroll
-              for (int i = 0; i < 16; ++i) {
-                const int row = r0 + c * 16 + i;
-                if (row < a.rows) a.logits[(int64_t)row * a.V + v] = __uint_as_float(r[i]);
+                for (int i = 0; i < 16; ++i) {
+                  const int row = r0 + c * 16 + i;
+                  if (row < a.rows) a.logits[(int64_t)row * a.V + v] = __uint_as_float(r[i]);
+                }
               }
             } else {
               const int slot = v / a.d, j = v % a.d, k = a.heads[slot];
@@ -287,6 +376,20 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       tc_fence_before();
       mbar_arrive(&tempty[acc]);
+      if (STATS) {  // the item's record per row: merge the warps' and tiles' partials in a fixed order
+        epilogue_sync();
+        const int group = item / a.nchunks;
+        for (int e = threadIdx.x - 64; e < a.npad; e += 128) {
+          StatRec m = stat_empty();
+          for (int q = 0; q < a.nt * 4; ++q) {
+            const StatRec y = stat_load(part[q * a.npad + e]);
+            m = a.stat_mode == 2 ? stat_merge<true>(m, y, a.inv_temp) : stat_merge<false>(m, y, a.inv_temp);
+          }
+          if (r0 + e < a.rows)
+            a.stats[(int64_t)group * a.rows + r0 + e] = make_float4(m.v, __int_as_float(m.i), m.S, m.A);
+        }
+        epilogue_sync();
+      }
       if (a.mode == 1 && item + 1 < i1) {
         __syncwarp();
         load_res(item + 1);  // this warp's own slice of the tile: no other warp reads it
@@ -407,18 +510,26 @@ namespace {
 
 // Plan and launch the tensor-core GEMM: `a` carries the epilogue fields; the
 // weight tensor has `wrows` rows of d (row-major) or is its tile copy.
+// Work plan along M: row chunks of at most kMaxN (padded to 16), and whether
+// a work item is one tile or two adjacent tiles sharing each hidden k-block.
+void plan_tc(int rows, int ntiles, int& nchunks, int& npad, int& nt, int& ngroups) {
+  nchunks = (rows + kMaxN - 1) / kMaxN;
+  npad = ((rows + nchunks - 1) / nchunks + 15) / 16 * 16;
+  // two tiles per work item halve the hidden re-reads per weight byte; used
+  // while both accumulators of both tiles fit in TMEM
+  nt = (npad <= 128 && ntiles > sm_count()) ? 2 : 1;
+  ngroups = (ntiles + nt - 1) / nt;
+}
+
 int launch_tc(LmArgs& a, const void* w, bool tiled, int64_t wrows, const void* hidden, int rows, int d,
               cudaStream_t s, const char* fn) {
   a.rows = rows; a.d = d; a.tiled = tiled;
-  a.nchunks = (rows + kMaxN - 1) / kMaxN;
-  a.npad = ((rows + a.nchunks - 1) / a.nchunks + 15) / 16 * 16;
-  // two tiles per work item halve the hidden re-reads per weight byte; used
-  // while both accumulators of both tiles fit in TMEM
-  a.nt = (a.npad <= 128 && a.ntiles > sm_count()) ? 2 : 1;
-  a.ngroups = (a.ntiles + a.nt - 1) / a.nt;
+  plan_tc(rows, a.ntiles, a.nchunks, a.npad, a.nt, a.ngroups);
   const size_t stage_bytes = (size_t)a.nt * BM * BK * 2 + (size_t)a.npad * BK * 2;
   const size_t res_bytes = a.mode == 1 ? (size_t)a.nt * a.npad * BM * 2 : 0;
-  a.stages = (int)std::min<size_t>(8, (kSmemBudget - 1024 - 256 - res_bytes) / stage_bytes);
+  const size_t part_bytes = a.stat_mode ? (size_t)a.nt * 4 * a.npad * 16 : 0;
+  a.stages = (int)std::min<size_t>(8, (kSmemBudget - 1024 - 256 - res_bytes - part_bytes) / stage_bytes);
+  a.part_off = (uint32_t)align_up((size_t)a.stages * stage_bytes + 1024 + res_bytes, 16);
   uint32_t cols = 32;
   while (cols < (uint32_t)(2 * a.nt * a.npad)) cols <<= 1;
   a.tmem_cols = cols;
@@ -430,13 +541,14 @@ int launch_tc(LmArgs& a, const void* w, bool tiled, int64_t wrows, const void* h
                          : make_map(&tmW, w, (uint64_t)d, (uint64_t)wrows, BM);
   if (!okw || !make_map(&tmH, hidden, (uint64_t)d, (uint64_t)rows, (uint32_t)a.npad))
     return fail(MEDUSA_ERR_CUDA, "%s: cuTensorMapEncodeTiled failed", fn);
-  const size_t smem = 1024 + (size_t)a.stages * stage_bytes + 1024 + res_bytes;  // ring | barriers | residuals
-  cudaFuncSetAttribute(lm_head_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  const size_t smem = 1024 + a.part_off + part_bytes;  // ring | barriers | residuals | partial records
+  auto kern = a.stat_mode ? lm_head_tc_kernel<true> : lm_head_tc_kernel<false>;
+  cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   // balanced: every CTA gets ceil or floor of items / grid work items
   const int items = a.ngroups * a.nchunks;
   const int per_cta = (items + sm_count() - 1) / sm_count();
   const int grid = (items + per_cta - 1) / per_cta;
-  launch_kernel(lm_head_tc_kernel, dim3(grid), dim3(kThreads), smem, s, tmW, tmH, a);
+  launch_kernel(kern, dim3(grid), dim3(kThreads), smem, s, tmW, tmH, a);
   return check_launch(fn);
 }
 
@@ -482,6 +594,7 @@ extern "C" int medusa_lm_head_verify(const void* hidden, const void* w_lm, float
     LmArgs a{};
     a.logits = logits; a.V = V; a.err = err;
     a.mode = 0;
+    a.write_logits = 1;
     a.ntiles = (V + BM - 1) / BM;
     return launch_tc(a, w_lm, w_layout == MEDUSA_W_TILES, V, hidden, rows, d, s, fn);
   }
@@ -535,4 +648,41 @@ extern "C" int medusa_heads_hidden(const void* hidden, int rows, const void* w1,
                 static_cast<const float*>(hidden), static_cast<const float*>(w1), static_cast<const float*>(b1),
                 static_cast<float*>(u), rows, d, K, nused, hs);
   return check_launch(fn);
+}
+
+extern "C" int medusa_lm_head_stat_groups(int rows, int V) {
+  if (rows < 1 || V < 1) return 0;
+  int nchunks, npad, nt, ngroups;
+  plan_tc(rows, (V + BM - 1) / BM, nchunks, npad, nt, ngroups);
+  return ngroups;
+}
+
+extern "C" int medusa_lm_head_verify_stats(const void* hidden, const void* w_lm, float* logits, int rows, int d,
+                                           int V, medusa_dtype dtype, medusa_w_layout w_layout, int mode,
+                                           float temperature, void* stats, size_t stats_bytes, int32_t* err,
+                                           void* stream) {
+  const char* fn = "medusa_lm_head_verify_stats";
+  if (!hidden || !w_lm || !stats) return fail(MEDUSA_ERR_INVALID, "%s: NULL tensor", fn);
+  if (rows < 1 || d < 1 || V < 1) return fail(MEDUSA_ERR_INVALID, "%s: rows=%d d=%d V=%d", fn, rows, d, V);
+  if (mode != 0 && mode != 1) return fail(MEDUSA_ERR_INVALID, "%s: mode %d", fn, mode);
+  if (mode == 1 && !(temperature > 0.f)) return fail(MEDUSA_ERR_INVALID, "%s: temperature must be > 0", fn);
+  if (mode == 1 && !logits) return fail(MEDUSA_ERR_INVALID, "%s: typical acceptance needs the logits", fn);
+  if (w_layout != MEDUSA_W_ROWS && w_layout != MEDUSA_W_TILES)
+    return fail(MEDUSA_ERR_INVALID, "%s: w_layout=%d", fn, (int)w_layout);
+  if (dtype != MEDUSA_BF16) return fail(MEDUSA_ERR_UNSUPPORTED, "%s: bf16 only", fn);
+  if (d % BK) return fail(MEDUSA_ERR_UNSUPPORTED, "%s: d=%d not a multiple of %d", fn, d, BK);
+  if ((reinterpret_cast<uintptr_t>(hidden) | reinterpret_cast<uintptr_t>(w_lm) |
+       reinterpret_cast<uintptr_t>(stats)) % 16)
+    return fail(MEDUSA_ERR_INVALID, "%s: hidden / w_lm / stats not 16-byte aligned", fn);
+  const size_t need = (size_t)medusa_lm_head_stat_groups(rows, V) * rows * 16;
+  if (stats_bytes < need) return fail(MEDUSA_ERR_CAPACITY, "%s: stats %zu < %zu bytes", fn, stats_bytes, need);
+  LmArgs a{};
+  a.logits = logits; a.V = V; a.err = err;
+  a.mode = 0;
+  a.write_logits = logits != nullptr;
+  a.stats = static_cast<float4*>(stats);
+  a.stat_mode = 1 + mode;
+  a.inv_temp = mode == 1 ? 1.f / temperature : 1.f;
+  a.ntiles = (V + BM - 1) / BM;
+  return launch_tc(a, w_lm, w_layout == MEDUSA_W_TILES, V, hidden, rows, d, as_stream(stream), fn);
 }

@@ -60,6 +60,9 @@ _SIGS = {
     "medusa_build_candidates": (I, [P, P, I, I, TREE, I, P, P]),
     "medusa_heads_hidden": (I, [P, I, P, I, P, P, I, I, I, P, P, P]),
     "medusa_append_tokens": (I, [P, P, P, I, I, I, P, P, I, P, P]),
+    "medusa_lm_head_stat_groups": (I, [I, I]),
+    "medusa_lm_head_verify_stats": (I, [P, P, P, I, I, I, I, I, I, F, P, SZ, P, P]),
+    "medusa_accept_stats": (I, [P, I, P, P, TREE, I, I, I, F, F, F, P, P, P, P, P, P, P]),
     "medusa_accept_rejection_workspace_size": (SZ, [I, I]),
     "medusa_accept_rejection": (I, [P, P, I, P, TREE, I, I, F, P, I, P, P, P, P, SZ, P, P]),
     "medusa_standin_embed": (I, [P, I, P, I, I, I, P, P, P]),
@@ -359,3 +362,27 @@ def medusa_accept_rejection(logits, draft_logits, tokens, tree: DeviceTree, temp
                                         _ptr(accept_len), _ptr(accepted_nodes), _ptr(next_token), _ptr(workspace),
                                         workspace.numel() * workspace.element_size(), _ptr(err),
                                         _stream(stream)), "medusa_accept_rejection")
+
+
+def medusa_lm_head_stat_groups(rows, V) -> int:
+    return int(_lib.medusa_lm_head_stat_groups(rows, V))
+
+
+def medusa_lm_head_verify_stats(hidden, w_lm, logits, stats, mode, temperature, V, err=None, stream=None,
+                                layout=W_ROWS):
+    """LM head + fused acceptance statistics; logits may be None in greedy mode (mode 0)."""
+    d = hidden.shape[-1]
+    rows = hidden.numel() // d
+    _check(_lib.medusa_lm_head_verify_stats(_ptr(hidden), _ptr(w_lm), _ptr(logits), rows, d, V, _dtype(hidden),
+                                            layout, mode, float(temperature), _ptr(stats),
+                                            stats.numel() * stats.element_size(), _ptr(err), _stream(stream)),
+           "medusa_lm_head_verify_stats")
+
+
+def medusa_accept_stats(stats, groups, logits, tokens, tree: DeviceTree, mode, temperature, eps, delta, V,
+                        accept_len, accepted_nodes, next_root, best_node, best_logp, err=None, stream=None):
+    B = tokens.shape[0]
+    _check(_lib.medusa_accept_stats(_ptr(stats), groups, _ptr(logits), _ptr(tokens), tree.ref, B, V, mode,
+                                    float(temperature), float(eps), float(delta), _ptr(accept_len),
+                                    _ptr(accepted_nodes), _ptr(next_root), _ptr(best_node), _ptr(best_logp),
+                                    _ptr(err), _stream(stream)), "medusa_accept_stats")

@@ -50,7 +50,7 @@ class VerifyStep:
     """Owns the outputs and scratch of one verify step for fixed shapes."""
 
     def __init__(self, w: dict, weights: dict, tree: M.DeviceTree, max_prefix: int, device="cuda",
-                 heads: str = "fused"):
+                 heads: str = "fused", accept: str = "separate", write_logits: bool = True):
         self.w, self.tree, self.max_prefix = w, tree, max_prefix
         B, H, Dh, d, V, K = w["B"], w["H"], w["Dh"], w["d"], w["V"], w["K"]
         T = tree.T
@@ -86,6 +86,14 @@ class VerifyStep:
         def ws(n):
             return torch.empty(max(int(n), 256), dtype=torch.uint8, device=device)
 
+        # accept="fused" (bf16): the LM head's epilogue writes per-group row
+        # statistics that medusa_accept_stats merges; greedy steps may then skip
+        # writing the logits (write_logits=False)
+        self.accept = accept if w["dtype"] == "bf16" else "separate"
+        self.write_logits = write_logits or self.mode == 1 or self.accept != "fused"
+        if self.accept == "fused":
+            self.stat_groups = M.medusa_lm_head_stat_groups(B * T, V)
+            self.stats = torch.zeros((self.stat_groups, B * T, 4), dtype=torch.float32, device=device)
         self.ws_attn = ws(M.medusa_tree_attn_workspace_size(B, H, Dh, T, max_prefix))
         self.ws_accept = ws(M.medusa_accept_workspace_size(B, T))
         self.ws_heads = ws(M.medusa_heads_topk_workspace_size(B, K, d, V, self.s_max))
@@ -121,17 +129,28 @@ class VerifyStep:
         M.medusa_tree_attn(x["q"], x["k_new"], x["v_new"], x["k_cache"], x["v_cache"], x["seq_start"],
                            x["prefix_len"], x["seq_cap"], self.tree, self.max_prefix, self.rope_theta,
                            self.scale, self.out, self.ws_attn, self.err, side)
-        M.medusa_lm_head_verify(x["hidden"], self.w_lm_run, self.logits, None, self.err, main,
-                                layout=self.w_layout)
+        if self.accept == "fused":
+            M.medusa_lm_head_verify_stats(x["hidden"], self.w_lm_run, self.logits if self.write_logits else None,
+                                          self.stats, self.mode, self.temperature, self.logits.shape[-1], self.err,
+                                          main, layout=self.w_layout)
+        else:
+            M.medusa_lm_head_verify(x["hidden"], self.w_lm_run, self.logits, None, self.err, main,
+                                    layout=self.w_layout)
         hs = heads_stream if heads_stream is not None else main
         if self.heads == "split":
             if hs is not main:
                 hs.wait_stream(main)  # after the LM head: beside the acceptance
             M.medusa_heads_hidden(x["hidden"], self.w1_run, self.b1, self.s_heads, self.u_all, self.err, hs,
                                   layout=self.w1_layout)
-        M.medusa_accept(self.logits, x["tokens"], self.tree, self.mode, self.temperature, self.eps,
-                        self.delta, self.accept_len, self.accepted_nodes, self.next_root, self.best_node,
-                        self.best_logp, self.ws_accept, self.err, main)
+        if self.accept == "fused":
+            M.medusa_accept_stats(self.stats, self.stat_groups, self.logits if self.write_logits else None,
+                                  x["tokens"], self.tree, self.mode, self.temperature, self.eps, self.delta,
+                                  self.logits.shape[-1], self.accept_len, self.accepted_nodes, self.next_root,
+                                  self.best_node, self.best_logp, self.err, main)
+        else:
+            M.medusa_accept(self.logits, x["tokens"], self.tree, self.mode, self.temperature, self.eps,
+                            self.delta, self.accept_len, self.accepted_nodes, self.next_root, self.best_node,
+                            self.best_logp, self.ws_accept, self.err, main)
         if append is not None:  # box step 6: the root and the accepted tokens to the output
             M.medusa_append_tokens(x["tokens"], self.accepted_nodes, self.accept_len, append[0], append[1],
                                    self.err, main)
@@ -155,5 +174,5 @@ class VerifyStep:
     @property
     def launches_per_step(self) -> int:
         """Kernels one run() launches: attention 1 (2 for f32), LM head 1,
-        acceptance 2, compaction 1, heads 2, candidates 1."""
-        return (1 if self.w["dtype"] == "bf16" else 2) + 1 + 2 + 1 + 2 + 1
+        acceptance 2 (1 fused), compaction 1, heads 2, candidates 1."""
+        return (1 if self.w["dtype"] == "bf16" else 2) + 1 + (1 if self.accept == "fused" else 2) + 1 + 2 + 1
