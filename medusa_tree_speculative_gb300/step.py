@@ -72,15 +72,20 @@ class VerifyStep:
         i32 = dict(dtype=torch.int32, device=device)
         self.out = torch.empty((B, T, H, Dh), dtype=dt, device=device)
         self.logits = torch.empty((B, T, V), dtype=torch.float32, device=device)
-        self.accept_len = torch.zeros(B, **i32)
-        self.accepted_nodes = torch.zeros((B, tree.K + 1), **i32)
-        self.next_root = torch.zeros(B, **i32)
-        self.best_node = torch.zeros(B, **i32)
+        # the step's integer results side by side in one buffer, so that a
+        # caller reads them back with a single copy (self.results)
+        Kp = tree.K + 1
+        self.results = torch.zeros(B * (3 + Kp + T), **i32)
+        r = self.results
+        self.accept_len = r[0:B]
+        self.next_root = r[B:2 * B]
+        self.best_node = r[2 * B:3 * B]
+        self.accepted_nodes = r[3 * B:3 * B + B * Kp].view(B, Kp)
         self.best_logp = torch.zeros(B, dtype=torch.float32, device=device)
         self.src_slots = torch.zeros((B, tree.K + 1), **i32)
         self.head_logits = torch.zeros((B, K, V), dtype=torch.float32, device=device)
         self.topk = torch.zeros((B, K, self.s_max), **i32)
-        self.next_tokens = torch.zeros((B, T), **i32)
+        self.next_tokens = r[3 * B + B * Kp:].view(B, T)
         self.err = torch.zeros(1, **i32)
 
         def ws(n):
