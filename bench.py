@@ -60,6 +60,11 @@ def parse_args():
                          "row (split), or both projections on the accepted row after it (fused)")
     ap.add_argument("--attn-branch", choices=["serial", "fork"], default="fork",
                     help="tree attention before the LM head on one stream, or on a forked graph branch")
+    ap.add_argument("--attn-order", choices=["first", "after_lm"], default="after_lm",
+                    help="attention enqueued before the LM head or right after it (its CTAs then fill the "
+                         "SMs the LM head leaves idle)")
+    ap.add_argument("--attn-splits", type=int, choices=[1, 2, 4, 8], default=None,
+                    help="CTAs that split one head's keys (default: 4 for bf16)")
     return ap.parse_args()
 
 
@@ -222,7 +227,8 @@ def step_calls(st, x, s):
 
     c = [("tree_attn", lambda: M.medusa_tree_attn(
             x["q"], x["k_new"], x["v_new"], x["k_cache"], x["v_cache"], x["seq_start"], x["prefix_len"],
-            x["seq_cap"], st.tree, st.max_prefix, st.rope_theta, st.scale, st.out, st.ws_attn, st.err, s)),
+            x["seq_cap"], st.tree, st.max_prefix, st.rope_theta, st.scale, st.out, st.ws_attn, st.err, s,
+            key_splits=st.attn_splits)),
          ("lm_head_verify", (lambda: M.medusa_lm_head_verify_stats(
              x["hidden"], st.w_lm_run, st.logits if st.write_logits else None, st.stats, st.mode, st.temperature,
              st.logits.shape[-1], st.err, s, layout=st.w_layout)) if st.accept == "fused" else
@@ -276,7 +282,8 @@ def run_native(args, w, rank, world, local_rank):
         x[k] = step.host_to_torch(v, dt).to(dev) if v.dtype in (np.uint16, np.float32) else torch.from_numpy(v).to(dev)
     L_list = xh["prefix_len"].copy()
     st = step.VerifyStep(w, wd, tree, max_prefix=int(L_list.max()), device=dev, heads=args.heads,
-                         accept=args.accept, write_logits=args.logits)
+                         accept=args.accept, write_logits=args.logits, attn_order=args.attn_order,
+                         attn_splits=args.attn_splits or "auto")
     plant(w, tree, st, x, args.plant_depth, torch)
     prefix0 = x["prefix_len"].clone()
     s = torch.cuda.Stream(device=dev)
@@ -364,7 +371,7 @@ def run_native(args, w, rank, world, local_rank):
     return dict(ms_step=ms_step, ms_events_step=ms_events / args.steps, per_call_ms=per_call, clocks=clocks,
                 dloop=dloop, rej=rej,
                 T=T, s_heads=st.s_heads, L_list=L_list, accept_len=accept_len, e2e=e2e,
-                launches=st.launches_per_step * args.steps, tree=ht)
+                launches=st.launches_per_step * args.steps, tree=ht, attn_splits=st.attn_splits or 8)
 
 
 def measure_rejection(st, x, s, torch, M, reps=20):
@@ -691,7 +698,7 @@ def main():
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": w["dtype"], "data": "synthetic (seeded random weights and activations)",
-        "config": config_dict(w, {"parallelism": f"replicas{world}" if world > 1 else "single-gpu", "attn_branch": args.attn_branch, "heads": args.heads, "accept_impl": args.accept,
+        "config": config_dict(w, {"parallelism": f"replicas{world}" if world > 1 else "single-gpu", "attn_branch": args.attn_branch, "attn_order": args.attn_order, "attn_splits": r["attn_splits"], "heads": args.heads, "accept_impl": args.accept,
                                   "logits_written": bool(args.logits or w["mode"] == "typical"),
                                   "T_rows": r["T"], "s": r["s_heads"], "planted_accept_len": r["accept_len"]}),
         "roofline": {"bound": "hbm", "kernel": f"medusa_{dom}", "achieved": achieved, "peak": peaks["hbm_gbs"],

@@ -164,6 +164,23 @@ int medusa_tree_attn(const void* q, const void* k_new, const void* v_new,
                      medusa_dtype dtype, void* out, void* workspace,
                      size_t workspace_bytes, int32_t* err, void* stream);
 
+/* medusa_tree_attn with the number of CTAs that split the keys of one
+ * (sequence, head, block of up to 80 query rows), bf16 only: key_splits = 8
+ * (what medusa_tree_attn uses) spreads the work over many short CTAs;
+ * key_splits = 1 runs one long CTA per unit (32 CTAs for one sequence of 32
+ * heads), for a caller that runs the attention on SMs that a concurrent
+ * kernel leaves idle; 2 and 4 lie between.  Same results up to the
+ * order of the fp32 softmax sums.  Other values: MEDUSA_ERR_UNSUPPORTED. */
+int medusa_tree_attn_splits(const void* q, const void* k_new,
+                            const void* v_new, void* k_cache, void* v_cache,
+                            const int64_t* seq_start,
+                            const int32_t* prefix_len, const int64_t* seq_cap,
+                            const medusa_tree_t* tree, int B, int H, int Dh,
+                            int max_prefix, float rope_theta, float scale,
+                            medusa_dtype dtype, void* out, void* workspace,
+                            size_t workspace_bytes, int key_splits,
+                            int32_t* err, void* stream);
+
 /* Scratch bytes medusa_lm_head_verify needs (currently 0). */
 size_t medusa_lm_head_workspace_size(int rows, int d, int V);
 

@@ -6,8 +6,8 @@
 // its own ancestors (and itself) only; its position id is prefix length +
 // depth.  Explainer "085 | Medusa", section 二.2: siblings must stay invisible.
 //
-// bf16: one kernel.  A thread-block cluster of CL CTAs serves one (sequence,
-// head, block of query rows).  Each CTA takes a balanced share of the L
+// bf16: one kernel.  A thread-block cluster of CL CTAs (CL = 1, 2, 4 or 8)
+// serves one (sequence, head, block of query rows).  Each CTA takes a balanced share of the L
 // cached prefix keys and a balanced share of the tree keys (flash-decoding
 // split; tree keys cost more, so every CTA gets a few).  Each CTA
 //   * issues the cp.async copies of its first prefix tile and the loads of
@@ -24,8 +24,10 @@
 //     robin), reusing its query buffer, which every CTA has released at an
 //     early split cluster barrier.
 // After one blocking cluster barrier each CTA merges its own rows from local
-// shared memory and writes the output.  No scratch memory, no inter-kernel
-// combine pass.
+// shared memory and writes the output.  With CL = 1 (few, long CTAs, for a
+// caller that runs the attention on the SMs another kernel leaves idle) the
+// CTA walks every key and writes its rows directly.  No scratch memory, no
+// inter-kernel combine pass.
 //
 // f32: rope_append (RoPE + KV append, q' staged in scratch) and a plain
 // CUDA-core kernel, one CTA per (row, head, sequence).
@@ -42,7 +44,7 @@ namespace {
 
 constexpr int KT = 64;        // keys per shared-memory tile
 constexpr int MAX_WARPS = 5;  // 16 query rows per warp; two CTAs per SM
-constexpr int CL = 8;         // CTAs per cluster (key splits)
+constexpr int kMaxSplits = 8; // most CTAs per cluster (key splits)
 constexpr float LOG2E = 1.4426950408889634f;
 
 struct AttnArgs {
@@ -73,20 +75,27 @@ void row_split(int T, int& rowblocks, int& warps) {
 }
 
 // Query rows are dealt to the cluster's CTAs round robin for the merge.
-__host__ __device__ constexpr int rows_per_owner(int nrows) { return (nrows + CL - 1) / CL; }
+__host__ __device__ constexpr int rows_per_owner(int nrows, int CL) { return (nrows + CL - 1) / CL; }
+
+// Key/value tile stages in flight.  A lone CTA (CL = 1) walks every key of
+// its head, so it keeps two tiles ahead instead of one; its query rows are
+// staged in the third stage's buffer, which is first filled after the query
+// fragments have moved to registers.
+__host__ __device__ constexpr int kv_stages(int CL) { return CL == 1 ? 3 : 2; }
 
 // Bytes of the region that first holds the rotated query rows (bf16) and
-// later the partials pushed by the cluster's CTAs (fp32 O and (max, sum)).
-__host__ __device__ constexpr int qrecv_bytes(int Dh, int warps) {
+// later the partials pushed by the cluster's CTAs (fp32 O and (max, sum));
+// none for CL = 1 (the query rows use a tile stage).
+__host__ __device__ constexpr int qrecv_bytes(int Dh, int warps, int CL) {
   const int q = warps * 16 * Dh * 2;
-  const int r = CL * rows_per_owner(warps * 16) * (Dh + 2) * 4;
-  return q > r ? q : r;
+  const int r = CL * rows_per_owner(warps * 16, CL) * (Dh + 2) * 4;
+  return CL == 1 ? 0 : (q > r ? q : r);
 }
 
-size_t smem_bytes(int Dh, int warps, int K) {
-  return (size_t)2 * 2 * KT * Dh * 2            // K and V tiles, double-buffered, bf16
-         + (size_t)qrecv_bytes(Dh, warps)       // query rows, then the pushed partials
-         + (size_t)2 * (K + 1) * (Dh / 2) * 4;  // cos / sin per tree depth
+size_t smem_bytes(int Dh, int warps, int K, int CL) {
+  return (size_t)kv_stages(CL) * 2 * KT * Dh * 2  // K and V tiles per stage, bf16
+         + (size_t)qrecv_bytes(Dh, warps, CL)     // query rows, then the pushed partials
+         + (size_t)2 * (K + 1) * (Dh / 2) * 4;    // cos / sin per tree depth
 }
 
 // Sequence b is usable iff 0 <= L <= max_prefix and L + T fits its capacity.
@@ -147,26 +156,28 @@ MDEV void st_cluster_f32x2(uint32_t addr, float x, float y) {
 // ---------------------------------------------------------------------------
 // bf16: clustered split-K tree attention
 // ---------------------------------------------------------------------------
-template <int DH>
+template <int DH, int CL>
 __global__ void __cluster_dims__(CL, 1, 1) __launch_bounds__(MAX_WARPS * 32, 2)
     attn_tree_kernel(const __grid_constant__ AttnArgs a) {
   constexpr int CH = DH / 8;    // 16-byte chunks per row
   constexpr int HALF = DH / 2;
   constexpr int HCH = CH / 2;   // chunks per rotary half
   constexpr int QI = HCH / 2;   // query items per thread: rows * HCH / (rows * 2)
+  constexpr int S = kv_stages(CL);
+  static_assert(CL > 1 || 2 * KT >= MAX_WARPS * 16, "query rows must fit one K+V stage");
   extern __shared__ __align__(128) uint8_t smem[];
-  uint16_t* kbuf = reinterpret_cast<uint16_t*>(smem);  // [2][KT][DH]
-  uint16_t* vbuf = kbuf + 2 * KT * DH;                // [2][KT][DH]
-  uint8_t* qrecv = reinterpret_cast<uint8_t*>(vbuf + 2 * KT * DH);
-  uint16_t* qbuf = reinterpret_cast<uint16_t*>(qrecv);  // [rows][DH] until the q fragments are loaded
+  uint16_t* kvbuf = reinterpret_cast<uint16_t*>(smem);  // [S][K, V][KT][DH]
+  uint8_t* qrecv = reinterpret_cast<uint8_t*>(kvbuf + S * 2 * KT * DH);
+  // [rows][DH] until the q fragments are loaded: the last stage (CL = 1) or qrecv
+  uint16_t* qbuf = CL == 1 ? kvbuf + (S - 1) * 2 * KT * DH : reinterpret_cast<uint16_t*>(qrecv);
   const int nrows = a.warps * 16;
-  const int RPO = rows_per_owner(nrows);
+  const int RPO = rows_per_owner(nrows, CL);
   float* recv_o = reinterpret_cast<float*>(qrecv);             // then [CL][RPO][DH]
   float* recv_ml = recv_o + CL * RPO * DH;                     //      [CL][RPO][2]
-  float* cs = reinterpret_cast<float*>(qrecv + qrecv_bytes(DH, a.warps));  // [K+1][HALF]
+  float* cs = reinterpret_cast<float*>(qrecv + qrecv_bytes(DH, a.warps, CL));  // [K+1][HALF]
   float* sn = cs + (a.K + 1) * HALF;
 
-  const uint32_t crank = cluster_ctarank();
+  const uint32_t crank = CL > 1 ? cluster_ctarank() : 0u;
   const int h = blockIdx.y, b = blockIdx.z / a.rowblocks, rb = blockIdx.z % a.rowblocks;
   const int tid = threadIdx.x, nthr = blockDim.x;
   const int warp = tid >> 5, lane = tid & 31;
@@ -186,20 +197,22 @@ __global__ void __cluster_dims__(CL, 1, 1) __launch_bounds__(MAX_WARPS * 32, 2)
   const int t0 = (int)crank * ntree / CL, t1 = ((int)crank + 1) * ntree / CL;
   const int np = p1 - p0, nv = np + (t1 - t0);
   const int ntiles = (nv + KT - 1) / KT;
-  // ancestor bits of this CTA's tree keys (nodes t0 .. t0 + 63) for this
-  // thread's two query rows, loaded once
+  // ancestor bits of 64 consecutive tree nodes n0 .. n0 + 63 for one query
+  // row (a tile's window of this CTA's tree keys)
   const int ra = row0 + (tid >> 5) * 16 + ((tid & 31) >> 2);
   const int rbw = ra + 8;
-  auto vis_bits = [&](int r) -> uint64_t {
-    if (!ok || r >= a.T || t1 <= t0) return 0;
+  auto vis_bits = [&](int r, int n0) -> uint64_t {
+    if (!ok || r >= a.T || n0 >= t1) return 0;
     const uint32_t* row = a.anc + (int64_t)r * a.W;
-    const int w0 = t0 >> 5, sh = t0 & 31;
+    const int w0 = n0 >> 5, sh = n0 & 31;
     const uint64_t lo = __ldg(row + w0);
     const uint64_t mid = w0 + 1 < a.W ? __ldg(row + w0 + 1) : 0;
     const uint64_t hi = w0 + 2 < a.W ? __ldg(row + w0 + 2) : 0;
     return ((lo | (mid << 32)) >> sh) | (sh ? hi << (64 - sh) : 0);
   };
-  const uint64_t vis_a = vis_bits(ra), vis_b = vis_bits(rbw);
+  // the window of this CTA's first tree keys, loaded before the long-latency work below
+  uint64_t vis_a = vis_bits(ra, t0), vis_b = vis_bits(rbw, t0);
+  int vis_win = 0;
 
   const uint16_t* kcache = static_cast<const uint16_t*>(a.k_cache);
   const uint16_t* vcache = static_cast<const uint16_t*>(a.v_cache);
@@ -217,8 +230,8 @@ __global__ void __cluster_dims__(CL, 1, 1) __launch_bounds__(MAX_WARPS * 32, 2)
     for (int e = tid; e < rows * HCH; e += nthr) {
       const int rr = e / HCH, c = e % HCH;
       const int v = v0 + rr;
-      uint16_t* kd = kbuf + (buf * KT + rr) * DH;
-      uint16_t* vd = vbuf + (buf * KT + rr) * DH;
+      uint16_t* kd = kvbuf + (buf * 2 * KT + rr) * DH;
+      uint16_t* vd = kd + KT * DH;
       const int s1 = (c ^ (rr & 7)) * 8, s2 = ((c + HCH) ^ (rr & 7)) * 8;
       if (v < np) {
         if (pass == 1) continue;
@@ -258,9 +271,13 @@ __global__ void __cluster_dims__(CL, 1, 1) __launch_bounds__(MAX_WARPS * 32, 2)
     }
   };
 
-  // ---- first the long-latency work: tile 0's prefix copies, the query loads
-  if (ntiles > 0) load_tile(0, 0, 0);
-  cp_async_commit();
+  // ---- first the long-latency work: the prefix copies of the first S - 1
+  // tiles (one commit group each), the query loads
+#pragma unroll
+  for (int j = 0; j < S - 1; ++j) {
+    if (j < ntiles) load_tile(j * KT, j, 0);
+    cp_async_commit();
+  }
   const uint16_t* q = static_cast<const uint16_t*>(a.q);
   uint4 qlo[QI], qhi[QI];
   int qd[QI];
@@ -300,7 +317,10 @@ __global__ void __cluster_dims__(CL, 1, 1) __launch_bounds__(MAX_WARPS * 32, 2)
     *reinterpret_cast<uint4*>(qbuf + rr * DH + ((c ^ (rr & 7)) * 8)) = lo;
     *reinterpret_cast<uint4*>(qbuf + rr * DH + (((c + HCH) ^ (rr & 7)) * 8)) = hi;
   }
-  if (ntiles > 0) load_tile(0, 0, 1);  // tree keys and zero rows of tile 0 (needs the tables)
+  // tree keys and zero rows of those tiles (they need the tables)
+#pragma unroll
+  for (int j = 0; j < S - 1; ++j)
+    if (j < ntiles) load_tile(j * KT, j, 1);
   __syncthreads();
   uint32_t qf[DH / 16][4];
   {
@@ -311,10 +331,11 @@ __global__ void __cluster_dims__(CL, 1, 1) __launch_bounds__(MAX_WARPS * 32, 2)
       ldmatrix_x4(qf[kk], smem_u32(qbuf + rr * DH + ((c ^ (rr & 7)) * 8)));
     }
   }
-  // the query buffer becomes the landing area of the pushed partials: no CTA
-  // pushes before every CTA of the cluster has arrived here
+  // the query buffer becomes the landing area of the pushed partials (no CTA
+  // pushes before every CTA of the cluster has arrived here) or, for CL = 1,
+  // the last tile stage
   __syncthreads();
-  cluster_arrive();
+  if (CL > 1) cluster_arrive();
 
   float m_a = -INFINITY, m_b = -INFINITY, l_a = 0.f, l_b = 0.f;
   float o[DH / 8][4];
@@ -323,17 +344,17 @@ __global__ void __cluster_dims__(CL, 1, 1) __launch_bounds__(MAX_WARPS * 32, 2)
 
   for (int t = 0; t < ntiles; ++t) {
     const int v0 = t * KT;
-    const int buf = t & 1;
-    if (t + 1 < ntiles) {
-      load_tile(v0 + KT, buf ^ 1, 2);
-      cp_async_commit();
-      cp_async_wait<1>();
-    } else {
-      cp_async_wait<0>();
-    }
+    const int buf = t % S;
+    // tile t + S - 1 into the stage tile t - 1 used (freed by the barrier that
+    // ended the previous iteration); one commit group per tile, empty past the
+    // end, so that S - 1 pending groups mean tile t has landed
+    const int nxt = t + S - 1;
+    if (nxt < ntiles) load_tile(nxt * KT, nxt % S, 2);
+    cp_async_commit();
+    cp_async_wait<S - 1>();
     __syncthreads();
-    const uint16_t* kb = kbuf + buf * KT * DH;
-    const uint16_t* vb = vbuf + buf * KT * DH;
+    const uint16_t* kb = kvbuf + buf * 2 * KT * DH;
+    const uint16_t* vb = kb + KT * DH;
     const int nb = min(KT / 16, (nv - v0 + 15) / 16);  // 16-key blocks holding keys
 
     // S = q' K^T  (16 rows x 64 keys per warp)
@@ -354,16 +375,22 @@ __global__ void __cluster_dims__(CL, 1, 1) __launch_bounds__(MAX_WARPS * 32, 2)
         }
       }
     }
-    // mask: past this CTA's keys; ancestor bits on tree keys
+    // mask: past this CTA's keys; ancestor bits on tree keys (bit v - np -
+    // vis_win of the window that starts at this tile's first tree key)
     if (v0 + KT > np) {
+      const int win = max(v0, np) - np;
+      if (win != vis_win) {
+        vis_a = vis_bits(ra, t0 + win);
+        vis_b = vis_bits(rbw, t0 + win);
+        vis_win = win;
+      }
 #pragma unroll
       for (int n = 0; n < KT / 8; ++n) {
 #pragma unroll
         for (int e = 0; e < 4; ++e) {
           const int v = v0 + n * 8 + (lane & 3) * 2 + (e & 1);
-          const int r = e < 2 ? ra : rbw;
           const uint64_t vis = e < 2 ? vis_a : vis_b;
-          if (v >= nv || (v >= np && !((vis >> (v - np)) & 1ull))) s[n][e] = -INFINITY;
+          if (v >= nv || (v >= np && !((vis >> (v - np - win)) & 1ull))) s[n][e] = -INFINITY;
         }
       }
     }
@@ -424,10 +451,27 @@ __global__ void __cluster_dims__(CL, 1, 1) __launch_bounds__(MAX_WARPS * 32, 2)
   l_b += __shfl_xor_sync(0xffffffffu, l_b, 1);
   l_b += __shfl_xor_sync(0xffffffffu, l_b, 2);
 
+  const int la = warp * 16 + (lane >> 2), lb = la + 8;
+  if constexpr (CL == 1) {
+    // ---- every key was this CTA's: normalise and write the rows
+    if (!ok) return;
+    uint16_t* out = static_cast<uint16_t*>(a.out);
+    const float ia = l_a > 0.f ? 1.f / l_a : 0.f, ib = l_b > 0.f ? 1.f / l_b : 0.f;
+    const bool wa = row0 + la < a.T, wb = row0 + lb < a.T;
+    uint16_t* oa = out + (((int64_t)b * a.T + row0 + la) * a.H + h) * DH;
+    uint16_t* ob = out + (((int64_t)b * a.T + row0 + lb) * a.H + h) * DH;
+#pragma unroll
+    for (int n = 0; n < DH / 8; ++n) {
+      const int col = n * 8 + (lane & 3) * 2;
+      if (wa) *reinterpret_cast<uint32_t*>(oa + col) = pack2_bf16(o[n][0] * ia, o[n][1] * ia);
+      if (wb) *reinterpret_cast<uint32_t*>(ob + col) = pack2_bf16(o[n][2] * ib, o[n][3] * ib);
+    }
+    return;
+  }
+
   // ---- push this CTA's partial of each local row to the row's owner
   // (rank rr % CL, slot rr / CL): every CTA has released its query buffer
   cluster_wait();
-  const int la = warp * 16 + (lane >> 2), lb = la + 8;
   const uint32_t o_base = smem_u32(recv_o), ml_base = smem_u32(recv_ml);
   if (row0 + la < a.T) {
     const uint32_t ra_o = map_to_rank(o_base + (((int)crank * RPO + la / CL) * DH) * 4, (uint32_t)(la % CL));
@@ -607,14 +651,53 @@ extern "C" size_t medusa_tree_attn_workspace_size(int B, int H, int Dh, int T, i
   return align_up((size_t)B * T * H * Dh * sizeof(float), 256);
 }
 
+namespace medusa {
+namespace {
+
+template <int DH, int CL>
+void launch_attn_bf16(const AttnArgs& a, int B, int H, cudaStream_t s) {
+  dim3 grid(CL, H, B * a.rowblocks);
+  const size_t sm = smem_bytes(DH, a.warps, a.K, CL);
+  cudaFuncSetAttribute(attn_tree_kernel<DH, CL>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sm);
+  launch_kernel(attn_tree_kernel<DH, CL>, grid, dim3(a.warps * 32), sm, s, a);
+}
+
+template <int DH>
+void launch_attn_bf16(const AttnArgs& a, int B, int H, int splits, cudaStream_t s) {
+  switch (splits) {
+    case 1: launch_attn_bf16<DH, 1>(a, B, H, s); break;
+    case 2: launch_attn_bf16<DH, 2>(a, B, H, s); break;
+    case 4: launch_attn_bf16<DH, 4>(a, B, H, s); break;
+    default: launch_attn_bf16<DH, kMaxSplits>(a, B, H, s); break;
+  }
+}
+
+}  // namespace
+}  // namespace medusa
+
 extern "C" int medusa_tree_attn(const void* q, const void* k_new, const void* v_new, void* k_cache,
                                 void* v_cache, const int64_t* seq_start, const int32_t* prefix_len,
                                 const int64_t* seq_cap, const medusa_tree_t* tree, int B, int H,
                                 int Dh, int max_prefix, float rope_theta, float scale,
                                 medusa_dtype dtype, void* out, void* workspace,
                                 size_t workspace_bytes, int32_t* err, void* stream) {
+  return medusa_tree_attn_splits(q, k_new, v_new, k_cache, v_cache, seq_start, prefix_len, seq_cap, tree, B, H,
+                                 Dh, max_prefix, rope_theta, scale, dtype, out, workspace, workspace_bytes,
+                                 kMaxSplits, err, stream);
+}
+
+extern "C" int medusa_tree_attn_splits(const void* q, const void* k_new, const void* v_new, void* k_cache,
+                                       void* v_cache, const int64_t* seq_start, const int32_t* prefix_len,
+                                       const int64_t* seq_cap, const medusa_tree_t* tree, int B, int H,
+                                       int Dh, int max_prefix, float rope_theta, float scale,
+                                       medusa_dtype dtype, void* out, void* workspace,
+                                       size_t workspace_bytes, int key_splits, int32_t* err, void* stream) {
   const char* fn = "medusa_tree_attn";
   if (int rc = check_tree(tree, fn)) return rc;
+  if (key_splits != 1 && key_splits != 2 && key_splits != 4 && key_splits != kMaxSplits)
+    return fail(MEDUSA_ERR_UNSUPPORTED, "%s: key_splits=%d not in {1,2,4,8}", fn, key_splits);
+  if (key_splits != kMaxSplits && dtype != MEDUSA_BF16)
+    return fail(MEDUSA_ERR_UNSUPPORTED, "%s: key_splits=%d needs bf16", fn, key_splits);
   if (!q || !k_new || !v_new || !k_cache || !v_cache || !seq_start || !prefix_len || !seq_cap || !out)
     return fail(MEDUSA_ERR_INVALID, "%s: NULL tensor", fn);
   if (B < 1 || B > MEDUSA_MAX_B || H < 1 || max_prefix < 0)
@@ -648,15 +731,10 @@ extern "C" int medusa_tree_attn(const void* q, const void* k_new, const void* v_
   cudaStream_t s = as_stream(stream);
 
   if (bf16) {
-    dim3 grid(CL, H, B * a.rowblocks);
-    const size_t sm = smem_bytes(Dh, a.warps, a.K);
-    if (Dh == 128) {
-      cudaFuncSetAttribute(attn_tree_kernel<128>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sm);
-      launch_kernel(attn_tree_kernel<128>, grid, dim3(a.warps * 32), sm, s, a);
-    } else {
-      cudaFuncSetAttribute(attn_tree_kernel<64>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sm);
-      launch_kernel(attn_tree_kernel<64>, grid, dim3(a.warps * 32), sm, s, a);
-    }
+    if (Dh == 128)
+      launch_attn_bf16<128>(a, B, H, key_splits, s);
+    else
+      launch_attn_bf16<64>(a, B, H, key_splits, s);
     return check_launch(fn);
   }
   dim3 g1(tree->T, B);

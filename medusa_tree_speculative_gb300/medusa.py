@@ -47,6 +47,7 @@ _SIGS = {
     "medusa_tree_greedy": (I, [P, I, I, I, P, P]),
     "medusa_tree_attn_workspace_size": (SZ, [I, I, I, I, I]),
     "medusa_tree_attn": (I, [P, P, P, P, P, P, P, P, TREE, I, I, I, I, F, F, I, P, P, SZ, P, P]),
+    "medusa_tree_attn_splits": (I, [P, P, P, P, P, P, P, P, TREE, I, I, I, I, F, F, I, P, P, SZ, I, P, P]),
     "medusa_lm_head_workspace_size": (SZ, [I, I, I]),
     "medusa_lm_head_tiled_bytes": (SZ, [I, I]),
     "medusa_lm_head_tile": (I, [P, P, I, I, P]),
@@ -208,13 +209,17 @@ def medusa_tree_attn_workspace_size(B, H, Dh, T, max_prefix) -> int:
 
 def medusa_tree_attn(q, k_new, v_new, k_cache, v_cache, seq_start, prefix_len, seq_cap,
                      tree: DeviceTree, max_prefix: int, rope_theta: float, scale: float, out,
-                     workspace, err=None, stream=None):
+                     workspace, err=None, stream=None, key_splits=None):
+    """key_splits None: medusa_tree_attn; 1, 2, 4 or 8: medusa_tree_attn_splits."""
     B, T, H, Dh = q.shape
-    _check(_lib.medusa_tree_attn(_ptr(q), _ptr(k_new), _ptr(v_new), _ptr(k_cache), _ptr(v_cache),
-                                 _ptr(seq_start), _ptr(prefix_len), _ptr(seq_cap), tree.ref, B, H, Dh,
-                                 max_prefix, rope_theta, scale, _dtype(q), _ptr(out), _ptr(workspace),
-                                 workspace.numel() * workspace.element_size(), _ptr(err),
-                                 _stream(stream)), "medusa_tree_attn")
+    args = (_ptr(q), _ptr(k_new), _ptr(v_new), _ptr(k_cache), _ptr(v_cache), _ptr(seq_start),
+            _ptr(prefix_len), _ptr(seq_cap), tree.ref, B, H, Dh, max_prefix, rope_theta, scale, _dtype(q),
+            _ptr(out), _ptr(workspace), workspace.numel() * workspace.element_size())
+    if key_splits is None:
+        _check(_lib.medusa_tree_attn(*args, _ptr(err), _stream(stream)), "medusa_tree_attn")
+    else:
+        _check(_lib.medusa_tree_attn_splits(*args, int(key_splits), _ptr(err), _stream(stream)),
+               "medusa_tree_attn_splits")
 
 
 def medusa_lm_head_workspace_size(rows, d, V) -> int:

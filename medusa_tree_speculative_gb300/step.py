@@ -50,8 +50,19 @@ class VerifyStep:
     """Owns the outputs and scratch of one verify step for fixed shapes."""
 
     def __init__(self, w: dict, weights: dict, tree: M.DeviceTree, max_prefix: int, device="cuda",
-                 heads: str = "fused", accept: str = "separate", write_logits: bool = True):
+                 heads: str = "fused", accept: str = "separate", write_logits: bool = True,
+                 attn_order: str = "after_lm", attn_splits="auto"):
         self.w, self.tree, self.max_prefix = w, tree, max_prefix
+        # attention on the forked branch: enqueued before the LM head ("first")
+        # or right after it ("after_lm": its CTAs then take the SMs the LM head
+        # leaves idle instead of holding the LM head back), with the library's
+        # default key split (None) or 1, 2, 4, 8 CTAs per head ("auto": 4 for
+        # bf16, the fastest measured beside the LM head at the 7B shape)
+        if attn_order not in ("first", "after_lm"):
+            raise ValueError(f"attn_order {attn_order!r}")
+        if attn_splits == "auto":
+            attn_splits = 4 if w["dtype"] == "bf16" else None
+        self.attn_order, self.attn_splits = attn_order, attn_splits
         B, H, Dh, d, V, K = w["B"], w["H"], w["Dh"], w["d"], w["V"], w["K"]
         T = tree.T
         self.B, self.T = B, T
@@ -131,9 +142,14 @@ class VerifyStep:
         side = side_stream if side_stream is not None else main
         if side is not main:
             side.wait_stream(main)
-        M.medusa_tree_attn(x["q"], x["k_new"], x["v_new"], x["k_cache"], x["v_cache"], x["seq_start"],
-                           x["prefix_len"], x["seq_cap"], self.tree, self.max_prefix, self.rope_theta,
-                           self.scale, self.out, self.ws_attn, self.err, side)
+
+        def attention():
+            M.medusa_tree_attn(x["q"], x["k_new"], x["v_new"], x["k_cache"], x["v_cache"], x["seq_start"],
+                               x["prefix_len"], x["seq_cap"], self.tree, self.max_prefix, self.rope_theta,
+                               self.scale, self.out, self.ws_attn, self.err, side, key_splits=self.attn_splits)
+
+        if self.attn_order == "first":
+            attention()
         if self.accept == "fused":
             M.medusa_lm_head_verify_stats(x["hidden"], self.w_lm_run, self.logits if self.write_logits else None,
                                           self.stats, self.mode, self.temperature, self.logits.shape[-1], self.err,
@@ -141,6 +157,8 @@ class VerifyStep:
         else:
             M.medusa_lm_head_verify(x["hidden"], self.w_lm_run, self.logits, None, self.err, main,
                                     layout=self.w_layout)
+        if self.attn_order == "after_lm":
+            attention()
         hs = heads_stream if heads_stream is not None else main
         if self.heads == "split":
             if hs is not main:

@@ -163,6 +163,12 @@ def test_validation_statuses(M):
                               1, FAKE, None, 0, None, None) == -1    # bf16 needs 16-byte alignment
     assert L.medusa_tree_attn(FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, ref, 17, 4, 64, 64, 1e4, 0.1,
                               1, FAKE, FAKE, 1 << 30, None, None) == -1
+    # key splits outside {1, 2, 4, 8}; fewer than 8 need bf16
+    for ks in (0, 3, 16, -1):
+        assert L.medusa_tree_attn_splits(FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, ref, 1, 4, 64, 64, 1e4,
+                                         0.1, 1, FAKE, FAKE, 1 << 30, ks, None, None) == -2
+    assert L.medusa_tree_attn_splits(FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, ref, 1, 4, 64, 64, 1e4,
+                                     0.1, 0, FAKE, FAKE, 1 << 30, 1, None, None) == -2
     # LM head: d not a multiple of 64 for bf16; misaligned pointers
     assert L.medusa_lm_head_verify(FAKE, FAKE, FAKE, 15, 100, 1000, 1, 0, None, 0, None, None) == -2
     assert L.medusa_lm_head_verify(FAKE + 2, FAKE, FAKE, 15, 256, 1000, 1, 0, None, 0, None, None) == -1

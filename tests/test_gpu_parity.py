@@ -76,8 +76,36 @@ ATTN_CASES = [
 ]
 
 
+_ATTN_ORACLE = {}
+
+
+def _attn_oracle(case, q, kn, vn, kc, vc, st, pl, ot, scale):
+    """The oracle's output and cache for one case (computed once per case)."""
+    key = repr(case)
+    if key not in _ATTN_ORACLE:
+        kc_o, vc_o = kc.copy(), vc.copy()
+        _, ref = oracle.tree_attn(q, kn, vn, kc_o, vc_o, st, pl, ot, 10000.0, scale)
+        _ATTN_ORACLE[key] = (ref, kc_o, vc_o)
+    return _ATTN_ORACLE[key]
+
+
 @pytest.mark.parametrize("case", ATTN_CASES, ids=lambda c: f"{c[0]}-H{c[1]}-Dh{c[2]}-L{c[3]}-{c[4][0]}")
 def test_tree_attn(M, case):
+    _check_tree_attn(M, case, None)
+
+
+# bf16 key splits other than the default 8 (one CTA per unit walks every key;
+# 512 tree rows make it cross several 64-node ancestor windows)
+SPLIT_CASES = [ATTN_CASES[i] for i in (3, 4, 7, 8, 9)]
+
+
+@pytest.mark.parametrize("key_splits", [1, 2, 4])
+@pytest.mark.parametrize("case", SPLIT_CASES, ids=lambda c: f"{c[0]}-H{c[1]}-Dh{c[2]}-L{c[3]}-{c[4][0]}")
+def test_tree_attn_key_splits(M, case, key_splits):
+    _check_tree_attn(M, case, key_splits)
+
+
+def _check_tree_attn(M, case, key_splits):
     dt, H, Dh, L, spec = case
     ot, dtree, q, kn, vn, kc, vc, st, pl, cap = _attn_case(M, dt, H, Dh, L, spec, seed=3)
     B, T = len(L), ot.T
@@ -88,12 +116,11 @@ def test_tree_attn(M, case):
     ws = torch.empty(M.medusa_tree_attn_workspace_size(B, H, Dh, T, max(L)), dtype=torch.uint8, device="cuda")
     e = err_flag()
     M.medusa_tree_attn(to_dev(q), to_dev(kn), to_dev(vn), kc_d, vc_d, to_dev(st), to_dev(pl), to_dev(cap),
-                       dtree, max(L), 10000.0, scale, out_d, ws, e)
+                       dtree, max(L), 10000.0, scale, out_d, ws, e, key_splits=key_splits)
     torch.cuda.synchronize()
     assert int(e.item()) == 0
     # oracle
-    kc_o, vc_o = kc.copy(), vc.copy()
-    _, ref = oracle.tree_attn(q, kn, vn, kc_o, vc_o, st, pl, ot, 10000.0, scale)
+    ref, kc_o, vc_o = _attn_oracle(case, q, kn, vn, kc, vc, st, pl, ot, scale)
     got = as_double(to_host(out_d))
     err = np.abs(got - ref).max()
     assert err <= TOL[dt]["attn"], f"attention max-abs error {err}"
