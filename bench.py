@@ -55,9 +55,10 @@ def parse_args():
                          "head's epilogue (fused)")
     ap.add_argument("--no-logits", dest="logits", action="store_false",
                     help="with --accept fused and greedy acceptance: do not write the logits")
-    ap.add_argument("--heads", choices=["split", "fused"], default="fused",
+    ap.add_argument("--heads", choices=["split", "fused", "joint"], default="fused",
                     help="heads' W1 over every tree row beside the acceptance, then W2 on the accepted "
-                         "row (split), or both projections on the accepted row after it (fused)")
+                         "row (split), W1 over every row inside the LM head's launch, then W2 (joint), or "
+                         "both projections on the accepted row after the acceptance (fused)")
     ap.add_argument("--attn-branch", choices=["serial", "fork"], default="fork",
                     help="tree attention before the LM head on one stream, or on a forked graph branch")
     ap.add_argument("--attn-order", choices=["first", "after_lm"], default="after_lm",
@@ -70,7 +71,7 @@ def parse_args():
 
 # ------------------------------------------------------------------ bytes --
 
-def algorithmic_bytes(w: dict, T: int, s_heads, L_list, split: bool, fused_accept: bool = False,
+def algorithmic_bytes(w: dict, T: int, s_heads, L_list, heads_mode: str, fused_accept: bool = False,
                       logits: bool = True) -> dict:
     """Bytes each call must move at least once per step (weights once, KV
     prefix once, activations and logits once each way)."""
@@ -98,8 +99,11 @@ def algorithmic_bytes(w: dict, T: int, s_heads, L_list, split: bool, fused_accep
     cand = B * T * 4
     out = dict(tree_attn=attn, lm_head_verify=lm, accept=accept, kv_compact=compact,
                build_candidates=cand)
-    if split:
+    if heads_mode == "split":
         out.update(heads_hidden=heads_hidden, heads_logits_topk=heads_w2)
+    elif heads_mode == "joint":  # W1 streams in the LM head's launch (hidden read once for both)
+        out["lm_head_verify"] += heads_hidden - B * T * d * e
+        out["heads_logits_topk"] = heads_w2
     else:
         out["heads_topk"] = heads
     out["step"] = sum(out.values())
@@ -225,11 +229,15 @@ def step_calls(st, x, s):
     """The step's library calls in stream order on one stream, as (name, call)."""
     from medusa_tree_speculative_gb300 import medusa as M
 
+    joint = st.heads == "joint"
     c = [("tree_attn", lambda: M.medusa_tree_attn(
             x["q"], x["k_new"], x["v_new"], x["k_cache"], x["v_cache"], x["seq_start"], x["prefix_len"],
             x["seq_cap"], st.tree, st.max_prefix, st.rope_theta, st.scale, st.out, st.ws_attn, st.err, s,
             key_splits=st.attn_splits)),
-         ("lm_head_verify", (lambda: M.medusa_lm_head_verify_stats(
+         ("lm_head_verify", (lambda: M.medusa_lm_head_verify_heads_hidden(
+             x["hidden"], st.w_lm_run, st.logits.shape[-1], st.logits, st.w1_run, st.b1, st.s_heads, st.u_all,
+             st.err, s, layout=st.w_layout, w1_layout=st.w1_layout)) if joint else
+          (lambda: M.medusa_lm_head_verify_stats(
              x["hidden"], st.w_lm_run, st.logits if st.write_logits else None, st.stats, st.mode, st.temperature,
              st.logits.shape[-1], st.err, s, layout=st.w_layout)) if st.accept == "fused" else
           (lambda: M.medusa_lm_head_verify(x["hidden"], st.w_lm_run, st.logits, None, st.err, s,
@@ -247,7 +255,7 @@ def step_calls(st, x, s):
           ("kv_compact", lambda: M.medusa_kv_compact(x["k_cache"], x["v_cache"], x["seq_start"], x["prefix_len"],
                                                      st.accepted_nodes, st.accept_len, st.tree.K, st.src_slots,
                                                      st.err, s))]
-    if st.heads == "split":
+    if st.heads in ("split", "joint"):
         c.append(("heads_logits_topk", lambda: M.medusa_heads_logits_topk(
             st.u_all, st.T, st.best_node, st.w2, st.s_heads, st.head_logits, st.topk, st.ws_w2, st.err, s)))
     else:
@@ -683,7 +691,7 @@ def main():
     if rank != 0:
         return
     peaks = load_peaks()
-    by = algorithmic_bytes(w, r["T"], r["s_heads"], r["L_list"], args.heads == "split", args.accept == "fused",
+    by = algorithmic_bytes(w, r["T"], r["s_heads"], r["L_list"], args.heads, args.accept == "fused" and args.heads != "joint",
                            args.logits or w["mode"] == "typical")
     fl = algorithmic_flops(w, r["T"], r["s_heads"], r["L_list"])
     ms = r["ms_step"]

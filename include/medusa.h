@@ -16,7 +16,9 @@
  *   medusa_kv_compact       accepted path's KV into place        (box 6)
  *   medusa_heads_topk       K Medusa heads + top-s               (box 1)
  *     (or: medusa_heads_hidden over every tree row, which can run beside the
- *      acceptance, then medusa_heads_logits_topk on the accepted row)
+ *      acceptance, then medusa_heads_logits_topk on the accepted row; or
+ *      medusa_lm_head_verify_heads_hidden in place of the LM head call, one
+ *      pass computing both, then medusa_heads_logits_topk)
  *   medusa_build_candidates next step's candidate tokens         (box 2)
  * In a decode loop, medusa_append_tokens (box step 6) appends each step's
  * tokens to the output.
@@ -344,7 +346,12 @@ size_t medusa_heads_topk_workspace_size(int B, int K, int d, int V,
  * medusa_accept's best_node); w1: device [K][d][d] (out x in); b1: device
  * [K][d] or NULL; w2: device [K][V][d]; s: host [K], 0 <= s[k] <= s_max <=
  * MEDUSA_MAX_S; head_logits: device [B][K][V] (rows of skipped heads are not
- * written); topk: device [B][K][s_max]. */
+ * written); topk: device [B][K][s_max].
+ * Both projections hand their rows out at run time from counters in the
+ * workspace, so that CTAs whose SMs are still busy with concurrent work take
+ * fewer rows.  Unlike other scratch, this workspace must be zero-filled
+ * (cudaMemset) before its first call; every call leaves the counters ready
+ * for the next one (zero it again only after a call that failed to launch). */
 int medusa_heads_topk(const void* hidden, const int32_t* last_node, int T,
                       const void* w1, const void* b1, const void* w2,
                       const int32_t* s, int K, int B, int d, int V,
@@ -371,6 +378,28 @@ int medusa_heads_hidden(const void* hidden, int rows, const void* w1,
                         medusa_w_layout w1_layout, const void* b1,
                         const int32_t* s, int K, int d, medusa_dtype dtype,
                         void* u, int32_t* err, void* stream);
+
+/* medusa_lm_head_verify and medusa_heads_hidden in one launch, bf16 only:
+ * the logits of every tree row and u (as medusa_heads_hidden) for every row
+ * and used head.  Both products take the same hidden rows as the MMA's N
+ * side, so one CTA streams its share of the W tiles and of the stacked W1
+ * tiles over a single pass of the hidden k-blocks; the launch takes the
+ * fewest CTAs (at most one per SM) that keep every CTA at no more than three
+ * (at most four) 128-row weight tiles, which leaves the other SMs free for
+ * concurrent work such as the tree attention.  Arguments as the two calls
+ * (w_lm [V][d] in w_layout, w1 [K][d][d] in w1_layout, b1 nullable, s host
+ * [K], logits [rows][V] fp32, u [rows][K][d] bf16).  rows <= 256, d a
+ * multiple of 128, 16-byte aligned tensors; MEDUSA_ERR_UNSUPPORTED when no
+ * plan fits (the caller then makes the two calls).  With no used head it is
+ * medusa_lm_head_verify. */
+int medusa_lm_head_verify_heads_hidden(const void* hidden, int rows, int d,
+                                       const void* w_lm,
+                                       medusa_w_layout w_layout, int V,
+                                       float* logits, const void* w1,
+                                       medusa_w_layout w1_layout,
+                                       const void* b1, const int32_t* s, int K,
+                                       void* u, medusa_dtype dtype,
+                                       int32_t* err, void* stream);
 
 /* Scratch bytes medusa_heads_logits_topk needs. */
 size_t medusa_heads_logits_topk_workspace_size(int B, int K, int V, int s_max);

@@ -12,15 +12,20 @@
 // HBM-bound GEMVs: 16-byte streaming loads, eight in flight per lane, the
 // input vector re-read from L1.  Two kernels:
 //   w1        u[b][k] = dtype(SiLU(W1_k h_b + b1_k) + h_b) into scratch.  A CTA
-//             takes four rows at a time, two warps per row (one half each),
-//             so the 16384 rows of a 7B-shaped step spread evenly over the
-//             CTAs; the halves meet in shared memory for the epilogue.
+//             takes four rows at a time, two warps per row (one half each);
+//             the halves meet in shared memory for the epilogue.
 //   w2_topk   head_logits[b][k] = W2_k u[b][k] (fp32), fused with top-s: a
-//             CTA owns a contiguous slice of one head's vocabulary; after its
-//             warps have streamed the slice it selects the slice's top S from
-//             the logits it just wrote (per-thread sorted lists merged warp by
-//             warp), and the last CTA of a head to finish merges every CTA's
-//             list into topk (value descending, index ascending).
+//             fixed set of CTAs serves each head; after its warps have
+//             streamed their rows a CTA selects their top S from the logits it
+//             just wrote (per-thread sorted lists merged warp by warp), and
+//             the last CTA of a head to finish merges every CTA's list into
+//             topk (value descending, index ascending).
+// Rows are handed out at run time, not split up front: W1's row quads and
+// each head's W2 rows come from atomic counters, the next one requested
+// before the current one is streamed.  CTAs whose SMs are busy with other
+// work when the call starts, or that get less bandwidth, then take fewer
+// rows, and the call ends within about one row's time of the last free one
+// instead of waiting for the slowest fixed share.
 #include <math.h>
 
 #include <algorithm>
@@ -34,6 +39,7 @@ namespace {
 constexpr int kWarps = 8;  // 256-thread CTAs
 constexpr int UNROLL = 8;  // 16-byte loads in flight per lane
 constexpr int kMaxS = MEDUSA_MAX_S;
+constexpr int kMaxGroups = 128;  // W2 row groups one CTA may take (recorded for its top-s)
 
 struct HeadsArgs {
   const void* w1;      // [K][d][d]
@@ -52,7 +58,10 @@ struct HeadsArgs {
   float* cand_v;                // [nused][B][cpc][kMaxS] per-CTA candidates (scratch)
   int* cand_i;
   int* counters;                // [nused] CTA arrivals per head, zeroed by w1
+  int* rowctr;                  // [nused] W2 row groups handed out per head, zeroed by w1
+  int* w1ctr;                   // W1 row quads handed out; zeroed by w2 for the next call
   int cpc;                      // w2 CTAs per used head
+  int rgroup;                   // W2 rows per warp in a group of kWarps * rgroup rows
   int32_t* err;
 };
 
@@ -105,7 +114,11 @@ template <typename TE, int NB>
 __global__ void __launch_bounds__(kWarps * 32) heads_w1_kernel(const __grid_constant__ HeadsArgs a) {
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   __shared__ float part[kWarps][NB];
-  if (blockIdx.x == 0 && threadIdx.x < a.nused) a.counters[threadIdx.x] = 0;  // for w2_topk
+  __shared__ int s_q;
+  if (blockIdx.x == 0 && threadIdx.x < a.nused) {  // for w2_topk
+    a.counters[threadIdx.x] = 0;
+    a.rowctr[threadIdx.x] = 0;
+  }
 
   // h_b = hidden[b][last_node[b]]; an out-of-range node reads row 0 and raises the error bit
   const TE* x[NB];
@@ -124,7 +137,11 @@ __global__ void __launch_bounds__(kWarps * 32) heads_w1_kernel(const __grid_cons
   const int64_t total = (int64_t)a.nused * a.d;
   const int64_t nquads = (total + kWarps / 2 - 1) / (kWarps / 2);
   const int hf = warp & 1;
-  for (int64_t q = blockIdx.x; q < nquads; q += gridDim.x) {
+  if (threadIdx.x == 0) s_q = atomicAdd(a.w1ctr, 1);
+  __syncthreads();
+  for (int64_t q = s_q; q < nquads;) {
+    int qn = 0;
+    if (threadIdx.x == 0) qn = atomicAdd(a.w1ctr, 1);  // the next quad; waited for after this one's loads
     const int64_t g = q * (kWarps / 2) + (warp >> 1);  // row of the stacked used heads
     float acc[NB];
 #pragma unroll
@@ -153,7 +170,9 @@ __global__ void __launch_bounds__(kWarps * 32) heads_w1_kernel(const __grid_cons
       const float silu = y / (1.f + expf(-y));
       static_cast<TE*>(a.u)[((int64_t)b * a.K + k) * a.d + j] = from_f32<TE>(silu + to_f32(x[b][j]));
     }
+    if (threadIdx.x == 0) s_q = qn;  // every thread read the current quad before the barrier above
     __syncthreads();
+    q = s_q;
   }
 }
 
@@ -227,10 +246,11 @@ __global__ void __launch_bounds__(kWarps * 32) heads_w2_topk_kernel(const __grid
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int slot = blockIdx.x / a.cpc, part = blockIdx.x % a.cpc;
   const int k = a.heads[slot];
-  const int j0 = (int)((int64_t)part * a.V / a.cpc), j1 = (int)((int64_t)(part + 1) * a.V / a.cpc);
   __shared__ float wv[32][S];
   __shared__ int wi[32][S];
   __shared__ bool last;
+  __shared__ int s_grp[kMaxGroups];  // row groups this CTA streamed
+  __shared__ int s_g[2];
 
   const TE* x[NB];
 #pragma unroll
@@ -249,29 +269,55 @@ __global__ void __launch_bounds__(kWarps * 32) heads_w2_topk_kernel(const __grid
   }
   const TE* W = static_cast<const TE*>(a.w2) + (int64_t)k * a.V * a.d;
   const int nvec = a.d / Vec<TE>::N;
-  for (int j = j0 + warp; j < j1; j += kWarps) {
-    float acc[NB];
+  // this head's rows in groups of GR = kWarps * RW (RW consecutive rows per
+  // warp) from its counter; a CTA stops taking groups at kMaxGroups (the host
+  // sizes RW so that the CTAs of the head can hold every group twice over),
+  // so every group is streamed and recorded exactly once
+  const int RW = a.rgroup, GR = kWarps * RW;
+  const int ngroups = (a.V + GR - 1) / GR;
+  int* ctr = a.rowctr + slot;
+  if (threadIdx.x == 0) s_g[0] = atomicAdd(ctr, 1);
+  if (blockIdx.x == 0 && threadIdx.x == 32 && a.w1ctr) *a.w1ctr = 0;  // this call's w1 is done
+  __syncthreads();
+  int g = s_g[0], cnt = 0;
+  for (int it = 0; g < ngroups; ++it) {
+    int gn = ngroups;
+    if (threadIdx.x == 0 && cnt + 1 < kMaxGroups)
+      gn = atomicAdd(ctr, 1);  // the next group; waited for after this one's loads
+    if (threadIdx.x == 0) s_grp[cnt] = g;
+    ++cnt;
+    const int jb = g * GR + warp * RW;
+    const int je = min(a.V, jb + RW);
+    for (int j = jb; j < je; ++j) {
+      float acc[NB];
 #pragma unroll
-    for (int b = 0; b < NB; ++b) acc[b] = 0.f;
-    dot_rows<TE, NB>(W + (int64_t)j * a.d, x, nvec, a.B, lane, acc);
+      for (int b = 0; b < NB; ++b) acc[b] = 0.f;
+      dot_rows<TE, NB>(W + (int64_t)j * a.d, x, nvec, a.B, lane, acc);
 #pragma unroll
-    for (int b = 0; b < NB; ++b) acc[b] = warp_sum(acc[b]);
-    if (lane < a.B && lane < NB) {
-      float y = 0.f;
+      for (int b = 0; b < NB; ++b) acc[b] = warp_sum(acc[b]);
+      if (lane < a.B && lane < NB) {
+        float y = 0.f;
 #pragma unroll
-      for (int b = 0; b < NB; ++b)
-        if (b == lane) y = acc[b];
-      a.logits[((int64_t)lane * a.K + k) * a.V + j] = y;
+        for (int b = 0; b < NB; ++b)
+          if (b == lane) y = acc[b];
+        a.logits[((int64_t)lane * a.K + k) * a.V + j] = y;
+      }
     }
+    if (threadIdx.x == 0) s_g[(it + 1) & 1] = gn;  // the other slot: read by all before the last barrier
+    __syncthreads();
+    g = s_g[(it + 1) & 1];
   }
   __syncthreads();  // this CTA's logits are written (visible to the whole CTA)
 
-  // this CTA's top S of its slice, per sequence, selected after the stream
+  // this CTA's top S of its rows, per sequence, selected after the stream
   for (int b = 0; b < a.B; ++b) {
     const float* z = a.logits + ((int64_t)b * a.K + k) * a.V;
     TopList<S> L;
     L.init();
-    for (int j = j0 + threadIdx.x; j < j1; j += blockDim.x) L.insert(z[j], j);
+    for (int e = threadIdx.x; e < cnt * GR; e += blockDim.x) {
+      const int j = s_grp[e / GR] * GR + e % GR;
+      if (j < a.V) L.insert(z[j], j);
+    }
     float ov[S];
     int oi[S];
     block_select<S>(L, wv, wi, ov, oi);
@@ -315,7 +361,10 @@ __global__ void __launch_bounds__(kWarps * 32) heads_w2_topk_kernel(const __grid
     }
     __syncthreads();
   }
-  if (threadIdx.x == 0) a.counters[slot] = 0;  // ready for the next call
+  if (threadIdx.x == 0) {  // ready for the next call (every CTA of the head has stopped taking rows)
+    a.counters[slot] = 0;
+    a.rowctr[slot] = 0;
+  }
 }
 
 // W2 CTAs per used head: about four per SM in total, at least 8 rows each.
@@ -362,7 +411,15 @@ int launch_heads_b(const HeadsArgs& a, int smax_used, cudaStream_t s) {
   return launch_heads<TE, MEDUSA_MAX_B>(a, smax_used, s);
 }
 
-// Scratch: u [B][K][d] | candidate values | candidate indices | counters.
+// W2 rows per warp in a group: the smallest count with which the CTAs serving
+// one head can record every group at half their capacity.
+int w2_row_group(int cpc, int V) {
+  const int64_t cap = (int64_t)cpc * kWarps * (kMaxGroups / 2);
+  return (int)std::max<int64_t>(1, (V + cap - 1) / cap);
+}
+
+// Scratch: u [B][K][d] | candidate values | candidate indices | counters
+// (CTA arrivals [MEDUSA_MAX_K], W2 row groups [MEDUSA_MAX_K], W1 quads [1]).
 struct Layout {
   size_t u, cand, counters, total;
 };
@@ -370,7 +427,7 @@ Layout heads_layout(int B, int K, int nused, int d, int V) {
   Layout l;
   l.u = align_up((size_t)B * K * d * sizeof(float), 256);  // fp32 size covers both element types
   l.cand = align_up((size_t)nused * B * w2_ctas_per_head(nused, V) * kMaxS * 4, 256);
-  l.counters = align_up((size_t)MEDUSA_MAX_K * sizeof(int), 256);
+  l.counters = align_up((size_t)(2 * MEDUSA_MAX_K + 1) * sizeof(int), 256);
   l.total = l.u + 2 * l.cand + l.counters;
   return l;
 }
@@ -431,7 +488,10 @@ extern "C" int medusa_heads_topk(const void* hidden, const int32_t* last_node, i
   a.cand_v = reinterpret_cast<float*>(ws + l.u);
   a.cand_i = reinterpret_cast<int*>(ws + l.u + l.cand);
   a.counters = reinterpret_cast<int*>(ws + l.u + 2 * l.cand);
+  a.rowctr = a.counters + MEDUSA_MAX_K;
+  a.w1ctr = a.counters + 2 * MEDUSA_MAX_K;
   a.cpc = w2_ctas_per_head(a.nused, V);
+  a.rgroup = w2_row_group(a.cpc, V);
   a.logits = head_logits; a.topk = topk; a.err = err;
   cudaStream_t st = as_stream(stream);
   return dtype == MEDUSA_BF16 ? launch_heads_b<uint16_t>(a, smax_used, st)
@@ -489,7 +549,9 @@ extern "C" int medusa_heads_logits_topk(const void* u, int T, const int32_t* nod
   a.cand_v = reinterpret_cast<float*>(ws);
   a.cand_i = reinterpret_cast<int*>(ws + l.cand);
   a.counters = reinterpret_cast<int*>(ws + 2 * l.cand);
+  a.rowctr = a.counters + MEDUSA_MAX_K;
   a.cpc = w2_ctas_per_head(a.nused, V);
+  a.rgroup = w2_row_group(a.cpc, V);
   a.logits = head_logits; a.topk = topk; a.err = err;
   cudaStream_t st = as_stream(stream);
   return dtype == MEDUSA_BF16 ? launch_w2_b<uint16_t>(a, smax_used, st, fn)

@@ -56,6 +56,7 @@ constexpr int BK = 64;         // k per stage: 128 bytes of bf16, one swizzle sp
 constexpr int UK = 16;         // k per MMA instruction
 constexpr int kThreads = 192;  // 6 warps
 constexpr int kMaxN = 256;     // tree rows per chunk (MMA N)
+constexpr int kMaxTiles = 4;   // weight tiles per work item (sharing each hidden k-block)
 constexpr size_t kSmemBudget = 200 * 1024;
 
 struct LmArgs {
@@ -89,6 +90,12 @@ struct LmArgs {
   float inv_temp;
   int write_logits;
   uint32_t part_off;  // byte offset of the per-warp partial records in shared memory
+  // joint launch (LM head and the heads' first projection in one pass over
+  // the same hidden k-blocks): CTA c owns vocabulary tiles [c*lm_tiles/G,
+  // (c+1)*lm_tiles/G) of W and stacked W1 tiles [c*w1_tiles/G, ...) of the
+  // second map, G = gridDim.x; mode 0 epilogue on the former (V rows), mode 1
+  // on the latter (Vu = used heads * d rows)
+  int lm_tiles, w1_tiles, tiled1, Vu;
   int32_t* err;
 };
 
@@ -158,6 +165,32 @@ MDEV int weight_block(const LmArgs& a, int tile) {
   return a.heads[tile / a.tpr] * a.tpr + tile % a.tpr;
 }
 
+// Where tile t of a work item comes from and how its epilogue runs.
+struct TileSrc {
+  int sel;   // 0: the W map, 1: the W1 map (joint launch)
+  int blk;   // 128-row weight block in that map (a.oob_block: past the tensor, reads zeros)
+  int mode;  // epilogue: 0 logits, 1 head projection u, -1 none (padding tile)
+  int v0;    // first output row of the tile (vocabulary row, or stacked W1 row)
+  int rs;    // residual slot of a mode-1 tile
+};
+template <bool JOINT>
+MDEV TileSrc tile_src(const LmArgs& a, int item, int t) {
+  if (!JOINT) {
+    const int tile = (item / a.nchunks) * a.nt + t;
+    return TileSrc{0, weight_block(a, tile), a.mode, tile * BM, t};
+  }
+  const int G = (int)gridDim.x;
+  const int l0 = (int)((int64_t)item * a.lm_tiles / G), l1 = (int)((int64_t)(item + 1) * a.lm_tiles / G);
+  const int w0 = (int)((int64_t)item * a.w1_tiles / G), w1 = (int)((int64_t)(item + 1) * a.w1_tiles / G);
+  if (t < l1 - l0) return TileSrc{0, l0 + t, 0, (l0 + t) * BM, 0};
+  const int k = t - (l1 - l0);
+  if (k < w1 - w0) {
+    const int tile = w0 + k;
+    return TileSrc{1, a.heads[tile / a.tpr] * a.tpr + tile % a.tpr, 1, tile * BM, k};
+  }
+  return TileSrc{0, a.oob_block, -1, 0, 0};
+}
+
 MDEV bool wait_or_abort(uint64_t* bar, uint32_t parity, volatile int* abort_flag) {
   for (uint32_t i = 0; i < kSpinLimit; ++i) {
     if (mbar_try_wait(bar, parity)) return true;
@@ -169,10 +202,12 @@ MDEV bool wait_or_abort(uint64_t* bar, uint32_t parity, volatile int* abort_flag
 
 // STATS: the epilogue also produces the acceptance statistics (a separate
 // instantiation, so that the plain path keeps its registers and barriers).
-template <bool STATS>
+// JOINT: one work item per CTA mixing W and W1 tiles (tile_src).
+template <bool STATS, bool JOINT>
 __global__ void __launch_bounds__(kThreads, 1)
     lm_head_tc_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CUtensorMap tmH,
-                      const __grid_constant__ LmArgs a) {
+                      const __grid_constant__ CUtensorMap tmW1, const __grid_constant__ LmArgs a) {
+  static_assert(!(STATS && JOINT), "the joint launch has no statistics epilogue");
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   const uint32_t a_bytes = (uint32_t)a.nt * BM * BK * 2;  // nt W tiles, 16 KB each
@@ -203,6 +238,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     s_abort = 0;
     tma_prefetch_desc(&tmW);
     tma_prefetch_desc(&tmH);
+    if (JOINT) tma_prefetch_desc(&tmW1);
   }
   if (warp == 1) {
     tmem_alloc(tmem_slot, a.tmem_cols);
@@ -214,7 +250,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint32_t tmem_base = *tmem_slot;
   volatile int* abort_flag = &s_abort;
 
-  const int items = a.ngroups * a.nchunks;
+  const int items = JOINT ? (int)gridDim.x : a.ngroups * a.nchunks;
   const uint32_t acc_cols = (uint32_t)(a.nt * a.npad);  // one accumulator: nt tiles side by side
   const int i0 = (int)((long)blockIdx.x * items / gridDim.x);
   const int i1 = (int)((long)(blockIdx.x + 1) * items / gridDim.x);
@@ -226,10 +262,14 @@ __global__ void __launch_bounds__(kThreads, 1)
       int it = 0;
       bool ok = true;
       for (int item = i0; item < i1 && ok; ++item) {
-        const int v0 = (item / a.nchunks) * a.nt * BM;
         const int r0 = (item % a.nchunks) * a.npad;
-        int blk[2];  // weight blocks of the item's tiles (rows past V, a missing second tile, read zeros)
-        for (int t = 0; t < a.nt; ++t) blk[t] = weight_block(a, v0 / BM + t);
+        // weight blocks of the item's tiles (rows past V, a missing tile, read zeros)
+        int blk[kMaxTiles], sel[kMaxTiles];
+        for (int t = 0; t < a.nt; ++t) {
+          const TileSrc ts = tile_src<JOINT>(a, item, t);
+          blk[t] = ts.blk;
+          sel[t] = ts.sel;
+        }
         for (int kb = 0; kb < nkb; ++kb, ++it) {
           const int s = it % a.stages;
           const uint32_t ph = (uint32_t)(it / a.stages) & 1u;
@@ -237,10 +277,11 @@ __global__ void __launch_bounds__(kThreads, 1)
           uint8_t* st = smem + (size_t)s * stage_bytes;
           mbar_expect_tx(&full[s], stage_bytes);
           for (int t = 0; t < a.nt; ++t) {
-            if (a.tiled)
-              tma_load_2d(st + t * (BM * BK * 2), &tmW, &full[s], 0, (blk[t] * nkb + kb) * BM);
+            const CUtensorMap* m = JOINT && sel[t] ? &tmW1 : &tmW;
+            if (JOINT && sel[t] ? a.tiled1 : a.tiled)
+              tma_load_2d(st + t * (BM * BK * 2), m, &full[s], 0, (blk[t] * nkb + kb) * BM);
             else
-              tma_load_2d(st + t * (BM * BK * 2), &tmW, &full[s], kb * BK, blk[t] * BM);
+              tma_load_2d(st + t * (BM * BK * 2), m, &full[s], kb * BK, blk[t] * BM);
           }
           tma_load_2d(st + a_bytes, &tmH, &full[s], kb * BK, r0);
         }
@@ -293,24 +334,27 @@ __global__ void __launch_bounds__(kThreads, 1)
     // mode 1: the residual values this thread will need, staged in shared
     // memory while the main loop runs (loads issued after the weight stream
     // has saturated HBM would each wait out the loaded latency)
+    const int u_rows = JOINT ? a.Vu : a.V;  // stacked W1 rows of the used heads
     auto load_res = [&](int item) {
       const int r0 = (item % a.nchunks) * a.npad;
       for (int t = 0; t < a.nt; ++t) {
-        const int v = (item / a.nchunks) * a.nt * BM + t * BM + 32 * g + lane;
+        const TileSrc ts = tile_src<JOINT>(a, item, t);
+        if (ts.mode != 1) continue;
+        const int v = ts.v0 + 32 * g + lane;
         const int j = v % a.d;
         for (int i0 = 0; i0 < a.npad; i0 += 16) {  // 16 loads in flight, then 16 stores
           uint16_t hv[16];
 #pragma unroll
           for (int i = 0; i < 16; ++i) {
             const int row = r0 + i0 + i;
-            hv[i] = (v < a.V && row < a.rows) ? __ldg(a.hidden + (int64_t)row * a.d + j) : (uint16_t)0;
+            hv[i] = (v < u_rows && row < a.rows) ? __ldg(a.hidden + (int64_t)row * a.d + j) : (uint16_t)0;
           }
 #pragma unroll
-          for (int i = 0; i < 16; ++i) res[(t * a.npad + i0 + i) * BM + 32 * g + lane] = hv[i];
+          for (int i = 0; i < 16; ++i) res[(ts.rs * a.npad + i0 + i) * BM + 32 * g + lane] = hv[i];
         }
       }
     };
-    if (a.mode == 1 && i0 < i1) load_res(i0);
+    if ((JOINT || a.mode == 1) && i0 < i1) load_res(i0);
     int local = 0;
     for (int item = i0; item < i1; ++item, ++local) {
       const int acc = local & 1;
@@ -325,7 +369,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       tc_fence_after();
       const int r0 = (item % a.nchunks) * a.npad;
       for (int t = 0; t < a.nt; ++t) {
-        const int v = (item / a.nchunks) * a.nt * BM + t * BM + 32 * g + lane;
+        const TileSrc ts = tile_src<JOINT>(a, item, t);
+        if (JOINT && ts.mode < 0) continue;  // padding tile: nothing to store
+        const int v = ts.v0 + 32 * g + lane;
+        const int tmode = JOINT ? ts.mode : a.mode;
         for (int c = 0; c < a.npad / 16; ++c) {
           uint32_t r[16];
           tmem_ld_32x32b_x16(tmem_base + ((uint32_t)(32 * g) << 16) + (uint32_t)acc * acc_cols +
@@ -348,8 +395,8 @@ __global__ void __launch_bounds__(kThreads, 1)
               part[(t * 4 + g) * a.npad + c * 16 + tr_column(lane)] =
                   make_float4(red.v, __int_as_float(red.i), red.S, red.A);
           }
-          if (v < a.V) {
-            if (a.mode == 0) {
+          if (v < (tmode == 0 ? a.V : u_rows)) {
+            if (tmode == 0) {
               if (a.write_logits) {
 #pragma unroll
                 for (int i = 0; i < 16; ++i) {
@@ -366,7 +413,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 if (row < a.rows) {
                   const float y = __uint_as_float(r[i]) + bias;
                   const float silu = y / (1.f + expf(-y));
-                  const float h = bf16_bits_to_f32(res[(t * a.npad + c * 16 + i) * BM + 32 * g + lane]);
+                  const float h = bf16_bits_to_f32(res[(ts.rs * a.npad + c * 16 + i) * BM + 32 * g + lane]);
                   a.u[((int64_t)row * a.K + k) * a.d + j] = f32_to_bf16_bits(silu + h);
                 }
               }
@@ -390,7 +437,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         epilogue_sync();
       }
-      if (a.mode == 1 && item + 1 < i1) {
+      if ((JOINT || a.mode == 1) && item + 1 < i1) {
         __syncwarp();
         load_res(item + 1);  // this warp's own slice of the tile: no other warp reads it
       }
@@ -508,6 +555,14 @@ extern "C" int medusa_lm_head_tile(const void* w_lm, void* w_tiled, int d, int V
 namespace medusa {
 namespace {
 
+// Map of a weight matrix with `wrows` rows of d: row-major, or its tile copy
+// (then a [blocks * (d / 64) * 128][64] matrix whose 128-row boxes are the tiles).
+bool make_weight_map(CUtensorMap* m, const void* w, bool tiled, int64_t wrows, int d) {
+  const int64_t wblocks = (wrows + BM - 1) / BM;
+  return tiled ? make_map(m, w, (uint64_t)BK, (uint64_t)wblocks * BM * (d / BK), BM)
+               : make_map(m, w, (uint64_t)d, (uint64_t)wrows, BM);
+}
+
 // Plan and launch the tensor-core GEMM: `a` carries the epilogue fields; the
 // weight tensor has `wrows` rows of d (row-major) or is its tile copy.
 // Work plan along M: row chunks of at most kMaxN (padded to 16), and whether
@@ -536,20 +591,30 @@ int launch_tc(LmArgs& a, const void* w, bool tiled, int64_t wrows, const void* h
   const int64_t wblocks = (wrows + BM - 1) / BM;
   a.oob_block = (int)wblocks;
   CUtensorMap tmW, tmH;
-  // tiled: a [blocks * (d / 64) * 128][64] matrix whose 128-row boxes are the tiles
-  const bool okw = tiled ? make_map(&tmW, w, (uint64_t)BK, (uint64_t)wblocks * BM * (d / BK), BM)
-                         : make_map(&tmW, w, (uint64_t)d, (uint64_t)wrows, BM);
-  if (!okw || !make_map(&tmH, hidden, (uint64_t)d, (uint64_t)rows, (uint32_t)a.npad))
+  if (!make_weight_map(&tmW, w, tiled, wrows, d) || !make_map(&tmH, hidden, (uint64_t)d, (uint64_t)rows, (uint32_t)a.npad))
     return fail(MEDUSA_ERR_CUDA, "%s: cuTensorMapEncodeTiled failed", fn);
   const size_t smem = 1024 + a.part_off + part_bytes;  // ring | barriers | residuals | partial records
-  auto kern = a.stat_mode ? lm_head_tc_kernel<true> : lm_head_tc_kernel<false>;
+  auto kern = a.stat_mode ? lm_head_tc_kernel<true, false> : lm_head_tc_kernel<false, false>;
   cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   // balanced: every CTA gets ceil or floor of items / grid work items
   const int items = a.ngroups * a.nchunks;
   const int per_cta = (items + sm_count() - 1) / sm_count();
   const int grid = (items + per_cta - 1) / per_cta;
-  launch_kernel(kern, dim3(grid), dim3(kThreads), smem, s, tmW, tmH, a);
+  launch_kernel(kern, dim3(grid), dim3(kThreads), smem, s, tmW, tmH, tmW, a);
   return check_launch(fn);
+}
+
+// Joint plan: the fewest CTAs (at most one per SM) whose shares of the W and
+// W1 tiles add up to at most nt tiles, for the smallest nt that has one.
+// Fewer CTAs leave SMs free for concurrent work; every CTA streams at most nt
+// tiles over one shared pass of the hidden k-blocks.  False if none fits.
+bool plan_joint(int lm_tiles, int w1_tiles, int npad, int& nt, int& grid) {
+  for (nt = 2; nt <= kMaxTiles; ++nt) {
+    if (nt * npad > 512) break;  // one accumulator of nt tiles in TMEM
+    for (grid = 1; grid <= sm_count(); ++grid)
+      if ((lm_tiles + grid - 1) / grid + (w1_tiles + grid - 1) / grid <= nt) return true;
+  }
+  return false;
 }
 
 // f32 heads projection: one warp per (row, used head, output j).
@@ -647,6 +712,69 @@ extern "C" int medusa_heads_hidden(const void* hidden, int rows, const void* w1,
   launch_kernel(heads_hidden_f32_kernel, dim3((unsigned)((warps + 7) / 8)), dim3(256), 0, s,
                 static_cast<const float*>(hidden), static_cast<const float*>(w1), static_cast<const float*>(b1),
                 static_cast<float*>(u), rows, d, K, nused, hs);
+  return check_launch(fn);
+}
+
+extern "C" int medusa_lm_head_verify_heads_hidden(const void* hidden, int rows, int d, const void* w_lm,
+                                                  medusa_w_layout w_layout, int V, float* logits, const void* w1,
+                                                  medusa_w_layout w1_layout, const void* b1, const int32_t* s_k,
+                                                  int K, void* u, medusa_dtype dtype, int32_t* err, void* stream) {
+  const char* fn = "medusa_lm_head_verify_heads_hidden";
+  if (!hidden || !w_lm || !logits || !w1 || !s_k || !u) return fail(MEDUSA_ERR_INVALID, "%s: NULL tensor", fn);
+  if (rows < 1 || d < 1 || V < 1 || K < 1)
+    return fail(MEDUSA_ERR_INVALID, "%s: rows=%d d=%d V=%d K=%d", fn, rows, d, V, K);
+  if (K > MEDUSA_MAX_K) return fail(MEDUSA_ERR_UNSUPPORTED, "%s: K=%d above the maximum", fn, K);
+  for (medusa_w_layout l : {w_layout, w1_layout})
+    if (l != MEDUSA_W_ROWS && l != MEDUSA_W_TILES) return fail(MEDUSA_ERR_INVALID, "%s: layout=%d", fn, (int)l);
+  if (dtype != MEDUSA_BF16) return fail(MEDUSA_ERR_UNSUPPORTED, "%s: bf16 only", fn);
+  if (d % BM) return fail(MEDUSA_ERR_UNSUPPORTED, "%s: d=%d not a multiple of %d", fn, d, BM);
+  if (rows > kMaxN) return fail(MEDUSA_ERR_UNSUPPORTED, "%s: rows=%d above %d", fn, rows, kMaxN);
+  if ((reinterpret_cast<uintptr_t>(hidden) | reinterpret_cast<uintptr_t>(w_lm) | reinterpret_cast<uintptr_t>(w1) |
+       reinterpret_cast<uintptr_t>(u)) % 16)
+    return fail(MEDUSA_ERR_INVALID, "%s: hidden / w_lm / w1 / u not 16-byte aligned", fn);
+  LmArgs a{};
+  int nused = 0;
+  for (int k = 0; k < K; ++k) {
+    if (s_k[k] < 0) return fail(MEDUSA_ERR_INVALID, "%s: s[%d]=%d", fn, k, s_k[k]);
+    if (s_k[k] > 0) a.heads[nused++] = k;
+  }
+  cudaStream_t s = as_stream(stream);
+  if (nused == 0)
+    return medusa_lm_head_verify(hidden, w_lm, logits, rows, d, V, dtype, w_layout, nullptr, 0, err, stream);
+  a.logits = logits; a.V = V; a.err = err; a.rows = rows; a.d = d;
+  a.mode = 0; a.write_logits = 1;
+  a.hidden = static_cast<const uint16_t*>(hidden);
+  a.b1 = static_cast<const uint16_t*>(b1);
+  a.u = static_cast<uint16_t*>(u);
+  a.K = K; a.tpr = d / BM;
+  a.lm_tiles = (V + BM - 1) / BM;
+  a.w1_tiles = nused * (d / BM);
+  a.Vu = nused * d;
+  a.tiled = w_layout == MEDUSA_W_TILES;
+  a.tiled1 = w1_layout == MEDUSA_W_TILES;
+  a.nchunks = 1;
+  a.npad = (rows + 15) / 16 * 16;
+  a.ntiles = a.lm_tiles;
+  a.oob_block = a.lm_tiles;  // a block past W: its loads read zeros
+  int grid = 0;
+  if (!plan_joint(a.lm_tiles, a.w1_tiles, a.npad, a.nt, grid))
+    return fail(MEDUSA_ERR_UNSUPPORTED, "%s: no joint plan for %d + %d tiles", fn, a.lm_tiles, a.w1_tiles);
+  a.ngroups = grid;
+  const size_t stage_bytes = (size_t)a.nt * BM * BK * 2 + (size_t)a.npad * BK * 2;
+  const size_t res_bytes = (size_t)((a.w1_tiles + grid - 1) / grid) * a.npad * BM * 2;
+  a.stages = (int)std::min<size_t>(8, (kSmemBudget - 1024 - 256 - res_bytes) / stage_bytes);
+  if (a.stages < 2) return fail(MEDUSA_ERR_UNSUPPORTED, "%s: shared memory for %d tiles", fn, a.nt);
+  a.part_off = (uint32_t)align_up((size_t)a.stages * stage_bytes + 1024 + res_bytes, 16);
+  uint32_t cols = 32;
+  while (cols < (uint32_t)(a.nt * a.npad)) cols <<= 1;  // one accumulator: one work item per CTA
+  a.tmem_cols = cols;
+  CUtensorMap tmW, tmH, tmW1;
+  if (!make_weight_map(&tmW, w_lm, a.tiled, V, d) || !make_weight_map(&tmW1, w1, a.tiled1, (int64_t)K * d, d) ||
+      !make_map(&tmH, hidden, (uint64_t)d, (uint64_t)rows, (uint32_t)a.npad))
+    return fail(MEDUSA_ERR_CUDA, "%s: cuTensorMapEncodeTiled failed", fn);
+  const size_t smem = 1024 + a.part_off;
+  cudaFuncSetAttribute(lm_head_tc_kernel<false, true>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  launch_kernel(lm_head_tc_kernel<false, true>, dim3(grid), dim3(kThreads), smem, s, tmW, tmH, tmW1, a);
   return check_launch(fn);
 }
 

@@ -60,6 +60,7 @@ _SIGS = {
     "medusa_heads_topk": (I, [P, P, I, P, P, P, P, I, I, I, I, I, P, P, I, P, SZ, P, P]),
     "medusa_build_candidates": (I, [P, P, I, I, TREE, I, P, P]),
     "medusa_heads_hidden": (I, [P, I, P, I, P, P, I, I, I, P, P, P]),
+    "medusa_lm_head_verify_heads_hidden": (I, [P, I, I, P, I, I, P, P, I, P, P, I, P, I, P, P]),
     "medusa_append_tokens": (I, [P, P, P, I, I, I, P, P, I, P, P]),
     "medusa_lm_head_stat_groups": (I, [I, I]),
     "medusa_lm_head_verify_stats": (I, [P, P, P, I, I, I, I, I, I, F, P, SZ, P, P]),
@@ -315,6 +316,19 @@ def medusa_heads_hidden(hidden, w1, b1, s, u, err=None, stream=None, layout=W_RO
     s_arr = np.ascontiguousarray(s, np.int32)
     _check(_lib.medusa_heads_hidden(_ptr(hidden), rows, _ptr(w1), layout, _ptr(b1), _ptr(s_arr), len(s_arr), d,
                                     _dtype(hidden), _ptr(u), _ptr(err), _stream(stream)), "medusa_heads_hidden")
+
+
+def medusa_lm_head_verify_heads_hidden(hidden, w_lm, V, logits, w1, b1, s, u, err=None, stream=None,
+                                       layout=W_ROWS, w1_layout=W_ROWS):
+    """logits [rows][V] and u [rows][K][d] in one launch (bf16).  w_lm: [V][d], or its tile copy (flat)
+    with layout=W_TILES; w1: [K][d][d], or the tile copy of w1 seen as [K*d][d] with w1_layout=W_TILES."""
+    d = hidden.shape[-1]
+    rows = hidden.numel() // d
+    s_arr = np.ascontiguousarray(s, np.int32)
+    _check(_lib.medusa_lm_head_verify_heads_hidden(_ptr(hidden), rows, d, _ptr(w_lm), layout, int(V), _ptr(logits),
+                                                   _ptr(w1), w1_layout, _ptr(b1), _ptr(s_arr), len(s_arr), _ptr(u),
+                                                   _dtype(hidden), _ptr(err), _stream(stream)),
+           "medusa_lm_head_verify_heads_hidden")
 
 
 def medusa_heads_logits_topk_workspace_size(B, K, V, s_max) -> int:

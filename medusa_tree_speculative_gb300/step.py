@@ -9,7 +9,9 @@ for the next step):
   heads = medusa_heads_topk on the accepted node ("fused"), or ("split")
   medusa_heads_hidden over every tree row -- forked after the LM head so that
   it runs beside the acceptance -- then medusa_heads_logits_topk on the
-  accepted node's row.
+  accepted node's row, or ("joint", bf16) medusa_lm_head_verify_heads_hidden
+  in place of the LM head call (logits and every row's u in one pass) and
+  then medusa_heads_logits_topk.
 """
 from __future__ import annotations
 
@@ -112,11 +114,20 @@ class VerifyStep:
             self.stats = torch.zeros((self.stat_groups, B * T, 4), dtype=torch.float32, device=device)
         self.ws_attn = ws(M.medusa_tree_attn_workspace_size(B, H, Dh, T, max_prefix))
         self.ws_accept = ws(M.medusa_accept_workspace_size(B, T))
-        self.ws_heads = ws(M.medusa_heads_topk_workspace_size(B, K, d, V, self.s_max))
+        # the heads' workspace holds their row counters: zero-filled once, each call leaves them ready
+        self.ws_heads = torch.zeros(max(256, M.medusa_heads_topk_workspace_size(B, K, d, V, self.s_max)),
+                                    dtype=torch.uint8, device=device)
         # split heads: W1 over every tree row (tile layout for bf16), u for all rows,
         # and the W2 pass's arrival counters (zero once; each call leaves them zero)
+        if heads not in ("fused", "split", "joint"):
+            raise ValueError(f"heads {heads!r}")
+        if heads == "joint" and (w["dtype"] != "bf16" or B * T > 256):
+            raise ValueError("heads='joint' needs bf16 and at most 256 tree rows")
+        if heads == "joint":
+            self.accept = "separate"  # the joint launch has no statistics epilogue
+            self.write_logits = True
         self.heads = heads
-        if heads == "split":
+        if heads in ("split", "joint"):
             self.w1_layout = M.W_TILES if w["dtype"] == "bf16" else M.W_ROWS
             self.w1_run = (M.medusa_lm_head_tile(self.w1.reshape(K * d, d)) if self.w1_layout == M.W_TILES
                            else self.w1)
@@ -150,7 +161,11 @@ class VerifyStep:
 
         if self.attn_order == "first":
             attention()
-        if self.accept == "fused":
+        if self.heads == "joint":
+            M.medusa_lm_head_verify_heads_hidden(x["hidden"], self.w_lm_run, self.logits.shape[-1], self.logits,
+                                                 self.w1_run, self.b1, self.s_heads, self.u_all, self.err, main,
+                                                 layout=self.w_layout, w1_layout=self.w1_layout)
+        elif self.accept == "fused":
             M.medusa_lm_head_verify_stats(x["hidden"], self.w_lm_run, self.logits if self.write_logits else None,
                                           self.stats, self.mode, self.temperature, self.logits.shape[-1], self.err,
                                           main, layout=self.w_layout)
@@ -182,8 +197,8 @@ class VerifyStep:
         M.medusa_kv_compact(x["k_cache"], x["v_cache"], x["seq_start"], x["prefix_len"],
                             self.accepted_nodes, self.accept_len, self.tree.K, self.src_slots, self.err,
                             side)
-        if self.heads == "split":
-            if hs is not main:
+        if self.heads in ("split", "joint"):
+            if hs is not main and self.heads == "split":
                 main.wait_stream(hs)
             M.medusa_heads_logits_topk(self.u_all, self.T, self.best_node, self.w2, self.s_heads, self.head_logits,
                                        self.topk, self.ws_w2, self.err, main)
@@ -197,5 +212,7 @@ class VerifyStep:
     @property
     def launches_per_step(self) -> int:
         """Kernels one run() launches: attention 1 (2 for f32), LM head 1,
-        acceptance 2 (1 fused), compaction 1, heads 2, candidates 1."""
-        return (1 if self.w["dtype"] == "bf16" else 2) + 1 + (1 if self.accept == "fused" else 2) + 1 + 2 + 1
+        acceptance 2 (1 fused), compaction 1, heads 2 (1 joint: W1 runs in the
+        LM head's launch), candidates 1."""
+        return ((1 if self.w["dtype"] == "bf16" else 2) + 1 + (1 if self.accept == "fused" else 2) + 1
+                + (1 if self.heads == "joint" else 2) + 1)

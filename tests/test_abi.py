@@ -163,6 +163,18 @@ def test_validation_statuses(M):
                               1, FAKE, None, 0, None, None) == -1    # bf16 needs 16-byte alignment
     assert L.medusa_tree_attn(FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, ref, 17, 4, 64, 64, 1e4, 0.1,
                               1, FAKE, FAKE, 1 << 30, None, None) == -1
+    # joint LM head + heads' W1: bf16 only, rows <= 256, d a multiple of 128
+    s3 = (C.c_int32 * 3)(2, 2, 2)
+    assert L.medusa_lm_head_verify_heads_hidden(FAKE, 15, 256, FAKE, 1, 1000, FAKE, FAKE, 1, None, s3, 3, FAKE,
+                                                0, None, None) == -2
+    assert L.medusa_lm_head_verify_heads_hidden(FAKE, 300, 256, FAKE, 1, 1000, FAKE, FAKE, 1, None, s3, 3, FAKE,
+                                                1, None, None) == -2
+    assert L.medusa_lm_head_verify_heads_hidden(FAKE, 15, 192, FAKE, 1, 1000, FAKE, FAKE, 1, None, s3, 3, FAKE,
+                                                1, None, None) == -2
+    assert L.medusa_lm_head_verify_heads_hidden(FAKE, 15, 256, FAKE, 1, 1000, None, FAKE, 1, None, s3, 3, FAKE,
+                                                1, None, None) == -1
+    assert L.medusa_lm_head_verify_heads_hidden(FAKE, 15, 256, FAKE, 3, 1000, FAKE, FAKE, 1, None, s3, 3, FAKE,
+                                                1, None, None) == -1
     # key splits outside {1, 2, 4, 8}; fewer than 8 need bf16
     for ks in (0, 3, 16, -1):
         assert L.medusa_tree_attn_splits(FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, ref, 1, 4, 64, 64, 1e4,

@@ -215,6 +215,66 @@ def test_lm_head_tiled_layout(M, case):
         assert np.abs(to_host(a_tiles) - ref).max() <= TOL["bf16"]["logit"] * np.abs(ref).max()
 
 
+JOINT_CASES = [
+    # rows, d, V, s, bias: plans of 2, 3 and 4 tiles per CTA (the last two at
+    # 7B and 13B sizes, checked on sampled rows)
+    (15, 256, 1000, (2, 2, 2), True),
+    (1, 128, 17, (1,), False),
+    (65, 512, 5000, (8, 6, 5, 2), False),
+    (65, 1024, 32000, (8, 0, 5, 2), True),
+    (65, 4096, 32000, (8, 6, 5, 2), False),
+    (65, 5120, 32000, (8, 6, 5, 2, 0), False),
+]
+
+
+@pytest.mark.parametrize("case", JOINT_CASES, ids=lambda c: f"r{c[0]}-d{c[1]}-V{c[2]}-s{len(c[3])}")
+def test_lm_head_heads_hidden_joint(M, case):
+    """medusa_lm_head_verify_heads_hidden: logits and u against the oracle
+    (every row for small shapes, sampled rows otherwise), and bit for bit the
+    same as the two separate calls, for row-major and tiled weights."""
+    rows, d, V, s, bias = case
+    K = len(s)
+    used = [k for k in range(K) if s[k] > 0]
+    h = synth.normal(15, "h", (rows, d), 1.0, "bf16")
+    w = synth.normal(15, "w", (V, d), 1.0 / math.sqrt(d), "bf16")
+    w1 = synth.normal(15, "w1", (K, d, d), 1.0 / math.sqrt(d), "bf16")
+    b1 = synth.normal(15, "b1", (K, d), 0.5, "bf16") if bias else None
+    hd, wd, w1d = to_dev(h), to_dev(w), to_dev(w1)
+    b1d = None if b1 is None else to_dev(b1)
+    chk = list(range(rows)) if rows * d * (V + K * d) <= 2**28 else sorted({0, 1, rows // 2, rows - 1})
+    ref = oracle.lm_head(np.ascontiguousarray(h[chk]), w)
+    one = np.ascontiguousarray(w1[:, :1])  # the W2 the oracle's head call needs (unused here)
+    _, _, u_ref = oracle.heads(np.ascontiguousarray(h[chk].reshape(len(chk), 1, d)), np.zeros(len(chk), np.int32),
+                               w1, b1, one, [1 if k in used else 0 for k in range(K)], 1)
+    # the separate calls, row-major weights
+    lg_sep = torch.empty((rows, V), dtype=torch.float32, device="cuda")
+    u_sep = torch.zeros((rows, K, d), dtype=torch.bfloat16, device="cuda")
+    M.medusa_lm_head_verify(hd, wd, lg_sep)
+    M.medusa_heads_hidden(hd, w1d, b1d, list(s), u_sep)
+    wt, w1t = M.medusa_lm_head_tile(wd), M.medusa_lm_head_tile(w1d.reshape(K * d, d))
+    for lay, lay1 in ((M.W_ROWS, M.W_ROWS), (M.W_TILES, M.W_TILES), (M.W_TILES, M.W_ROWS)):
+        lg = torch.full((rows, V), float("nan"), dtype=torch.float32, device="cuda")
+        u = torch.zeros((rows, K, d), dtype=torch.bfloat16, device="cuda")
+        e = err_flag()
+        M.medusa_lm_head_verify_heads_hidden(hd, wt if lay == M.W_TILES else wd, V, lg,
+                                             w1t if lay1 == M.W_TILES else w1d, b1d, list(s), u, e,
+                                             layout=lay, w1_layout=lay1)
+        torch.cuda.synchronize()
+        assert int(e.item()) == 0
+        assert torch.equal(lg, lg_sep), "logits differ from medusa_lm_head_verify"
+        assert torch.equal(u, u_sep), "u differs from medusa_heads_hidden"
+        lgh = to_host(lg)[chk]
+        assert np.abs(lgh - ref).max() <= TOL["bf16"]["logit"] * np.abs(ref).max()
+        ug = as_double(to_host(u))
+        for i, r in enumerate(chk):
+            for k in range(K):
+                if k not in used:
+                    assert not np.any(ug[r, k])  # skipped head: not written
+                    continue
+                rk = as_double(u_ref[i, k])
+                assert np.all(np.abs(ug[r, k] - rk) <= 2.0 ** -7 * np.abs(rk) + 1e-3), f"u row {r} head {k}"
+
+
 # -------------------------------------------------------------- acceptance
 
 def _accept_inputs(ot, B, V, mode, seed, plant_nodes):
@@ -406,12 +466,19 @@ def test_heads_topk(M, case):
     last = np.array([(3 * b + 1) % T for b in range(B)], np.int32)
     hl = torch.zeros((B, K, V), dtype=torch.float32, device="cuda")
     tk = torch.zeros((B, K, s_max), dtype=torch.int32, device="cuda")
-    ws = torch.empty(M.medusa_heads_topk_workspace_size(B, K, d, V, s_max), dtype=torch.uint8, device="cuda")
+    ws = torch.zeros(M.medusa_heads_topk_workspace_size(B, K, d, V, s_max), dtype=torch.uint8, device="cuda")
     e = err_flag()
-    M.medusa_heads_topk(to_dev(hidden), to_dev(last), to_dev(w1), None if b1 is None else to_dev(b1), to_dev(w2),
-                        list(s), hl, tk, ws, e)
+    args = (to_dev(hidden), to_dev(last), to_dev(w1), None if b1 is None else to_dev(b1), to_dev(w2), list(s))
+    M.medusa_heads_topk(*args, hl, tk, ws, e)
+    # a second call on the same workspace (its row counters must be ready again) gives the same bits
+    hl2, tk2 = torch.full_like(hl, float("nan")), torch.full_like(tk, -7)
+    M.medusa_heads_topk(*args, hl2, tk2, ws, e)
     torch.cuda.synchronize()
     assert int(e.item()) == 0
+    for k in range(K):
+        if s[k] > 0:
+            assert torch.equal(hl[:, k], hl2[:, k])
+    assert torch.equal(tk, torch.where(tk2 == -7, torch.zeros_like(tk2), tk2))
     z_ref, tk_ref, _ = oracle.heads(hidden, last, w1, b1, w2, list(s), s_max)
     zg, tg = to_host(hl), to_host(tk)
     for b in range(B):
@@ -509,7 +576,7 @@ def test_heads_init_reproduce_lm_head(M):
     last = np.array([4], np.int32)
     hl = torch.zeros((1, K, V), dtype=torch.float32, device="cuda")
     tk = torch.zeros((1, K, 2), dtype=torch.int32, device="cuda")
-    ws = torch.empty(M.medusa_heads_topk_workspace_size(1, K, d, V, 2), dtype=torch.uint8, device="cuda")
+    ws = torch.zeros(M.medusa_heads_topk_workspace_size(1, K, d, V, 2), dtype=torch.uint8, device="cuda")
     M.medusa_heads_topk(to_dev(hidden), to_dev(last), to_dev(w1), None, to_dev(w2), [2, 2, 2], hl, tk, ws)
     logits = torch.empty((T, V), dtype=torch.float32, device="cuda")
     M.medusa_lm_head_verify(to_dev(hidden), to_dev(wlm), logits)

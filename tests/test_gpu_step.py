@@ -90,7 +90,7 @@ def test_step_tiny_fp32_full(M, heads):
     assert np.array_equal(to_host(st.next_tokens), oracle.build_candidates(r["next_root"], tk, ot))
 
 
-@pytest.mark.parametrize("heads", ["fused", "split"])
+@pytest.mark.parametrize("heads", ["fused", "split", "joint"])
 def test_step_vicuna7b_sampled(M, heads):
     w, ot, wts, x, tok, st, dev, node, path, lg_par, parents, gaps = _run(
         M, "vicuna7b_L1024_tree64", lambda ot: int(np.nonzero(ot.depth == 3)[0][4]), heads=heads)
