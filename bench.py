@@ -61,7 +61,7 @@ def parse_args():
                          "both projections on the accepted row after the acceptance (fused)")
     ap.add_argument("--attn-branch", choices=["serial", "fork"], default="fork",
                     help="tree attention before the LM head on one stream, or on a forked graph branch")
-    ap.add_argument("--attn-order", choices=["first", "after_lm"], default="after_lm",
+    ap.add_argument("--attn-order", choices=["first", "after_lm", "after_accept"], default="after_lm",
                     help="attention enqueued before the LM head or right after it (its CTAs then fill the "
                          "SMs the LM head leaves idle)")
     ap.add_argument("--attn-splits", type=int, choices=[1, 2, 4, 8], default=None,
@@ -104,8 +104,8 @@ def algorithmic_bytes(w: dict, T: int, s_heads, L_list, heads_mode: str, fused_a
     elif heads_mode == "joint":  # W1 streams in the LM head's launch (hidden read once for both)
         out["lm_head_verify"] += heads_hidden - B * T * d * e
         out["heads_logits_topk"] = heads_w2
-    else:
-        out["heads_topk"] = heads
+    else:  # medusa_heads_topk_candidates: the candidate fill runs in the heads' last CTA
+        out["heads_topk"] = heads + out.pop("build_candidates")
     out["step"] = sum(out.values())
     return out
 
@@ -258,12 +258,12 @@ def step_calls(st, x, s):
     if st.heads in ("split", "joint"):
         c.append(("heads_logits_topk", lambda: M.medusa_heads_logits_topk(
             st.u_all, st.T, st.best_node, st.w2, st.s_heads, st.head_logits, st.topk, st.ws_w2, st.err, s)))
-    else:
-        c.append(("heads_topk", lambda: M.medusa_heads_topk(x["hidden"], st.best_node, st.w1, st.b1, st.w2,
-                                                            st.s_heads, st.head_logits, st.topk, st.ws_heads,
-                                                            st.err, s)))
-    c.append(("build_candidates", lambda: M.medusa_build_candidates(st.next_root, st.topk, st.tree,
-                                                                    st.next_tokens, s)))
+        c.append(("build_candidates", lambda: M.medusa_build_candidates(st.next_root, st.topk, st.tree,
+                                                                        st.next_tokens, s)))
+    else:  # the heads' last CTA fills the candidates too
+        c.append(("heads_topk", lambda: M.medusa_heads_topk_candidates(
+            x["hidden"], st.best_node, st.w1, st.b1, st.w2, st.s_heads, st.head_logits, st.topk, st.ws_heads,
+            st.next_root, st.tree, st.next_tokens, st.err, s)))
     return c
 
 
@@ -709,7 +709,7 @@ def main():
         "config": config_dict(w, {"parallelism": f"replicas{world}" if world > 1 else "single-gpu", "attn_branch": args.attn_branch, "attn_order": args.attn_order, "attn_splits": r["attn_splits"], "heads": args.heads, "accept_impl": args.accept,
                                   "logits_written": bool(args.logits or w["mode"] == "typical"),
                                   "T_rows": r["T"], "s": r["s_heads"], "planted_accept_len": r["accept_len"]}),
-        "roofline": {"bound": "hbm", "kernel": f"medusa_{dom}", "achieved": achieved, "peak": peaks["hbm_gbs"],
+        "roofline": {"bound": "hbm", "kernel": "medusa_heads_topk_candidates" if dom == "heads_topk" else f"medusa_{dom}", "achieved": achieved, "peak": peaks["hbm_gbs"],
                      "unit": "GB/s", "frac": achieved / peaks["hbm_gbs"], "traffic": traffic,
                      "algorithmic_bytes_per_launch": by[dom], "ms_per_launch": dom_ms,
                      "peak_source": peaks["source"] + " hbm_gbs (copy)"},

@@ -20,6 +20,7 @@
  *      medusa_lm_head_verify_heads_hidden in place of the LM head call, one
  *      pass computing both, then medusa_heads_logits_topk)
  *   medusa_build_candidates next step's candidate tokens         (box 2)
+ *     (medusa_heads_topk_candidates: the last two in one call)
  * In a decode loop, medusa_append_tokens (box step 6) appends each step's
  * tokens to the output.
  *
@@ -33,7 +34,11 @@
  *   - Work is enqueued on `stream` (a cudaStream_t; 0 = legacy default).
  *   - Scratch ("workspace") is caller-provided device memory of at least the
  *     size returned by the matching *_workspace_size query, 256-byte aligned.
- *     Its contents need no initialisation and are not preserved.
+ *     Its contents are not preserved.  Calls whose kernels hand out work or
+ *     elect a last CTA through counters kept in it (medusa_accept,
+ *     medusa_heads_topk, medusa_heads_logits_topk) need it zero-filled before
+ *     the first call and leave the counters zero again; the others need no
+ *     initialisation.
  *   - Device-side data errors (a token or node index out of range, a prefix
  *     that overflows its sequence's capacity) cannot be seen by the host
  *     without a synchronisation.  Calls that read such data take `err`, a
@@ -279,7 +284,11 @@ size_t medusa_accept_workspace_size(int B, int T);
  * accepted_nodes [B][K+1] (root .. best, -1 padded; K = tree->K);
  * next_root [B] = argmax of the best node's row; best_node [B];
  * best_logp [B] float32 (summed log p^ of the accepted non-root nodes;
- * 0 for greedy; nullable). */
+ * 0 for greedy; nullable).
+ * One kernel: a CTA per tree row, and the last row of each sequence to finish
+ * (a counter in the workspace) makes that sequence's decisions.  The
+ * workspace must therefore be zero-filled (cudaMemset) before its first call;
+ * every call leaves its counters zero again. */
 int medusa_accept(const float* logits, const int32_t* tokens,
                   const medusa_tree_t* tree, int B, int V, int mode,
                   float temperature, float eps, float delta,
@@ -295,19 +304,20 @@ int medusa_accept(const float* logits, const int32_t* tokens,
  * loop that must not call cudaMalloc because it can synchronise the device
  * and take unbounded time.
  * Arguments, outputs and errors are those of medusa_accept, without the
- * workspace.  Its scratch is one file-scope __device__ array of
- * MEDUSA_ACCEPT_NOALLOC_MAX_ROWS row records of 16 bytes (128 KiB), which
- * every GPU that loads the library holds until the process exits.
+ * workspace.  Its scratch is one file-scope __device__ array, zero when the
+ * library loads, of 256 bytes of counters and MEDUSA_ACCEPT_NOALLOC_MAX_ROWS
+ * row records of 16 bytes (128 KiB), which every GPU that loads the library
+ * holds until the process exits.
  *   - The first call on each device looks up the array's device address
  *     (cudaGetSymbolAddress, with that device current) and caches it; make
  *     that first call before any stream capture.
  *   - B * tree->T above MEDUSA_ACCEPT_NOALLOC_MAX_ROWS returns
  *     MEDUSA_ERR_CAPACITY.
  *   - It calls no cudaMalloc, cudaFree or other allocating routine.
- *   - Every call shares the one array, which keeps the last call's contents.
- *     Nothing in it needs to start at zero (a call writes every record it
- *     reads), but calls that overlap on the GPU (other streams or threads
- *     without ordering between them) race on it: the caller serialises them. */
+ *   - Every call shares the one array, which keeps the last call's row
+ *     records and leaves its counters zero.  Calls that overlap on the GPU
+ *     (other streams or threads without ordering between them) race on it:
+ *     the caller serialises them. */
 #define MEDUSA_ACCEPT_NOALLOC_MAX_ROWS (MEDUSA_MAX_B * MEDUSA_MAX_T)
 int medusa_accept_noalloc(const float* logits, const int32_t* tokens,
                           const medusa_tree_t* tree, int B, int V, int mode,
@@ -358,6 +368,23 @@ int medusa_heads_topk(const void* hidden, const int32_t* last_node, int T,
                       medusa_dtype dtype, float* head_logits, int32_t* topk,
                       int s_max, void* workspace, size_t workspace_bytes,
                       int32_t* err, void* stream);
+
+/* medusa_heads_topk followed by medusa_build_candidates in one call: the
+ * heads' W2 kernel, once the last head's top-s is merged, writes the next
+ * step's candidate tokens (tokens[b][0] = next_root[b], tokens[b][n] =
+ * topk[b][depth[n]-1][rank[n]-1]), saving the candidate kernel's launch on
+ * the step's critical path.  Arguments and workspace (zero-filled once) as
+ * medusa_heads_topk; next_root, tree and tokens as medusa_build_candidates
+ * (K >= tree->K, tree->s[k] <= s_max). */
+int medusa_heads_topk_candidates(const void* hidden, const int32_t* last_node,
+                                 int T, const void* w1, const void* b1,
+                                 const void* w2, const int32_t* s, int K, int B,
+                                 int d, int V, medusa_dtype dtype,
+                                 float* head_logits, int32_t* topk, int s_max,
+                                 void* workspace, size_t workspace_bytes,
+                                 const int32_t* next_root,
+                                 const medusa_tree_t* tree, int32_t* tokens,
+                                 int32_t* err, void* stream);
 
 /* The heads' first projection for every tree row ([MED] Method 1, computed
  * ahead of the acceptance):

@@ -9,12 +9,13 @@
 // code", typical acceptance).  Explainer "085 | Medusa", section 二.3: a
 // rejected token ends the accepted prefix.
 //
-// Kernel 1 (one 1024-thread CTA per tree row, eight 16-byte loads in flight
+// One kernel, one 1024-thread CTA per tree row (eight 16-byte loads in flight
 // per thread, so a 32K-wide row arrives in one round of loads): argmax of the
 // row and, for typical acceptance, the row's log-sum-exp and entropy at the
-// given temperature.
-// Kernel 2 (one CTA per sequence, one thread per node): per-node decision,
-// the accepted-prefix chain level by level, and the best node.
+// given temperature.  The last CTA of a sequence to finish its row (a counter
+// in the workspace) then makes the sequence's decisions, one thread per node:
+// per-node acceptance, the accepted-prefix chain level by level, and the best
+// node (select_body).
 #include <math.h>
 
 #include <mutex>
@@ -53,9 +54,34 @@ __device__ __forceinline__ Soft soft_merge(Soft x, Soft y) {
 constexpr int kRowThreads = 1024;
 constexpr int kRowLoads = 8;  // 16-byte loads in flight per thread: 128 KB per CTA, a 32K-wide row at once
 
+// Barrier 1 over the first n threads of the block (n a multiple of 32).
+MDEV void sel_sync(int n) { asm volatile("bar.sync 1, %0;\n" ::"r"(n) : "memory"); }
+
+MDEV void select_body(int b, const float* logits, const int32_t* tokens, const medusa_tree_t& tree, int V,
+                      int mode, float inv_temp, float eps, float delta, const RowStat* st, int32_t* accept_len,
+                      int32_t* accepted_nodes, int32_t* next_root, int32_t* best_node, float* best_logp,
+                      int32_t* err, int nthreads);
+
+// The arguments of the row pass and of the decisions that follow it.
+struct AcceptArgs {
+  const float* logits;
+  const int32_t* tokens;
+  medusa_tree_t tree;
+  int V, mode;
+  float inv_temp, eps, delta;
+  RowStat* stats;  // [B][T] row records
+  int* counters;   // [B] rows finished per sequence; zero on entry, left zero
+  int32_t *accept_len, *accepted_nodes, *next_root, *best_node;
+  float* best_logp;
+  int32_t* err;
+};
+
 template <bool TYPICAL>
-__global__ void __launch_bounds__(kRowThreads) accept_rowstat_kernel(const float* logits, int T, int V,
-                                                                     float inv_temp, RowStat* stats) {
+__global__ void __launch_bounds__(kRowThreads) accept_rowstat_kernel(const __grid_constant__ AcceptArgs a) {
+  const float* logits = a.logits;
+  const int T = a.tree.T, V = a.V;
+  const float inv_temp = a.inv_temp;
+  RowStat* stats = a.stats;
   const int p = blockIdx.x, b = blockIdx.y;
   const float* z = logits + ((int64_t)b * T + p) * V;
   float bv = -INFINITY;
@@ -139,14 +165,40 @@ __global__ void __launch_bounds__(kRowThreads) accept_rowstat_kernel(const float
       stats[(int64_t)b * T + p] = r;
     }
   }
+  // the last row of the sequence to finish makes its decisions
+  __shared__ bool s_last;
+  __shared__ RowStat rs[MEDUSA_MAX_T];
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    __threadfence();
+    s_last = atomicAdd(a.counters + b, 1) == T - 1;
+  }
+  __syncthreads();
+  if (!s_last) return;
+  // one thread per node: the other warps leave, so the decisions' barriers
+  // wait for ceil(T / 32) warps only
+  const int nthr = (T + 31) & ~31;
+  if ((int)threadIdx.x >= nthr) return;
+  __threadfence();
+  const int c = threadIdx.x;
+  if (c < T) {
+    const int4 x = __ldcg(reinterpret_cast<const int4*>(stats + (int64_t)b * T + c));
+    rs[c] = RowStat{x.x, __int_as_float(x.y), __int_as_float(x.z), 0.f};
+  }
+  sel_sync(nthr);
+  select_body(b, a.logits, a.tokens, a.tree, V, a.mode, inv_temp, a.eps, a.delta, rs, a.accept_len,
+              a.accepted_nodes, a.next_root, a.best_node, a.best_logp, a.err, nthr);
+  if (threadIdx.x == 0) a.counters[b] = 0;  // every row of the sequence has arrived
 }
 
 // Sequence b's decisions from its rows' statistics `st` ([T], global or
-// shared memory); one thread per node, any block size >= T.
+// shared memory); one thread per node: threads 0 .. nthreads-1 of the block
+// take part (nthreads >= T, a multiple of 32; the block's other warps may
+// have exited), synchronised on barrier 1.
 MDEV void select_body(int b, const float* logits, const int32_t* tokens, const medusa_tree_t& tree, int V,
                       int mode, float inv_temp, float eps, float delta, const RowStat* st, int32_t* accept_len,
                       int32_t* accepted_nodes, int32_t* next_root, int32_t* best_node, float* best_logp,
-                      int32_t* err) {
+                      int32_t* err, int nthreads) {
   const int c = threadIdx.x;
   const int T = tree.T;
   __shared__ uint8_t ok[MEDUSA_MAX_T];
@@ -192,17 +244,17 @@ MDEV void select_body(int b, const float* logits, const int32_t* tokens, const m
     ok[c] = c == 0 ? 1 : 0;
     lp[c] = 0.f;
   }
-  __syncthreads();
+  sel_sync(nthreads);
   // the accepted-prefix chain, one depth level at a time
   for (int k = 1; k <= tree.K; ++k) {
     if (c < T && depth_c == k) {
       ok[c] = (pass && ok[parent_c]) ? 1 : 0;
       lp[c] = lp[parent_c] + lpc;
     }
-    __syncthreads();
+    sel_sync(nthreads);
   }
   // best node: max depth; typical: then max log-prob; then min index
-  const int warp = c >> 5, lane = c & 31, nw = (blockDim.x + 31) >> 5;
+  const int warp = c >> 5, lane = c & 31, nw = (nthreads + 31) >> 5;
   int key = (c < T && ok[c]) ? (depth_c << 16) | (0xffff - c) : -1;
   float mylp = (c < T && ok[c]) ? lp[c] : -INFINITY;
   // pass 1: deepest accepted depth
@@ -210,21 +262,21 @@ MDEV void select_body(int b, const float* logits, const int32_t* tokens, const m
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) kmax = max(kmax, __shfl_xor_sync(0xffffffffu, kmax, o));
   if (lane == 0) red_key[warp] = kmax;
-  __syncthreads();
+  sel_sync(nthreads);
   if (c == 0) {
     int m = -1;
     for (int w = 0; w < nw; ++w) m = max(m, red_key[w]);
     red_key[0] = m;
   }
-  __syncthreads();
+  sel_sync(nthreads);
   const int best_depth = red_key[0] >> 16;
-  __syncthreads();
+  sel_sync(nthreads);
   // pass 2 among nodes at that depth: (log-prob for typical, then low index)
   float cand_lp = (key >= 0 && depth_c == best_depth) ? (mode == 1 ? mylp : 0.f) : -INFINITY;
   int cand_i = (key >= 0 && depth_c == best_depth) ? c : 0x7fffffff;
   warp_argmax(cand_lp, cand_i);
   if (lane == 0) { red_lp[warp] = cand_lp; red_key[warp] = cand_i; }
-  __syncthreads();
+  sel_sync(nthreads);
   if (c == 0) {
     float bl = -INFINITY;
     int bi = 0x7fffffff;
@@ -245,15 +297,6 @@ MDEV void select_body(int b, const float* logits, const int32_t* tokens, const m
     best_node[b] = bi;
     if (best_logp) best_logp[b] = mode == 1 ? lp[bi] : 0.f;
   }
-}
-
-__global__ void __launch_bounds__(MEDUSA_MAX_T) accept_select_kernel(
-    const float* logits, const int32_t* tokens, medusa_tree_t tree, int V, int mode, float inv_temp,
-    float eps, float delta, const RowStat* stats, int32_t* accept_len, int32_t* accepted_nodes,
-    int32_t* next_root, int32_t* best_node, float* best_logp, int32_t* err) {
-  const int b = blockIdx.x;
-  select_body(b, logits, tokens, tree, V, mode, inv_temp, eps, delta, stats + (int64_t)b * tree.T, accept_len,
-              accepted_nodes, next_root, best_node, best_logp, err);
 }
 
 // Acceptance from the LM head's fused statistics (medusa_lm_head_verify_stats):
@@ -293,13 +336,21 @@ __global__ void __launch_bounds__(kStatThreads) accept_stats_kernel(
   }
   __syncthreads();
   select_body(b, logits, tokens, tree, V, mode, inv_temp, eps, delta, rs, accept_len, accepted_nodes, next_root,
-              best_node, best_logp, err);
+              best_node, best_logp, err, blockDim.x);
 }
 
-// Scratch of medusa_accept_noalloc: one row record per (sequence, tree row)
-// at the library's maximum sizes, 16 x 512 x 16 bytes = 128 KiB per device.
+// Workspace: per-sequence counters (256 bytes, at a fixed place so that
+// calls of any size find them zero), then one row record per (sequence, tree
+// row).
+constexpr size_t kCounterBytes = 256;
+static_assert(MEDUSA_MAX_B * sizeof(int) <= kCounterBytes, "counters");
+
+// Scratch of medusa_accept_noalloc: the counters and one row record per
+// (sequence, tree row) at the library's maximum sizes, 256 bytes + 16 x 512
+// x 16 bytes = 128 KiB per device, zero when the library loads.
 constexpr int kNoAllocRows = MEDUSA_ACCEPT_NOALLOC_MAX_ROWS;
-static __device__ __align__(256) RowStat g_accept_scratch[kNoAllocRows];
+constexpr size_t kNoAllocBytes = kCounterBytes + sizeof(RowStat) * (size_t)kNoAllocRows;
+static __device__ __align__(256) uint8_t g_accept_scratch[kNoAllocBytes];
 
 std::mutex g_noalloc_mu;
 void* g_noalloc_addr[64] = {};
@@ -331,7 +382,7 @@ using namespace medusa;
 
 extern "C" size_t medusa_accept_workspace_size(int B, int T) {
   if (B < 1 || T < 1) return 0;
-  return align_up((size_t)B * T * sizeof(RowStat), 256);
+  return kCounterBytes + align_up((size_t)B * T * sizeof(RowStat), 256);
 }
 
 extern "C" int medusa_accept(const float* logits, const int32_t* tokens, const medusa_tree_t* tree,
@@ -349,18 +400,22 @@ extern "C" int medusa_accept(const float* logits, const int32_t* tokens, const m
   const size_t need = medusa_accept_workspace_size(B, tree->T);
   if (!workspace || workspace_bytes < need)
     return fail(MEDUSA_ERR_WORKSPACE, "%s: workspace %zu < %zu bytes", fn, workspace_bytes, need);
+  if (reinterpret_cast<uintptr_t>(workspace) % 16)
+    return fail(MEDUSA_ERR_INVALID, "%s: workspace not 16-byte aligned", fn);
   cudaStream_t s = as_stream(stream);
-  RowStat* stats = static_cast<RowStat*>(workspace);
-  const float inv_temp = mode == 1 ? 1.f / temperature : 1.f;
+  AcceptArgs a{};
+  a.logits = logits; a.tokens = tokens; a.tree = *tree; a.V = V; a.mode = mode;
+  a.inv_temp = mode == 1 ? 1.f / temperature : 1.f;
+  a.eps = eps; a.delta = delta;
+  a.counters = static_cast<int*>(workspace);
+  a.stats = reinterpret_cast<RowStat*>(static_cast<uint8_t*>(workspace) + kCounterBytes);
+  a.accept_len = accept_len; a.accepted_nodes = accepted_nodes; a.next_root = next_root;
+  a.best_node = best_node; a.best_logp = best_logp; a.err = err;
   dim3 g(tree->T, B);
   if (mode == 1)
-    launch_kernel(accept_rowstat_kernel<true>, g, dim3(kRowThreads), 0, s, logits, tree->T, V, inv_temp, stats);
+    launch_kernel(accept_rowstat_kernel<true>, g, dim3(kRowThreads), 0, s, a);
   else
-    launch_kernel(accept_rowstat_kernel<false>, g, dim3(kRowThreads), 0, s, logits, tree->T, V, inv_temp, stats);
-  if (int rc = check_launch(fn)) return rc;
-  const int threads = (tree->T + 31) / 32 * 32;
-  launch_kernel(accept_select_kernel, dim3(B), dim3(threads), 0, s, logits, tokens, *tree, V, mode, inv_temp, eps,
-             delta, (const RowStat*)stats, accept_len, accepted_nodes, next_root, best_node, best_logp, err);
+    launch_kernel(accept_rowstat_kernel<false>, g, dim3(kRowThreads), 0, s, a);
   return check_launch(fn);
 }
 
@@ -381,8 +436,7 @@ extern "C" int medusa_accept_noalloc(const float* logits, const int32_t* tokens,
   void* scratch = nullptr;
   if (int rc = noalloc_scratch(fn, &scratch)) return rc;
   return medusa_accept(logits, tokens, tree, B, V, mode, temperature, eps, delta, accept_len, accepted_nodes,
-                       next_root, best_node, best_logp, scratch, sizeof(RowStat) * (size_t)kNoAllocRows, err,
-                       stream);
+                       next_root, best_node, best_logp, scratch, kNoAllocBytes, err, stream);
 }
 
 extern "C" int medusa_accept_stats(const void* stats, int groups, const float* logits, const int32_t* tokens,

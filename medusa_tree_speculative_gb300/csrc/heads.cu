@@ -62,6 +62,14 @@ struct HeadsArgs {
   int* w1ctr;                   // W1 row quads handed out; zeroed by w2 for the next call
   int cpc;                      // w2 CTAs per used head
   int rgroup;                   // W2 rows per warp in a group of kWarps * rgroup rows
+  // optional candidate fill (medusa_heads_topk_candidates): the last head to
+  // finish writes tokens[b][n] as medusa_build_candidates does
+  int32_t* tokens;              // [B][cT], or null
+  const int32_t* next_root;     // [B]
+  const int32_t* c_depth;       // tree depth / rank, device [cT]
+  const int32_t* c_rank;
+  int cT;
+  int* heads_done;              // heads merged so far; zero on entry, left zero
   int32_t* err;
 };
 
@@ -118,6 +126,7 @@ __global__ void __launch_bounds__(kWarps * 32) heads_w1_kernel(const __grid_cons
   if (blockIdx.x == 0 && threadIdx.x < a.nused) {  // for w2_topk
     a.counters[threadIdx.x] = 0;
     a.rowctr[threadIdx.x] = 0;
+    if (threadIdx.x == 0 && a.heads_done) *a.heads_done = 0;
   }
 
   // h_b = hidden[b][last_node[b]]; an out-of-range node reads row 0 and raises the error bit
@@ -365,6 +374,29 @@ __global__ void __launch_bounds__(kWarps * 32) heads_w2_topk_kernel(const __grid
     a.counters[slot] = 0;
     a.rowctr[slot] = 0;
   }
+  if (!a.tokens) return;
+  // the last head to be merged fills the next step's candidates
+  __syncthreads();  // this head's topk is written
+  if (threadIdx.x == 0) {
+    __threadfence();
+    last = atomicAdd(a.heads_done, 1) == a.nused - 1;
+  }
+  __syncthreads();
+  if (!last) return;
+  __threadfence();
+  for (int e = threadIdx.x; e < a.B * a.cT; e += blockDim.x) {
+    const int b = e / a.cT, n = e % a.cT;
+    int32_t tok;
+    if (n == 0) {
+      tok = a.next_root[b];
+    } else {
+      const int kk = a.c_depth[n] - 1, r = a.c_rank[n] - 1;
+      tok = (kk >= 0 && kk < a.K && r >= 0 && r < a.s_max) ? __ldcg(a.topk + ((int64_t)b * a.K + kk) * a.s_max + r)
+                                                           : -1;
+    }
+    a.tokens[(int64_t)b * a.cT + n] = tok;
+  }
+  if (threadIdx.x == 0) *a.heads_done = 0;
 }
 
 // W2 CTAs per used head: about four per SM in total, at least 8 rows each.
@@ -419,7 +451,8 @@ int w2_row_group(int cpc, int V) {
 }
 
 // Scratch: u [B][K][d] | candidate values | candidate indices | counters
-// (CTA arrivals [MEDUSA_MAX_K], W2 row groups [MEDUSA_MAX_K], W1 quads [1]).
+// (CTA arrivals [MEDUSA_MAX_K], W2 row groups [MEDUSA_MAX_K], W1 quads [1],
+// heads merged [1]).
 struct Layout {
   size_t u, cand, counters, total;
 };
@@ -427,7 +460,7 @@ Layout heads_layout(int B, int K, int nused, int d, int V) {
   Layout l;
   l.u = align_up((size_t)B * K * d * sizeof(float), 256);  // fp32 size covers both element types
   l.cand = align_up((size_t)nused * B * w2_ctas_per_head(nused, V) * kMaxS * 4, 256);
-  l.counters = align_up((size_t)(2 * MEDUSA_MAX_K + 1) * sizeof(int), 256);
+  l.counters = align_up((size_t)(2 * MEDUSA_MAX_K + 2) * sizeof(int), 256);
   l.total = l.u + 2 * l.cand + l.counters;
   return l;
 }
@@ -445,11 +478,17 @@ extern "C" size_t medusa_heads_topk_workspace_size(int B, int K, int d, int V, i
   return best;
 }
 
-extern "C" int medusa_heads_topk(const void* hidden, const int32_t* last_node, int T, const void* w1,
-                                 const void* b1, const void* w2, const int32_t* s, int K, int B, int d,
-                                 int V, medusa_dtype dtype, float* head_logits, int32_t* topk, int s_max,
-                                 void* workspace, size_t workspace_bytes, int32_t* err, void* stream) {
-  const char* fn = "medusa_heads_topk";
+namespace {
+struct CandFill {
+  const int32_t* next_root;
+  const medusa_tree_t* tree;
+  int32_t* tokens;
+};
+
+int heads_topk_impl(const void* hidden, const int32_t* last_node, int T, const void* w1, const void* b1,
+                    const void* w2, const int32_t* s, int K, int B, int d, int V, medusa_dtype dtype,
+                    float* head_logits, int32_t* topk, int s_max, void* workspace, size_t workspace_bytes,
+                    const CandFill* cf, int32_t* err, void* stream, const char* fn) {
   if (!hidden || !last_node || !w1 || !w2 || !s || !head_logits || !topk)
     return fail(MEDUSA_ERR_INVALID, "%s: NULL tensor", fn);
   if (T < 1 || K < 1 || B < 1 || d < 1 || V < 1 || s_max < 1)
@@ -493,9 +532,45 @@ extern "C" int medusa_heads_topk(const void* hidden, const int32_t* last_node, i
   a.cpc = w2_ctas_per_head(a.nused, V);
   a.rgroup = w2_row_group(a.cpc, V);
   a.logits = head_logits; a.topk = topk; a.err = err;
+  if (cf) {
+    a.tokens = cf->tokens; a.next_root = cf->next_root;
+    a.c_depth = cf->tree->depth; a.c_rank = cf->tree->rank; a.cT = cf->tree->T;
+    a.heads_done = a.counters + 2 * MEDUSA_MAX_K + 1;
+  }
   cudaStream_t st = as_stream(stream);
   return dtype == MEDUSA_BF16 ? launch_heads_b<uint16_t>(a, smax_used, st)
                               : launch_heads_b<float>(a, smax_used, st);
+}
+}  // namespace
+
+extern "C" int medusa_heads_topk(const void* hidden, const int32_t* last_node, int T, const void* w1,
+                                 const void* b1, const void* w2, const int32_t* s, int K, int B, int d,
+                                 int V, medusa_dtype dtype, float* head_logits, int32_t* topk, int s_max,
+                                 void* workspace, size_t workspace_bytes, int32_t* err, void* stream) {
+  return heads_topk_impl(hidden, last_node, T, w1, b1, w2, s, K, B, d, V, dtype, head_logits, topk, s_max, workspace,
+                         workspace_bytes, nullptr, err, stream, "medusa_heads_topk");
+}
+
+extern "C" int medusa_heads_topk_candidates(const void* hidden, const int32_t* last_node, int T, const void* w1,
+                                            const void* b1, const void* w2, const int32_t* s, int K, int B, int d,
+                                            int V, medusa_dtype dtype, float* head_logits, int32_t* topk,
+                                            int s_max, void* workspace, size_t workspace_bytes,
+                                            const int32_t* next_root, const medusa_tree_t* tree, int32_t* tokens,
+                                            int32_t* err, void* stream) {
+  const char* fn = "medusa_heads_topk_candidates";
+  if (int rc = check_tree(tree, fn)) return rc;
+  if (!next_root || !tokens) return fail(MEDUSA_ERR_INVALID, "%s: NULL tensor", fn);
+  if (K < tree->K || s_max < 1)
+    return fail(MEDUSA_ERR_INVALID, "%s: K=%d below the tree depth %d", fn, K, tree->K);
+  for (int k = 0; k < tree->K; ++k)
+    if (tree->s[k] > s_max) return fail(MEDUSA_ERR_INVALID, "%s: tree s[%d]=%d > s_max=%d", fn, k, tree->s[k], s_max);
+  bool any = false;
+  for (int k = 0; k < K && s; ++k) any = any || s[k] > 0;
+  if (!any)  // no head runs: the fill alone
+    return medusa_build_candidates(next_root, topk, s_max, K, tree, B, tokens, stream);
+  const CandFill cf{next_root, tree, tokens};
+  return heads_topk_impl(hidden, last_node, T, w1, b1, w2, s, K, B, d, V, dtype, head_logits, topk, s_max, workspace,
+                         workspace_bytes, &cf, err, stream, fn);
 }
 
 extern "C" size_t medusa_heads_logits_topk_workspace_size(int B, int K, int V, int s_max) {

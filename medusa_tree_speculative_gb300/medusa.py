@@ -58,6 +58,7 @@ _SIGS = {
     "medusa_kv_compact": (I, [P, P, P, P, P, P, I, I, I, I, I, P, P, P]),
     "medusa_heads_topk_workspace_size": (SZ, [I, I, I, I, I]),
     "medusa_heads_topk": (I, [P, P, I, P, P, P, P, I, I, I, I, I, P, P, I, P, SZ, P, P]),
+    "medusa_heads_topk_candidates": (I, [P, P, I, P, P, P, P, I, I, I, I, I, P, P, I, P, SZ, P, TREE, P, P, P]),
     "medusa_build_candidates": (I, [P, P, I, I, TREE, I, P, P]),
     "medusa_heads_hidden": (I, [P, I, P, I, P, P, I, I, I, P, P, P]),
     "medusa_lm_head_verify_heads_hidden": (I, [P, I, I, P, I, I, P, P, I, P, P, I, P, I, P, P]),
@@ -307,6 +308,21 @@ def medusa_heads_topk(hidden, last_node, w1, b1, w2, s, head_logits, topk, works
                                   _ptr(s_arr), K, B, d, V, _dtype(hidden), _ptr(head_logits), _ptr(topk),
                                   s_max, _ptr(workspace), workspace.numel() * workspace.element_size(),
                                   _ptr(err), _stream(stream)), "medusa_heads_topk")
+
+
+def medusa_heads_topk_candidates(hidden, last_node, w1, b1, w2, s, head_logits, topk, workspace, next_root,
+                                 tree: "DeviceTree", tokens, err=None, stream=None):
+    """medusa_heads_topk, then the next step's candidate tokens from next_root and topk, in one call."""
+    B, T, d = hidden.shape
+    K, V = w2.shape[0], w2.shape[1]
+    s_arr = np.ascontiguousarray(s, np.int32)
+    assert len(s_arr) == K
+    s_max = topk.shape[-1]
+    _check(_lib.medusa_heads_topk_candidates(_ptr(hidden), _ptr(last_node), T, _ptr(w1), _ptr(b1), _ptr(w2),
+                                             _ptr(s_arr), K, B, d, V, _dtype(hidden), _ptr(head_logits), _ptr(topk),
+                                             s_max, _ptr(workspace), workspace.numel() * workspace.element_size(),
+                                             _ptr(next_root), tree.ref, _ptr(tokens), _ptr(err), _stream(stream)),
+           "medusa_heads_topk_candidates")
 
 
 def medusa_heads_hidden(hidden, w1, b1, s, u, err=None, stream=None, layout=W_ROWS):

@@ -3,10 +3,11 @@ library calls.  Plumbing only: every step of the method runs in libmedusa.
 
 Call order (decoding-step box of the Medusa paper digest, steps 3-6 then 1-2
 for the next step):
-  main chain: medusa_lm_head_verify -> medusa_accept -> heads ->
-  medusa_build_candidates; medusa_tree_attn and then medusa_kv_compact either
+  main chain: medusa_lm_head_verify -> medusa_accept -> heads (->
+  medusa_build_candidates); medusa_tree_attn and then medusa_kv_compact either
   on the same stream or on a forked branch that joins at the end.
-  heads = medusa_heads_topk on the accepted node ("fused"), or ("split")
+  heads = medusa_heads_topk_candidates on the accepted node ("fused": the
+  heads' last CTA also fills the next candidates), or ("split")
   medusa_heads_hidden over every tree row -- forked after the LM head so that
   it runs beside the acceptance -- then medusa_heads_logits_topk on the
   accepted node's row, or ("joint", bf16) medusa_lm_head_verify_heads_hidden
@@ -55,12 +56,14 @@ class VerifyStep:
                  heads: str = "fused", accept: str = "separate", write_logits: bool = True,
                  attn_order: str = "after_lm", attn_splits="auto"):
         self.w, self.tree, self.max_prefix = w, tree, max_prefix
-        # attention on the forked branch: enqueued before the LM head ("first")
-        # or right after it ("after_lm": its CTAs then take the SMs the LM head
-        # leaves idle instead of holding the LM head back), with the library's
-        # default key split (None) or 1, 2, 4, 8 CTAs per head ("auto": 4 for
-        # bf16, the fastest measured beside the LM head at the 7B shape)
-        if attn_order not in ("first", "after_lm"):
+        # attention on the forked branch: enqueued before the LM head ("first"),
+        # right after it ("after_lm": its CTAs then take the SMs the LM head
+        # leaves idle instead of holding the LM head back), or after the
+        # acceptance ("after_accept": beside the heads, whose rows are handed
+        # out at run time), with the library's default key split (None) or 1,
+        # 2, 4, 8 CTAs per head ("auto": 4 for bf16, the fastest measured
+        # beside the LM head at the 7B shape)
+        if attn_order not in ("first", "after_lm", "after_accept"):
             raise ValueError(f"attn_order {attn_order!r}")
         if attn_splits == "auto":
             attn_splits = 4 if w["dtype"] == "bf16" else None
@@ -113,7 +116,9 @@ class VerifyStep:
             self.stat_groups = M.medusa_lm_head_stat_groups(B * T, V)
             self.stats = torch.zeros((self.stat_groups, B * T, 4), dtype=torch.float32, device=device)
         self.ws_attn = ws(M.medusa_tree_attn_workspace_size(B, H, Dh, T, max_prefix))
-        self.ws_accept = ws(M.medusa_accept_workspace_size(B, T))
+        # the acceptance keeps per-sequence counters in its workspace: zero-filled once
+        self.ws_accept = torch.zeros(max(256, M.medusa_accept_workspace_size(B, T)), dtype=torch.uint8,
+                                     device=device)
         # the heads' workspace holds their row counters: zero-filled once, each call leaves them ready
         self.ws_heads = torch.zeros(max(256, M.medusa_heads_topk_workspace_size(B, K, d, V, self.s_max)),
                                     dtype=torch.uint8, device=device)
@@ -151,7 +156,7 @@ class VerifyStep:
 
         main = stream if stream is not None else torch.cuda.current_stream()
         side = side_stream if side_stream is not None else main
-        if side is not main:
+        if side is not main and self.attn_order != "after_accept":
             side.wait_stream(main)
 
         def attention():
@@ -194,6 +199,8 @@ class VerifyStep:
                                    self.err, main)
         if side is not main:
             side.wait_stream(main)  # compaction needs the accepted path
+        if self.attn_order == "after_accept":
+            attention()
         M.medusa_kv_compact(x["k_cache"], x["v_cache"], x["seq_start"], x["prefix_len"],
                             self.accepted_nodes, self.accept_len, self.tree.K, self.src_slots, self.err,
                             side)
@@ -202,17 +209,19 @@ class VerifyStep:
                 main.wait_stream(hs)
             M.medusa_heads_logits_topk(self.u_all, self.T, self.best_node, self.w2, self.s_heads, self.head_logits,
                                        self.topk, self.ws_w2, self.err, main)
-        else:
-            M.medusa_heads_topk(x["hidden"], self.best_node, self.w1, self.b1, self.w2, self.s_heads,
-                                self.head_logits, self.topk, self.ws_heads, self.err, main)
-        M.medusa_build_candidates(self.next_root, self.topk, self.tree, self.next_tokens, main)
+            M.medusa_build_candidates(self.next_root, self.topk, self.tree, self.next_tokens, main)
+        else:  # the heads' last CTA also fills the next step's candidates
+            M.medusa_heads_topk_candidates(x["hidden"], self.best_node, self.w1, self.b1, self.w2, self.s_heads,
+                                           self.head_logits, self.topk, self.ws_heads, self.next_root, self.tree,
+                                           self.next_tokens, self.err, main)
         if side is not main:
             main.wait_stream(side)
 
     @property
     def launches_per_step(self) -> int:
         """Kernels one run() launches: attention 1 (2 for f32), LM head 1,
-        acceptance 2 (1 fused), compaction 1, heads 2 (1 joint: W1 runs in the
-        LM head's launch), candidates 1."""
-        return ((1 if self.w["dtype"] == "bf16" else 2) + 1 + (1 if self.accept == "fused" else 2) + 1
-                + (1 if self.heads == "joint" else 2) + 1)
+        acceptance 1, compaction 1, heads 2 with the candidate fill ("fused"),
+        or heads 2 ("split"; 1 "joint": W1 runs in the LM head's launch) and
+        candidates 1."""
+        heads = {"fused": 2, "split": 3, "joint": 2}[self.heads]
+        return (1 if self.w["dtype"] == "bf16" else 2) + 1 + 1 + 1 + heads

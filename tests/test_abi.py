@@ -205,6 +205,15 @@ def test_validation_statuses(M):
     assert L.medusa_heads_topk(FAKE, FAKE, 15, FAKE, None, FAKE, s, 9, 1, 256, 1000, 1, FAKE, FAKE, 8,
                                FAKE, 1 << 30, None, None) == -2
     assert b"medusa_heads_topk" in L.medusa_last_error()
+    # heads + candidate fill: no tree, no tokens, fewer heads than tree levels, tree s above s_max
+    assert L.medusa_heads_topk_candidates(FAKE, FAKE, 15, FAKE, None, FAKE, s, 3, 1, 256, 1000, 1, FAKE, FAKE, 8,
+                                          FAKE, 1 << 30, FAKE, None, FAKE, None, None) == -1
+    assert L.medusa_heads_topk_candidates(FAKE, FAKE, 15, FAKE, None, FAKE, s, 3, 1, 256, 1000, 1, FAKE, FAKE, 8,
+                                          FAKE, 1 << 30, FAKE, ref, None, None, None) == -1
+    assert L.medusa_heads_topk_candidates(FAKE, FAKE, 15, FAKE, None, FAKE, s, 2, 1, 256, 1000, 1, FAKE, FAKE, 8,
+                                          FAKE, 1 << 30, FAKE, ref, FAKE, None, None) == -1
+    assert L.medusa_heads_topk_candidates(FAKE, FAKE, 15, FAKE, None, FAKE, s, 3, 1, 256, 1000, 1, FAKE, FAKE, 1,
+                                          FAKE, 1 << 30, FAKE, ref, FAKE, None, None) == -1
     # heads over every row: bf16 needs d a multiple of 128; K above the maximum; bad layout
     s = (C.c_int32 * 3)(2, 2, 2)
     assert L.medusa_heads_hidden(FAKE, 65, FAKE, 0, None, s, 3, 320, 1, FAKE, None, None) == -2

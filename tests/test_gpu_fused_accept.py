@@ -106,7 +106,7 @@ def test_fused_accept_matches_accept(M, mode, write_logits):
                 torch.zeros(B, **i32), torch.zeros(B, dtype=torch.float32, device="cuda")]
 
     o1 = outs()
-    ws = torch.empty(M.medusa_accept_workspace_size(B, T), dtype=torch.uint8, device="cuda")
+    ws = torch.zeros(M.medusa_accept_workspace_size(B, T), dtype=torch.uint8, device="cuda")
     M.medusa_accept(lg, tk, dtree, mode, tau, eps, delta, *o1, ws)
     G = M.medusa_lm_head_stat_groups(B * T, V)
     stats = torch.zeros((G, B * T, 4), dtype=torch.float32, device="cuda")

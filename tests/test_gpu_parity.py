@@ -311,11 +311,18 @@ def _gpu_accept(M, dtree, logits, tokens, mode, temp=0.7, eps=0.09, delta=0.3):
                next_root=torch.zeros(B, dtype=torch.int32, device="cuda"),
                best_node=torch.zeros(B, dtype=torch.int32, device="cuda"),
                best_logp=torch.zeros(B, dtype=torch.float32, device="cuda"))
-    ws = torch.empty(M.medusa_accept_workspace_size(B, T), dtype=torch.uint8, device="cuda")
+    ws = torch.zeros(M.medusa_accept_workspace_size(B, T), dtype=torch.uint8, device="cuda")
     e = err_flag()
-    M.medusa_accept(to_dev(logits), to_dev(tokens), dtree, mode, temp, eps, delta, out["accept_len"],
-                    out["accepted_nodes"], out["next_root"], out["best_node"], out["best_logp"], ws, e)
+    args = (to_dev(logits), to_dev(tokens), dtree, mode, temp, eps, delta)
+    M.medusa_accept(*args, out["accept_len"], out["accepted_nodes"], out["next_root"], out["best_node"],
+                    out["best_logp"], ws, e)
+    # a second call on the same workspace (its counters must be zero again) gives the same results
+    again = {k: torch.full_like(v, -5) for k, v in out.items()}
+    M.medusa_accept(*args, again["accept_len"], again["accepted_nodes"], again["next_root"], again["best_node"],
+                    again["best_logp"], ws, e)
     torch.cuda.synchronize()
+    for k in out:
+        assert torch.equal(out[k], again[k]), k
     return {k: to_host(v) for k, v in out.items()}, int(e.item())
 
 
@@ -602,3 +609,37 @@ def test_build_candidates(M):
         torch.cuda.synchronize()
         ref = oracle.build_candidates(root, topk, ot)
         assert np.array_equal(to_host(out), ref)
+
+
+@pytest.mark.parametrize("dt", ["bf16", "f32"])
+def test_heads_topk_candidates(M, dt):
+    """medusa_heads_topk_candidates: the same head logits and top-s as
+    medusa_heads_topk, and the candidates the oracle builds from that top-s;
+    three calls on one workspace (its counters, the merged-heads one
+    included, must be ready again each time)."""
+    for spec, B, d, V in [(("cartesian", (2, 2, 2), None), 2, 256, 1000), (("greedy", 4, 10, 64), 1, 512, 4096)]:
+        ot, dtree = both_trees(M, spec)
+        K = ot.K + 1  # one head past the tree's depth, unused (s = 0)
+        s = [int(v) for v in ot.s[:ot.K]] + [0]
+        s_max = max(s)
+        T = ot.T
+        hidden = synth.normal(21, "hidden", (B, T, d), 1.0, dt)
+        w1 = synth.normal(21, "w1", (K, d, d), 1 / math.sqrt(d), dt)
+        w2 = synth.normal(21, "w2", (K, V, d), 1 / math.sqrt(d), dt)
+        node = to_dev(np.array([(2 * b + 1) % T for b in range(B)], np.int32))
+        root = np.array([(7 * b + 3) % V for b in range(B)], np.int32)
+        hd, w1d, w2d = to_dev(hidden), to_dev(w1), to_dev(w2)
+        hl_ref = torch.zeros((B, K, V), dtype=torch.float32, device="cuda")
+        tk_ref = torch.zeros((B, K, s_max), dtype=torch.int32, device="cuda")
+        ws = torch.zeros(M.medusa_heads_topk_workspace_size(B, K, d, V, s_max), dtype=torch.uint8, device="cuda")
+        M.medusa_heads_topk(hd, node, w1d, None, w2d, s, hl_ref, tk_ref, ws)
+        for rep in range(3):
+            hl = torch.zeros_like(hl_ref)
+            tk = torch.zeros_like(tk_ref)
+            tok = torch.full((B, T), -9, dtype=torch.int32, device="cuda")
+            e = err_flag()
+            M.medusa_heads_topk_candidates(hd, node, w1d, None, w2d, s, hl, tk, ws, to_dev(root), dtree, tok, e)
+            torch.cuda.synchronize()
+            assert int(e.item()) == 0
+            assert torch.equal(hl[:, :ot.K], hl_ref[:, :ot.K]) and torch.equal(tk, tk_ref)
+            assert np.array_equal(to_host(tok), oracle.build_candidates(root, to_host(tk), ot)), f"call {rep}"

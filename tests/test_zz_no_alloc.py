@@ -69,7 +69,7 @@ def test_accept_noalloc_matches_accept_on_two_calls(M):
     for mode, seed in ((1, 11), (0, 12)):
         logits, tokens = _inputs(tree, B, V, mode, seed)
         ref, got = _outputs(B, tree.K), _outputs(B, tree.K)
-        ws = torch.empty(M.medusa_accept_workspace_size(B, tree.T), dtype=torch.uint8, device="cuda")
+        ws = torch.zeros(M.medusa_accept_workspace_size(B, tree.T), dtype=torch.uint8, device="cuda")
         err_ref = torch.zeros(1, dtype=torch.int32, device="cuda")
         err_got = torch.zeros(1, dtype=torch.int32, device="cuda")
         M.medusa_accept(logits, tokens, tree, mode, 0.7, 0.09, 0.3, ref["accept_len"], ref["accepted_nodes"],
