@@ -61,7 +61,7 @@ def parse_args():
                          "both projections on the accepted row after the acceptance (fused)")
     ap.add_argument("--attn-branch", choices=["serial", "fork"], default="fork",
                     help="tree attention before the LM head on one stream, or on a forked graph branch")
-    ap.add_argument("--attn-order", choices=["first", "after_lm", "after_accept"], default="after_lm",
+    ap.add_argument("--attn-order", choices=["first", "after_lm", "after_accept", "after_heads"], default="after_lm",
                     help="attention enqueued before the LM head or right after it (its CTAs then fill the "
                          "SMs the LM head leaves idle)")
     ap.add_argument("--attn-splits", type=int, choices=[1, 2, 4, 8], default=None,

@@ -59,6 +59,8 @@ struct HeadsArgs {
   int* cand_i;
   int* counters;                // [nused] CTA arrivals per head, zeroed by w1
   int* rowctr;                  // [nused] W2 row groups handed out per head, zeroed by w1
+  int* tickets;                 // W2 CTAs started: a CTA serves head (ticket % nused)
+  int* exited;                  // W2 CTAs finished
   int* w1ctr;                   // W1 row quads handed out; zeroed by w2 for the next call
   int cpc;                      // w2 CTAs per used head
   int rgroup;                   // W2 rows per warp in a group of kWarps * rgroup rows
@@ -126,6 +128,7 @@ __global__ void __launch_bounds__(kWarps * 32) heads_w1_kernel(const __grid_cons
   if (blockIdx.x == 0 && threadIdx.x < a.nused) {  // for w2_topk
     a.counters[threadIdx.x] = 0;
     a.rowctr[threadIdx.x] = 0;
+    if (threadIdx.x == 0) *a.tickets = *a.exited = 0;
     if (threadIdx.x == 0 && a.heads_done) *a.heads_done = 0;
   }
 
@@ -253,13 +256,18 @@ MDEV void block_select(TopList<S>& L, float (*wv)[S], int (*wi)[S], float* ov, i
 template <typename TE, int NB, int S>
 __global__ void __launch_bounds__(kWarps * 32) heads_w2_topk_kernel(const __grid_constant__ HeadsArgs a) {
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int slot = blockIdx.x / a.cpc, part = blockIdx.x % a.cpc;
-  const int k = a.heads[slot];
   __shared__ float wv[32][S];
   __shared__ int wi[32][S];
   __shared__ bool last;
   __shared__ int s_grp[kMaxGroups];  // row groups this CTA streamed
   __shared__ int s_g[2];
+  __shared__ int s_ticket;
+  // the head this CTA serves goes by the order in which CTAs start, not by
+  // blockIdx, so CTAs held back by other work spread over every head
+  if (threadIdx.x == 0) s_ticket = atomicAdd(a.tickets, 1);
+  __syncthreads();
+  const int slot = s_ticket % a.nused, part = s_ticket / a.nused;
+  const int k = a.heads[slot];
 
   const TE* x[NB];
 #pragma unroll
@@ -344,59 +352,68 @@ __global__ void __launch_bounds__(kWarps * 32) heads_w2_topk_kernel(const __grid
     last = atomicAdd(a.counters + slot, 1) == a.cpc - 1;
   }
   __syncthreads();
-  if (!last) return;
-  __threadfence();
-  const int s_k = a.s[slot];
-  for (int b = 0; b < a.B; ++b) {
-    const int64_t base = ((int64_t)slot * a.B + b) * a.cpc * kMaxS;
-    TopList<S> L;
-    L.init();
-    for (int e = threadIdx.x; e < a.cpc * S; e += blockDim.x) {
-      const int c = e / S, t = e % S;
-      L.insert(__ldcg(a.cand_v + base + (int64_t)c * kMaxS + t), __ldcg(a.cand_i + base + (int64_t)c * kMaxS + t));
-    }
-    float ov[S];
-    int oi[S];
-    block_select<S>(L, wv, wi, ov, oi);
-    if (warp == 0) {
-      int32_t* out = a.topk + ((int64_t)b * a.K + k) * a.s_max;
-      for (int t = lane; t < a.s_max; t += 32) {
-        int idx = -1;
+  if (last) {
+    __threadfence();
+    const int s_k = a.s[slot];
+    for (int b = 0; b < a.B; ++b) {
+      const int64_t base = ((int64_t)slot * a.B + b) * a.cpc * kMaxS;
+      TopList<S> L;
+      L.init();
+      for (int e = threadIdx.x; e < a.cpc * S; e += blockDim.x) {
+        const int c = e / S, t = e % S;
+        L.insert(__ldcg(a.cand_v + base + (int64_t)c * kMaxS + t), __ldcg(a.cand_i + base + (int64_t)c * kMaxS + t));
+      }
+      float ov[S];
+      int oi[S];
+      block_select<S>(L, wv, wi, ov, oi);
+      if (warp == 0) {
+        int32_t* out = a.topk + ((int64_t)b * a.K + k) * a.s_max;
+        for (int t = lane; t < a.s_max; t += 32) {
+          int idx = -1;
 #pragma unroll
-        for (int q = 0; q < S; ++q)
-          if (q == t) idx = oi[q];
-        out[t] = (t < s_k && idx >= 0 && idx < a.V) ? idx : -1;
+          for (int q = 0; q < S; ++q)
+            if (q == t) idx = oi[q];
+          out[t] = (t < s_k && idx >= 0 && idx < a.V) ? idx : -1;
+        }
+      }
+      __syncthreads();
+    }
+    if (threadIdx.x == 0) {  // ready for the next call (every CTA of the head has stopped taking rows)
+      a.counters[slot] = 0;
+      a.rowctr[slot] = 0;
+    }
+    if (a.tokens) {
+      // the last head to be merged fills the next step's candidates
+      __syncthreads();  // this head's topk is written
+      if (threadIdx.x == 0) {
+        __threadfence();
+        last = atomicAdd(a.heads_done, 1) == a.nused - 1;
+      }
+      __syncthreads();
+      if (last) {
+        __threadfence();
+        for (int e = threadIdx.x; e < a.B * a.cT; e += blockDim.x) {
+          const int b = e / a.cT, n = e % a.cT;
+          int32_t tok;
+          if (n == 0) {
+            tok = a.next_root[b];
+          } else {
+            const int kk = a.c_depth[n] - 1, r = a.c_rank[n] - 1;
+            tok = (kk >= 0 && kk < a.K && r >= 0 && r < a.s_max)
+                      ? __ldcg(a.topk + ((int64_t)b * a.K + kk) * a.s_max + r)
+                      : -1;
+          }
+          a.tokens[(int64_t)b * a.cT + n] = tok;
+        }
+        if (threadIdx.x == 0) *a.heads_done = 0;
       }
     }
-    __syncthreads();
   }
-  if (threadIdx.x == 0) {  // ready for the next call (every CTA of the head has stopped taking rows)
-    a.counters[slot] = 0;
-    a.rowctr[slot] = 0;
-  }
-  if (!a.tokens) return;
-  // the last head to be merged fills the next step's candidates
-  __syncthreads();  // this head's topk is written
+  // the last CTA to leave (every CTA has drawn its ticket) resets the tickets
   if (threadIdx.x == 0) {
     __threadfence();
-    last = atomicAdd(a.heads_done, 1) == a.nused - 1;
+    if (atomicAdd(a.exited, 1) == (int)gridDim.x - 1) *a.tickets = *a.exited = 0;
   }
-  __syncthreads();
-  if (!last) return;
-  __threadfence();
-  for (int e = threadIdx.x; e < a.B * a.cT; e += blockDim.x) {
-    const int b = e / a.cT, n = e % a.cT;
-    int32_t tok;
-    if (n == 0) {
-      tok = a.next_root[b];
-    } else {
-      const int kk = a.c_depth[n] - 1, r = a.c_rank[n] - 1;
-      tok = (kk >= 0 && kk < a.K && r >= 0 && r < a.s_max) ? __ldcg(a.topk + ((int64_t)b * a.K + kk) * a.s_max + r)
-                                                           : -1;
-    }
-    a.tokens[(int64_t)b * a.cT + n] = tok;
-  }
-  if (threadIdx.x == 0) *a.heads_done = 0;
 }
 
 // W2 CTAs per used head: about four per SM in total, at least 8 rows each.
@@ -452,7 +469,7 @@ int w2_row_group(int cpc, int V) {
 
 // Scratch: u [B][K][d] | candidate values | candidate indices | counters
 // (CTA arrivals [MEDUSA_MAX_K], W2 row groups [MEDUSA_MAX_K], W1 quads [1],
-// heads merged [1]).
+// heads merged [1], W2 tickets [1], W2 CTAs finished [1]).
 struct Layout {
   size_t u, cand, counters, total;
 };
@@ -460,7 +477,7 @@ Layout heads_layout(int B, int K, int nused, int d, int V) {
   Layout l;
   l.u = align_up((size_t)B * K * d * sizeof(float), 256);  // fp32 size covers both element types
   l.cand = align_up((size_t)nused * B * w2_ctas_per_head(nused, V) * kMaxS * 4, 256);
-  l.counters = align_up((size_t)(2 * MEDUSA_MAX_K + 2) * sizeof(int), 256);
+  l.counters = align_up((size_t)(2 * MEDUSA_MAX_K + 4) * sizeof(int), 256);
   l.total = l.u + 2 * l.cand + l.counters;
   return l;
 }
@@ -529,6 +546,8 @@ int heads_topk_impl(const void* hidden, const int32_t* last_node, int T, const v
   a.counters = reinterpret_cast<int*>(ws + l.u + 2 * l.cand);
   a.rowctr = a.counters + MEDUSA_MAX_K;
   a.w1ctr = a.counters + 2 * MEDUSA_MAX_K;
+  a.tickets = a.counters + 2 * MEDUSA_MAX_K + 2;
+  a.exited = a.counters + 2 * MEDUSA_MAX_K + 3;
   a.cpc = w2_ctas_per_head(a.nused, V);
   a.rgroup = w2_row_group(a.cpc, V);
   a.logits = head_logits; a.topk = topk; a.err = err;
@@ -625,6 +644,8 @@ extern "C" int medusa_heads_logits_topk(const void* u, int T, const int32_t* nod
   a.cand_i = reinterpret_cast<int*>(ws + l.cand);
   a.counters = reinterpret_cast<int*>(ws + 2 * l.cand);
   a.rowctr = a.counters + MEDUSA_MAX_K;
+  a.tickets = a.counters + 2 * MEDUSA_MAX_K + 2;
+  a.exited = a.counters + 2 * MEDUSA_MAX_K + 3;
   a.cpc = w2_ctas_per_head(a.nused, V);
   a.rgroup = w2_row_group(a.cpc, V);
   a.logits = head_logits; a.topk = topk; a.err = err;

@@ -60,10 +60,11 @@ class VerifyStep:
         # right after it ("after_lm": its CTAs then take the SMs the LM head
         # leaves idle instead of holding the LM head back), or after the
         # acceptance ("after_accept": beside the heads, whose rows are handed
-        # out at run time), with the library's default key split (None) or 1,
+        # out at run time; "after_heads": forked there but enqueued after the
+        # heads' kernels), with the library's default key split (None) or 1,
         # 2, 4, 8 CTAs per head ("auto": 4 for bf16, the fastest measured
         # beside the LM head at the 7B shape)
-        if attn_order not in ("first", "after_lm", "after_accept"):
+        if attn_order not in ("first", "after_lm", "after_accept", "after_heads"):
             raise ValueError(f"attn_order {attn_order!r}")
         if attn_splits == "auto":
             attn_splits = 4 if w["dtype"] == "bf16" else None
@@ -156,7 +157,7 @@ class VerifyStep:
 
         main = stream if stream is not None else torch.cuda.current_stream()
         side = side_stream if side_stream is not None else main
-        if side is not main and self.attn_order != "after_accept":
+        if side is not main and self.attn_order not in ("after_accept", "after_heads"):
             side.wait_stream(main)
 
         def attention():
@@ -199,11 +200,16 @@ class VerifyStep:
                                    self.err, main)
         if side is not main:
             side.wait_stream(main)  # compaction needs the accepted path
+
+        def compaction():
+            M.medusa_kv_compact(x["k_cache"], x["v_cache"], x["seq_start"], x["prefix_len"],
+                                self.accepted_nodes, self.accept_len, self.tree.K, self.src_slots, self.err,
+                                side)
+
         if self.attn_order == "after_accept":
             attention()
-        M.medusa_kv_compact(x["k_cache"], x["v_cache"], x["seq_start"], x["prefix_len"],
-                            self.accepted_nodes, self.accept_len, self.tree.K, self.src_slots, self.err,
-                            side)
+        if self.attn_order != "after_heads":
+            compaction()
         if self.heads in ("split", "joint"):
             if hs is not main and self.heads == "split":
                 main.wait_stream(hs)
@@ -214,6 +220,9 @@ class VerifyStep:
             M.medusa_heads_topk_candidates(x["hidden"], self.best_node, self.w1, self.b1, self.w2, self.s_heads,
                                            self.head_logits, self.topk, self.ws_heads, self.next_root, self.tree,
                                            self.next_tokens, self.err, main)
+        if self.attn_order == "after_heads":  # forked after the acceptance, enqueued after the heads' launches
+            attention()
+            compaction()
         if side is not main:
             main.wait_stream(side)
 
