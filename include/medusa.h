@@ -457,7 +457,8 @@ int medusa_build_candidates(const int32_t* next_root, const int32_t* topk,
                             int s_max, int K, const medusa_tree_t* tree,
                             int B, int32_t* tokens, void* stream);
 
-/* Scratch bytes medusa_accept_rejection needs (B rows of V floats). */
+/* Scratch bytes medusa_accept_rejection needs (2 B rows of V floats: the
+ * target and draft rows of each sequence). */
 size_t medusa_accept_rejection_workspace_size(int B, int V);
 
 /* Rejection-sampling acceptance over the tree, an alternative to
