@@ -15,15 +15,18 @@
 // is drawn from p (inverse CDF).  Lossless when a node's children are
 // independent draws from q_k.  The uniforms are inputs.
 //
-// One CTA of 1024 threads per sequence.  At each node the kernel
-// exponentiates every logit once: a pass of maxima (the node's logits and
-// the drafting head's, no exponentials), then a pass that writes
-// e^(z/tau - max) for both to two workspace rows and sums them, so p and q
-// are the rows times scalars.  A rejection is one pass that writes the
+// A thread-block cluster of 8 CTAs (1024 threads each) per sequence, each
+// CTA owning one eighth of the vocabulary, so that the V-wide passes run on
+// eight SMs; their maxima and sums are combined through distributed shared
+// memory.  At each node the kernel exponentiates every logit once: a pass of
+// maxima (the node's logits and the drafting head's), then a pass that
+// writes e^(z/tau - max) for both to two workspace rows and sums them, so p
+// and q are the rows times scalars.  A rejection is one pass that writes the
 // residual [p - q]_+ over the target row and sums it; the acceptance tests
-// and the final draw (per-warp segment sums in double, a prefix over the
-// segments, a scan of one segment) read the rows.  Every pass keeps 16 loads
-// in flight per thread: one CTA per sequence is latency-bound otherwise.
+// read the rows (from L2: another CTA may own the token) and the final draw
+// takes per-warp segment sums in double, a prefix over the CTAs and the
+// segments, and a scan of one segment.  Every pass keeps 16 loads in flight
+// per thread.
 #include <math.h>
 
 #include "common.cuh"
@@ -34,16 +37,11 @@ namespace {
 
 constexpr int kThreads = 1024;
 constexpr int kWarps = kThreads / 32;
+constexpr int kCluster = 8;  // CTAs per sequence, each owning a slice of the vocabulary
+constexpr int kU = 16;       // loads in flight per thread in every V-wide pass
 
-MDEV float block_sum(float v, float* red) {
-  v = warp_sum(v);
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  __syncthreads();
-  if (lane == 0) red[warp] = v;
-  __syncthreads();
-  v = lane < kWarps ? red[lane] : 0.f;
-  return warp_sum(v);
-}
+template <bool MAX>
+MDEV float op2(float x, float y) { return MAX ? fmaxf(x, y) : x + y; }
 
 // Two block-wide reductions at once (max or sum); every thread gets both.
 template <bool MAX>
@@ -51,9 +49,8 @@ MDEV void block_pair(float& a, float& b, float2* red) {
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) {
-    const float xa = __shfl_xor_sync(0xffffffffu, a, o), xb = __shfl_xor_sync(0xffffffffu, b, o);
-    a = MAX ? fmaxf(a, xa) : a + xa;
-    b = MAX ? fmaxf(b, xb) : b + xb;
+    a = op2<MAX>(a, __shfl_xor_sync(0xffffffffu, a, o));
+    b = op2<MAX>(b, __shfl_xor_sync(0xffffffffu, b, o));
   }
   __syncthreads();
   if (lane == 0) red[warp] = make_float2(a, b);
@@ -64,32 +61,99 @@ MDEV void block_pair(float& a, float& b, float2* red) {
   b = r.y;
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) {
-    const float xa = __shfl_xor_sync(0xffffffffu, a, o), xb = __shfl_xor_sync(0xffffffffu, b, o);
-    a = MAX ? fmaxf(a, xa) : a + xa;
-    b = MAX ? fmaxf(b, xb) : b + xb;
+    a = op2<MAX>(a, __shfl_xor_sync(0xffffffffu, a, o));
+    b = op2<MAX>(b, __shfl_xor_sync(0xffffffffu, b, o));
   }
 }
 
-constexpr int kU = 16;  // loads in flight per thread in every V-wide pass
+MDEV double warp_sum_d(double x) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) x += __shfl_xor_sync(0xffffffffu, x, o);
+  return x;
+}
 
-// Rows are read in rounds of kU coalesced loads per thread: element
-// v = base + u * kThreads + threadIdx.x of round `base`.
-#define MEDUSA_ROUNDS(V) for (int base = 0; base < (V); base += kU * kThreads)
+// ---- thread-block cluster: barrier and distributed shared memory
+MDEV void cluster_sync_all() {
+  asm volatile("barrier.cluster.arrive.release.aligned;\n" ::: "memory");
+  asm volatile("barrier.cluster.wait.acquire.aligned;\n" ::: "memory");
+}
+MDEV uint32_t cluster_addr(const void* p, uint32_t rank) {
+  uint32_t r;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;\n" : "=r"(r) : "r"(smem_u32(p)), "r"(rank));
+  return r;
+}
+MDEV float2 ld_cluster_f2(uint32_t addr) {
+  float2 v;
+  asm volatile("ld.shared::cluster.v2.f32 {%0, %1}, [%2];\n" : "=f"(v.x), "=f"(v.y) : "r"(addr) : "memory");
+  return v;
+}
+MDEV double ld_cluster_f64(uint32_t addr) {
+  double v;
+  asm volatile("ld.shared::cluster.f64 %0, [%1];\n" : "=d"(v) : "r"(addr) : "memory");
+  return v;
+}
+
+// Reductions over the cluster's CTAs: a block reduction, each CTA's result
+// in its exchange slot (two slots used in turn: a CTA reuses a slot only
+// after the next cluster barrier, which every reader of it has reached),
+// one cluster barrier, then every thread combines the CTAs' values in rank
+// order, so every CTA gets the same bits.  The barrier's release / acquire
+// also publishes the workspace rows each CTA wrote before it.
+struct ClusterRed {
+  float2* red;   // [kWarps] block scratch
+  float2* xf;    // [2] exchange slots, floats
+  double* xd;    // [2] exchange slots, doubles
+  int ph;
+  template <bool MAX>
+  MDEV void pair(float& a, float& b) {
+    block_pair<MAX>(a, b, red);
+    const int slot = ph++ & 1;
+    if (threadIdx.x == 0) xf[slot] = make_float2(a, b);
+    cluster_sync_all();
+    float ra = MAX ? -INFINITY : 0.f, rb = ra;
+#pragma unroll
+    for (int r = 0; r < kCluster; ++r) {
+      const float2 v = ld_cluster_f2(cluster_addr(&xf[slot], (uint32_t)r));
+      ra = op2<MAX>(ra, v.x);
+      rb = op2<MAX>(rb, v.y);
+    }
+    a = ra;
+    b = rb;
+  }
+  MDEV float sum(float a) {
+    float b = 0.f;
+    pair<false>(a, b);
+    return a;
+  }
+  // every CTA's double (one per CTA, written by thread 0) in rank order
+  MDEV void gather_d(double mine, double* out) {
+    const int slot = ph++ & 1;
+    if (threadIdx.x == 0) xd[slot] = mine;
+    cluster_sync_all();
+#pragma unroll
+    for (int r = 0; r < kCluster; ++r) out[r] = ld_cluster_f64(cluster_addr(&xd[slot], (uint32_t)r));
+  }
+};
+
+// A CTA's passes cover its slice [lo, hi) of the vocabulary in rounds of kU
+// coalesced loads per thread: element lo + base + u * kThreads + threadIdx.x.
+#define MEDUSA_ROUNDS(lo, hi) for (int base = (lo); base < (hi); base += kU * kThreads)
 #define MEDUSA_IDX(u) (base + (u) * kThreads + (int)threadIdx.x)
 
-// The node's target row Pw and the drafting head's row Qw (workspace):
-// p(v) = Pw[v] * sp, q(v) = Qw[v] * sq.  Rows are written with e^(y - max)
-// of y = logit / tau once per node.
-MDEV void exp_rows(const float* z, const float* dz, int V, float inv_tau, float* Pw, float* Qw, float& sp,
-                   float& sq, float2* red) {
+// The node's target row Pw and the drafting head's row Qw (workspace, this
+// CTA's slice): p(v) = Pw[v] * sp, q(v) = Qw[v] * sq, written with
+// e^(y - max) of y = logit / tau once per node.  The maxima and sums are
+// cluster-wide.
+MDEV void exp_rows(const float* z, const float* dz, int lo, int hi, float inv_tau, float* Pw, float* Qw,
+                   float& sp, float& sq, ClusterRed& R) {
   float mp = -INFINITY, mq = -INFINITY;
-  MEDUSA_ROUNDS(V) {
+  MEDUSA_ROUNDS(lo, hi) {
     float a[kU], c[kU];
 #pragma unroll
     for (int u = 0; u < kU; ++u) {
       const int v = MEDUSA_IDX(u);
-      a[u] = v < V ? z[v] : -INFINITY;
-      c[u] = (dz && v < V) ? dz[v] : -INFINITY;
+      a[u] = v < hi ? z[v] : -INFINITY;
+      c[u] = (dz && v < hi) ? dz[v] : -INFINITY;
     }
 #pragma unroll
     for (int u = 0; u < kU; ++u) {
@@ -97,20 +161,20 @@ MDEV void exp_rows(const float* z, const float* dz, int V, float inv_tau, float*
       mq = fmaxf(mq, c[u] * inv_tau);
     }
   }
-  block_pair<true>(mp, mq, red);
+  R.pair<true>(mp, mq);
   float Sp = 0.f, Sq = 0.f;
-  MEDUSA_ROUNDS(V) {
+  MEDUSA_ROUNDS(lo, hi) {
     float a[kU], c[kU];
 #pragma unroll
     for (int u = 0; u < kU; ++u) {
       const int v = MEDUSA_IDX(u);
-      a[u] = v < V ? z[v] : 0.f;
-      c[u] = (dz && v < V) ? dz[v] : 0.f;
+      a[u] = v < hi ? z[v] : 0.f;
+      c[u] = (dz && v < hi) ? dz[v] : 0.f;
     }
 #pragma unroll
     for (int u = 0; u < kU; ++u) {
       const int v = MEDUSA_IDX(u);
-      if (v < V) {
+      if (v < hi) {
         const float ep = expf(a[u] * inv_tau - mp);
         Pw[v] = ep;
         Sp += ep;
@@ -122,51 +186,59 @@ MDEV void exp_rows(const float* z, const float* dz, int V, float inv_tau, float*
       }
     }
   }
-  block_pair<false>(Sp, Sq, red);  // its barriers also publish the rows
+  R.pair<false>(Sp, Sq);  // its cluster barrier also publishes the rows
   sp = 1.f / Sp;
   sq = dz ? 1.f / Sq : 0.f;
 }
 
-// p <- [p - q]_+ (unnormalised, over Pw); returns its sum.
-MDEV float residual(float* Pw, const float* Qw, float sp, float sq, int V, float* red) {
+// p <- [p - q]_+ (unnormalised, over this CTA's slice of Pw); returns the
+// cluster-wide sum.
+MDEV float residual(float* Pw, const float* Qw, float sp, float sq, int lo, int hi, ClusterRed& R) {
   float S = 0.f;
-  MEDUSA_ROUNDS(V) {
+  MEDUSA_ROUNDS(lo, hi) {
     float a[kU], c[kU];
 #pragma unroll
     for (int u = 0; u < kU; ++u) {
       const int v = MEDUSA_IDX(u);
-      a[u] = v < V ? Pw[v] : 0.f;
-      c[u] = v < V ? Qw[v] : 0.f;
+      a[u] = v < hi ? Pw[v] : 0.f;
+      c[u] = v < hi ? Qw[v] : 0.f;
     }
 #pragma unroll
     for (int u = 0; u < kU; ++u) {
       const int v = MEDUSA_IDX(u);
-      if (v < V) {
+      if (v < hi) {
         const float r = fmaxf(0.f, a[u] * sp - c[u] * sq);
         Pw[v] = r;
         S += r;
       }
     }
   }
-  return block_sum(S, red);  // its barriers also publish the residual row
+  return R.sum(S);  // its cluster barrier also publishes the residual row
 }
 
-MDEV double warp_sum_d(double x) {
-#pragma unroll
-  for (int o = 16; o > 0; o >>= 1) x += __shfl_xor_sync(0xffffffffu, x, o);
-  return x;
+// The last v in [lo, hi) with p(v) > 0 (-1 if none), in every thread.
+MDEV int last_with_mass(const float* Pw, float sp, int lo, int hi, float2* red) {
+  float best = -1.f, dummy = -1.f;  // indices below 2^24 are exact in float
+  for (int v = lo + (int)threadIdx.x; v < hi; v += kThreads)
+    if (Pw[v] * sp > 0.f) best = (float)v;
+  block_pair<true>(best, dummy, red);
+  return (int)best;
 }
 
-// Inverse CDF: the first v with p(v) = Pw[v] * sp > 0 whose running sum of p,
-// in index order and in double, exceeds u; the last v with mass when u is
-// beyond the total.  Warp w takes the w-th contiguous segment of V: segment
-// sums, an exclusive prefix over the segments, then the one warp whose
-// interval holds u scans its segment 32 elements at a time.  Result valid
-// in every thread.
-MDEV int draw(const float* Pw, float sp, int V, double u, double* wsum, int* s_tok) {
+// Inverse CDF over the cluster: the first v with p(v) = Pw[v] * sp > 0
+// whose running sum of p, in index order and in double, exceeds u; the last
+// v with mass when u is beyond the total.  Each warp of each CTA sums a
+// contiguous segment of the CTA's slice; the CTAs' totals are exchanged and
+// summed in rank order (the same bits in every CTA, so the CTAs' intervals
+// are disjoint); the CTA whose interval holds u finds the warp whose
+// segment holds it, and that warp scans its segment 32 elements at a time.
+// Returns the token in the CTA that found it (rank 0 for the beyond-total
+// case), -2 in the others.
+MDEV int draw(const float* Pw, float sp, int lo, int hi, double u, double* wsum, int* s_tok, ClusterRed& R,
+              int crank) {
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int seg = (V + kWarps - 1) / kWarps;
-  const int s0 = min(V, warp * seg), s1 = min(V, s0 + seg);
+  const int seg = (hi - lo + kWarps - 1) / kWarps;
+  const int s0 = min(hi, lo + warp * seg), s1 = min(hi, s0 + seg);
   double acc = 0.0;
   for (int base = s0; base < s1; base += 32 * kU) {
     float a[kU];
@@ -180,65 +252,85 @@ MDEV int draw(const float* Pw, float sp, int V, double u, double* wsum, int* s_t
   }
   acc = warp_sum_d(acc);
   if (lane == 0) wsum[warp] = acc;
-  if (threadIdx.x == 0) *s_tok = -1;
+  if (threadIdx.x == 0) *s_tok = -2;
   __syncthreads();
-  double before = 0.0;  // the same sums in the same order in every warp: the intervals are disjoint
-  for (int w = 0; w < warp; ++w) before += wsum[w];
-  if (s0 < s1 && u >= before && u < before + wsum[warp]) {
-    double run = before;
-    int tok = -1;
-    for (int base = s0; base < s1 && tok < 0; base += 32) {
-      const int v = base + lane;
-      const float pv = v < s1 ? Pw[v] * sp : 0.f;
-      double c = (double)pv;
+  double mine = 0.0, off = 0.0;  // this CTA's total, and the mass before this warp's segment
+  for (int w = 0; w < kWarps; ++w) {
+    if (w == warp) off = mine;
+    mine += wsum[w];
+  }
+  double tot[kCluster];
+  R.gather_d(mine, tot);
+  double before = 0.0, total = 0.0;
+  for (int r = 0; r < kCluster; ++r) {
+    if (r == crank) before = total;
+    total += tot[r];
+  }
+  if (u >= total) {  // beyond the rounded total: the last token with mass, cluster-wide
+    float last = (float)last_with_mass(Pw, sp, lo, hi, R.red), dummy = -1.f;
+    R.pair<true>(last, dummy);
+    return crank == 0 ? (int)last : -2;
+  }
+  const bool mine_u = u >= before && u < before + tot[crank];  // exactly one CTA
+  if (mine_u) {
+    const double ul = u - before;
+    if (s0 < s1 && ul >= off && ul < off + wsum[warp]) {
+      double run = off;
+      int tok = -1;
+      for (int base = s0; base < s1 && tok < 0; base += 32) {
+        const int v = base + lane;
+        const float pv = v < s1 ? Pw[v] * sp : 0.f;
+        double c = (double)pv;
 #pragma unroll
-      for (int o = 1; o < 32; o <<= 1) {
-        const double y = __shfl_up_sync(0xffffffffu, c, o);
-        if (lane >= o) c += y;
+        for (int o = 1; o < 32; o <<= 1) {
+          const double y = __shfl_up_sync(0xffffffffu, c, o);
+          if (lane >= o) c += y;
+        }
+        const unsigned hit = __ballot_sync(0xffffffffu, pv > 0.f && ul < run + c);
+        if (hit) tok = base + __ffs(hit) - 1;
+        run += __shfl_sync(0xffffffffu, c, 31);
       }
-      const unsigned hit = __ballot_sync(0xffffffffu, pv > 0.f && u < run + c);
-      if (hit) tok = base + __ffs(hit) - 1;
-      run += __shfl_sync(0xffffffffu, c, 31);
+      for (int base = s1 - 32; tok < 0 && base > s0 - 32; base -= 32) {  // rounding: the segment's last with mass
+        const int v = base + lane;
+        const unsigned hit = __ballot_sync(0xffffffffu, v >= s0 && v < s1 && Pw[v] * sp > 0.f);
+        if (hit) tok = base + 31 - __clz(hit);
+      }
+      if (lane == 0) *s_tok = tok;
     }
-    for (int base = s1 - 32; tok < 0 && base > s0 - 32; base -= 32) {  // rounding: the segment's last with mass
-      const int v = base + lane;
-      const unsigned hit = __ballot_sync(0xffffffffu, v >= s0 && v < s1 && Pw[v] * sp > 0.f);
-      if (hit) tok = base + 31 - __clz(hit);
-    }
-    if (lane == 0) *s_tok = tok;
   }
   __syncthreads();
   int tok = *s_tok;
-  if (tok < 0) {  // u beyond the rounded total: the last token with mass
-    __syncthreads();
-    if (threadIdx.x == 0)
-      for (int v = V - 1; v >= 0 && *s_tok < 0; --v)
-        if (Pw[v] * sp > 0.f) *s_tok = v;
-    __syncthreads();
-    tok = *s_tok;
-  }
-  return tok;
+  if (mine_u && tok < 0) tok = last_with_mass(Pw, sp, lo, hi, R.red);  // rounding between the warps' intervals
+  return mine_u ? tok : -2;
 }
 
-__global__ void __launch_bounds__(kThreads) reject_tree_kernel(
+__global__ void __cluster_dims__(kCluster, 1, 1) __launch_bounds__(kThreads) reject_tree_kernel(
     const float* logits, const float* draft, int Kd, const int32_t* tokens, medusa_tree_t tree, int V,
     float inv_tau, const float* uni, int u_stride, int32_t* accept_len, int32_t* accepted_nodes,
     int32_t* next_token, float* pws, int32_t* err) {
-  const int b = blockIdx.x, tid = threadIdx.x;
+  const int crank = blockIdx.x, b = blockIdx.y, tid = threadIdx.x;  // gridDim.x == kCluster
   const int T = tree.T, K = tree.K;
-  float* Pw = pws + (int64_t)b * 2 * V;  // target row
+  const int lo = (int)((int64_t)crank * V / kCluster), hi = (int)((int64_t)(crank + 1) * V / kCluster);
+  float* Pw = pws + (int64_t)b * 2 * V;  // target row (each CTA writes its slice)
   float* Qw = Pw + V;                    // drafting head's row
-  __shared__ float red[kWarps];
-  __shared__ float2 red2[kWarps];
+  __shared__ float2 red[kWarps];
+  __shared__ float2 xf[2];
+  __shared__ double xd[2];
   __shared__ int kid_by_rank[MEDUSA_MAX_S + 1];
   __shared__ int kids[MEDUSA_MAX_S + 1];
   __shared__ int s_m, s_tok;
   __shared__ double wsum[kWarps];
+  ClusterRed R{red, xf, xd, 0};
 
   int32_t* an = accepted_nodes + (int64_t)b * (K + 1);
-  for (int j = tid; j <= K; j += kThreads) an[j] = j == 0 ? 0 : -1;
+  if (crank == 0)
+    for (int j = tid; j <= K; j += kThreads) an[j] = j == 0 ? 0 : -1;
   float sp = 0.f, sq = 0.f;
   int cur = 0, len = 0, m = 0;
+  // every decision below depends only on values that are the same in every
+  // CTA of the cluster (tree, tokens, uniforms, cluster-reduced scalars and
+  // workspace entries read from L2), so all CTAs take the same path through
+  // the same cluster barriers
   for (int guard = 0;; ++guard) {
     // children of cur in rank order (ranks of siblings are distinct, 1..MEDUSA_MAX_S)
     if (tid <= MEDUSA_MAX_S) kid_by_rank[tid] = -1;
@@ -247,7 +339,7 @@ __global__ void __launch_bounds__(kThreads) reject_tree_kernel(
       if (tree.parent[n] == cur) {
         const int r = tree.rank[n];
         if (r >= 1 && r <= MEDUSA_MAX_S) kid_by_rank[r] = n;
-        else set_err(err, MEDUSA_DEVERR_NODE);
+        else if (crank == 0) set_err(err, MEDUSA_DEVERR_NODE);
       }
     __syncthreads();
     if (tid == 0) {
@@ -262,40 +354,41 @@ __global__ void __launch_bounds__(kThreads) reject_tree_kernel(
     const bool walk = guard <= K && m > 0 && m < u_stride && k >= 1 && k <= K && k <= Kd;
     const float* dz = walk ? draft + ((int64_t)b * Kd + (k - 1)) * V : nullptr;
     // p at this node (and q of the children's head when the walk goes on)
-    exp_rows(logits + ((int64_t)b * T + cur) * V, dz, V, inv_tau, Pw, Qw, sp, sq, red2);
+    exp_rows(logits + ((int64_t)b * T + cur) * V, dz, lo, hi, inv_tau, Pw, Qw, sp, sq, R);
     if (!walk) break;
     int acc = -1;
     for (int j = 0; j < m; ++j) {
       const int n = kids[j];
       const int x = tokens[(int64_t)b * T + n];
       if (x < 0 || x >= V) {  // an invalid draft is never accepted
-        if (tid == 0) set_err(err, MEDUSA_DEVERR_TOKEN);
+        if (tid == 0 && crank == 0) set_err(err, MEDUSA_DEVERR_TOKEN);
         continue;
       }
       const float u = uni[((int64_t)b * T + cur) * u_stride + j];
-      const float qx = Qw[x] * sq;
-      const float px = Pw[x] * sp;
+      const float qx = __ldcg(Qw + x) * sq;  // L2: another CTA may own x
+      const float px = __ldcg(Pw + x) * sp;
       if (u * qx < px) {
         acc = n;
         break;
       }
       // rejected: p <- [p - q]_+ / sum, the residual and its sum in one pass
-      const float S = residual(Pw, Qw, sp, sq, V, red);
+      const float S = residual(Pw, Qw, sp, sq, lo, hi, R);
       sp = S > 0.f ? 1.f / S : 0.f;
     }
     if (acc < 0) break;
     ++len;
-    if (tid == 0) an[len] = acc;
+    if (tid == 0 && crank == 0) an[len] = acc;
     cur = acc;
     m = 0;
   }
   // final draw from p at the node where the walk stopped
   const float u = uni[((int64_t)b * T + cur) * u_stride + (m < u_stride ? m : u_stride - 1)];
-  const int tok = draw(Pw, sp, V, (double)u, wsum, &s_tok);
+  const int tok = draw(Pw, sp, lo, hi, (double)u, wsum, &s_tok, R, crank);
   if (tid == 0) {
-    accept_len[b] = len;
-    next_token[b] = tok;
+    if (tok != -2) next_token[b] = tok;
+    if (crank == 0) accept_len[b] = len;
   }
+  cluster_sync_all();  // no CTA leaves while another may still read its exchange slots
 }
 
 }  // namespace
@@ -324,7 +417,7 @@ extern "C" int medusa_accept_rejection(const float* logits, const float* draft_l
   const size_t need = medusa_accept_rejection_workspace_size(B, V);
   if (!workspace || workspace_bytes < need)
     return fail(MEDUSA_ERR_WORKSPACE, "%s: workspace %zu < %zu bytes", fn, workspace_bytes, need);
-  launch_kernel(reject_tree_kernel, dim3(B), dim3(kThreads), 0, as_stream(stream), logits, draft_logits, Kd,
+  launch_kernel(reject_tree_kernel, dim3(kCluster, B), dim3(kThreads), 0, as_stream(stream), logits, draft_logits, Kd,
                 tokens, *tree, V, 1.f / temperature, uniforms, u_stride, accept_len, accepted_nodes, next_token,
                 static_cast<float*>(workspace), err);
   return check_launch(fn);
