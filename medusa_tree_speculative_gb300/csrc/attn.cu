@@ -13,17 +13,18 @@
 //   * issues the cp.async copies of its first prefix tile and the loads of
 //     its query rows before building the cos/sin tables at pos = L + depth,
 //   * rotates its query rows and folds in scale * log2(e),
-//   * streams its keys through double-buffered shared tiles: prefix keys by
+//   * streams its keys through three shared tile stages (two tiles in flight
+//     while one is used; the query rows are staged in the third): prefix keys by
 //     cp.async from the cache; tree keys rotated from k_new on the fly and,
 //     by the CTAs of the last row block, appended to the cache at slot L + i,
 //   * applies the ancestor bitmask to tree keys, runs QK^T and PV on tensor
 //     cores (bf16 in, fp32 accumulate) over the 16-key blocks that hold keys,
 //     with the online softmax in registers,
-//   * pushes its partial (max, sum, unnormalised O) for each query row into
-//     the shared memory of the CTA that owns the row (rows are dealt round
-//     robin), reusing its query buffer, which every CTA has released at an
-//     early split cluster barrier.
-// After one blocking cluster barrier each CTA merges its own rows from local
+//   * after a cluster barrier that every CTA reaches when it has left its key
+//     loop, pushes its partial (max, sum, unnormalised O) for each query row
+//     into the tile buffers of the CTA that owns the row (rows are dealt
+//     round robin).
+// After a second cluster barrier each CTA merges its own rows from local
 // shared memory and writes the output.  With CL = 1 (few, long CTAs, for a
 // caller that runs the attention on the SMs another kernel leaves idle) the
 // CTA walks every key and writes its rows directly.  No scratch memory, no
@@ -77,25 +78,25 @@ void row_split(int T, int& rowblocks, int& warps) {
 // Query rows are dealt to the cluster's CTAs round robin for the merge.
 __host__ __device__ constexpr int rows_per_owner(int nrows, int CL) { return (nrows + CL - 1) / CL; }
 
-// Key/value tile stages in flight.  A lone CTA (CL = 1) walks every key of
-// its head, so it keeps two tiles ahead instead of one; its query rows are
-// staged in the third stage's buffer, which is first filled after the query
-// fragments have moved to registers.
-__host__ __device__ constexpr int kv_stages(int CL) { return CL == 1 ? 3 : 2; }
+// Key/value tile stages: three, so that two tiles are in flight while one is
+// used (beside a kernel that keeps HBM busy, a tile's loads take several
+// microseconds).  The tile buffers also hold the query rows (the last stage,
+// first filled after the query fragments have moved to registers) and, once
+// every CTA of the cluster has left its key loop, the partials pushed by the
+// cluster's CTAs (fp32 O and (max, sum), from the first stage on).
+constexpr int kStages = 3;
 
-// Bytes of the region that first holds the rotated query rows (bf16) and
-// later the partials pushed by the cluster's CTAs (fp32 O and (max, sum));
-// none for CL = 1 (the query rows use a tile stage).
-__host__ __device__ constexpr int qrecv_bytes(int Dh, int warps, int CL) {
-  const int q = warps * 16 * Dh * 2;
-  const int r = CL * rows_per_owner(warps * 16, CL) * (Dh + 2) * 4;
-  return CL == 1 ? 0 : (q > r ? q : r);
+// Bytes of the pushed partials a CTA receives.
+__host__ __device__ constexpr int recv_bytes(int Dh, int warps, int CL) {
+  return CL == 1 ? 0 : CL * rows_per_owner(warps * 16, CL) * (Dh + 2) * 4;
 }
+static_assert(recv_bytes(128, MAX_WARPS, 8) <= kStages * 2 * KT * 128 * 2, "partials fit the tile buffers");
+static_assert(recv_bytes(64, MAX_WARPS, 8) <= kStages * 2 * KT * 64 * 2, "partials fit the tile buffers");
+static_assert(2 * KT >= MAX_WARPS * 16, "query rows must fit one K+V stage");
 
-size_t smem_bytes(int Dh, int warps, int K, int CL) {
-  return (size_t)kv_stages(CL) * 2 * KT * Dh * 2  // K and V tiles per stage, bf16
-         + (size_t)qrecv_bytes(Dh, warps, CL)     // query rows, then the pushed partials
-         + (size_t)2 * (K + 1) * (Dh / 2) * 4;    // cos / sin per tree depth
+size_t smem_bytes(int Dh, int K) {
+  return (size_t)kStages * 2 * KT * Dh * 2     // K and V tiles per stage, bf16
+         + (size_t)2 * (K + 1) * (Dh / 2) * 4;  // cos / sin per tree depth
 }
 
 // Sequence b is usable iff 0 <= L <= max_prefix and L + T fits its capacity.
@@ -147,8 +148,6 @@ MDEV uint32_t map_to_rank(uint32_t local_smem_addr, uint32_t rank) {
   asm volatile("mapa.shared::cluster.u32 %0, %1, %2;\n" : "=r"(r) : "r"(local_smem_addr), "r"(rank));
   return r;
 }
-MDEV void cluster_arrive() { asm volatile("barrier.cluster.arrive.release.aligned;\n" ::: "memory"); }
-MDEV void cluster_wait() { asm volatile("barrier.cluster.wait.acquire.aligned;\n" ::: "memory"); }
 MDEV void st_cluster_f32x2(uint32_t addr, float x, float y) {
   asm volatile("st.shared::cluster.v2.f32 [%0], {%1, %2};\n" ::"r"(addr), "f"(x), "f"(y) : "memory");
 }
@@ -163,18 +162,17 @@ __global__ void __cluster_dims__(CL, 1, 1) __launch_bounds__(MAX_WARPS * 32, 2)
   constexpr int HALF = DH / 2;
   constexpr int HCH = CH / 2;   // chunks per rotary half
   constexpr int QI = HCH / 2;   // query items per thread: rows * HCH / (rows * 2)
-  constexpr int S = kv_stages(CL);
-  static_assert(CL > 1 || 2 * KT >= MAX_WARPS * 16, "query rows must fit one K+V stage");
+  constexpr int S = kStages;
   extern __shared__ __align__(128) uint8_t smem[];
   uint16_t* kvbuf = reinterpret_cast<uint16_t*>(smem);  // [S][K, V][KT][DH]
-  uint8_t* qrecv = reinterpret_cast<uint8_t*>(kvbuf + S * 2 * KT * DH);
-  // [rows][DH] until the q fragments are loaded: the last stage (CL = 1) or qrecv
-  uint16_t* qbuf = CL == 1 ? kvbuf + (S - 1) * 2 * KT * DH : reinterpret_cast<uint16_t*>(qrecv);
+  // [rows][DH] until the q fragments are loaded: the last stage
+  uint16_t* qbuf = kvbuf + (S - 1) * 2 * KT * DH;
   const int nrows = a.warps * 16;
   const int RPO = rows_per_owner(nrows, CL);
-  float* recv_o = reinterpret_cast<float*>(qrecv);             // then [CL][RPO][DH]
-  float* recv_ml = recv_o + CL * RPO * DH;                     //      [CL][RPO][2]
-  float* cs = reinterpret_cast<float*>(qrecv + qrecv_bytes(DH, a.warps, CL));  // [K+1][HALF]
+  // after every CTA of the cluster has left its key loop: the pushed partials
+  float* recv_o = reinterpret_cast<float*>(smem);  // [CL][RPO][DH]
+  float* recv_ml = recv_o + CL * RPO * DH;         // [CL][RPO][2]
+  float* cs = reinterpret_cast<float*>(kvbuf + S * 2 * KT * DH);  // [K+1][HALF]
   float* sn = cs + (a.K + 1) * HALF;
 
   const uint32_t crank = CL > 1 ? cluster_ctarank() : 0u;
@@ -331,11 +329,8 @@ __global__ void __cluster_dims__(CL, 1, 1) __launch_bounds__(MAX_WARPS * 32, 2)
       ldmatrix_x4(qf[kk], smem_u32(qbuf + rr * DH + ((c ^ (rr & 7)) * 8)));
     }
   }
-  // the query buffer becomes the landing area of the pushed partials (no CTA
-  // pushes before every CTA of the cluster has arrived here) or, for CL = 1,
-  // the last tile stage
+  // the query buffer becomes the last tile stage
   __syncthreads();
-  if (CL > 1) cluster_arrive();
 
   float m_a = -INFINITY, m_b = -INFINITY, l_a = 0.f, l_b = 0.f;
   float o[DH / 8][4];
@@ -470,8 +465,9 @@ __global__ void __cluster_dims__(CL, 1, 1) __launch_bounds__(MAX_WARPS * 32, 2)
   }
 
   // ---- push this CTA's partial of each local row to the row's owner
-  // (rank rr % CL, slot rr / CL): every CTA has released its query buffer
-  cluster_wait();
+  // (rank rr % CL, slot rr / CL), into the owner's tile buffers: every CTA
+  // has left its key loop (and its copies have landed) at this barrier
+  cluster_sync();
   const uint32_t o_base = smem_u32(recv_o), ml_base = smem_u32(recv_ml);
   if (row0 + la < a.T) {
     const uint32_t ra_o = map_to_rank(o_base + (((int)crank * RPO + la / CL) * DH) * 4, (uint32_t)(la % CL));
@@ -657,7 +653,7 @@ namespace {
 template <int DH, int CL>
 void launch_attn_bf16(const AttnArgs& a, int B, int H, cudaStream_t s) {
   dim3 grid(CL, H, B * a.rowblocks);
-  const size_t sm = smem_bytes(DH, a.warps, a.K, CL);
+  const size_t sm = smem_bytes(DH, a.K);
   cudaFuncSetAttribute(attn_tree_kernel<DH, CL>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sm);
   launch_kernel(attn_tree_kernel<DH, CL>, grid, dim3(a.warps * 32), sm, s, a);
 }
