@@ -61,9 +61,10 @@ class VerifyStep:
         # leaves idle instead of holding the LM head back), or after the
         # acceptance ("after_accept": beside the heads, whose rows are handed
         # out at run time; "after_heads": forked there but enqueued after the
-        # heads' kernels), with the library's default key split (None) or 1,
-        # 2, 4, 8 CTAs per head ("auto": 4 for bf16, the fastest measured
-        # beside the LM head at the 7B shape)
+        # heads' kernels), with the library's default key split (None), 1, 2,
+        # 4, 8 CTAs per head, or "tc" (medusa_tree_attn_tc: bf16, Dh 128);
+        # "auto": 4 for bf16, the fastest measured beside the LM head at the
+        # 7B shape
         if attn_order not in ("first", "after_lm", "after_accept", "after_heads"):
             raise ValueError(f"attn_order {attn_order!r}")
         if attn_splits == "auto":
@@ -161,9 +162,14 @@ class VerifyStep:
             side.wait_stream(main)
 
         def attention():
-            M.medusa_tree_attn(x["q"], x["k_new"], x["v_new"], x["k_cache"], x["v_cache"], x["seq_start"],
-                               x["prefix_len"], x["seq_cap"], self.tree, self.max_prefix, self.rope_theta,
-                               self.scale, self.out, self.ws_attn, self.err, side, key_splits=self.attn_splits)
+            if self.attn_splits == "tc":
+                M.medusa_tree_attn_tc(x["q"], x["k_new"], x["v_new"], x["k_cache"], x["v_cache"], x["seq_start"],
+                                      x["prefix_len"], x["seq_cap"], self.tree, self.max_prefix, self.rope_theta,
+                                      self.scale, self.out, self.err, side)
+            else:
+                M.medusa_tree_attn(x["q"], x["k_new"], x["v_new"], x["k_cache"], x["v_cache"], x["seq_start"],
+                                   x["prefix_len"], x["seq_cap"], self.tree, self.max_prefix, self.rope_theta,
+                                   self.scale, self.out, self.ws_attn, self.err, side, key_splits=self.attn_splits)
 
         if self.attn_order == "first":
             attention()
