@@ -64,9 +64,9 @@ def parse_args():
     ap.add_argument("--attn-order", choices=["first", "after_lm", "after_accept", "after_heads"], default="after_lm",
                     help="attention enqueued before the LM head or right after it (its CTAs then fill the "
                          "SMs the LM head leaves idle)")
-    ap.add_argument("--attn-splits", choices=["1", "2", "4", "8", "tc"], default=None,
-                    help="CTAs that split one head's keys, or tc for the tensor-core attention "
-                         "(default: 4 for bf16)")
+    ap.add_argument("--attn-splits", choices=["1", "2", "4", "8", "tc", "tc1", "tc2", "tc4", "tc8"], default=None,
+                    help="CTAs that split one head's keys, or tc[N] for the tensor-core attention with N "
+                         "(default: one wave of CTAs) (default: 4 for bf16)")
     return ap.parse_args()
 
 
@@ -231,13 +231,7 @@ def step_calls(st, x, s):
     from medusa_tree_speculative_gb300 import medusa as M
 
     joint = st.heads == "joint"
-    c = [("tree_attn", (lambda: M.medusa_tree_attn_tc(
-            x["q"], x["k_new"], x["v_new"], x["k_cache"], x["v_cache"], x["seq_start"], x["prefix_len"],
-            x["seq_cap"], st.tree, st.max_prefix, st.rope_theta, st.scale, st.out, st.err, s))
-          if st.attn_splits == "tc" else (lambda: M.medusa_tree_attn(
-            x["q"], x["k_new"], x["v_new"], x["k_cache"], x["v_cache"], x["seq_start"], x["prefix_len"],
-            x["seq_cap"], st.tree, st.max_prefix, st.rope_theta, st.scale, st.out, st.ws_attn, st.err, s,
-            key_splits=st.attn_splits))),
+    c = [("tree_attn", lambda: st.attention(x, s)),
          ("lm_head_verify", (lambda: M.medusa_lm_head_verify_heads_hidden(
              x["hidden"], st.w_lm_run, st.logits.shape[-1], st.logits, st.w1_run, st.b1, st.s_heads, st.u_all,
              st.err, s, layout=st.w_layout, w1_layout=st.w1_layout)) if joint else
@@ -295,7 +289,7 @@ def run_native(args, w, rank, world, local_rank):
     L_list = xh["prefix_len"].copy()
     st = step.VerifyStep(w, wd, tree, max_prefix=int(L_list.max()), device=dev, heads=args.heads,
                          accept=args.accept, write_logits=args.logits, attn_order=args.attn_order,
-                         attn_splits=(args.attn_splits if args.attn_splits == "tc" else int(args.attn_splits))
+                         attn_splits=(args.attn_splits if args.attn_splits.startswith("tc") else int(args.attn_splits))
                          if args.attn_splits else "auto")
     plant(w, tree, st, x, args.plant_depth, torch)
     prefix0 = x["prefix_len"].clone()
@@ -384,7 +378,8 @@ def run_native(args, w, rank, world, local_rank):
     return dict(ms_step=ms_step, ms_events_step=ms_events / args.steps, per_call_ms=per_call, clocks=clocks,
                 dloop=dloop, rej=rej,
                 T=T, s_heads=st.s_heads, L_list=L_list, accept_len=accept_len, e2e=e2e,
-                launches=st.launches_per_step * args.steps, tree=ht, attn_splits=st.attn_splits or 8)
+                launches=st.launches_per_step * args.steps, tree=ht,
+                attn_splits=f"tc{st.tc_splits}" if st.attn_splits == "tc" else st.attn_splits or 8)
 
 
 def measure_rejection(st, x, s, torch, M, reps=20):

@@ -189,23 +189,28 @@ int medusa_tree_attn_splits(const void* q, const void* k_new,
                             int32_t* err, void* stream);
 
 /* medusa_tree_attn on the tensor cores (tcgen05 MMAs with the accumulators
- * in tensor memory, TMA tile loads), bf16 with Dh = 128 only: one CTA per
- * (sequence, head, block of up to 128 query rows) walks every key in tiles of
- * 128; S = Q K^T and P V run on the tensor cores, the masked online softmax
- * on one thread per query row.  It appends the tree's keys and values to the
- * cache first (every row block of a sequence writes the same bytes) and reads
- * them back with the prefix.  cache_rows: rows of k_cache / v_cache (the
- * tiles' loads stop there).  Same arguments otherwise (no workspace), same
- * results up to the order of the fp32 sums; a bounded on-chip wait that gives
- * up sets MEDUSA_DEVERR_TIMEOUT.  Other dtypes or head sizes:
- * MEDUSA_ERR_UNSUPPORTED. */
+ * in tensor memory, TMA tile loads), bf16 with Dh = 128 only.  A cluster of
+ * key_splits CTAs (1, 2, 4 or 8) per (sequence, head, block of up to 128
+ * query rows) takes contiguous runs of the key tiles of 128; S = Q K^T and
+ * P V run on the tensor cores, the masked online softmax on two threads per
+ * query row.  With key_splits > 1 each CTA keeps its partial (max, sum, O) in
+ * its shared memory and, after a cluster barrier, finalises one slice of the
+ * output columns from every CTA's partial through distributed shared memory.
+ * The CTA whose tiles hold the tree's keys first appends them (rotated) and
+ * the values to the cache (every row block of a sequence writes the same
+ * bytes) and reads them back with the prefix.  cache_rows: rows of k_cache /
+ * v_cache (the tiles' loads stop there).  Same arguments otherwise (no
+ * workspace), same results up to the order of the fp32 sums; a bounded
+ * on-chip wait that gives up sets MEDUSA_DEVERR_TIMEOUT.  Other dtypes, head
+ * sizes or key_splits: MEDUSA_ERR_UNSUPPORTED. */
 int medusa_tree_attn_tc(const void* q, const void* k_new, const void* v_new,
                         void* k_cache, void* v_cache, int64_t cache_rows,
                         const int64_t* seq_start, const int32_t* prefix_len,
                         const int64_t* seq_cap, const medusa_tree_t* tree,
                         int B, int H, int Dh, int max_prefix,
                         float rope_theta, float scale, medusa_dtype dtype,
-                        void* out, int32_t* err, void* stream);
+                        void* out, int key_splits, int32_t* err,
+                        void* stream);
 
 /* Scratch bytes medusa_lm_head_verify needs (currently 0). */
 size_t medusa_lm_head_workspace_size(int rows, int d, int V);

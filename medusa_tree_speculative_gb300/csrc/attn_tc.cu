@@ -20,12 +20,14 @@
 //     S_t = Q K_t^T (M = 128 query rows, N = 128 keys, K = 128) into one of
 //     two S accumulators, two tiles ahead, and PV_t = P_t V_t (N = 128 value
 //     columns, K = 128 keys; V is read in its cache layout, keys x values,
-//     as an MN-major operand) into a third accumulator;
-//   * warps 2-5 own one query row per thread (its tensor-memory lane): read
-//     S_t, mask it (keys past the sequence; tree keys that are not an
-//     ancestor-or-self of the row), update the running max, write
-//     P_t = 2^(S - max) in bf16 to shared memory for the PV MMA, and fold
-//     PV_t into the row's output registers with the online-softmax rescale.
+//     as an MN-major operand) into one of two more accumulators in turn;
+//   * warps 2-9 give each query row (its tensor-memory lane) two threads,
+//     one per half of the tile's keys and of the output columns: read S_t,
+//     mask it (keys past the sequence; tree keys that are not an
+//     ancestor-or-self of the row), agree on the row's running max through
+//     shared memory, write P_t = 2^(S - max) in bf16 to shared memory for the
+//     PV MMA, and fold PV_{t-1} into the output registers with the
+//     online-softmax rescale while PV_t runs.
 // Every mbarrier wait is bounded; a wait that gives up sets
 // MEDUSA_DEVERR_TIMEOUT, lets the copies in flight land, frees tensor memory
 // and returns.
@@ -48,7 +50,8 @@ using namespace sm100;
 constexpr int DH = 128;        // head dimension (two 64-wide swizzle spans)
 constexpr int BN = 128;        // keys per tile (MMA N of S, K of PV)
 constexpr int BMR = 128;       // query rows per CTA (MMA M)
-constexpr int kThreads = 192;  // warp 0 loads, warp 1 MMAs, warps 2-5 softmax
+constexpr int kThreads = 320;  // warp 0 loads, warp 1 MMAs, warps 2-9 softmax (two per row quarter)
+constexpr int kSoftThreads = 256;
 constexpr int kMaxWords = (MEDUSA_MAX_T + 31) / 32;
 constexpr float kLog2e = 1.4426950408889634f;
 
@@ -59,9 +62,13 @@ constexpr uint32_t kKOff = 65536;                // K   [2 stages][2 k-chunks][1
 constexpr uint32_t kVOff = 131072;               // V   [2 stages][2 column halves][128 keys][128 B]
 constexpr uint32_t kTileBytes = 32768;           // one K or V tile
 constexpr uint32_t kBarOff = 196608;             // mbarriers, tensor-memory slot, flags
-constexpr uint32_t kAncOff = kBarOff + 256;      // ancestor words [128 rows][kMaxWords]
+constexpr uint32_t kAncOff = kBarOff + 192 + 2048;  // ancestor words [128 rows][kMaxWords]
 constexpr uint32_t kCsOff = kAncOff + BMR * kMaxWords * 4;  // cos / sin [K+1][64] each
-constexpr uint32_t kTmemCols = 512;              // S0, S1, PV (128 columns each)
+constexpr uint32_t kTmemCols = 512;              // S0, S1, PV0, PV1 (128 columns each)
+constexpr int kPartStride = DH + 4;              // merge: floats per partial row (padded)
+constexpr uint32_t kPartOff = kKOff;             // merge: this CTA's O partial [128 rows][kPartStride] fp32
+constexpr uint32_t kMlOff = kPartOff + BMR * kPartStride * 4;  // merge: (max, sum) [128 rows]
+constexpr uint32_t kXOff = kBarOff + 192;        // partial row maxima [2 tiles][2 halves][128 rows] (floats)
 
 struct AttnTcArgs {
   const uint16_t* q;
@@ -137,12 +144,62 @@ MDEV void rope8(const uint4& lo, const uint4& hi, const float* c, const float* s
                    pack2_bf16(r2[6], r2[7]));
 }
 
+// (a, b) += (x, y) as one packed fp32x2 add, round to nearest.
+MDEV void add2(float& a, float& b, float x, float y) {
+  asm("{\n .reg .b64 A, X;\n mov.b64 A, {%0, %1};\n mov.b64 X, {%2, %3};\n add.rn.f32x2 A, A, X;\n"
+      " mov.b64 {%0, %1}, A;\n}\n"
+      : "+f"(a), "+f"(b)
+      : "f"(x), "f"(y));
+}
+// (a, b) = (a, b) * s + (x, y) as one packed fp32x2 fused multiply-add.
+MDEV void fma2(float& a, float& b, float s, float x, float y) {
+  asm("{\n .reg .b64 A, S, X;\n mov.b64 A, {%0, %1};\n mov.b64 S, {%2, %2};\n mov.b64 X, {%3, %4};\n"
+      " fma.rn.f32x2 A, A, S, X;\n mov.b64 {%0, %1}, A;\n}\n"
+      : "+f"(a), "+f"(b)
+      : "f"(s), "f"(x), "f"(y));
+}
+// 2^x with the hardware approximation (subnormal results flush to 0; 2^-inf = 0).
+MDEV float ex2_ftz(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
+MDEV void sync_cluster() {
+  asm volatile("barrier.cluster.arrive.release.aligned;\n" ::: "memory");
+  asm volatile("barrier.cluster.wait.acquire.aligned;\n" ::: "memory");
+}
+// This CTA's shared address `a` as seen in the shared memory of cluster CTA `rank`.
+MDEV uint32_t remote_addr(uint32_t a, uint32_t rank) {
+  uint32_t r;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;\n" : "=r"(r) : "r"(a), "r"(rank));
+  return r;
+}
+MDEV float4 ld_cluster_f4(uint32_t addr) {
+  float4 v;
+  asm volatile("ld.shared::cluster.v4.f32 {%0, %1, %2, %3}, [%4];\n"
+               : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w)
+               : "r"(addr)
+               : "memory");
+  return v;
+}
+MDEV void ld_cluster_f2(uint32_t addr, float& x, float& y) {
+  asm volatile("ld.shared::cluster.v2.f32 {%0, %1}, [%2];\n" : "=f"(x), "=f"(y) : "r"(addr) : "memory");
+}
+MDEV void st_shared_f4(uint32_t addr, float x, float y, float z, float w) {
+  asm volatile("st.shared.v4.f32 [%0], {%1, %2, %3, %4};\n" ::"r"(addr), "f"(x), "f"(y), "f"(z), "f"(w) : "memory");
+}
+MDEV void st_shared_f2(uint32_t addr, float x, float y) {
+  asm volatile("st.shared.v2.f32 [%0], {%1, %2};\n" ::"r"(addr), "f"(x), "f"(y) : "memory");
+}
+
 MDEV void st_shared_v4(uint32_t addr, const uint4& v) {
   asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};\n" ::"r"(addr), "r"(v.x), "r"(v.y), "r"(v.z), "r"(v.w)
                : "memory");
 }
 
-__global__ void __launch_bounds__(kThreads, 1)
+template <int CL>
+__global__ void __cluster_dims__(CL, 1, 1) __launch_bounds__(kThreads, 1)
     attn_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV,
                    const __grid_constant__ AttnTcArgs a) {
   extern __shared__ uint8_t smem_raw[];
@@ -154,13 +211,15 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint64_t* v_full = bars + 4;   // [2]
   uint64_t* v_empty = bars + 6;  // [2]
   uint64_t* s_full = bars + 8;   // [2] MMA -> softmax: S_t ready
-  uint64_t* s_empty = bars + 10; // [2] softmax -> MMA: S buffer read (128 arrivals)
-  uint64_t* p_full = bars + 12;  // softmax -> MMA: P_t written (128 arrivals)
-  uint64_t* pv_full = bars + 13; // MMA -> softmax: PV_t ready
-  uint64_t* pv_empty = bars + 14;// softmax -> MMA: PV accumulator read (128 arrivals)
-  uint64_t* mma_done = bars + 15;// every MMA issued so far has completed
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 16);
-  int* s_abort = reinterpret_cast<int*>(bars + 17);
+  uint64_t* s_empty = bars + 10; // [2] softmax -> MMA: S buffer read (256 arrivals)
+  uint64_t* p_full = bars + 12;  // softmax -> MMA: P_t written (256 arrivals)
+  uint64_t* pv_full = bars + 13; // [2] MMA -> softmax: PV_t ready (accumulator t & 1)
+  uint64_t* pv_empty = bars + 15;// [2] softmax -> MMA: PV accumulator read (256 arrivals)
+  uint64_t* mma_done = bars + 17;// every MMA issued so far has completed
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 18);
+  int* s_abort = reinterpret_cast<int*>(bars + 19);
+  uint64_t* xm_full = bars + 20; // [2] softmax halves: the row's partial maxima written (256 arrivals)
+  float* xmax = reinterpret_cast<float*>(smem + kXOff);  // [2 tiles][2 halves][128 rows]
   uint32_t* ancs = reinterpret_cast<uint32_t*>(smem + kAncOff);
   float* cs = reinterpret_cast<float*>(smem + kCsOff);
   float* sn = cs + (a.K + 1) * (DH / 2);
@@ -171,11 +230,21 @@ __global__ void __launch_bounds__(kThreads, 1)
   int L;
   int64_t st;
   if (!seq_ok(a, b, L, st)) {  // the whole CTA leaves before any barrier or allocation
-    if (h == 0 && rb == 0 && tid == 0) set_err(a.err, MEDUSA_DEVERR_CAPACITY);
+    if (h == 0 && rb == 0 && blockIdx.x == 0 && tid == 0) set_err(a.err, MEDUSA_DEVERR_CAPACITY);
     return;
   }
   const int nkeys = L + a.T, ntiles = (nkeys + BN - 1) / BN;
   const int HD = a.H * DH;
+  // this CTA's run of key tiles, [t_begin, t_begin + nt): the first CTAs of
+  // the unit take the extra tiles, the last one holds the tree's keys
+  constexpr int sp = CL;
+  const int crank = blockIdx.x;
+  const int t_begin = (int)(((int64_t)crank * ntiles + sp - 1) / sp);
+  const int nt = (int)(((int64_t)(crank + 1) * ntiles + sp - 1) / sp) - t_begin;
+  // tree nodes whose keys fall in this CTA's tiles (this CTA appends them)
+  const int n_lo = max(0, t_begin * BN - L), n_hi = min(a.T, (t_begin + nt) * BN - L);
+  const int nlive = min(BMR, a.T - row0);  // query rows of this block
+  int n_early = 0;  // tiles the loader issued before the prologue (thread 0 only)
 
   if (tid == 0) {
     for (int i = 0; i < 2; ++i) {
@@ -184,20 +253,50 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(&v_full[i], 1);
       mbar_init(&v_empty[i], 1);
       mbar_init(&s_full[i], 1);
-      mbar_init(&s_empty[i], 128);
+      mbar_init(&s_empty[i], kSoftThreads);
+      mbar_init(&pv_full[i], 1);
+      mbar_init(&pv_empty[i], kSoftThreads);
+      mbar_init(&xm_full[i], kSoftThreads);
     }
-    mbar_init(p_full, 128);
-    mbar_init(pv_full, 1);
-    mbar_init(pv_empty, 128);
+    mbar_init(p_full, kSoftThreads);
     mbar_init(mma_done, 1);
     fence_barrier_init();
     *s_abort = 0;
     tma_prefetch_desc(&tmK);
     tma_prefetch_desc(&tmV);
+    // the first tiles that hold prefix keys only need no appended row: they
+    // load while the prologue runs (fresh stages, nothing to wait for)
+    for (; n_early < 2 && n_early < nt && (t_begin + n_early + 1) * BN <= L; ++n_early) {
+      const int y = (int)(st + (int64_t)(t_begin + n_early) * BN);
+      mbar_expect_tx(&k_full[n_early], kTileBytes);
+      for (int kc = 0; kc < 2; ++kc)
+        tma_load_2d(smem + kKOff + n_early * kTileBytes + kc * 16384, &tmK, &k_full[n_early], h * DH + kc * 64, y);
+      mbar_expect_tx(&v_full[n_early], kTileBytes);
+      for (int kc = 0; kc < 2; ++kc)
+        tma_load_2d(smem + kVOff + n_early * kTileBytes + kc * 16384, &tmV, &v_full[n_early], h * DH + kc * 64, y);
+    }
   }
   if (warp == 1) {
     tmem_alloc(tmem_slot, kTmemCols);
     tmem_relinquish();
+  }
+  // query rows of this block: their loads go out first and land while the
+  // rotation tables are formed
+  constexpr int kQPer = (BMR * 8 + kThreads - 1) / kThreads;
+  uint4 qlo[kQPer], qhi[kQPer];
+  int qd[kQPer];
+#pragma unroll
+  for (int k = 0; k < kQPer; ++k) {
+    const int e = tid + k * kThreads, r = e >> 3, c = e & 7;  // row, 16-byte chunk of the first half
+    qlo[k] = make_uint4(0, 0, 0, 0);
+    qhi[k] = qlo[k];
+    qd[k] = 0;
+    if (r < nlive) {
+      const int64_t src = (((int64_t)b * a.T + row0 + r) * a.H + h) * DH;
+      qd[k] = min(max(__ldg(a.depth + row0 + r), 0), a.K);
+      qlo[k] = ldg_v4(a.q + src + c * 8);
+      qhi[k] = ldg_v4(a.q + src + 64 + c * 8);
+    }
   }
   // cos / sin at positions L + d for every tree depth d
   for (int e = tid; e < (a.K + 1) * (DH / 2); e += kThreads) {
@@ -208,43 +307,60 @@ __global__ void __launch_bounds__(kThreads, 1)
     cs[e] = c;
     sn[e] = s;
   }
-  __syncthreads();
-  // the tree's keys (rotated at L + depth) and values into the cache at slot
-  // L + i; every row block of the sequence writes the same bytes
-  for (int e = tid; e < a.T * 8; e += kThreads) {
-    const int i = e >> 3, c = e & 7;  // node, 16-byte chunk of the first half
-    const int64_t src = (((int64_t)b * a.T + i) * a.H + h) * DH;
-    const int64_t dst = (st + L + i) * HD + (int64_t)h * DH;
-    const int d = min(max(__ldg(a.depth + i), 0), a.K);
-    uint4 klo, khi;
-    rope8(ldg_v4(a.k_new + src + c * 8), ldg_v4(a.k_new + src + 64 + c * 8), cs + d * 64 + c * 8,
-          sn + d * 64 + c * 8, 1.f, klo, khi);
-    *reinterpret_cast<uint4*>(a.k_cache + dst + c * 8) = klo;
-    *reinterpret_cast<uint4*>(a.k_cache + dst + 64 + c * 8) = khi;
-    *reinterpret_cast<uint4*>(a.v_cache + dst + c * 8) = ldg_v4(a.v_new + src + c * 8);
-    *reinterpret_cast<uint4*>(a.v_cache + dst + 64 + c * 8) = ldg_v4(a.v_new + src + 64 + c * 8);
-  }
-  fence_async_global();  // the appended rows are read back through the tensor maps
-  // query rows: rotated at L + depth, times scale * log2(e), bf16, swizzled K-major
-  for (int e = tid; e < BMR * 8; e += kThreads) {
-    const int r = e >> 3, c = e & 7;
-    const int rr = row0 + r;
-    uint4 lo = make_uint4(0, 0, 0, 0), hi = lo;
-    if (rr < a.T) {
-      const int64_t src = (((int64_t)b * a.T + rr) * a.H + h) * DH;
-      const int d = min(max(__ldg(a.depth + rr), 0), a.K);
-      rope8(ldg_v4(a.q + src + c * 8), ldg_v4(a.q + src + 64 + c * 8), cs + d * 64 + c * 8, sn + d * 64 + c * 8,
-            a.qscale, lo, hi);
-    }
-    st_shared_v4(sw128(sbase + kQOff, r, c), lo);
-    st_shared_v4(sw128(sbase + kQOff + 16384, r, c), hi);
-  }
   // ancestor words of this block's rows
   for (int e = tid; e < BMR * a.W; e += kThreads) {
     const int r = e / a.W, w = e % a.W;
-    const int rr = row0 + r;
-    ancs[r * kMaxWords + w] = rr < a.T ? __ldg(a.anc + (int64_t)rr * a.W + w) : 0u;
+    ancs[r * kMaxWords + w] = r < nlive ? __ldg(a.anc + (int64_t)(row0 + r) * a.W + w) : 0u;
   }
+  __syncthreads();
+  // query rows rotated at L + depth, times scale * log2(e), bf16, swizzled
+  // K-major; rows past the tree are zero
+#pragma unroll
+  for (int k = 0; k < kQPer; ++k) {
+    const int e = tid + k * kThreads, r = e >> 3, c = e & 7;
+    if (e < BMR * 8) {
+      uint4 lo = make_uint4(0, 0, 0, 0), hi = lo;
+      if (r < nlive) rope8(qlo[k], qhi[k], cs + qd[k] * 64 + c * 8, sn + qd[k] * 64 + c * 8, a.qscale, lo, hi);
+      st_shared_v4(sw128(sbase + kQOff, r, c), lo);
+      st_shared_v4(sw128(sbase + kQOff + 16384, r, c), hi);
+    }
+  }
+  // the tree's keys (rotated at L + depth) and values into the cache at slot
+  // L + i, for the nodes whose keys fall in this CTA's tiles; every row block
+  // of the sequence writes the same bytes
+  const int items = (n_hi - n_lo) * 8;  // 16-byte chunks of the first half
+  for (int e0 = tid; e0 < items; e0 += 2 * kThreads) {
+    uint4 kl[2], kh[2], vl[2], vh[2];
+    int dd[2];
+#pragma unroll
+    for (int u = 0; u < 2; ++u) {
+      const int e = e0 + u * kThreads;
+      if (e < items) {
+        const int i = n_lo + (e >> 3), c = e & 7;
+        const int64_t src = (((int64_t)b * a.T + i) * a.H + h) * DH + c * 8;
+        dd[u] = min(max(__ldg(a.depth + i), 0), a.K);
+        kl[u] = ldg_v4(a.k_new + src);
+        kh[u] = ldg_v4(a.k_new + src + 64);
+        vl[u] = ldg_v4(a.v_new + src);
+        vh[u] = ldg_v4(a.v_new + src + 64);
+      }
+    }
+#pragma unroll
+    for (int u = 0; u < 2; ++u) {
+      const int e = e0 + u * kThreads;
+      if (e < items) {
+        const int i = n_lo + (e >> 3), c = e & 7;
+        const int64_t dst = (st + L + i) * HD + (int64_t)h * DH + c * 8;
+        uint4 klo, khi;
+        rope8(kl[u], kh[u], cs + dd[u] * 64 + c * 8, sn + dd[u] * 64 + c * 8, 1.f, klo, khi);
+        *reinterpret_cast<uint4*>(a.k_cache + dst) = klo;
+        *reinterpret_cast<uint4*>(a.k_cache + dst + 64) = khi;
+        *reinterpret_cast<uint4*>(a.v_cache + dst) = vl[u];
+        *reinterpret_cast<uint4*>(a.v_cache + dst + 64) = vh[u];
+      }
+    }
+  }
+  if (items > 0) fence_async_global();  // the appended rows are read back through the tensor maps
   fence_async_smem();  // Q is read by the tensor cores
   tc_fence_before();
   __syncthreads();
@@ -255,12 +371,12 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (warp == 0) {
     // ---------------- TMA: key and value tiles, two stages each
     if (lane == 0) {
-      int t = 0;
+      int t = n_early;  // local tile index: key tile t_begin + t
       bool ok = true;
-      for (; t < ntiles && ok; ++t) {
+      for (; t < nt && ok; ++t) {
         const int s = t & 1;
         const uint32_t ph = (uint32_t)(t >> 1) & 1u;
-        const int y = (int)(st + (int64_t)t * BN);
+        const int y = (int)(st + (int64_t)(t_begin + t) * BN);
         if (!wait_or_abort(&k_empty[s], ph ^ 1u, abort_flag)) { ok = false; break; }
         mbar_expect_tx(&k_full[s], kTileBytes);
         for (int kc = 0; kc < 2; ++kc)
@@ -282,6 +398,11 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         set_err(a.err, MEDUSA_DEVERR_TIMEOUT);
       }
+    }
+    if constexpr (CL > 1) {  // the merge's two cluster barriers
+      __syncwarp();
+      sync_cluster();
+      sync_cluster();
     }
   } else if (warp == 1) {
     // ---------------- MMA issuer
@@ -308,19 +429,19 @@ __global__ void __launch_bounds__(kThreads, 1)
         umma_commit(&k_empty[s]);  // the key stage is free once these MMAs have read it
         umma_commit(&s_full[s]);
       };
-      issue_s(0);
-      if (ok && ntiles > 1) issue_s(1);
-      int t = 0;
-      for (; t < ntiles && ok; ++t) {
+      if (nt > 0) issue_s(0);
+      if (ok && nt > 1) issue_s(1);
+      int t = 0;  // local tile index
+      for (; t < nt && ok; ++t) {
         const int s = t & 1;
         const uint32_t ph = (uint32_t)(t >> 1) & 1u;
         if (!wait_or_abort(p_full, (uint32_t)t & 1u, abort_flag) || !wait_or_abort(&v_full[s], ph, abort_flag) ||
-            !wait_or_abort(pv_empty, ((uint32_t)t & 1u) ^ 1u, abort_flag)) {
+            !wait_or_abort(&pv_empty[s], ph ^ 1u, abort_flag)) {
           ok = false;
           break;
         }
         tc_fence_after();
-        const uint32_t dPV = tmem_base + 2 * BN;
+        const uint32_t dPV = tmem_base + (uint32_t)(2 + s) * BN;  // two accumulators in turn
         for (int kc = 0; kc < 2; ++kc) {
           const uint64_t da = desc_kmajor_sw128(sbase + kPOff + kc * 16384);
 #pragma unroll
@@ -331,38 +452,58 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
         }
         umma_commit(&v_empty[s]);
-        umma_commit(pv_full);
-        if (t + 2 < ntiles) issue_s(t + 2);
+        umma_commit(&pv_full[s]);
+        if (t + 2 < nt) issue_s(t + 2);
       }
       if (!ok) set_err(a.err, MEDUSA_DEVERR_TIMEOUT);
       // every MMA issued completes before tensor memory or the stages go away
       umma_commit(mma_done);
       if (!mbar_wait(mma_done, 0)) set_err(a.err, MEDUSA_DEVERR_TIMEOUT);
     }
+    if constexpr (CL > 1) {  // the merge's two cluster barriers
+      __syncwarp();
+      sync_cluster();
+      sync_cluster();
+    }
   } else {
-    // ---------------- softmax: one query row per thread (tensor-memory lane)
-    const int g = warp & 3;  // this warp may read lanes 32g .. 32g+31
+    // ---------------- softmax: two threads per query row (its tensor-memory
+    // lane); each owns 64 of a tile's keys and 64 of the output columns
+    const int g = warp & 3;          // this warp may read lanes 32g .. 32g+31
+    const int hh = (warp - 2) >> 2;  // key half of S_t, column half of PV_t
     const int r = 32 * g + lane;
-    const uint32_t trow = tmem_base + ((uint32_t)(32 * g) << 16);
+    const uint32_t trow = tmem_base + ((uint32_t)(32 * g) << 16) + (uint32_t)(hh * 64);
+    const uint32_t preg = sbase + kPOff + (uint32_t)hh * 16384;  // P rows, keys hh*64 .. hh*64+63
     const uint32_t* myanc = ancs + r * kMaxWords;
-    float o[DH];
+    float o[64];
 #pragma unroll
-    for (int j = 0; j < DH; ++j) o[j] = 0.f;
-    float m = -INFINITY, l = 0.f;
+    for (int j = 0; j < 64; ++j) o[j] = 0.f;
+    float m = -INFINITY, l = 0.f, a_prev = 1.f;
     bool ok = true;
-    for (int t = 0; t < ntiles; ++t) {
+    // PV_j folded into the output: o = o * alpha_j + PV_j
+    auto fold = [&](int j, float alpha) {
+      uint32_t v[64];
+#pragma unroll
+      for (int q = 0; q < 4; ++q) tmem_ld_32x32b_x16(trow + (uint32_t)((2 + (j & 1)) * BN + q * 16), v + q * 16);
+      tmem_ld_wait();
+#pragma unroll
+      for (int i = 0; i < 64; i += 2) fma2(o[i], o[i + 1], alpha, __uint_as_float(v[i]), __uint_as_float(v[i + 1]));
+      tc_fence_before();
+      mbar_arrive(&pv_empty[j & 1]);
+    };
+    int t = 0;  // local tile index: key tile t_begin + t
+    for (; t < nt; ++t) {
       const int s = t & 1;
       const uint32_t ph = (uint32_t)(t >> 1) & 1u;
       const bool got = wait_or_abort(&s_full[s], ph, abort_flag);
       if (__any_sync(0xffffffffu, !got)) { ok = false; break; }
       __syncwarp();
       tc_fence_after();
-      const int key0 = t * BN;
-      // this row's visible keys of the tile as 128 bits: prefix keys always,
-      // tree node n = j - L when it is an ancestor-or-self, nothing past the keys
-      uint32_t vm[4];
+      const int key0 = (t_begin + t) * BN + hh * 64;
+      // this thread's visible keys as 64 bits: prefix keys always, tree node
+      // n = j - L when it is an ancestor-or-self of the row, nothing past the keys
+      uint32_t vm[2];
 #pragma unroll
-      for (int w = 0; w < 4; ++w) {
+      for (int w = 0; w < 2; ++w) {
         const int j0 = key0 + 32 * w;
         uint32_t bits = 0u;
         if (j0 + 32 <= L) {
@@ -381,95 +522,156 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         vm[w] = bits;
       }
-      // pass 1: the tile's maximum over visible keys, 64 columns per load
-      float mx[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
-#pragma unroll 1
-      for (int hc = 0; hc < BN / 64; ++hc) {
-        const uint32_t vw[2] = {hc ? vm[2] : vm[0], hc ? vm[3] : vm[1]};
-        uint32_t v[64];
+      uint32_t v[64];
 #pragma unroll
-        for (int q = 0; q < 4; ++q) tmem_ld_32x32b_x16(trow + (uint32_t)(s * BN + hc * 64 + q * 16), v + q * 16);
-        tmem_ld_wait();
+      for (int q = 0; q < 4; ++q) tmem_ld_32x32b_x16(trow + (uint32_t)(s * BN + q * 16), v + q * 16);
+      tmem_ld_wait();
+      // hidden keys become -inf (2^-inf = 0 below); most tiles hide nothing
+      if (!__all_sync(0xffffffffu, (vm[0] & vm[1]) == 0xffffffffu)) {
 #pragma unroll
-        for (int i = 0; i < 64; ++i) {
-          const float x = ((vw[i >> 5] >> (i & 31)) & 1u) ? __uint_as_float(v[i]) : -INFINITY;
-          mx[i & 3] = fmaxf(mx[i & 3], x);
-        }
+        for (int i = 0; i < 64; ++i) v[i] = ((vm[i >> 5] >> (i & 31)) & 1u) ? v[i] : 0xff800000u;
       }
-      const float mt = fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3]));
+      float mx[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
+#pragma unroll
+      for (int i = 0; i < 64; ++i) mx[i & 3] = fmaxf(mx[i & 3], __uint_as_float(v[i]));
+      // the row's tile maximum from both halves
+      xmax[((t & 1) * 2 + hh) * BMR + r] = fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3]));
+      mbar_arrive(&xm_full[s]);
+      const bool xgot = wait_or_abort(&xm_full[s], ph, abort_flag);
+      if (__any_sync(0xffffffffu, !xgot)) { ok = false; break; }
+      const float mt = fmaxf(xmax[((t & 1) * 2 + hh) * BMR + r], xmax[((t & 1) * 2 + (hh ^ 1)) * BMR + r]);
       const float mn = fmaxf(m, mt);
       const float base = mn == -INFINITY ? 0.f : mn;
       const float alpha = exp2f(m - base);  // 0 while nothing was visible
-      // pass 2: p = 2^(s - max) into P (bf16, swizzled K-major), and its sum
-      float sm[4] = {0.f, 0.f, 0.f, 0.f};
-#pragma unroll 1
-      for (int hc = 0; hc < BN / 64; ++hc) {
-        const uint32_t vw[2] = {hc ? vm[2] : vm[0], hc ? vm[3] : vm[1]};
-        uint32_t v[64];
-#pragma unroll
-        for (int q = 0; q < 4; ++q) tmem_ld_32x32b_x16(trow + (uint32_t)(s * BN + hc * 64 + q * 16), v + q * 16);
-        tmem_ld_wait();
-        const uint32_t region = sbase + kPOff + (uint32_t)hc * 16384;  // keys hc*64 .. hc*64+63
-#pragma unroll
-        for (int ch = 0; ch < 8; ++ch) {  // 16-byte chunks of the 128-byte row: 8 keys each
-          float p[8];
-#pragma unroll
-          for (int i = 0; i < 8; ++i) {
-            const int k = ch * 8 + i;
-            const float x = __uint_as_float(v[k]) - base;
-            p[i] = ((vw[k >> 5] >> (k & 31)) & 1u) ? exp2f(x) : 0.f;
-            sm[i & 3] += p[i];
-          }
-          st_shared_v4(sw128(region, r, ch), make_uint4(pack2_bf16(p[0], p[1]), pack2_bf16(p[2], p[3]),
-                                                         pack2_bf16(p[4], p[5]), pack2_bf16(p[6], p[7])));
-        }
+      // P_{t-1} stays in shared memory until PV_{t-1} has completed (it
+      // normally has: it was issued a tile's softmax ago)
+      if (t > 0) {
+        const bool pgot = wait_or_abort(&pv_full[(t - 1) & 1], (uint32_t)((t - 1) >> 1) & 1u, abort_flag);
+        if (__any_sync(0xffffffffu, !pgot)) { ok = false; break; }
+        __syncwarp();
       }
-      const float ls = (sm[0] + sm[1]) + (sm[2] + sm[3]);
-      l = l * alpha + ls;
+      // p = 2^(s - max) into P (bf16, swizzled K-major), and its sum (pairs
+      // of lanes in f32x2)
+      float sa[2] = {0.f, 0.f}, sb[2] = {0.f, 0.f};
+#pragma unroll
+      for (int ch = 0; ch < 8; ++ch) {  // 16-byte chunks of the 128-byte row: 8 keys each
+        uint32_t pk[4];
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          float x0 = __uint_as_float(v[8 * ch + 2 * i]), x1 = __uint_as_float(v[8 * ch + 2 * i + 1]);
+          add2(x0, x1, -base, -base);
+          const float p0 = ex2_ftz(x0), p1 = ex2_ftz(x1);
+          add2(sa[i & 1], sb[i & 1], p0, p1);
+          pk[i] = pack2_bf16(p0, p1);
+        }
+        st_shared_v4(sw128(preg, r, ch), make_uint4(pk[0], pk[1], pk[2], pk[3]));
+      }
+      l = l * alpha + ((sa[0] + sb[0]) + (sa[1] + sb[1]));
       m = mn;
       // the last tile's value rows past the sequence's keys are zeroed (their
       // p is 0, but the rows hold whatever the cache has there)
-      if (key0 + BN > nkeys && key0 + r >= nkeys) {
-        const bool vgot = wait_or_abort(&v_full[s], ph, abort_flag);
-        if (vgot) {
-          const uint4 z = make_uint4(0, 0, 0, 0);
-          for (int c = 0; c < 8; ++c) {
-            st_shared_v4(sbase + kVOff + s * kTileBytes + r * 128 + c * 16, z);
-            st_shared_v4(sbase + kVOff + s * kTileBytes + 16384 + r * 128 + c * 16, z);
-          }
+      if ((t_begin + t) * BN + BN > nkeys && (t_begin + t) * BN + r >= nkeys) {
+        if (wait_or_abort(&v_full[s], ph, abort_flag)) {
+          const uint32_t vrow = sbase + kVOff + s * kTileBytes + (uint32_t)hh * 16384 + r * 128;
+          for (int c = 0; c < 8; ++c) st_shared_v4(vrow + c * 16, make_uint4(0, 0, 0, 0));
         }
       }
       fence_async_smem();  // P (and zeroed V rows) are read by the tensor cores
       tc_fence_before();
       mbar_arrive(&s_empty[s]);
       mbar_arrive(p_full);
-      // PV_t folded into the output with the rescale of the running max
-      const bool pgot = wait_or_abort(pv_full, (uint32_t)t & 1u, abort_flag);
-      if (__any_sync(0xffffffffu, !pgot)) { ok = false; break; }
-      __syncwarp();
-      tc_fence_after();
-#pragma unroll
-      for (int hc = 0; hc < DH / 64; ++hc) {
-        uint32_t v[64];
-#pragma unroll
-        for (int q = 0; q < 4; ++q) tmem_ld_32x32b_x16(trow + (uint32_t)(2 * BN + hc * 64 + q * 16), v + q * 16);
-        tmem_ld_wait();
-#pragma unroll
-        for (int i = 0; i < 64; ++i) o[hc * 64 + i] = o[hc * 64 + i] * alpha + __uint_as_float(v[i]);
+      // PV_{t-1} folds in while PV_t runs
+      if (t > 0) {
+        tc_fence_after();
+        fold(t - 1, a_prev);
       }
-      tc_fence_before();
-      mbar_arrive(pv_empty);
+      a_prev = alpha;
     }
-    if (!ok) {
-      if (lane == 0) set_err(a.err, MEDUSA_DEVERR_TIMEOUT);
-    } else if (row0 + r < a.T) {
-      const float inv = l > 0.f ? 1.f / l : 0.f;
-      uint16_t* dst = a.out + (((int64_t)b * a.T + row0 + r) * a.H + h) * DH;
+    if (ok && nt > 0) {
+      const int j = nt - 1;
+      const bool pgot = wait_or_abort(&pv_full[j & 1], (uint32_t)(j >> 1) & 1u, abort_flag);
+      if (__any_sync(0xffffffffu, !pgot)) {
+        ok = false;
+      } else {
+        __syncwarp();
+        tc_fence_after();
+        fold(j, a_prev);
+      }
+    }
+    // the row's sum from both halves
+    if (ok) {
+      const int s = nt & 1;
+      xmax[(s * 2 + hh) * BMR + r] = l;
+      mbar_arrive(&xm_full[s]);
+      const bool lgot = wait_or_abort(&xm_full[s], (uint32_t)(nt >> 1) & 1u, abort_flag);
+      if (__any_sync(0xffffffffu, !lgot)) ok = false;
+      else l += xmax[(s * 2 + (hh ^ 1)) * BMR + r];
+    }
+    if (!ok && lane == 0) set_err(a.err, MEDUSA_DEVERR_TIMEOUT);
+    const bool live = r < nlive;
+    if constexpr (CL == 1) {
+      if (live) {
+        const float inv = l > 0.f ? 1.f / l : 0.f;
+        uint16_t* dst = a.out + (((int64_t)b * a.T + row0 + r) * a.H + h) * DH + hh * 64;
 #pragma unroll
-      for (int c = 0; c < DH / 8; ++c)
-        *reinterpret_cast<uint4*>(dst + c * 8) =
-            make_uint4(pack2_bf16(o[c * 8] * inv, o[c * 8 + 1] * inv), pack2_bf16(o[c * 8 + 2] * inv, o[c * 8 + 3] * inv),
-                       pack2_bf16(o[c * 8 + 4] * inv, o[c * 8 + 5] * inv), pack2_bf16(o[c * 8 + 6] * inv, o[c * 8 + 7] * inv));
+        for (int c = 0; c < 8; ++c)
+          *reinterpret_cast<uint4*>(dst + c * 8) = make_uint4(
+              pack2_bf16(o[c * 8] * inv, o[c * 8 + 1] * inv), pack2_bf16(o[c * 8 + 2] * inv, o[c * 8 + 3] * inv),
+              pack2_bf16(o[c * 8 + 4] * inv, o[c * 8 + 5] * inv), pack2_bf16(o[c * 8 + 6] * inv, o[c * 8 + 7] * inv));
+      }
+    } else {
+      // the cluster's CTAs hold partials (max m_c, sum l_c, O_c) over disjoint
+      // key runs; CTA c finalises output columns c*CW .. c*CW+CW-1:
+      //   O = sum_c 2^(m_c - M) O_c / sum_c 2^(m_c - M) l_c,  M = max_c m_c
+      // Each partial goes to its own CTA's key/value stages (free: the last
+      // PV has completed) and is read from there by the other CTAs.
+      if (live) {
+        const uint32_t row = sbase + kPartOff + (uint32_t)(r * kPartStride + hh * 64) * 4;
+#pragma unroll
+        for (int k = 0; k < 16; ++k) st_shared_f4(row + k * 16, o[4 * k], o[4 * k + 1], o[4 * k + 2], o[4 * k + 3]);
+        if (hh == 0) st_shared_f2(sbase + kMlOff + r * 8, m, l);
+      }
+      __syncwarp();
+      sync_cluster();  // every partial is in place
+      constexpr int CW = DH / CL, tpr = CW / 8;  // columns per CTA; threads per row, 8 columns each
+      const int u = tid - 64;
+      for (int rr = u / tpr; rr < nlive; rr += kSoftThreads / tpr) {
+        const int col = crank * CW + (u % tpr) * 8;
+        float pm[CL], pl[CL];
+#pragma unroll
+        for (int c = 0; c < CL; ++c) ld_cluster_f2(remote_addr(sbase + kMlOff + rr * 8, (uint32_t)c), pm[c], pl[c]);
+        float mmax = -INFINITY;
+#pragma unroll
+        for (int c = 0; c < CL; ++c) mmax = fmaxf(mmax, pm[c]);
+        float lsum = 0.f;
+#pragma unroll
+        for (int c = 0; c < CL; ++c) {
+          pm[c] = pm[c] == -INFINITY ? 0.f : exp2f(pm[c] - mmax);  // the partial's weight
+          lsum += pm[c] * pl[c];
+        }
+        const float inv = lsum > 0.f ? 1.f / lsum : 0.f;
+        float acc[8];
+#pragma unroll
+        for (int hf = 0; hf < 2; ++hf) {  // four columns at a time: every partial's loads in flight
+          float4 x[CL];
+#pragma unroll
+          for (int c = 0; c < CL; ++c)
+            x[c] = ld_cluster_f4(
+                remote_addr(sbase + kPartOff + (uint32_t)(rr * kPartStride + col + hf * 4) * 4, (uint32_t)c));
+          float s0 = 0.f, s1 = 0.f, s2 = 0.f, s3 = 0.f;
+#pragma unroll
+          for (int c = 0; c < CL; ++c) {
+            s0 += pm[c] * x[c].x; s1 += pm[c] * x[c].y; s2 += pm[c] * x[c].z; s3 += pm[c] * x[c].w;
+          }
+          acc[hf * 4] = s0; acc[hf * 4 + 1] = s1; acc[hf * 4 + 2] = s2; acc[hf * 4 + 3] = s3;
+        }
+        uint16_t* dst = a.out + (((int64_t)b * a.T + row0 + rr) * a.H + h) * DH + col;
+        *reinterpret_cast<uint4*>(dst) =
+            make_uint4(pack2_bf16(acc[0] * inv, acc[1] * inv), pack2_bf16(acc[2] * inv, acc[3] * inv),
+                       pack2_bf16(acc[4] * inv, acc[5] * inv), pack2_bf16(acc[6] * inv, acc[7] * inv));
+      }
+      __syncwarp();
+      sync_cluster();  // no CTA leaves while its partial may still be read
     }
   }
   tc_fence_before();
@@ -514,6 +716,13 @@ bool make_cache_map(CUtensorMap* m, const void* base, int64_t rows, int H) {
              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+template <int CL>
+void launch_tc(dim3 grid, size_t smem, cudaStream_t s, const CUtensorMap& tmK, const CUtensorMap& tmV,
+               const AttnTcArgs& a) {
+  cudaFuncSetAttribute(attn_tc_kernel<CL>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  launch_kernel(attn_tc_kernel<CL>, grid, dim3(kThreads), smem, s, tmK, tmV, a);
+}
+
 }  // namespace
 }  // namespace medusa
 
@@ -523,8 +732,10 @@ extern "C" int medusa_tree_attn_tc(const void* q, const void* k_new, const void*
                                    void* v_cache, int64_t cache_rows, const int64_t* seq_start,
                                    const int32_t* prefix_len, const int64_t* seq_cap, const medusa_tree_t* tree,
                                    int B, int H, int Dh, int max_prefix, float rope_theta, float scale,
-                                   medusa_dtype dtype, void* out, int32_t* err, void* stream) {
+                                   medusa_dtype dtype, void* out, int key_splits, int32_t* err, void* stream) {
   const char* fn = "medusa_tree_attn_tc";
+  if (key_splits != 1 && key_splits != 2 && key_splits != 4 && key_splits != 8)
+    return fail(MEDUSA_ERR_UNSUPPORTED, "%s: key_splits=%d not in {1,2,4,8}", fn, key_splits);
   if (int rc = check_tree(tree, fn)) return rc;
   if (!q || !k_new || !v_new || !k_cache || !v_cache || !seq_start || !prefix_len || !seq_cap || !out)
     return fail(MEDUSA_ERR_INVALID, "%s: NULL tensor", fn);
@@ -557,7 +768,12 @@ extern "C" int medusa_tree_attn_tc(const void* q, const void* k_new, const void*
   if (!make_cache_map(&tmK, k_cache, cache_rows, H) || !make_cache_map(&tmV, v_cache, cache_rows, H))
     return fail(MEDUSA_ERR_CUDA, "%s: cuTensorMapEncodeTiled failed", fn);
   const size_t smem = 1024 + kCsOff + (size_t)2 * (tree->K + 1) * (DH / 2) * 4;
-  cudaFuncSetAttribute(attn_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-  launch_kernel(attn_tc_kernel, dim3(1, H, B * a.rowblocks), dim3(kThreads), smem, as_stream(stream), tmK, tmV, a);
+  const dim3 grid(key_splits, H, B * a.rowblocks);
+  switch (key_splits) {  // the key_splits CTAs of a (sequence, head, row block) form one cluster
+    case 1: launch_tc<1>(grid, smem, as_stream(stream), tmK, tmV, a); break;
+    case 2: launch_tc<2>(grid, smem, as_stream(stream), tmK, tmV, a); break;
+    case 4: launch_tc<4>(grid, smem, as_stream(stream), tmK, tmV, a); break;
+    default: launch_tc<8>(grid, smem, as_stream(stream), tmK, tmV, a); break;
+  }
   return check_launch(fn);
 }

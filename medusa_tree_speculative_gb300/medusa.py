@@ -48,7 +48,7 @@ _SIGS = {
     "medusa_tree_attn_workspace_size": (SZ, [I, I, I, I, I]),
     "medusa_tree_attn": (I, [P, P, P, P, P, P, P, P, TREE, I, I, I, I, F, F, I, P, P, SZ, P, P]),
     "medusa_tree_attn_splits": (I, [P, P, P, P, P, P, P, P, TREE, I, I, I, I, F, F, I, P, P, SZ, I, P, P]),
-    "medusa_tree_attn_tc": (I, [P, P, P, P, P, C.c_int64, P, P, P, TREE, I, I, I, I, F, F, I, P, P, P]),
+    "medusa_tree_attn_tc": (I, [P, P, P, P, P, C.c_int64, P, P, P, TREE, I, I, I, I, F, F, I, P, I, P, P]),
     "medusa_lm_head_workspace_size": (SZ, [I, I, I]),
     "medusa_lm_head_tiled_bytes": (SZ, [I, I]),
     "medusa_lm_head_tile": (I, [P, P, I, I, P]),
@@ -212,13 +212,14 @@ def medusa_tree_attn_workspace_size(B, H, Dh, T, max_prefix) -> int:
 
 def medusa_tree_attn_tc(q, k_new, v_new, k_cache, v_cache, seq_start, prefix_len, seq_cap,
                         tree: DeviceTree, max_prefix: int, rope_theta: float, scale: float, out, err=None,
-                        stream=None):
-    """Tensor-core tree attention (bf16, Dh 128); k_cache / v_cache [rows][H][Dh]."""
+                        stream=None, key_splits=1):
+    """Tensor-core tree attention (bf16, Dh 128); k_cache / v_cache [rows][H][Dh]; a cluster of
+    key_splits CTAs (1, 2, 4 or 8) shares each (sequence, head, row block)'s key tiles."""
     B, T, H, Dh = q.shape
     _check(_lib.medusa_tree_attn_tc(_ptr(q), _ptr(k_new), _ptr(v_new), _ptr(k_cache), _ptr(v_cache),
                                     int(k_cache.shape[0]), _ptr(seq_start), _ptr(prefix_len), _ptr(seq_cap),
                                     tree.ref, B, H, Dh, max_prefix, rope_theta, scale, _dtype(q), _ptr(out),
-                                    _ptr(err), _stream(stream)), "medusa_tree_attn_tc")
+                                    int(key_splits), _ptr(err), _stream(stream)), "medusa_tree_attn_tc")
 
 
 def medusa_tree_attn(q, k_new, v_new, k_cache, v_cache, seq_start, prefix_len, seq_cap,

@@ -62,16 +62,29 @@ class VerifyStep:
         # acceptance ("after_accept": beside the heads, whose rows are handed
         # out at run time; "after_heads": forked there but enqueued after the
         # heads' kernels), with the library's default key split (None), 1, 2,
-        # 4, 8 CTAs per head, or "tc" (medusa_tree_attn_tc: bf16, Dh 128);
-        # "auto": 4 for bf16, the fastest measured beside the LM head at the
-        # 7B shape
+        # 4, 8 CTAs per head, or "tc" (medusa_tree_attn_tc: bf16, Dh 128;
+        # "tc1" .. "tc8" name its key split, "tc" takes the largest that keeps
+        # the grid within one CTA per SM); "auto": 4 for bf16, the fastest
+        # measured beside the LM head at the 7B shape
         if attn_order not in ("first", "after_lm", "after_accept", "after_heads"):
             raise ValueError(f"attn_order {attn_order!r}")
         if attn_splits == "auto":
             attn_splits = 4 if w["dtype"] == "bf16" else None
-        self.attn_order, self.attn_splits = attn_order, attn_splits
         B, H, Dh, d, V, K = w["B"], w["H"], w["Dh"], w["d"], w["V"], w["K"]
         T = tree.T
+        self.tc_splits = None
+        if isinstance(attn_splits, str) and attn_splits.startswith("tc"):
+            if attn_splits[2:]:
+                self.tc_splits = int(attn_splits[2:])
+            else:
+                sms = torch.cuda.get_device_properties(device).multi_processor_count if torch.cuda.is_available() else 152
+                ctas = B * H * -(-T // 128)
+                tiles = -(-(max_prefix + T) // 128)
+                self.tc_splits = next(c for c in (8, 4, 2, 1) if c == 1 or (c * ctas <= sms and c <= tiles))
+            if self.tc_splits not in (1, 2, 4, 8):
+                raise ValueError(f"attn_splits {attn_splits!r}")
+            attn_splits = "tc"
+        self.attn_order, self.attn_splits = attn_order, attn_splits
         self.B, self.T = B, T
         dt = TORCH_DT[w["dtype"]]
         self.w_lm, self.w1, self.b1, self.w2 = weights["w_lm"], weights["w1"], weights.get("b1"), weights["w2"]
@@ -162,14 +175,7 @@ class VerifyStep:
             side.wait_stream(main)
 
         def attention():
-            if self.attn_splits == "tc":
-                M.medusa_tree_attn_tc(x["q"], x["k_new"], x["v_new"], x["k_cache"], x["v_cache"], x["seq_start"],
-                                      x["prefix_len"], x["seq_cap"], self.tree, self.max_prefix, self.rope_theta,
-                                      self.scale, self.out, self.err, side)
-            else:
-                M.medusa_tree_attn(x["q"], x["k_new"], x["v_new"], x["k_cache"], x["v_cache"], x["seq_start"],
-                                   x["prefix_len"], x["seq_cap"], self.tree, self.max_prefix, self.rope_theta,
-                                   self.scale, self.out, self.ws_attn, self.err, side, key_splits=self.attn_splits)
+            self.attention(x, side)
 
         if self.attn_order == "first":
             attention()
@@ -231,6 +237,17 @@ class VerifyStep:
             compaction()
         if side is not main:
             main.wait_stream(side)
+
+    def attention(self, x: dict, stream):
+        """The step's tree attention (box step 1) on `stream`."""
+        if self.attn_splits == "tc":
+            M.medusa_tree_attn_tc(x["q"], x["k_new"], x["v_new"], x["k_cache"], x["v_cache"], x["seq_start"],
+                                  x["prefix_len"], x["seq_cap"], self.tree, self.max_prefix, self.rope_theta,
+                                  self.scale, self.out, self.err, stream, key_splits=self.tc_splits)
+        else:
+            M.medusa_tree_attn(x["q"], x["k_new"], x["v_new"], x["k_cache"], x["v_cache"], x["seq_start"],
+                               x["prefix_len"], x["seq_cap"], self.tree, self.max_prefix, self.rope_theta,
+                               self.scale, self.out, self.ws_attn, self.err, stream, key_splits=self.attn_splits)
 
     @property
     def launches_per_step(self) -> int:

@@ -181,6 +181,14 @@ def test_validation_statuses(M):
                                          0.1, 1, FAKE, FAKE, 1 << 30, ks, None, None) == -2
     assert L.medusa_tree_attn_splits(FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, ref, 1, 4, 64, 64, 1e4,
                                      0.1, 0, FAKE, FAKE, 1 << 30, 1, None, None) == -2
+    # tensor-core attention: key splits outside {1, 2, 4, 8}, Dh other than 128, f32
+    def tc(dh, dt, ks):
+        return L.medusa_tree_attn_tc(FAKE, FAKE, FAKE, FAKE, FAKE, 1 << 20, FAKE, FAKE, FAKE, ref, 1, 4, dh, 64,
+                                     1e4, 0.1, dt, FAKE, ks, None, None)
+    for ks in (0, 3, 16, -1):
+        assert tc(128, 1, ks) == -2
+    assert tc(64, 1, 1) == -2
+    assert tc(128, 0, 1) == -2
     # LM head: d not a multiple of 64 for bf16; misaligned pointers
     assert L.medusa_lm_head_verify(FAKE, FAKE, FAKE, 15, 100, 1000, 1, 0, None, 0, None, None) == -2
     assert L.medusa_lm_head_verify(FAKE + 2, FAKE, FAKE, 15, 256, 1000, 1, 0, None, 0, None, None) == -1

@@ -106,16 +106,18 @@ def test_tree_attn_key_splits(M, case, key_splits):
 
 
 # the tensor-core path (bf16, Dh 128): one, several and 512 tree rows, ragged
-# prefixes across sequences, an empty prefix
+# prefixes across sequences, an empty prefix; 1 to 8 CTAs per head's keys
+# (with 8, some CTAs of a short sequence get no key tile at all)
 TC_CASES = [c for c in ATTN_CASES if c[0] == "bf16" and c[2] == 128] + [
     ("bf16", 1, 128, [70], ("cartesian", (8, 8, 8), 511)),
     ("bf16", 2, 128, [127, 128, 129], ("cartesian", (2, 2, 2), None)),
 ]
 
 
+@pytest.mark.parametrize("key_splits", [1, 2, 4, 8])
 @pytest.mark.parametrize("case", TC_CASES, ids=lambda c: f"{c[0]}-H{c[1]}-Dh{c[2]}-L{c[3]}-{c[4][0]}")
-def test_tree_attn_tc(M, case):
-    _check_tree_attn(M, case, "tc")
+def test_tree_attn_tc(M, case, key_splits):
+    _check_tree_attn(M, case, f"tc{key_splits}")
 
 
 def _check_tree_attn(M, case, key_splits):
@@ -128,9 +130,11 @@ def _check_tree_attn(M, case, key_splits):
     out_d = to_dev(np.zeros_like(q))
     ws = torch.empty(M.medusa_tree_attn_workspace_size(B, H, Dh, T, max(L)), dtype=torch.uint8, device="cuda")
     e = err_flag()
-    if key_splits == "tc":
-        M.medusa_tree_attn_tc(to_dev(q), to_dev(kn), to_dev(vn), kc_d, vc_d, to_dev(st), to_dev(pl), to_dev(cap),
-                              dtree, max(L), 10000.0, scale, out_d, e)
+    if isinstance(key_splits, str):  # "tcN": the tensor-core path with N CTAs per head's keys
+        ns = int(key_splits[2:])
+        for _ in range(2):  # repeated calls append the same tree rows and give the same output
+            M.medusa_tree_attn_tc(to_dev(q), to_dev(kn), to_dev(vn), kc_d, vc_d, to_dev(st), to_dev(pl),
+                                  to_dev(cap), dtree, max(L), 10000.0, scale, out_d, e, key_splits=ns)
     else:
         M.medusa_tree_attn(to_dev(q), to_dev(kn), to_dev(vn), kc_d, vc_d, to_dev(st), to_dev(pl), to_dev(cap),
                            dtree, max(L), 10000.0, scale, out_d, ws, e, key_splits=key_splits)
