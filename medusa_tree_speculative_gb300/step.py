@@ -64,12 +64,13 @@ class VerifyStep:
         # heads' kernels), with the library's default key split (None), 1, 2,
         # 4, 8 CTAs per head, or "tc" (medusa_tree_attn_tc: bf16, Dh 128;
         # "tc1" .. "tc8" name its key split, "tc" takes the largest that keeps
-        # the grid within one CTA per SM); "auto": 4 for bf16, the fastest
-        # measured beside the LM head at the 7B shape
+        # the grid within one CTA per SM); "auto": "tc1" for bf16 with Dh 128
+        # (one CTA per head: the fewest SMs taken from the LM head it runs
+        # beside, the fastest step measured at the 7B shape), else 4 for bf16
         if attn_order not in ("first", "after_lm", "after_accept", "after_heads"):
             raise ValueError(f"attn_order {attn_order!r}")
         if attn_splits == "auto":
-            attn_splits = 4 if w["dtype"] == "bf16" else None
+            attn_splits = ("tc1" if w["Dh"] == 128 else 4) if w["dtype"] == "bf16" else None
         B, H, Dh, d, V, K = w["B"], w["H"], w["Dh"], w["d"], w["V"], w["K"]
         T = tree.T
         self.tc_splits = None
