@@ -22,6 +22,13 @@ WORKLOADS = {
         tree=("cartesian", (2, 2, 2), None), mode="greedy",
         w1_std=0.02, lm_std="inv_sqrt_d", w2="lm_plus_noise", w2_noise_std=0.01,
     ),
+    # Tiny bf16 step on the tensor-core paths (Dh 128; 300 prefix + 15 tree keys
+    # give the attention a ragged third key tile, V = 2048 sixteen vocabulary tiles).
+    "tiny_bf16": dict(
+        dtype="bf16", d=256, V=2048, H=2, Dh=128, B=1, L=(300,), K=3,
+        tree=("cartesian", (2, 2, 2), None), mode="greedy",
+        w1_std="inv_sqrt_d", lm_std="inv_sqrt_d", w2="independent",
+    ),
     # Vicuna-7B-shaped single-sequence step (the headline).
     "vicuna7b_L1024_tree64": dict(
         dtype="bf16", d=4096, V=32000, H=32, Dh=128, B=1, L=(1024,), K=4,

@@ -2,6 +2,8 @@
 times), checked against the oracle.
 
 tiny_fp32: every output compared in full.
+tiny_bf16: the tensor-core paths (attention, LM head) at a small size, every
+head and vocabulary row compared.
 vicuna7b_L1024_tree64 (the benchmark's workload, full size): attention on
 sampled heads, LM-head logits on sampled vocabulary rows plus the planted
 path's parent rows in full, acceptance against the planted path plus validity
@@ -91,14 +93,26 @@ def test_step_tiny_fp32_full(M, heads):
 
 
 @pytest.mark.parametrize("heads", ["fused", "split", "joint"])
+def test_step_tiny_bf16_full(M, heads):
+    _check_bf16_step(M, "tiny_bf16", heads, head_list=(0, 1), n_cols=None)
+
+
+@pytest.mark.parametrize("heads", ["fused", "split", "joint"])
 def test_step_vicuna7b_sampled(M, heads):
+    _check_bf16_step(M, "vicuna7b_L1024_tree64", heads, head_list=(0, 17, 31), n_cols=512)
+
+
+def _check_bf16_step(M, name, heads, head_list, n_cols):
+    """A bf16 step in the default launch configuration: attention on `head_list`,
+    logits on the path's parent rows in full and on n_cols sampled vocabulary rows
+    (None: every row), acceptance, compaction, heads and candidates."""
     w, ot, wts, x, tok, st, dev, node, path, lg_par, parents, gaps = _run(
-        M, "vicuna7b_L1024_tree64", lambda ot: int(np.nonzero(ot.depth == 3)[0][4]), heads=heads)
+        M, name, lambda ot: int(np.nonzero(ot.depth == 3)[0][4]), heads=heads)
     assert int(st.err.item()) == 0
     T, V, H, Dh = ot.T, w["V"], w["H"], w["Dh"]
-    # --- attention on three heads (oracle on single-head slices)
+    # --- attention (oracle on single-head slices)
     out = as_double(to_host(st.out))
-    for h in (0, 17, 31):
+    for h in head_list:
         sl = lambda a: np.ascontiguousarray(a[..., h:h + 1, :])
         kc, vc = sl(x["k_cache"]), sl(x["v_cache"])
         _, ref = oracle.tree_attn(sl(x["q"]), sl(x["k_new"]), sl(x["v_new"]), kc, vc, x["seq_start"],
@@ -108,7 +122,7 @@ def test_step_vicuna7b_sampled(M, heads):
     logits = to_host(st.logits)[0]
     for i, p in enumerate(parents):
         assert np.abs(logits[p] - lg_par[i]).max() <= 2e-2 * np.abs(lg_par[i]).max()
-    cols = np.random.default_rng(0).choice(V, 512, replace=False)
+    cols = np.arange(V) if n_cols is None else np.random.default_rng(0).choice(V, n_cols, replace=False)
     ref = oracle.lm_head(x["hidden"][0], np.ascontiguousarray(wts["w_lm"][cols]))
     assert np.abs(logits[:, cols] - ref).max() <= 2e-2 * np.abs(ref).max()
     # --- acceptance: the planted path (decisions there are clear of rounding)
