@@ -330,7 +330,7 @@ int medusa_accept(const float* logits, const int32_t* tokens,
  * Arguments, outputs and errors are those of medusa_accept, without the
  * workspace.  Its scratch is one file-scope __device__ array, zero when the
  * library loads, of 256 bytes of counters and MEDUSA_ACCEPT_NOALLOC_MAX_ROWS
- * row records of 16 bytes (128 KiB), which every GPU that loads the library
+ * row records of 64 bytes (512 KiB), which every GPU that loads the library
  * holds until the process exits.
  *   - The first call on each device looks up the array's device address
  *     (cudaGetSymbolAddress, with that device current) and caches it; make

@@ -9,13 +9,16 @@
 // code", typical acceptance).  Explainer "085 | Medusa", section 二.3: a
 // rejected token ends the accepted prefix.
 //
-// One kernel, one 1024-thread CTA per tree row (eight 16-byte loads in flight
-// per thread, so a 32K-wide row arrives in one round of loads): argmax of the
-// row and, for typical acceptance, the row's log-sum-exp and entropy at the
-// given temperature.  The last CTA of a sequence to finish its row (a counter
-// in the workspace) then makes the sequence's decisions, one thread per node:
-// per-node acceptance, the accepted-prefix chain level by level, and the best
-// node (select_body).
+// One kernel, two 512-thread CTAs per tree row, one per half of the
+// vocabulary (eight 16-byte loads in flight per thread, so a 32K-wide row
+// arrives in one round of loads): argmax of the half and, for typical
+// acceptance, its running softmax (max, sum, entropy term) at the given
+// temperature.  The last CTA of a sequence to finish (a counter in the
+// workspace) merges each row's halves into its argmax, log-sum-exp and
+// entropy and makes the sequence's decisions, one thread per node: per-node
+// acceptance, the accepted-prefix chain level by level, and the best node
+// (select_body).  The nodes' depth, parent and token are loaded before the
+// row pass, so the decisions start without waiting on global memory.
 #include <math.h>
 
 #include <mutex>
@@ -51,13 +54,37 @@ __device__ __forceinline__ Soft soft_merge(Soft x, Soft y) {
   return r;
 }
 
-constexpr int kRowThreads = 1024;
-constexpr int kRowLoads = 8;  // 16-byte loads in flight per thread: 128 KB per CTA, a 32K-wide row at once
+// One half row's record: its argmax (index, value) and running softmax.
+struct HalfStat {
+  int idx;
+  float val;
+  float m, S, A;
+  float pad[3];
+};
+
+constexpr int kRowSplit = 2;     // CTAs per row
+constexpr int kRowThreads = 512;  // >= MEDUSA_MAX_T: the last CTA gives every node a thread
+constexpr int kRowLoads = 8;     // 16-byte loads in flight per thread: 64 KB per CTA, half a 32K-wide row at once
+static_assert(kRowThreads >= MEDUSA_MAX_T, "one thread per node in the decisions");
 
 // Barrier 1 over the first n threads of the block (n a multiple of 32).
 MDEV void sel_sync(int n) { asm volatile("bar.sync 1, %0;\n" ::"r"(n) : "memory"); }
 
-MDEV void select_body(int b, const float* logits, const int32_t* tokens, const medusa_tree_t& tree, int V,
+// A node's tree row and token, loaded before they are needed.
+struct NodeIn {
+  int depth, parent, token;
+};
+MDEV NodeIn load_node(const medusa_tree_t& tree, const int32_t* tokens, int b, int c) {
+  NodeIn n{0, -1, 0};
+  if (c < tree.T) {
+    n.depth = __ldg(tree.depth + c);
+    n.parent = __ldg(tree.parent + c);
+    n.token = __ldg(tokens + (int64_t)b * tree.T + c);
+  }
+  return n;
+}
+
+MDEV void select_body(int b, const float* logits, NodeIn node, const medusa_tree_t& tree, int V,
                       int mode, float inv_temp, float eps, float delta, const RowStat* st, int32_t* accept_len,
                       int32_t* accepted_nodes, int32_t* next_root, int32_t* best_node, float* best_logp,
                       int32_t* err, int nthreads);
@@ -69,7 +96,7 @@ struct AcceptArgs {
   medusa_tree_t tree;
   int V, mode;
   float inv_temp, eps, delta;
-  RowStat* stats;  // [B][T] row records
+  HalfStat* stats;  // [B][T][kRowSplit] half-row records
   int* counters;   // [B] rows finished per sequence; zero on entry, left zero
   int32_t *accept_len, *accepted_nodes, *next_root, *best_node;
   float* best_logp;
@@ -78,12 +105,12 @@ struct AcceptArgs {
 
 template <bool TYPICAL>
 __global__ void __launch_bounds__(kRowThreads) accept_rowstat_kernel(const __grid_constant__ AcceptArgs a) {
-  const float* logits = a.logits;
   const int T = a.tree.T, V = a.V;
   const float inv_temp = a.inv_temp;
-  RowStat* stats = a.stats;
-  const int p = blockIdx.x, b = blockIdx.y;
-  const float* z = logits + ((int64_t)b * T + p) * V;
+  const int p = blockIdx.x / kRowSplit, half = blockIdx.x % kRowSplit, b = blockIdx.y;
+  // the node this thread would decide for, were this CTA the sequence's last
+  const NodeIn node = load_node(a.tree, a.tokens, b, threadIdx.x);
+  const float* z = a.logits + ((int64_t)b * T + p) * V;
   float bv = -INFINITY;
   int bi = 0x7fffffff;
   Soft sf{-INFINITY, 0.f, 0.f};
@@ -105,18 +132,18 @@ __global__ void __launch_bounds__(kRowThreads) accept_rowstat_kernel(const __gri
   };
   if ((V & 3) == 0) {
     const float4* z4 = reinterpret_cast<const float4*>(z);
-    const int n4 = V >> 2;
-    for (int i = threadIdx.x; i < n4; i += kRowLoads * kRowThreads) {
+    const int n4 = V >> 2, lo = (int)((int64_t)n4 * half / kRowSplit), hi = (int)((int64_t)n4 * (half + 1) / kRowSplit);
+    for (int i = lo + threadIdx.x; i < hi; i += kRowLoads * kRowThreads) {
       float4 r[kRowLoads];
 #pragma unroll
       for (int u = 0; u < kRowLoads; ++u) {
         const int ii = i + u * kRowThreads;
-        if (ii < n4) r[u] = __ldg(z4 + ii);
+        if (ii < hi) r[u] = __ldg(z4 + ii);
       }
 #pragma unroll
       for (int u = 0; u < kRowLoads; ++u) {
         const int ii = i + u * kRowThreads;
-        if (ii < n4) {
+        if (ii < hi) {
           consume(r[u].x, 4 * ii);
           consume(r[u].y, 4 * ii + 1);
           consume(r[u].z, 4 * ii + 2);
@@ -125,7 +152,8 @@ __global__ void __launch_bounds__(kRowThreads) accept_rowstat_kernel(const __gri
       }
     }
   } else {
-    for (int v = threadIdx.x; v < V; v += kRowThreads) consume(z[v], v);
+    const int lo = (int)((int64_t)V * half / kRowSplit), hi = (int)((int64_t)V * (half + 1) / kRowSplit);
+    for (int v = lo + threadIdx.x; v < hi; v += kRowThreads) consume(z[v], v);
   }
   constexpr int NW = kRowThreads / 32;
   __shared__ float sv[NW], sS[NW], sA[NW], sm[NW];
@@ -143,11 +171,11 @@ __global__ void __launch_bounds__(kRowThreads) accept_rowstat_kernel(const __gri
   if (lane == 0) { sv[warp] = bv; si[warp] = bi; sm[warp] = sf.m; sS[warp] = sf.S; sA[warp] = sf.A; }
   __syncthreads();
   if (warp == 0) {
-    bv = sv[lane];
-    bi = si[lane];
+    bv = lane < NW ? sv[lane] : -INFINITY;
+    bi = lane < NW ? si[lane] : 0x7fffffff;
     warp_argmax(bv, bi);
     if (TYPICAL) {
-      sf = Soft{sm[lane], sS[lane], sA[lane]};
+      sf = lane < NW ? Soft{sm[lane], sS[lane], sA[lane]} : Soft{-INFINITY, 0.f, 0.f};
 #pragma unroll
       for (int o = 16; o > 0; o >>= 1) {
         Soft y{__shfl_xor_sync(0xffffffffu, sf.m, o), __shfl_xor_sync(0xffffffffu, sf.S, o),
@@ -156,22 +184,18 @@ __global__ void __launch_bounds__(kRowThreads) accept_rowstat_kernel(const __gri
       }
     }
     if (lane == 0) {
-      RowStat r;
-      r.argmax = bi;
-      // H = log S - A / S  (p^_v = e^(z_v - m) / S)
-      r.lse = TYPICAL ? sf.m + logf(sf.S) : 0.f;
-      r.entropy = TYPICAL ? logf(sf.S) - sf.A / sf.S : 0.f;
-      r.pad = 0.f;
-      stats[(int64_t)b * T + p] = r;
+      float4* rec = reinterpret_cast<float4*>(a.stats + ((int64_t)b * T + p) * kRowSplit + half);
+      rec[0] = make_float4(__int_as_float(bi), bv, sf.m, sf.S);
+      rec[1] = make_float4(sf.A, 0.f, 0.f, 0.f);
     }
   }
-  // the last row of the sequence to finish makes its decisions
+  // the last CTA of the sequence to finish makes its decisions
   __shared__ bool s_last;
   __shared__ RowStat rs[MEDUSA_MAX_T];
   __syncthreads();
   if (threadIdx.x == 0) {
     __threadfence();
-    s_last = atomicAdd(a.counters + b, 1) == T - 1;
+    s_last = atomicAdd(a.counters + b, 1) == kRowSplit * T - 1;
   }
   __syncthreads();
   if (!s_last) return;
@@ -182,20 +206,33 @@ __global__ void __launch_bounds__(kRowThreads) accept_rowstat_kernel(const __gri
   __threadfence();
   const int c = threadIdx.x;
   if (c < T) {
-    const int4 x = __ldcg(reinterpret_cast<const int4*>(stats + (int64_t)b * T + c));
-    rs[c] = RowStat{x.x, __int_as_float(x.y), __int_as_float(x.z), 0.f};
+    // the row's halves: argmax (value, then lower index), softmax merged
+    const float4* rec = reinterpret_cast<const float4*>(a.stats + ((int64_t)b * T + c) * kRowSplit);
+    int ri = 0x7fffffff;
+    float rv = -INFINITY;
+    Soft rsf{-INFINITY, 0.f, 0.f};
+#pragma unroll
+    for (int h = 0; h < kRowSplit; ++h) {
+      const float4 x0 = __ldcg(rec + 2 * h), x1 = __ldcg(rec + 2 * h + 1);
+      const int xi = __float_as_int(x0.x);
+      if (ranks_before(x0.y, xi, rv, ri)) { rv = x0.y; ri = xi; }
+      if (TYPICAL) rsf = soft_merge(rsf, Soft{x0.z, x0.w, x1.x});
+    }
+    // H = log S - A / S  (p^_v = e^(z_v - m) / S)
+    rs[c] = RowStat{ri, TYPICAL ? rsf.m + logf(rsf.S) : 0.f, TYPICAL ? logf(rsf.S) - rsf.A / rsf.S : 0.f, 0.f};
   }
   sel_sync(nthr);
-  select_body(b, a.logits, a.tokens, a.tree, V, a.mode, inv_temp, a.eps, a.delta, rs, a.accept_len,
+  select_body(b, a.logits, node, a.tree, V, a.mode, inv_temp, a.eps, a.delta, rs, a.accept_len,
               a.accepted_nodes, a.next_root, a.best_node, a.best_logp, a.err, nthr);
   if (threadIdx.x == 0) a.counters[b] = 0;  // every row of the sequence has arrived
 }
 
 // Sequence b's decisions from its rows' statistics `st` ([T], global or
-// shared memory); one thread per node: threads 0 .. nthreads-1 of the block
+// shared memory) and each thread's node (loaded by the caller); one thread
+// per node: threads 0 .. nthreads-1 of the block
 // take part (nthreads >= T, a multiple of 32; the block's other warps may
 // have exited), synchronised on barrier 1.
-MDEV void select_body(int b, const float* logits, const int32_t* tokens, const medusa_tree_t& tree, int V,
+MDEV void select_body(int b, const float* logits, NodeIn node, const medusa_tree_t& tree, int V,
                       int mode, float inv_temp, float eps, float delta, const RowStat* st, int32_t* accept_len,
                       int32_t* accepted_nodes, int32_t* next_root, int32_t* best_node, float* best_logp,
                       int32_t* err, int nthreads) {
@@ -214,8 +251,8 @@ MDEV void select_body(int b, const float* logits, const int32_t* tokens, const m
   bool pass = false;
   float lpc = 0.f;
   if (c < T) {
-    depth_c = tree.depth[c];
-    parent_c = tree.parent[c];
+    depth_c = node.depth;
+    parent_c = node.parent;
     amax[c] = st[c].argmax;
     if (c == 0) {
       pass = true;
@@ -226,7 +263,7 @@ MDEV void select_body(int b, const float* logits, const int32_t* tokens, const m
       parent_c = 0;
       depth_c = 0;
     } else {
-      const int tok = tokens[(int64_t)b * T + c];
+      const int tok = node.token;
       const RowStat rp = st[parent_c];
       if (mode == 0) {
         pass = tok == rp.argmax;
@@ -309,6 +346,7 @@ __global__ void __launch_bounds__(kStatThreads) accept_stats_kernel(
     medusa_tree_t tree, int V, int mode, float inv_temp, float eps, float delta, int32_t* accept_len,
     int32_t* accepted_nodes, int32_t* next_root, int32_t* best_node, float* best_logp, int32_t* err) {
   const int b = blockIdx.x, tid = threadIdx.x, T = tree.T;
+  const NodeIn node = load_node(tree, tokens, b, tid);
   __shared__ RowStat rs[MEDUSA_MAX_T];
   __shared__ float4 share[kStatThreads];
   const int P = max(1, kStatThreads / T);  // threads per row
@@ -335,21 +373,21 @@ __global__ void __launch_bounds__(kStatThreads) accept_stats_kernel(
     rs[r] = o;
   }
   __syncthreads();
-  select_body(b, logits, tokens, tree, V, mode, inv_temp, eps, delta, rs, accept_len, accepted_nodes, next_root,
+  select_body(b, logits, node, tree, V, mode, inv_temp, eps, delta, rs, accept_len, accepted_nodes, next_root,
               best_node, best_logp, err, blockDim.x);
 }
 
 // Workspace: per-sequence counters (256 bytes, at a fixed place so that
-// calls of any size find them zero), then one row record per (sequence, tree
-// row).
+// calls of any size find them zero), then two half-row records of 32 bytes
+// per (sequence, tree row).
 constexpr size_t kCounterBytes = 256;
 static_assert(MEDUSA_MAX_B * sizeof(int) <= kCounterBytes, "counters");
 
-// Scratch of medusa_accept_noalloc: the counters and one row record per
-// (sequence, tree row) at the library's maximum sizes, 256 bytes + 16 x 512
-// x 16 bytes = 128 KiB per device, zero when the library loads.
+// Scratch of medusa_accept_noalloc: the counters and the half-row records
+// of every (sequence, tree row) at the library's maximum sizes, 256 bytes +
+// 16 x 512 x 64 bytes = 512 KiB per device, zero when the library loads.
 constexpr int kNoAllocRows = MEDUSA_ACCEPT_NOALLOC_MAX_ROWS;
-constexpr size_t kNoAllocBytes = kCounterBytes + sizeof(RowStat) * (size_t)kNoAllocRows;
+constexpr size_t kNoAllocBytes = kCounterBytes + sizeof(HalfStat) * kRowSplit * (size_t)kNoAllocRows;
 static __device__ __align__(256) uint8_t g_accept_scratch[kNoAllocBytes];
 
 std::mutex g_noalloc_mu;
@@ -382,7 +420,7 @@ using namespace medusa;
 
 extern "C" size_t medusa_accept_workspace_size(int B, int T) {
   if (B < 1 || T < 1) return 0;
-  return kCounterBytes + align_up((size_t)B * T * sizeof(RowStat), 256);
+  return kCounterBytes + align_up((size_t)B * T * kRowSplit * sizeof(HalfStat), 256);
 }
 
 extern "C" int medusa_accept(const float* logits, const int32_t* tokens, const medusa_tree_t* tree,
@@ -408,10 +446,10 @@ extern "C" int medusa_accept(const float* logits, const int32_t* tokens, const m
   a.inv_temp = mode == 1 ? 1.f / temperature : 1.f;
   a.eps = eps; a.delta = delta;
   a.counters = static_cast<int*>(workspace);
-  a.stats = reinterpret_cast<RowStat*>(static_cast<uint8_t*>(workspace) + kCounterBytes);
+  a.stats = reinterpret_cast<HalfStat*>(static_cast<uint8_t*>(workspace) + kCounterBytes);
   a.accept_len = accept_len; a.accepted_nodes = accepted_nodes; a.next_root = next_root;
   a.best_node = best_node; a.best_logp = best_logp; a.err = err;
-  dim3 g(tree->T, B);
+  dim3 g(tree->T * kRowSplit, B);
   if (mode == 1)
     launch_kernel(accept_rowstat_kernel<true>, g, dim3(kRowThreads), 0, s, a);
   else
