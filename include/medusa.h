@@ -37,8 +37,8 @@
  *     Its contents are not preserved.  Calls whose kernels hand out work or
  *     elect a last CTA through counters kept in it (medusa_accept,
  *     medusa_heads_topk, medusa_heads_logits_topk) need it zero-filled before
- *     the first call and leave the counters zero again; the others need no
- *     initialisation.
+ *     the first call and leave it ready for the next call of the same entry
+ *     point; the others need no initialisation.
  *   - Device-side data errors (a token or node index out of range, a prefix
  *     that overflows its sequence's capacity) cannot be seen by the host
  *     without a synchronisation.  Calls that read such data take `err`, a

@@ -16,10 +16,10 @@
 //             the halves meet in shared memory for the epilogue.
 //   w2_topk   head_logits[b][k] = W2_k u[b][k] (fp32), fused with top-s: a
 //             fixed set of CTAs serves each head; after its warps have
-//             streamed their rows a CTA selects their top S from the logits it
-//             just wrote (per-thread sorted lists merged warp by warp), and
-//             the last CTA of a head to finish merges every CTA's list into
-//             topk (value descending, index ascending).
+//             streamed their rows a CTA merges the running top-S lists its
+//             warps kept while streaming (one per warp and sequence, in shared
+//             memory), and the last CTA of a head to finish merges every
+//             CTA's list into topk (value descending, index ascending).
 // Rows are handed out at run time, not split up front: W1's row quads and
 // each head's W2 rows come from atomic counters, the next one requested
 // before the current one is streamed.  CTAs whose SMs are busy with other
@@ -39,7 +39,7 @@ namespace {
 constexpr int kWarps = 8;  // 256-thread CTAs
 constexpr int UNROLL = 8;  // 16-byte loads in flight per lane
 constexpr int kMaxS = MEDUSA_MAX_S;
-constexpr int kMaxGroups = 128;  // W2 row groups one CTA may take (recorded for its top-s)
+constexpr int kMaxGroups = 128;  // W2 row groups per CTA above which a group grows (w2_row_group)
 
 struct HeadsArgs {
   const void* w1;      // [K][d][d]
@@ -128,7 +128,7 @@ __global__ void __launch_bounds__(kWarps * 32) heads_w1_kernel(const __grid_cons
   if (blockIdx.x == 0 && threadIdx.x < a.nused) {  // for w2_topk
     a.counters[threadIdx.x] = 0;
     a.rowctr[threadIdx.x] = 0;
-    if (threadIdx.x == 0) *a.tickets = *a.exited = 0;
+    if (threadIdx.x == 0) *a.tickets = 0;  // W2's tickets: W2 leaves them counted when W1 runs first
     if (threadIdx.x == 0 && a.heads_done) *a.heads_done = 0;
   }
 
@@ -231,6 +231,21 @@ struct TopList {
   }
 };
 
+// Insert (x, xi) into a sorted list of S (value, index) pairs in shared
+// memory, kept by one thread.
+template <int S>
+MDEV void list_insert(float* v, int* i, float x, int xi) {
+  if (!ranks_before(x, xi, v[S - 1], i[S - 1])) return;
+  int t = S - 1;
+  while (t > 0 && ranks_before(x, xi, v[t - 1], i[t - 1])) {
+    v[t] = v[t - 1];
+    i[t] = i[t - 1];
+    --t;
+  }
+  v[t] = x;
+  i[t] = xi;
+}
+
 // Block-wide: the S best of all threads' lists, valid in warp 0.
 template <int S>
 MDEV void block_select(TopList<S>& L, float (*wv)[S], int (*wi)[S], float* ov, int* oi) {
@@ -259,7 +274,8 @@ __global__ void __launch_bounds__(kWarps * 32) heads_w2_topk_kernel(const __grid
   __shared__ float wv[32][S];
   __shared__ int wi[32][S];
   __shared__ bool last;
-  __shared__ int s_grp[kMaxGroups];  // row groups this CTA streamed
+  __shared__ float lv[kWarps][NB][S];  // per-warp running top S, per sequence
+  __shared__ int li[kWarps][NB][S];
   __shared__ int s_g[2];
   __shared__ int s_ticket;
   // the head this CTA serves goes by the order in which CTAs start, not by
@@ -287,22 +303,24 @@ __global__ void __launch_bounds__(kWarps * 32) heads_w2_topk_kernel(const __grid
   const TE* W = static_cast<const TE*>(a.w2) + (int64_t)k * a.V * a.d;
   const int nvec = a.d / Vec<TE>::N;
   // this head's rows in groups of GR = kWarps * RW (RW consecutive rows per
-  // warp) from its counter; a CTA stops taking groups at kMaxGroups (the host
-  // sizes RW so that the CTAs of the head can hold every group twice over),
-  // so every group is streamed and recorded exactly once
+  // warp) from its counter, every group streamed exactly once
   const int RW = a.rgroup, GR = kWarps * RW;
   const int ngroups = (a.V + GR - 1) / GR;
   int* ctr = a.rowctr + slot;
   if (threadIdx.x == 0) s_g[0] = atomicAdd(ctr, 1);
   if (blockIdx.x == 0 && threadIdx.x == 32 && a.w1ctr) *a.w1ctr = 0;  // this call's w1 is done
+  // each warp keeps the running top S of the rows it streams, one list per
+  // sequence in shared memory (lane b keeps sequence b's)
+#pragma unroll 1
+  for (int e = lane; e < NB * S; e += 32) {
+    lv[warp][e / S][e % S] = -INFINITY;
+    li[warp][e / S][e % S] = 0x7fffffff;
+  }
   __syncthreads();
-  int g = s_g[0], cnt = 0;
+  int g = s_g[0];
   for (int it = 0; g < ngroups; ++it) {
     int gn = ngroups;
-    if (threadIdx.x == 0 && cnt + 1 < kMaxGroups)
-      gn = atomicAdd(ctr, 1);  // the next group; waited for after this one's loads
-    if (threadIdx.x == 0) s_grp[cnt] = g;
-    ++cnt;
+    if (threadIdx.x == 0) gn = atomicAdd(ctr, 1);  // the next group; waited for after this one's loads
     const int jb = g * GR + warp * RW;
     const int je = min(a.V, jb + RW);
     for (int j = jb; j < je; ++j) {
@@ -318,32 +336,29 @@ __global__ void __launch_bounds__(kWarps * 32) heads_w2_topk_kernel(const __grid
         for (int b = 0; b < NB; ++b)
           if (b == lane) y = acc[b];
         a.logits[((int64_t)lane * a.K + k) * a.V + j] = y;
+        list_insert<S>(lv[warp][lane], li[warp][lane], y, j);
       }
     }
     if (threadIdx.x == 0) s_g[(it + 1) & 1] = gn;  // the other slot: read by all before the last barrier
     __syncthreads();
     g = s_g[(it + 1) & 1];
   }
-  __syncthreads();  // this CTA's logits are written (visible to the whole CTA)
+  __syncthreads();  // every warp's lists are complete
 
-  // this CTA's top S of its rows, per sequence, selected after the stream
-  for (int b = 0; b < a.B; ++b) {
-    const float* z = a.logits + ((int64_t)b * a.K + k) * a.V;
+  // this CTA's top S per sequence: one warp per sequence merges the warps' lists
+  for (int b = warp; b < a.B; b += kWarps) {
     TopList<S> L;
     L.init();
-    for (int e = threadIdx.x; e < cnt * GR; e += blockDim.x) {
-      const int j = s_grp[e / GR] * GR + e % GR;
-      if (j < a.V) L.insert(z[j], j);
-    }
+    for (int e = lane; e < kWarps * S; e += 32) L.insert(lv[e / S][b][e % S], li[e / S][b][e % S]);
     float ov[S];
     int oi[S];
-    block_select<S>(L, wv, wi, ov, oi);
-    if (threadIdx.x == 0) {
+    L.warp_select(ov, oi);
+    if (lane == 0) {
       const int64_t base = (((int64_t)slot * a.B + b) * a.cpc + part) * kMaxS;
 #pragma unroll
       for (int t = 0; t < S; ++t) { a.cand_v[base + t] = ov[t]; a.cand_i[base + t] = oi[t]; }
+      __threadfence();  // before the head's counter below
     }
-    __syncthreads();
   }
   // the last CTA of this head to arrive merges all its CTAs' candidates
   __syncthreads();
@@ -359,9 +374,23 @@ __global__ void __launch_bounds__(kWarps * 32) heads_w2_topk_kernel(const __grid
       const int64_t base = ((int64_t)slot * a.B + b) * a.cpc * kMaxS;
       TopList<S> L;
       L.init();
-      for (int e = threadIdx.x; e < a.cpc * S; e += blockDim.x) {
-        const int c = e / S, t = e % S;
-        L.insert(__ldcg(a.cand_v + base + (int64_t)c * kMaxS + t), __ldcg(a.cand_i + base + (int64_t)c * kMaxS + t));
+      // the CTAs' lists from L2: eight loads in flight per thread, then the inserts
+      for (int e0 = threadIdx.x; e0 < a.cpc * S; e0 += 8 * blockDim.x) {
+        float cv[8];
+        int ci[8];
+#pragma unroll
+        for (int u = 0; u < 8; ++u) {
+          const int e = e0 + u * blockDim.x;
+          cv[u] = -INFINITY;
+          ci[u] = 0x7fffffff;
+          if (e < a.cpc * S) {
+            const int64_t at = base + (int64_t)(e / S) * kMaxS + e % S;
+            cv[u] = __ldcg(a.cand_v + at);
+            ci[u] = __ldcg(a.cand_i + at);
+          }
+        }
+#pragma unroll
+        for (int u = 0; u < 8; ++u) L.insert(cv[u], ci[u]);
       }
       float ov[S];
       int oi[S];
@@ -409,8 +438,9 @@ __global__ void __launch_bounds__(kWarps * 32) heads_w2_topk_kernel(const __grid
       }
     }
   }
-  // the last CTA to leave (every CTA has drawn its ticket) resets the tickets
-  if (threadIdx.x == 0) {
+  // W2 on its own: the last CTA to leave (every CTA has drawn its ticket)
+  // resets the tickets (after W1, W1 resets them at the next call's start)
+  if (a.exited && threadIdx.x == 0) {
     __threadfence();
     if (atomicAdd(a.exited, 1) == (int)gridDim.x - 1) *a.tickets = *a.exited = 0;
   }
@@ -460,8 +490,8 @@ int launch_heads_b(const HeadsArgs& a, int smax_used, cudaStream_t s) {
   return launch_heads<TE, MEDUSA_MAX_B>(a, smax_used, s);
 }
 
-// W2 rows per warp in a group: the smallest count with which the CTAs serving
-// one head can record every group at half their capacity.
+// W2 rows per warp in a group: one, unless the head's CTAs would take more
+// than kMaxGroups / 2 groups each (fewer counter requests for huge V).
 int w2_row_group(int cpc, int V) {
   const int64_t cap = (int64_t)cpc * kWarps * (kMaxGroups / 2);
   return (int)std::max<int64_t>(1, (V + cap - 1) / cap);
@@ -547,7 +577,7 @@ int heads_topk_impl(const void* hidden, const int32_t* last_node, int T, const v
   a.rowctr = a.counters + MEDUSA_MAX_K;
   a.w1ctr = a.counters + 2 * MEDUSA_MAX_K;
   a.tickets = a.counters + 2 * MEDUSA_MAX_K + 2;
-  a.exited = a.counters + 2 * MEDUSA_MAX_K + 3;
+  a.exited = nullptr;  // W1 resets the tickets at the start of each call
   a.cpc = w2_ctas_per_head(a.nused, V);
   a.rgroup = w2_row_group(a.cpc, V);
   a.logits = head_logits; a.topk = topk; a.err = err;
