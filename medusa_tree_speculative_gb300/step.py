@@ -34,6 +34,16 @@ def host_to_torch(a: np.ndarray, dt: str) -> torch.Tensor:
     return t if dt == "f32" else t.to(torch.bfloat16)
 
 
+def tc_key_splits(B: int, H: int, T: int, max_prefix: int, sms: int) -> int:
+    """Key split for medusa_tree_attn_tc on its own: the largest of 8, 4, 2
+    that keeps the grid (splits x heads x sequences x 128-row blocks, one CTA
+    per SM) within one wave and gives every CTA at least one 128-key tile;
+    else 1."""
+    ctas = B * H * -(-T // 128)
+    tiles = -(-(max_prefix + T) // 128)
+    return next(c for c in (8, 4, 2, 1) if c == 1 or (c * ctas <= sms and c <= tiles))
+
+
 def build_tree(w: dict) -> M.HostTree:
     """The workload's candidate tree via the library's host helpers."""
     kind = w["tree"][0]
@@ -79,9 +89,7 @@ class VerifyStep:
                 self.tc_splits = int(attn_splits[2:])
             else:
                 sms = torch.cuda.get_device_properties(device).multi_processor_count if torch.cuda.is_available() else 152
-                ctas = B * H * -(-T // 128)
-                tiles = -(-(max_prefix + T) // 128)
-                self.tc_splits = next(c for c in (8, 4, 2, 1) if c == 1 or (c * ctas <= sms and c <= tiles))
+                self.tc_splits = tc_key_splits(B, H, T, max_prefix, sms)
             if self.tc_splits not in (1, 2, 4, 8):
                 raise ValueError(f"attn_splits {attn_splits!r}")
             attn_splits = "tc"

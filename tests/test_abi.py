@@ -248,3 +248,17 @@ def test_workspace_queries(M):
     assert M.medusa_lm_head_tiled_bytes(4096, 32000) == 32000 * 4096 * 2
     assert M.medusa_lm_head_tiled_bytes(256, 1000) == 1024 * 256 * 2  # last block padded to 128 rows
     assert M.medusa_lm_head_tiled_bytes(100, 1000) == 0
+
+
+def test_tc_key_splits(M):
+    """The tensor-core attention's default key split (host logic): one wave of
+    one-CTA-per-SM clusters, at least one key tile per CTA."""
+    from medusa_tree_speculative_gb300.step import tc_key_splits
+
+    assert tc_key_splits(1, 32, 65, 1024, 152) == 4    # 7B, one sequence: 128 CTAs
+    assert tc_key_splits(1, 40, 65, 2048, 152) == 2    # 13B: 40 heads
+    assert tc_key_splits(4, 52, 65, 8192, 152) == 1    # 33B, four sequences: 208 CTAs already
+    assert tc_key_splits(1, 2, 15, 300, 152) == 2      # 3 key tiles: 4 would leave a CTA none
+    assert tc_key_splits(1, 1, 15, 0, 152) == 1        # one key tile only
+    assert tc_key_splits(1, 32, 257, 4096, 152) == 1   # three row blocks: 96 CTAs
+    assert tc_key_splits(1, 16, 65, 1024, 152) == 8
