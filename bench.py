@@ -499,8 +499,17 @@ def measure_e2e(args, w, st, x, xh, prefix0, s, s2, s3, torch, M):
     d2h = st.results.numel() * st.results.element_size()
     steps = max(10, args.steps // 2)
 
+    # the attention's inputs (q, k_new, v_new) on the forked branch that runs
+    # the attention; the LM head's and the acceptance's (hidden, tokens,
+    # prefix_len) on the main stream, so that the LM head starts after its own
+    # inputs only; both by copy kernels reading the pinned buffer
+    split = offs["hidden"]
+
     def enqueue():
-        dev_buf.copy_(host_buf, non_blocking=True)
+        s2.wait_stream(s)
+        with torch.cuda.stream(s2):
+            M.medusa_copy_from_host(dev_buf[:split], host_buf[:split], s2)
+        M.medusa_copy_from_host(dev_buf[split:], host_buf[split:], s)
         st.run(xe, s, side_stream=s2, heads_stream=s3)
         host_res.copy_(st.results, non_blocking=True)
 
@@ -528,8 +537,9 @@ def measure_e2e(args, w, st, x, xh, prefix0, s, s2, s3, torch, M):
     dt = time.perf_counter() - t0
     return {"value": steps / dt, "unit": UNIT, "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h),
             "steps": steps,
-            "launch": "one CUDA graph per step: inputs (one pinned buffer) -> device, the six calls, the step's "
-                      "integer results -> pinned host; the host waits for every step"}
+            "launch": "one CUDA graph per step: inputs (one pinned buffer) -> device by medusa_copy_from_host (q, "
+                      "k_new, v_new on the attention's branch, the rest on the main stream), the six calls, the "
+                      "step's integer results -> pinned host; the host waits for every step"}
 
 
 # ------------------------------------------------------------- CPU oracle --

@@ -212,6 +212,16 @@ int medusa_tree_attn_tc(const void* q, const void* k_new, const void* v_new,
                         void* out, int key_splits, int32_t* err,
                         void* stream);
 
+/* Copy `bytes` from page-locked, device-mapped host memory (src_host, e.g.
+ * cudaHostAlloc) into device memory (dst) with a kernel of 16-byte loads,
+ * enqueued on `stream`: the step's inputs staged from host buffers.  Both
+ * pointers and `bytes` must be multiples of 16; the runtime is asked for the
+ * host buffer's device address first, and memory that is not mapped returns
+ * MEDUSA_ERR_INVALID without launching anything.  No counterpart in the
+ * pages: the end-to-end step's host-to-device leg. */
+int medusa_copy_from_host(void* dst, const void* src_host, size_t bytes,
+                          void* stream);
+
 /* Scratch bytes medusa_lm_head_verify needs (currently 0). */
 size_t medusa_lm_head_workspace_size(int rows, int d, int V);
 

@@ -49,6 +49,7 @@ _SIGS = {
     "medusa_tree_attn": (I, [P, P, P, P, P, P, P, P, TREE, I, I, I, I, F, F, I, P, P, SZ, P, P]),
     "medusa_tree_attn_splits": (I, [P, P, P, P, P, P, P, P, TREE, I, I, I, I, F, F, I, P, P, SZ, I, P, P]),
     "medusa_tree_attn_tc": (I, [P, P, P, P, P, C.c_int64, P, P, P, TREE, I, I, I, I, F, F, I, P, I, P, P]),
+    "medusa_copy_from_host": (I, [P, P, SZ, P]),
     "medusa_lm_head_workspace_size": (SZ, [I, I, I]),
     "medusa_lm_head_tiled_bytes": (SZ, [I, I]),
     "medusa_lm_head_tile": (I, [P, P, I, I, P]),
@@ -220,6 +221,15 @@ def medusa_tree_attn_tc(q, k_new, v_new, k_cache, v_cache, seq_start, prefix_len
                                     int(k_cache.shape[0]), _ptr(seq_start), _ptr(prefix_len), _ptr(seq_cap),
                                     tree.ref, B, H, Dh, max_prefix, rope_theta, scale, _dtype(q), _ptr(out),
                                     int(key_splits), _ptr(err), _stream(stream)), "medusa_tree_attn_tc")
+
+
+def medusa_copy_from_host(dst, src_host, stream=None):
+    """dst (device tensor) <- src_host (pinned CPU tensor of the same byte size) by a copy kernel."""
+    nb = src_host.numel() * src_host.element_size()
+    if dst.numel() * dst.element_size() != nb:
+        raise ValueError("medusa_copy_from_host: byte sizes differ")
+    _check(_lib.medusa_copy_from_host(_ptr(dst), C.c_void_p(src_host.data_ptr()), nb, _stream(stream)),
+           "medusa_copy_from_host")
 
 
 def medusa_tree_attn(q, k_new, v_new, k_cache, v_cache, seq_start, prefix_len, seq_cap,

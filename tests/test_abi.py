@@ -189,6 +189,13 @@ def test_validation_statuses(M):
         assert tc(128, 1, ks) == -2
     assert tc(64, 1, 1) == -2
     assert tc(128, 0, 1) == -2
+    # host-to-device staging copy: nothing to do, NULL, misaligned, memory that is not mapped pinned memory
+    assert L.medusa_copy_from_host(FAKE, FAKE, 0, None) == 0
+    assert L.medusa_copy_from_host(None, FAKE, 64, None) == -1
+    assert L.medusa_copy_from_host(FAKE, FAKE + 8, 64, None) == -1
+    assert L.medusa_copy_from_host(FAKE, FAKE, 40, None) == -1
+    buf = np.zeros(64, np.uint8)
+    assert L.medusa_copy_from_host(FAKE, buf.ctypes.data + (-buf.ctypes.data % 16), 32, None) == -1
     # LM head: d not a multiple of 64 for bf16; misaligned pointers
     assert L.medusa_lm_head_verify(FAKE, FAKE, FAKE, 15, 100, 1000, 1, 0, None, 0, None, None) == -2
     assert L.medusa_lm_head_verify(FAKE + 2, FAKE, FAKE, 15, 256, 1000, 1, 0, None, 0, None, None) == -1

@@ -664,3 +664,37 @@ def test_heads_topk_candidates(M, dt):
             assert int(e.item()) == 0
             assert torch.equal(hl[:, :ot.K], hl_ref[:, :ot.K]) and torch.equal(tk, tk_ref)
             assert np.array_equal(to_host(tok), oracle.build_candidates(root, to_host(tk), ot)), f"call {rep}"
+
+
+@pytest.mark.parametrize("nbytes", [16, 4096 + 48, 2130688, 8 << 20])
+def test_copy_from_host(M, nbytes):
+    """The staging copy moves pinned host bytes to the device exactly, inside a
+    CUDA graph too; unmapped host memory is refused without a launch."""
+    g = torch.Generator().manual_seed(nbytes)
+    src = torch.randint(0, 256, (nbytes,), dtype=torch.uint8, generator=g).pin_memory()
+    dst = torch.zeros(nbytes, dtype=torch.uint8, device="cuda")
+    M.medusa_copy_from_host(dst, src)
+    torch.cuda.synchronize()
+    assert torch.equal(dst.cpu(), src)
+    s = torch.cuda.Stream()
+    dst.zero_()
+    torch.cuda.synchronize()
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph, stream=s):
+        M.medusa_copy_from_host(dst, src, s)
+    src.add_(1)  # the replay reads the buffer as it is then
+    graph.replay()
+    torch.cuda.synchronize()
+    assert torch.equal(dst.cpu(), src)
+    # pageable memory: refused, unless the runtime maps it for the device (a
+    # host whose memory the GPU reads coherently), and then copied exactly
+    pageable = torch.arange(64, dtype=torch.uint8)
+    if pageable.data_ptr() % 16 == 0:
+        out = torch.zeros(64, dtype=torch.uint8, device="cuda")
+        try:
+            M.medusa_copy_from_host(out, pageable)
+        except RuntimeError:
+            pass
+        else:
+            torch.cuda.synchronize()
+            assert torch.equal(out.cpu(), pageable)
