@@ -15,18 +15,19 @@
 // is drawn from p (inverse CDF).  Lossless when a node's children are
 // independent draws from q_k.  The uniforms are inputs.
 //
-// A thread-block cluster of 8 CTAs (1024 threads each) per sequence, each
+// Two kernels.  The first computes, for every tree row's target logits and
+// every drafting head's logits at once (two 512-thread CTAs per row), the
+// softmax statistics (max, sum e^(y - max)) of y = logit / tau, so that the
+// walk tests a drafted token in O(1): p(x) = e^(y_x - m) / S.  The walk runs
+// on a thread-block cluster of 8 CTAs (1024 threads each) per sequence, each
 // CTA owning one eighth of the vocabulary, so that the V-wide passes run on
-// eight SMs; their maxima and sums are combined through distributed shared
-// memory.  At each node the kernel exponentiates every logit once: a pass of
-// maxima (the node's logits and the drafting head's), then a pass that
-// writes e^(z/tau - max) for both to two workspace rows and sums them, so p
-// and q are the rows times scalars.  A rejection is one pass that writes the
-// residual [p - q]_+ over the target row and sums it; the acceptance tests
-// read the rows (from L2: another CTA may own the token) and the final draw
-// takes per-warp segment sums in double, a prefix over the CTAs and the
-// segments, and a scan of one segment.  Every pass keeps 16 loads in flight
-// per thread.
+// eight SMs; their sums are combined through distributed shared memory.  A
+// rejection is one pass that writes the residual [p - q]_+ (p from the
+// logits and the statistics, or from the row an earlier rejection at the
+// node wrote) and sums it; the final draw writes p out first unless a
+// rejection there did, then takes per-warp segment sums in double, a prefix
+// over the CTAs and the segments, and a scan of one segment.  Every pass
+// keeps 16 loads in flight per thread.
 #include <math.h>
 
 #include "common.cuh"
@@ -140,74 +141,113 @@ struct ClusterRed {
 #define MEDUSA_ROUNDS(lo, hi) for (int base = (lo); base < (hi); base += kU * kThreads)
 #define MEDUSA_IDX(u) (base + (u) * kThreads + (int)threadIdx.x)
 
-// The node's target row Pw and the drafting head's row Qw (workspace, this
-// CTA's slice): p(v) = Pw[v] * sp, q(v) = Qw[v] * sq, written with
-// e^(y - max) of y = logit / tau once per node.  The maxima and sums are
-// cluster-wide.
-MDEV void exp_rows(const float* z, const float* dz, int lo, int hi, float inv_tau, float* Pw, float* Qw,
-                   float& sp, float& sq, ClusterRed& R) {
-  float mp = -INFINITY, mq = -INFINITY;
-  MEDUSA_ROUNDS(lo, hi) {
-    float a[kU], c[kU];
+// ---- row statistics, all rows at once (a separate kernel before the walk)
+// (max, sum e^(y - max)) of y = logit / tau for every tree row's target
+// logits and every drafting head's logits, two 512-thread CTAs per row (one
+// per half of the vocabulary), so that the walk tests a drafted token in
+// O(1): p(x) = e^(y_x - m) / S.
+constexpr int kStatThreads = 512;
+
+struct Soft2 {
+  float m, S;
+};
+MDEV Soft2 soft2_merge(Soft2 a, Soft2 b) {
+  if (a.m == -INFINITY) return b;
+  if (b.m == -INFINITY) return a;
+  const float M = fmaxf(a.m, b.m);
+  return Soft2{M, a.S * expf(a.m - M) + b.S * expf(b.m - M)};
+}
+
+__global__ void __launch_bounds__(kStatThreads) reject_stats_kernel(const float* logits, const float* draft, int T,
+                                                                    int Kd, int V, float inv_tau, float2* stats) {
+  const int row = blockIdx.x >> 1, half = blockIdx.x & 1, b = blockIdx.y;
+  const float* z = row < T ? logits + ((int64_t)b * T + row) * V : draft + ((int64_t)b * Kd + (row - T)) * V;
+  const int lo = (int)((int64_t)V * half / 2), hi = (int)((int64_t)V * (half + 1) / 2);
+  Soft2 t{-INFINITY, 0.f};
+  for (int v0 = lo + (int)threadIdx.x; v0 < hi; v0 += kU * kStatThreads) {
+    float y[kU];
 #pragma unroll
     for (int u = 0; u < kU; ++u) {
-      const int v = MEDUSA_IDX(u);
-      a[u] = v < hi ? z[v] : -INFINITY;
-      c[u] = (dz && v < hi) ? dz[v] : -INFINITY;
+      const int v = v0 + u * kStatThreads;
+      y[u] = v < hi ? __ldg(z + v) * inv_tau : -INFINITY;
     }
+    float m = t.m;
 #pragma unroll
-    for (int u = 0; u < kU; ++u) {
-      mp = fmaxf(mp, a[u] * inv_tau);
-      mq = fmaxf(mq, c[u] * inv_tau);
-    }
+    for (int u = 0; u < kU; ++u) m = fmaxf(m, y[u]);
+    float S = t.m == -INFINITY ? 0.f : t.S * expf(t.m - m);
+#pragma unroll
+    for (int u = 0; u < kU; ++u) S += y[u] == -INFINITY ? 0.f : expf(y[u] - m);
+    t = Soft2{m, S};
   }
-  R.pair<true>(mp, mq);
-  float Sp = 0.f, Sq = 0.f;
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1)
+    t = soft2_merge(t, Soft2{__shfl_xor_sync(0xffffffffu, t.m, o), __shfl_xor_sync(0xffffffffu, t.S, o)});
+  __shared__ float2 part[kStatThreads / 32];
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  if (lane == 0) part[warp] = make_float2(t.m, t.S);
+  __syncthreads();
+  if (warp == 0) {
+    t = lane < kStatThreads / 32 ? Soft2{part[lane].x, part[lane].y} : Soft2{-INFINITY, 0.f};
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1)
+      t = soft2_merge(t, Soft2{__shfl_xor_sync(0xffffffffu, t.m, o), __shfl_xor_sync(0xffffffffu, t.S, o)});
+    if (lane == 0) stats[((int64_t)b * (T + Kd) + row) * 2 + half] = make_float2(t.m, t.S);
+  }
+}
+
+// A row's (max, sum) from its two halves (the same bits in every CTA).
+MDEV Soft2 row_soft(const float2* stats, int64_t idx) {
+  const float2 a = __ldcg(stats + 2 * idx), c = __ldcg(stats + 2 * idx + 1);
+  return soft2_merge(Soft2{a.x, a.y}, Soft2{c.x, c.y});
+}
+
+// p <- e^(y - m) / S over this CTA's slice of Pw, unnormalised in the row
+// (Pw = e^(y - m)); returns the cluster-wide sum, so that p = Pw / sum.
+MDEV float materialize(const float* z, float inv_tau, float m, float* Pw, int lo, int hi, ClusterRed& R) {
+  float S = 0.f;
   MEDUSA_ROUNDS(lo, hi) {
-    float a[kU], c[kU];
+    float a[kU];
 #pragma unroll
     for (int u = 0; u < kU; ++u) {
       const int v = MEDUSA_IDX(u);
       a[u] = v < hi ? z[v] : 0.f;
-      c[u] = (dz && v < hi) ? dz[v] : 0.f;
     }
 #pragma unroll
     for (int u = 0; u < kU; ++u) {
       const int v = MEDUSA_IDX(u);
       if (v < hi) {
-        const float ep = expf(a[u] * inv_tau - mp);
-        Pw[v] = ep;
-        Sp += ep;
-        if (dz) {
-          const float eq = expf(c[u] * inv_tau - mq);
-          Qw[v] = eq;
-          Sq += eq;
-        }
+        const float e = expf(a[u] * inv_tau - m);
+        Pw[v] = e;
+        S += e;
       }
     }
   }
-  R.pair<false>(Sp, Sq);  // its cluster barrier also publishes the rows
-  sp = 1.f / Sp;
-  sq = dz ? 1.f / Sq : 0.f;
+  return R.sum(S);  // its cluster barrier also publishes the row
 }
 
-// p <- [p - q]_+ (unnormalised, over this CTA's slice of Pw); returns the
-// cluster-wide sum.
-MDEV float residual(float* Pw, const float* Qw, float sp, float sq, int lo, int hi, ClusterRed& R) {
+// p <- [p - q]_+ (unnormalised, over this CTA's slice of Pw); p(v) is
+// Pw[v] * sp once the row holds p (MAT), else e^(y_v - P.m) / P.S from the
+// node's logits; q(v) = e^(y'_v - Q.m) / Q.S from the drafting head's.
+// Returns the cluster-wide sum.
+template <bool MAT>
+MDEV float residual(const float* z, const float* dz, float inv_tau, Soft2 P, Soft2 Q, float* Pw, float sp, int lo,
+                    int hi, ClusterRed& R) {
+  const float ip = 1.f / P.S, iq = 1.f / Q.S;
   float S = 0.f;
   MEDUSA_ROUNDS(lo, hi) {
     float a[kU], c[kU];
 #pragma unroll
     for (int u = 0; u < kU; ++u) {
       const int v = MEDUSA_IDX(u);
-      a[u] = v < hi ? Pw[v] : 0.f;
-      c[u] = v < hi ? Qw[v] : 0.f;
+      a[u] = v < hi ? (MAT ? Pw[v] : z[v]) : 0.f;
+      c[u] = v < hi ? dz[v] : 0.f;
     }
 #pragma unroll
     for (int u = 0; u < kU; ++u) {
       const int v = MEDUSA_IDX(u);
       if (v < hi) {
-        const float r = fmaxf(0.f, a[u] * sp - c[u] * sq);
+        const float pv = MAT ? a[u] * sp : expf(a[u] * inv_tau - P.m) * ip;
+        const float r = fmaxf(0.f, pv - expf(c[u] * inv_tau - Q.m) * iq);
         Pw[v] = r;
         S += r;
       }
@@ -307,12 +347,11 @@ MDEV int draw(const float* Pw, float sp, int lo, int hi, double u, double* wsum,
 __global__ void __cluster_dims__(kCluster, 1, 1) __launch_bounds__(kThreads) reject_tree_kernel(
     const float* logits, const float* draft, int Kd, const int32_t* tokens, medusa_tree_t tree, int V,
     float inv_tau, const float* uni, int u_stride, int32_t* accept_len, int32_t* accepted_nodes,
-    int32_t* next_token, float* pws, int32_t* err) {
+    int32_t* next_token, float* pws, const float2* stats, int32_t* err) {
   const int crank = blockIdx.x, b = blockIdx.y, tid = threadIdx.x;  // gridDim.x == kCluster
   const int T = tree.T, K = tree.K;
   const int lo = (int)((int64_t)crank * V / kCluster), hi = (int)((int64_t)(crank + 1) * V / kCluster);
-  float* Pw = pws + (int64_t)b * 2 * V;  // target row (each CTA writes its slice)
-  float* Qw = Pw + V;                    // drafting head's row
+  float* Pw = pws + (int64_t)b * 2 * V;  // the current p, once a pass has written it (each CTA its slice)
   __shared__ float2 red[kWarps];
   __shared__ float2 xf[2];
   __shared__ double xd[2];
@@ -325,7 +364,10 @@ __global__ void __cluster_dims__(kCluster, 1, 1) __launch_bounds__(kThreads) rej
   int32_t* an = accepted_nodes + (int64_t)b * (K + 1);
   if (crank == 0)
     for (int j = tid; j <= K; j += kThreads) an[j] = j == 0 ? 0 : -1;
-  float sp = 0.f, sq = 0.f;
+  float sp = 0.f;     // p(v) = Pw[v] * sp once `mat`
+  bool mat = false;   // Pw holds the current node's p (after a rejection there)
+  Soft2 P{-INFINITY, 0.f};
+  const float* zc = logits;
   int cur = 0, len = 0, m = 0;
   // every decision below depends only on values that are the same in every
   // CTA of the cluster (tree, tokens, uniforms, cluster-reduced scalars and
@@ -352,10 +394,13 @@ __global__ void __cluster_dims__(kCluster, 1, 1) __launch_bounds__(kThreads) rej
     m = s_m;
     const int k = m > 0 ? tree.depth[kids[0]] : 0;
     const bool walk = guard <= K && m > 0 && m < u_stride && k >= 1 && k <= K && k <= Kd;
-    const float* dz = walk ? draft + ((int64_t)b * Kd + (k - 1)) * V : nullptr;
-    // p at this node (and q of the children's head when the walk goes on)
-    exp_rows(logits + ((int64_t)b * T + cur) * V, dz, lo, hi, inv_tau, Pw, Qw, sp, sq, R);
+    // p at this node and q of the children's head, from the row statistics
+    zc = logits + ((int64_t)b * T + cur) * V;
+    P = row_soft(stats, (int64_t)b * (T + Kd) + cur);
+    mat = false;
     if (!walk) break;
+    const float* dz = draft + ((int64_t)b * Kd + (k - 1)) * V;
+    const Soft2 Q = row_soft(stats, (int64_t)b * (T + Kd) + T + (k - 1));
     int acc = -1;
     for (int j = 0; j < m; ++j) {
       const int n = kids[j];
@@ -365,15 +410,18 @@ __global__ void __cluster_dims__(kCluster, 1, 1) __launch_bounds__(kThreads) rej
         continue;
       }
       const float u = uni[((int64_t)b * T + cur) * u_stride + j];
-      const float qx = __ldcg(Qw + x) * sq;  // L2: another CTA may own x
-      const float px = __ldcg(Pw + x) * sp;
+      const float qx = expf(__ldg(dz + x) * inv_tau - Q.m) / Q.S;
+      const float px = mat ? __ldcg(Pw + x) * sp  // L2: another CTA may own x
+                           : expf(__ldg(zc + x) * inv_tau - P.m) / P.S;
       if (u * qx < px) {
         acc = n;
         break;
       }
       // rejected: p <- [p - q]_+ / sum, the residual and its sum in one pass
-      const float S = residual(Pw, Qw, sp, sq, lo, hi, R);
+      const float S = mat ? residual<true>(zc, dz, inv_tau, P, Q, Pw, sp, lo, hi, R)
+                          : residual<false>(zc, dz, inv_tau, P, Q, Pw, sp, lo, hi, R);
       sp = S > 0.f ? 1.f / S : 0.f;
+      mat = true;
     }
     if (acc < 0) break;
     ++len;
@@ -381,7 +429,12 @@ __global__ void __cluster_dims__(kCluster, 1, 1) __launch_bounds__(kThreads) rej
     cur = acc;
     m = 0;
   }
-  // final draw from p at the node where the walk stopped
+  // final draw from p at the node where the walk stopped (written out first
+  // unless a rejection there already did)
+  if (!mat) {
+    const float S = materialize(zc, inv_tau, P.m, Pw, lo, hi, R);
+    sp = S > 0.f ? 1.f / S : 0.f;
+  }
   const float u = uni[((int64_t)b * T + cur) * u_stride + (m < u_stride ? m : u_stride - 1)];
   const int tok = draw(Pw, sp, lo, hi, (double)u, wsum, &s_tok, R, crank);
   if (tid == 0) {
@@ -396,9 +449,14 @@ __global__ void __cluster_dims__(kCluster, 1, 1) __launch_bounds__(kThreads) rej
 
 using namespace medusa;
 
+// Workspace: a row of V floats per sequence for the current p (and a spare
+// row), then the row statistics [B][T + Kd][2] (float2) at the library's
+// maximum T and K.
+static size_t rows_bytes(int B, int V) { return align_up((size_t)B * 2 * V * sizeof(float), 256); }
+
 extern "C" size_t medusa_accept_rejection_workspace_size(int B, int V) {
   if (B < 1 || V < 1) return 0;
-  return align_up((size_t)B * 2 * V * sizeof(float), 256);  // target and draft rows per sequence
+  return rows_bytes(B, V) + align_up((size_t)B * (MEDUSA_MAX_T + MEDUSA_MAX_K) * 2 * sizeof(float2), 256);
 }
 
 extern "C" int medusa_accept_rejection(const float* logits, const float* draft_logits, int Kd,
@@ -417,8 +475,12 @@ extern "C" int medusa_accept_rejection(const float* logits, const float* draft_l
   const size_t need = medusa_accept_rejection_workspace_size(B, V);
   if (!workspace || workspace_bytes < need)
     return fail(MEDUSA_ERR_WORKSPACE, "%s: workspace %zu < %zu bytes", fn, workspace_bytes, need);
+  if (Kd > MEDUSA_MAX_K) return fail(MEDUSA_ERR_UNSUPPORTED, "%s: Kd=%d above the maximum", fn, Kd);
+  float2* stats = reinterpret_cast<float2*>(static_cast<uint8_t*>(workspace) + rows_bytes(B, V));
+  launch_kernel(reject_stats_kernel, dim3((tree->T + Kd) * 2, B), dim3(kStatThreads), 0, as_stream(stream), logits,
+                draft_logits, tree->T, Kd, V, 1.f / temperature, stats);
   launch_kernel(reject_tree_kernel, dim3(kCluster, B), dim3(kThreads), 0, as_stream(stream), logits, draft_logits, Kd,
                 tokens, *tree, V, 1.f / temperature, uniforms, u_stride, accept_len, accepted_nodes, next_token,
-                static_cast<float*>(workspace), err);
+                static_cast<float*>(workspace), stats, err);
   return check_launch(fn);
 }
