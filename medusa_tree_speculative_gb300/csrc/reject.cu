@@ -20,14 +20,16 @@
 // softmax statistics (max, sum e^(y - max)) of y = logit / tau, so that the
 // walk tests a drafted token in O(1): p(x) = e^(y_x - m) / S.  The walk runs
 // on a thread-block cluster of 8 CTAs (1024 threads each) per sequence, each
-// CTA owning one eighth of the vocabulary, so that the V-wide passes run on
-// eight SMs; their sums are combined through distributed shared memory.  A
-// rejection is one pass that writes the residual [p - q]_+ (p from the
-// logits and the statistics, or from the row an earlier rejection at the
-// node wrote) and sums it; the final draw writes p out first unless a
-// rejection there did, then takes per-warp segment sums in double, a prefix
-// over the CTAs and the segments, and a scan of one segment.  Every pass
-// keeps 16 loads in flight per thread.
+// CTA owning one eighth of the vocabulary and keeping its slices of the
+// current p and of the node's q in shared memory; sums are combined through
+// distributed shared memory.  A rejection is one pass over the slices that
+// writes the residual [p - q]_+ (at a node's first rejection p and q come
+// from the logits and the statistics) and returns, through the same cluster
+// reduction as its sum, the residual at the next child's token, so the CTAs
+// never read one another's slices; the final draw writes p out first unless
+// a rejection there did, then takes per-warp segment sums in double, a
+// prefix over the CTAs and the segments, and a scan of one segment.  Every
+// pass keeps 16 loads in flight per thread.
 #include <math.h>
 
 #include "common.cuh"
@@ -201,9 +203,9 @@ MDEV Soft2 row_soft(const float2* stats, int64_t idx) {
   return soft2_merge(Soft2{a.x, a.y}, Soft2{c.x, c.y});
 }
 
-// p <- e^(y - m) / S over this CTA's slice of Pw, unnormalised in the row
-// (Pw = e^(y - m)); returns the cluster-wide sum, so that p = Pw / sum.
-MDEV float materialize(const float* z, float inv_tau, float m, float* Pw, int lo, int hi, ClusterRed& R) {
+// This CTA's slice of p, unnormalised (sP[v - lo] = e^(y_v - m)); returns
+// the cluster-wide sum, so that p = sP / sum.
+MDEV float materialize(const float* z, float inv_tau, float m, float* sP, int lo, int hi, ClusterRed& R) {
   float S = 0.f;
   MEDUSA_ROUNDS(lo, hi) {
     float a[kU];
@@ -217,55 +219,64 @@ MDEV float materialize(const float* z, float inv_tau, float m, float* Pw, int lo
       const int v = MEDUSA_IDX(u);
       if (v < hi) {
         const float e = expf(a[u] * inv_tau - m);
-        Pw[v] = e;
+        sP[v - lo] = e;
         S += e;
       }
     }
   }
-  return R.sum(S);  // its cluster barrier also publishes the row
+  return R.sum(S);  // its cluster barrier also publishes the slice
 }
 
-// p <- [p - q]_+ (unnormalised, over this CTA's slice of Pw); p(v) is
-// Pw[v] * sp once the row holds p (MAT), else e^(y_v - P.m) / P.S from the
-// node's logits; q(v) = e^(y'_v - Q.m) / Q.S from the drafting head's.
-// Returns the cluster-wide sum.
+// p <- [p - q]_+ over this CTA's slice sP (unnormalised).  At a node's first
+// rejection (!MAT) p and q come from the logits and the row statistics
+// (p(v) = e^(y_v - P.m) / P.S, q likewise from the drafting head's logits)
+// and q is kept in sQ for the node's later rejections; afterwards p(v) =
+// sP[v - lo] * sp.  Returns the cluster-wide sum and the new (unnormalised)
+// value at token xn (-1: none), which only the CTA owning xn contributes, so
+// that every CTA tests the next child on the same bits without reading
+// another CTA's slice.
 template <bool MAT>
-MDEV float residual(const float* z, const float* dz, float inv_tau, Soft2 P, Soft2 Q, float* Pw, float sp, int lo,
-                    int hi, ClusterRed& R) {
+MDEV float2 residual(const float* z, const float* dz, float inv_tau, Soft2 P, Soft2 Q, float* sP, float* sQ,
+                     float sp, int xn, int lo, int hi, ClusterRed& R) {
   const float ip = 1.f / P.S, iq = 1.f / Q.S;
-  float S = 0.f;
+  float S = 0.f, rx = 0.f;
   MEDUSA_ROUNDS(lo, hi) {
     float a[kU], c[kU];
 #pragma unroll
     for (int u = 0; u < kU; ++u) {
       const int v = MEDUSA_IDX(u);
-      a[u] = v < hi ? (MAT ? Pw[v] : z[v]) : 0.f;
-      c[u] = v < hi ? dz[v] : 0.f;
+      a[u] = v < hi ? (MAT ? sP[v - lo] : z[v]) : 0.f;
+      c[u] = v < hi ? (MAT ? sQ[v - lo] : dz[v]) : 0.f;
     }
 #pragma unroll
     for (int u = 0; u < kU; ++u) {
       const int v = MEDUSA_IDX(u);
       if (v < hi) {
         const float pv = MAT ? a[u] * sp : expf(a[u] * inv_tau - P.m) * ip;
-        const float r = fmaxf(0.f, pv - expf(c[u] * inv_tau - Q.m) * iq);
-        Pw[v] = r;
+        const float qv = MAT ? c[u] : expf(c[u] * inv_tau - Q.m) * iq;
+        if (!MAT) sQ[v - lo] = qv;
+        const float r = fmaxf(0.f, pv - qv);
+        sP[v - lo] = r;
         S += r;
+        if (v == xn) rx = r;
       }
     }
   }
-  return R.sum(S);  // its cluster barrier also publishes the residual row
+  R.pair<false>(S, rx);  // rx is nonzero in one thread of one CTA at most
+  return make_float2(S, rx);
 }
 
-// The last v in [lo, hi) with p(v) > 0 (-1 if none), in every thread.
-MDEV int last_with_mass(const float* Pw, float sp, int lo, int hi, float2* red) {
+// The last v in [lo, hi) with p(v) > 0 (-1 if none), in every thread; sP is
+// this CTA's slice (sP[v - lo]).
+MDEV int last_with_mass(const float* sP, float sp, int lo, int hi, float2* red) {
   float best = -1.f, dummy = -1.f;  // indices below 2^24 are exact in float
   for (int v = lo + (int)threadIdx.x; v < hi; v += kThreads)
-    if (Pw[v] * sp > 0.f) best = (float)v;
+    if (sP[v - lo] * sp > 0.f) best = (float)v;
   block_pair<true>(best, dummy, red);
   return (int)best;
 }
 
-// Inverse CDF over the cluster: the first v with p(v) = Pw[v] * sp > 0
+// Inverse CDF over the cluster: the first v with p(v) = sP[v - lo] * sp > 0
 // whose running sum of p, in index order and in double, exceeds u; the last
 // v with mass when u is beyond the total.  Each warp of each CTA sums a
 // contiguous segment of the CTA's slice; the CTAs' totals are exchanged and
@@ -274,7 +285,7 @@ MDEV int last_with_mass(const float* Pw, float sp, int lo, int hi, float2* red) 
 // segment holds it, and that warp scans its segment 32 elements at a time.
 // Returns the token in the CTA that found it (rank 0 for the beyond-total
 // case), -2 in the others.
-MDEV int draw(const float* Pw, float sp, int lo, int hi, double u, double* wsum, int* s_tok, ClusterRed& R,
+MDEV int draw(const float* sP, float sp, int lo, int hi, double u, double* wsum, int* s_tok, ClusterRed& R,
               int crank) {
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int seg = (hi - lo + kWarps - 1) / kWarps;
@@ -285,7 +296,7 @@ MDEV int draw(const float* Pw, float sp, int lo, int hi, double u, double* wsum,
 #pragma unroll
     for (int q = 0; q < kU; ++q) {
       const int v = base + q * 32 + lane;
-      a[q] = v < s1 ? Pw[v] : 0.f;
+      a[q] = v < s1 ? sP[v - lo] : 0.f;
     }
 #pragma unroll
     for (int q = 0; q < kU; ++q) acc += (double)(a[q] * sp);
@@ -307,7 +318,7 @@ MDEV int draw(const float* Pw, float sp, int lo, int hi, double u, double* wsum,
     total += tot[r];
   }
   if (u >= total) {  // beyond the rounded total: the last token with mass, cluster-wide
-    float last = (float)last_with_mass(Pw, sp, lo, hi, R.red), dummy = -1.f;
+    float last = (float)last_with_mass(sP, sp, lo, hi, R.red), dummy = -1.f;
     R.pair<true>(last, dummy);
     return crank == 0 ? (int)last : -2;
   }
@@ -319,7 +330,7 @@ MDEV int draw(const float* Pw, float sp, int lo, int hi, double u, double* wsum,
       int tok = -1;
       for (int base = s0; base < s1 && tok < 0; base += 32) {
         const int v = base + lane;
-        const float pv = v < s1 ? Pw[v] * sp : 0.f;
+        const float pv = v < s1 ? sP[v - lo] * sp : 0.f;
         double c = (double)pv;
 #pragma unroll
         for (int o = 1; o < 32; o <<= 1) {
@@ -332,7 +343,7 @@ MDEV int draw(const float* Pw, float sp, int lo, int hi, double u, double* wsum,
       }
       for (int base = s1 - 32; tok < 0 && base > s0 - 32; base -= 32) {  // rounding: the segment's last with mass
         const int v = base + lane;
-        const unsigned hit = __ballot_sync(0xffffffffu, v >= s0 && v < s1 && Pw[v] * sp > 0.f);
+        const unsigned hit = __ballot_sync(0xffffffffu, v >= s0 && v < s1 && sP[v - lo] * sp > 0.f);
         if (hit) tok = base + 31 - __clz(hit);
       }
       if (lane == 0) *s_tok = tok;
@@ -340,18 +351,22 @@ MDEV int draw(const float* Pw, float sp, int lo, int hi, double u, double* wsum,
   }
   __syncthreads();
   int tok = *s_tok;
-  if (mine_u && tok < 0) tok = last_with_mass(Pw, sp, lo, hi, R.red);  // rounding between the warps' intervals
+  if (mine_u && tok < 0) tok = last_with_mass(sP, sp, lo, hi, R.red);  // rounding between the warps' intervals
   return mine_u ? tok : -2;
 }
 
 __global__ void __cluster_dims__(kCluster, 1, 1) __launch_bounds__(kThreads) reject_tree_kernel(
     const float* logits, const float* draft, int Kd, const int32_t* tokens, medusa_tree_t tree, int V,
     float inv_tau, const float* uni, int u_stride, int32_t* accept_len, int32_t* accepted_nodes,
-    int32_t* next_token, float* pws, const float2* stats, int32_t* err) {
+    int32_t* next_token, const float2* stats, int32_t* err) {
   const int crank = blockIdx.x, b = blockIdx.y, tid = threadIdx.x;  // gridDim.x == kCluster
   const int T = tree.T, K = tree.K;
   const int lo = (int)((int64_t)crank * V / kCluster), hi = (int)((int64_t)(crank + 1) * V / kCluster);
-  float* Pw = pws + (int64_t)b * 2 * V;  // the current p, once a pass has written it (each CTA its slice)
+  // this CTA's slices of the current p (once a pass has written it) and of
+  // the node's q (from its first rejection on)
+  extern __shared__ float s_slices[];
+  float* sP = s_slices;
+  float* sQ = s_slices + (V + kCluster - 1) / kCluster;
   __shared__ float2 red[kWarps];
   __shared__ float2 xf[2];
   __shared__ double xd[2];
@@ -364,8 +379,9 @@ __global__ void __cluster_dims__(kCluster, 1, 1) __launch_bounds__(kThreads) rej
   int32_t* an = accepted_nodes + (int64_t)b * (K + 1);
   if (crank == 0)
     for (int j = tid; j <= K; j += kThreads) an[j] = j == 0 ? 0 : -1;
-  float sp = 0.f;     // p(v) = Pw[v] * sp once `mat`
-  bool mat = false;   // Pw holds the current node's p (after a rejection there)
+  float sp = 0.f;     // p(v) = sP[v - lo] * sp once `mat`
+  bool mat = false;   // sP holds the current node's p (after a rejection there)
+  float pnext = 0.f;  // once `mat`: the unnormalised p at the next child's token
   Soft2 P{-INFINITY, 0.f};
   const float* zc = logits;
   int cur = 0, len = 0, m = 0;
@@ -409,18 +425,23 @@ __global__ void __cluster_dims__(kCluster, 1, 1) __launch_bounds__(kThreads) rej
         if (tid == 0 && crank == 0) set_err(err, MEDUSA_DEVERR_TOKEN);
         continue;
       }
+      int xn = -1;  // the token of the next child with a valid draft
+      for (int jj = j + 1; jj < m && xn < 0; ++jj) {
+        const int t = tokens[(int64_t)b * T + kids[jj]];
+        if (t >= 0 && t < V) xn = t;
+      }
       const float u = uni[((int64_t)b * T + cur) * u_stride + j];
       const float qx = expf(__ldg(dz + x) * inv_tau - Q.m) / Q.S;
-      const float px = mat ? __ldcg(Pw + x) * sp  // L2: another CTA may own x
-                           : expf(__ldg(zc + x) * inv_tau - P.m) / P.S;
+      const float px = mat ? pnext * sp : expf(__ldg(zc + x) * inv_tau - P.m) / P.S;
       if (u * qx < px) {
         acc = n;
         break;
       }
       // rejected: p <- [p - q]_+ / sum, the residual and its sum in one pass
-      const float S = mat ? residual<true>(zc, dz, inv_tau, P, Q, Pw, sp, lo, hi, R)
-                          : residual<false>(zc, dz, inv_tau, P, Q, Pw, sp, lo, hi, R);
-      sp = S > 0.f ? 1.f / S : 0.f;
+      const float2 r = mat ? residual<true>(zc, dz, inv_tau, P, Q, sP, sQ, sp, xn, lo, hi, R)
+                           : residual<false>(zc, dz, inv_tau, P, Q, sP, sQ, sp, xn, lo, hi, R);
+      sp = r.x > 0.f ? 1.f / r.x : 0.f;
+      pnext = r.y;
       mat = true;
     }
     if (acc < 0) break;
@@ -432,11 +453,11 @@ __global__ void __cluster_dims__(kCluster, 1, 1) __launch_bounds__(kThreads) rej
   // final draw from p at the node where the walk stopped (written out first
   // unless a rejection there already did)
   if (!mat) {
-    const float S = materialize(zc, inv_tau, P.m, Pw, lo, hi, R);
+    const float S = materialize(zc, inv_tau, P.m, sP, lo, hi, R);
     sp = S > 0.f ? 1.f / S : 0.f;
   }
   const float u = uni[((int64_t)b * T + cur) * u_stride + (m < u_stride ? m : u_stride - 1)];
-  const int tok = draw(Pw, sp, lo, hi, (double)u, wsum, &s_tok, R, crank);
+  const int tok = draw(sP, sp, lo, hi, (double)u, wsum, &s_tok, R, crank);
   if (tid == 0) {
     if (tok != -2) next_token[b] = tok;
     if (crank == 0) accept_len[b] = len;
@@ -479,8 +500,11 @@ extern "C" int medusa_accept_rejection(const float* logits, const float* draft_l
   float2* stats = reinterpret_cast<float2*>(static_cast<uint8_t*>(workspace) + rows_bytes(B, V));
   launch_kernel(reject_stats_kernel, dim3((tree->T + Kd) * 2, B), dim3(kStatThreads), 0, as_stream(stream), logits,
                 draft_logits, tree->T, Kd, V, 1.f / temperature, stats);
-  launch_kernel(reject_tree_kernel, dim3(kCluster, B), dim3(kThreads), 0, as_stream(stream), logits, draft_logits, Kd,
+  const size_t smem = 2 * (size_t)((V + kCluster - 1) / kCluster) * sizeof(float);  // p and q slices
+  if (smem > 200 * 1024) return fail(MEDUSA_ERR_UNSUPPORTED, "%s: V=%d above the shared-memory slices", fn, V);
+  cudaFuncSetAttribute(reject_tree_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  launch_kernel(reject_tree_kernel, dim3(kCluster, B), dim3(kThreads), smem, as_stream(stream), logits, draft_logits, Kd,
                 tokens, *tree, V, 1.f / temperature, uniforms, u_stride, accept_len, accepted_nodes, next_token,
-                static_cast<float*>(workspace), stats, err);
+                stats, err);
   return check_launch(fn);
 }
