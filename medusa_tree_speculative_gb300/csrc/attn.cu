@@ -37,6 +37,7 @@
 #include <algorithm>
 #include <cmath>
 
+#include "cluster.cuh"
 #include "common.cuh"
 #include "internal.h"
 
@@ -134,23 +135,6 @@ __device__ __forceinline__ void rope8(const uint4& lo, const uint4& hi, const fl
                    pack2_bf16(r2[6], r2[7]));
 }
 
-MDEV uint32_t cluster_ctarank() {
-  uint32_t r;
-  asm volatile("mov.u32 %0, %%cluster_ctarank;\n" : "=r"(r));
-  return r;
-}
-MDEV void cluster_sync() {
-  asm volatile("barrier.cluster.arrive.release.aligned;\n" ::: "memory");
-  asm volatile("barrier.cluster.wait.acquire.aligned;\n" ::: "memory");
-}
-MDEV uint32_t map_to_rank(uint32_t local_smem_addr, uint32_t rank) {
-  uint32_t r;
-  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;\n" : "=r"(r) : "r"(local_smem_addr), "r"(rank));
-  return r;
-}
-MDEV void st_cluster_f32x2(uint32_t addr, float x, float y) {
-  asm volatile("st.shared::cluster.v2.f32 [%0], {%1, %2};\n" ::"r"(addr), "f"(x), "f"(y) : "memory");
-}
 
 // ---------------------------------------------------------------------------
 // bf16: clustered split-K tree attention
@@ -175,7 +159,7 @@ __global__ void __cluster_dims__(CL, 1, 1) __launch_bounds__(MAX_WARPS * 32, 2)
   float* cs = reinterpret_cast<float*>(kvbuf + S * 2 * KT * DH);  // [K+1][HALF]
   float* sn = cs + (a.K + 1) * HALF;
 
-  const uint32_t crank = CL > 1 ? cluster_ctarank() : 0u;
+  const uint32_t crank = CL > 1 ? cluster_rank() : 0u;
   const int h = blockIdx.y, b = blockIdx.z / a.rowblocks, rb = blockIdx.z % a.rowblocks;
   const int tid = threadIdx.x, nthr = blockDim.x;
   const int warp = tid >> 5, lane = tid & 31;
@@ -470,8 +454,8 @@ __global__ void __cluster_dims__(CL, 1, 1) __launch_bounds__(MAX_WARPS * 32, 2)
   cluster_sync();
   const uint32_t o_base = smem_u32(recv_o), ml_base = smem_u32(recv_ml);
   if (row0 + la < a.T) {
-    const uint32_t ra_o = map_to_rank(o_base + (((int)crank * RPO + la / CL) * DH) * 4, (uint32_t)(la % CL));
-    const uint32_t rb_o = map_to_rank(o_base + (((int)crank * RPO + lb / CL) * DH) * 4, (uint32_t)(lb % CL));
+    const uint32_t ra_o = cluster_map(o_base + (((int)crank * RPO + la / CL) * DH) * 4, (uint32_t)(la % CL));
+    const uint32_t rb_o = cluster_map(o_base + (((int)crank * RPO + lb / CL) * DH) * 4, (uint32_t)(lb % CL));
     const bool push_b = row0 + lb < a.T;
 #pragma unroll
     for (int n = 0; n < DH / 8; ++n) {
@@ -480,9 +464,9 @@ __global__ void __cluster_dims__(CL, 1, 1) __launch_bounds__(MAX_WARPS * 32, 2)
       if (push_b) st_cluster_f32x2(rb_o + col * 4, o[n][2], o[n][3]);
     }
     if ((lane & 3) == 0) {
-      st_cluster_f32x2(map_to_rank(ml_base + (((int)crank * RPO + la / CL) * 2) * 4, (uint32_t)(la % CL)), m_a, l_a);
+      st_cluster_f32x2(cluster_map(ml_base + (((int)crank * RPO + la / CL) * 2) * 4, (uint32_t)(la % CL)), m_a, l_a);
       if (push_b)
-        st_cluster_f32x2(map_to_rank(ml_base + (((int)crank * RPO + lb / CL) * 2) * 4, (uint32_t)(lb % CL)), m_b,
+        st_cluster_f32x2(cluster_map(ml_base + (((int)crank * RPO + lb / CL) * 2) * 4, (uint32_t)(lb % CL)), m_b,
                          l_b);
     }
   }

@@ -38,6 +38,7 @@
 #include <cmath>
 #include <mutex>
 
+#include "cluster.cuh"
 #include "common.cuh"
 #include "internal.h"
 #include "sm100.cuh"
@@ -165,27 +166,6 @@ MDEV float ex2_ftz(float x) {
   return y;
 }
 
-MDEV void sync_cluster() {
-  asm volatile("barrier.cluster.arrive.release.aligned;\n" ::: "memory");
-  asm volatile("barrier.cluster.wait.acquire.aligned;\n" ::: "memory");
-}
-// This CTA's shared address `a` as seen in the shared memory of cluster CTA `rank`.
-MDEV uint32_t remote_addr(uint32_t a, uint32_t rank) {
-  uint32_t r;
-  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;\n" : "=r"(r) : "r"(a), "r"(rank));
-  return r;
-}
-MDEV float4 ld_cluster_f4(uint32_t addr) {
-  float4 v;
-  asm volatile("ld.shared::cluster.v4.f32 {%0, %1, %2, %3}, [%4];\n"
-               : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w)
-               : "r"(addr)
-               : "memory");
-  return v;
-}
-MDEV void ld_cluster_f2(uint32_t addr, float& x, float& y) {
-  asm volatile("ld.shared::cluster.v2.f32 {%0, %1}, [%2];\n" : "=f"(x), "=f"(y) : "r"(addr) : "memory");
-}
 MDEV void st_shared_f4(uint32_t addr, float x, float y, float z, float w) {
   asm volatile("st.shared.v4.f32 [%0], {%1, %2, %3, %4};\n" ::"r"(addr), "f"(x), "f"(y), "f"(z), "f"(w) : "memory");
 }
@@ -401,8 +381,8 @@ __global__ void __cluster_dims__(CL, 1, 1) __launch_bounds__(kThreads, 1)
     }
     if constexpr (CL > 1) {  // the merge's two cluster barriers
       __syncwarp();
-      sync_cluster();
-      sync_cluster();
+      cluster_sync();
+      cluster_sync();
     }
   } else if (warp == 1) {
     // ---------------- MMA issuer
@@ -462,8 +442,8 @@ __global__ void __cluster_dims__(CL, 1, 1) __launch_bounds__(kThreads, 1)
     }
     if constexpr (CL > 1) {  // the merge's two cluster barriers
       __syncwarp();
-      sync_cluster();
-      sync_cluster();
+      cluster_sync();
+      cluster_sync();
     }
   } else {
     // ---------------- softmax: two threads per query row (its tensor-memory
@@ -632,14 +612,18 @@ __global__ void __cluster_dims__(CL, 1, 1) __launch_bounds__(kThreads, 1)
         if (hh == 0) st_shared_f2(sbase + kMlOff + r * 8, m, l);
       }
       __syncwarp();
-      sync_cluster();  // every partial is in place
+      cluster_sync();  // every partial is in place
       constexpr int CW = DH / CL, tpr = CW / 8;  // columns per CTA; threads per row, 8 columns each
       const int u = tid - 64;
       for (int rr = u / tpr; rr < nlive; rr += kSoftThreads / tpr) {
         const int col = crank * CW + (u % tpr) * 8;
         float pm[CL], pl[CL];
 #pragma unroll
-        for (int c = 0; c < CL; ++c) ld_cluster_f2(remote_addr(sbase + kMlOff + rr * 8, (uint32_t)c), pm[c], pl[c]);
+        for (int c = 0; c < CL; ++c) {
+          const float2 t = ld_cluster_f2(cluster_map(sbase + kMlOff + rr * 8, (uint32_t)c));
+          pm[c] = t.x;
+          pl[c] = t.y;
+        }
         float mmax = -INFINITY;
 #pragma unroll
         for (int c = 0; c < CL; ++c) mmax = fmaxf(mmax, pm[c]);
@@ -657,7 +641,7 @@ __global__ void __cluster_dims__(CL, 1, 1) __launch_bounds__(kThreads, 1)
 #pragma unroll
           for (int c = 0; c < CL; ++c)
             x[c] = ld_cluster_f4(
-                remote_addr(sbase + kPartOff + (uint32_t)(rr * kPartStride + col + hf * 4) * 4, (uint32_t)c));
+                cluster_map(sbase + kPartOff + (uint32_t)(rr * kPartStride + col + hf * 4) * 4, (uint32_t)c));
           float s0 = 0.f, s1 = 0.f, s2 = 0.f, s3 = 0.f;
 #pragma unroll
           for (int c = 0; c < CL; ++c) {
@@ -671,7 +655,7 @@ __global__ void __cluster_dims__(CL, 1, 1) __launch_bounds__(kThreads, 1)
                        pack2_bf16(acc[4] * inv, acc[5] * inv), pack2_bf16(acc[6] * inv, acc[7] * inv));
       }
       __syncwarp();
-      sync_cluster();  // no CTA leaves while its partial may still be read
+      cluster_sync();  // no CTA leaves while its partial may still be read
     }
   }
   tc_fence_before();

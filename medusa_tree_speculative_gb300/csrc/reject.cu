@@ -32,6 +32,7 @@
 // pass keeps 16 loads in flight per thread.
 #include <math.h>
 
+#include "cluster.cuh"
 #include "common.cuh"
 #include "internal.h"
 
@@ -76,25 +77,6 @@ MDEV double warp_sum_d(double x) {
 }
 
 // ---- thread-block cluster: barrier and distributed shared memory
-MDEV void cluster_sync_all() {
-  asm volatile("barrier.cluster.arrive.release.aligned;\n" ::: "memory");
-  asm volatile("barrier.cluster.wait.acquire.aligned;\n" ::: "memory");
-}
-MDEV uint32_t cluster_addr(const void* p, uint32_t rank) {
-  uint32_t r;
-  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;\n" : "=r"(r) : "r"(smem_u32(p)), "r"(rank));
-  return r;
-}
-MDEV float2 ld_cluster_f2(uint32_t addr) {
-  float2 v;
-  asm volatile("ld.shared::cluster.v2.f32 {%0, %1}, [%2];\n" : "=f"(v.x), "=f"(v.y) : "r"(addr) : "memory");
-  return v;
-}
-MDEV double ld_cluster_f64(uint32_t addr) {
-  double v;
-  asm volatile("ld.shared::cluster.f64 %0, [%1];\n" : "=d"(v) : "r"(addr) : "memory");
-  return v;
-}
 
 // Reductions over the cluster's CTAs: a block reduction, each CTA's result
 // in its exchange slot (two slots used in turn: a CTA reuses a slot only
@@ -112,11 +94,11 @@ struct ClusterRed {
     block_pair<MAX>(a, b, red);
     const int slot = ph++ & 1;
     if (threadIdx.x == 0) xf[slot] = make_float2(a, b);
-    cluster_sync_all();
+    cluster_sync();
     float ra = MAX ? -INFINITY : 0.f, rb = ra;
 #pragma unroll
     for (int r = 0; r < kCluster; ++r) {
-      const float2 v = ld_cluster_f2(cluster_addr(&xf[slot], (uint32_t)r));
+      const float2 v = ld_cluster_f2(cluster_map(smem_u32(&xf[slot]), (uint32_t)r));
       ra = op2<MAX>(ra, v.x);
       rb = op2<MAX>(rb, v.y);
     }
@@ -132,9 +114,9 @@ struct ClusterRed {
   MDEV void gather_d(double mine, double* out) {
     const int slot = ph++ & 1;
     if (threadIdx.x == 0) xd[slot] = mine;
-    cluster_sync_all();
+    cluster_sync();
 #pragma unroll
-    for (int r = 0; r < kCluster; ++r) out[r] = ld_cluster_f64(cluster_addr(&xd[slot], (uint32_t)r));
+    for (int r = 0; r < kCluster; ++r) out[r] = ld_cluster_f64(cluster_map(smem_u32(&xd[slot]), (uint32_t)r));
   }
 };
 
@@ -462,7 +444,7 @@ __global__ void __cluster_dims__(kCluster, 1, 1) __launch_bounds__(kThreads) rej
     if (tok != -2) next_token[b] = tok;
     if (crank == 0) accept_len[b] = len;
   }
-  cluster_sync_all();  // no CTA leaves while another may still read its exchange slots
+  cluster_sync();  // no CTA leaves while another may still read its exchange slots
 }
 
 }  // namespace
