@@ -360,11 +360,7 @@ def run_native(args, w, rank, world, local_rank):
     if int(st.err.item()) != 0:
         raise RuntimeError(f"device error flag {int(st.err.item())} in the timed region")
 
-    ms_total = ms_plain
-    if world > 1:
-        t = torch.tensor([ms_total], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        ms_total = float(t.item())
+    ms_total = max_over_ranks(ms_plain, dev) if world > 1 else ms_plain
     ms_step = ms_total / args.steps
 
     e2e = None
@@ -631,6 +627,24 @@ def cpu_baseline(w, reps=3):
             "seconds_per_step_est": sec, "parts_s": {k: round(v, 4) for k, v in parts.items()}}
 
 
+def max_over_ranks(x: float, device) -> float:
+    """The largest of every rank's x (the slowest rank sets a replicated
+    job's time); device: where the collective's tensor lives (cuda for NCCL,
+    cpu for gloo)."""
+    import torch
+    import torch.distributed as dist
+
+    t = torch.tensor([float(x)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def whole_job_value(world: int, steps: int, ms_total: float) -> float:
+    """Verify-steps per second of the whole job: every rank runs `steps`
+    steps of its own replica in ms_total (the slowest rank's time)."""
+    return world * steps * 1e3 / ms_total
+
+
 def run_reference(args, w, rank, world):
     """--impl reference: the CPU oracle as it stands, on host cores."""
     if rank != 0:
@@ -705,7 +719,7 @@ def main():
                            args.logits or w["mode"] == "typical")
     fl = algorithmic_flops(w, r["T"], r["s_heads"], r["L_list"])
     ms = r["ms_step"]
-    value = world * 1e3 / ms
+    value = whole_job_value(world, args.steps, ms * args.steps)
     step_gbs = by["step"] / (ms * 1e-3) / 1e9
     dom = max((c for c in ("heads_topk", "heads_logits_topk", "lm_head_verify", "tree_attn")
                if c in r["per_call_ms"]), key=lambda c: r["per_call_ms"][c])
