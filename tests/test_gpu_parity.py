@@ -474,6 +474,9 @@ HEAD_CASES = [
     ("bf16", 3, 65, 512, 3000, (8, 6, 5, 2, 0), True, False),
     ("bf16", 4, 9, 640, 5000, (16, 1), False, False),
     ("bf16", 1, 65, 4096, 32000, (8, 6, 5, 2), False, False),
+    # more than four sequences: the 16-sequence kernels, a warp merging two sequences' lists
+    ("bf16", 9, 9, 256, 2000, (16, 4), False, False),
+    ("f32", 6, 15, 256, 1024, (3, 2), True, True),
 ]
 
 
