@@ -281,6 +281,12 @@ __global__ void __launch_bounds__(kWarps * 32) heads_w2_topk_kernel(const __grid
   // the head this CTA serves goes by the order in which CTAs start, not by
   // blockIdx, so CTAs held back by other work spread over every head
   if (threadIdx.x == 0) s_ticket = atomicAdd(a.tickets, 1);
+  // the candidate fill's first node per thread, in case this CTA does it
+  int fill_depth = 0, fill_rank = 0;
+  if (a.tokens && (int)threadIdx.x < a.B * a.cT) {
+    fill_depth = __ldg(a.c_depth + threadIdx.x % a.cT);
+    fill_rank = __ldg(a.c_rank + threadIdx.x % a.cT);
+  }
   __syncthreads();
   const int slot = s_ticket % a.nused, part = s_ticket / a.nused;
   const int k = a.heads[slot];
@@ -360,12 +366,10 @@ __global__ void __launch_bounds__(kWarps * 32) heads_w2_topk_kernel(const __grid
       __threadfence();  // before the head's counter below
     }
   }
-  // the last CTA of this head to arrive merges all its CTAs' candidates
+  // the last CTA of this head to arrive merges all its CTAs' candidates (the
+  // lists' writers fenced after writing them)
   __syncthreads();
-  if (threadIdx.x == 0) {
-    __threadfence();
-    last = atomicAdd(a.counters + slot, 1) == a.cpc - 1;
-  }
+  if (threadIdx.x == 0) last = atomicAdd(a.counters + slot, 1) == a.cpc - 1;
   __syncthreads();
   if (last) {
     __threadfence();
@@ -427,7 +431,9 @@ __global__ void __launch_bounds__(kWarps * 32) heads_w2_topk_kernel(const __grid
           if (n == 0) {
             tok = a.next_root[b];
           } else {
-            const int kk = a.c_depth[n] - 1, r = a.c_rank[n] - 1;
+            // the first round's node was loaded when the CTA started
+            const int kk = (e == (int)threadIdx.x ? fill_depth : a.c_depth[n]) - 1;
+            const int r = (e == (int)threadIdx.x ? fill_rank : a.c_rank[n]) - 1;
             tok = (kk >= 0 && kk < a.K && r >= 0 && r < a.s_max)
                       ? __ldcg(a.topk + ((int64_t)b * a.K + kk) * a.s_max + r)
                       : -1;
