@@ -193,17 +193,13 @@ __global__ void __launch_bounds__(kRowThreads) accept_rowstat_kernel(const __gri
   __shared__ bool s_last;
   __shared__ RowStat rs[MEDUSA_MAX_T];
   __syncthreads();
-  if (threadIdx.x == 0) {
-    __threadfence();
-    s_last = atomicAdd(a.counters + b, 1) == kRowSplit * T - 1;
-  }
+  if (threadIdx.x == 0) s_last = arrive_acq_rel(a.counters + b) == kRowSplit * T - 1;
   __syncthreads();
   if (!s_last) return;
   // one thread per node: the other warps leave, so the decisions' barriers
   // wait for ceil(T / 32) warps only
   const int nthr = (T + 31) & ~31;
   if ((int)threadIdx.x >= nthr) return;
-  __threadfence();
   const int c = threadIdx.x;
   if (c < T) {
     // the row's halves: argmax (value, then lower index), softmax merged

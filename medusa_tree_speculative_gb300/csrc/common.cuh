@@ -116,6 +116,16 @@ MDEV void warp_argmax(float& v, int& i) {
   }
 }
 
+// Counter arrival that publishes the block's earlier writes and, for the
+// thread that sees the final count, acquires every other block's: call it
+// from one thread after a __syncthreads() that follows the block's writes,
+// and have the block read the others' data after another __syncthreads().
+MDEV int arrive_acq_rel(int* counter) {
+  int old;
+  asm volatile("atom.acq_rel.gpu.global.add.s32 %0, [%1], 1;\n" : "=r"(old) : "l"(counter) : "memory");
+  return old;
+}
+
 MDEV void set_err(int32_t* err, int code) {
   if (err) atomicOr(err, code);
 }

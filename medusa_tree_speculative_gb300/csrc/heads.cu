@@ -363,16 +363,13 @@ __global__ void __launch_bounds__(kWarps * 32) heads_w2_topk_kernel(const __grid
       const int64_t base = (((int64_t)slot * a.B + b) * a.cpc + part) * kMaxS;
 #pragma unroll
       for (int t = 0; t < S; ++t) { a.cand_v[base + t] = ov[t]; a.cand_i[base + t] = oi[t]; }
-      __threadfence();  // before the head's counter below
     }
   }
-  // the last CTA of this head to arrive merges all its CTAs' candidates (the
-  // lists' writers fenced after writing them)
+  // the last CTA of this head to arrive merges all its CTAs' candidates
   __syncthreads();
-  if (threadIdx.x == 0) last = atomicAdd(a.counters + slot, 1) == a.cpc - 1;
+  if (threadIdx.x == 0) last = arrive_acq_rel(a.counters + slot) == a.cpc - 1;
   __syncthreads();
   if (last) {
-    __threadfence();
     const int s_k = a.s[slot];
     for (int b = 0; b < a.B; ++b) {
       const int64_t base = ((int64_t)slot * a.B + b) * a.cpc * kMaxS;
@@ -418,13 +415,9 @@ __global__ void __launch_bounds__(kWarps * 32) heads_w2_topk_kernel(const __grid
     if (a.tokens) {
       // the last head to be merged fills the next step's candidates
       __syncthreads();  // this head's topk is written
-      if (threadIdx.x == 0) {
-        __threadfence();
-        last = atomicAdd(a.heads_done, 1) == a.nused - 1;
-      }
+      if (threadIdx.x == 0) last = arrive_acq_rel(a.heads_done) == a.nused - 1;
       __syncthreads();
       if (last) {
-        __threadfence();
         for (int e = threadIdx.x; e < a.B * a.cT; e += blockDim.x) {
           const int b = e / a.cT, n = e % a.cT;
           int32_t tok;
