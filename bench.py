@@ -251,8 +251,8 @@ def step_calls(st, x, s):
                                     st.accept_len, st.accepted_nodes, st.next_root, st.best_node, st.best_logp,
                                     st.ws_accept, st.err, s))),
           ("kv_compact", lambda: M.medusa_kv_compact(x["k_cache"], x["v_cache"], x["seq_start"], x["prefix_len"],
-                                                     st.accepted_nodes, st.accept_len, st.tree.K, st.src_slots,
-                                                     st.err, s))]
+                                                     st.accepted_nodes, st.accept_len, st.tree.K, st.tree.T,
+                                                     st.src_slots, st.err, s))]
     if st.heads in ("split", "joint"):
         c.append(("heads_logits_topk", lambda: M.medusa_heads_logits_topk(
             st.u_all, st.T, st.best_node, st.w2, st.s_heads, st.head_logits, st.topk, st.ws_w2, st.err, s)))

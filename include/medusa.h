@@ -222,6 +222,18 @@ int medusa_tree_attn_tc(const void* q, const void* k_new, const void* v_new,
 int medusa_copy_from_host(void* dst, const void* src_host, size_t bytes,
                           void* stream);
 
+/* Read-out of a device error word (the `err` argument of the step calls).
+ * Enqueues on `stream` one single-thread kernel that writes *err into *out
+ * and then, if clear != 0, sets *err back to 0, so that the next step starts
+ * from a clean word.  err: device memory.  out: device memory or page-locked
+ * host memory mapped into the device's address space (e.g. cudaHostAlloc, or
+ * a pinned torch tensor); *out holds the word once the stream has reached
+ * this point, and the call itself does not synchronise.  The bits are the
+ * MEDUSA_DEVERR_* values above.  Returns MEDUSA_ERR_INVALID for a NULL or
+ * misaligned pointer, or memory the device cannot address.  No counterpart
+ * in the pages: the error convention of this library. */
+int medusa_check_errors(int32_t* err, int32_t* out, int clear, void* stream);
+
 /* Scratch bytes medusa_lm_head_verify needs (currently 0). */
 size_t medusa_lm_head_workspace_size(int rows, int d, int V);
 
@@ -343,8 +355,11 @@ int medusa_accept(const float* logits, const int32_t* tokens,
  * row records of 64 bytes (512 KiB), which every GPU that loads the library
  * holds until the process exits.
  *   - The first call on each device looks up the array's device address
- *     (cudaGetSymbolAddress, with that device current) and caches it; make
- *     that first call before any stream capture.
+ *     (cudaGetSymbolAddress, with that device current) and caches it for the
+ *     device's current context; make that first call before any stream
+ *     capture.  After cudaDeviceReset the next call finds a new context and
+ *     looks the address up again (the array, reloaded with the module, is
+ *     zero again): make that call outside capture too.
  *   - B * tree->T above MEDUSA_ACCEPT_NOALLOC_MAX_ROWS returns
  *     MEDUSA_ERR_CAPACITY.
  *   - It calls no cudaMalloc, cudaFree or other allocating routine.
@@ -368,11 +383,15 @@ int medusa_accept_noalloc(const float* logits, const int32_t* tokens,
  *   prefix_len[b] = L + A + 1;  src_slots[b][j] = L + accepted_nodes[b][j]
  *   for j <= A, -1 after (nullable).
  * accepted_nodes, accept_len, prefix_len (in-out), src_slots: device.
- * Kmax: the row stride of accepted_nodes minus one (= tree->K). */
+ * Kmax: the row stride of accepted_nodes minus one (= tree->K).  T: the
+ * tree's rows (= tree->T), which medusa_tree_attn appended at slots
+ * L .. L + T - 1.  A sequence whose accept_len is outside [0, Kmax] sets
+ * MEDUSA_DEVERR_LENGTH, one whose accepted_nodes[b][j] is outside [j, T)
+ * sets MEDUSA_DEVERR_NODE; either is left untouched (prefix_len included). */
 int medusa_kv_compact(void* k_cache, void* v_cache, const int64_t* seq_start,
                       int32_t* prefix_len, const int32_t* accepted_nodes,
                       const int32_t* accept_len, int B, int H, int Dh,
-                      int Kmax, medusa_dtype dtype, int32_t* src_slots,
+                      int Kmax, int T, medusa_dtype dtype, int32_t* src_slots,
                       int32_t* err, void* stream);
 
 /* Scratch bytes medusa_heads_topk needs. */

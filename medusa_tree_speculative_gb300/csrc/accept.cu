@@ -386,24 +386,67 @@ constexpr int kNoAllocRows = MEDUSA_ACCEPT_NOALLOC_MAX_ROWS;
 constexpr size_t kNoAllocBytes = kCounterBytes + sizeof(HalfStat) * kRowSplit * (size_t)kNoAllocRows;
 static __device__ __align__(256) uint8_t g_accept_scratch[kNoAllocBytes];
 
+// The scratch's device address, cached per device together with the unique
+// id of the context it was looked up in.  A context created after
+// cudaDeviceReset loads the module again, and the array may move; its id
+// differs (context ids are never reused in a process), so the address is
+// looked up again.
+constexpr int kMaxDevices = 64;
 std::mutex g_noalloc_mu;
-void* g_noalloc_addr[64] = {};
+void* g_noalloc_addr[kMaxDevices] = {};
+unsigned long long g_noalloc_ctx[kMaxDevices] = {};
 
-// Device address of g_accept_scratch on the current device.  The host-side
-// symbol is only a stand-in, so the address is looked up once per device,
-// with that device current, and cached.
+// cuCtxGetCurrent and cuCtxGetId through the runtime's driver entry points
+// (the library does not link libcuda).
+using CtxGetCurrentFn = int (*)(void**);
+using CtxGetIdFn = int (*)(void*, unsigned long long*);
+
+int current_context_id(const char* fn, unsigned long long* id) {
+  static CtxGetCurrentFn get_current = nullptr;
+  static CtxGetIdFn get_id = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &p, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      get_current = reinterpret_cast<CtxGetCurrentFn>(p);
+    p = nullptr;
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetId", &p, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      get_id = reinterpret_cast<CtxGetIdFn>(p);
+  });
+  if (!get_current || !get_id) return fail(MEDUSA_ERR_CUDA, "%s: cuCtxGetCurrent / cuCtxGetId unavailable", fn);
+  void* ctx = nullptr;
+  *id = 0;
+  if (get_current(&ctx) != 0) return fail(MEDUSA_ERR_CUDA, "%s: cuCtxGetCurrent failed", fn);
+  if (ctx && get_id(ctx, id) != 0) return fail(MEDUSA_ERR_CUDA, "%s: cuCtxGetId failed", fn);
+  return MEDUSA_OK;
+}
+
+// Device address of g_accept_scratch in the current device's context.  The
+// host-side symbol is only a stand-in, so the address is looked up with that
+// device current (cudaGetSymbolAddress) and cached for the context.
 int noalloc_scratch(const char* fn, void** out) {
   int dev = -1;
   cudaError_t e = cudaGetDevice(&dev);
-  if (e != cudaSuccess || dev < 0 || dev >= 64)
-    return fail(MEDUSA_ERR_CUDA, "%s: cudaGetDevice: %s", fn, cudaGetErrorString(e));
+  if (e != cudaSuccess) return fail(MEDUSA_ERR_CUDA, "%s: cudaGetDevice: %s", fn, cudaGetErrorString(e));
+  if (dev < 0 || dev >= kMaxDevices)
+    return fail(MEDUSA_ERR_UNSUPPORTED, "%s: device ordinal %d outside 0..%d", fn, dev, kMaxDevices - 1);
+  unsigned long long id = 0;
+  if (int rc = current_context_id(fn, &id)) return rc;
   std::lock_guard<std::mutex> lock(g_noalloc_mu);
-  if (!g_noalloc_addr[dev]) {
+  if (!g_noalloc_addr[dev] || id == 0 || g_noalloc_ctx[dev] != id) {
     void* p = nullptr;
     e = cudaGetSymbolAddress(&p, g_accept_scratch);
     if (e != cudaSuccess || !p)
       return fail(MEDUSA_ERR_CUDA, "%s: cudaGetSymbolAddress: %s", fn, cudaGetErrorString(e));
+    if (id == 0) {  // no context was current: the lookup made the primary context current
+      if (int rc = current_context_id(fn, &id)) return rc;
+      if (id == 0) return fail(MEDUSA_ERR_CUDA, "%s: no current context after the symbol lookup", fn);
+    }
     g_noalloc_addr[dev] = p;
+    g_noalloc_ctx[dev] = id;
   }
   *out = g_noalloc_addr[dev];
   return MEDUSA_OK;

@@ -23,7 +23,7 @@ __global__ void __launch_bounds__(512) kv_compact_kernel(uint8_t* k_cache, uint8
                                                           const int64_t* seq_start, int32_t* prefix_len,
                                                           const int32_t* accepted_nodes,
                                                           const int32_t* accept_len, int row_bytes,
-                                                          int Kmax, int32_t* src_slots, int32_t* err) {
+                                                          int Kmax, int T, int32_t* src_slots, int32_t* err) {
   const int b = blockIdx.x;
   const int L = prefix_len[b];
   const int64_t st = seq_start[b];
@@ -38,7 +38,9 @@ __global__ void __launch_bounds__(512) kv_compact_kernel(uint8_t* k_cache, uint8
     if (!bad) {
       for (int j = 0; j <= A; ++j) {
         const int a = an[j];
-        if (a < j || a >= MEDUSA_MAX_T) bad = MEDUSA_DEVERR_NODE;
+        // a node at depth j has index >= j (breadth-first order) and lies
+        // inside the tree, whose rows were appended at slots L .. L + T - 1
+        if (a < j || a >= T) bad = MEDUSA_DEVERR_NODE;
         src[j] = a;
         if (a != j) {  // row j moves: slot L+a -> slot L+j
           soff[n] = (st + L + a) * (int64_t)row_bytes;
@@ -90,7 +92,7 @@ using namespace medusa;
 
 extern "C" int medusa_kv_compact(void* k_cache, void* v_cache, const int64_t* seq_start,
                                  int32_t* prefix_len, const int32_t* accepted_nodes,
-                                 const int32_t* accept_len, int B, int H, int Dh, int Kmax,
+                                 const int32_t* accept_len, int B, int H, int Dh, int Kmax, int T,
                                  medusa_dtype dtype, int32_t* src_slots, int32_t* err, void* stream) {
   const char* fn = "medusa_kv_compact";
   if (!k_cache || !v_cache || !seq_start || !prefix_len || !accepted_nodes || !accept_len)
@@ -98,6 +100,7 @@ extern "C" int medusa_kv_compact(void* k_cache, void* v_cache, const int64_t* se
   if (B < 1 || B > MEDUSA_MAX_B || H < 1 || Dh < 1 || Kmax < 0)
     return fail(MEDUSA_ERR_INVALID, "%s: B=%d H=%d Dh=%d Kmax=%d", fn, B, H, Dh, Kmax);
   if (Kmax > MEDUSA_MAX_K) return fail(MEDUSA_ERR_UNSUPPORTED, "%s: Kmax=%d > %d", fn, Kmax, MEDUSA_MAX_K);
+  if (T < 1 || T > MEDUSA_MAX_T) return fail(MEDUSA_ERR_INVALID, "%s: T=%d outside 1..%d", fn, T, MEDUSA_MAX_T);
   if (dtype != MEDUSA_F32 && dtype != MEDUSA_BF16) return fail(MEDUSA_ERR_UNSUPPORTED, "%s: dtype", fn);
   const int row_bytes = H * Dh * (dtype == MEDUSA_BF16 ? 2 : 4);
   if (row_bytes % 16) return fail(MEDUSA_ERR_UNSUPPORTED, "%s: H*Dh row of %d bytes is not a multiple of 16", fn, row_bytes);
@@ -107,9 +110,9 @@ extern "C" int medusa_kv_compact(void* k_cache, void* v_cache, const int64_t* se
   auto* vc = static_cast<uint8_t*>(v_cache);
   if (Kmax <= 4)
     launch_kernel(kv_compact_kernel<5, 2>, dim3(B), dim3(512), 0, as_stream(stream), kc, vc, seq_start, prefix_len,
-               accepted_nodes, accept_len, row_bytes, Kmax, src_slots, err);
+               accepted_nodes, accept_len, row_bytes, Kmax, T, src_slots, err);
   else
     launch_kernel(kv_compact_kernel<MEDUSA_MAX_K + 1, 1>, dim3(B), dim3(512), 0, as_stream(stream), kc, vc,
-               seq_start, prefix_len, accepted_nodes, accept_len, row_bytes, Kmax, src_slots, err);
+               seq_start, prefix_len, accepted_nodes, accept_len, row_bytes, Kmax, T, src_slots, err);
   return check_launch(fn);
 }

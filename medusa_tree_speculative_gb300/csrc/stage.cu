@@ -1,3 +1,6 @@
+// Host <-> device plumbing of a step: the inputs' copy from pinned host
+// memory, and the read-out of the device error word.
+//
 // Copy of a step's inputs from pinned host memory into device memory by a
 // kernel.  On a GPU that reads host memory over a coherent chip-to-chip link,
 // many CTAs with 16-byte loads in flight move a few megabytes sooner than one
@@ -33,10 +36,51 @@ __global__ void __launch_bounds__(kCopyThreads) copy_from_host_kernel(uint4* __r
   }
 }
 
+// One thread: the error word to its destination, then (clear) back to zero.
+__global__ void check_errors_kernel(int32_t* err, int32_t* out, int clear) {
+  const int32_t v = *reinterpret_cast<volatile int32_t*>(err);
+  *out = v;
+  if (clear) *err = 0;
+}
+
+// Device address of a pointer that is either device (or managed) memory or
+// page-locked host memory mapped into the device's address space.
+int device_view(const char* fn, void* p, void** out) {
+  cudaPointerAttributes a{};
+  cudaError_t e = cudaPointerGetAttributes(&a, p);
+  if (e != cudaSuccess) {
+    cudaGetLastError();
+    return fail(MEDUSA_ERR_INVALID, "%s: pointer attributes: %s", fn, cudaGetErrorString(e));
+  }
+  if (a.type == cudaMemoryTypeDevice || a.type == cudaMemoryTypeManaged) {
+    *out = p;
+    return MEDUSA_OK;
+  }
+  if (a.type == cudaMemoryTypeHost && a.devicePointer) {
+    *out = a.devicePointer;
+    return MEDUSA_OK;
+  }
+  return fail(MEDUSA_ERR_INVALID, "%s: not device memory nor mapped pinned host memory", fn);
+}
+
 }  // namespace
 }  // namespace medusa
 
 using namespace medusa;
+
+extern "C" int medusa_check_errors(int32_t* err, int32_t* out, int clear, void* stream) {
+  const char* fn = "medusa_check_errors";
+  if (!err || !out) return fail(MEDUSA_ERR_INVALID, "%s: NULL pointer", fn);
+  if ((reinterpret_cast<uintptr_t>(err) | reinterpret_cast<uintptr_t>(out)) % 4)
+    return fail(MEDUSA_ERR_INVALID, "%s: pointers must be 4-byte aligned", fn);
+  void* err_dev = nullptr;
+  void* out_dev = nullptr;
+  if (int rc = device_view(fn, err, &err_dev)) return rc;
+  if (int rc = device_view(fn, out, &out_dev)) return rc;
+  launch_kernel(check_errors_kernel, dim3(1), dim3(1), 0, as_stream(stream), static_cast<int32_t*>(err_dev),
+                static_cast<int32_t*>(out_dev), clear);
+  return check_launch(fn);
+}
 
 extern "C" int medusa_copy_from_host(void* dst, const void* src_host, size_t bytes, void* stream) {
   const char* fn = "medusa_copy_from_host";

@@ -50,6 +50,7 @@ _SIGS = {
     "medusa_tree_attn_splits": (I, [P, P, P, P, P, P, P, P, TREE, I, I, I, I, F, F, I, P, P, SZ, I, P, P]),
     "medusa_tree_attn_tc": (I, [P, P, P, P, P, C.c_int64, P, P, P, TREE, I, I, I, I, F, F, I, P, I, P, P]),
     "medusa_copy_from_host": (I, [P, P, SZ, P]),
+    "medusa_check_errors": (I, [P, P, I, P]),
     "medusa_lm_head_workspace_size": (SZ, [I, I, I]),
     "medusa_lm_head_tiled_bytes": (SZ, [I, I]),
     "medusa_lm_head_tile": (I, [P, P, I, I, P]),
@@ -57,7 +58,7 @@ _SIGS = {
     "medusa_accept_workspace_size": (SZ, [I, I]),
     "medusa_accept": (I, [P, P, TREE, I, I, I, F, F, F, P, P, P, P, P, P, SZ, P, P]),
     "medusa_accept_noalloc": (I, [P, P, TREE, I, I, I, F, F, F, P, P, P, P, P, P, P]),
-    "medusa_kv_compact": (I, [P, P, P, P, P, P, I, I, I, I, I, P, P, P]),
+    "medusa_kv_compact": (I, [P, P, P, P, P, P, I, I, I, I, I, I, P, P, P]),
     "medusa_heads_topk_workspace_size": (SZ, [I, I, I, I, I]),
     "medusa_heads_topk": (I, [P, P, I, P, P, P, P, I, I, I, I, I, P, P, I, P, SZ, P, P]),
     "medusa_heads_topk_candidates": (I, [P, P, I, P, P, P, P, I, I, I, I, I, P, P, I, P, SZ, P, TREE, P, P, P]),
@@ -232,6 +233,14 @@ def medusa_copy_from_host(dst, src_host, stream=None):
            "medusa_copy_from_host")
 
 
+def medusa_check_errors(err, out, clear: bool = False, stream=None):
+    """out (device tensor or pinned CPU tensor, int32, one element) <- the
+    device error word err; with clear, err is then reset to 0.  Enqueued on
+    the stream, no synchronisation."""
+    _check(_lib.medusa_check_errors(_ptr(err), C.c_void_p(out.data_ptr()), 1 if clear else 0, _stream(stream)),
+           "medusa_check_errors")
+
+
 def medusa_tree_attn(q, k_new, v_new, k_cache, v_cache, seq_start, prefix_len, seq_cap,
                      tree: DeviceTree, max_prefix: int, rope_theta: float, scale: float, out,
                      workspace, err=None, stream=None, key_splits=None):
@@ -307,12 +316,12 @@ def medusa_accept_noalloc(logits, tokens, tree: DeviceTree, mode: int, temperatu
                                       _ptr(best_logp), _ptr(err), _stream(stream)), "medusa_accept_noalloc")
 
 
-def medusa_kv_compact(k_cache, v_cache, seq_start, prefix_len, accepted_nodes, accept_len, Kmax: int,
+def medusa_kv_compact(k_cache, v_cache, seq_start, prefix_len, accepted_nodes, accept_len, Kmax: int, T: int,
                       src_slots=None, err=None, stream=None):
     _, H, Dh = k_cache.shape
     B = prefix_len.numel()
     _check(_lib.medusa_kv_compact(_ptr(k_cache), _ptr(v_cache), _ptr(seq_start), _ptr(prefix_len),
-                                  _ptr(accepted_nodes), _ptr(accept_len), B, H, Dh, Kmax, _dtype(k_cache),
+                                  _ptr(accepted_nodes), _ptr(accept_len), B, H, Dh, Kmax, T, _dtype(k_cache),
                                   _ptr(src_slots), _ptr(err), _stream(stream)), "medusa_kv_compact")
 
 

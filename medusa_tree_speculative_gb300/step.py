@@ -224,8 +224,8 @@ class VerifyStep:
 
         def compaction():
             M.medusa_kv_compact(x["k_cache"], x["v_cache"], x["seq_start"], x["prefix_len"],
-                                self.accepted_nodes, self.accept_len, self.tree.K, self.src_slots, self.err,
-                                side)
+                                self.accepted_nodes, self.accept_len, self.tree.K, self.tree.T, self.src_slots,
+                                self.err, side)
 
         if self.attn_order == "after_accept":
             attention()

@@ -84,3 +84,77 @@ def plant_tokens(ot, logits64: np.ndarray, node: int, V: int, rng) -> np.ndarray
 def row_gaps(logits64: np.ndarray) -> np.ndarray:
     s = np.sort(logits64, axis=-1)
     return s[..., -1] - s[..., -2]
+
+
+def gpu_topk_matches_oracle(z_gpu: np.ndarray, topk_gpu: np.ndarray, s: int) -> bool:
+    """The oracle's top-s (value descending, lowest index first among equal
+    values) run on the GPU's own float32 logits equals the GPU's top-s."""
+    import oracle
+
+    return list(oracle.topk_f32(np.ascontiguousarray(z_gpu, np.float32), s)) == list(topk_gpu[:s])
+
+
+def check_accept_on_gpu_logits(ot, logits, tokens, mode, tau, eps, delta, got, rel_tol=1e-4):
+    """Acceptance parity with the oracle run on the GPU's own float32 logits.
+
+    got: host arrays accept_len [B], accepted_nodes [B,K+1], next_root [B],
+    best_node [B], best_logp [B] (typical) from the GPU.
+
+    Greedy decisions are exact comparisons of the same float32 values, so
+    every sequence is compared bit for bit.  A typical decision compares
+    p-hat(token) with min(eps, delta exp(-H)); the GPU forms both in float32
+    (relative error of order 1e-5 at V = 32000: p-hat and exp(-H) are
+    exponentials of log-space quantities with absolute errors near 1e-5), the
+    oracle in double.  A decision whose oracle margin |p-hat - threshold|
+    exceeds `rel_tol` times the larger of the two cannot change between them;
+    neither can the tie-break between accepted nodes of equal depth when their
+    summed log-probabilities differ by more than 1e-4.  (p-hat itself is the
+    oracle's margin with eps = 0, where the threshold is 0.)  Sequences with a
+    closer decision on a reachable node are checked for validity instead
+    (every node of the GPU's path passes up to the margin, and its depth lies
+    between what certainly passes and what may pass).  Returns the number of
+    sequences compared bit for bit."""
+    import oracle
+
+    logits = np.ascontiguousarray(logits, np.float32)
+    tokens = np.ascontiguousarray(tokens, np.int32)
+    B, T, _ = logits.shape
+    r = oracle.accept(logits, tokens, ot, mode, tau, eps, delta)
+    if mode == 1:
+        p_hat = oracle.accept(logits, tokens, ot, mode, tau, 0.0, delta)["node_margin"]
+        tol = rel_tol * np.maximum(p_hat, p_hat - r["node_margin"])
+    else:
+        tol = np.zeros((B, T))
+    exact = 0
+    for b in range(B):
+        mg = r["node_margin"][b]
+        sure = np.zeros(T, bool)
+        maybe = np.zeros(T, bool)
+        sure[0] = maybe[0] = True
+        for c in range(1, T):
+            p = ot.parent[c]
+            sure[c] = sure[p] and mg[c] > tol[b, c]
+            maybe[c] = maybe[p] and mg[c] > -tol[b, c]
+        clear = np.array_equal(sure, maybe)
+        if clear and mode == 1:
+            lp = r["node_logp"][b]
+            dmax = ot.depth[np.nonzero(sure)[0]].max()
+            top = np.sort(lp[(ot.depth == dmax) & sure])[::-1]
+            clear = len(top) < 2 or top[0] - top[1] > 1e-4
+        if clear:
+            assert got["accept_len"][b] == r["accept_len"][b], b
+            assert np.array_equal(got["accepted_nodes"][b], r["accepted_nodes"][b]), b
+            assert got["next_root"][b] == r["next_root"][b], b
+            assert got["best_node"][b] == r["best_node"][b], b
+            if mode == 1:
+                assert abs(float(got["best_logp"][b]) - r["best_logp"][b]) <= 1e-4 * max(1.0, abs(r["best_logp"][b]))
+            exact += 1
+        else:
+            bn = int(got["best_node"][b])
+            assert maybe[bn] and got["accept_len"][b] == ot.depth[bn]
+            assert ot.depth[np.nonzero(sure)[0]].max() <= ot.depth[bn] <= ot.depth[np.nonzero(maybe)[0]].max()
+            path = ancestors(ot.parent, bn)
+            an = got["accepted_nodes"][b]
+            assert list(an[:len(path)]) == path and np.all(an[len(path):] == -1)
+            assert got["next_root"][b] == oracle.topk_f32(logits[b, bn], 1)[0]
+    return exact

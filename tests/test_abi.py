@@ -207,9 +207,14 @@ def test_validation_statuses(M):
     assert L.medusa_lm_head_tile(FAKE + 8, FAKE + (1 << 24), 256, 1000, None) == -1
     assert L.medusa_lm_head_tile(FAKE, FAKE + 4096, 256, 1000, None) == -1
     assert b"overlaps" in L.medusa_last_error()
-    # KV compaction: Kmax above the maximum, misaligned cache
-    assert L.medusa_kv_compact(FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, 1, 4, 64, 9, 1, None, None, None) == -2
-    assert L.medusa_kv_compact(FAKE + 4, FAKE, FAKE, FAKE, FAKE, FAKE, 1, 4, 64, 3, 1, None, None, None) == -1
+    # error-word read-out: NULL or misaligned pointers (rejected before any CUDA call)
+    assert L.medusa_check_errors(None, FAKE, 1, None) == -1
+    assert L.medusa_check_errors(FAKE + 2, FAKE, 1, None) == -1
+    # KV compaction: Kmax above the maximum, misaligned cache, tree rows outside 1..MEDUSA_MAX_T
+    assert L.medusa_kv_compact(FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, 1, 4, 64, 9, 65, 1, None, None, None) == -2
+    assert L.medusa_kv_compact(FAKE + 4, FAKE, FAKE, FAKE, FAKE, FAKE, 1, 4, 64, 3, 65, 1, None, None, None) == -1
+    assert L.medusa_kv_compact(FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, 1, 4, 64, 3, 0, 1, None, None, None) == -1
+    assert L.medusa_kv_compact(FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, 1, 4, 64, 3, 513, 1, None, None, None) == -1
     # heads: s_k above s_max, too-small workspace, K above the maximum
     s = (C.c_int32 * 3)(2, 9, 2)
     assert L.medusa_heads_topk(FAKE, FAKE, 15, FAKE, None, FAKE, s, 3, 1, 256, 1000, 1, FAKE, FAKE, 8,

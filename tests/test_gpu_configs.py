@@ -10,20 +10,20 @@ bench.py runs them (VerifyStep with the attention/compaction side branch):
 Checks against the oracle on samples it computes one by one (two attention
 heads of every sequence, 256 vocabulary rows of the LM head for every tree
 row, the W1 pass in full and 256 vocabulary rows of every head), and
-properties that hold at any size: the accepted path follows the acceptance
-rule on the GPU's own logits wherever the decision is clear of rounding, the
-compacted cache holds exactly the accepted rows, the top-s are the top-s of
-the GPU's own head logits, and the next candidates are filled from them.
+properties that hold at any size: the acceptance equals the oracle's
+acceptance run on the GPU's own logits (bit for bit wherever a typical
+decision is clear of float32 rounding), the compacted cache holds exactly the
+accepted rows, the top-s equal the oracle's top-s of the GPU's own head
+logits, and the next candidates are filled from them.
 """
-import math
-
 import numpy as np
 import pytest
 import torch
 
 import oracle
 from medusa_tree_speculative_gb300 import synth, workloads
-from parity_util import ancestors, as_double, both_trees, to_dev, to_host
+from parity_util import (ancestors, as_double, both_trees, check_accept_on_gpu_logits, gpu_topk_matches_oracle,
+                         to_dev, to_host)
 
 pytestmark = pytest.mark.gpu
 
@@ -46,18 +46,6 @@ def M():
 def _tree_spec(w):
     t = w["tree"]
     return ("cartesian", t[1], t[2]) if t[0] == "cartesian" else ("greedy", w["K"], t[2], t[1])
-
-
-def _typical_decisions(logits_row, tok, tau, eps, delta):
-    """(passes, margin, threshold) of the typical rule in float64 from float32 logits."""
-    z = logits_row.astype(np.float64) / tau
-    m = z.max()
-    lse = m + np.log(np.exp(z - m).sum())
-    lp = z - lse
-    H = -(np.exp(lp) * lp).sum()
-    thr = min(eps, delta * math.exp(-H))
-    p = math.exp(lp[tok])
-    return p > thr, p - thr, thr
 
 
 @pytest.mark.parametrize("name", CONFIGS)
@@ -107,38 +95,16 @@ def test_config_step(M, name):
     assert np.abs(logits[:, cols] - ref).max() <= 2e-2 * np.abs(ref).max()
     logits = logits.reshape(B, T, V)
 
-    # ---- acceptance: the rule on the GPU's own logits, where decisions are clear
+    # ---- acceptance: the oracle's acceptance on the GPU's own logits
     mode = 1 if w["mode"] == "typical" else 0
     tau, eps, delta = w.get("temperature", 1.0), w.get("eps", 0.09), w.get("delta", 0.3)
-    acc_len = to_host(st.accept_len)
-    acc_nodes = to_host(st.accepted_nodes)
-    best = to_host(st.best_node)
-    checked = 0
-    for b in range(B):
-        gam = np.argmax(logits[b], axis=1)
-        ok = np.zeros(T, bool)
-        clear = np.ones(T, bool)
-        ok[0] = True
-        for c in range(1, T):
-            p = ot.parent[c]
-            if mode == 0:
-                passes = tok[b, c] == gam[p]
-            else:
-                passes, margin, thr = _typical_decisions(logits[b, p], tok[b, c], tau, eps, delta)
-                clear[c] = abs(margin) > 1e-4 * thr  # float32 p-hat is far closer than this
-            ok[c] = ok[p] and passes
-        if not clear.all():
-            continue  # a decision within rounding of its threshold: skip the exact check
-        depth_best = max(ot.depth[n] for n in range(T) if ok[n])
-        assert acc_len[b] == depth_best
-        assert ok[best[b]] and ot.depth[best[b]] == depth_best
-        path = ancestors(ot.parent, int(best[b]))
-        assert list(acc_nodes[b, :len(path)]) == path and np.all(acc_nodes[b, len(path):] == -1)
-        assert int(to_host(st.next_root)[b]) == int(gam[best[b]])
-        if mode == 0:
-            assert acc_len[b] >= min(3, ot.K)  # the planted path is accepted
-        checked += 1
-    assert checked >= 1
+    got = {k: to_host(getattr(st, k)) for k in ("accept_len", "accepted_nodes", "next_root", "best_node",
+                                                 "best_logp")}
+    exact = check_accept_on_gpu_logits(ot, logits, tok, mode, tau, eps, delta, got)
+    assert exact >= 0.95 * B
+    if mode == 0:
+        assert np.all(got["accept_len"] >= min(3, ot.K))  # the planted paths are accepted
+    acc_len, acc_nodes, best = got["accept_len"], got["accepted_nodes"], got["best_node"]
 
     # ---- compaction: slot L+j holds tree row a_j (V exact, K rotated)
     vcd, kcd = to_host(dev["v_cache"]), to_host(dev["k_cache"])
@@ -163,8 +129,8 @@ def test_config_step(M, name):
         for k in used:
             ref = oracle.lm_head(np.ascontiguousarray(u[b, k][None]), np.ascontiguousarray(wts["w2"][k][cols]))[0]
             assert np.abs(hl[b, k, cols] - ref).max() <= 2e-2 * np.abs(ref).max()
-            order = np.lexsort((np.arange(V), -hl[b, k].astype(np.float64)))[:s_heads[k]]
-            assert list(tk[b, k, :s_heads[k]]) == list(order)
+            # the oracle's top-s on the GPU's own head logits
+            assert gpu_topk_matches_oracle(hl[b, k], tk[b, k], s_heads[k])
     # ---- next candidates from the GPU's own top-s and root
     nt = to_host(st.next_tokens)
     for b in range(B):

@@ -3,6 +3,8 @@
 (medusa_accept_stats): the per-group records reproduce each row's argmax,
 log-sum-exp and entropy (checked against float64 on the same logits), the
 logits come out bit-identical to medusa_lm_head_verify, and the acceptance
+matches the oracle's acceptance (the decoding-step box of the Medusa paper
+digest, steps 4-5, and its Method item 5) run on the GPU's own logits, and
 gives the same outputs as medusa_accept -- also with the logits not written
 (greedy)."""
 import math
@@ -13,7 +15,7 @@ import torch
 
 import oracle
 from medusa_tree_speculative_gb300 import synth
-from parity_util import ancestors, both_trees, to_dev, to_host
+from parity_util import ancestors, both_trees, check_accept_on_gpu_logits, to_dev, to_host
 
 pytestmark = pytest.mark.gpu
 
@@ -117,6 +119,11 @@ def test_fused_accept_matches_accept(M, mode, write_logits):
     M.medusa_accept_stats(stats, G, lg2 if write_logits else None, tk, dtree, mode, tau, eps, delta, V, *o2, e)
     torch.cuda.synchronize()
     assert int(e.item()) == 0
+    # the oracle decides on the logits the LM head wrote (bit-identical to the
+    # ones the fused epilogue reduced: test_fused_stats_records)
+    got = dict(zip(("accept_len", "accepted_nodes", "next_root", "best_node", "best_logp"), map(to_host, o2)))
+    exact = check_accept_on_gpu_logits(ot, z, tok, mode, tau, eps, delta, got)
+    assert exact == B
     for a_, b_ in zip(o1[:4], o2[:4]):
         assert torch.equal(a_, b_)
     if mode == 0:

@@ -18,7 +18,8 @@ import torch
 
 import oracle
 from medusa_tree_speculative_gb300 import synth
-from parity_util import (ancestors, as_double, both_trees, plant_tokens, row_gaps, to_dev, to_host)
+from parity_util import (ancestors, as_double, both_trees, gpu_topk_matches_oracle, plant_tokens, row_gaps, to_dev,
+                         to_host)
 
 pytestmark = pytest.mark.gpu
 
@@ -415,6 +416,31 @@ def test_accept_bad_token_flag(M):
     assert g["accept_len"][0] >= 0
 
 
+def test_check_errors_reads_and_clears(M):
+    """medusa_check_errors: the word raised by a bad token reaches pinned host
+    memory and device memory in stream order; with clear the word is zero
+    again for the next step."""
+    ot, dtree = both_trees(M, ("cartesian", (2, 2), None))
+    logits = torch.zeros((1, ot.T, 10), dtype=torch.float32, device="cuda")
+    tokens = to_dev(np.array([[0, 3, 99, 1, 1, 1, 1]], np.int32))
+    i32 = dict(dtype=torch.int32, device="cuda")
+    outs = [torch.zeros(1, **i32), torch.zeros((1, ot.K + 1), **i32), torch.zeros(1, **i32), torch.zeros(1, **i32),
+            torch.zeros(1, dtype=torch.float32, device="cuda")]
+    ws = torch.zeros(M.medusa_accept_workspace_size(1, ot.T), dtype=torch.uint8, device="cuda")
+    e = err_flag()
+    host = torch.full((1,), -1, dtype=torch.int32).pin_memory()
+    dev_out = torch.full((1,), -1, **i32)
+    s = torch.cuda.current_stream()
+    M.medusa_accept(logits, tokens, dtree, 1, 1.0, 0.09, 0.3, *outs, ws, e)
+    M.medusa_check_errors(e, dev_out, clear=False, stream=s)
+    M.medusa_check_errors(e, host, clear=True, stream=s)
+    torch.cuda.synchronize()
+    assert int(host[0]) == 1 and int(dev_out.item()) == 1  # MEDUSA_DEVERR_TOKEN
+    assert int(e.item()) == 0
+    with pytest.raises(M.MedusaError, match="INVALID"):
+        M.medusa_check_errors(e, torch.zeros(1, dtype=torch.int32))  # pageable host memory
+
+
 # ------------------------------------------------------------ KV compaction
 
 @pytest.mark.parametrize("dt", ["bf16", "f32"])
@@ -440,7 +466,7 @@ def test_kv_compact(M, dt):
     kd, vd, pld = to_dev(kc), to_dev(vc), to_dev(pl)
     src = torch.zeros((B, K + 1), dtype=torch.int32, device="cuda")
     e = err_flag()
-    M.medusa_kv_compact(kd, vd, to_dev(st), pld, to_dev(acc_nodes), to_dev(acc_len), K, src, e)
+    M.medusa_kv_compact(kd, vd, to_dev(st), pld, to_dev(acc_nodes), to_dev(acc_len), K, T, src, e)
     torch.cuda.synchronize()
     assert int(e.item()) == 0
     ko, vo, plo = kc.copy(), vc.copy(), pl.copy()
@@ -457,12 +483,33 @@ def test_kv_compact_in_place_hazard(M):
     st, pl = np.array([0], np.int64), np.array([5], np.int32)
     an, al = np.array([[0, 2, 3, -1]], np.int32), np.array([2], np.int32)
     kd, vd, pld = to_dev(kc), to_dev(vc), to_dev(pl)
-    M.medusa_kv_compact(kd, vd, to_dev(st), pld, to_dev(an), to_dev(al), 3)
+    M.medusa_kv_compact(kd, vd, to_dev(st), pld, to_dev(an), to_dev(al), 3, 7)
     ko, vo = kc.copy(), vc.copy()
     oracle.kv_compact(ko, vo, st, pl.copy(), an, al, 3)
     torch.cuda.synchronize()
     assert np.array_equal(to_host(kd), ko) and np.array_equal(to_host(vd), vo)
     assert to_host(pld)[0] == 8
+
+
+def test_kv_compact_node_outside_tree(M):
+    """An accepted node at or past the tree's T rows (here 400 with a 7-row
+    tree) raises MEDUSA_DEVERR_NODE and leaves that sequence untouched; a
+    valid sequence in the same call is still compacted."""
+    H, Dh = 2, 64
+    kc = np.arange(40 * H * Dh, dtype=np.float32).reshape(40, H, Dh)
+    vc = -kc
+    st, pl = np.array([0, 20], np.int64), np.array([5, 5], np.int32)
+    an = np.array([[0, 2, 400, -1], [0, 2, 5, -1]], np.int32)
+    al = np.array([2, 2], np.int32)
+    kd, vd, pld = to_dev(kc), to_dev(vc), to_dev(pl)
+    e = err_flag()
+    M.medusa_kv_compact(kd, vd, to_dev(st), pld, to_dev(an), to_dev(al), 3, 7, None, e)
+    torch.cuda.synchronize()
+    assert int(e.item()) & 2  # MEDUSA_DEVERR_NODE
+    ko, vo = kc.copy(), vc.copy()
+    oracle.kv_compact(ko[20:], vo[20:], st[1:] - 20, pl[1:].copy(), an[1:], al[1:], 3)
+    assert np.array_equal(to_host(kd), ko) and np.array_equal(to_host(vd), vo)
+    assert list(to_host(pld)) == [5, 8]
 
 
 # ------------------------------------------------------------------- heads
@@ -520,9 +567,8 @@ def test_heads_topk(M, case):
             scale = np.abs(z_ref[b, k]).max()
             err = np.abs(zg[b, k] - z_ref[b, k]).max()
             assert err <= TOL[dt]["logit"] * scale, f"head logit error {err} (max {scale})"
-            # validity: the GPU's top-s is the exact top-s of its own logits
-            order = np.lexsort((np.arange(V), -zg[b, k].astype(np.float64)))[:s[k]]
-            assert list(tg[b, k, :s[k]]) == list(order)
+            # the oracle's top-s of the GPU's own logits equals the GPU's top-s
+            assert gpu_topk_matches_oracle(zg[b, k], tg[b, k], s[k])
             assert np.all(tg[b, k, s[k]:] == -1)
             # parity with the oracle where the ranking is decided by more than
             # the GPU's rounding error
@@ -592,8 +638,7 @@ def test_heads_split(M, case):
             scale = np.abs(z_ref[b, k]).max()
             err = np.abs(zg[b, k] - z_ref[b, k]).max()
             assert err <= TOL[dt]["logit"] * scale, f"head logit error {err} (max {scale})"
-            order = np.lexsort((np.arange(V), -zg[b, k].astype(np.float64)))[:s[k]]
-            assert list(tg[b, k, :s[k]]) == list(order)
+            assert gpu_topk_matches_oracle(zg[b, k], tg[b, k], s[k])
             assert np.all(tg[b, k, s[k]:] == -1)
 
 

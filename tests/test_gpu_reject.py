@@ -67,13 +67,26 @@ def test_rejection_parity(M, spec, V, tau):
         pick = rng.integers(0, 4, B)
         tokens[:, n] = np.where(rng.random(B) < 0.4, top[np.arange(B), pick], rng.integers(0, V, B))
     u = rng.random((B, T, 17)).astype(np.float32)
+    # The oracle's margin of a sequence is the smallest distance of any of its
+    # decisions from the other outcome: |u q(x) - p(x)| / max(p(x), q(x)) for
+    # an acceptance test, and |u - F| for the final inverse-CDF draw, with F
+    # the nearer bound of the drawn token's cumulative interval.  The GPU's
+    # probabilities are float32 exponentials over sums of <= 32000 terms
+    # (relative error below 1e-6; the cumulative sums are carried in double),
+    # so a decision whose margin exceeds 1e-5 cannot go the other way.  A
+    # sequence with a closer decision gets fresh uniforms (the oracle alone
+    # decides which), at most 20 times.
+    for _ in range(20):
+        r = oracle.rejection_tree(logits, draft, tokens, ot, tau, u)
+        close = r["margin"] <= 1e-5
+        if not close.any():
+            break
+        u[close] = rng.random((int(close.sum()), T, 17)).astype(np.float32)
+    r = oracle.rejection_tree(logits, draft, tokens, ot, tau, u)
+    clear = r["margin"] > 1e-5
+    assert clear.mean() >= 0.95
     al, an, nt, err = _run(M, dtree, logits, draft, tokens, tau, u)
     assert err == 0
-    r = oracle.rejection_tree(logits, draft, tokens, ot, tau, u)
-    # decisions closer than 1e-6 (relative for a test, absolute for the final
-    # draw) may round either way between float32 and double
-    clear = r["margin"] > 1e-6
-    assert clear.mean() >= 0.75
     for b in np.nonzero(clear)[0]:
         assert al[b] == r["accept_len"][b]
         assert np.array_equal(an[b], r["accepted_nodes"][b])

@@ -6,8 +6,9 @@ that must not call cudaMalloc because it can synchronise the device.  For
 them, medusa_accept_noalloc takes no workspace and uses a fixed scratch array
 inside the library.  This test calls it through the C ABI twice in a row, on
 different inputs (typical acceptance, then greedy), and checks each result
-against medusa_accept on the same inputs: integer outputs bit-exact, the
-summed log-probability within 1e-6.
+against medusa_accept on the same inputs (integer outputs bit-exact, the
+summed log-probability within 1e-6) and against the oracle's acceptance on
+the same logits (integer outputs bit-exact).
 
 This file is collected last so that a run stopping at the first failure has
 already run every other test.  It also passes on its own in a fresh process.
@@ -15,6 +16,8 @@ already run every other test.  It also passes on its own in a fresh process.
 import numpy as np
 import pytest
 import torch
+
+from parity_util import both_trees, check_accept_on_gpu_logits, to_host
 
 pytestmark = pytest.mark.gpu
 
@@ -32,10 +35,8 @@ def M():
 
 
 def _tree(M):
-    from medusa_tree_speculative_gb300.synth import accuracy_table
-
-    paths, plen = M.medusa_tree_greedy(accuracy_table(4, 10), 64)
-    return M.DeviceTree(M.medusa_tree_compile(paths, plen, 4))
+    """The 64-node greedy tree, as the oracle's tree and as the library's."""
+    return both_trees(M, ("greedy", 4, 10, 64))
 
 
 def _inputs(tree, B, V, mode, seed):
@@ -64,7 +65,7 @@ def _outputs(B, K):
 
 
 def test_accept_noalloc_matches_accept_on_two_calls(M):
-    tree = _tree(M)
+    ot, tree = _tree(M)
     B, V = 3, 32000
     for mode, seed in ((1, 11), (0, 12)):
         logits, tokens = _inputs(tree, B, V, mode, seed)
@@ -83,6 +84,8 @@ def test_accept_noalloc_matches_accept_on_two_calls(M):
             assert torch.equal(ref[key], got[key]), key
         assert torch.allclose(ref["best_logp"], got["best_logp"], rtol=0, atol=1e-6)
         assert int(got["accept_len"].max().item()) >= 1  # the planted paths were taken
+        host = {k: to_host(v) for k, v in got.items()}
+        assert check_accept_on_gpu_logits(ot, to_host(logits), to_host(tokens), mode, 0.7, 0.09, 0.3, host) == B
 
 
 def test_accept_noalloc_rejects_oversize(M):
