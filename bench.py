@@ -282,7 +282,9 @@ def run_native(args, w, rank, world, local_rank):
     xh = synth.make_step(w, T, seed)
     dt = w["dtype"]
     wd = {k: (None if v is None else step.host_to_torch(v, dt).to(dev)) for k, v in wts.items()}
-    del wts
+    keep_host = world == 1 and not args.no_cpu_baseline  # the CPU baseline runs on the same inputs
+    if not keep_host:
+        del wts
     x = {}
     for k, v in xh.items():
         x[k] = step.host_to_torch(v, dt).to(dev) if v.dtype in (np.uint16, np.float32) else torch.from_numpy(v).to(dev)
@@ -371,7 +373,8 @@ def run_native(args, w, rank, world, local_rank):
     if args.loop_steps > 0 and world == 1:
         dloop = measure_loop(args, w, dev, torch, M)
 
-    return dict(ms_step=ms_step, ms_events_step=ms_events / args.steps, per_call_ms=per_call, clocks=clocks,
+    return dict(host_inputs=(wts, xh) if keep_host else None,
+                ms_step=ms_step, ms_events_step=ms_events / args.steps, per_call_ms=per_call, clocks=clocks,
                 dloop=dloop, rej=rej,
                 T=T, s_heads=st.s_heads, L_list=L_list, accept_len=accept_len, e2e=e2e,
                 launches=st.launches_per_step * args.steps, tree=ht,
@@ -540,19 +543,22 @@ def measure_e2e(args, w, st, x, xh, prefix0, s, s2, s3, torch, M):
 
 # ------------------------------------------------------------- CPU oracle --
 
-class OracleSample:
-    """The CPU oracle on a bounded sample of one step, scaled to a full step:
-    attention on 1/frac of the heads, the LM head and W2 on 1/frac of the
-    vocabulary rows (each timed and scaled by frac), W1, acceptance (on a full
-    [T, V] logit array), compaction and candidate fill in full.  Inputs are
-    drawn once; each call times only the oracle."""
+class OracleStep:
+    """One full verify step of the CPU oracle on the bench workload's own
+    inputs (the same seeded weights and activations as the GPU run), chained
+    as the GPU chains it: tree attention over every head, the LM head over
+    every tree row and the whole vocabulary, the acceptance on the oracle's
+    own logits, compaction, both head projections at the accepted node and
+    the candidate fill.  `seqs` < B keeps only the first sequences of the
+    batch (a sample of whole sequences; the step's time scales by B / seqs).
+    Inputs are drawn once; each call times only the oracle."""
 
-    def __init__(self, w, frac=32, seed=0):
+    def __init__(self, w, seed=0, seqs=None, wts=None, xh=None):
         import oracle
         from medusa_tree_speculative_gb300 import synth
 
         oracle.build()
-        self.w, self.frac = w, frac
+        self.w = w
         if w["tree"][0] == "cartesian":
             s = list(w["tree"][1])
             n = w["tree"][2] or sum(math.prod(s[:k]) for k in range(1, len(s) + 1))
@@ -560,71 +566,78 @@ class OracleSample:
         else:
             paths, plen = oracle.tree_greedy(synth.accuracy_table(w["K"], w["tree"][2]), w["tree"][1])
         self.ot = ot = oracle.tree_compile(paths, plen, paths.shape[1])
-        T, B, H, d, V = ot.T, w["B"], w["H"], w["d"], w["V"]
-        dt = w["dtype"]
-        self.hs = max(1, H // frac)
-        self.vs = max(1, V // frac)
-        self.x = synth.make_step(dict(w, H=self.hs), T, seed)
-        self.w_lm = synth.normal(seed, "w_lm_sample", (self.vs, d), 1 / math.sqrt(d), dt)
+        self.B = w["B"]
+        self.nb = nb = min(self.B, seqs or self.B)
+        wts = wts if wts is not None else synth.make_weights(w, seed)
+        x = xh if xh is not None else synth.make_step(w, ot.T, seed)
         s_heads = [int(ot.s[k]) if k < ot.K else 0 for k in range(w["K"])]
-        self.k_used = [k for k in range(w["K"]) if s_heads[k] > 0]
-        self.s_used = [s_heads[k] for k in self.k_used]
-        ku = len(self.k_used)
-        self.w1 = synth.normal(seed, "w1_sample", (ku, d, d), 1 / math.sqrt(d), dt)
-        self.w2 = synth.normal(seed, "w2_sample", (ku, self.vs, d), 1 / math.sqrt(d), dt)
-        self.w2_one = np.ascontiguousarray(self.w2[:, :1])
-        self.logits = synth.normal(seed, "logits_sample", (B, T, V), 2.0, "f32")
+        self.s_heads = s_heads
+        self.s_max = max(1, max(s_heads))
+        self.w_lm, self.w1, self.w2 = wts["w_lm"], wts["w1"], wts["w2"]
+        end = int(x["seq_start"][nb - 1] + x["seq_cap"][nb - 1])  # cache rows of the first nb sequences
+        self.x = {k: np.ascontiguousarray(v[:nb]) for k, v in x.items() if k not in ("k_cache", "v_cache")}
+        self.k_cache = np.ascontiguousarray(x["k_cache"][:end])
+        self.v_cache = np.ascontiguousarray(x["v_cache"][:end])
 
     def step(self):
+        """Seconds for one step of the sampled sequences, per part."""
         import oracle
 
         w, x, ot = self.w, self.x, self.ot
-        H, V = w["H"], w["V"]
+        nb, T, d, V = self.nb, ot.T, w["d"], w["V"]
         t_all = {}
-        kc, vc = x["k_cache"].copy(), x["v_cache"].copy()
+        kc, vc = self.k_cache.copy(), self.v_cache.copy()
         t = time.perf_counter()
         oracle.tree_attn(x["q"], x["k_new"], x["v_new"], kc, vc, x["seq_start"], x["prefix_len"], ot)
-        t_all["tree_attn"] = (time.perf_counter() - t) * (H / self.hs)
+        t_all["tree_attn"] = time.perf_counter() - t
         t = time.perf_counter()
-        oracle.lm_head(x["hidden"], self.w_lm)
-        t_all["lm_head_verify"] = (time.perf_counter() - t) * (V / self.vs)
+        logits = oracle.lm_head(x["hidden"].reshape(nb * T, d), self.w_lm)
+        t_all["lm_head_verify"] = time.perf_counter() - t
         mode = 1 if w["mode"] == "typical" else 0
         t = time.perf_counter()
-        r = oracle.accept(self.logits, x["tokens"], ot, mode, w.get("temperature", 1.0), w.get("eps", 0.09),
-                          w.get("delta", 0.3))
+        r = oracle.accept(logits.astype(np.float32).reshape(nb, T, V), x["tokens"], ot, mode,
+                          w.get("temperature", 1.0), w.get("eps", 0.09), w.get("delta", 0.3))
         t_all["accept"] = time.perf_counter() - t
         t = time.perf_counter()
         oracle.kv_compact(kc, vc, x["seq_start"], x["prefix_len"].copy(), r["accepted_nodes"], r["accept_len"],
                           ot.K)
-        t_all["kv_compact"] = (time.perf_counter() - t) * (H / self.hs)
+        t_all["kv_compact"] = time.perf_counter() - t
         t = time.perf_counter()
-        _, tk, _ = oracle.heads(x["hidden"], r["best_node"], self.w1, None, self.w2, self.s_used, max(self.s_used))
-        t_heads = time.perf_counter() - t
-        # W1's share: the same call with a one-row vocabulary
-        t = time.perf_counter()
-        oracle.heads(x["hidden"], r["best_node"], self.w1, None, self.w2_one, [1] * len(self.k_used), 1)
-        t_w1 = time.perf_counter() - t
-        t_all["heads_topk"] = t_w1 + max(0.0, t_heads - t_w1) * (V / self.vs)
+        _, tk, _ = oracle.heads(x["hidden"], r["best_node"], self.w1, None, self.w2, self.s_heads, self.s_max)
+        t_all["heads_topk"] = time.perf_counter() - t
         t = time.perf_counter()
         oracle.build_candidates(r["next_root"], tk, ot)
         t_all["build_candidates"] = time.perf_counter() - t
         return sum(t_all.values()), t_all
 
 
-def cpu_baseline(w, reps=3):
-    smp = OracleSample(w)
+def oracle_seqs(w) -> int:
+    """Sequences of the batch in one timed oracle step: all of them, except
+    for batches whose full step would take well over half a minute on one
+    core (the 33B-shaped batch of four: one sequence)."""
+    return 1 if w["B"] > 1 and w["d"] * w["V"] * w["B"] > 4 * 4096 * 32000 else w["B"]
+
+
+def cpu_baseline(w, wts=None, xh=None, budget_s=30.0):
+    """The oracle as it stands, single-threaded, timed on full steps of the
+    bench workload (whole sequences; every head, every vocabulary row)."""
+    orc = OracleStep(w, seqs=oracle_seqs(w), wts=wts, xh=xh)
     vals = []
     parts = None
-    for _ in range(reps):
-        tot, parts = smp.step()
-        vals.append(tot)
-    sec = statistics.median(vals)
+    t0 = time.perf_counter()
+    while not vals or (len(vals) < 3 and time.perf_counter() - t0 + vals[-1] < budget_s):
+        sec, parts = orc.step()
+        vals.append(sec)
+    sec = statistics.median(vals) * orc.B / orc.nb  # seconds per step of the whole batch
+    sample = (f"single-threaded C oracle on one host core, full verify steps (every attention head, every "
+              f"vocabulary row of the LM head and of each head's W2, acceptance on the oracle's own logits); "
+              f"median of {len(vals)} step(s)")
+    if orc.nb < orc.B:
+        sample += f"; {orc.nb} of the batch's {orc.B} sequences per step, time scaled by {orc.B}/{orc.nb}"
     return {"value": 1.0 / sec, "unit": UNIT, "cores": 1, "kind": "oracle",
-            "sample": ("single-threaded C oracle on the host; per step: attention on 1/32 of the heads and the "
-                       "LM head and W2 on 1/32 of the vocabulary rows, timed and scaled x32; W1, acceptance "
-                       "(on a full [T,V] logit array), compaction and candidate fill in full; "
-                       f"median of {reps} sampled steps; host has {os.cpu_count()} cores"),
-            "seconds_per_step_est": sec, "parts_s": {k: round(v, 4) for k, v in parts.items()}}
+            "sample": sample + f"; host has {os.cpu_count()} cores",
+            "seconds_per_step": sec, "steps_timed": len(vals),
+            "parts_s": {k: round(v, 4) for k, v in parts.items()}}
 
 
 def max_over_ranks(x: float, device) -> float:
@@ -645,35 +658,41 @@ def whole_job_value(world: int, steps: int, ms_total: float) -> float:
     return world * steps * 1e3 / ms_total
 
 
-def run_reference(args, w, rank, world):
-    """--impl reference: the CPU oracle as it stands, on host cores."""
+def run_reference(args, w, rank, world, budget_s=60.0):
+    """--impl reference: the CPU oracle as it stands, single-threaded, on full
+    verify steps of the same workload.  A full step takes seconds, so the arm
+    times as many of the requested steps as fit in about a minute (at least
+    one) and reports that count: every number it prints is measured."""
     if rank != 0:
         return
     import oracle
 
     oracle.build()
-    smp = OracleSample(w, frac=64)
-    for _ in range(min(args.warmup, 1)):
-        smp.step()
+    orc = OracleStep(w, seqs=oracle_seqs(w))
     vals = []
-    t0 = time.perf_counter()
     parts = None
-    for _ in range(args.steps):
-        sec, parts = smp.step()
+    t0 = time.perf_counter()
+    while len(vals) < max(1, args.steps):
+        sec, parts = orc.step()
         vals.append(sec)
+        if time.perf_counter() - t0 + sec > budget_s:
+            break
     wall = time.perf_counter() - t0
-    sec = statistics.mean(vals)
+    sec = statistics.mean(vals) * orc.B / orc.nb
     v = 1.0 / sec
+    sample = (f"full verify steps of the single-threaded C oracle on one host core (every attention head, every "
+              f"vocabulary row, acceptance on the oracle's own logits); {len(vals)} of the {args.steps} requested "
+              f"steps timed in {wall:.1f} s wall (a full step takes {sec:.3g} s), no warm-up step")
+    if orc.nb < orc.B:
+        sample += f"; {orc.nb} of the batch's {orc.B} sequences per step, time scaled by {orc.B}/{orc.nb}"
     line = {
         "impl": "reference", "metric": METRIC, "value": v, "unit": UNIT, "n_gpus": args.gpus,
-        "steps": args.steps, "warmup": args.warmup, "ms_per_step": sec * 1e3, "higher_is_better": True,
+        "steps": len(vals), "warmup": 0, "steps_requested": args.steps, "warmup_requested": args.warmup,
+        "ms_per_step": sec * 1e3, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
         "config": config_dict(w),
         "cpu_baseline": {"value": v, "unit": UNIT, "cores": 1, "kind": "oracle",
-                         "sample": ("each step: attention on 1/64 of the heads (at least one), LM head and W2 on "
-                                    "1/64 of the vocabulary rows (scaled up), the rest in full; single-threaded C "
-                                    "oracle; "
-                                    f"{args.steps} steps in {wall:.1f} s wall")},
+                         "sample": sample + f"; host has {os.cpu_count()} cores"},
         "e2e": {"value": v, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
         "parts_s": {k: round(x, 4) for k, x in parts.items()},
     }
@@ -754,7 +773,7 @@ def main():
     if r["rej"] is not None:
         line["rejection_accept"] = r["rej"]
     if world == 1 and not args.no_cpu_baseline:
-        line["cpu_baseline"] = cpu_baseline(w)
+        line["cpu_baseline"] = cpu_baseline(w, *r["host_inputs"])
     print(json.dumps(line), flush=True)
 
 

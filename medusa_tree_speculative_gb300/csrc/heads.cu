@@ -20,6 +20,12 @@
 //             warps kept while streaming (one per warp and sequence, in shared
 //             memory), and the last CTA of a head to finish merges every
 //             CTA's list into topk (value descending, index ascending).
+// With several sequences (bf16) the dot products run on the tensor cores
+// instead (mma.sync m16n8k16: the sequences as M, eight weight rows as N): a
+// CTA takes eight rows at a time and splits the hidden dimension over its
+// warps, so each 16-byte weight load feeds every sequence without being
+// widened to fp32, and the sequences' vectors are read once per eight rows
+// instead of once per row.
 // Rows are handed out at run time, not split up front: W1's row quads and
 // each head's W2 rows come from atomic counters, the next one requested
 // before the current one is streamed.  CTAs whose SMs are busy with other
@@ -119,6 +125,53 @@ MDEV void dot_rows(const TE* w, const TE* const* x, int nvec, int B, int lane, f
   }
 }
 
+// C (16 sequences x 8 weight rows, the m16n8k16 accumulator fragment) +=
+// X . W^T over the 32-column chunks [c0, c1) of the hidden dimension.  Lane
+// (g, t) = (lane / 4, lane % 4) streams 16 bytes of weight row g (columns
+// 32 ch + 8 t .. + 8) per chunk and the same columns of sequences g and g + 8
+// (xlo, xhi: null past B); its eight columns feed two MMAs.  In each MMA
+// lane t holds the k slots {2t, 2t+1, 2t+8, 2t+9} of both operands, which
+// here are columns {8t, 8t+1, 8t+2, 8t+3} (first MMA) and {8t+4 .. 8t+7}
+// (second): one permutation of k shared by the two operands, so every dot
+// product is unchanged.  wrow, xlo, xhi already include the lane's 8 t.
+template <bool HI>
+MDEV void mma_rows8(const uint16_t* wrow, const uint16_t* xlo, const uint16_t* xhi, int c0, int c1, float* c) {
+  for (int cb = c0; cb < c1; cb += UNROLL) {
+    uint4 wv[UNROLL], xl[UNROLL], xh[UNROLL];
+#pragma unroll
+    for (int u = 0; u < UNROLL; ++u) {
+      const int ch = cb + u;
+      if (ch < c1) {
+        wv[u] = ldg_stream(wrow + ch * 32);
+        xl[u] = xlo ? ldg_v4(xlo + ch * 32) : make_uint4(0, 0, 0, 0);
+        if (HI) xh[u] = xhi ? ldg_v4(xhi + ch * 32) : make_uint4(0, 0, 0, 0);
+      }
+    }
+#pragma unroll
+    for (int u = 0; u < UNROLL; ++u) {
+      if (cb + u < c1) {
+        const uint32_t a0[4] = {xl[u].x, HI ? xh[u].x : 0u, xl[u].y, HI ? xh[u].y : 0u};
+        mma_bf16_16816(c, a0, wv[u].x, wv[u].y);
+        const uint32_t a1[4] = {xl[u].z, HI ? xh[u].z : 0u, xl[u].w, HI ? xh[u].w : 0u};
+        mma_bf16_16816(c, a1, wv[u].z, wv[u].w);
+      }
+    }
+  }
+}
+
+// Element (sequence s, row r) of the warps' summed fragments, or, for the
+// thread that calls it, which (lane, register) holds it.
+MDEV float frag_sum(const float4 (*part)[32], int s, int r) {
+  const int src = 4 * (s & 7) + (r >> 1), reg = ((s >> 3) << 1) + (r & 1);
+  float y = 0.f;
+#pragma unroll
+  for (int w = 0; w < kWarps; ++w) {
+    const float4 v = part[w][src];
+    y += reg == 0 ? v.x : reg == 1 ? v.y : reg == 2 ? v.z : v.w;
+  }
+  return y;
+}
+
 // ---------------------------------------------------------------- W1 pass --
 template <typename TE, int NB>
 __global__ void __launch_bounds__(kWarps * 32) heads_w1_kernel(const __grid_constant__ HeadsArgs a) {
@@ -185,6 +238,64 @@ __global__ void __launch_bounds__(kWarps * 32) heads_w1_kernel(const __grid_cons
     if (threadIdx.x == 0) s_q = qn;  // every thread read the current quad before the barrier above
     __syncthreads();
     q = s_q;
+  }
+}
+
+// W1 on the tensor cores (bf16, several sequences): eight stacked W1 rows per
+// CTA at a time, handed out from the same counter as the row quads above,
+// the hidden dimension split over the eight warps; the warps' fragments meet
+// in shared memory and one thread per (sequence, row) applies the epilogue.
+template <bool HI>
+__global__ void __launch_bounds__(kWarps * 32) heads_w1_mma_kernel(const __grid_constant__ HeadsArgs a) {
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int g = lane >> 2, t = lane & 3;
+  __shared__ float4 part[2][kWarps][32];
+  __shared__ int s_q[2];
+  if (blockIdx.x == 0 && threadIdx.x < a.nused) {  // for w2_topk (as in heads_w1_kernel)
+    a.counters[threadIdx.x] = 0;
+    a.rowctr[threadIdx.x] = 0;
+    if (threadIdx.x == 0) *a.tickets = 0;
+    if (threadIdx.x == 0 && a.heads_done) *a.heads_done = 0;
+  }
+  // h_b = hidden[b][last_node[b]]; an out-of-range node reads row 0 and raises the error bit
+  auto seq_row = [&](int b) -> const uint16_t* {
+    int n = a.last_node[b];
+    if (n < 0 || n >= a.T) {
+      if (blockIdx.x == 0) set_err(a.err, MEDUSA_DEVERR_NODE);
+      n = 0;
+    }
+    return static_cast<const uint16_t*>(a.hidden) + ((int64_t)b * a.T + n) * a.d;
+  };
+  const uint16_t* xlo = g < a.B ? seq_row(g) + 8 * t : nullptr;
+  const uint16_t* xhi = HI && g + 8 < a.B ? seq_row(g + 8) + 8 * t : nullptr;
+  // the epilogue thread's sequence (s, row r of the eight)
+  const int es = threadIdx.x >> 3, er = threadIdx.x & 7;
+  const uint16_t* xe = es < a.B ? seq_row(es) : nullptr;
+  const uint16_t* W = static_cast<const uint16_t*>(a.w1);
+  const int nch = a.d / 32;
+  const int c0 = warp * nch / kWarps, c1 = (warp + 1) * nch / kWarps;
+  const int64_t units = (int64_t)a.nused * a.d / 8;
+  if (threadIdx.x == 0) s_q[0] = atomicAdd(a.w1ctr, 1);
+  __syncthreads();
+  int64_t q = s_q[0];
+  for (int it = 0; q < units; ++it) {
+    int qn = 0;
+    if (threadIdx.x == 0) qn = atomicAdd(a.w1ctr, 1);  // the next unit; waited for after this one's loads
+    const int64_t r0 = q * 8;  // first stacked row; eight rows never straddle two heads (d % 8 == 0)
+    const int slot = (int)(r0 / a.d), j0 = (int)(r0 % a.d), k = a.heads[slot];
+    float c[4] = {0.f, 0.f, 0.f, 0.f};
+    mma_rows8<HI>(W + ((int64_t)k * a.d + j0 + g) * a.d + 8 * t, xlo, xhi, c0, c1, c);
+    part[it & 1][warp][lane] = make_float4(c[0], c[1], c[2], c[3]);
+    if (threadIdx.x == 0) s_q[(it + 1) & 1] = qn;
+    __syncthreads();
+    if (xe) {
+      const int j = j0 + er;
+      float y = frag_sum(part[it & 1], es, er);
+      if (a.b1) y += bf16_bits_to_f32(static_cast<const uint16_t*>(a.b1)[(int64_t)k * a.d + j]);
+      const float silu = y / (1.f + expf(-y));
+      static_cast<uint16_t*>(a.u)[((int64_t)es * a.K + k) * a.d + j] = f32_to_bf16_bits(silu + bf16_bits_to_f32(xe[j]));
+    }
+    q = s_q[(it + 1) & 1];
   }
 }
 
@@ -268,7 +379,10 @@ MDEV void block_select(TopList<S>& L, float (*wv)[S], int (*wi)[S], float* ov, i
 }
 
 // ------------------------------------------------------- W2 pass + top-s --
-template <typename TE, int NB, int S>
+// MMA (bf16, several sequences): the rows stream through mma_rows8 in units
+// of eight per CTA (the hidden dimension split over the warps), and one
+// thread per sequence keeps that sequence's running top S (list 0).
+template <typename TE, int NB, int S, bool MMA = false>
 __global__ void __launch_bounds__(kWarps * 32) heads_w2_topk_kernel(const __grid_constant__ HeadsArgs a) {
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   __shared__ float wv[32][S];
@@ -291,21 +405,19 @@ __global__ void __launch_bounds__(kWarps * 32) heads_w2_topk_kernel(const __grid
   const int slot = s_ticket % a.nused, part = s_ticket / a.nused;
   const int k = a.heads[slot];
 
-  const TE* x[NB];
-#pragma unroll
-  for (int b = 0; b < NB; ++b) {
+  auto seq_x = [&](int b) -> const TE* {
     const int bb = b < a.B ? b : 0;
     int64_t row = bb;
     if (a.u_node) {  // an out-of-range node reads row 0 of the sequence and raises the error bit
       int n = a.u_node[bb];
       if (n < 0 || n >= a.T) {
-        if (threadIdx.x == 0 && blockIdx.x == 0) set_err(a.err, MEDUSA_DEVERR_NODE);
+        if (blockIdx.x == 0) set_err(a.err, MEDUSA_DEVERR_NODE);
         n = 0;
       }
       row = (int64_t)bb * a.T + n;
     }
-    x[b] = static_cast<const TE*>(a.u) + (row * a.K + k) * a.d;
-  }
+    return static_cast<const TE*>(a.u) + (row * a.K + k) * a.d;
+  };
   const TE* W = static_cast<const TE*>(a.w2) + (int64_t)k * a.V * a.d;
   const int nvec = a.d / Vec<TE>::N;
   // this head's rows in groups of GR = kWarps * RW (RW consecutive rows per
@@ -323,31 +435,75 @@ __global__ void __launch_bounds__(kWarps * 32) heads_w2_topk_kernel(const __grid
     li[warp][e / S][e % S] = 0x7fffffff;
   }
   __syncthreads();
-  int g = s_g[0];
-  for (int it = 0; g < ngroups; ++it) {
-    int gn = ngroups;
-    if (threadIdx.x == 0) gn = atomicAdd(ctr, 1);  // the next group; waited for after this one's loads
-    const int jb = g * GR + warp * RW;
-    const int je = min(a.V, jb + RW);
-    for (int j = jb; j < je; ++j) {
-      float acc[NB];
+  if constexpr (MMA) {
+    static_assert(sizeof(TE) == 2 && (NB == 8 || NB == 16), "tensor-core rows: bf16, 8 or 16 sequences");
+    constexpr bool HI = NB == 16;
+    __shared__ float4 part[2][kWarps][32];
+    const int gl = lane >> 2, t = lane & 3;
+    const TE* xlo = gl < a.B ? seq_x(gl) + 8 * t : nullptr;
+    const TE* xhi = HI && gl + 8 < a.B ? seq_x(gl + 8) + 8 * t : nullptr;
+    const int nch = a.d / 32;
+    const int c0 = warp * nch / kWarps, c1 = (warp + 1) * nch / kWarps;
+    const int units = (a.V + 7) / 8;
+    const int es = threadIdx.x >> 3, er = threadIdx.x & 7;  // epilogue: sequence, row of the eight
+    int g = s_g[0];
+    for (int it = 0; g < units; ++it) {
+      int gn = units;
+      if (threadIdx.x == 0) gn = atomicAdd(ctr, 1);  // the next unit; waited for after this one's loads
+      const int row0 = g * 8;
+      float c[4] = {0.f, 0.f, 0.f, 0.f};
+      mma_rows8<HI>(W + (int64_t)min(row0 + gl, a.V - 1) * a.d + 8 * t, xlo, xhi, c0, c1, c);
+      part[it & 1][warp][lane] = make_float4(c[0], c[1], c[2], c[3]);
+      if (threadIdx.x == 0) s_g[(it + 1) & 1] = gn;
+      __syncthreads();
+      if (warp < NB / 4) {  // threads 8 s .. 8 s + 7 hold sequence s's eight rows
+        const int row = row0 + er;
+        float y = -INFINITY;
+        if (es < a.B && row < a.V) {
+          y = frag_sum(part[it & 1], es, er);
+          a.logits[((int64_t)es * a.K + k) * a.V + row] = y;
+        }
+        float yq[8];
 #pragma unroll
-      for (int b = 0; b < NB; ++b) acc[b] = 0.f;
-      dot_rows<TE, NB>(W + (int64_t)j * a.d, x, nvec, a.B, lane, acc);
+        for (int q = 0; q < 8; ++q) yq[q] = __shfl_sync(0xffffffffu, y, (lane & ~7) + q);
+        if (er == 0 && es < a.B) {
 #pragma unroll
-      for (int b = 0; b < NB; ++b) acc[b] = warp_sum(acc[b]);
-      if (lane < a.B && lane < NB) {
-        float y = 0.f;
-#pragma unroll
-        for (int b = 0; b < NB; ++b)
-          if (b == lane) y = acc[b];
-        a.logits[((int64_t)lane * a.K + k) * a.V + j] = y;
-        list_insert<S>(lv[warp][lane], li[warp][lane], y, j);
+          for (int q = 0; q < 8; ++q)
+            if (row0 + q < a.V) list_insert<S>(lv[0][es], li[0][es], yq[q], row0 + q);
+        }
       }
+      g = s_g[(it + 1) & 1];
     }
-    if (threadIdx.x == 0) s_g[(it + 1) & 1] = gn;  // the other slot: read by all before the last barrier
-    __syncthreads();
-    g = s_g[(it + 1) & 1];
+  } else {
+    const TE* x[NB];
+#pragma unroll
+    for (int b = 0; b < NB; ++b) x[b] = seq_x(b);
+    int g = s_g[0];
+    for (int it = 0; g < ngroups; ++it) {
+      int gn = ngroups;
+      if (threadIdx.x == 0) gn = atomicAdd(ctr, 1);  // the next group; waited for after this one's loads
+      const int jb = g * GR + warp * RW;
+      const int je = min(a.V, jb + RW);
+      for (int j = jb; j < je; ++j) {
+        float acc[NB];
+#pragma unroll
+        for (int b = 0; b < NB; ++b) acc[b] = 0.f;
+        dot_rows<TE, NB>(W + (int64_t)j * a.d, x, nvec, a.B, lane, acc);
+#pragma unroll
+        for (int b = 0; b < NB; ++b) acc[b] = warp_sum(acc[b]);
+        if (lane < a.B && lane < NB) {
+          float y = 0.f;
+#pragma unroll
+          for (int b = 0; b < NB; ++b)
+            if (b == lane) y = acc[b];
+          a.logits[((int64_t)lane * a.K + k) * a.V + j] = y;
+          list_insert<S>(lv[warp][lane], li[warp][lane], y, j);
+        }
+      }
+      if (threadIdx.x == 0) s_g[(it + 1) & 1] = gn;  // the other slot: read by all before the last barrier
+      __syncthreads();
+      g = s_g[(it + 1) & 1];
+    }
   }
   __syncthreads();  // every warp's lists are complete
 
@@ -475,8 +631,41 @@ int launch_w2(const HeadsArgs& a, int smax_used, cudaStream_t s, const char* fn)
   return check_launch(fn);
 }
 
+// Tensor-core rows (bf16): several sequences and a hidden dimension of at
+// least one 32-column chunk per warp.
+bool use_mma(const HeadsArgs& a, bool bf16) { return bf16 && a.B >= 2 && a.d % 32 == 0 && a.d / 32 >= kWarps; }
+
+template <int NB>
+void launch_w2_mma(const HeadsArgs& a, int smax_used, cudaStream_t s) {
+  const dim3 g2(a.nused * a.cpc);
+  if (smax_used <= 8)
+    launch_kernel(heads_w2_topk_kernel<uint16_t, NB, 8, true>, g2, dim3(kWarps * 32), 0, s, a);
+  else
+    launch_kernel(heads_w2_topk_kernel<uint16_t, NB, 16, true>, g2, dim3(kWarps * 32), 0, s, a);
+}
+
+int launch_heads_mma(const HeadsArgs& a, int smax_used, cudaStream_t s) {
+  const int64_t units = (int64_t)a.nused * a.d / 8;
+  const int g1 = (int)std::max<int64_t>(1, std::min<int64_t>(4 * sm_count(), units));
+  if (a.B <= 8) {
+    launch_kernel(heads_w1_mma_kernel<false>, dim3(g1), dim3(kWarps * 32), 0, s, a);
+    launch_w2_mma<8>(a, smax_used, s);
+  } else {
+    launch_kernel(heads_w1_mma_kernel<true>, dim3(g1), dim3(kWarps * 32), 0, s, a);
+    launch_w2_mma<16>(a, smax_used, s);
+  }
+  return check_launch("medusa_heads_topk");
+}
+
 template <typename TE>
 int launch_w2_b(const HeadsArgs& a, int smax_used, cudaStream_t s, const char* fn) {
+  if (use_mma(a, sizeof(TE) == 2)) {
+    if (a.B <= 8)
+      launch_w2_mma<8>(a, smax_used, s);
+    else
+      launch_w2_mma<16>(a, smax_used, s);
+    return check_launch(fn);
+  }
   if (a.B == 1) return launch_w2<TE, 1>(a, smax_used, s, fn);
   if (a.B <= 4) return launch_w2<TE, 4>(a, smax_used, s, fn);
   return launch_w2<TE, MEDUSA_MAX_B>(a, smax_used, s, fn);
@@ -484,6 +673,7 @@ int launch_w2_b(const HeadsArgs& a, int smax_used, cudaStream_t s, const char* f
 
 template <typename TE>
 int launch_heads_b(const HeadsArgs& a, int smax_used, cudaStream_t s) {
+  if (use_mma(a, sizeof(TE) == 2)) return launch_heads_mma(a, smax_used, s);
   if (a.B == 1) return launch_heads<TE, 1>(a, smax_used, s);
   if (a.B <= 4) return launch_heads<TE, 4>(a, smax_used, s);
   return launch_heads<TE, MEDUSA_MAX_B>(a, smax_used, s);

@@ -524,10 +524,19 @@ HEAD_CASES = [
     # more than four sequences: the 16-sequence kernels, a warp merging two sequences' lists
     ("bf16", 9, 9, 256, 2000, (16, 4), False, False),
     ("f32", 6, 15, 256, 1024, (3, 2), True, True),
+    # bf16 with several sequences runs on the tensor cores: sixteen sequences
+    # (both halves of the MMA's M), a vocabulary that is not a multiple of the
+    # eight-row unit, and the 33B shape's hidden size with two sequences
+    ("bf16", 16, 5, 256, 2003, (3, 2), True, False),
+    ("bf16", 2, 65, 6656, 1001, (8, 6, 5, 2), False, False),
 ]
+# d not a multiple of 32: the CUDA-core kernels for several sequences (the
+# fused call only: medusa_heads_hidden takes bf16 d in multiples of 128)
+FUSED_ONLY_CASES = [("bf16", 3, 9, 144, 700, (2, 2), False, False)]
 
 
-@pytest.mark.parametrize("case", HEAD_CASES, ids=lambda c: f"{c[0]}-B{c[1]}-d{c[3]}-V{c[4]}-s{len(c[5])}")
+@pytest.mark.parametrize("case", HEAD_CASES + FUSED_ONLY_CASES,
+                         ids=lambda c: f"{c[0]}-B{c[1]}-d{c[3]}-V{c[4]}-s{len(c[5])}")
 def test_heads_topk(M, case):
     dt, B, T, d, V, s, bias, lm_noise = case
     K = len(s)
