@@ -63,7 +63,10 @@ struct LmArgs {
   float* logits;
   int rows, d, V;
   int npad;     // MMA N of every chunk (multiple of 16, <= kMaxN)
-  int nchunks;  // chunks of tree rows
+  int cpi;      // row chunks per work item: they share each weight k-block (more than kMaxN rows)
+  int ncol;     // accumulator columns per weight tile = cpi * npad (tree rows r0 .. r0 + ncol)
+  int nacc;     // accumulators in TMEM: 2 (the epilogue of one item overlaps the next) or 1
+  int nchunks;  // work items along the tree rows (each cpi chunks)
   int nt;       // vocabulary tiles per work item (1 or 2): they share each hidden k-block
   int ngroups;  // work items along the vocabulary = ceil(tiles / nt)
   int stages;
@@ -211,16 +214,16 @@ __global__ void __launch_bounds__(kThreads, 1)
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   const uint32_t a_bytes = (uint32_t)a.nt * BM * BK * 2;  // nt W tiles, 16 KB each
-  const uint32_t b_bytes = (uint32_t)a.npad * BK * 2;
+  const uint32_t b_bytes = (uint32_t)a.ncol * BK * 2;
   const uint32_t stage_bytes = a_bytes + b_bytes;
   uint64_t* full = reinterpret_cast<uint64_t*>(smem + (size_t)a.stages * stage_bytes);
   uint64_t* empty = full + a.stages;
   uint64_t* tfull = empty + a.stages;
   uint64_t* tempty = tfull + 2;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(tempty + 2);
-  // mode 1: the residual tile hidden[r0 + i][j] of the current item, [nt][npad][128] bf16
+  // mode 1: the residual tile hidden[r0 + i][j] of the current item, [nt][ncol][128] bf16
   uint16_t* res = reinterpret_cast<uint16_t*>(smem + (size_t)a.stages * stage_bytes + 1024);
-  // acceptance statistics: partial records [nt][4 warps][npad]
+  // acceptance statistics: partial records [nt][4 warps][ncol]
   float4* part = reinterpret_cast<float4*>(smem + a.part_off);
   __shared__ int s_abort;
 
@@ -251,7 +254,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   volatile int* abort_flag = &s_abort;
 
   const int items = JOINT ? (int)gridDim.x : a.ngroups * a.nchunks;
-  const uint32_t acc_cols = (uint32_t)(a.nt * a.npad);  // one accumulator: nt tiles side by side
+  const uint32_t acc_cols = (uint32_t)(a.nt * a.ncol);  // one accumulator: nt tiles side by side
   const int i0 = (int)((long)blockIdx.x * items / gridDim.x);
   const int i1 = (int)((long)(blockIdx.x + 1) * items / gridDim.x);
   const int nkb = a.d / BK;
@@ -262,7 +265,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       int it = 0;
       bool ok = true;
       for (int item = i0; item < i1 && ok; ++item) {
-        const int r0 = (item % a.nchunks) * a.npad;
+        const int r0 = (item % a.nchunks) * a.ncol;
         // weight blocks of the item's tiles (rows past V, a missing tile, read zeros)
         int blk[kMaxTiles], sel[kMaxTiles];
         for (int t = 0; t < a.nt; ++t) {
@@ -283,7 +286,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             else
               tma_load_2d(st + t * (BM * BK * 2), m, &full[s], kb * BK, blk[t] * BM);
           }
-          tma_load_2d(st + a_bytes, &tmH, &full[s], kb * BK, r0);
+          for (int c = 0; c < a.cpi; ++c)  // the item's row chunks (rows past the last read zeros)
+            tma_load_2d(st + a_bytes + c * (a.npad * BK * 2), &tmH, &full[s], kb * BK, r0 + c * a.npad);
         }
       }
       if (!ok) {
@@ -300,8 +304,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       int it = 0, local = 0;
       bool ok = true;
       for (int item = i0; item < i1 && ok; ++item, ++local) {
-        const int acc = local & 1;
-        const uint32_t aph = (uint32_t)(local >> 1) & 1u;
+        const int acc = local % a.nacc;
+        const uint32_t aph = (uint32_t)(local / a.nacc) & 1u;
         if (!wait_or_abort(&tempty[acc], aph ^ 1u, abort_flag)) { ok = false; break; }
         tc_fence_after();
         const uint32_t d_tmem = tmem_base + (uint32_t)acc * acc_cols;
@@ -311,13 +315,15 @@ __global__ void __launch_bounds__(kThreads, 1)
           if (!wait_or_abort(&full[s], ph, abort_flag)) { ok = false; break; }
           tc_fence_after();
           const uint32_t sa = smem_u32(smem + (size_t)s * stage_bytes);
-          const uint64_t db = desc_kmajor_sw128(sa + a_bytes);
           for (int t = 0; t < a.nt; ++t) {
             const uint64_t da = desc_kmajor_sw128(sa + t * (BM * BK * 2));
+            for (int c = 0; c < a.cpi; ++c) {  // every row chunk against the same weight block
+              const uint64_t db = desc_kmajor_sw128(sa + a_bytes + c * (a.npad * BK * 2));
 #pragma unroll
-            for (int kk = 0; kk < BK / UK; ++kk)  // +32 bytes of K per instruction
-              umma_bf16(d_tmem + (uint32_t)(t * a.npad), da + (uint64_t)(kk * 2), db + (uint64_t)(kk * 2),
-                        idesc, (kb | kk) != 0);
+              for (int kk = 0; kk < BK / UK; ++kk)  // +32 bytes of K per instruction
+                umma_bf16(d_tmem + (uint32_t)(t * a.ncol + c * a.npad), da + (uint64_t)(kk * 2),
+                          db + (uint64_t)(kk * 2), idesc, (kb | kk) != 0);
+            }
           }
           umma_commit(&empty[s]);  // the stage is free once these MMAs have read it
         }
@@ -336,13 +342,13 @@ __global__ void __launch_bounds__(kThreads, 1)
     // has saturated HBM would each wait out the loaded latency)
     const int u_rows = JOINT ? a.Vu : a.V;  // stacked W1 rows of the used heads
     auto load_res = [&](int item) {
-      const int r0 = (item % a.nchunks) * a.npad;
+      const int r0 = (item % a.nchunks) * a.ncol;
       for (int t = 0; t < a.nt; ++t) {
         const TileSrc ts = tile_src<JOINT>(a, item, t);
         if (ts.mode != 1) continue;
         const int v = ts.v0 + 32 * g + lane;
         const int j = v % a.d;
-        for (int i0 = 0; i0 < a.npad; i0 += 16) {  // 16 loads in flight, then 16 stores
+        for (int i0 = 0; i0 < a.ncol; i0 += 16) {  // 16 loads in flight, then 16 stores
           uint16_t hv[16];
 #pragma unroll
           for (int i = 0; i < 16; ++i) {
@@ -350,15 +356,15 @@ __global__ void __launch_bounds__(kThreads, 1)
             hv[i] = (v < u_rows && row < a.rows) ? __ldg(a.hidden + (int64_t)row * a.d + j) : (uint16_t)0;
           }
 #pragma unroll
-          for (int i = 0; i < 16; ++i) res[(ts.rs * a.npad + i0 + i) * BM + 32 * g + lane] = hv[i];
+          for (int i = 0; i < 16; ++i) res[(ts.rs * a.ncol + i0 + i) * BM + 32 * g + lane] = hv[i];
         }
       }
     };
     if ((JOINT || a.mode == 1) && i0 < i1) load_res(i0);
     int local = 0;
     for (int item = i0; item < i1; ++item, ++local) {
-      const int acc = local & 1;
-      const uint32_t aph = (uint32_t)(local >> 1) & 1u;
+      const int acc = local % a.nacc;
+      const uint32_t aph = (uint32_t)(local / a.nacc) & 1u;
       const bool got = wait_or_abort(&tfull[acc], aph, abort_flag);
       // with statistics the four warps share named barriers, so they take one decision
       if (STATS ? epilogue_any(!got) : __any_sync(0xffffffffu, !got)) {
@@ -367,16 +373,16 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       __syncwarp();
       tc_fence_after();
-      const int r0 = (item % a.nchunks) * a.npad;
+      const int r0 = (item % a.nchunks) * a.ncol;
       for (int t = 0; t < a.nt; ++t) {
         const TileSrc ts = tile_src<JOINT>(a, item, t);
         if (JOINT && ts.mode < 0) continue;  // padding tile: nothing to store
         const int v = ts.v0 + 32 * g + lane;
         const int tmode = JOINT ? ts.mode : a.mode;
-        for (int c = 0; c < a.npad / 16; ++c) {
+        for (int c = 0; c < a.ncol / 16; ++c) {  // column c * 16 + i holds tree row r0 + c * 16 + i
           uint32_t r[16];
           tmem_ld_32x32b_x16(tmem_base + ((uint32_t)(32 * g) << 16) + (uint32_t)acc * acc_cols +
-                                 (uint32_t)(t * a.npad + c * 16),
+                                 (uint32_t)(t * a.ncol + c * 16),
                              r);
           tmem_ld_wait();
           if (STATS) {  // this warp's 32 vocabulary rows reduced per column
@@ -392,7 +398,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             const StatRec red = a.stat_mode == 2 ? transpose_reduce<true>(x, lane, a.inv_temp)
                                              : transpose_reduce<false>(x, lane, a.inv_temp);
             if (!(lane & 1))
-              part[(t * 4 + g) * a.npad + c * 16 + tr_column(lane)] =
+              part[(t * 4 + g) * a.ncol + c * 16 + tr_column(lane)] =
                   make_float4(red.v, __int_as_float(red.i), red.S, red.A);
           }
           if (v < (tmode == 0 ? a.V : u_rows)) {
@@ -413,7 +419,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 if (row < a.rows) {
                   const float y = __uint_as_float(r[i]) + bias;
                   const float silu = y / (1.f + expf(-y));
-                  const float h = bf16_bits_to_f32(res[(ts.rs * a.npad + c * 16 + i) * BM + 32 * g + lane]);
+                  const float h = bf16_bits_to_f32(res[(ts.rs * a.ncol + c * 16 + i) * BM + 32 * g + lane]);
                   a.u[((int64_t)row * a.K + k) * a.d + j] = f32_to_bf16_bits(silu + h);
                 }
               }
@@ -426,10 +432,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (STATS) {  // the item's record per row: merge the warps' and tiles' partials in a fixed order
         epilogue_sync();
         const int group = item / a.nchunks;
-        for (int e = threadIdx.x - 64; e < a.npad; e += 128) {
+        for (int e = threadIdx.x - 64; e < a.ncol; e += 128) {
           StatRec m = stat_empty();
           for (int q = 0; q < a.nt * 4; ++q) {
-            const StatRec y = stat_load(part[q * a.npad + e]);
+            const StatRec y = stat_load(part[q * a.ncol + e]);
             m = a.stat_mode == 2 ? stat_merge<true>(m, y, a.inv_temp) : stat_merge<false>(m, y, a.inv_temp);
           }
           if (r0 + e < a.rows)
@@ -565,28 +571,58 @@ bool make_weight_map(CUtensorMap* m, const void* w, bool tiled, int64_t wrows, i
 
 // Plan and launch the tensor-core GEMM: `a` carries the epilogue fields; the
 // weight tensor has `wrows` rows of d (row-major) or is its tile copy.
-// Work plan along M: row chunks of at most kMaxN (padded to 16), and whether
-// a work item is one tile or two adjacent tiles sharing each hidden k-block.
-void plan_tc(int rows, int ntiles, int& nchunks, int& npad, int& nt, int& ngroups) {
-  nchunks = (rows + kMaxN - 1) / kMaxN;
-  npad = ((rows + nchunks - 1) / nchunks + 15) / 16 * 16;
-  // two tiles per work item halve the hidden re-reads per weight byte; used
-  // while both accumulators of both tiles fit in TMEM
-  nt = (npad <= 128 && ntiles > sm_count()) ? 2 : 1;
-  ngroups = (ntiles + nt - 1) / nt;
+// Work plan: the tree rows in MMA column chunks of at most kMaxN (padded to
+// 16); as many chunks per work item (cpi) as one accumulator of 512 TMEM
+// columns holds, so that more than kMaxN rows still read each weight block
+// once; and whether a work item is one tile or two adjacent tiles sharing
+// each hidden k-block (nt = 2 halves the hidden re-reads per weight byte,
+// while one accumulator of both tiles fits in TMEM and there are more tiles
+// than SMs).  The shared-memory ring must keep at least three stages (two
+// for the smallest plan), counting the residual tile of the heads'
+// projection (mode 1) and the partial records of the statistics epilogue;
+// where it would not, fewer chunks or tiles share an item.
+struct LmPlan {
+  int nchunks, npad, cpi, ncol, nt, nacc, ngroups, stages;
+  size_t stage_bytes, res_bytes, part_bytes;
+};
+LmPlan plan_tc(int rows, int ntiles, bool mode1, bool stats) {
+  LmPlan p{};
+  const int nct = (rows + kMaxN - 1) / kMaxN;
+  p.npad = ((rows + nct - 1) / nct + 15) / 16 * 16;
+  for (int cpi = std::max(1, std::min(nct, 512 / p.npad)); cpi >= 1; --cpi) {
+    for (int nt = 2; nt >= 1; --nt) {
+      if (nt == 2 && !(2 * cpi * p.npad <= 512 && ntiles > sm_count())) continue;
+      p.cpi = cpi;
+      p.nt = nt;
+      p.ncol = cpi * p.npad;
+      p.stage_bytes = (size_t)nt * BM * BK * 2 + (size_t)p.ncol * BK * 2;
+      p.res_bytes = mode1 ? (size_t)nt * p.ncol * BM * 2 : 0;
+      p.part_bytes = stats ? (size_t)nt * 4 * p.ncol * 16 : 0;
+      const size_t fixed = 1024 + 256 + p.res_bytes + p.part_bytes;
+      p.stages = kSmemBudget > fixed ? (int)std::min<size_t>(8, (kSmemBudget - fixed) / p.stage_bytes) : 0;
+      if (p.stages >= 3 || (p.stages >= 2 && cpi == 1 && nt == 1)) {
+        p.nchunks = (nct + cpi - 1) / cpi;
+        p.nacc = 2 * nt * p.ncol <= 512 ? 2 : 1;  // a second accumulator where it fits
+        p.ngroups = (ntiles + nt - 1) / nt;
+        return p;
+      }
+    }
+  }
+  p.stages = 0;  // nothing fits
+  return p;
 }
 
 int launch_tc(LmArgs& a, const void* w, bool tiled, int64_t wrows, const void* hidden, int rows, int d,
               cudaStream_t s, const char* fn) {
   a.rows = rows; a.d = d; a.tiled = tiled;
-  plan_tc(rows, a.ntiles, a.nchunks, a.npad, a.nt, a.ngroups);
-  const size_t stage_bytes = (size_t)a.nt * BM * BK * 2 + (size_t)a.npad * BK * 2;
-  const size_t res_bytes = a.mode == 1 ? (size_t)a.nt * a.npad * BM * 2 : 0;
-  const size_t part_bytes = a.stat_mode ? (size_t)a.nt * 4 * a.npad * 16 : 0;
-  a.stages = (int)std::min<size_t>(8, (kSmemBudget - 1024 - 256 - res_bytes - part_bytes) / stage_bytes);
+  const LmPlan p = plan_tc(rows, a.ntiles, a.mode == 1, a.stat_mode != 0);
+  if (p.stages < 2) return fail(MEDUSA_ERR_UNSUPPORTED, "%s: shared memory for %d tree rows", fn, rows);
+  a.nchunks = p.nchunks; a.npad = p.npad; a.cpi = p.cpi; a.ncol = p.ncol;
+  a.nt = p.nt; a.nacc = p.nacc; a.ngroups = p.ngroups; a.stages = p.stages;
+  const size_t stage_bytes = p.stage_bytes, res_bytes = p.res_bytes, part_bytes = p.part_bytes;
   a.part_off = (uint32_t)align_up((size_t)a.stages * stage_bytes + 1024 + res_bytes, 16);
   uint32_t cols = 32;
-  while (cols < (uint32_t)(2 * a.nt * a.npad)) cols <<= 1;
+  while (cols < (uint32_t)(a.nacc * a.nt * a.ncol)) cols <<= 1;
   a.tmem_cols = cols;
   const int64_t wblocks = (wrows + BM - 1) / BM;
   a.oob_block = (int)wblocks;
@@ -754,6 +790,9 @@ extern "C" int medusa_lm_head_verify_heads_hidden(const void* hidden, int rows, 
   a.tiled1 = w1_layout == MEDUSA_W_TILES;
   a.nchunks = 1;
   a.npad = (rows + 15) / 16 * 16;
+  a.cpi = 1;
+  a.ncol = a.npad;
+  a.nacc = 1;  // one work item per CTA
   a.ntiles = a.lm_tiles;
   a.oob_block = a.lm_tiles;  // a block past W: its loads read zeros
   int grid = 0;
@@ -780,9 +819,7 @@ extern "C" int medusa_lm_head_verify_heads_hidden(const void* hidden, int rows, 
 
 extern "C" int medusa_lm_head_stat_groups(int rows, int V) {
   if (rows < 1 || V < 1) return 0;
-  int nchunks, npad, nt, ngroups;
-  plan_tc(rows, (V + BM - 1) / BM, nchunks, npad, nt, ngroups);
-  return ngroups;
+  return plan_tc(rows, (V + BM - 1) / BM, false, true).ngroups;
 }
 
 extern "C" int medusa_lm_head_verify_stats(const void* hidden, const void* w_lm, float* logits, int rows, int d,

@@ -58,7 +58,8 @@ def _ref_stats(z, inv_temp):
     return np.argmax(z, axis=1), lse, -(np.exp(lp) * lp).sum(1)
 
 
-@pytest.mark.parametrize("rows,d,V", [(15, 256, 1000), (65, 4096, 32000), (130, 512, 333), (65, 256, 40000)])
+@pytest.mark.parametrize("rows,d,V", [(15, 256, 1000), (65, 4096, 32000), (130, 512, 333), (65, 256, 40000),
+                                      (200, 256, 40000), (300, 256, 5000)])
 @pytest.mark.parametrize("mode", [0, 1])
 def test_fused_stats_records(M, rows, d, V, mode):
     h = to_dev(synth.normal(51, "h", (rows, d), 1.0, "bf16"))

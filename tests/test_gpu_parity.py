@@ -185,7 +185,11 @@ def test_tree_attn_capacity_flag(M):
 
 LM_CASES = [("f32", 15, 256, 1024), ("bf16", 15, 256, 1024), ("bf16", 65, 256, 1000),
             ("bf16", 130, 512, 3000), ("bf16", 1, 64, 17), ("bf16", 260, 128, 333),
-            ("bf16", 65, 4096, 2048), ("bf16", 65, 256, 20000), ("bf16", 17, 128, 40000)]
+            ("bf16", 65, 4096, 2048), ("bf16", 65, 256, 20000), ("bf16", 17, 128, 40000),
+            # two tiles per item with one accumulator (129..256 rows, more tiles than SMs);
+            # two row chunks sharing each weight block (257..512 rows); two such items
+            ("bf16", 200, 256, 40000), ("bf16", 300, 256, 40000), ("bf16", 512, 128, 5000),
+            ("bf16", 1000, 128, 700)]
 
 
 @pytest.mark.parametrize("case", LM_CASES, ids=lambda c: "-".join(map(str, c)))
@@ -529,6 +533,8 @@ HEAD_CASES = [
     # eight-row unit, and the 33B shape's hidden size with two sequences
     ("bf16", 16, 5, 256, 2003, (3, 2), True, False),
     ("bf16", 2, 65, 6656, 1001, (8, 6, 5, 2), False, False),
+    # 325 tree rows: W1 over every row in two row chunks per weight block
+    ("bf16", 5, 65, 256, 1000, (4, 3, 2), True, False),
 ]
 # d not a multiple of 32: the CUDA-core kernels for several sequences (the
 # fused call only: medusa_heads_hidden takes bf16 d in multiples of 128)
