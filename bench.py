@@ -114,11 +114,34 @@ def algorithmic_bytes(w: dict, T: int, s_heads, L_list, heads_mode: str, fused_a
 def algorithmic_flops(w, T, s_heads, L_list):
     B, H, Dh, d, V = w["B"], w["H"], w["Dh"], w["d"], w["V"]
     k_used = sum(1 for s in s_heads if s > 0)
-    return dict(tree_attn=4 * T * (int(np.sum(L_list)) + T) * H * Dh,
+    return dict(tree_attn=4 * T * (int(np.sum(L_list)) + B * T) * H * Dh,
                 lm_head_verify=2 * B * T * d * V,
                 heads_topk=2 * B * k_used * (d * d + d * V),
                 heads_hidden=2 * B * T * k_used * d * d,
                 heads_logits_topk=2 * B * k_used * d * V)
+
+
+def weight_bytes(w, s_heads):
+    """Weights one step streams: the vocabulary matrix and the heads in use."""
+    e = 2 if w["dtype"] == "bf16" else 4
+    k_used = sum(1 for s in s_heads if s > 0)
+    return (w["V"] * w["d"] + k_used * (w["d"] * w["d"] + w["V"] * w["d"])) * e
+
+
+def floor_us(nbytes, flops, peaks):
+    """max(bytes / measured copy bandwidth, flops / sustained bf16 tensor
+    rate) in microseconds: the roofline floor of one call."""
+    return max(nbytes / (peaks["hbm_gbs"] * 1e3), flops / (peaks["bf16_tflops_sustained"] * 1e6))
+
+
+def step_floor(by, fl, peaks, ms):
+    """The step's floor: all its bytes at the copy bandwidth, or all its
+    flops at the sustained tensor rate, whichever is longer."""
+    tb = by["step"]
+    tf = sum(fl[c] for c in ("tree_attn", "lm_head_verify", "heads_topk") if c in fl)
+    us = floor_us(tb, tf, peaks)
+    return {"bytes": tb, "flops": tf, "floor_us": round(us, 2), "frac": round(us / (ms * 1e3), 4),
+            "bound": "hbm" if tb / (peaks["hbm_gbs"] * 1e3) >= tf / (peaks["bf16_tflops_sustained"] * 1e6) else "tensor"}
 
 
 def load_peaks():
@@ -132,15 +155,16 @@ def load_peaks():
     return dict(hbm_gbs=6800.0, bf16_tflops=1900.0, bf16_tflops_sustained=1700.0, source="fallback")
 
 
-def ncu_traffic(kernel_key: str):
-    """DRAM bytes per launch from the committed ncu summary, or None when the
+def ncu_traffic(kernel_key: str, workload: str):
+    """DRAM bytes per launch of a call on a workload, from the committed ncu
+    summary (key "call@workload"), or None when there is none or the
     kernel's source changed since the counters were taken."""
     p = os.path.join(ROOT, "profiles", "ncu_traffic.json")
     if not os.path.exists(p):
         return None
     with open(p) as f:
         j = json.load(f)
-    ent = j.get(kernel_key)
+    ent = j.get(f"{kernel_key}@{workload}")
     if not ent:
         return None
     src = os.path.join(ROOT, ent["source"])
@@ -369,16 +393,61 @@ def run_native(args, w, rank, world, local_rank):
     if not args.no_e2e:
         e2e = measure_e2e(args, w, st, x, xh, prefix0, s, s2, s3, torch, M)
     rej = measure_rejection(st, x, s, torch, M) if world == 1 else None
+    attn_alone = (measure_attn_alone(st, x, prefix0, L_list, torch, M)
+                  if world == 1 and st.attn_splits == "tc" else None)
     dloop = None
     if args.loop_steps > 0 and world == 1:
-        dloop = measure_loop(args, w, dev, torch, M)
+        if len(set(int(v) for v in L_list)) == 1:
+            dloop = measure_loop(args, w, dev, torch, M)
+        else:  # DecodeLoop starts every sequence at one prefix length
+            dloop = {"skipped": "ragged prefix lengths; the decode loop runs with one prefix length for the batch"}
 
-    return dict(host_inputs=(wts, xh) if keep_host else None,
+    return dict(host_inputs=(wts, xh) if keep_host else None, attn_alone=attn_alone,
                 ms_step=ms_step, ms_events_step=ms_events / args.steps, per_call_ms=per_call, clocks=clocks,
                 dloop=dloop, rej=rej,
                 T=T, s_heads=st.s_heads, L_list=L_list, accept_len=accept_len, e2e=e2e,
                 launches=st.launches_per_step * args.steps, tree=ht,
                 attn_splits=f"tc{st.tc_splits}" if st.attn_splits == "tc" else st.attn_splits or 8)
+
+
+def measure_attn_alone(st, x, prefix0, L_list, torch, M, reps=10):
+    """The tree attention on its own, as its roofline is judged: the key split
+    that fills the GPU (step.tc_key_splits over every SM), L2 flushed before
+    each launch (a 256 MB write), CUDA events around the launch alone; median
+    of `reps`.  The step itself runs it beside the LM head instead."""
+    from medusa_tree_speculative_gb300 import step
+
+    B, T, H, Dh = st.out.shape
+    sms = torch.cuda.get_device_properties(st.out.device).multi_processor_count
+    ns = step.tc_key_splits(B, H, T, int(max(L_list)), sms)
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device=st.out.device)
+    s = torch.cuda.Stream(device=st.out.device)
+
+    def call():
+        M.medusa_tree_attn_tc(x["q"], x["k_new"], x["v_new"], x["k_cache"], x["v_cache"], x["seq_start"],
+                              x["prefix_len"], x["seq_cap"], st.tree, st.max_prefix, st.rope_theta, st.scale,
+                              st.out, st.err, s, key_splits=ns)
+
+    ts = []
+    for i in range(reps + 1):
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        with torch.cuda.stream(s):
+            x["prefix_len"].copy_(prefix0)  # the steps before advanced it by the accepted tokens
+            flush.fill_(1)
+            e0.record(s)
+            call()
+            e1.record(s)
+        torch.cuda.synchronize()
+        if i:  # the first launch is a warm-up
+            ts.append(e0.elapsed_time(e1) * 1e3)
+    if int(st.err.item()) != 0:
+        raise RuntimeError(f"device error flag {int(st.err.item())} in the attention-alone launches")
+    us = statistics.median(ts)
+    e = st.out.element_size()
+    kv = 2 * int(np.sum(L_list)) * H * Dh * e
+    act = 6 * B * T * H * Dh * e  # q, k_new, v_new read; K', V' appended; out written
+    return {"key_splits": ns, "us": us, "kv_bytes": kv, "bytes": kv + act, "gbs": (kv + act) / us / 1e3,
+            "how": "median of %d launches, each after a 256 MB write that flushes L2" % reps}
 
 
 def measure_rejection(st, x, s, torch, M, reps=20):
@@ -429,11 +498,11 @@ def measure_loop(args, w, dev, torch, M):
     tree = M.DeviceTree(step.build_tree(w), dev)
     model = loop.StandInModel(w, seed=3, device=dev)
     x0 = np.array([(97 * b + 5) % w["V"] for b in range(w["B"])])
-    lp = loop.DecodeLoop(w, model, tree, n, L0=int(w["L"][0]), x0=x0, device=dev, heads=args.heads)
+    L0 = int(w["L"][0])
+    lp = loop.DecodeLoop(w, model, tree, n, L0=L0, x0=x0, device=dev, heads=args.heads)
     s = torch.cuda.Stream(device=dev)
     s2 = torch.cuda.Stream(device=dev) if args.attn_branch == "fork" else None
     s3 = torch.cuda.Stream(device=dev) if args.heads == "split" else None
-    L0 = int(w["L"][0])
 
     def reset():
         with torch.cuda.stream(s):
@@ -690,7 +759,7 @@ def run_reference(args, w, rank, world, budget_s=60.0):
         "steps": len(vals), "warmup": 0, "steps_requested": args.steps, "warmup_requested": args.warmup,
         "ms_per_step": sec * 1e3, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-        "config": config_dict(w),
+        "config": config_dict(w, weight_bytes=weight_bytes(w, orc.s_heads)),
         "cpu_baseline": {"value": v, "unit": UNIT, "cores": 1, "kind": "oracle",
                          "sample": sample + f"; host has {os.cpu_count()} cores"},
         "e2e": {"value": v, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
@@ -699,10 +768,15 @@ def run_reference(args, w, rank, world, budget_s=60.0):
     print(json.dumps(line), flush=True)
 
 
-def config_dict(w, extra=None):
+def config_dict(w, extra=None, weight_bytes=None):
     c = {"workload": w["name"], "dtype": w["dtype"], "d": w["d"], "V": w["V"], "H": w["H"], "Dh": w["Dh"],
-         "B": w["B"], "prefix": str(w["L"]), "K_heads": w["K"], "tree": str(w["tree"]), "accept": w["mode"],
-         "l2": "inputs larger than L2 (1.48 GB of weights stream per step)"}
+         "B": w["B"], "prefix": str(w["L"]), "K_heads": w["K"], "tree": str(w["tree"]), "accept": w["mode"]}
+    if weight_bytes is not None:
+        c["l2"] = (f"inputs larger than L2 ({weight_bytes / 1e9:.2f} GB of weights stream per step)"
+                   if weight_bytes > 126e6 else "inputs within L2")
+    if extra:
+        c.update(extra)
+    return c
     if extra:
         c.update(extra)
     return c
@@ -744,14 +818,15 @@ def main():
                if c in r["per_call_ms"]), key=lambda c: r["per_call_ms"][c])
     dom_ms = r["per_call_ms"][dom]
     achieved = by[dom] / (dom_ms * 1e-3) / 1e9
-    traffic = ncu_traffic(dom)
+    traffic = ncu_traffic(dom, w["name"])
     line = {
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": w["dtype"], "data": "synthetic (seeded random weights and activations)",
         "config": config_dict(w, {"parallelism": f"replicas{world}" if world > 1 else "single-gpu", "attn_branch": args.attn_branch, "attn_order": args.attn_order, "attn_splits": r["attn_splits"], "heads": args.heads, "accept_impl": args.accept,
                                   "logits_written": bool(args.logits or w["mode"] == "typical"),
-                                  "T_rows": r["T"], "s": r["s_heads"], "planted_accept_len": r["accept_len"]}),
+                                  "T_rows": r["T"], "s": r["s_heads"], "planted_accept_len": r["accept_len"]},
+                              weight_bytes=weight_bytes(w, r["s_heads"])),
         "roofline": {"bound": "hbm", "kernel": "medusa_heads_topk_candidates" if dom == "heads_topk" else f"medusa_{dom}", "achieved": achieved, "peak": peaks["hbm_gbs"],
                      "unit": "GB/s", "frac": achieved / peaks["hbm_gbs"], "traffic": traffic,
                      "algorithmic_bytes_per_launch": by[dom], "ms_per_launch": dom_ms,
@@ -760,8 +835,11 @@ def main():
                           "frac_of_measured": step_gbs / peaks["hbm_gbs"], "frac_of_8tbs": step_gbs / 8000.0},
         "per_call": {c: {"ms": round(r["per_call_ms"][c], 5), "bytes": by[c],
                          "gbs": round(by[c] / (r["per_call_ms"][c] * 1e-3) / 1e9, 1),
-                         **({"tflops": round(fl[c] / (r["per_call_ms"][c] * 1e-3) / 1e12, 1)} if c in fl else {})}
+                         **({"tflops": round(fl[c] / (r["per_call_ms"][c] * 1e-3) / 1e12, 1)} if c in fl else {}),
+                         "floor_us": round(floor_us(by[c], fl.get(c, 0), peaks), 2),
+                         "frac_of_floor": round(floor_us(by[c], fl.get(c, 0), peaks) / (r["per_call_ms"][c] * 1e3), 3)}
                      for c in r["per_call_ms"]},
+        "step_floor": step_floor(by, fl, peaks, ms),
         "ms_per_step_with_call_events": r["ms_events_step"],
         "clocks": r["clocks"],
         "gpu_launches": r["launches"],
@@ -772,6 +850,10 @@ def main():
         line["decode_loop"] = r["dloop"]
     if r["rej"] is not None:
         line["rejection_accept"] = r["rej"]
+    if r["attn_alone"] is not None:
+        a = r["attn_alone"]
+        a["frac_of_measured"] = a["gbs"] / peaks["hbm_gbs"]
+        line["attn_alone"] = a
     if world == 1 and not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline(w, *r["host_inputs"])
     print(json.dumps(line), flush=True)

@@ -279,6 +279,12 @@ int medusa_lm_head_verify(const void* hidden, const void* w_lm, float* logits,
                           medusa_w_layout w_layout, void* workspace,
                           size_t workspace_bytes, int32_t* err, void* stream);
 
+/* CTAs (one per SM) that medusa_lm_head_verify launches for bf16 `rows` x V
+ * on the current device, 0 for invalid sizes.  A caller that runs other work
+ * beside the LM head (the tree attention of the same step) sizes it to the
+ * SMs left free.  No counterpart in the pages. */
+int medusa_lm_head_ctas(int rows, int V);
+
 /* The LM head with the acceptance's row statistics fused into its epilogue
  * (the logits round trip skipped).  For every tree row r and vocabulary group
  * g (a run of 128 or 256 vocabulary rows; medusa_lm_head_stat_groups(rows, V)

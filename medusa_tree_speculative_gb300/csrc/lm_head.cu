@@ -817,6 +817,15 @@ extern "C" int medusa_lm_head_verify_heads_hidden(const void* hidden, int rows, 
   return check_launch(fn);
 }
 
+extern "C" int medusa_lm_head_ctas(int rows, int V) {
+  if (rows < 1 || V < 1) return 0;
+  const LmPlan p = plan_tc(rows, (V + BM - 1) / BM, false, false);
+  if (p.stages < 2) return 0;
+  const int items = p.ngroups * p.nchunks;
+  const int per_cta = (items + sm_count() - 1) / sm_count();
+  return (items + per_cta - 1) / per_cta;
+}
+
 extern "C" int medusa_lm_head_stat_groups(int rows, int V) {
   if (rows < 1 || V < 1) return 0;
   return plan_tc(rows, (V + BM - 1) / BM, false, true).ngroups;

@@ -67,6 +67,7 @@ _SIGS = {
     "medusa_lm_head_verify_heads_hidden": (I, [P, I, I, P, I, I, P, P, I, P, P, I, P, I, P, P]),
     "medusa_append_tokens": (I, [P, P, P, I, I, I, P, P, I, P, P]),
     "medusa_lm_head_stat_groups": (I, [I, I]),
+    "medusa_lm_head_ctas": (I, [I, I]),
     "medusa_lm_head_verify_stats": (I, [P, P, P, I, I, I, I, I, I, F, P, SZ, P, P]),
     "medusa_accept_stats": (I, [P, I, P, P, TREE, I, I, I, F, F, F, P, P, P, P, P, P, P]),
     "medusa_accept_rejection_workspace_size": (SZ, [I, I]),
@@ -433,6 +434,11 @@ def medusa_accept_rejection(logits, draft_logits, tokens, tree: DeviceTree, temp
 
 def medusa_lm_head_stat_groups(rows, V) -> int:
     return int(_lib.medusa_lm_head_stat_groups(rows, V))
+
+
+def medusa_lm_head_ctas(rows: int, V: int) -> int:
+    """CTAs the bf16 LM head launches for rows x V on the current device."""
+    return int(_lib.medusa_lm_head_ctas(rows, V))
 
 
 def medusa_lm_head_verify_stats(hidden, w_lm, logits, stats, mode, temperature, V, err=None, stream=None,

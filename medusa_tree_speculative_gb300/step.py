@@ -35,10 +35,11 @@ def host_to_torch(a: np.ndarray, dt: str) -> torch.Tensor:
 
 
 def tc_key_splits(B: int, H: int, T: int, max_prefix: int, sms: int) -> int:
-    """Key split for medusa_tree_attn_tc on its own: the largest of 8, 4, 2
-    that keeps the grid (splits x heads x sequences x 128-row blocks, one CTA
-    per SM) within one wave and gives every CTA at least one 128-key tile;
-    else 1."""
+    """Key split for medusa_tree_attn_tc: the largest of 8, 4, 2 that keeps
+    the grid (splits x heads x sequences x 128-row blocks, one CTA per SM)
+    within `sms` SMs and gives every CTA at least one 128-key tile; else 1.
+    On its own the attention may take every SM; in the step it runs beside
+    the LM head and gets the SMs the LM head leaves free."""
     ctas = B * H * -(-T // 128)
     tiles = -(-(max_prefix + T) // 128)
     return next(c for c in (8, 4, 2, 1) if c == 1 or (c * ctas <= sms and c <= tiles))
@@ -74,13 +75,14 @@ class VerifyStep:
         # heads' kernels), with the library's default key split (None), 1, 2,
         # 4, 8 CTAs per head, or "tc" (medusa_tree_attn_tc: bf16, Dh 128;
         # "tc1" .. "tc8" name its key split, "tc" takes the largest that keeps
-        # the grid within one CTA per SM); "auto": "tc1" for bf16 with Dh 128
-        # (one CTA per head: the fewest SMs taken from the LM head it runs
-        # beside, the fastest step measured at the 7B shape), else 4 for bf16
+        # the grid within the SMs the LM head leaves free, see tc_key_splits);
+        # "auto": "tc" for bf16 with Dh 128, else 4 for bf16.  (At the
+        # 7B/13B/33B shapes the heads alone outnumber the free SMs, so this is
+        # one CTA per head, the fastest step measured at L = 1024 and 4096.)
         if attn_order not in ("first", "after_lm", "after_accept", "after_heads"):
             raise ValueError(f"attn_order {attn_order!r}")
         if attn_splits == "auto":
-            attn_splits = ("tc1" if w["Dh"] == 128 else 4) if w["dtype"] == "bf16" else None
+            attn_splits = ("tc" if w["Dh"] == 128 else 4) if w["dtype"] == "bf16" else None
         B, H, Dh, d, V, K = w["B"], w["H"], w["Dh"], w["d"], w["V"], w["K"]
         T = tree.T
         self.tc_splits = None
@@ -89,7 +91,10 @@ class VerifyStep:
                 self.tc_splits = int(attn_splits[2:])
             else:
                 sms = torch.cuda.get_device_properties(device).multi_processor_count if torch.cuda.is_available() else 152
-                self.tc_splits = tc_key_splits(B, H, T, max_prefix, sms)
+                free = sms
+                if attn_order in ("first", "after_lm"):  # it runs beside the LM head
+                    free = max(0, sms - M.medusa_lm_head_ctas(B * T, V))
+                self.tc_splits = tc_key_splits(B, H, T, max_prefix, free)
             if self.tc_splits not in (1, 2, 4, 8):
                 raise ValueError(f"attn_splits {attn_splits!r}")
             attn_splits = "tc"

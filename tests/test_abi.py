@@ -274,3 +274,6 @@ def test_tc_key_splits(M):
     assert tc_key_splits(1, 1, 15, 0, 152) == 1        # one key tile only
     assert tc_key_splits(1, 32, 257, 4096, 152) == 1   # three row blocks: 96 CTAs
     assert tc_key_splits(1, 16, 65, 1024, 152) == 8
+    # in the step: the 27 SMs the 7B LM head (125 CTAs) leaves free
+    assert tc_key_splits(1, 32, 65, 4096, 27) == 1
+    assert tc_key_splits(1, 4, 65, 4096, 27) == 4      # 16 CTAs; 8 splits would need 32 SMs
