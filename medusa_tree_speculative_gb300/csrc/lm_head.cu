@@ -286,8 +286,11 @@ __global__ void __launch_bounds__(kThreads, 1)
             else
               tma_load_2d(st + t * (BM * BK * 2), m, &full[s], kb * BK, blk[t] * BM);
           }
-          for (int c = 0; c < a.cpi; ++c)  // the item's row chunks (rows past the last read zeros)
-            tma_load_2d(st + a_bytes + c * (a.npad * BK * 2), &tmH, &full[s], kb * BK, r0 + c * a.npad);
+          if (a.cpi == 1)
+            tma_load_2d(st + a_bytes, &tmH, &full[s], kb * BK, r0);
+          else
+            for (int c = 0; c < a.cpi; ++c)  // the item's row chunks (rows past the last read zeros)
+              tma_load_2d(st + a_bytes + c * (a.npad * BK * 2), &tmH, &full[s], kb * BK, r0 + c * a.npad);
         }
       }
       if (!ok) {
@@ -304,8 +307,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       int it = 0, local = 0;
       bool ok = true;
       for (int item = i0; item < i1 && ok; ++item, ++local) {
-        const int acc = local % a.nacc;
-        const uint32_t aph = (uint32_t)(local / a.nacc) & 1u;
+        const int acc = a.nacc == 2 ? local & 1 : 0;
+        const uint32_t aph = (uint32_t)(a.nacc == 2 ? local >> 1 : local) & 1u;
         if (!wait_or_abort(&tempty[acc], aph ^ 1u, abort_flag)) { ok = false; break; }
         tc_fence_after();
         const uint32_t d_tmem = tmem_base + (uint32_t)acc * acc_cols;
@@ -315,14 +318,25 @@ __global__ void __launch_bounds__(kThreads, 1)
           if (!wait_or_abort(&full[s], ph, abort_flag)) { ok = false; break; }
           tc_fence_after();
           const uint32_t sa = smem_u32(smem + (size_t)s * stage_bytes);
-          for (int t = 0; t < a.nt; ++t) {
-            const uint64_t da = desc_kmajor_sw128(sa + t * (BM * BK * 2));
-            for (int c = 0; c < a.cpi; ++c) {  // every row chunk against the same weight block
-              const uint64_t db = desc_kmajor_sw128(sa + a_bytes + c * (a.npad * BK * 2));
+          if (a.cpi == 1) {
+            const uint64_t db = desc_kmajor_sw128(sa + a_bytes);
+            for (int t = 0; t < a.nt; ++t) {
+              const uint64_t da = desc_kmajor_sw128(sa + t * (BM * BK * 2));
 #pragma unroll
               for (int kk = 0; kk < BK / UK; ++kk)  // +32 bytes of K per instruction
-                umma_bf16(d_tmem + (uint32_t)(t * a.ncol + c * a.npad), da + (uint64_t)(kk * 2),
-                          db + (uint64_t)(kk * 2), idesc, (kb | kk) != 0);
+                umma_bf16(d_tmem + (uint32_t)(t * a.npad), da + (uint64_t)(kk * 2), db + (uint64_t)(kk * 2),
+                          idesc, (kb | kk) != 0);
+            }
+          } else {
+            for (int t = 0; t < a.nt; ++t) {
+              const uint64_t da = desc_kmajor_sw128(sa + t * (BM * BK * 2));
+              for (int c = 0; c < a.cpi; ++c) {  // every row chunk against the same weight block
+                const uint64_t db = desc_kmajor_sw128(sa + a_bytes + c * (a.npad * BK * 2));
+#pragma unroll
+                for (int kk = 0; kk < BK / UK; ++kk)  // +32 bytes of K per instruction
+                  umma_bf16(d_tmem + (uint32_t)(t * a.ncol + c * a.npad), da + (uint64_t)(kk * 2),
+                            db + (uint64_t)(kk * 2), idesc, (kb | kk) != 0);
+              }
             }
           }
           umma_commit(&empty[s]);  // the stage is free once these MMAs have read it
@@ -363,8 +377,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     if ((JOINT || a.mode == 1) && i0 < i1) load_res(i0);
     int local = 0;
     for (int item = i0; item < i1; ++item, ++local) {
-      const int acc = local % a.nacc;
-      const uint32_t aph = (uint32_t)(local / a.nacc) & 1u;
+      const int acc = a.nacc == 2 ? local & 1 : 0;
+      const uint32_t aph = (uint32_t)(a.nacc == 2 ? local >> 1 : local) & 1u;
       const bool got = wait_or_abort(&tfull[acc], aph, abort_flag);
       // with statistics the four warps share named barriers, so they take one decision
       if (STATS ? epilogue_any(!got) : __any_sync(0xffffffffu, !got)) {
