@@ -327,6 +327,20 @@ __global__ void __launch_bounds__(kThreads, 1)
                 umma_bf16(d_tmem + (uint32_t)(t * a.npad), da + (uint64_t)(kk * 2), db + (uint64_t)(kk * 2),
                           idesc, (kb | kk) != 0);
             }
+          } else if (a.cpi == 2) {  // two row chunks against the same weight block
+            const uint64_t db0 = desc_kmajor_sw128(sa + a_bytes);
+            const uint64_t db1 = desc_kmajor_sw128(sa + a_bytes + a.npad * BK * 2);
+            for (int t = 0; t < a.nt; ++t) {
+              const uint64_t da = desc_kmajor_sw128(sa + t * (BM * BK * 2));
+              const uint32_t d0 = d_tmem + (uint32_t)(t * a.ncol);
+#pragma unroll
+              for (int kk = 0; kk < BK / UK; ++kk)
+                umma_bf16(d0, da + (uint64_t)(kk * 2), db0 + (uint64_t)(kk * 2), idesc, (kb | kk) != 0);
+#pragma unroll
+              for (int kk = 0; kk < BK / UK; ++kk)
+                umma_bf16(d0 + (uint32_t)a.npad, da + (uint64_t)(kk * 2), db1 + (uint64_t)(kk * 2), idesc,
+                          (kb | kk) != 0);
+            }
           } else {
             for (int t = 0; t < a.nt; ++t) {
               const uint64_t da = desc_kmajor_sw128(sa + t * (BM * BK * 2));
