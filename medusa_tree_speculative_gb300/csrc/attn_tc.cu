@@ -14,20 +14,24 @@
 //     through the same tensor-map loads as the prefix; the query rows are
 //     rotated, scaled by scale * log2(e) and stored in shared memory in the
 //     128-byte-swizzled K-major layout the MMA reads;
-//   * warp 0 (one thread) loads key and value tiles with TMA into two rings
-//     of two stages;
+//   * warp 0 (one thread) loads key tiles with TMA into a ring of three
+//     stages and value tiles into a ring of two;
 //   * warp 1 allocates tensor memory and one thread issues the MMAs:
 //     S_t = Q K_t^T (M = 128 query rows, N = 128 keys, K = 128) into one of
 //     two S accumulators, two tiles ahead, and PV_t = P_t V_t (N = 128 value
-//     columns, K = 128 keys; V is read in its cache layout, keys x values,
-//     as an MN-major operand) into one of two more accumulators in turn;
+//     columns, K = 128 keys; P is read from tensor memory, where it replaced
+//     S_t; V is read in its cache layout, keys x values, as an MN-major
+//     operand) into one of two more accumulators in turn;
 //   * warps 2-9 give each query row (its tensor-memory lane) two threads,
 //     one per half of the tile's keys and of the output columns: read S_t,
 //     mask it (keys past the sequence; tree keys that are not an
 //     ancestor-or-self of the row), agree on the row's running max through
-//     shared memory, write P_t = 2^(S - max) in bf16 to shared memory for the
-//     PV MMA, and fold PV_{t-1} into the output registers with the
-//     online-softmax rescale while PV_t runs.
+//     shared memory, write P_t = 2^(S - max) in bf16 over S_t in tensor
+//     memory for the PV MMA, and fold PV_{t-1} into the output registers with
+//     the online-softmax rescale while PV_t runs.
+// Keeping P in tensor memory leaves the shared memory it would take to a
+// third key stage: a key tile's load is issued three tiles before its S MMA
+// instead of two, which covers the HBM latency under load (2-4 us).
 // Every mbarrier wait is bounded; a wait that gives up sets
 // MEDUSA_DEVERR_TIMEOUT, lets the copies in flight land, frees tensor memory
 // and returns.
@@ -58,14 +62,14 @@ constexpr float kLog2e = 1.4426950408889634f;
 
 // Shared memory (1024-byte aligned regions).
 constexpr uint32_t kQOff = 0;                    // Q   [2 k-chunks][128 rows][128 B]
-constexpr uint32_t kPOff = 32768;                // P   [2 k-chunks][128 rows][128 B]
-constexpr uint32_t kKOff = 65536;                // K   [2 stages][2 k-chunks][128 keys][128 B]
+constexpr uint32_t kKOff = 32768;                // K   [3 stages][2 k-chunks][128 keys][128 B]
 constexpr uint32_t kVOff = 131072;               // V   [2 stages][2 column halves][128 keys][128 B]
+constexpr int kKStages = 3;
 constexpr uint32_t kTileBytes = 32768;           // one K or V tile
 constexpr uint32_t kBarOff = 196608;             // mbarriers, tensor-memory slot, flags
 constexpr uint32_t kAncOff = kBarOff + 192 + 2048;  // ancestor words [128 rows][kMaxWords]
 constexpr uint32_t kCsOff = kAncOff + BMR * kMaxWords * 4;  // cos / sin [K+1][64] each
-constexpr uint32_t kTmemCols = 512;              // S0, S1, PV0, PV1 (128 columns each)
+constexpr uint32_t kTmemCols = 512;              // S0, S1 (P_t over S_t), PV0, PV1 (128 columns each)
 constexpr int kPartStride = DH + 4;              // merge: floats per partial row (padded)
 constexpr uint32_t kPartOff = kKOff;             // merge: this CTA's O partial [128 rows][kPartStride] fp32
 constexpr uint32_t kMlOff = kPartOff + BMR * kPartStride * 4;  // merge: (max, sum) [128 rows]
@@ -186,13 +190,12 @@ __global__ void __cluster_dims__(CL, 1, 1) __launch_bounds__(kThreads, 1)
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   const uint32_t sbase = smem_u32(smem);
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + kBarOff);
-  uint64_t* k_full = bars;       // [2] TMA -> MMA
-  uint64_t* k_empty = bars + 2;  // [2] MMA -> TMA
-  uint64_t* v_full = bars + 4;   // [2]
-  uint64_t* v_empty = bars + 6;  // [2]
-  uint64_t* s_full = bars + 8;   // [2] MMA -> softmax: S_t ready
-  uint64_t* s_empty = bars + 10; // [2] softmax -> MMA: S buffer read (256 arrivals)
-  uint64_t* p_full = bars + 12;  // softmax -> MMA: P_t written (256 arrivals)
+  uint64_t* k_full = bars;       // [3] TMA -> MMA
+  uint64_t* k_empty = bars + 3;  // [3] MMA -> TMA
+  uint64_t* v_full = bars + 6;   // [2]
+  uint64_t* v_empty = bars + 8;  // [2]
+  uint64_t* s_full = bars + 10;  // [2] MMA -> softmax: S_t ready
+  uint64_t* p_full = bars + 12;  // softmax -> MMA: P_t written over S_t (256 arrivals)
   uint64_t* pv_full = bars + 13; // [2] MMA -> softmax: PV_t ready (accumulator t & 1)
   uint64_t* pv_empty = bars + 15;// [2] softmax -> MMA: PV accumulator read (256 arrivals)
   uint64_t* mma_done = bars + 17;// every MMA issued so far has completed
@@ -227,13 +230,14 @@ __global__ void __cluster_dims__(CL, 1, 1) __launch_bounds__(kThreads, 1)
   int n_early = 0;  // tiles the loader issued before the prologue (thread 0 only)
 
   if (tid == 0) {
-    for (int i = 0; i < 2; ++i) {
+    for (int i = 0; i < kKStages; ++i) {
       mbar_init(&k_full[i], 1);
       mbar_init(&k_empty[i], 1);
+    }
+    for (int i = 0; i < 2; ++i) {
       mbar_init(&v_full[i], 1);
       mbar_init(&v_empty[i], 1);
       mbar_init(&s_full[i], 1);
-      mbar_init(&s_empty[i], kSoftThreads);
       mbar_init(&pv_full[i], 1);
       mbar_init(&pv_empty[i], kSoftThreads);
       mbar_init(&xm_full[i], kSoftThreads);
@@ -349,33 +353,55 @@ __global__ void __cluster_dims__(CL, 1, 1) __launch_bounds__(kThreads, 1)
   volatile int* abort_flag = s_abort;
 
   if (warp == 0) {
-    // ---------------- TMA: key and value tiles, two stages each
+    // ---------------- TMA: key tiles (three stages) and value tiles (two)
+    // The two rings advance on their own: a key tile goes out as soon as its
+    // stage is free (S of the tile three back has completed), a value tile
+    // as soon as its stage is (PV of the tile two back), never before its
+    // key tile; the thread polls both without blocking on either, sleeping
+    // briefly between polls.
     if (lane == 0) {
-      int t = n_early;  // local tile index: key tile t_begin + t
+      int tk = n_early, tv = n_early;  // next key / value tile to load
       bool ok = true;
-      for (; t < nt && ok; ++t) {
-        const int s = t & 1;
-        const uint32_t ph = (uint32_t)(t >> 1) & 1u;
-        const int y = (int)(st + (int64_t)(t_begin + t) * BN);
-        if (!wait_or_abort(&k_empty[s], ph ^ 1u, abort_flag)) { ok = false; break; }
-        mbar_expect_tx(&k_full[s], kTileBytes);
-        for (int kc = 0; kc < 2; ++kc)
-          tma_load_2d(smem + kKOff + s * kTileBytes + kc * 16384, &tmK, &k_full[s], h * DH + kc * 64, y);
-        if (!wait_or_abort(&v_empty[s], ph ^ 1u, abort_flag)) {
-          ok = false;
-          mbar_wait(&k_full[s], ph);  // the key tile issued above lands first
-          break;
+      uint32_t idle = 0;
+      while (tk < nt || tv < nt) {
+        bool moved = false;
+        if (tk < nt) {
+          const int ks = tk % kKStages;
+          if (mbar_test_wait(&k_empty[ks], ((uint32_t)(tk / kKStages) & 1u) ^ 1u)) {
+            const int y = (int)(st + (int64_t)(t_begin + tk) * BN);
+            mbar_expect_tx(&k_full[ks], kTileBytes);
+            for (int kc = 0; kc < 2; ++kc)
+              tma_load_2d(smem + kKOff + ks * kTileBytes + kc * 16384, &tmK, &k_full[ks], h * DH + kc * 64, y);
+            ++tk;
+            moved = true;
+          }
         }
-        mbar_expect_tx(&v_full[s], kTileBytes);
-        for (int kc = 0; kc < 2; ++kc)
-          tma_load_2d(smem + kVOff + s * kTileBytes + kc * 16384, &tmV, &v_full[s], h * DH + kc * 64, y);
+        if (tv < tk) {
+          const int vs = tv & 1;
+          if (mbar_test_wait(&v_empty[vs], ((uint32_t)(tv >> 1) & 1u) ^ 1u)) {
+            const int y = (int)(st + (int64_t)(t_begin + tv) * BN);
+            mbar_expect_tx(&v_full[vs], kTileBytes);
+            for (int kc = 0; kc < 2; ++kc)
+              tma_load_2d(smem + kVOff + vs * kTileBytes + kc * 16384, &tmV, &v_full[vs], h * DH + kc * 64, y);
+            ++tv;
+            moved = true;
+          }
+        }
+        if (moved) {
+          idle = 0;
+        } else if (++idle > kSpinLimit || ((idle & 255) == 255 && *abort_flag)) {
+          if (idle > kSpinLimit) *abort_flag = 1;
+          ok = false;
+          break;
+        } else {
+          __nanosleep(64);  // leave the issue slots to the softmax warps on this sub-partition
+        }
       }
       if (!ok) {
-        // let the tiles already issued land before the CTA can exit
-        for (int j = max(0, t - 2); j < t; ++j) {
-          mbar_wait(&k_full[j & 1], (uint32_t)(j >> 1) & 1u);
-          mbar_wait(&v_full[j & 1], (uint32_t)(j >> 1) & 1u);
-        }
+        // let the tiles already issued land before the CTA can exit (a key
+        // tile is issued at most three tiles ahead of its use, a value tile two)
+        for (int j = max(0, tk - kKStages); j < tk; ++j) mbar_wait(&k_full[j % kKStages], (uint32_t)(j / kKStages) & 1u);
+        for (int j = max(0, tv - 2); j < tv; ++j) mbar_wait(&v_full[j & 1], (uint32_t)(j >> 1) & 1u);
         set_err(a.err, MEDUSA_DEVERR_TIMEOUT);
       }
     }
@@ -390,10 +416,13 @@ __global__ void __cluster_dims__(CL, 1, 1) __launch_bounds__(kThreads, 1)
       const uint32_t idS = idesc_bf16_f32(BMR, BN);
       const uint32_t idPV = idesc_bf16_f32(BMR, DH) | (1u << 16);  // B (V) MN-major
       bool ok = true;
+      // S_t into accumulator t & 1, which P_{t-2} occupied until PV_{t-2}
+      // completed
       auto issue_s = [&](int t) {
-        const int s = t & 1;
-        const uint32_t ph = (uint32_t)(t >> 1) & 1u;
-        if (!wait_or_abort(&k_full[s], ph, abort_flag) || !wait_or_abort(&s_empty[s], ph ^ 1u, abort_flag)) {
+        const int s = t & 1, ks = t % kKStages;
+        const uint32_t kph = (uint32_t)(t / kKStages) & 1u;
+        if (!wait_or_abort(&k_full[ks], kph, abort_flag) ||
+            (t >= 2 && !wait_or_abort(&pv_full[s], (uint32_t)((t - 2) >> 1) & 1u, abort_flag))) {
           ok = false;
           return;
         }
@@ -401,12 +430,12 @@ __global__ void __cluster_dims__(CL, 1, 1) __launch_bounds__(kThreads, 1)
         const uint32_t dS = tmem_base + (uint32_t)s * BN;
         for (int kc = 0; kc < 2; ++kc) {
           const uint64_t da = desc_kmajor_sw128(sbase + kQOff + kc * 16384);
-          const uint64_t db = desc_kmajor_sw128(sbase + kKOff + s * kTileBytes + kc * 16384);
+          const uint64_t db = desc_kmajor_sw128(sbase + kKOff + ks * kTileBytes + kc * 16384);
 #pragma unroll
           for (int kk = 0; kk < 4; ++kk)  // +32 bytes of K per instruction
             umma_bf16(dS, da + (uint64_t)(kk * 2), db + (uint64_t)(kk * 2), idS, (kc | kk) != 0);
         }
-        umma_commit(&k_empty[s]);  // the key stage is free once these MMAs have read it
+        umma_commit(&k_empty[ks]);  // the key stage is free once these MMAs have read it
         umma_commit(&s_full[s]);
       };
       if (nt > 0) issue_s(0);
@@ -422,14 +451,12 @@ __global__ void __cluster_dims__(CL, 1, 1) __launch_bounds__(kThreads, 1)
         }
         tc_fence_after();
         const uint32_t dPV = tmem_base + (uint32_t)(2 + s) * BN;  // two accumulators in turn
-        for (int kc = 0; kc < 2; ++kc) {
-          const uint64_t da = desc_kmajor_sw128(sbase + kPOff + kc * 16384);
+        const uint32_t aP = tmem_base + (uint32_t)s * BN;         // P_t: keys 2c, 2c+1 in column c
 #pragma unroll
-          for (int kk = 0; kk < 4; ++kk) {
-            const int key0 = kc * 64 + kk * 16;  // 16 keys per instruction: two 8-row groups of V
-            const uint64_t db = desc_mnmajor_sw128(sbase + kVOff + s * kTileBytes + key0 * 128, 16384, 1024);
-            umma_bf16(dPV, da + (uint64_t)(kk * 2), db, idPV, (kc | kk) != 0);
-          }
+        for (int j = 0; j < BN / 16; ++j) {
+          const int key0 = j * 16;  // 16 keys per instruction: eight columns of P, two 8-row groups of V
+          const uint64_t db = desc_mnmajor_sw128(sbase + kVOff + s * kTileBytes + key0 * 128, 16384, 1024);
+          umma_bf16_ts(dPV, aP + (uint32_t)(j * 8), db, idPV, j != 0);
         }
         umma_commit(&v_empty[s]);
         umma_commit(&pv_full[s]);
@@ -452,7 +479,6 @@ __global__ void __cluster_dims__(CL, 1, 1) __launch_bounds__(kThreads, 1)
     const int hh = (warp - 2) >> 2;  // key half of S_t, column half of PV_t
     const int r = 32 * g + lane;
     const uint32_t trow = tmem_base + ((uint32_t)(32 * g) << 16) + (uint32_t)(hh * 64);
-    const uint32_t preg = sbase + kPOff + (uint32_t)hh * 16384;  // P rows, keys hh*64 .. hh*64+63
     const uint32_t* myanc = ancs + r * kMaxWords;
     float o[64];
 #pragma unroll
@@ -523,29 +549,25 @@ __global__ void __cluster_dims__(CL, 1, 1) __launch_bounds__(kThreads, 1)
       const float mn = fmaxf(m, mt);
       const float base = mn == -INFINITY ? 0.f : mn;
       const float alpha = exp2f(m - base);  // 0 while nothing was visible
-      // P_{t-1} stays in shared memory until PV_{t-1} has completed (it
-      // normally has: it was issued a tile's softmax ago)
-      if (t > 0) {
-        const bool pgot = wait_or_abort(&pv_full[(t - 1) & 1], (uint32_t)((t - 1) >> 1) & 1u, abort_flag);
-        if (__any_sync(0xffffffffu, !pgot)) { ok = false; break; }
-        __syncwarp();
-      }
-      // p = 2^(s - max) into P (bf16, swizzled K-major), and its sum (pairs
-      // of lanes in f32x2)
+      // p = 2^(s - max) as bf16 pairs over this thread's half of S_t in
+      // tensor memory (columns hh*32 .. hh*32+31 of accumulator t & 1: every
+      // thread has read its S_t before the row-max exchange above), and its
+      // sum (pairs of lanes in f32x2)
       float sa[2] = {0.f, 0.f}, sb[2] = {0.f, 0.f};
 #pragma unroll
-      for (int ch = 0; ch < 8; ++ch) {  // 16-byte chunks of the 128-byte row: 8 keys each
-        uint32_t pk[4];
+      for (int hq = 0; hq < 2; ++hq) {  // 32 keys, 16 columns at a time
+        uint32_t pk[16];
 #pragma unroll
-        for (int i = 0; i < 4; ++i) {
-          float x0 = __uint_as_float(v[8 * ch + 2 * i]), x1 = __uint_as_float(v[8 * ch + 2 * i + 1]);
+        for (int i = 0; i < 16; ++i) {
+          float x0 = __uint_as_float(v[32 * hq + 2 * i]), x1 = __uint_as_float(v[32 * hq + 2 * i + 1]);
           add2(x0, x1, -base, -base);
           const float p0 = ex2_ftz(x0), p1 = ex2_ftz(x1);
           add2(sa[i & 1], sb[i & 1], p0, p1);
           pk[i] = pack2_bf16(p0, p1);
         }
-        st_shared_v4(sw128(preg, r, ch), make_uint4(pk[0], pk[1], pk[2], pk[3]));
+        tmem_st_32x32b_x16(tmem_base + ((uint32_t)(32 * g) << 16) + (uint32_t)(s * BN + hh * 32 + hq * 16), pk);
       }
+      tmem_st_wait();
       l = l * alpha + ((sa[0] + sb[0]) + (sa[1] + sb[1]));
       m = mn;
       // the last tile's value rows past the sequence's keys are zeroed (their
@@ -556,12 +578,15 @@ __global__ void __cluster_dims__(CL, 1, 1) __launch_bounds__(kThreads, 1)
           for (int c = 0; c < 8; ++c) st_shared_v4(vrow + c * 16, make_uint4(0, 0, 0, 0));
         }
       }
-      fence_async_smem();  // P (and zeroed V rows) are read by the tensor cores
+      fence_async_smem();  // zeroed V rows are read by the tensor cores
       tc_fence_before();
-      mbar_arrive(&s_empty[s]);
       mbar_arrive(p_full);
-      // PV_{t-1} folds in while PV_t runs
+      // PV_{t-1} folds in while PV_t runs (it normally has completed: it was
+      // issued a tile's softmax ago)
       if (t > 0) {
+        const bool pgot = wait_or_abort(&pv_full[(t - 1) & 1], (uint32_t)((t - 1) >> 1) & 1u, abort_flag);
+        if (__any_sync(0xffffffffu, !pgot)) { ok = false; break; }
+        __syncwarp();
         tc_fence_after();
         fold(t - 1, a_prev);
       }
