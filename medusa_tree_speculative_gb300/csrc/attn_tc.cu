@@ -195,13 +195,17 @@ __global__ void __cluster_dims__(CL, 1, 1) __launch_bounds__(kThreads, 1)
   uint64_t* v_full = bars + 6;   // [2]
   uint64_t* v_empty = bars + 8;  // [2]
   uint64_t* s_full = bars + 10;  // [2] MMA -> softmax: S_t ready
-  uint64_t* p_full = bars + 12;  // softmax -> MMA: P_t written over S_t (256 arrivals)
-  uint64_t* pv_full = bars + 13; // [2] MMA -> softmax: PV_t ready (accumulator t & 1)
-  uint64_t* pv_empty = bars + 15;// [2] softmax -> MMA: PV accumulator read (256 arrivals)
-  uint64_t* mma_done = bars + 17;// every MMA issued so far has completed
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 18);
-  int* s_abort = reinterpret_cast<int*>(bars + 19);
-  uint64_t* xm_full = bars + 20; // [2] softmax halves: the row's partial maxima written (256 arrivals)
+  // [2] softmax -> MMA: P_t written over S_t (256 arrivals).  Two barriers,
+  // tile t on t & 1: the softmax may finish P_{t+1} before the MMA thread
+  // has waited for P_t (P_{t+1} does not wait for PV_t), and with one
+  // barrier the phase the MMA thread waits for would already be two back.
+  uint64_t* p_full = bars + 12;
+  uint64_t* pv_full = bars + 14; // [2] MMA -> softmax: PV_t ready (accumulator t & 1)
+  uint64_t* pv_empty = bars + 16;// [2] softmax -> MMA: PV accumulator read (256 arrivals)
+  uint64_t* mma_done = bars + 18;// every MMA issued so far has completed
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 19);
+  int* s_abort = reinterpret_cast<int*>(bars + 20);
+  uint64_t* xm_full = bars + 21; // [2] softmax halves: the row's partial maxima written (256 arrivals)
   float* xmax = reinterpret_cast<float*>(smem + kXOff);  // [2 tiles][2 halves][128 rows]
   uint32_t* ancs = reinterpret_cast<uint32_t*>(smem + kAncOff);
   float* cs = reinterpret_cast<float*>(smem + kCsOff);
@@ -238,11 +242,11 @@ __global__ void __cluster_dims__(CL, 1, 1) __launch_bounds__(kThreads, 1)
       mbar_init(&v_full[i], 1);
       mbar_init(&v_empty[i], 1);
       mbar_init(&s_full[i], 1);
+      mbar_init(&p_full[i], kSoftThreads);
       mbar_init(&pv_full[i], 1);
       mbar_init(&pv_empty[i], kSoftThreads);
       mbar_init(&xm_full[i], kSoftThreads);
     }
-    mbar_init(p_full, kSoftThreads);
     mbar_init(mma_done, 1);
     fence_barrier_init();
     *s_abort = 0;
@@ -444,7 +448,7 @@ __global__ void __cluster_dims__(CL, 1, 1) __launch_bounds__(kThreads, 1)
       for (; t < nt && ok; ++t) {
         const int s = t & 1;
         const uint32_t ph = (uint32_t)(t >> 1) & 1u;
-        if (!wait_or_abort(p_full, (uint32_t)t & 1u, abort_flag) || !wait_or_abort(&v_full[s], ph, abort_flag) ||
+        if (!wait_or_abort(&p_full[s], ph, abort_flag) || !wait_or_abort(&v_full[s], ph, abort_flag) ||
             !wait_or_abort(&pv_empty[s], ph ^ 1u, abort_flag)) {
           ok = false;
           break;
@@ -580,7 +584,7 @@ __global__ void __cluster_dims__(CL, 1, 1) __launch_bounds__(kThreads, 1)
       }
       fence_async_smem();  // zeroed V rows are read by the tensor cores
       tc_fence_before();
-      mbar_arrive(p_full);
+      mbar_arrive(&p_full[s]);
       // PV_{t-1} folds in while PV_t runs (it normally has completed: it was
       // issued a tile's softmax ago)
       if (t > 0) {
