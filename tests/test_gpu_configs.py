@@ -137,3 +137,38 @@ def test_config_step(M, name):
         assert nt[b, 0] == int(to_host(st.next_root)[b])
         for n in range(1, T):
             assert nt[b, n] == tk[b, ot.depth[n] - 1, ot.rank[n] - 1]
+
+
+def test_step_repeated_in_a_graph(M):
+    """Thirty verify steps at L = 4096 replayed from one CUDA graph, the
+    attention on its forked branch beside the LM head (the bench's launch):
+    no bounded wait gives up (the device error word stays zero) and every
+    step recomputes the same attention output and accepted path.  The
+    attention's barriers are timing-sensitive: a hand-off whose phase could be
+    overtaken shows up here as MEDUSA_DEVERR_TIMEOUT."""
+    from medusa_tree_speculative_gb300 import step
+
+    w = workloads.get("vicuna7b_L4096_tree64")
+    ot, dtree = both_trees(M, _tree_spec(w))
+    wts = synth.make_weights(w, 0)
+    x = synth.make_step(w, ot.T, 0)
+    dev = {k: to_dev(v) for k, v in x.items()}
+    wd = {k: (None if v is None else to_dev(v)) for k, v in wts.items()}
+    st = step.VerifyStep(w, wd, dtree, max_prefix=int(x["prefix_len"].max()))
+    prefix0 = dev["prefix_len"].clone()
+    s, side = torch.cuda.Stream(), torch.cuda.Stream()
+    with torch.cuda.stream(s):
+        st.run(dev, s, side_stream=side)
+    torch.cuda.synchronize()
+    ref_out, ref_len = st.out.clone(), st.accept_len.clone()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=s):
+        for _ in range(30):
+            dev["prefix_len"].copy_(prefix0)
+            st.run(dev, s, side_stream=side)
+    with torch.cuda.stream(s):
+        dev["prefix_len"].copy_(prefix0)
+        g.replay()
+    torch.cuda.synchronize()
+    assert int(st.err.item()) == 0
+    assert torch.equal(st.out, ref_out) and torch.equal(st.accept_len, ref_len)
