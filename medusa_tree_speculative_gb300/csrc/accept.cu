@@ -133,7 +133,7 @@ __global__ void __launch_bounds__(kRowThreads) accept_rowstat_kernel(const __gri
   if ((V & 3) == 0) {
     const float4* z4 = reinterpret_cast<const float4*>(z);
     const int n4 = V >> 2, lo = (int)((int64_t)n4 * half / kRowSplit), hi = (int)((int64_t)n4 * (half + 1) / kRowSplit);
-    for (int i = lo + threadIdx.x; i < hi; i += kRowLoads * kRowThreads) {
+    for (int i = lo + threadIdx.x; i < hi && !TYPICAL; i += kRowLoads * kRowThreads) {  // greedy: argmax only
       float4 r[kRowLoads];
 #pragma unroll
       for (int u = 0; u < kRowLoads; ++u) {
@@ -149,6 +149,44 @@ __global__ void __launch_bounds__(kRowThreads) accept_rowstat_kernel(const __gri
           consume(r[u].z, 4 * ii + 2);
           consume(r[u].w, 4 * ii + 3);
         }
+      }
+    }
+    for (int i = lo + threadIdx.x; i < hi && TYPICAL; i += kRowLoads * kRowThreads) {
+      float4 r[kRowLoads];
+#pragma unroll
+      for (int u = 0; u < kRowLoads; ++u) {
+        const int ii = i + u * kRowThreads;
+        r[u] = ii < hi ? __ldg(z4 + ii) : make_float4(-INFINITY, -INFINITY, -INFINITY, -INFINITY);
+      }
+      // the round's values are all in registers: argmax, then (typical) the
+      // round's max and its sums as independent exponentials, merged into the
+      // running softmax once per round instead of once per value
+      float rm = -INFINITY;
+#pragma unroll
+      for (int u = 0; u < kRowLoads; ++u) {
+        const int ii = i + u * kRowThreads;
+        const float e[4] = {r[u].x, r[u].y, r[u].z, r[u].w};
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+          if (ii < hi && ranks_before(e[q], 4 * ii + q, bv, bi)) { bv = e[q]; bi = 4 * ii + q; }
+          rm = fmaxf(rm, e[q]);  // padding values are -inf
+        }
+      }
+      if (rm > -INFINITY) {
+        const float my = rm * inv_temp;  // the round's max of y = z / temperature
+        float rS = 0.f, rA = 0.f;
+#pragma unroll
+        for (int u = 0; u < kRowLoads; ++u) {
+          const float e[4] = {r[u].x, r[u].y, r[u].z, r[u].w};
+#pragma unroll
+          for (int q = 0; q < 4; ++q) {
+            const float d = e[q] * inv_temp - my;  // -inf for a padding value: exp 0, and 0 * -inf skipped
+            const float x = expf(d);
+            rS += x;
+            rA += x > 0.f ? x * d : 0.f;
+          }
+        }
+        sf = soft_merge(sf, Soft{my, rS, rA});
       }
     }
   } else {
