@@ -273,14 +273,17 @@ int medusa_lm_head_tile(const void* w_lm, void* w_tiled, int d, int V,
  * f32 accepts MEDUSA_W_ROWS only.  The tensor-core kernel's bounded on-chip
  * waits report MEDUSA_DEVERR_TIMEOUT through err (nullable) if they ever
  * give up.  Rows beyond 256 are processed in balanced chunks of at most 256
- * (the weights are streamed once per chunk). */
+ * that multiply the same weight k-block (the weights are read once); 129 to
+ * 256 rows run on clusters of two CTAs (one tcgen05 MMA of M = 256 over a
+ * vocabulary tile of each, each CTA loading half of the hidden rows). */
 int medusa_lm_head_verify(const void* hidden, const void* w_lm, float* logits,
                           int rows, int d, int V, medusa_dtype dtype,
                           medusa_w_layout w_layout, void* workspace,
                           size_t workspace_bytes, int32_t* err, void* stream);
 
-/* CTAs (one per SM) that medusa_lm_head_verify launches for bf16 `rows` x V
- * on the current device, 0 for invalid sizes.  A caller that runs other work
+/* CTAs (one per SM; both CTAs of each pair counted) that
+ * medusa_lm_head_verify launches for bf16 `rows` x V on the current device,
+ * 0 for invalid sizes.  A caller that runs other work
  * beside the LM head (the tree attention of the same step) sizes it to the
  * SMs left free.  No counterpart in the pages. */
 int medusa_lm_head_ctas(int rows, int V);

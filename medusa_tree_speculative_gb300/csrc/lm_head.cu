@@ -35,12 +35,16 @@
 // all rows"): M runs over the stacked W1 rows of the heads in use and each
 // accumulator becomes u = bf16(SiLU(acc + b1) + h); the residual values are
 // staged in shared memory by the idle epilogue warps during the main loop.
+// From 129 to 256 tree rows the logits run on CTA pairs instead
+// (lm_head_pair_kernel, tcgen05 cta_group::2): one MMA of M = 256 covers a
+// vocabulary tile of each CTA, and each CTA loads half of the hidden rows.
 // f32: plain CUDA-core kernels (one warp per output element).
 #include <cuda.h>
 
 #include <algorithm>
 #include <mutex>
 
+#include "cluster.cuh"
 #include "common.cuh"
 #include "internal.h"
 #include "sm100.cuh"
@@ -485,6 +489,206 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
 }
 
+// ---- the same GEMM on CTA pairs (tcgen05 cta_group::2), logits only
+//
+// Each cluster of two CTAs owns runs of work items of 2 * nt vocabulary
+// tiles; one MMA of M = 256 covers a tile of each CTA (tile (group * nt + j)
+// * 2 + rank) against all of a row chunk, whose hidden k-block is split
+// between the two CTAs' stages (the first npad / 2 rows in the even CTA, the
+// rest in the odd one).  So each SM pulls half of every hidden k-block where
+// the one-CTA kernel pulls all of it: with more tree rows than a weight tile
+// has (256 and more), the hidden k-blocks are most of what an SM loads, and
+// what one SM can pull into shared memory bounds the call.
+//   warp 0     (both CTAs) TMA: its weight tiles and its half of each row
+//              chunk into its own stage; completion is counted on the even
+//              CTA's `full` barrier, which expects both CTAs' bytes;
+//   warp 1     (both CTAs) allocates the pair's tensor memory; in the even
+//              CTA one thread issues the MMAs and commits stage releases and
+//              finished accumulators to the barriers of both CTAs;
+//   warps 2-5  (both CTAs) read their own tensor memory (their 128
+//              vocabulary rows) and store the logits; each warp then arrives
+//              on the even CTA's `tempty`.
+// Every wait is bounded; a CTA that gave up waits 20 us for its copies in
+// flight before the closing cluster barrier, after which the tensor memory
+// is freed.
+__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
+    lm_head_pair_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CUtensorMap tmH,
+                        const __grid_constant__ LmArgs a) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  const uint32_t rank = cluster_rank();            // 0: the CTA that issues the MMAs
+  const int hrows = a.npad / 2;                    // rows of a chunk this CTA holds
+  const uint32_t a_bytes = (uint32_t)a.nt * BM * BK * 2;
+  const uint32_t h_bytes = (uint32_t)hrows * BK * 2;  // one chunk's half k-block
+  const uint32_t stage_bytes = a_bytes + (uint32_t)a.cpi * h_bytes;
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + (size_t)a.stages * stage_bytes);
+  uint64_t* empty = full + a.stages;
+  uint64_t* tfull = empty + a.stages;
+  uint64_t* tempty = tfull + 2;
+  uint64_t* mma_done = tempty + 2;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(mma_done + 1);
+  __shared__ int s_abort;
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < a.stages; ++s) {
+      mbar_init(&full[s], 1);   // the even CTA's expect_tx; both CTAs' bytes
+      mbar_init(&empty[s], 1);  // the pair MMAs that read the stage
+    }
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(&tfull[i], 1);
+      mbar_init(&tempty[i], 2 * 4);  // one arrival per epilogue warp of either CTA
+    }
+    mbar_init(mma_done, 1);
+    fence_barrier_init();
+    s_abort = 0;
+    tma_prefetch_desc(&tmW);
+    tma_prefetch_desc(&tmH);
+  }
+  if (warp == 1) {
+    tmem_alloc_pair(tmem_slot, a.tmem_cols);
+    tmem_relinquish_pair();
+  }
+  tc_fence_before();
+  cluster_sync();  // both CTAs' barriers initialised, the pair's tensor memory allocated
+  tc_fence_after();
+  const uint32_t tmem_base = *tmem_slot;
+  volatile int* abort_flag = &s_abort;
+
+  const int items = a.ngroups * a.nchunks;
+  const int pairs = (int)gridDim.x / 2, pair = (int)blockIdx.x / 2;
+  const int i0 = (int)((long)pair * items / pairs), i1 = (int)((long)(pair + 1) * items / pairs);
+  const uint32_t acc_cols = (uint32_t)(a.nt * a.ncol);
+  const int nkb = a.d / BK;
+
+  if (warp == 0) {
+    // ---------------- TMA producer (both CTAs)
+    if (lane == 0) {
+      const uint32_t full0 = cluster_map(smem_u32(full), 0);  // the even CTA's `full` barriers
+      int it = 0;
+      bool ok = true;
+      for (int item = i0; item < i1 && ok; ++item) {
+        const int r0 = (item % a.nchunks) * a.ncol;
+        int blk[2];
+        for (int j = 0; j < a.nt; ++j) blk[j] = weight_block(a, ((item / a.nchunks) * a.nt + j) * 2 + (int)rank);
+        for (int kb = 0; kb < nkb; ++kb, ++it) {
+          const int s = it % a.stages;
+          const uint32_t ph = (uint32_t)(it / a.stages) & 1u;
+          if (!wait_or_abort(&empty[s], ph ^ 1u, abort_flag)) { ok = false; break; }
+          uint8_t* st = smem + (size_t)s * stage_bytes;
+          if (rank == 0) mbar_expect_tx(&full[s], 2 * stage_bytes);
+          const uint32_t bar = full0 + (uint32_t)s * 8u;
+          for (int j = 0; j < a.nt; ++j) {
+            if (a.tiled)
+              tma_load_2d_pair(st + j * (BM * BK * 2), &tmW, bar, 0, (blk[j] * nkb + kb) * BM);
+            else
+              tma_load_2d_pair(st + j * (BM * BK * 2), &tmW, bar, kb * BK, blk[j] * BM);
+          }
+          for (int c = 0; c < a.cpi; ++c)  // this CTA's half of each row chunk (rows past the last read zeros)
+            tma_load_2d_pair(st + a_bytes + c * h_bytes, &tmH, bar, kb * BK, r0 + c * a.npad + (int)rank * hrows);
+        }
+      }
+      if (!ok) set_err(a.err, MEDUSA_DEVERR_TIMEOUT);
+    }
+  } else if (warp == 1) {
+    // ---------------- MMA issuer (even CTA)
+    if (rank == 0 && lane == 0) {
+      const uint32_t idesc = idesc_bf16_f32(2 * BM, a.npad);
+      int it = 0, local = 0;
+      bool ok = true;
+      for (int item = i0; item < i1 && ok; ++item, ++local) {
+        const int acc = a.nacc == 2 ? local & 1 : 0;
+        const uint32_t aph = (uint32_t)(a.nacc == 2 ? local >> 1 : local) & 1u;
+        bool got = false;  // both CTAs' epilogues have drained the accumulator
+        for (uint32_t i = 0; i < kSpinLimit && !got; ++i) {
+          got = mbar_try_wait_cluster(&tempty[acc], aph ^ 1u);
+          if (!got && (i & 255) == 255 && *abort_flag) break;
+        }
+        if (!got) { *abort_flag = 1; ok = false; break; }
+        tc_fence_after();
+        const uint32_t d_tmem = tmem_base + (uint32_t)acc * acc_cols;
+        for (int kb = 0; kb < nkb; ++kb, ++it) {
+          const int s = it % a.stages;
+          const uint32_t ph = (uint32_t)(it / a.stages) & 1u;
+          if (!wait_or_abort(&full[s], ph, abort_flag)) { ok = false; break; }
+          tc_fence_after();
+          const uint32_t sa = smem_u32(smem + (size_t)s * stage_bytes);
+          for (int j = 0; j < a.nt; ++j) {
+            const uint64_t da = desc_kmajor_sw128(sa + j * (BM * BK * 2));
+            for (int c = 0; c < a.cpi; ++c) {
+              const uint64_t db = desc_kmajor_sw128(sa + a_bytes + c * h_bytes);
+#pragma unroll
+              for (int kk = 0; kk < BK / UK; ++kk)  // +32 bytes of K per instruction
+                umma_bf16_pair(d_tmem + (uint32_t)(j * a.ncol + c * a.npad), da + (uint64_t)(kk * 2),
+                               db + (uint64_t)(kk * 2), idesc, (kb | kk) != 0);
+            }
+          }
+          umma_commit_pair_mc(&empty[s], 0x3);  // both CTAs' stages are free once these MMAs have read them
+        }
+        if (ok) umma_commit_pair_mc(&tfull[acc], 0x3);  // both halves of the accumulator complete
+      }
+      if (!ok) set_err(a.err, MEDUSA_DEVERR_TIMEOUT);
+      // every MMA issued completes before either CTA's stages or tensor memory go away
+      umma_commit_pair(mma_done);
+      if (!mbar_wait(mma_done, 0)) set_err(a.err, MEDUSA_DEVERR_TIMEOUT);
+    }
+  } else {
+    // ---------------- epilogue (both CTAs): TMEM -> registers -> logits
+    const int g = warp & 3;  // this warp may read TMEM lanes 32g .. 32g+31
+    const uint32_t tempty0 = cluster_map(smem_u32(tempty), 0);
+    int local = 0;
+    for (int item = i0; item < i1; ++item, ++local) {
+      const int acc = a.nacc == 2 ? local & 1 : 0;
+      const uint32_t aph = (uint32_t)(a.nacc == 2 ? local >> 1 : local) & 1u;
+      const bool got = wait_or_abort(&tfull[acc], aph, abort_flag);
+      if (__any_sync(0xffffffffu, !got)) {
+        if (lane == 0) set_err(a.err, MEDUSA_DEVERR_TIMEOUT);
+        break;
+      }
+      __syncwarp();
+      tc_fence_after();
+      const int r0 = (item % a.nchunks) * a.ncol;
+      for (int j = 0; j < a.nt; ++j) {
+        const int v = (((item / a.nchunks) * a.nt + j) * 2 + (int)rank) * BM + 32 * g + lane;
+        for (int c = 0; c < a.ncol / 16; ++c) {  // column c * 16 + i holds tree row r0 + c * 16 + i
+          uint32_t r[16];
+          tmem_ld_32x32b_x16(tmem_base + ((uint32_t)(32 * g) << 16) + (uint32_t)acc * acc_cols +
+                                 (uint32_t)(j * a.ncol + c * 16),
+                             r);
+          tmem_ld_wait();
+          if (v < a.V) {
+#pragma unroll
+            for (int i = 0; i < 16; ++i) {
+              const int row = r0 + c * 16 + i;
+              if (row < a.rows) a.logits[(int64_t)row * a.V + v] = __uint_as_float(r[i]);
+            }
+          }
+        }
+      }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive_cluster(tempty0 + (uint32_t)acc * 8u);
+    }
+  }
+  __syncwarp();
+  if (threadIdx.x == 0 && *abort_flag) {
+    // a wait gave up: let the copies this CTA issued land before the pair can exit
+    uint64_t t0, t;
+    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t0));
+    do {
+      __nanosleep(1000);
+      asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+    } while (t - t0 < 20000);
+  }
+  __syncwarp();
+  tc_fence_before();
+  cluster_sync();  // no CTA leaves while the pair's MMAs or the other CTA may still use its memory
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc_pair(tmem_base, a.tmem_cols);
+  }
+}
+
 // Row-major [V][d] -> 128 x 64 tiles (16 bytes per thread, grid-stride);
 // rows past V in the last tile are written as zeros.
 __global__ void __launch_bounds__(256) lm_head_tile_kernel(const uint16_t* __restrict__ w,
@@ -640,8 +844,106 @@ LmPlan plan_tc(int rows, int ntiles, bool mode1, bool stats) {
   return p;
 }
 
+// Pair plan (lm_head_pair_kernel): as plan_tc, with each CTA's stage holding
+// its nt weight tiles and half of every row chunk's hidden k-block.
+LmPlan plan_pair(int rows, int ntiles) {
+  LmPlan p{};
+  const int nct = (rows + kMaxN - 1) / kMaxN;
+  p.npad = ((rows + nct - 1) / nct + 15) / 16 * 16;
+  for (int cpi = std::max(1, std::min(nct, 512 / p.npad)); cpi >= 1; --cpi) {
+    for (int nt = 2; nt >= 1; --nt) {
+      if (nt == 2 && !(2 * cpi * p.npad <= 512 && ntiles > sm_count())) continue;
+      p.cpi = cpi;
+      p.nt = nt;
+      p.ncol = cpi * p.npad;
+      p.stage_bytes = (size_t)nt * BM * BK * 2 + (size_t)cpi * (p.npad / 2) * BK * 2;
+      p.stages = (int)std::min<size_t>(8, (kSmemBudget - 1024 - 256) / p.stage_bytes);
+      if (p.stages >= 3) {
+        p.nchunks = (nct + cpi - 1) / cpi;
+        p.nacc = 2 * nt * p.ncol <= 512 ? 2 : 1;
+        p.ngroups = (ntiles + 2 * nt - 1) / (2 * nt);
+        return p;
+      }
+    }
+  }
+  p.stages = 0;
+  return p;
+}
+
+// The pair kernel serves plain logits for one row chunk of more than 128
+// rows, where it measured faster (256 rows: 63.5 against 66.0 us at d = 4096,
+// 90.1 against 94.5 us at d = 6656).  Below that, and with two chunks, it is
+// not: a pair MMA of M = 256 takes longer than an M = 128 one on each SM,
+// which gives back what the halved hidden k-blocks save (257 rows: 94.2
+// against 92.4 us; one row: 51.2 against 45.8 us).
+constexpr int kPairMinRows = 129;
+
+bool use_pair(const LmArgs& a, int rows) {
+  return a.mode == 0 && a.stat_mode == 0 && rows >= kPairMinRows && rows <= kMaxN &&
+         plan_pair(rows, a.ntiles).stages >= 3;
+}
+
+// CTA pairs that can run at once with one CTA per SM (a GPC with an odd
+// number of SMs leaves one idle), cached per device; half the SMs if the
+// query fails.
+int pair_slots() {
+  static int cached[64] = {0};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return std::max(1, sm_count() / 2);
+  if (cached[dev] > 0) return cached[dev];
+  const int smem = 1024 + (int)kSmemBudget;  // enough to hold one CTA per SM
+  int n = 0;
+  cudaLaunchConfig_t cfg = {};
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = 2;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.gridDim = dim3((unsigned)(2 * std::max(1, sm_count() / 2)));
+  cfg.blockDim = dim3(kThreads);
+  cfg.dynamicSmemBytes = (size_t)smem;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  if (cudaFuncSetAttribute(lm_head_pair_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) != cudaSuccess ||
+      cudaOccupancyMaxActiveClusters(&n, lm_head_pair_kernel, &cfg) != cudaSuccess || n <= 0) {
+    cudaGetLastError();  // clear a failed query
+    n = std::max(1, sm_count() / 2);
+  }
+  cached[dev] = std::min(n, std::max(1, sm_count() / 2));
+  return cached[dev];
+}
+
+// Clusters of the pair plan, each CTA of a cluster with the same number of
+// work items (ceil or floor of items / pairs).
+int pair_grid(const LmPlan& p) {
+  const int items = p.ngroups * p.nchunks, npairs = pair_slots();
+  const int per_pair = (items + npairs - 1) / npairs;
+  return 2 * ((items + per_pair - 1) / per_pair);
+}
+
+int launch_pair(LmArgs& a, const void* w, bool tiled, int64_t wrows, const void* hidden, int rows, int d,
+                cudaStream_t s, const char* fn) {
+  a.rows = rows; a.d = d; a.tiled = tiled;
+  const LmPlan p = plan_pair(rows, a.ntiles);
+  a.nchunks = p.nchunks; a.npad = p.npad; a.cpi = p.cpi; a.ncol = p.ncol;
+  a.nt = p.nt; a.nacc = p.nacc; a.ngroups = p.ngroups; a.stages = p.stages;
+  uint32_t cols = 32;
+  while (cols < (uint32_t)(a.nacc * a.nt * a.ncol)) cols <<= 1;
+  a.tmem_cols = cols;
+  a.oob_block = (int)((wrows + BM - 1) / BM);
+  CUtensorMap tmW, tmH;
+  if (!make_weight_map(&tmW, w, tiled, wrows, d) ||
+      !make_map(&tmH, hidden, (uint64_t)d, (uint64_t)rows, (uint32_t)(a.npad / 2)))
+    return fail(MEDUSA_ERR_CUDA, "%s: cuTensorMapEncodeTiled failed", fn);
+  const size_t smem = 1024 + (size_t)a.stages * p.stage_bytes + 256;  // ring | barriers, tensor-memory slot
+  cudaFuncSetAttribute(lm_head_pair_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  launch_kernel(lm_head_pair_kernel, dim3(pair_grid(p)), dim3(kThreads), smem, s, tmW, tmH, a);
+  return check_launch(fn);
+}
+
 int launch_tc(LmArgs& a, const void* w, bool tiled, int64_t wrows, const void* hidden, int rows, int d,
               cudaStream_t s, const char* fn) {
+  if (use_pair(a, rows)) return launch_pair(a, w, tiled, wrows, hidden, rows, d, s, fn);
   a.rows = rows; a.d = d; a.tiled = tiled;
   const LmPlan p = plan_tc(rows, a.ntiles, a.mode == 1, a.stat_mode != 0);
   if (p.stages < 2) return fail(MEDUSA_ERR_UNSUPPORTED, "%s: shared memory for %d tree rows", fn, rows);
@@ -847,6 +1149,9 @@ extern "C" int medusa_lm_head_verify_heads_hidden(const void* hidden, int rows, 
 
 extern "C" int medusa_lm_head_ctas(int rows, int V) {
   if (rows < 1 || V < 1) return 0;
+  LmArgs a{};
+  a.ntiles = (V + BM - 1) / BM;
+  if (use_pair(a, rows)) return pair_grid(plan_pair(rows, a.ntiles));
   const LmPlan p = plan_tc(rows, (V + BM - 1) / BM, false, false);
   if (p.stages < 2) return 0;
   const int items = p.ngroups * p.nchunks;

@@ -241,6 +241,40 @@ def test_lm_head_tiled_layout(M, case):
         assert np.abs(to_host(a_tiles) - ref).max() <= TOL["bf16"]["logit"] * np.abs(ref).max()
 
 
+PAIR_CASES = [(129, 128, 777), (256, 192, 3000), (200, 4096, 2048), (256, 4096, 32000)]
+
+
+@pytest.mark.parametrize("case", PAIR_CASES, ids=lambda c: "-".join(map(str, c)))
+def test_lm_head_cta_pairs(M, case):
+    """129..256 rows run on CTA pairs (one MMA of M = 256 over a vocabulary
+    tile of each CTA, each CTA holding half of the hidden rows): an odd tile
+    count leaves the last pair's second CTA a tile past V; both weight
+    layouts give the same logits bit for bit, within tolerance of the oracle."""
+    rows, d, V = case
+    h = synth.normal(13, "h", (rows, d), 1.0, "bf16")
+    w = synth.normal(13, "w", (V, d), 1.0 / math.sqrt(d), "bf16")
+    hd, wd = to_dev(h), to_dev(w)
+    assert M.medusa_lm_head_ctas(rows, V) % 2 == 0
+    a_rows = torch.full((rows, V), float("nan"), dtype=torch.float32, device="cuda")
+    a_tiles = torch.full((rows, V), float("nan"), dtype=torch.float32, device="cuda")
+    err = torch.zeros(1, dtype=torch.int32, device="cuda")
+    M.medusa_lm_head_verify(hd, wd, a_rows, err=err)
+    M.medusa_lm_head_verify(hd, M.medusa_lm_head_tile(wd), a_tiles, err=err, layout=M.W_TILES)
+    torch.cuda.synchronize()
+    assert int(err.item()) == 0
+    assert torch.equal(a_rows, a_tiles)
+    if d * V <= 4096 * 2048:
+        ref = oracle.lm_head(h, w)
+        assert np.abs(to_host(a_rows) - ref).max() <= TOL["bf16"]["logit"] * np.abs(ref).max()
+    else:  # sampled logits against the oracle's dot products
+        rng = np.random.default_rng(1)
+        got = to_host(a_rows)
+        scale = np.abs(got).max()
+        for r, v in zip(rng.integers(0, rows, 64), rng.integers(0, V, 64)):
+            want = oracle.lm_head(h[r:r + 1], w[v:v + 1])[0, 0]
+            assert abs(got[r, v] - want) <= TOL["bf16"]["logit"] * scale
+
+
 JOINT_CASES = [
     # rows, d, V, s, bias: plans of 2, 3 and 4 tiles per CTA (the last two at
     # 7B and 13B sizes, checked on sampled rows)
