@@ -422,14 +422,17 @@ def run_native(args, w, rank, world, local_rank):
 def measure_attn_alone(st, x, prefix0, L_list, torch, M, reps=10):
     """The tree attention on its own, as its roofline is judged: the key split
     that fills the GPU (step.tc_key_splits over every SM), L2 flushed before
-    each launch (a 256 MB write), CUDA events around the launch alone; median
-    of `reps`.  The step itself runs it beside the LM head instead."""
+    each launch (a 256 MB buffer written, then read back so that L2 holds its
+    clean lines: after a write alone the dirty lines' write-back lands in the
+    timed launch), CUDA events around the launch alone; median of `reps`.  The
+    step itself runs it beside the LM head instead."""
     from medusa_tree_speculative_gb300 import step
 
     B, T, H, Dh = st.out.shape
     sms = torch.cuda.get_device_properties(st.out.device).multi_processor_count
     ns = step.tc_key_splits(B, H, T, int(max(L_list)), sms)
     flush = torch.empty(256 << 20, dtype=torch.uint8, device=st.out.device)
+    sink = torch.zeros(1, dtype=torch.int64, device=st.out.device)
     s = torch.cuda.Stream(device=st.out.device)
 
     def call():
@@ -443,6 +446,7 @@ def measure_attn_alone(st, x, prefix0, L_list, torch, M, reps=10):
         with torch.cuda.stream(s):
             x["prefix_len"].copy_(prefix0)  # the steps before advanced it by the accepted tokens
             flush.fill_(1)
+            sink.add_(flush.view(torch.int32).sum(dtype=torch.int64))
             e0.record(s)
             call()
             e1.record(s)
@@ -456,7 +460,7 @@ def measure_attn_alone(st, x, prefix0, L_list, torch, M, reps=10):
     kv = 2 * int(np.sum(L_list)) * H * Dh * e
     act = 6 * B * T * H * Dh * e  # q, k_new, v_new read; K', V' appended; out written
     return {"key_splits": ns, "us": us, "kv_bytes": kv, "bytes": kv + act, "gbs": (kv + act) / us / 1e3,
-            "how": "median of %d launches, each after a 256 MB write that flushes L2" % reps}
+            "how": "median of %d launches, each after a 256 MB write and read-back that flush L2" % reps}
 
 
 def measure_rejection(st, x, s, torch, M, reps=20):

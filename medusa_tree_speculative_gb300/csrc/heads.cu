@@ -380,8 +380,9 @@ MDEV void block_select(TopList<S>& L, float (*wv)[S], int (*wi)[S], float* ov, i
 
 // ------------------------------------------------------- W2 pass + top-s --
 // MMA (bf16, several sequences): the rows stream through mma_rows8 in units
-// of eight per CTA (the hidden dimension split over the warps), and one
-// thread per sequence keeps that sequence's running top S (list 0).
+// of eight per CTA (the hidden dimension split over the warps); after each
+// unit warp w sums row w's fragments and lane s inserts sequence s's value
+// into warp w's running top S of that sequence.
 template <typename TE, int NB, int S, bool MMA = false>
 __global__ void __launch_bounds__(kWarps * 32) heads_w2_topk_kernel(const __grid_constant__ HeadsArgs a) {
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -445,7 +446,6 @@ __global__ void __launch_bounds__(kWarps * 32) heads_w2_topk_kernel(const __grid
     const int nch = a.d / 32;
     const int c0 = warp * nch / kWarps, c1 = (warp + 1) * nch / kWarps;
     const int units = (a.V + 7) / 8;
-    const int es = threadIdx.x >> 3, er = threadIdx.x & 7;  // epilogue: sequence, row of the eight
     int g = s_g[0];
     for (int it = 0; g < units; ++it) {
       int gn = units;
@@ -456,20 +456,13 @@ __global__ void __launch_bounds__(kWarps * 32) heads_w2_topk_kernel(const __grid
       part[it & 1][warp][lane] = make_float4(c[0], c[1], c[2], c[3]);
       if (threadIdx.x == 0) s_g[(it + 1) & 1] = gn;
       __syncthreads();
-      if (warp < NB / 4) {  // threads 8 s .. 8 s + 7 hold sequence s's eight rows
-        const int row = row0 + er;
-        float y = -INFINITY;
-        if (es < a.B && row < a.V) {
-          y = frag_sum(part[it & 1], es, er);
-          a.logits[((int64_t)es * a.K + k) * a.V + row] = y;
-        }
-        float yq[8];
-#pragma unroll
-        for (int q = 0; q < 8; ++q) yq[q] = __shfl_sync(0xffffffffu, y, (lane & ~7) + q);
-        if (er == 0 && es < a.B) {
-#pragma unroll
-          for (int q = 0; q < 8; ++q)
-            if (row0 + q < a.V) list_insert<S>(lv[0][es], li[0][es], yq[q], row0 + q);
+      {  // warp w takes row w of the eight, lane s sequence s (into warp w's list of s):
+         // every warp does an equal share, so none lags into the next unit's loads
+        const int row = row0 + warp;
+        if (lane < a.B && lane < NB && row < a.V) {
+          const float y = frag_sum(part[it & 1], lane, warp);
+          a.logits[((int64_t)lane * a.K + k) * a.V + row] = y;
+          list_insert<S>(lv[warp][lane], li[warp][lane], y, row);
         }
       }
       g = s_g[(it + 1) & 1];
