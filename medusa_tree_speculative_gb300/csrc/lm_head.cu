@@ -62,6 +62,7 @@ constexpr int kThreads = 192;  // 6 warps
 constexpr int kMaxN = 256;     // tree rows per chunk (MMA N)
 constexpr int kMaxTiles = 4;   // weight tiles per work item (sharing each hidden k-block)
 constexpr size_t kSmemBudget = 200 * 1024;
+constexpr int kMaxXRows = 2;   // rows past 256 formed on the CUDA cores (XROWS plan)
 
 struct LmArgs {
   float* logits;
@@ -103,6 +104,11 @@ struct LmArgs {
   // second map, G = gridDim.x; mode 0 epilogue on the former (V rows), mode 1
   // on the latter (Vu = used heads * d rows)
   int lm_tiles, w1_tiles, tiled1, Vu;
+  // rows past one 256-row chunk (1 .. kMaxXRows; lm_head_tc_kernel<.., .., true>):
+  // their hidden k-block sits at byte xr_off of each stage and the epilogue
+  // warps form their logits on the CUDA cores from the same weight stage
+  int xr;
+  uint32_t xr_off;
   int32_t* err;
 };
 
@@ -142,6 +148,12 @@ MDEV StatRec transpose_reduce(StatRec (&x)[16], int lane, float inv_temp) {
   tr_step<TYP, 2, 2>(x, lane, inv_temp);
   return stat_merge<TYP>(x[0], rec_shfl<TYP>(x[0], 1), inv_temp);
 }
+MDEV uint4 lds_v4(uint32_t addr) {
+  uint4 v;
+  asm volatile("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4];\n" : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "r"(addr));
+  return v;
+}
+
 MDEV int tr_column(int lane) {
   return ((lane >> 4) & 1) * 8 + ((lane >> 3) & 1) * 4 + ((lane >> 2) & 1) * 2 + ((lane >> 1) & 1);
 }
@@ -210,16 +222,20 @@ MDEV bool wait_or_abort(uint64_t* bar, uint32_t parity, volatile int* abort_flag
 // STATS: the epilogue also produces the acceptance statistics (a separate
 // instantiation, so that the plain path keeps its registers and barriers).
 // JOINT: one work item per CTA mixing W and W1 tiles (tile_src).
-template <bool STATS, bool JOINT>
+// XROWS: 257 .. 256 + kMaxXRows rows: one 256-row chunk on the tensor cores
+// and the a.xr rows past it on the CUDA cores of the epilogue warps, which
+// read each weight stage too (the third map is then the extra rows' hidden).
+template <bool STATS, bool JOINT, bool XROWS = false>
 __global__ void __launch_bounds__(kThreads, 1)
     lm_head_tc_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CUtensorMap tmH,
                       const __grid_constant__ CUtensorMap tmW1, const __grid_constant__ LmArgs a) {
   static_assert(!(STATS && JOINT), "the joint launch has no statistics epilogue");
+  static_assert(!(XROWS && (STATS || JOINT)), "extra rows: plain logits only");
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   const uint32_t a_bytes = (uint32_t)a.nt * BM * BK * 2;  // nt W tiles, 16 KB each
   const uint32_t b_bytes = (uint32_t)a.ncol * BK * 2;
-  const uint32_t stage_bytes = a_bytes + b_bytes;
+  const uint32_t stage_bytes = a_bytes + b_bytes + (XROWS ? 16u * BK * 2 : 0u);  // XROWS: a 16-row box at xr_off
   uint64_t* full = reinterpret_cast<uint64_t*>(smem + (size_t)a.stages * stage_bytes);
   uint64_t* empty = full + a.stages;
   uint64_t* tfull = empty + a.stages;
@@ -235,7 +251,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (threadIdx.x == 0) {
     for (int s = 0; s < a.stages; ++s) {
       mbar_init(&full[s], 1);
-      mbar_init(&empty[s], 1);
+      mbar_init(&empty[s], XROWS ? 1 + 4 : 1);  // XROWS: the MMAs and the four epilogue warps read it
     }
     for (int i = 0; i < 2; ++i) {
       mbar_init(&tfull[i], 1);
@@ -245,7 +261,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     s_abort = 0;
     tma_prefetch_desc(&tmW);
     tma_prefetch_desc(&tmH);
-    if (JOINT) tma_prefetch_desc(&tmW1);
+    if (JOINT || XROWS) tma_prefetch_desc(&tmW1);
   }
   if (warp == 1) {
     tmem_alloc(tmem_slot, a.tmem_cols);
@@ -295,6 +311,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           else
             for (int c = 0; c < a.cpi; ++c)  // the item's row chunks (rows past the last read zeros)
               tma_load_2d(st + a_bytes + c * (a.npad * BK * 2), &tmH, &full[s], kb * BK, r0 + c * a.npad);
+          if (XROWS) tma_load_2d(st + a.xr_off, &tmW1, &full[s], kb * BK, a.npad);  // the rows past the chunk
         }
       }
       if (!ok) {
@@ -393,10 +410,68 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
     };
     if ((JOINT || a.mode == 1) && i0 < i1) load_res(i0);
-    int local = 0;
+    int local = 0, xit = 0;
     for (int item = i0; item < i1; ++item, ++local) {
       const int acc = a.nacc == 2 ? local & 1 : 0;
       const uint32_t aph = (uint32_t)(a.nacc == 2 ? local >> 1 : local) & 1u;
+      // XROWS: the rows past the chunk against this thread's weight row of
+      // each tile, stage by stage beside the MMAs (each stage released by
+      // the four warps and the MMAs); 16-byte chunk c of a row r of a
+      // 128-byte-swizzled box sits at chunk c ^ (r & 7)
+      float xacc[2][kMaxXRows];
+      if constexpr (XROWS) {
+#pragma unroll
+        for (int t = 0; t < 2; ++t)
+#pragma unroll
+          for (int j = 0; j < kMaxXRows; ++j) xacc[t][j] = 0.f;
+        const int rr = 32 * g + lane;
+        bool xok = true;
+        for (int kb = 0; kb < nkb; ++kb, ++xit) {
+          const int s = xit % a.stages;
+          const bool xgot = wait_or_abort(&full[s], (uint32_t)(xit / a.stages) & 1u, abort_flag);
+          if (__any_sync(0xffffffffu, !xgot)) { xok = false; break; }
+          const uint32_t st = smem_u32(smem + (size_t)s * stage_bytes);
+          // the weight row of each tile first (16 loads in flight), then each
+          // extra row's k-block (8 more), two partial sums per tile
+          uint4 wr0[8], wr1[8];
+#pragma unroll
+          for (int c = 0; c < 8; ++c) wr0[c] = lds_v4(st + rr * 128 + ((c ^ (rr & 7)) << 4));
+#pragma unroll
+          for (int c = 0; c < 8; ++c)
+            wr1[c] = a.nt == 2 ? lds_v4(st + BM * BK * 2 + rr * 128 + ((c ^ (rr & 7)) << 4)) : make_uint4(0u, 0u, 0u, 0u);
+#pragma unroll
+          for (int j = 0; j < kMaxXRows; ++j) {
+            if (j < a.xr) {
+              uint4 hv[8];
+#pragma unroll
+              for (int c = 0; c < 8; ++c) hv[c] = lds_v4(st + a.xr_off + j * 128 + ((c ^ (j & 7)) << 4));
+              float p0 = 0.f, q0 = 0.f, p1 = 0.f, q1 = 0.f;
+#pragma unroll
+              for (int c = 0; c < 8; ++c) {
+                const uint32_t h4[4] = {hv[c].x, hv[c].y, hv[c].z, hv[c].w};
+                const uint32_t a4[4] = {wr0[c].x, wr0[c].y, wr0[c].z, wr0[c].w};
+                const uint32_t b4[4] = {wr1[c].x, wr1[c].y, wr1[c].z, wr1[c].w};
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                  const float hl = bf16_lo(h4[e]), hh = bf16_hi(h4[e]);
+                  p0 = fmaf(bf16_lo(a4[e]), hl, p0);
+                  q0 = fmaf(bf16_hi(a4[e]), hh, q0);
+                  p1 = fmaf(bf16_lo(b4[e]), hl, p1);
+                  q1 = fmaf(bf16_hi(b4[e]), hh, q1);
+                }
+              }
+              xacc[0][j] += p0 + q0;
+              xacc[1][j] += p1 + q1;
+            }
+          }
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&empty[s]);
+        }
+        if (!xok) {
+          if (lane == 0) set_err(a.err, MEDUSA_DEVERR_TIMEOUT);
+          break;
+        }
+      }
       const bool got = wait_or_abort(&tfull[acc], aph, abort_flag);
       // with statistics the four warps share named barriers, so they take one decision
       if (STATS ? epilogue_any(!got) : __any_sync(0xffffffffu, !got)) {
@@ -455,6 +530,19 @@ __global__ void __launch_bounds__(kThreads, 1)
                   a.u[((int64_t)row * a.K + k) * a.d + j] = f32_to_bf16_bits(silu + h);
                 }
               }
+            }
+          }
+        }
+      }
+      if constexpr (XROWS) {
+#pragma unroll
+        for (int t = 0; t < 2; ++t) {
+          const int v = tile_src<JOINT>(a, item, t).v0 + 32 * g + lane;
+          if (t < a.nt && v < a.V) {
+#pragma unroll
+            for (int j = 0; j < kMaxXRows; ++j) {
+              const int row = r0 + a.npad + j;
+              if (j < a.xr && row < a.rows) a.logits[(int64_t)row * a.V + v] = xacc[t][j];
             }
           }
         }
@@ -941,9 +1029,62 @@ int launch_pair(LmArgs& a, const void* w, bool tiled, int64_t wrows, const void*
   return check_launch(fn);
 }
 
+// Extra-rows plan (lm_head_tc_kernel<false, false, true>): 257 .. 256 +
+// kMaxXRows rows as one 256-row chunk, so that every weight k-block takes
+// four MMAs per tile where two chunks of 144 rows took eight (the MMAs
+// bounded the two-chunk call: an instruction of M = 128 costs about the same
+// at N = 144 as at N = 256), and the rows past it on the CUDA cores of the
+// epilogue warps, which read each weight stage beside the MMAs.  Each such
+// row costs the epilogue warps about 0.4 us per 64-wide k-block, so beyond
+// two of them they, not the MMAs, would set the pace (measured 257 rows:
+// 79.9 against 92.4 us at d = 4096; 260 rows: 157.7 against 92.2 us).
+struct XPlan {
+  int nt, stages, grid;
+  size_t stage_bytes;
+};
+XPlan plan_xrows(int ntiles) {
+  XPlan p{};
+  p.nt = ntiles > sm_count() ? 2 : 1;  // two tiles on one 512-column accumulator share each hidden k-block
+  p.stage_bytes = (size_t)p.nt * BM * BK * 2 + (size_t)kMaxN * BK * 2 + 16 * BK * 2;
+  p.stages = (int)std::min<size_t>(8, (kSmemBudget - 1024 - 256) / p.stage_bytes);
+  const int items = (ntiles + p.nt - 1) / p.nt;
+  const int per_cta = (items + sm_count() - 1) / sm_count();
+  p.grid = (items + per_cta - 1) / per_cta;
+  return p;
+}
+
+bool use_xrows(const LmArgs& a, int rows) {
+  return a.mode == 0 && a.stat_mode == 0 && rows > kMaxN && rows <= kMaxN + kMaxXRows &&
+         plan_xrows(a.ntiles).stages >= 3;
+}
+
+int launch_xrows(LmArgs& a, const void* w, bool tiled, int64_t wrows, const void* hidden, int rows, int d,
+                 cudaStream_t s, const char* fn) {
+  const XPlan p = plan_xrows(a.ntiles);
+  a.rows = rows; a.d = d; a.tiled = tiled;
+  a.npad = kMaxN; a.cpi = 1; a.ncol = kMaxN; a.nchunks = 1;
+  a.nt = p.nt; a.nacc = 1; a.stages = p.stages;
+  a.ngroups = (a.ntiles + a.nt - 1) / a.nt;
+  a.xr = rows - kMaxN;
+  a.xr_off = (uint32_t)((size_t)a.nt * BM * BK * 2 + (size_t)kMaxN * BK * 2);
+  a.part_off = (uint32_t)align_up((size_t)a.stages * p.stage_bytes + 1024, 16);
+  a.tmem_cols = a.nt == 2 ? 512u : 256u;
+  a.oob_block = (int)((wrows + BM - 1) / BM);
+  CUtensorMap tmW, tmH, tmX;
+  if (!make_weight_map(&tmW, w, tiled, wrows, d) || !make_map(&tmH, hidden, (uint64_t)d, (uint64_t)rows, kMaxN) ||
+      !make_map(&tmX, hidden, (uint64_t)d, (uint64_t)rows, 16))
+    return fail(MEDUSA_ERR_CUDA, "%s: cuTensorMapEncodeTiled failed", fn);
+  const size_t smem = 1024 + a.part_off;
+  auto kern = lm_head_tc_kernel<false, false, true>;
+  cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  launch_kernel(kern, dim3(p.grid), dim3(kThreads), smem, s, tmW, tmH, tmX, a);
+  return check_launch(fn);
+}
+
 int launch_tc(LmArgs& a, const void* w, bool tiled, int64_t wrows, const void* hidden, int rows, int d,
               cudaStream_t s, const char* fn) {
   if (use_pair(a, rows)) return launch_pair(a, w, tiled, wrows, hidden, rows, d, s, fn);
+  if (use_xrows(a, rows)) return launch_xrows(a, w, tiled, wrows, hidden, rows, d, s, fn);
   a.rows = rows; a.d = d; a.tiled = tiled;
   const LmPlan p = plan_tc(rows, a.ntiles, a.mode == 1, a.stat_mode != 0);
   if (p.stages < 2) return fail(MEDUSA_ERR_UNSUPPORTED, "%s: shared memory for %d tree rows", fn, rows);
@@ -1152,6 +1293,7 @@ extern "C" int medusa_lm_head_ctas(int rows, int V) {
   LmArgs a{};
   a.ntiles = (V + BM - 1) / BM;
   if (use_pair(a, rows)) return pair_grid(plan_pair(rows, a.ntiles));
+  if (use_xrows(a, rows)) return plan_xrows(a.ntiles).grid;
   const LmPlan p = plan_tc(rows, (V + BM - 1) / BM, false, false);
   if (p.stages < 2) return 0;
   const int items = p.ngroups * p.nchunks;

@@ -189,7 +189,10 @@ LM_CASES = [("f32", 15, 256, 1024), ("bf16", 15, 256, 1024), ("bf16", 65, 256, 1
             # two tiles per item with one accumulator (129..256 rows, more tiles than SMs);
             # two row chunks sharing each weight block (257..512 rows); two such items
             ("bf16", 200, 256, 40000), ("bf16", 300, 256, 40000), ("bf16", 512, 128, 5000),
-            ("bf16", 1000, 128, 700)]
+            ("bf16", 1000, 128, 700),
+            # 257, 258 rows: one 256-row chunk on the tensor cores, the rest on the CUDA cores
+            # (one tile per item; two tiles per item); 259 rows: two chunks again
+            ("bf16", 257, 4096, 2048), ("bf16", 258, 192, 40000), ("bf16", 259, 6656, 1000)]
 
 
 @pytest.mark.parametrize("case", LM_CASES, ids=lambda c: "-".join(map(str, c)))
@@ -241,20 +244,23 @@ def test_lm_head_tiled_layout(M, case):
         assert np.abs(to_host(a_tiles) - ref).max() <= TOL["bf16"]["logit"] * np.abs(ref).max()
 
 
-PAIR_CASES = [(129, 128, 777), (256, 192, 3000), (200, 4096, 2048), (256, 4096, 32000)]
+PAIR_CASES = [(129, 128, 777), (256, 192, 3000), (200, 4096, 2048), (256, 4096, 32000),
+              (257, 4096, 32000), (258, 6656, 32000), (258, 128, 777)]
 
 
 @pytest.mark.parametrize("case", PAIR_CASES, ids=lambda c: "-".join(map(str, c)))
 def test_lm_head_cta_pairs(M, case):
     """129..256 rows run on CTA pairs (one MMA of M = 256 over a vocabulary
     tile of each CTA, each CTA holding half of the hidden rows): an odd tile
-    count leaves the last pair's second CTA a tile past V; both weight
+    count leaves the last pair's second CTA a tile past V; 257 and 258 rows
+    run as one 256-row chunk plus extra rows on the CUDA cores.  Both weight
     layouts give the same logits bit for bit, within tolerance of the oracle."""
     rows, d, V = case
     h = synth.normal(13, "h", (rows, d), 1.0, "bf16")
     w = synth.normal(13, "w", (V, d), 1.0 / math.sqrt(d), "bf16")
     hd, wd = to_dev(h), to_dev(w)
-    assert M.medusa_lm_head_ctas(rows, V) % 2 == 0
+    if rows <= 256:
+        assert M.medusa_lm_head_ctas(rows, V) % 2 == 0
     a_rows = torch.full((rows, V), float("nan"), dtype=torch.float32, device="cuda")
     a_tiles = torch.full((rows, V), float("nan"), dtype=torch.float32, device="cuda")
     err = torch.zeros(1, dtype=torch.int32, device="cuda")
