@@ -273,8 +273,8 @@ int medusa_lm_head_tile(const void* w_lm, void* w_tiled, int d, int V,
  * f32 accepts MEDUSA_W_ROWS only.  The tensor-core kernel's bounded on-chip
  * waits report MEDUSA_DEVERR_TIMEOUT through err (nullable) if they ever
  * give up.  Rows beyond 256 are processed in balanced chunks of at most 256
- * that multiply the same weight k-block (the weights are read once); 257 and
- * 258 rows as one 256-row chunk plus the rest on CUDA cores beside it; 129 to
+ * that multiply the same weight k-block (the weights are read once); 257 to
+ * 264 rows as one 256-row chunk plus the rest by mma.sync beside it; 129 to
  * 256 rows run on clusters of two CTAs (one tcgen05 MMA of M = 256 over a
  * vocabulary tile of each, each CTA loading half of the hidden rows). */
 int medusa_lm_head_verify(const void* hidden, const void* w_lm, float* logits,

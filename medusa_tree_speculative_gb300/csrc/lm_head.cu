@@ -62,7 +62,7 @@ constexpr int kThreads = 192;  // 6 warps
 constexpr int kMaxN = 256;     // tree rows per chunk (MMA N)
 constexpr int kMaxTiles = 4;   // weight tiles per work item (sharing each hidden k-block)
 constexpr size_t kSmemBudget = 200 * 1024;
-constexpr int kMaxXRows = 2;   // rows past 256 formed on the CUDA cores (XROWS plan)
+constexpr int kMaxXRows = 8;   // rows past 256 formed by the epilogue warps (XROWS plan): one mma.sync N
 
 struct LmArgs {
   float* logits;
@@ -148,6 +148,17 @@ MDEV StatRec transpose_reduce(StatRec (&x)[16], int lane, float inv_temp) {
   tr_step<TYP, 2, 2>(x, lane, inv_temp);
   return stat_merge<TYP>(x[0], rec_shfl<TYP>(x[0], 1), inv_temp);
 }
+// ldmatrix: four (two) 8x8 bf16 matrices, lane l giving the address of row
+// l % 8 of matrix l / 8.
+MDEV void ldsm_x4(uint32_t addr, uint32_t (&r)[4]) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0, %1, %2, %3}, [%4];\n"
+               : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
+               : "r"(addr));
+}
+MDEV void ldsm_x2(uint32_t addr, uint32_t& r0, uint32_t& r1) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x2.shared.b16 {%0, %1}, [%2];\n" : "=r"(r0), "=r"(r1) : "r"(addr));
+}
+
 MDEV uint4 lds_v4(uint32_t addr) {
   uint4 v;
   asm volatile("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4];\n" : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "r"(addr));
@@ -414,54 +425,40 @@ __global__ void __launch_bounds__(kThreads, 1)
     for (int item = i0; item < i1; ++item, ++local) {
       const int acc = a.nacc == 2 ? local & 1 : 0;
       const uint32_t aph = (uint32_t)(a.nacc == 2 ? local >> 1 : local) & 1u;
-      // XROWS: the rows past the chunk against this thread's weight row of
-      // each tile, stage by stage beside the MMAs (each stage released by
-      // the four warps and the MMAs); 16-byte chunk c of a row r of a
-      // 128-byte-swizzled box sits at chunk c ^ (r & 7)
-      float xacc[2][kMaxXRows];
+      // XROWS: the rows past the chunk (up to eight, N of an mma.sync
+      // m16n8k16) against this warp's 64 weight rows (four 16-row blocks of
+      // tile g / 2), k-block by k-block beside the MMAs; each stage is
+      // released by the four warps and the MMAs.  Operands come from the
+      // stage by ldmatrix, the 128-byte swizzle undone in the row addresses
+      // (16-byte chunk c of a row r at chunk c ^ (r & 7)).
+      float xc[4][4];
       if constexpr (XROWS) {
 #pragma unroll
-        for (int t = 0; t < 2; ++t)
+        for (int m = 0; m < 4; ++m)
 #pragma unroll
-          for (int j = 0; j < kMaxXRows; ++j) xacc[t][j] = 0.f;
-        const int rr = 32 * g + lane;
+          for (int q = 0; q < 4; ++q) xc[m][q] = 0.f;
+        const int xt = g >> 1, xrow0 = (g & 1) * 64;  // this warp's tile and first row in it
+        const int lr = lane & 7, lm = lane >> 3;      // row in an 8x8 matrix, which matrix
         bool xok = true;
         for (int kb = 0; kb < nkb; ++kb, ++xit) {
           const int s = xit % a.stages;
           const bool xgot = wait_or_abort(&full[s], (uint32_t)(xit / a.stages) & 1u, abort_flag);
           if (__any_sync(0xffffffffu, !xgot)) { xok = false; break; }
           const uint32_t st = smem_u32(smem + (size_t)s * stage_bytes);
-          // the weight row of each tile first (16 loads in flight), then each
-          // extra row's k-block (8 more), two partial sums per tile
-          uint4 wr0[8], wr1[8];
+          if (xt < a.nt) {
+            const uint32_t wb = st + (uint32_t)xt * (BM * BK * 2), hb = st + a.xr_off;
 #pragma unroll
-          for (int c = 0; c < 8; ++c) wr0[c] = lds_v4(st + rr * 128 + ((c ^ (rr & 7)) << 4));
+            for (int ks = 0; ks < BK / UK; ++ks) {
+              uint32_t b0, b1;  // extra rows lr, k chunk 2 ks + (lm & 1)
+              const int bch = 2 * ks + (lm & 1);
+              ldsm_x2(hb + lr * 128 + ((bch ^ lr) << 4), b0, b1);
 #pragma unroll
-          for (int c = 0; c < 8; ++c)
-            wr1[c] = a.nt == 2 ? lds_v4(st + BM * BK * 2 + rr * 128 + ((c ^ (rr & 7)) << 4)) : make_uint4(0u, 0u, 0u, 0u);
-#pragma unroll
-          for (int j = 0; j < kMaxXRows; ++j) {
-            if (j < a.xr) {
-              uint4 hv[8];
-#pragma unroll
-              for (int c = 0; c < 8; ++c) hv[c] = lds_v4(st + a.xr_off + j * 128 + ((c ^ (j & 7)) << 4));
-              float p0 = 0.f, q0 = 0.f, p1 = 0.f, q1 = 0.f;
-#pragma unroll
-              for (int c = 0; c < 8; ++c) {
-                const uint32_t h4[4] = {hv[c].x, hv[c].y, hv[c].z, hv[c].w};
-                const uint32_t a4[4] = {wr0[c].x, wr0[c].y, wr0[c].z, wr0[c].w};
-                const uint32_t b4[4] = {wr1[c].x, wr1[c].y, wr1[c].z, wr1[c].w};
-#pragma unroll
-                for (int e = 0; e < 4; ++e) {
-                  const float hl = bf16_lo(h4[e]), hh = bf16_hi(h4[e]);
-                  p0 = fmaf(bf16_lo(a4[e]), hl, p0);
-                  q0 = fmaf(bf16_hi(a4[e]), hh, q0);
-                  p1 = fmaf(bf16_lo(b4[e]), hl, p1);
-                  q1 = fmaf(bf16_hi(b4[e]), hh, q1);
-                }
+              for (int m = 0; m < 4; ++m) {
+                const int ar = xrow0 + m * 16 + (lm & 1) * 8 + lr, ach = 2 * ks + (lm >> 1);
+                uint32_t af[4];
+                ldsm_x4(wb + ar * 128 + ((ach ^ (ar & 7)) << 4), af);
+                mma_bf16_16816(xc[m], af, b0, b1);
               }
-              xacc[0][j] += p0 + q0;
-              xacc[1][j] += p1 + q1;
             }
           }
           __syncwarp();
@@ -534,17 +531,18 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
         }
       }
-      if constexpr (XROWS) {
+      if constexpr (XROWS) {  // C fragment: (row lane / 4 [+ 8], extra row 2 (lane % 4) [+ 1])
+        const int xt = g >> 1;
+        if (xt < a.nt) {
+          const int v0 = tile_src<JOINT>(a, item, xt).v0 + (g & 1) * 64 + (lane >> 2);
 #pragma unroll
-        for (int t = 0; t < 2; ++t) {
-          const int v = tile_src<JOINT>(a, item, t).v0 + 32 * g + lane;
-          if (t < a.nt && v < a.V) {
+          for (int m = 0; m < 4; ++m)
 #pragma unroll
-            for (int j = 0; j < kMaxXRows; ++j) {
+            for (int q = 0; q < 4; ++q) {
+              const int v = v0 + m * 16 + (q >> 1) * 8, j = 2 * (lane & 3) + (q & 1);
               const int row = r0 + a.npad + j;
-              if (j < a.xr && row < a.rows) a.logits[(int64_t)row * a.V + v] = xacc[t][j];
+              if (j < a.xr && row < a.rows && v < a.V) a.logits[(int64_t)row * a.V + v] = xc[m][q];
             }
-          }
         }
       }
       tc_fence_before();
@@ -1034,10 +1032,8 @@ int launch_pair(LmArgs& a, const void* w, bool tiled, int64_t wrows, const void*
 // four MMAs per tile where two chunks of 144 rows took eight (the MMAs
 // bounded the two-chunk call: an instruction of M = 128 costs about the same
 // at N = 144 as at N = 256), and the rows past it on the CUDA cores of the
-// epilogue warps, which read each weight stage beside the MMAs.  Each such
-// row costs the epilogue warps about 0.4 us per 64-wide k-block, so beyond
-// two of them they, not the MMAs, would set the pace (measured 257 rows:
-// 79.9 against 92.4 us at d = 4096; 260 rows: 157.7 against 92.2 us).
+// epilogue warps, which read each weight stage beside the MMAs with
+// ldmatrix + mma.sync (eight extra rows are one N = 8 fragment).
 struct XPlan {
   int nt, stages, grid;
   size_t stage_bytes;

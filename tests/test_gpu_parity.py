@@ -190,9 +190,10 @@ LM_CASES = [("f32", 15, 256, 1024), ("bf16", 15, 256, 1024), ("bf16", 65, 256, 1
             # two row chunks sharing each weight block (257..512 rows); two such items
             ("bf16", 200, 256, 40000), ("bf16", 300, 256, 40000), ("bf16", 512, 128, 5000),
             ("bf16", 1000, 128, 700),
-            # 257, 258 rows: one 256-row chunk on the tensor cores, the rest on the CUDA cores
-            # (one tile per item; two tiles per item); 259 rows: two chunks again
-            ("bf16", 257, 4096, 2048), ("bf16", 258, 192, 40000), ("bf16", 259, 6656, 1000)]
+            # 257..264 rows: one 256-row chunk on tcgen05, the rest beside it by mma.sync
+            # (one tile per item; two tiles per item with eight extra rows); 265: two chunks again
+            ("bf16", 257, 4096, 2048), ("bf16", 264, 192, 40000), ("bf16", 260, 6656, 1000),
+            ("bf16", 265, 128, 3000)]
 
 
 @pytest.mark.parametrize("case", LM_CASES, ids=lambda c: "-".join(map(str, c)))
@@ -245,15 +246,15 @@ def test_lm_head_tiled_layout(M, case):
 
 
 PAIR_CASES = [(129, 128, 777), (256, 192, 3000), (200, 4096, 2048), (256, 4096, 32000),
-              (257, 4096, 32000), (258, 6656, 32000), (258, 128, 777)]
+              (257, 4096, 32000), (260, 6656, 32000), (264, 128, 777)]
 
 
 @pytest.mark.parametrize("case", PAIR_CASES, ids=lambda c: "-".join(map(str, c)))
 def test_lm_head_cta_pairs(M, case):
     """129..256 rows run on CTA pairs (one MMA of M = 256 over a vocabulary
     tile of each CTA, each CTA holding half of the hidden rows): an odd tile
-    count leaves the last pair's second CTA a tile past V; 257 and 258 rows
-    run as one 256-row chunk plus extra rows on the CUDA cores.  Both weight
+    count leaves the last pair's second CTA a tile past V; 257 to 264 rows
+    run as one 256-row chunk plus the extra rows by mma.sync beside it.  Both weight
     layouts give the same logits bit for bit, within tolerance of the oracle."""
     rows, d, V = case
     h = synth.normal(13, "h", (rows, d), 1.0, "bf16")
