@@ -577,9 +577,12 @@ HEAD_CASES = [
     # 325 tree rows: W1 over every row in two row chunks per weight block
     ("bf16", 5, 65, 256, 1000, (4, 3, 2), True, False),
 ]
-# d not a multiple of 32: the CUDA-core kernels for several sequences (the
-# fused call only: medusa_heads_hidden takes bf16 d in multiples of 128)
-FUSED_ONLY_CASES = [("bf16", 3, 9, 144, 700, (2, 2), False, False)]
+# The fused call only (medusa_heads_hidden takes bf16 d in multiples of 128):
+# d not a multiple of 32, the CUDA-core kernels for several sequences; d a
+# multiple of 32 but not of 128 (twelve sequences: both halves of M)
+FUSED_ONLY_CASES = [("bf16", 3, 9, 144, 700, (2, 2), False, False),
+                    ("bf16", 4, 9, 288, 1500, (4, 2), True, False),
+                    ("bf16", 12, 9, 416, 777, (3, 3, 1), False, False)]
 
 
 @pytest.mark.parametrize("case", HEAD_CASES + FUSED_ONLY_CASES,
