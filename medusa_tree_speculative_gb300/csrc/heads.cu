@@ -78,6 +78,7 @@ struct HeadsArgs {
   const int32_t* c_rank;
   int cT;
   int* heads_done;              // heads merged so far; zero on entry, left zero
+  int fill_levels;              // every tree level's head is in use: each head fills its own level
   int32_t* err;
 };
 
@@ -561,7 +562,25 @@ __global__ void __launch_bounds__(kWarps * 32) heads_w2_topk_kernel(const __grid
       a.counters[slot] = 0;
       a.rowctr[slot] = 0;
     }
-    if (a.tokens) {
+    if (a.tokens && a.fill_levels) {
+      // a node at depth k + 1 takes head k's token of its rank, so each head
+      // fills its own tree level as soon as its top-s is merged (slot 0 also
+      // the roots), without waiting for the other heads
+      __syncthreads();  // this head's topk is written (by warp 0 of this CTA)
+      for (int e = threadIdx.x; e < a.B * a.cT; e += blockDim.x) {
+        const int b = e / a.cT, n = e % a.cT;
+        if (n == 0) {
+          if (slot == 0) a.tokens[(int64_t)b * a.cT] = a.next_root[b];
+          continue;
+        }
+        // the first round's node was loaded when the CTA started
+        const int dep = e == (int)threadIdx.x ? fill_depth : a.c_depth[n];
+        if (dep - 1 != k) continue;
+        const int r = (e == (int)threadIdx.x ? fill_rank : a.c_rank[n]) - 1;
+        a.tokens[(int64_t)b * a.cT + n] =
+            (r >= 0 && r < a.s_max) ? __ldcg(a.topk + ((int64_t)b * a.K + k) * a.s_max + r) : -1;
+      }
+    } else if (a.tokens) {
       // the last head to be merged fills the next step's candidates
       __syncthreads();  // this head's topk is written
       if (threadIdx.x == 0) last = arrive_acq_rel(a.heads_done) == a.nused - 1;
@@ -767,6 +786,8 @@ int heads_topk_impl(const void* hidden, const int32_t* last_node, int T, const v
     a.tokens = cf->tokens; a.next_root = cf->next_root;
     a.c_depth = cf->tree->depth; a.c_rank = cf->tree->rank; a.cT = cf->tree->T;
     a.heads_done = a.counters + 2 * MEDUSA_MAX_K + 1;
+    a.fill_levels = 1;
+    for (int k = 0; k < cf->tree->K; ++k) a.fill_levels &= s[k] > 0;
   }
   cudaStream_t st = as_stream(stream);
   return dtype == MEDUSA_BF16 ? launch_heads_b<uint16_t>(a, smax_used, st)
