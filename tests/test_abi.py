@@ -277,3 +277,18 @@ def test_tc_key_splits(M):
     # in the step: the 27 SMs the 7B LM head (125 CTAs) leaves free
     assert tc_key_splits(1, 32, 65, 4096, 27) == 1
     assert tc_key_splits(1, 4, 65, 4096, 27) == 4      # 16 CTAs; 8 splits would need 32 SMs
+
+
+def test_lm_head_plans(M):
+    """CTAs the bf16 LM head launches per row plan (host logic, one CTA per
+    SM): two weight tiles per work item up to 128 rows; CTA pairs (an even
+    count) from 129 to 256 rows; one 256-row chunk plus the extra rows by
+    mma.sync from 257 to 264; chunks sharing each weight block beyond."""
+    assert M.medusa_lm_head_ctas(0, 32000) == 0
+    assert M.medusa_lm_head_ctas(65, 0) == 0
+    assert M.medusa_lm_head_ctas(65, 32000) == 125            # 250 tiles, two per item
+    for rows in (129, 200, 256):
+        assert M.medusa_lm_head_ctas(rows, 32000) == 126      # 63 pairs, four tiles each
+        assert M.medusa_lm_head_ctas(rows, 1000) % 2 == 0     # 8 tiles: four pairs
+    for rows in (257, 260, 264, 265, 512):
+        assert M.medusa_lm_head_ctas(rows, 32000) == 125
