@@ -43,7 +43,12 @@ namespace medusa {
 namespace {
 
 constexpr int kWarps = 8;  // 256-thread CTAs
-constexpr int UNROLL = 8;  // 16-byte loads in flight per lane
+constexpr int UNROLL = 8;  // 16-byte loads in flight per lane (CUDA-core GEMVs)
+// mma_rows8: 16-byte weight loads in flight per lane (each with the
+// sequences' 16 bytes).  Four keep the tensor-core kernels at 64 registers,
+// four CTAs per SM: 32 warps per SM hide each other's unit barriers, where
+// eight loads per lane at two CTAs per SM streamed about 13% slower.
+constexpr int kMmaLoads = 4;
 constexpr int kMaxS = MEDUSA_MAX_S;
 constexpr int kMaxGroups = 128;  // W2 row groups per CTA above which a group grows (w2_row_group)
 
@@ -137,10 +142,10 @@ MDEV void dot_rows(const TE* w, const TE* const* x, int nvec, int B, int lane, f
 // product is unchanged.  wrow, xlo, xhi already include the lane's 8 t.
 template <bool HI>
 MDEV void mma_rows8(const uint16_t* wrow, const uint16_t* xlo, const uint16_t* xhi, int c0, int c1, float* c) {
-  for (int cb = c0; cb < c1; cb += UNROLL) {
-    uint4 wv[UNROLL], xl[UNROLL], xh[UNROLL];
+  for (int cb = c0; cb < c1; cb += kMmaLoads) {
+    uint4 wv[kMmaLoads], xl[kMmaLoads], xh[kMmaLoads];
 #pragma unroll
-    for (int u = 0; u < UNROLL; ++u) {
+    for (int u = 0; u < kMmaLoads; ++u) {
       const int ch = cb + u;
       if (ch < c1) {
         wv[u] = ldg_stream(wrow + ch * 32);
@@ -149,7 +154,7 @@ MDEV void mma_rows8(const uint16_t* wrow, const uint16_t* xlo, const uint16_t* x
       }
     }
 #pragma unroll
-    for (int u = 0; u < UNROLL; ++u) {
+    for (int u = 0; u < kMmaLoads; ++u) {
       if (cb + u < c1) {
         const uint32_t a0[4] = {xl[u].x, HI ? xh[u].x : 0u, xl[u].y, HI ? xh[u].y : 0u};
         mma_bf16_16816(c, a0, wv[u].x, wv[u].y);
@@ -247,7 +252,7 @@ __global__ void __launch_bounds__(kWarps * 32) heads_w1_kernel(const __grid_cons
 // the hidden dimension split over the eight warps; the warps' fragments meet
 // in shared memory and one thread per (sequence, row) applies the epilogue.
 template <bool HI>
-__global__ void __launch_bounds__(kWarps * 32) heads_w1_mma_kernel(const __grid_constant__ HeadsArgs a) {
+__global__ void __launch_bounds__(kWarps * 32, 4) heads_w1_mma_kernel(const __grid_constant__ HeadsArgs a) {
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int g = lane >> 2, t = lane & 3;
   __shared__ float4 part[2][kWarps][32];
@@ -384,8 +389,8 @@ MDEV void block_select(TopList<S>& L, float (*wv)[S], int (*wi)[S], float* ov, i
 // of eight per CTA (the hidden dimension split over the warps); after each
 // unit warp w sums row w's fragments and lane s inserts sequence s's value
 // into warp w's running top S of that sequence.
-template <typename TE, int NB, int S, bool MMA = false>
-__global__ void __launch_bounds__(kWarps * 32) heads_w2_topk_kernel(const __grid_constant__ HeadsArgs a) {
+template <typename TE, int NB, int S, bool MMA>
+MDEV void w2_topk_body(const HeadsArgs& a) {
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   __shared__ float wv[32][S];
   __shared__ int wi[32][S];
@@ -613,6 +618,18 @@ __global__ void __launch_bounds__(kWarps * 32) heads_w2_topk_kernel(const __grid
   }
 }
 
+// The CUDA-core W2 kernel, and the tensor-core one bounded to 64 registers
+// (four CTAs per SM); separate kernels so that each keeps its own register
+// budget.
+template <typename TE, int NB, int S>
+__global__ void __launch_bounds__(kWarps * 32) heads_w2_topk_kernel(const __grid_constant__ HeadsArgs a) {
+  w2_topk_body<TE, NB, S, false>(a);
+}
+template <int NB, int S>
+__global__ void __launch_bounds__(kWarps * 32, 4) heads_w2_mma_kernel(const __grid_constant__ HeadsArgs a) {
+  w2_topk_body<uint16_t, NB, S, true>(a);
+}
+
 // W2 CTAs per used head: about four per SM in total, at least 8 rows each.
 int w2_ctas_per_head(int nused, int V) {
   const int target = std::max(1, 4 * sm_count() / std::max(1, nused));
@@ -651,9 +668,9 @@ template <int NB>
 void launch_w2_mma(const HeadsArgs& a, int smax_used, cudaStream_t s) {
   const dim3 g2(a.nused * a.cpc);
   if (smax_used <= 8)
-    launch_kernel(heads_w2_topk_kernel<uint16_t, NB, 8, true>, g2, dim3(kWarps * 32), 0, s, a);
+    launch_kernel(heads_w2_mma_kernel<NB, 8>, g2, dim3(kWarps * 32), 0, s, a);
   else
-    launch_kernel(heads_w2_topk_kernel<uint16_t, NB, 16, true>, g2, dim3(kWarps * 32), 0, s, a);
+    launch_kernel(heads_w2_mma_kernel<NB, 16>, g2, dim3(kWarps * 32), 0, s, a);
 }
 
 int launch_heads_mma(const HeadsArgs& a, int smax_used, cudaStream_t s) {
