@@ -420,7 +420,7 @@ def run_native(args, w, rank, world, local_rank):
 
 
 def measure_attn_alone(st, x, prefix0, L_list, torch, M, reps=10):
-    """The tree attention on its own, as its roofline is judged: the key split
+    """The tree attention on its own, as its roofline is measured: the key split
     that fills the GPU (step.tc_key_splits over every SM), L2 flushed before
     each launch (a 256 MB buffer written, then read back so that L2 holds its
     clean lines: after a write alone the dirty lines' write-back lands in the

@@ -1,4 +1,4 @@
-"""The parity helpers that judge GPU results with the oracle (CPU only):
+"""The parity helpers that check GPU results with the oracle (CPU only):
 check_accept_on_gpu_logits accepts the oracle's own outputs, rejects a
 planted mistake on a clear decision, and falls back to validity only for a
 typical decision within rounding of its threshold; gpu_topk_matches_oracle
